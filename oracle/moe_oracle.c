@@ -1,0 +1,256 @@
+/*
+ * moe_oracle.c -- plain, slow CPU oracle of the routed-experts MoE step over
+ * NVFP4 expert weights.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or call
+ * this file: only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg use it.  It shares no code with the CUDA library.
+ *
+ * What it computes (the plain definition, written out):
+ *
+ *   y_t = sum_{j=0..k-1, valid} w_tj * W_down[e_tj] ( SiLU(W_gate[e_tj] x_t) (.) (W_up[e_tj] x_t) )
+ *
+ * the routed-experts step the serving pages build their "lna2" kernel for
+ * ("LNA-CANON.md", section "lna2 とは": resident expert teams, rows per expert
+ * R_e, m <= 24; "dsv4-carve" README, section "house kernel lna2").  The pages'
+ * EXL3 trellis format is never defined there, so the expert weights are NVFP4
+ * (the format the V100 page, section 7.1, adopts because it expands into FP16
+ * in registers): an E2M1 value times its 16-element block's E4M3 scale times
+ * the (expert, projection) FP32 tensor scale.
+ *
+ * Precision: every dequantised weight is formed exactly in double
+ * (E2M1 x E4M3 x fp32 needs at most 2+4+24 significant bits); x (bf16) and the
+ * routing weights (fp32) convert to double exactly; dot products, SiLU and the
+ * combine run in double, each sum in plain index order.  The result is the
+ * definition's value up to double rounding.
+ *
+ * Slot rules (the pages are silent; plainest reading): an id < 0 is an empty
+ * slot and contributes nothing; an id >= E contributes nothing and is counted
+ * as bad; duplicate ids within a token are independent slots.
+ *
+ * Grouping (the pairs-by-expert tables an expert-team kernel works from):
+ * counts[e] = number of valid pairs with id e; offsets = exclusive prefix sum
+ * (offsets[E] = number of valid pairs); perm lists the flat pair indices
+ * p = t*k + j of valid pairs sorted by (expert, p) -- a stable counting sort,
+ * the unique answer.
+ *
+ * Parallelism: optional OpenMP over independent output rows only; every
+ * individual sum keeps its sequential order, so the result does not depend on
+ * the thread count.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------- formats */
+
+/* E2M1 (OCP Microscaling formats v1.0, FP4 E2M1): bit 3 sign, bits 2..1
+ * exponent with bias 1, bit 0 mantissa; exponent 0 is subnormal (0 or 0.5). */
+double oracle_dec_e2m1(unsigned code)
+{
+    unsigned s = (code >> 3) & 1u, e = (code >> 1) & 3u, m = code & 1u;
+    double mag = (e == 0) ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, (int)e - 1);
+    return s ? -mag : mag;
+}
+
+/* E4M3FN (OCP 8-bit floating point, E4M3): bit 7 sign, bits 6..3 exponent
+ * with bias 7, bits 2..0 mantissa; exponent 0 is subnormal (m/8 * 2^-6);
+ * S.1111.111 is NaN; there is no infinity (max 448). */
+double oracle_dec_e4m3(unsigned code)
+{
+    unsigned s = (code >> 7) & 1u, e = (code >> 3) & 15u, m = code & 7u;
+    if (e == 15u && m == 7u)
+        return NAN;
+    double mag = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+    return s ? -mag : mag;
+}
+
+/* Value tables built from the two definitions above (code -> value). */
+static double tab_e2m1[16], tab_e4m3[256];
+static int tabs_ready = 0;
+
+static void build_tables(void)
+{
+    if (tabs_ready)
+        return;
+    for (unsigned c = 0; c < 16; ++c)
+        tab_e2m1[c] = oracle_dec_e2m1(c);
+    for (unsigned c = 0; c < 256; ++c)
+        tab_e4m3[c] = oracle_dec_e4m3(c);
+    tabs_ready = 1;
+}
+
+/* bf16 bit pattern -> double (exact). */
+static double bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* One dequantised weight: row r, column c of a [rows, K] NVFP4 matrix whose
+ * packed bytes start at q (K/2 bytes per row) and scales at s (K/16 per row). */
+static double weight_at(const uint8_t *q, const uint8_t *s, double ts, int K, size_t r, int c)
+{
+    uint8_t byte = q[r * (size_t)(K / 2) + (size_t)(c / 2)];
+    unsigned nib = (c & 1) ? (byte >> 4) : (byte & 15u);
+    uint8_t sc = s[r * (size_t)(K / 16) + (size_t)(c / 16)];
+    return tab_e2m1[nib] * tab_e4m3[sc] * ts;
+}
+
+/* Dequantise a whole [rows, K] matrix into out (double, row-major). */
+void oracle_dequant(const uint8_t *q, const uint8_t *s, float ts, int rows, int K, double *out)
+{
+    build_tables();
+    for (size_t r = 0; r < (size_t)rows; ++r)
+        for (int c = 0; c < K; ++c)
+            out[r * (size_t)K + (size_t)c] = weight_at(q, s, (double)ts, K, r, c);
+}
+
+static int n_threads_eff(int n)
+{
+#ifdef _OPENMP
+    return n > 0 ? n : omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
+/* ---------------------------------------------------------------- one pair */
+
+/* One (token, expert) pair: xr (double [H]) through expert e.
+ *   g[i] = sum_c Wg[e][i][c] x[c]      u[i] likewise       (i < I)
+ *   h[i] = g[i] / (1 + exp(-g[i])) * u[i]
+ *   o[r] = sum_i Wd[e][r][i] h[i]      (r < H)
+ * Any of g, u, h may be NULL (scratch is then allocated internally). */
+void oracle_expert_pair(int H, int I, int e, const double *xr,
+                        const uint8_t *gate_q, const uint8_t *gate_s, const float *gate_ts,
+                        const uint8_t *up_q, const uint8_t *up_s, const float *up_ts,
+                        const uint8_t *down_q, const uint8_t *down_s, const float *down_ts,
+                        double *g, double *u, double *h, double *o, int n_threads)
+{
+    build_tables();
+    double *gbuf = g ? g : (double *)malloc(sizeof(double) * (size_t)I);
+    double *ubuf = u ? u : (double *)malloc(sizeof(double) * (size_t)I);
+    double *hbuf = h ? h : (double *)malloc(sizeof(double) * (size_t)I);
+    const uint8_t *gq = gate_q + (size_t)e * I * (H / 2), *gs = gate_s + (size_t)e * I * (H / 16);
+    const uint8_t *uq = up_q + (size_t)e * I * (H / 2), *us = up_s + (size_t)e * I * (H / 16);
+    const uint8_t *dq = down_q + (size_t)e * H * (I / 2), *ds = down_s + (size_t)e * H * (I / 16);
+    double tg = (double)gate_ts[e], tu = (double)up_ts[e], td = (double)down_ts[e];
+    int nt = n_threads_eff(n_threads);
+    (void)nt;
+
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nt)
+#endif
+    for (int i = 0; i < I; ++i) {
+        double sg = 0.0, su = 0.0;
+        for (int c = 0; c < H; ++c) {
+            sg += weight_at(gq, gs, tg, H, (size_t)i, c) * xr[c];
+            su += weight_at(uq, us, tu, H, (size_t)i, c) * xr[c];
+        }
+        gbuf[i] = sg;
+        ubuf[i] = su;
+        hbuf[i] = sg / (1.0 + exp(-sg)) * su;
+    }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nt)
+#endif
+    for (int r = 0; r < H; ++r) {
+        double acc = 0.0;
+        for (int i = 0; i < I; ++i)
+            acc += weight_at(dq, ds, td, I, (size_t)r, i) * hbuf[i];
+        o[r] = acc;
+    }
+    if (!g) free(gbuf);
+    if (!u) free(ubuf);
+    if (!h) free(hbuf);
+}
+
+/* ---------------------------------------------------------------- full step */
+
+/* y (double [n_tok, H]) for the tokens listed in `tokens` (NULL: all T, in
+ * order).  Returns the number of slots whose id is >= E, or -1 on a bad
+ * argument.  x holds bf16 bit patterns [T, H]; ids int32 [T, k]; w fp32 [T, k]. */
+int oracle_moe_forward(int H, int I, int E, int k, int T,
+                       const uint16_t *x, const int32_t *ids, const float *w,
+                       const uint8_t *gate_q, const uint8_t *gate_s, const float *gate_ts,
+                       const uint8_t *up_q, const uint8_t *up_s, const float *up_ts,
+                       const uint8_t *down_q, const uint8_t *down_s, const float *down_ts,
+                       const int32_t *tokens, int n_tok, double *y, int n_threads)
+{
+    if (H <= 0 || I <= 0 || E <= 0 || k <= 0 || T < 0 || (H % 16) || (I % 16))
+        return -1;
+    if (!tokens)
+        n_tok = T;
+    double *xr = (double *)malloc(sizeof(double) * (size_t)H);
+    double *o = (double *)malloc(sizeof(double) * (size_t)H);
+    int bad = 0;
+    for (int n = 0; n < n_tok; ++n) {
+        int t = tokens ? tokens[n] : n;
+        double *yt = y + (size_t)n * H;
+        for (int r = 0; r < H; ++r)
+            yt[r] = 0.0;
+        if (t < 0 || t >= T)
+            continue;
+        for (int c = 0; c < H; ++c)
+            xr[c] = bf16_to_double(x[(size_t)t * H + (size_t)c]);
+        for (int j = 0; j < k; ++j) {
+            int e = ids[(size_t)t * k + (size_t)j];
+            if (e < 0)
+                continue;
+            if (e >= E) {
+                ++bad;
+                continue;
+            }
+            oracle_expert_pair(H, I, e, xr, gate_q, gate_s, gate_ts, up_q, up_s, up_ts,
+                               down_q, down_s, down_ts, NULL, NULL, NULL, o, n_threads);
+            double wj = (double)w[(size_t)t * k + (size_t)j];
+            for (int r = 0; r < H; ++r)
+                yt[r] += wj * o[r];
+        }
+    }
+    free(xr);
+    free(o);
+    return bad;
+}
+
+/* ---------------------------------------------------------------- grouping */
+
+/* Stable counting sort of the P = T*k flat pairs by expert id.
+ * counts int32 [E], offsets int32 [E+1], perm int32 [P] (entries past
+ * offsets[E] are set to -1).  Returns the number of ids >= E. */
+int oracle_group(const int32_t *ids, int P, int E, int32_t *counts, int32_t *offsets, int32_t *perm)
+{
+    int bad = 0;
+    for (int e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (int p = 0; p < P; ++p) {
+        int e = ids[p];
+        if (e >= E)
+            ++bad;
+        else if (e >= 0)
+            ++counts[e];
+    }
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e)
+        offsets[e + 1] = offsets[e] + counts[e];
+    int32_t *cursor = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
+    for (int e = 0; e < E; ++e)
+        cursor[e] = offsets[e];
+    for (int p = 0; p < P; ++p)
+        perm[p] = -1;
+    for (int p = 0; p < P; ++p) {
+        int e = ids[p];
+        if (e >= 0 && e < E)
+            perm[cursor[e]++] = p;
+    }
+    free(cursor);
+    return bad;
+}
