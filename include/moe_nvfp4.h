@@ -1,0 +1,183 @@
+/*
+ * moe_nvfp4.h -- C ABI of the GB300 (sm_103a) routed-experts MoE step over
+ * NVFP4 expert weights.
+ *
+ * The operation (one MoE layer's routed experts, one step):
+ *
+ *   y_t = sum_{j < k, slot valid} w_tj * W_down[e_tj] ( SiLU(W_gate[e_tj] x_t) (.) (W_up[e_tj] x_t) )
+ *
+ * for T tokens with router ids e_tj and weights w_tj.  This is the step the
+ * serving pages' "lna2" kernel computes ("LNA-CANON.md", section "lna2 とは":
+ * resident expert teams pulling dynamic tickets with no grid-wide barrier, rows
+ * per expert R_e, m <= 24 tokens; "dsv4-carve" README, section "house kernel
+ * lna2": 104.0 us per launch against exl3_moe's 232.6 us).  The pages' EXL3
+ * trellis weights are never defined there; the expert weights here are NVFP4
+ * (V100 page, section 7.1: NVFP4 expands into FP16 in registers almost for
+ * free): E2M1 values, one E4M3 scale per 16 elements along the reduction axis,
+ * one FP32 tensor scale per (expert, projection).
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers named *_dev are CUDA device pointers on the plan's device; the
+ *    caller owns them (allocates, frees, keeps them alive while work that
+ *    uses them is in flight).  The library never frees caller memory and
+ *    allocates no device memory.
+ *  - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *    stream.  Work is enqueued asynchronously; no entry point below
+ *    synchronises except moe_check.
+ *  - A status other than MOE_OK leaves nothing enqueued; moe_last_error()
+ *    returns a message for the calling thread's last failure.
+ *  - There is no CPU fallback and no other backend: a shape or argument the
+ *    sm_103a kernels do not take is an error, never a silent detour.
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_NVFP4_ABI_VERSION 1
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,       /* null pointer, bad size, T > T_max, ...          */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2, /* H, I, E or top_k outside what the kernels take  */
+    MOE_ERR_NOT_FAST_PATH = 3,     /* strict mode: call would leave the named path     */
+    MOE_ERR_MISALIGNED = 4,        /* a pointer is not aligned as documented          */
+    MOE_ERR_CUDA = 5,              /* a CUDA runtime call failed (message has details) */
+    MOE_ERR_TIMEOUT = 6,           /* device: a bounded wait gave up (see moe_check)   */
+    MOE_ERR_BAD_EXPERT_ID = 7,     /* device: an id >= E was seen (slot skipped)       */
+    MOE_ERR_RANGE = 8              /* device: an fp16 intermediate overflowed          */
+} moe_status_t;
+
+/* Opaque plan: host memory owned by the library (moe_plan_destroy frees it). */
+typedef struct moe_plan *moe_plan_t;
+
+/* Plan description.  Weight layouts (row-major, C order):
+ *   gate_q, up_q  uint8 [E, I, H/2]  element c of a row: low nibble of byte c/2
+ *   down_q        uint8 [E, H, I/2]  if c is even, high nibble if c is odd
+ *   gate_s, up_s  uint8 [E, I, H/16] E4M3 scale of elements 16b .. 16b+15
+ *   down_s        uint8 [E, H, I/16]
+ *   gate_ts, up_ts, down_ts  float [E]  FP32 tensor scale per (expert, projection)
+ * A weight is  E2M1(nibble) * E4M3(block scale) * tensor scale.
+ * Every weight pointer must be 16-byte aligned; the *_ts arrays 4-byte aligned. */
+typedef struct {
+    int H;      /* hidden size, multiple of 128                                  */
+    int I;      /* expert intermediate size, multiple of 128                     */
+    int E;      /* number of experts, 1 .. 1024                                  */
+    int top_k;  /* slots per token, 1 .. 16                                      */
+    int T_max;  /* largest T any call on this plan may pass (sizes workspaces)   */
+    const uint8_t *gate_q_dev, *up_q_dev, *down_q_dev;
+    const uint8_t *gate_s_dev, *up_s_dev, *down_s_dev;
+    const float *gate_ts_dev, *up_ts_dev, *down_ts_dev;
+    int device; /* CUDA device ordinal the pointers live on; -1 = current device */
+    int strict; /* 1: refuse (MOE_ERR_NOT_FAST_PATH) anything but the named path; */
+                /*    the environment variable MOE_STRICT=1 forces it on          */
+    int pdl;    /* 1: launch with programmatic dependent launch allowed          */
+} moe_plan_desc;
+
+/* Per-plan launch counters (host side; how many times each path ran). */
+typedef struct {
+    uint64_t decode_launches;  /* persistent ticket kernel, T <= 24             */
+    uint64_t prefill_launches; /* persistent ticket kernel, prefill chunks      */
+    uint64_t null_launches;    /* measurement variant (no dequant, no math)     */
+    uint64_t group_launches;   /* stand-alone grouping kernel                   */
+    uint64_t rejected_calls;   /* calls that returned an error status           */
+    int num_sms;               /* SMs on the plan's device (grid size)          */
+    int stages;                /* shared-memory ring stages at the largest T    */
+    int smem_bytes;            /* dynamic shared memory per CTA at the largest T */
+} moe_stats_t;
+
+/* Validate `desc`, record its pointers and choose tile sizes from the device's
+ * SM count and shared memory.  Host only: no device allocation, no launch.
+ * Errors: INVALID_ARG (null desc/out/pointer, T_max < 1), UNSUPPORTED_SHAPE
+ * (H or I not a multiple of 128, E or top_k out of range, tiles do not fit in
+ * shared memory, device is not sm_103), MISALIGNED, CUDA (device query failed). */
+moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out);
+
+/* Free the plan (host memory only).  NULL is ignored. */
+void moe_plan_destroy(moe_plan_t plan);
+
+/* Bytes of device workspace a call with up to T tokens needs (1 <= T <= T_max).
+ * The layout is fixed per plan (sized for min(T_max, 4096 / top_k) tokens), so
+ * one workspace serves every T the plan accepts.
+ * One workspace per stream that runs MoE steps concurrently: two launches
+ * sharing a workspace at the same time corrupt each other's counters (the
+ * pages' two-stream deadlock, "dsv4-carve" README, trap 3).  Returns 0 for
+ * an invalid plan or T. */
+size_t moe_workspace_bytes(moe_plan_t plan, int T);
+
+/* Zero a workspace of `bytes` bytes (>= moe_workspace_bytes(plan, T_max))
+ * on `stream`.  Required once after allocation and after any device-side
+ * error; the kernels reset their own counters after every successful launch.
+ * ws_dev must be 256-byte aligned. */
+moe_status_t moe_workspace_init(moe_plan_t plan, void *ws_dev, size_t bytes, void *stream);
+
+/* Grouping only (bit-exact, integer): for the P = T*top_k flat pairs
+ * p = t*top_k + j, counts_dev[e] = number of pairs with ids[p] == e,
+ * offsets_dev[0..E] = exclusive prefix sum, perm_dev[0..P) = the pair
+ * indices with a valid id sorted by (id, p) (stable), then -1 padding.
+ * ids outside [0, E) are left out (>= E also sets MOE_ERR_BAD_EXPERT_ID in
+ * the workspace error word).  ids_dev int32 [T, top_k]; counts int32 [E];
+ * offsets int32 [E+1]; perm int32 [T*top_k].  1 <= T, T*top_k <= 4096. */
+moe_status_t moe_group(moe_plan_t plan, const int32_t *ids_dev, int T, void *ws_dev,
+                       int32_t *counts_dev, int32_t *offsets_dev, int32_t *perm_dev, void *stream);
+
+/* The routed-experts step for 0 <= T <= 24 tokens (decode; T == 0 is a no-op).
+ *   x_dev    bf16 [T, H] row-major, 16-byte aligned; values must fit fp16
+ *            (|x| <= 65504) because the tensor-core operands are fp16
+ *   ids_dev  int32 [T, top_k]: id < 0 = empty slot, id >= E = skipped + flagged
+ *   w_dev    float [T, top_k] routing weights, used as given
+ *   y_dev    float [T, H] row-major, 16-byte aligned; fully written
+ *   ws_dev   workspace of moe_workspace_bytes(plan, T) bytes, 256-byte aligned
+ * One persistent launch: grouping in the prologue, gate/up and down tickets,
+ * deterministic combine (bitwise identical run to run).  T > 24 is forwarded
+ * to moe_prefill unless strict mode is on (then MOE_ERR_NOT_FAST_PATH).
+ * No allocation and no synchronisation inside. */
+moe_status_t moe_decode(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
+                        float *y_dev, int T, void *ws_dev, void *stream);
+
+/* The same step for 1 <= T <= T_max (prefill chunks), same arguments.  Runs
+ * the persistent ticket kernel over chunks of at most 4096 / top_k tokens. */
+moe_status_t moe_prefill(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
+                         float *y_dev, int T, void *ws_dev, void *stream);
+
+/* Measurement variant of moe_decode/moe_prefill: streams exactly the same
+ * weight bytes through the same ticket schedule but skips dequantisation and
+ * all arithmetic; y receives a checksum, not the step's result (the pages'
+ * "null-decode" variant, "LNA-CANON.md", section "lna2 とは"). */
+moe_status_t moe_null_step(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
+                           float *y_dev, int T, void *ws_dev, void *stream);
+
+/* Synchronise `stream`, read and clear the workspace's device error word.
+ * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_BAD_EXPERT_ID or MOE_ERR_RANGE
+ * (the first set, in that order), or MOE_ERR_CUDA. */
+moe_status_t moe_check(moe_plan_t plan, void *ws_dev, void *stream);
+
+/* Test support for the failure path: set every phase-A completion counter in
+ * the workspace to a value no launch reaches, so the next step's bounded
+ * dependency waits expire (after the plan's wait limit, 1 s by default or
+ * MOE_WAIT_TIMEOUT_MS) and it reports MOE_ERR_TIMEOUT through moe_check
+ * instead of hanging.  Re-initialise the workspace afterwards. */
+moe_status_t moe_debug_poison_workspace(moe_plan_t plan, void *ws_dev, void *stream);
+
+/* Copy the plan's counters into *out. */
+moe_status_t moe_stats(moe_plan_t plan, moe_stats_t *out);
+
+/* Message for the calling thread's last error ("" if none). */
+const char *moe_last_error(void);
+
+/* Static name of a status code. */
+const char *moe_status_string(moe_status_t s);
+
+/* ABI version the library was built with (MOE_NVFP4_ABI_VERSION). */
+int moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_NVFP4_H */

@@ -1,0 +1,245 @@
+"""ctypes binding of libmoe_nvfp4.so (the C ABI in include/moe_nvfp4.h).
+
+Argument marshalling only: every step of the routed-experts computation runs
+in the library's sm_103a kernels.  The functions keep the ABI's names and take
+torch CUDA tensors where the ABI takes device pointers.  If the library is not
+built, or a call fails, a MoeError is raised -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmoe_nvfp4.so")
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_NOT_FAST_PATH",
+                4: "MOE_ERR_MISALIGNED", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_BAD_EXPERT_ID",
+                8: "MOE_ERR_RANGE"}
+MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_NOT_FAST_PATH, MOE_ERR_MISALIGNED = 1, 2, 3, 4
+MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_BAD_EXPERT_ID, MOE_ERR_RANGE = 5, 6, 7, 8
+
+# Every function include/moe_nvfp4.h declares: name -> (restype, argtypes).
+_P, _I, _S = C.c_void_p, C.c_int, C.c_size_t
+
+
+class moe_plan_desc(C.Structure):
+    _fields_ = [("H", C.c_int), ("I", C.c_int), ("E", C.c_int), ("top_k", C.c_int), ("T_max", C.c_int),
+                ("gate_q_dev", C.c_void_p), ("up_q_dev", C.c_void_p), ("down_q_dev", C.c_void_p),
+                ("gate_s_dev", C.c_void_p), ("up_s_dev", C.c_void_p), ("down_s_dev", C.c_void_p),
+                ("gate_ts_dev", C.c_void_p), ("up_ts_dev", C.c_void_p), ("down_ts_dev", C.c_void_p),
+                ("device", C.c_int), ("strict", C.c_int), ("pdl", C.c_int)]
+
+
+class moe_stats_t(C.Structure):
+    _fields_ = [("decode_launches", C.c_uint64), ("prefill_launches", C.c_uint64), ("null_launches", C.c_uint64),
+                ("group_launches", C.c_uint64), ("rejected_calls", C.c_uint64), ("num_sms", C.c_int),
+                ("stages", C.c_int), ("smem_bytes", C.c_int)]
+
+
+SIGNATURES = {
+    "moe_plan_create": (_I, [C.POINTER(moe_plan_desc), C.POINTER(C.c_void_p)]),
+    "moe_plan_destroy": (None, [_P]),
+    "moe_workspace_bytes": (_S, [_P, _I]),
+    "moe_workspace_init": (_I, [_P, _P, _S, _P]),
+    "moe_group": (_I, [_P, _P, _I, _P, _P, _P, _P, _P]),
+    "moe_decode": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
+    "moe_prefill": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
+    "moe_null_step": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
+    "moe_check": (_I, [_P, _P, _P]),
+    "moe_debug_poison_workspace": (_I, [_P, _P, _P]),
+    "moe_stats": (_I, [_P, C.POINTER(moe_stats_t)]),
+    "moe_last_error": (C.c_char_p, []),
+    "moe_status_string": (C.c_char_p, [_I]),
+    "moe_abi_version": (_I, []),
+}
+ABI_SYMBOLS = tuple(SIGNATURES)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load (once) and prototype the library; raises MoeError if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise MoeError(MOE_ERR_CUDA, f"{path} is not built (run __graft_entry__.build()); "
+                                         "there is no fallback path")
+        lib = C.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != MOE_OK:
+        raise MoeError(status, load_library().moe_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise MoeError(MOE_ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise MoeError(MOE_ERR_INVALID_ARG, f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise MoeError(MOE_ERR_INVALID_ARG, f"{name} must be contiguous")
+
+
+# ----------------------------------------------------------------------------- ABI functions
+def moe_plan_create(weights: dict, H: int, I: int, E: int, top_k: int, T_max: int, device: int = -1,
+                    strict: bool = False, pdl: bool = False):
+    """weights: dict with gate_q/up_q/down_q/gate_s/up_s/down_s (uint8) and
+    gate_ts/up_ts/down_ts (float32) CUDA tensors in the ABI layout."""
+    lib = load_library()
+    for n in ("gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s"):
+        _need(weights[n], torch.uint8, n)
+    for n in ("gate_ts", "up_ts", "down_ts"):
+        _need(weights[n], torch.float32, n)
+    d = moe_plan_desc(H, I, E, top_k, T_max,
+                      *[weights[n].data_ptr() for n in ("gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s",
+                                                        "gate_ts", "up_ts", "down_ts")],
+                      device, int(strict), int(pdl))
+    out = C.c_void_p()
+    _check(lib.moe_plan_create(C.byref(d), C.byref(out)))
+    return out
+
+
+def moe_plan_destroy(plan):
+    load_library().moe_plan_destroy(plan)
+
+
+def moe_workspace_bytes(plan, T: int) -> int:
+    return int(load_library().moe_workspace_bytes(plan, T))
+
+
+def moe_workspace_init(plan, ws, stream=None):
+    _check(load_library().moe_workspace_init(plan, _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_group(plan, ids, ws, counts, offsets, perm, stream=None):
+    _need(ids, torch.int32, "ids")
+    _check(load_library().moe_group(plan, _ptr(ids), ids.shape[0], _ptr(ws), _ptr(counts), _ptr(offsets),
+                                    _ptr(perm), _stream(stream)))
+
+
+def _step(fn, plan, x, ids, w, y, ws, stream):
+    _need(x, torch.bfloat16, "x")
+    _need(ids, torch.int32, "ids")
+    _need(w, torch.float32, "w")
+    _need(y, torch.float32, "y")
+    _check(fn(plan, _ptr(x), _ptr(ids), _ptr(w), _ptr(y), x.shape[0], _ptr(ws), _stream(stream)))
+
+
+def moe_decode(plan, x, ids, w, y, ws, stream=None):
+    _step(load_library().moe_decode, plan, x, ids, w, y, ws, stream)
+
+
+def moe_prefill(plan, x, ids, w, y, ws, stream=None):
+    _step(load_library().moe_prefill, plan, x, ids, w, y, ws, stream)
+
+
+def moe_null_step(plan, x, ids, w, y, ws, stream=None):
+    _step(load_library().moe_null_step, plan, x, ids, w, y, ws, stream)
+
+
+def moe_check(plan, ws, stream=None) -> int:
+    """Synchronise and return the device status code (0 = MOE_OK); clears it."""
+    return int(load_library().moe_check(plan, _ptr(ws), _stream(stream)))
+
+
+def moe_debug_poison_workspace(plan, ws, stream=None):
+    _check(load_library().moe_debug_poison_workspace(plan, _ptr(ws), _stream(stream)))
+
+
+def moe_stats(plan) -> dict:
+    s = moe_stats_t()
+    _check(load_library().moe_stats(plan, C.byref(s)))
+    return {f: getattr(s, f) for f, _ in moe_stats_t._fields_}
+
+
+def moe_last_error() -> str:
+    return load_library().moe_last_error().decode(errors="replace")
+
+
+def moe_status_string(status: int) -> str:
+    return load_library().moe_status_string(status).decode()
+
+
+def moe_abi_version() -> int:
+    return int(load_library().moe_abi_version())
+
+
+# ----------------------------------------------------------------------------- convenience wrapper
+class MoePlan:
+    """Owns a plan handle and keeps the weight tensors alive."""
+
+    def __init__(self, weights: dict, H: int, I: int, E: int, top_k: int, T_max: int, device=None,
+                 strict: bool = False, pdl: bool = False):
+        self.weights = weights
+        self.H, self.I, self.E, self.top_k, self.T_max = H, I, E, top_k, T_max
+        dev = weights["gate_q"].device.index if device is None else device
+        self.handle = moe_plan_create(weights, H, I, E, top_k, T_max, device=dev, strict=strict, pdl=pdl)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and _lib is not None:
+            _lib.moe_plan_destroy(h)
+            self.handle = None
+
+    def new_workspace(self, stream=None) -> torch.Tensor:
+        n = moe_workspace_bytes(self.handle, 1)
+        ws = torch.empty(n, dtype=torch.uint8, device=self.weights["gate_q"].device)
+        moe_workspace_init(self.handle, ws, stream)
+        return ws
+
+    def step(self, x, ids, w, ws, y=None, stream=None, null: bool = False):
+        if y is None:
+            y = torch.empty((x.shape[0], self.H), dtype=torch.float32, device=x.device)
+        if null:
+            moe_null_step(self.handle, x, ids, w, y, ws, stream)
+        elif x.shape[0] <= 24:
+            moe_decode(self.handle, x, ids, w, y, ws, stream)
+        else:
+            moe_prefill(self.handle, x, ids, w, y, ws, stream)
+        return y
+
+    def group(self, ids, ws, stream=None):
+        dev = ids.device
+        counts = torch.empty(self.E, dtype=torch.int32, device=dev)
+        offsets = torch.empty(self.E + 1, dtype=torch.int32, device=dev)
+        perm = torch.empty(ids.numel(), dtype=torch.int32, device=dev)
+        moe_group(self.handle, ids, ws, counts, offsets, perm, stream)
+        return counts, offsets, perm
+
+    def check(self, ws, stream=None) -> int:
+        return moe_check(self.handle, ws, stream)
+
+    def stats(self) -> dict:
+        return moe_stats(self.handle)

@@ -1,0 +1,481 @@
+// moe_abi.cu -- host side of the C ABI declared in include/moe_nvfp4.h:
+// argument validation, tile choice, workspace layout, launches, counters.
+// Every step of the routed-experts computation runs in moe_kernels.cu; this
+// file only checks, plans and enqueues.
+#include "moe_internal.h"
+#include "moe_nvfp4.h"
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status_t fail(moe_status_t s, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+int align16i(int v) { return (v + 15) & ~15; }
+
+bool env_flag(const char *name)
+{
+    const char *v = std::getenv(name);
+    return v && v[0] && std::strcmp(v, "0") != 0;
+}
+
+std::once_flag g_active_once;
+
+}  // namespace
+
+struct moe_plan {
+    moe_plan_desc d;
+    int device = 0, num_sms = 0, smem_optin = 0;
+    // tiling
+    int KA = 0, nPA = 0, KB = 0, nPB = 0, nHt = 0;
+    int strideA = 0, sstrideA = 0, strideB = 0, sstrideB = 0, blockScaleA = 0, blockScaleB = 0;
+    int stage_bytes = 0;
+    int Tc = 0;  // tokens per launch chunk
+    long long timeout_ns = 1000000000LL;
+    bool strict = false, pdl = false;
+    int smem_attr = 0;  // dynamic smem the kernel attribute currently allows
+    // workspace layout (bytes from the base)
+    size_t off_done = 0, off_cnt = 0, off_h = 0, off_part = 0, ws_bytes = 0;
+    std::mutex mu;
+    moe_stats_t stats{};
+};
+
+namespace {
+
+// Part size along K (a multiple of 128 dividing K, at most cap) and the smem
+// strides that make the consumer's shared-memory reads conflict-free:
+// nibble rows at a stride = 64 (mod 128); scale rows at an odd multiple of 16
+// (per-row copies, 16-byte aligned destinations) or the natural K/16 when that
+// is an odd multiple of 8 or 16 (one block copy, only when a part spans the
+// whole row).
+bool choose_part(int K, int cap, int *KP, int *stride, int *sstride, int *block)
+{
+    for (int kp = (K < cap ? K : cap) / 128 * 128; kp >= 128; kp -= 128) {
+        if (K % kp) continue;
+        int s = kp / 2;
+        if ((s / 64) % 2 == 0) s += 64;
+        const int kb = kp / 16;
+        if (kb % 16 == 0 && (K / 16) % 16 == 0) {
+            *KP = kp;
+            *stride = s;
+            *sstride = ((kb / 16) % 2 == 1) ? kb : kb + 16;
+            *block = 0;
+            return true;
+        }
+        const int nat = K / 16;
+        const bool odd8 = (nat % 8 == 0) && ((nat / 8) % 2 == 1);
+        const bool odd16 = (nat % 16 == 0) && ((nat / 16) % 2 == 1);
+        if (kp == K && (odd8 || odd16)) {
+            *KP = kp;
+            *stride = s;
+            *sstride = nat;
+            *block = 1;
+            return true;
+        }
+    }
+    return false;
+}
+
+moe::SmemLayout layout_for(const moe_plan *pl, int T)
+{
+    moe::SmemLayout L{};
+    const int P = T * pl->d.top_k;
+    const int pc = P < moe::kGroupPairs ? P : moe::kGroupPairs;
+    int ntmax = (pc + 7) / 8;
+    if (ntmax < 1) ntmax = 1;
+    const int red_need = 8192 * ntmax;
+    const int scr_need = align16i(2 * P) + 8 * pl->d.E + 4 + 16;
+    L.red_bytes = static_cast<int>(up(red_need > scr_need ? red_need : scr_need, 128));
+    L.tab_bytes = static_cast<int>(up(512 + 4 * align16i(2 * P) + align16i(P) + align16i(T), 128));
+    L.stage_bytes = pl->stage_bytes;
+    const int avail = pl->smem_optin - L.red_bytes - L.tab_bytes;
+    int ns = avail / pl->stage_bytes;
+    if (ns > moe::kMaxStages) ns = moe::kMaxStages;
+    L.NS = ns;
+    L.red_off = ns * pl->stage_bytes;
+    L.tab_off = L.red_off + L.red_bytes;
+    L.total = L.tab_off + L.tab_bytes;
+    return L;
+}
+
+moe_status_t check_device(const moe_plan *pl)
+{
+    int cur = -1;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (cur != pl->device)
+        return fail(MOE_ERR_INVALID_ARG, "current device %d is not the plan's device %d", cur, pl->device);
+    return MOE_OK;
+}
+
+void reject(moe_plan *pl)
+{
+    std::lock_guard<std::mutex> lk(pl->mu);
+    pl->stats.rejected_calls++;
+}
+
+enum class Path { Decode, Prefill, Null };
+
+moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, int T, void *ws,
+                      void *stream, Path path)
+{
+    if (!pl) return fail(MOE_ERR_INVALID_ARG, "null plan");
+    if (T < 0 || T > pl->d.T_max) {
+        reject(pl);
+        return fail(MOE_ERR_INVALID_ARG, "T=%d outside [0, T_max=%d]", T, pl->d.T_max);
+    }
+    if (T == 0) return MOE_OK;
+    if (!x || !ids || !w || !y || !ws) {
+        reject(pl);
+        return fail(MOE_ERR_INVALID_ARG, "null x/ids/w/y/workspace pointer");
+    }
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ids, 4) || !aligned(w, 4) || !aligned(ws, 256)) {
+        reject(pl);
+        return fail(MOE_ERR_MISALIGNED, "x and y need 16-byte, ids and w 4-byte, workspace 256-byte alignment");
+    }
+    if (path == Path::Decode && T > moe::kDecodeMaxT) {
+        if (pl->strict) {
+            reject(pl);
+            return fail(MOE_ERR_NOT_FAST_PATH, "strict: moe_decode takes T <= %d, got %d", moe::kDecodeMaxT, T);
+        }
+        path = Path::Prefill;
+    }
+    moe_status_t st = check_device(pl);
+    if (st != MOE_OK) {
+        reject(pl);
+        return st;
+    }
+    // kernel smem attribute: allow up to the device's opt-in limit (once per plan)
+    {
+        std::lock_guard<std::mutex> lk(pl->mu);
+        if (pl->smem_attr == 0) {
+            cudaError_t e = moe::set_step_smem_limit(pl->smem_optin);
+            if (e != cudaSuccess) {
+                pl->stats.rejected_calls++;
+                return fail(MOE_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            }
+            pl->smem_attr = pl->smem_optin;
+        }
+    }
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    moe::KernelParams p{};
+    p.gq = pl->d.gate_q_dev;
+    p.uq = pl->d.up_q_dev;
+    p.dq = pl->d.down_q_dev;
+    p.gs = pl->d.gate_s_dev;
+    p.us = pl->d.up_s_dev;
+    p.ds = pl->d.down_s_dev;
+    p.gts = pl->d.gate_ts_dev;
+    p.uts = pl->d.up_ts_dev;
+    p.dts = pl->d.down_ts_dev;
+    p.ctrl = reinterpret_cast<uint32_t *>(wsb);
+    p.doneA = reinterpret_cast<uint32_t *>(wsb + pl->off_done);
+    p.cnt = reinterpret_cast<uint32_t *>(wsb + pl->off_cnt);
+    p.hbuf = reinterpret_cast<uint16_t *>(wsb + pl->off_h);
+    p.part = reinterpret_cast<float *>(wsb + pl->off_part);
+    p.H = pl->d.H;
+    p.I = pl->d.I;
+    p.E = pl->d.E;
+    p.k = pl->d.top_k;
+    p.KA = pl->KA;
+    p.nPA = pl->nPA;
+    p.KB = pl->KB;
+    p.nPB = pl->nPB;
+    p.nHt = pl->nHt;
+    p.strideA = pl->strideA;
+    p.sstrideA = pl->sstrideA;
+    p.strideB = pl->strideB;
+    p.sstrideB = pl->sstrideB;
+    p.blockScaleA = pl->blockScaleA;
+    p.blockScaleB = pl->blockScaleB;
+    p.stage_bytes = pl->stage_bytes;
+    p.timeout_ns = pl->timeout_ns;
+    p.null_mode = path == Path::Null ? 1 : 0;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    for (int t0 = 0; t0 < T; t0 += pl->Tc) {
+        const int Tn = (T - t0) < pl->Tc ? (T - t0) : pl->Tc;
+        const moe::SmemLayout L = layout_for(pl, Tn);
+        if (L.NS < 2 || L.total > pl->smem_attr) {
+            reject(pl);
+            return fail(MOE_ERR_UNSUPPORTED_SHAPE, "shared-memory layout does not fit (%d stages, %d bytes)", L.NS,
+                        L.total);
+        }
+        p.T = Tn;
+        p.x = static_cast<const uint16_t *>(x) + static_cast<size_t>(t0) * pl->d.H;
+        p.ids = ids + static_cast<size_t>(t0) * pl->d.top_k;
+        p.w = w + static_cast<size_t>(t0) * pl->d.top_k;
+        p.y = y + static_cast<size_t>(t0) * pl->d.H;
+        p.NS = L.NS;
+        p.stage_bytes = L.stage_bytes;
+        p.red_off = L.red_off;
+        p.red_bytes = L.red_bytes;
+        p.tab_off = L.tab_off;
+        const int P = Tn * pl->d.top_k;
+        const int pc = P < moe::kGroupPairs ? P : moe::kGroupPairs;
+        p.ntmax = (pc + 7) / 8;
+        cudaError_t e = moe::launch_step(p, pl->num_sms, L.total, pl->pdl, cs);
+        if (e != cudaSuccess) {
+            reject(pl);
+            return fail(MOE_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+        }
+        ++launches;
+    }
+    {
+        std::lock_guard<std::mutex> lk(pl->mu);
+        if (path == Path::Null) pl->stats.null_launches += launches;
+        else if (path == Path::Prefill) pl->stats.prefill_launches += launches;
+        else pl->stats.decode_launches += launches;
+    }
+    if (!env_flag("MOE_QUIET"))
+        std::call_once(g_active_once, [&] {
+            std::fprintf(stderr, "moe_nvfp4: sm_103a routed-experts ticket kernel ACTIVE (%d SMs, %d-byte stages)\n",
+                         pl->num_sms, pl->stage_bytes);
+        });
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_NVFP4_ABI_VERSION; }
+
+const char *moe_last_error(void) { return g_last_error.c_str(); }
+
+const char *moe_status_string(moe_status_t s)
+{
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+        case MOE_ERR_NOT_FAST_PATH: return "MOE_ERR_NOT_FAST_PATH";
+        case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_BAD_EXPERT_ID: return "MOE_ERR_BAD_EXPERT_ID";
+        case MOE_ERR_RANGE: return "MOE_ERR_RANGE";
+    }
+    return "MOE_ERR_UNKNOWN";
+}
+
+moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
+{
+    if (!desc || !out) return fail(MOE_ERR_INVALID_ARG, "null desc or out");
+    *out = nullptr;
+    const moe_plan_desc &d = *desc;
+    if (d.H <= 0 || d.I <= 0 || d.H % 128 || d.I % 128)
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "H=%d and I=%d must be positive multiples of 128", d.H, d.I);
+    if (d.E < 1 || d.E > moe::kMaxExperts)
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "E=%d outside [1, %d]", d.E, moe::kMaxExperts);
+    if (d.top_k < 1 || d.top_k > moe::kMaxTopK)
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "top_k=%d outside [1, %d]", d.top_k, moe::kMaxTopK);
+    if (d.T_max < 1) return fail(MOE_ERR_INVALID_ARG, "T_max=%d must be >= 1", d.T_max);
+    const void *wp[] = {d.gate_q_dev, d.up_q_dev, d.down_q_dev, d.gate_s_dev, d.up_s_dev, d.down_s_dev};
+    for (const void *q : wp) {
+        if (!q) return fail(MOE_ERR_INVALID_ARG, "null weight pointer");
+        if (!aligned(q, 16)) return fail(MOE_ERR_MISALIGNED, "weight pointers must be 16-byte aligned");
+    }
+    const float *tp[] = {d.gate_ts_dev, d.up_ts_dev, d.down_ts_dev};
+    for (const float *q : tp) {
+        if (!q) return fail(MOE_ERR_INVALID_ARG, "null tensor-scale pointer");
+        if (!aligned(q, 4)) return fail(MOE_ERR_MISALIGNED, "tensor-scale pointers must be 4-byte aligned");
+    }
+    int dev = d.device;
+    cudaError_t e;
+    if (dev < 0) {
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    }
+    int sms = 0, optin = 0, major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+        return fail(MOE_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+    if (major != 10 || minor != 3)
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
+                    major, minor);
+
+    moe_plan *pl = new moe_plan();
+    pl->d = d;
+    pl->device = dev;
+    pl->num_sms = sms;
+    pl->smem_optin = optin;
+    pl->strict = d.strict != 0 || env_flag("MOE_STRICT");
+    pl->pdl = d.pdl != 0;
+    if (const char *t = std::getenv("MOE_WAIT_TIMEOUT_MS")) {
+        const long long ms = std::atoll(t);
+        if (ms > 0) pl->timeout_ns = ms * 1000000LL;
+    }
+    if (!choose_part(d.H, 2048, &pl->KA, &pl->strideA, &pl->sstrideA, &pl->blockScaleA) ||
+        !choose_part(d.I, 1024, &pl->KB, &pl->strideB, &pl->sstrideB, &pl->blockScaleB)) {
+        delete pl;
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "no stage tiling for H=%d, I=%d", d.H, d.I);
+    }
+    pl->nPA = d.H / pl->KA;
+    pl->nPB = d.I / pl->KB;
+    pl->nHt = d.H / moe::kMB;
+    const int stA = 32 * pl->strideA + 32 * pl->sstrideA;
+    const int stB = moe::kMB * pl->strideB + moe::kMB * pl->sstrideB;
+    pl->stage_bytes = static_cast<int>(up(stA > stB ? stA : stB, 128));
+    const int tc = moe::kMaxPairs / d.top_k;
+    pl->Tc = d.T_max < tc ? d.T_max : tc;
+    const moe::SmemLayout L = layout_for(pl, pl->Tc);
+    if (L.NS < 2 || L.total > optin) {
+        delete pl;
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "shared memory: %d stages of %d bytes do not fit", L.NS,
+                    pl->stage_bytes);
+    }
+    // workspace layout (fixed per plan)
+    size_t o = moe::kCtrlBytes;
+    pl->off_done = o;
+    o = up(o + 4 * static_cast<size_t>(moe::kMaxPairs), 256);
+    pl->off_cnt = o;
+    o = up(o + 4 * static_cast<size_t>(pl->Tc) * pl->nHt, 256);
+    const size_t Pc = static_cast<size_t>(pl->Tc) * d.top_k;
+    pl->off_h = o;
+    o = up(o + 2 * Pc * d.I, 256);
+    pl->off_part = o;
+    o = up(o + 4 * Pc * d.H, 256);
+    pl->ws_bytes = o;
+    pl->stats.num_sms = sms;
+    pl->stats.stages = L.NS;
+    pl->stats.smem_bytes = L.total;
+    *out = pl;
+    return MOE_OK;
+}
+
+void moe_plan_destroy(moe_plan_t plan) { delete plan; }
+
+size_t moe_workspace_bytes(moe_plan_t plan, int T)
+{
+    if (!plan || T < 1 || T > plan->d.T_max) return 0;
+    return plan->ws_bytes;
+}
+
+moe_status_t moe_workspace_init(moe_plan_t plan, void *ws_dev, size_t bytes, void *stream)
+{
+    if (!plan) return fail(MOE_ERR_INVALID_ARG, "null plan");
+    if (!ws_dev) return fail(MOE_ERR_INVALID_ARG, "null workspace");
+    if (!aligned(ws_dev, 256)) return fail(MOE_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    if (bytes < plan->ws_bytes)
+        return fail(MOE_ERR_INVALID_ARG, "workspace of %zu bytes < %zu needed", bytes, plan->ws_bytes);
+    moe_status_t st = check_device(plan);
+    if (st != MOE_OK) return st;
+    cudaError_t e = cudaMemsetAsync(ws_dev, 0, plan->ws_bytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+    return MOE_OK;
+}
+
+moe_status_t moe_group(moe_plan_t plan, const int32_t *ids_dev, int T, void *ws_dev, int32_t *counts_dev,
+                       int32_t *offsets_dev, int32_t *perm_dev, void *stream)
+{
+    if (!plan) return fail(MOE_ERR_INVALID_ARG, "null plan");
+    const int P = T * plan->d.top_k;
+    if (T < 1 || P > moe::kMaxPairs) {
+        reject(plan);
+        return fail(MOE_ERR_INVALID_ARG, "moe_group takes 1 <= T and T*top_k <= %d (T=%d)", moe::kMaxPairs, T);
+    }
+    if (!ids_dev || !counts_dev || !offsets_dev || !perm_dev || !ws_dev) {
+        reject(plan);
+        return fail(MOE_ERR_INVALID_ARG, "null pointer");
+    }
+    if (!aligned(ids_dev, 4) || !aligned(counts_dev, 4) || !aligned(offsets_dev, 4) || !aligned(perm_dev, 4) ||
+        !aligned(ws_dev, 256)) {
+        reject(plan);
+        return fail(MOE_ERR_MISALIGNED, "int32 arrays need 4-byte, workspace 256-byte alignment");
+    }
+    moe_status_t st = check_device(plan);
+    if (st != MOE_OK) {
+        reject(plan);
+        return st;
+    }
+    cudaError_t e = moe::launch_group(ids_dev, P, plan->d.E, static_cast<uint32_t *>(ws_dev), counts_dev,
+                                      offsets_dev, perm_dev, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        reject(plan);
+        return fail(MOE_ERR_CUDA, "grouping launch: %s", cudaGetErrorString(e));
+    }
+    std::lock_guard<std::mutex> lk(plan->mu);
+    plan->stats.group_launches++;
+    return MOE_OK;
+}
+
+moe_status_t moe_decode(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
+                        float *y_dev, int T, void *ws_dev, void *stream)
+{
+    return run_step(plan, x_dev, ids_dev, w_dev, y_dev, T, ws_dev, stream, Path::Decode);
+}
+
+moe_status_t moe_prefill(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
+                         float *y_dev, int T, void *ws_dev, void *stream)
+{
+    if (plan && T == 0) {
+        reject(plan);
+        return fail(MOE_ERR_INVALID_ARG, "moe_prefill takes T >= 1");
+    }
+    return run_step(plan, x_dev, ids_dev, w_dev, y_dev, T, ws_dev, stream, Path::Prefill);
+}
+
+moe_status_t moe_null_step(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
+                           float *y_dev, int T, void *ws_dev, void *stream)
+{
+    return run_step(plan, x_dev, ids_dev, w_dev, y_dev, T, ws_dev, stream, Path::Null);
+}
+
+moe_status_t moe_check(moe_plan_t plan, void *ws_dev, void *stream)
+{
+    if (!plan || !ws_dev) return fail(MOE_ERR_INVALID_ARG, "null plan or workspace");
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    cudaError_t e = cudaStreamSynchronize(cs);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&word, static_cast<uint8_t *>(ws_dev) + 8, 4, cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+    if (e == cudaSuccess && word) e = cudaMemsetAsync(static_cast<uint8_t *>(ws_dev) + 8, 0, 4, cs);
+    if (e == cudaSuccess && word) e = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "moe_check: %s", cudaGetErrorString(e));
+    if (word & moe::kErrTimeout) return fail(MOE_ERR_TIMEOUT, "a device-side wait timed out");
+    if (word & moe::kErrBadId) return fail(MOE_ERR_BAD_EXPERT_ID, "an expert id >= E was seen and skipped");
+    if (word & moe::kErrRange) return fail(MOE_ERR_RANGE, "an fp16 intermediate (h) overflowed");
+    return MOE_OK;
+}
+
+moe_status_t moe_debug_poison_workspace(moe_plan_t plan, void *ws_dev, void *stream)
+{
+    if (!plan || !ws_dev) return fail(MOE_ERR_INVALID_ARG, "null plan or workspace");
+    if (!aligned(ws_dev, 256)) return fail(MOE_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    cudaError_t e = moe::launch_poison(reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws_dev) + plan->off_done),
+                                       moe::kMaxPairs, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "poison launch: %s", cudaGetErrorString(e));
+    return MOE_OK;
+}
+
+moe_status_t moe_stats(moe_plan_t plan, moe_stats_t *out)
+{
+    if (!plan || !out) return fail(MOE_ERR_INVALID_ARG, "null plan or out");
+    std::lock_guard<std::mutex> lk(plan->mu);
+    *out = plan->stats;
+    return MOE_OK;
+}
+
+}  // extern "C"

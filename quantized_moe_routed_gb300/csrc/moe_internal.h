@@ -1,0 +1,75 @@
+// moe_internal.h -- parameter block and limits shared by the host ABI layer
+// (moe_abi.cu) and the sm_103a kernels (moe_kernels.cu).  Not part of the ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// CTA shape of the persistent ticket kernel: 8 consumer warps + 1 producer warp.
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;
+constexpr int kMaxPairs = 4096;     // T*k per launch (prefill is chunked to this)
+constexpr int kGroupPairs = 32;     // pairs per expert group = 4 MMA n-tiles of 8
+constexpr int kMaxTopK = 16;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxStages = 8;
+constexpr int kDecodeMaxT = 24;     // the pages' m <= 24 decode bound
+constexpr int kMB = 64;             // down-projection rows per phase-B ticket
+
+// Device error word bits (workspace control block, word 2).
+constexpr uint32_t kErrTimeout = 1u;
+constexpr uint32_t kErrBadId = 2u;
+constexpr uint32_t kErrRange = 4u;
+
+// Workspace control block (first 256 bytes of the workspace).
+//   word 0: ticket counter   word 1: CTAs finished   word 2: error bits
+constexpr size_t kCtrlBytes = 256;
+
+struct KernelParams {
+    // weights (NVFP4, layouts as in moe_nvfp4.h)
+    const uint8_t *gq, *uq, *dq;
+    const uint8_t *gs, *us, *ds;
+    const float *gts, *uts, *dts;
+    // step inputs / output
+    const uint16_t *x;  // bf16 bits [T, H]
+    const int32_t *ids; // [T, k]
+    const float *w;     // [T, k]
+    float *y;           // [T, H]
+    // workspace pieces
+    uint32_t *ctrl;     // control block
+    uint32_t *doneA;    // [kMaxPairs] per-group count of finished gate/up tickets
+    uint32_t *cnt;      // [T * nHt] per (token, H-tile) arrivals
+    uint16_t *hbuf;     // [P, I] fp16 h, rows in sorted pair order
+    float *part;        // [P, H] fp32 per-pair down-projection outputs
+    // shape
+    int H, I, E, k, T;
+    // tiling (chosen on the host)
+    int KA, nPA;        // gate/up: K elements per stage part, parts per ticket
+    int KB, nPB;        // down: K elements per stage part, parts per ticket
+    int nHt;            // H / kMB
+    int strideA, sstrideA, strideB, sstrideB;  // smem row strides (bytes)
+    int blockScaleA, blockScaleB;               // 1: scale rows copied as one block
+    int stage_bytes, NS;
+    int red_off, red_bytes, tab_off;            // smem layout (bytes)
+    int ntmax;                                  // MMA n-tiles needed (1..4)
+    long long timeout_ns;
+    int null_mode;      // 1: measurement variant (no dequant / math)
+};
+
+// Dynamic shared memory layout of the persistent kernel for P pairs.
+struct SmemLayout {
+    int stage_bytes, NS, red_off, red_bytes, tab_off, tab_bytes, total;
+};
+
+// Launch helpers implemented in moe_kernels.cu.
+cudaError_t launch_step(const KernelParams &p, int grid, int smem_bytes, bool pdl, cudaStream_t st);
+cudaError_t launch_group(const int32_t *ids, int P, int E, uint32_t *ctrl, int32_t *counts,
+                         int32_t *offsets, int32_t *perm, cudaStream_t st);
+cudaError_t launch_poison(uint32_t *doneA, int n, cudaStream_t st);
+cudaError_t set_step_smem_limit(int bytes);
+int group_smem_bytes(int P, int E);
+
+}  // namespace moe

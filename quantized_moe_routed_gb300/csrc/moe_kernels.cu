@@ -1,0 +1,1002 @@
+// moe_kernels.cu -- sm_103a kernels of the routed-experts MoE step over NVFP4
+// expert weights.
+//
+// The step (one MoE layer's routed experts):
+//   y_t = sum_j w_tj * W_down[e_tj] ( SiLU(W_gate[e_tj] x_t) (.) (W_up[e_tj] x_t) )
+//
+// Design (GB300 re-design of the pages' "lna2" idea -- "LNA-CANON.md",
+// section "lna2 とは": resident expert teams pull dynamic tickets, no grid-wide
+// barrier, small-R inner loops over the R_e rows an expert serves):
+//
+//  * One persistent CTA per SM.  Every CTA groups the T*k (token, slot) pairs
+//    by expert in shared memory (a stable counting sort; no separate launch),
+//    splitting an expert's pairs into groups of at most 32 (four 8-wide MMA
+//    n-tiles).
+//  * Tickets come from one atomic counter (the first one is the CTA index, so
+//    the first weight loads need no atomic).  Phase-A tickets (group, 16
+//    intermediate rows of gate and up) come first, then phase-B tickets
+//    (group, 64 rows of down).  Each CTA takes tickets in increasing order, so
+//    every phase-A ticket is held by a running CTA before any phase-B ticket
+//    is handed out: the per-group completion counter a phase-B ticket waits on
+//    is guaranteed to fill, and no grid barrier is needed (the pages' barrier
+//    version F1 was correct but not faster, "LNA-CANON.md", "含めないもの").
+//  * A producer warp streams each ticket's packed E2M1 rows and E4M3 scale
+//    rows HBM -> shared memory with cp.async.bulk (one row per lane, L2
+//    evict-first), into a ring of stages guarded by mbarriers; it keeps
+//    prefetching while consumers wait on a dependency.
+//  * Eight consumer warps dequantise in registers -- cvt e2m1x2 -> f16x2, times
+//    the block scale (E2M1 x E4M3 is exact in fp16) -- and run mma.sync
+//    m16n8k16 (fp16 operands, fp32 accumulate) with weight rows as M and the
+//    group's pairs as N.  Activations (x for gate/up, h for down) are the
+//    B operand; the K order inside each thread is permuted identically on both
+//    operands, so every thread reads 16 contiguous bytes of a weight row.
+//  * h = SiLU(g) * u goes to a workspace buffer (fp16) after a fixed-order
+//    cross-warp reduction; down outputs go to per-pair fp32 partials; the last
+//    CTA to finish a (token, 64-row tile) sums its k partials in slot order.
+//    No floating-point atomics anywhere: results are bitwise reproducible.
+//  * Every wait is bounded (globaltimer); a timeout sets the workspace error
+//    word and the CTA drains and returns.  The last CTA out resets the
+//    workspace counters, so a workspace needs zeroing only once.
+#include "moe_internal.h"
+
+#include <cuda_fp16.h>
+
+namespace moe {
+namespace {
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t gtimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_nc16(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_cg16(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ldg_cg_f32(const float *p)
+{
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void consumer_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+}
+
+// Four E2M1 pairs (one 32-bit word, element 2i in the low nibble of byte i)
+// -> four f16x2 {element 2i (low half), element 2i+1 (high half)}.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t &o0, uint32_t &o1, uint32_t &o2, uint32_t &o3)
+{
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+        : "r"(w));
+}
+
+// Two E4M3 scale bytes (low byte first) -> f16x2 {low, high}; exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v)
+{
+    uint32_t o;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o) : "h"(v));
+    return o;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Two bf16 (element 2i low) -> f16x2 (round to nearest even; exact in range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u)
+{
+    float lo = __uint_as_float(u << 16), hi = __uint_as_float(u & 0xffff0000u);
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t u4w(const uint4 &v, int i)
+{
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// ------------------------------------------------------------------ shared state
+struct SmemHdr {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    int4 stage_hdr[kMaxStages];  // {kind, group, tile, part}
+    int n_groups, n_valid, n_bad, abort_flag;  // abort_flag: any role gave up (read by waits)
+    int n_comb, fill_cnt, cons_cnt, cflag;     // fills issued / fills seen complete / consumer verdict
+    int comb_tok[kGroupPairs];
+};
+static_assert(sizeof(SmemHdr) <= 512, "header too large");
+
+enum { KIND_A = 0, KIND_B = 1, KIND_END = 2 };
+
+struct Tabs {
+    SmemHdr *hdr;
+    uint16_t *perm;   // [P] sorted pair list (flat pair index t*k+j)
+    uint16_t *pos;    // [P] inverse: sorted position of pair p, 0xFFFF if invalid
+    uint16_t *gexp;   // [P] group -> expert
+    uint16_t *gbeg;   // [P] group -> first sorted position
+    uint8_t *gcnt;    // [P] group -> number of pairs (1..32)
+    uint8_t *kvalid;  // [T] valid slots per token
+};
+
+__host__ __device__ inline int align16(int v) { return (v + 15) & ~15; }
+
+__device__ Tabs make_tabs(uint8_t *smem, int tab_off, int P)
+{
+    Tabs t;
+    uint8_t *b = smem + tab_off;
+    t.hdr = reinterpret_cast<SmemHdr *>(b);
+    int o = 512;
+    t.perm = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
+    t.pos = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
+    t.gexp = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
+    t.gbeg = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
+    t.gcnt = b + o; o += align16(P);
+    t.kvalid = b + o;
+    return t;
+}
+
+// ------------------------------------------------------------------ grouping
+// Stable counting sort of the P flat pairs p = t*k + j by expert id, run by all
+// threads of the CTA.  Scratch (ids16 [P], ecnt [E], eoff [E+1]) may alias
+// anything not otherwise live.  Results: perm/pos (see Tabs), *n_valid, *n_bad,
+// eoff (exclusive offsets, eoff[E] = n_valid) and ecnt (counts).
+__device__ void group_pairs(const int32_t *__restrict__ ids, int P, int E, int16_t *ids16, int32_t *ecnt,
+                            int32_t *eoff, uint16_t *perm, uint16_t *pos, int *n_valid, int *n_bad)
+{
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) *n_bad = 0;
+    for (int e = tid; e < E; e += nthr) ecnt[e] = 0;
+    __syncthreads();
+    int bad = 0;
+    for (int p = tid; p < P; p += nthr) {
+        int e = ids[p];
+        if (e >= E) ++bad;
+        ids16[p] = (e >= 0 && e < E) ? static_cast<int16_t>(e) : static_cast<int16_t>(-1);
+    }
+    if (bad) atomicAdd(n_bad, bad);
+    __syncthreads();
+    for (int p = tid; p < P; p += nthr) {
+        int e = ids16[p];
+        if (e >= 0) atomicAdd(&ecnt[e], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive scan of ecnt over E entries, lanes own contiguous ranges
+        const int per = (E + 31) / 32;
+        const int lo = min(E, lane * per), hi = min(E, lo + per);
+        int s = 0;
+        for (int e = lo; e < hi; ++e) s += ecnt[e];
+        int incl = s;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        int run = incl - s;
+        for (int e = lo; e < hi; ++e) {
+            eoff[e] = run;
+            run += ecnt[e];
+        }
+        if (lane == 31) eoff[E] = incl;
+        __syncwarp();
+        // stable scatter: pairs in index order, 32 at a time
+        for (int base = 0; base < P; base += 32) {
+            const int p = base + lane;
+            const int e = (p < P) ? ids16[p] : -2;
+            const uint32_t peers = __match_any_sync(0xffffffffu, e);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            int dst = 0;
+            if (e >= 0) dst = eoff[e] + rank;  // eoff doubles as the running cursor
+            __syncwarp();
+            if (e >= 0) {
+                perm[dst] = static_cast<uint16_t>(p);
+                pos[p] = static_cast<uint16_t>(dst);
+                if (rank == 0) eoff[e] += __popc(peers);
+            } else if (p < P) {
+                pos[p] = 0xFFFFu;
+            }
+            __syncwarp();
+        }
+        // restore exclusive offsets (the cursor now points one past each range)
+        for (int e = lo; e < hi; ++e) eoff[e] -= ecnt[e];
+        __syncwarp();
+        if (lane == 0) *n_valid = eoff[E];
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------ bounded waits
+__device__ __noinline__ void raise_error(const KernelParams &p, volatile int *abort_flag, uint32_t bits)
+{
+    atomicOr(p.ctrl + 2, bits);
+    if (abort_flag) *abort_flag = 1;
+}
+
+// Wait for an mbarrier phase; false if the CTA aborted or the wait timed out.
+__device__ bool wait_bar(uint64_t *bar, uint32_t parity, const KernelParams &p, volatile int *abort_flag)
+{
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_test(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
+                raise_error(p, abort_flag, kErrTimeout);
+                return false;
+            }
+            if ((it & 1023u) == 0 && (ld_relaxed(p.ctrl + 2) & kErrTimeout)) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Wait until *ctr == target (acquire); false on abort / timeout.
+__device__ bool wait_count(const uint32_t *ctr, uint32_t target, const KernelParams &p, volatile int *abort_flag)
+{
+    if (ld_acquire(ctr) == target) return true;
+    const uint64_t t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(64);
+        if (ld_acquire(ctr) == target) return true;
+        if ((it & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
+                raise_error(p, abort_flag, kErrTimeout);
+                return false;
+            }
+            if (ld_relaxed(p.ctrl + 2) & kErrTimeout) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ MMA over one 128-element chunk
+// rows0/srows0: first nibble/scale row of this warp's m-group in the stage,
+// already offset to the chunk (64 bytes / 8 bytes per chunk).  bq: the chunk's
+// B operand for this thread (elements 32t .. 32t+31 of the chunk for the pair
+// of n-tile nt, column g), bf16 (x) or fp16 (h).
+//
+// K order inside a k16 step: thread t holds elements 4s..4s+3 of its 32-element
+// slice at k-step s; A register 0/1 (rows g, g+8) and B register 0 take
+// elements 4s, 4s+1; A register 2/3 and B register 1 take 4s+2, 4s+3.  Both
+// operands follow the same order, so the dot products are the plain ones.
+template <int MT, int NT, bool BF16B, bool NULLM>
+__device__ __forceinline__ void chunk_mma(const uint8_t *rows0, int stride, const uint8_t *srows0, int sstride,
+                                          const uint4 (&bq)[NT][4], float (&acc)[MT][NT][4], int g, int t)
+{
+    uint4 ra[MT], rb[MT];
+    uint32_t sa[MT][2], sb[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const uint8_t *r0 = rows0 + (mt * 16 + g) * stride + t * 16;
+        ra[mt] = *reinterpret_cast<const uint4 *>(r0);
+        rb[mt] = *reinterpret_cast<const uint4 *>(r0 + 8 * stride);
+        const uint8_t *s0 = srows0 + (mt * 16 + g) * sstride + t * 2;
+        const uint32_t s_a = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(s0));
+        const uint32_t s_b = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(s0 + 8 * sstride));
+        sa[mt][0] = __byte_perm(s_a, 0, 0x1010);
+        sa[mt][1] = __byte_perm(s_a, 0, 0x3232);
+        sb[mt][0] = __byte_perm(s_b, 0, 0x1010);
+        sb[mt][1] = __byte_perm(s_b, 0, 0x3232);
+    }
+    if constexpr (NULLM) {
+        // measurement variant: keep the loads live, no dequant, no MMA
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            uint32_t x = ra[mt].x ^ ra[mt].y ^ ra[mt].z ^ ra[mt].w ^ rb[mt].x ^ rb[mt].y ^ rb[mt].z ^ rb[mt].w ^
+                         sa[mt][0] ^ sb[mt][1];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) x ^= bq[nt][0].x ^ bq[nt][3].w;
+            acc[mt][0][0] += __uint_as_float(x & 0x3f7fffffu);
+        }
+    } else {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            uint32_t bf[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t u = u4w(bq[nt][v], i);
+                    bf[nt][i] = BF16B ? bf16x2_to_f16x2(u) : u;
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                uint32_t fa0, fa1, fa2, fa3, fb0, fb1, fb2, fb3;
+                e2m1x8_to_f16x2(u4w(ra[mt], v), fa0, fa1, fa2, fa3);
+                e2m1x8_to_f16x2(u4w(rb[mt], v), fb0, fb1, fb2, fb3);
+                const uint32_t sA = sa[mt][v >> 1], sB = sb[mt][v >> 1];
+                fa0 = hmul2(fa0, sA); fa1 = hmul2(fa1, sA); fa2 = hmul2(fa2, sA); fa3 = hmul2(fa3, sA);
+                fb0 = hmul2(fb0, sB); fb1 = hmul2(fb1, sB); fb2 = hmul2(fb2, sB); fb3 = hmul2(fb3, sB);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma16816(acc[mt][nt], fa0, fb0, fa1, fb1, bf[nt][0], bf[nt][1]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma16816(acc[mt][nt], fa2, fb2, fa3, fb3, bf[nt][2], bf[nt][3]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ consumer context
+struct Cons {
+    const KernelParams *p;
+    uint8_t *smem;
+    Tabs tb;
+    float4 *red;
+    int warp, lane, g, t, tid;
+    int s;          // ring stage
+    uint32_t ph;    // parity of the ring pass
+    volatile int *abort_flag;
+};
+
+__device__ __forceinline__ void cons_release_stage(Cons &c)
+{
+    __syncwarp();
+    if (c.lane == 0) mbar_arrive(&c.tb.hdr->empty[c.s]);
+    if (++c.s == c.p->NS) {
+        c.s = 0;
+        c.ph ^= 1u;
+    }
+}
+
+// Wait for the next stage; returns its header (KIND_END on abort).  Consumer
+// thread 0 takes the bounded wait and publishes the verdict before a named
+// barrier, so all 256 consumer threads take the same branch; every thread then
+// observes the completed phase itself (acquire) before reading the stage.
+__device__ __forceinline__ int4 cons_next_stage(Cons &c)
+{
+    SmemHdr *hd = c.tb.hdr;
+    if (c.tid == 0) {
+        const bool ok = wait_bar(&hd->full[c.s], c.ph, *c.p, c.abort_flag);
+        hd->cflag = ok ? 1 : 0;
+        if (ok) hd->cons_cnt += 1;
+    }
+    consumer_sync();
+    if (!hd->cflag) return make_int4(KIND_END, 0, 0, 0);
+    for (int i = 0; i < 64 && !mbar_test(&hd->full[c.s], c.ph); ++i) {
+    }
+    return hd->stage_hdr[c.s];
+}
+
+// B-operand loads for one chunk: 4 x 16 bytes per n-tile.
+template <int NT, bool CG>
+__device__ __forceinline__ void load_bq(uint4 (&bq)[NT][4], const uint16_t *const (&bptr)[NT], int kglob)
+{
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        if (bptr[nt]) {
+            const uint16_t *src = bptr[nt] + kglob;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) bq[nt][v] = CG ? ldg_cg16(src + 8 * v) : ldg_nc16(src + 8 * v);
+        } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) bq[nt][v] = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+// ---- phase A: gate/up rows i0..i0+15 for one group -> h (fp16)
+template <int NT, bool NULLM>
+__device__ __noinline__ bool ticket_A(Cons &c, int grp, int tile)
+{
+    const KernelParams &p = *c.p;
+    const int e = c.tb.gexp[grp], gbeg = c.tb.gbeg[grp], gcnt = c.tb.gcnt[grp];
+    const int i0 = tile * 16;
+    const uint16_t *bptr[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int n = nt * 8 + c.g;
+        bptr[nt] = nullptr;
+        if (n < gcnt) {
+            const int pr = c.tb.perm[gbeg + n];
+            bptr[nt] = p.x + static_cast<size_t>(pr / p.k) * p.H + c.t * 32;
+        }
+    }
+    float acc[2][NT][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < NT; ++b)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[a][b][r] = 0.f;
+
+    const int chunks = p.KA / 128;
+    const int ks = c.warp;  // K-slices = 8 consumer warps
+    for (int part = 0; part < p.nPA; ++part) {
+        if (part > 0) {
+            const int4 h = cons_next_stage(c);
+            if (h.x == KIND_END) return false;
+        }
+        const uint8_t *st = c.smem + c.s * p.stage_bytes;
+        const uint8_t *srows = st + 32 * p.strideA;
+        constexpr bool DB = NT <= 2;  // prefetch the next chunk's B operand (register budget)
+        int q = ks;
+        uint4 bq[NT][4], bn[NT][4];
+        if (DB && q < chunks) load_bq<NT, false>(bq, bptr, part * p.KA + q * 128);
+        for (; q < chunks; q += kConsumerWarps) {
+            const int qn = q + kConsumerWarps;
+            if (!DB) load_bq<NT, false>(bq, bptr, part * p.KA + q * 128);
+            if (DB && qn < chunks) load_bq<NT, false>(bn, bptr, part * p.KA + qn * 128);
+            chunk_mma<2, NT, true, NULLM>(st + q * 64, p.strideA, srows + q * 8, p.sstrideA, bq, acc, c.g, c.t);
+            if (DB && qn < chunks) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) bq[nt][v] = bn[nt][v];
+            }
+        }
+        cons_release_stage(c);
+    }
+    // cross-warp reduction (fixed order) -> g, u -> h
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            c.red[((ks * 2 + mt) * NT + nt) * 32 + c.lane] =
+                make_float4(acc[mt][nt][0], acc[mt][nt][1], acc[mt][nt][2], acc[mt][nt][3]);
+    consumer_sync();
+    const float tsg = p.gts[e], tsu = p.uts[e];
+    const float *redf = reinterpret_cast<const float *>(c.red);
+    bool range_bad = false;
+    for (int idx = c.tid; idx < NT * 128; idx += kConsumerThreads) {
+        const int nt = idx >> 7, ls = (idx >> 2) & 31, r = idx & 3;
+        float sg = 0.f, su = 0.f;
+#pragma unroll
+        for (int k2 = 0; k2 < kConsumerWarps; ++k2) {
+            sg += redf[(((k2 * 2 + 0) * NT + nt) * 32 + ls) * 4 + r];
+            su += redf[(((k2 * 2 + 1) * NT + nt) * 32 + ls) * 4 + r];
+        }
+        const int row = (ls >> 2) + 8 * (r >> 1);
+        const int n = nt * 8 + 2 * (ls & 3) + (r & 1);
+        if (n < gcnt) {
+            const float gv = sg * tsg, uv = su * tsu;
+            float hv = gv / (1.0f + __expf(-gv)) * uv;
+            if (NULLM) hv = 0.f;
+            if (!(fabsf(hv) <= 65504.0f)) range_bad = true;
+            p.hbuf[static_cast<size_t>(gbeg + n) * p.I + i0 + row] = __half_as_ushort(__float2half_rn(hv));
+        }
+    }
+    if (range_bad) atomicOr(p.ctrl + 2, kErrRange);
+    consumer_sync();
+    if (c.tid == 0) {
+        __threadfence();
+        atomicAdd(p.doneA + grp, 1u);
+    }
+    return true;
+}
+
+// ---- phase B: down rows h0..h0+63 for one group -> partials, then combine
+template <int NT, bool NULLM>
+__device__ __noinline__ bool ticket_B(Cons &c, int grp, int tile)
+{
+    const KernelParams &p = *c.p;
+    const int e = c.tb.gexp[grp], gbeg = c.tb.gbeg[grp], gcnt = c.tb.gcnt[grp];
+    const int h0 = tile * kMB;
+    // the group's h rows must be complete: one thread waits (acquire), the
+    // verdict is published before the barrier so every consumer agrees
+    if (c.tid == 0) {
+        const bool ok = wait_count(p.doneA + grp, static_cast<uint32_t>(p.I / 16), p, c.abort_flag);
+        c.tb.hdr->cflag = ok ? 1 : 0;
+        if (!ok) *c.abort_flag = 1;
+    }
+    consumer_sync();
+    if (!c.tb.hdr->cflag) return false;
+    const uint16_t *bptr[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int n = nt * 8 + c.g;
+        bptr[nt] = (n < gcnt) ? p.hbuf + static_cast<size_t>(gbeg + n) * p.I + c.t * 32 : nullptr;
+    }
+    float acc[2][NT][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < NT; ++b)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[a][b][r] = 0.f;
+
+    const int chunks = p.KB / 128;
+    const int ks = c.warp & 3, mg = c.warp >> 2;  // 4 K-slices x 2 m-groups of 2 m-tiles
+    for (int part = 0; part < p.nPB; ++part) {
+        if (part > 0) {
+            const int4 h = cons_next_stage(c);
+            if (h.x == KIND_END) return false;
+        }
+        const uint8_t *st = c.smem + c.s * p.stage_bytes;
+        const uint8_t *rows = st + mg * 32 * p.strideB;
+        const uint8_t *srows = st + kMB * p.strideB + mg * 32 * p.sstrideB;
+        constexpr bool DB = NT <= 2;
+        int q = ks;
+        uint4 bq[NT][4], bn[NT][4];
+        if (DB && q < chunks) load_bq<NT, true>(bq, bptr, part * p.KB + q * 128);
+        for (; q < chunks; q += 4) {
+            const int qn = q + 4;
+            if (!DB) load_bq<NT, true>(bq, bptr, part * p.KB + q * 128);
+            if (DB && qn < chunks) load_bq<NT, true>(bn, bptr, part * p.KB + qn * 128);
+            chunk_mma<2, NT, false, NULLM>(rows + q * 64, p.strideB, srows + q * 8, p.sstrideB, bq, acc, c.g, c.t);
+            if (DB && qn < chunks) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) bq[nt][v] = bn[nt][v];
+            }
+        }
+        cons_release_stage(c);
+    }
+    // cross-warp reduction over the 4 K-slices -> o -> per-pair partials
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            c.red[((ks * 4 + mg * 2 + mt) * NT + nt) * 32 + c.lane] =
+                make_float4(acc[mt][nt][0], acc[mt][nt][1], acc[mt][nt][2], acc[mt][nt][3]);
+    if (c.tid == 0) c.tb.hdr->n_comb = 0;
+    consumer_sync();
+    const float tsd = p.dts[e];
+    const float *redf = reinterpret_cast<const float *>(c.red);
+    for (int idx = c.tid; idx < 4 * NT * 128; idx += kConsumerThreads) {
+        const int mm = idx / (NT * 128), rem = idx - mm * (NT * 128);
+        const int nt = rem >> 7, ls = (rem >> 2) & 31, r = rem & 3;
+        float so = 0.f;
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) so += redf[(((k2 * 4 + mm) * NT + nt) * 32 + ls) * 4 + r];
+        const int row = mm * 16 + (ls >> 2) + 8 * (r >> 1);
+        const int n = nt * 8 + 2 * (ls & 3) + (r & 1);
+        if (n < gcnt) p.part[static_cast<size_t>(gbeg + n) * p.H + h0 + row] = so * tsd;
+    }
+    consumer_sync();
+    // count arrivals per (token, tile); the last arriver combines that token
+    if (c.tid < gcnt) {
+        const int pr = c.tb.perm[gbeg + c.tid];
+        const int tok = pr / p.k;
+        uint32_t *ctr = p.cnt + static_cast<size_t>(tok) * p.nHt + tile;
+        __threadfence();
+        const uint32_t old = atomicAdd(ctr, 1u);
+        if (old + 1u == static_cast<uint32_t>(c.tb.kvalid[tok])) {
+            *ctr = 0u;  // last arrival: reset for the next launch
+            __threadfence();
+            const int slot = atomicAdd(&c.tb.hdr->n_comb, 1);
+            c.tb.hdr->comb_tok[slot] = tok;
+        }
+    }
+    consumer_sync();
+    const int ncomb = c.tb.hdr->n_comb;
+    for (int idx = c.tid; idx < ncomb * kMB; idx += kConsumerThreads) {
+        const int tok = c.tb.hdr->comb_tok[idx / kMB];
+        const int row = idx % kMB;
+        float yv = 0.f;
+        for (int j = 0; j < p.k; ++j) {
+            const int ps = c.tb.pos[tok * p.k + j];
+            if (ps != 0xFFFF) yv += p.w[tok * p.k + j] * ldg_cg_f32(p.part + static_cast<size_t>(ps) * p.H + h0 + row);
+        }
+        p.y[static_cast<size_t>(tok) * p.H + h0 + row] = yv;
+    }
+    consumer_sync();
+    return true;
+}
+
+template <bool NULLM>
+__device__ __forceinline__ void consumer_loop(Cons &c)
+{
+    for (;;) {
+        const int4 h = cons_next_stage(c);
+        if (h.x == KIND_END) break;
+        const int grp = h.y, tile = h.z;
+        const int nt = (c.tb.gcnt[grp] + 7) >> 3;
+        bool ok;
+        if (h.x == KIND_A) {
+            switch (nt) {
+                case 1: ok = ticket_A<1, NULLM>(c, grp, tile); break;
+                case 2: ok = ticket_A<2, NULLM>(c, grp, tile); break;
+                case 3: ok = ticket_A<3, NULLM>(c, grp, tile); break;
+                default: ok = ticket_A<4, NULLM>(c, grp, tile); break;
+            }
+        } else {
+            switch (nt) {
+                case 1: ok = ticket_B<1, NULLM>(c, grp, tile); break;
+                case 2: ok = ticket_B<2, NULLM>(c, grp, tile); break;
+                case 3: ok = ticket_B<3, NULLM>(c, grp, tile); break;
+                default: ok = ticket_B<4, NULLM>(c, grp, tile); break;
+            }
+        }
+        if (!ok) break;  // uniform: decided from a flag published before a barrier
+    }
+}
+
+// ------------------------------------------------------------------ producer
+__device__ __noinline__ void producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, volatile int *abort_flag)
+{
+    const int lane = threadIdx.x & 31;
+    SmemHdr *hd = tb.hdr;
+    const uint64_t pol = policy_evict_first();
+    const int ng = hd->n_groups;
+    const int TA = p.I / 16;
+    const int nA = ng * TA;
+    const int total = nA + ng * p.nHt;
+    const uint32_t bytesA = 32u * (p.KA / 2) + 32u * (p.KA / 16);
+    const uint32_t bytesB = kMB * (p.KB / 2) + kMB * (p.KB / 16);
+    int s = 0;
+    uint32_t ph = 0;
+    int ticket = blockIdx.x;
+    while (ticket < total) {
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        int next = 0;
+        if (lane == 0) next = static_cast<int>(gridDim.x + atomicAdd(p.ctrl, 1u));
+        const bool isA = ticket < nA;
+        const int tt = isA ? ticket : ticket - nA;
+        const int grp = isA ? tt / TA : tt / p.nHt;
+        const int tile = isA ? tt % TA : tt % p.nHt;
+        const int e = tb.gexp[grp];
+        const int nparts = isA ? p.nPA : p.nPB;
+        bool ok = true;
+        for (int part = 0; part < nparts; ++part) {
+            int got = 0;
+            if (lane == 0) got = wait_bar(&hd->empty[s], ph ^ 1u, p, abort_flag) ? 1 : 0;
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) {
+                ok = false;
+                break;
+            }
+            uint8_t *st = smem + s * p.stage_bytes;
+            if (lane == 0) {
+                hd->stage_hdr[s] = make_int4(isA ? KIND_A : KIND_B, grp, tile, part);
+                mbar_expect_tx(&hd->full[s], isA ? bytesA : bytesB);
+            }
+            __syncwarp();
+            if (isA) {
+                // 32 rows: 0..15 gate rows i0.., 16..31 up rows i0..
+                const int r = lane;
+                const size_t row = static_cast<size_t>(e) * p.I + tile * 16 + (r & 15);
+                const uint8_t *q = (r < 16 ? p.gq : p.uq) + row * (p.H / 2) + part * (p.KA / 2);
+                bulk_g2s(st + r * p.strideA, q, p.KA / 2, &hd->full[s], pol);
+                uint8_t *sdst = st + 32 * p.strideA;
+                if (p.blockScaleA) {
+                    if (lane < 2) {
+                        const uint8_t *sc =
+                            (lane == 0 ? p.gs : p.us) + (static_cast<size_t>(e) * p.I + tile * 16) * (p.H / 16);
+                        bulk_g2s(sdst + lane * 16 * p.sstrideA, sc, 16 * (p.H / 16), &hd->full[s], pol);
+                    }
+                } else {
+                    const uint8_t *sc = (r < 16 ? p.gs : p.us) + row * (p.H / 16) + part * (p.KA / 16);
+                    bulk_g2s(sdst + r * p.sstrideA, sc, p.KA / 16, &hd->full[s], pol);
+                }
+            } else {
+                uint8_t *sdst = st + kMB * p.strideB;
+                for (int r = lane; r < kMB; r += 32) {
+                    const size_t row = static_cast<size_t>(e) * p.H + tile * kMB + r;
+                    bulk_g2s(st + r * p.strideB, p.dq + row * (p.I / 2) + part * (p.KB / 2), p.KB / 2, &hd->full[s],
+                             pol);
+                    if (!p.blockScaleB)
+                        bulk_g2s(sdst + r * p.sstrideB, p.ds + row * (p.I / 16) + part * (p.KB / 16), p.KB / 16,
+                                 &hd->full[s], pol);
+                }
+                if (p.blockScaleB && lane == 0) {
+                    const uint8_t *sc = p.ds + (static_cast<size_t>(e) * p.H + tile * kMB) * (p.I / 16);
+                    bulk_g2s(sdst, sc, kMB * (p.I / 16), &hd->full[s], pol);
+                }
+            }
+            if (lane == 0) hd->fill_cnt += 1;
+            if (++s == p.NS) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+        ticket = __shfl_sync(0xffffffffu, next, 0);
+        if (!ok) break;
+    }
+    // end marker (the consumers' waits also end on the abort flag)
+    if (lane == 0) {
+        if (wait_bar(&hd->empty[s], ph ^ 1u, p, abort_flag)) {
+            hd->stage_hdr[s] = make_int4(KIND_END, 0, 0, 0);
+            mbar_arrive(&hd->full[s]);
+        } else {
+            *abort_flag = 1;
+        }
+    }
+    __syncwarp();
+}
+
+// ------------------------------------------------------------------ the persistent step kernel
+template <bool NULLM>
+__global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_constant__ KernelParams p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x;
+    const int P = p.T * p.k;
+    Tabs tb = make_tabs(smem, p.tab_off, P);
+    SmemHdr *hd = tb.hdr;
+    volatile int *abort_flag = &hd->abort_flag;
+
+    // the previous grid on this stream (if launched with PDL) must finish first
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    if (tid == 0) {
+        for (int i = 0; i < p.NS; ++i) {
+            mbar_init(&hd->full[i], 1);
+            mbar_init(&hd->empty[i], kConsumerWarps);
+        }
+        hd->abort_flag = 0;
+        hd->fill_cnt = 0;
+        hd->cons_cnt = 0;
+        hd->cflag = 1;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // grouping (every CTA, redundantly; scratch aliases the reduction buffer)
+    {
+        uint8_t *scr = smem + p.red_off;
+        int16_t *ids16 = reinterpret_cast<int16_t *>(scr);
+        int32_t *ecnt = reinterpret_cast<int32_t *>(scr + align16(2 * P));
+        int32_t *eoff = ecnt + p.E;
+        group_pairs(p.ids, P, p.E, ids16, ecnt, eoff, tb.perm, tb.pos, &hd->n_valid, &hd->n_bad);
+        // split each expert's pairs into groups of <= 32
+        if (tid < 32) {
+            const int lane = tid;
+            const int per = (p.E + 31) / 32;
+            const int lo = min(p.E, lane * per), hi = min(p.E, lo + per);
+            int s = 0;
+            for (int e2 = lo; e2 < hi; ++e2) s += (ecnt[e2] + kGroupPairs - 1) / kGroupPairs;
+            int incl = s;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                int v = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += v;
+            }
+            int gi = incl - s;
+            for (int e2 = lo; e2 < hi; ++e2) {
+                const int cnt = ecnt[e2];
+                for (int b = 0; b < cnt; b += kGroupPairs) {
+                    tb.gexp[gi] = static_cast<uint16_t>(e2);
+                    tb.gbeg[gi] = static_cast<uint16_t>(eoff[e2] + b);
+                    tb.gcnt[gi] = static_cast<uint8_t>(min(kGroupPairs, cnt - b));
+                    ++gi;
+                }
+            }
+            if (lane == 31) hd->n_groups = incl;
+        }
+        for (int t = tid; t < p.T; t += blockDim.x) {
+            int v = 0;
+            for (int j = 0; j < p.k; ++j) v += (tb.pos[t * p.k + j] != 0xFFFFu);
+            tb.kvalid[t] = static_cast<uint8_t>(v);
+        }
+        __syncthreads();
+        if (blockIdx.x == 0 && tid == 0 && hd->n_bad) atomicOr(p.ctrl + 2, kErrBadId);
+        // tokens without a valid slot: y = 0 (nobody else writes them)
+        for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
+            if (tb.kvalid[t] == 0)
+                for (int r = tid; r < p.H; r += blockDim.x) p.y[static_cast<size_t>(t) * p.H + r] = 0.f;
+        }
+        __syncthreads();
+    }
+
+    if (tid >= kConsumerThreads) {
+        producer_loop(p, smem, tb, abort_flag);
+    } else {
+        Cons c;
+        c.p = &p;
+        c.smem = smem;
+        c.tb = tb;
+        c.red = reinterpret_cast<float4 *>(smem + p.red_off);
+        c.tid = tid;
+        c.warp = tid >> 5;
+        c.lane = tid & 31;
+        c.g = c.lane >> 2;
+        c.t = c.lane & 3;
+        c.s = 0;
+        c.ph = 0;
+        c.abort_flag = abort_flag;
+        consumer_loop<NULLM>(c);
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __syncthreads();
+
+    if (tid == 0) {
+        if (*abort_flag) {
+            // drain: wait (bounded) for the copies of every stage filled but not
+            // yet seen complete, so no bulk copy lands after the CTA exits
+            for (int i = hd->cons_cnt; i < hd->fill_cnt; ++i) {
+                const uint64_t t0 = gtimer();
+                while (!mbar_test(&hd->full[i % p.NS], static_cast<uint32_t>((i / p.NS) & 1))) {
+                    if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) break;
+                }
+            }
+        }
+        __threadfence();
+        const uint32_t done = atomicAdd(p.ctrl + 1, 1u);
+        if (done == gridDim.x - 1) {
+            // last CTA out: reset the counters for the next launch
+            __threadfence();
+            const bool err = (ld_relaxed(p.ctrl + 2) & kErrTimeout) != 0;
+            const int ng = hd->n_groups;
+            for (int i = 0; i < ng; ++i) p.doneA[i] = 0u;
+            if (err) {
+                for (int i = 0; i < kMaxPairs; ++i) p.doneA[i] = 0u;
+                for (int i = 0; i < p.T * p.nHt; ++i) p.cnt[i] = 0u;
+            }
+            p.ctrl[0] = 0u;
+            p.ctrl[1] = 0u;
+            __threadfence();
+        }
+    }
+}
+
+// ------------------------------------------------------------------ stand-alone grouping
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_group_kernel(const int32_t *__restrict__ ids, int P, int E, uint32_t *ctrl, int32_t *counts,
+                     int32_t *offsets, int32_t *perm_out)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int n_valid, n_bad;
+    int16_t *ids16 = reinterpret_cast<int16_t *>(smem);
+    int32_t *ecnt = reinterpret_cast<int32_t *>(smem + align16(2 * P));
+    int32_t *eoff = ecnt + E;
+    uint16_t *perm = reinterpret_cast<uint16_t *>(eoff + E + 1);
+    uint16_t *pos = perm + P;
+    group_pairs(ids, P, E, ids16, ecnt, eoff, perm, pos, &n_valid, &n_bad);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        counts[e] = ecnt[e];
+        offsets[e] = eoff[e];
+    }
+    if (threadIdx.x == 0) {
+        offsets[E] = eoff[E];
+        if (n_bad && ctrl) atomicOr(ctrl + 2, kErrBadId);
+    }
+    for (int i = threadIdx.x; i < P; i += blockDim.x) perm_out[i] = i < n_valid ? static_cast<int32_t>(perm[i]) : -1;
+}
+
+__global__ void moe_poison_kernel(uint32_t *doneA, int n)
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) doneA[i] = 0x40000000u;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launch helpers
+int group_smem_bytes(int P, int E)
+{
+    return align16(2 * P) + 4 * E + 4 * (E + 1) + 4 * P + 64;
+}
+
+cudaError_t set_step_smem_limit(int bytes)
+{
+    cudaError_t e = cudaFuncSetAttribute(moe_step_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(moe_step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+cudaError_t launch_step(const KernelParams &p, int grid, int smem_bytes, bool pdl, cudaStream_t st)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (p.null_mode) return cudaLaunchKernelEx(&cfg, moe_step_kernel<true>, p);
+    return cudaLaunchKernelEx(&cfg, moe_step_kernel<false>, p);
+}
+
+cudaError_t launch_group(const int32_t *ids, int P, int E, uint32_t *ctrl, int32_t *counts, int32_t *offsets,
+                         int32_t *perm, cudaStream_t st)
+{
+    const int smem = group_smem_bytes(P, E);
+    cudaError_t e = cudaFuncSetAttribute(moe_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    moe_group_kernel<<<1, kThreads, smem, st>>>(ids, P, E, ctrl, counts, offsets, perm);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_poison(uint32_t *doneA, int n, cudaStream_t st)
+{
+    moe_poison_kernel<<<8, 256, 0, st>>>(doneA, n);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
