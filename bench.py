@@ -1,0 +1,344 @@
+"""Benchmark of the routed-experts MoE step over NVFP4 experts on GB300.
+
+One "step" is one moe_decode call (grouping, gate/up, SiLU*mul, down, combine)
+over a batch of T tokens.  Default workload: single-stream decode, T=1,
+H=4096, I=1024, E=256, top-k=8.  Reported metric: achieved HBM GB/s
+(algorithmic bytes of the touched experts' weights and scales plus x, ids,
+weights and y, divided by the step time); ms_per_step and us_per_step beside
+it.  The T=16 and T=24 decode workloads are measured the same way and reported
+under "decode_sweep".
+
+Cold reads: every step relabels the expert ids by (id + step*delta) mod E, with
+delta chosen so that 8 consecutive steps touch disjoint experts; the bytes
+between reuses of an expert exceed the L2 size.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload decode|spec_verify|upper_decode|prefill|tiny]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "routed-MoE decode µs/step and HBM GB/s vs GB300 peak at T=1/16/24"
+GRAPH_STEPS = 64
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    def __init__(self, path):
+        self.path = path
+        self.proc = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(torch.cuda.current_device())],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            self.proc.wait()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def setup(wl_name, device):
+    from quantized_moe_routed_gb300 import MoePlan
+    from quantized_moe_routed_gb300.inputs import (WORKLOADS, algorithmic_bytes, make_expert_weights,
+                                                   make_topk_ids, make_topk_w, make_x, rotate_ids, rotation_delta)
+    wl = WORKLOADS[wl_name]
+    x, ids, w = make_x(wl), make_topk_ids(wl), make_topk_w(wl)
+    W = make_expert_weights(wl, device=device, experts=None)
+    delta = rotation_delta(ids, wl.E, window=8)
+    plan = MoePlan(W, wl.H, wl.I, wl.E, wl.k, T_max=wl.T, strict=True)
+    ws = plan.new_workspace()
+    nrot = max(8, GRAPH_STEPS)
+    ids_rot = [rotate_ids(ids, s, delta, wl.E).to(device) for s in range(nrot)]
+    return dict(wl=wl, x=x, ids=ids, w=w, W=W, plan=plan, ws=ws, ids_rot=ids_rot, delta=delta,
+                bytes=algorithmic_bytes(wl, ids), xd=x.to(device), wd=w.to(device),
+                y=torch.empty((wl.T, wl.H), dtype=torch.float32, device=device))
+
+
+def capture(S, null=False):
+    """One CUDA graph of GRAPH_STEPS consecutive steps over rotated ids."""
+    from quantized_moe_routed_gb300 import binding
+    fn = binding.moe_null_step if null else binding.moe_decode
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        for i in range(3):  # warm-up outside capture (sets kernel attributes)
+            fn(S["plan"].handle, S["xd"], S["ids_rot"][i], S["wd"], S["y"], S["ws"], st)
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for i in range(GRAPH_STEPS):
+            fn(S["plan"].handle, S["xd"], S["ids_rot"][i % len(S["ids_rot"])], S["wd"], S["y"], S["ws"], st)
+    torch.cuda.synchronize()
+    return g, st
+
+
+def time_graph(g, st, reps, warm):
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(st):
+        e0.record(st)
+        for _ in range(reps):
+            g.replay()
+        e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * GRAPH_STEPS)  # ms per step
+
+
+def time_e2e(S, steps):
+    """Per step through the public binding with host buffers: pinned host ->
+    device copies of x, ids, w; the step; the device -> host copy of y."""
+    from quantized_moe_routed_gb300 import binding
+    wl = S["wl"]
+    hx = S["x"].pin_memory()
+    hids = [r.cpu().pin_memory() for r in S["ids_rot"][:8]]
+    hw = S["w"].pin_memory()
+    hy = torch.empty((wl.T, wl.H), dtype=torch.float32).pin_memory()
+    dx, dids, dw = torch.empty_like(S["xd"]), torch.empty_like(S["ids_rot"][0]), torch.empty_like(S["wd"])
+    st = torch.cuda.current_stream()
+    for i in range(3):
+        dx.copy_(hx, non_blocking=True)
+        binding.moe_decode(S["plan"].handle, dx, dids.copy_(hids[i], non_blocking=True),
+                           dw.copy_(hw, non_blocking=True), S["y"], S["ws"])
+        hy.copy_(S["y"], non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(steps):
+        dx.copy_(hx, non_blocking=True)
+        dids.copy_(hids[i % 8], non_blocking=True)
+        dw.copy_(hw, non_blocking=True)
+        binding.moe_decode(S["plan"].handle, dx, dids, dw, S["y"], S["ws"])
+        hy.copy_(S["y"], non_blocking=True)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = hx.numel() * 2 + hids[0].numel() * 4 + hw.numel() * 4
+    d2h = hy.numel() * 4
+    return ms, h2d, d2h
+
+
+def cpu_baseline(S, seconds=10.0):
+    """The oracle, as it is, on the host cores, over whole steps of the same
+    workload (bounded to about `seconds`)."""
+    import oracle
+    from quantized_moe_routed_gb300.inputs import touched_experts
+    wl = S["wl"]
+    used = touched_experts(S["ids"], wl.E)
+    Wc = {}
+    for k, v in S["W"].items():
+        c = torch.zeros(v.shape, dtype=v.dtype)
+        for e in used:
+            c[e] = v[e].cpu()
+        Wc[k] = c
+    cores = os.cpu_count() or 1
+    toks = list(range(wl.T))
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.moe_forward(S["x"], S["ids"], S["w"], Wc, tokens=toks, n_threads=cores)
+        n += 1
+        if time.perf_counter() - t0 > seconds or n >= 20:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": S["bytes"] / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} whole step(s) of the {wl.name} workload (T={wl.T}, all touched experts), "
+                      f"{dt * 1e3:.1f} ms per step, OpenMP over output rows"}
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    device = "cuda:0" if torch.cuda.is_available() else "cpu"
+    from quantized_moe_routed_gb300.inputs import (WORKLOADS, algorithmic_bytes, make_expert_weights,
+                                                   make_topk_ids, make_topk_w, make_x, touched_experts)
+    import oracle
+    wl = WORKLOADS[args.workload]
+    x, ids, w = make_x(wl), make_topk_ids(wl), make_topk_w(wl)
+    used = touched_experts(ids, wl.E)
+    W = make_expert_weights(wl, device=device, experts=used, fill="zero")
+    Wc = {k: v.cpu() for k, v in W.items()}
+    nbytes = algorithmic_bytes(wl, ids)
+    cores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle.moe_forward(x, ids, w, Wc, n_threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.moe_forward(x, ids, w, Wc, n_threads=cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    val = nbytes / dt / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "top_k": wl.k,
+                   "routing": wl.routing},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} whole steps of the {wl.name} workload"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        if args.steps > 50:
+            args.steps = 5
+        return run_reference(args)
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device(f"cuda:{local}")
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    __graft_entry__.build()
+
+    S = setup(args.workload, device)
+    g, st = capture(S)
+    reps = max(1, args.steps // GRAPH_STEPS)
+    steps = reps * GRAPH_STEPS
+    warm = max(args.warmup, 3)
+    time_graph(g, st, 1, warm)  # warm-up replays (untimed)
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) as ck:
+        ms = time_graph(g, st, reps, 0)
+    torch.cuda.synchronize()
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t)
+    st_code = S["plan"].check(S["ws"])
+    if st_code != 0:
+        raise SystemExit(f"device status {st_code} after the timed region")
+
+    hbm, peak_kind = peaks()
+    gbs = S["bytes"] / (ms * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": gbs * world, "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": warm * GRAPH_STEPS, "ms_per_step": ms, "us_per_step": ms * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
+        "data": "synthetic (seeded NVFP4 experts, N(0,0.02) quantised)",
+        "config": {"workload": S["wl"].name, "T": S["wl"].T, "H": S["wl"].H, "I": S["wl"].I, "E": S["wl"].E,
+                   "top_k": S["wl"].k, "routing": S["wl"].routing, "parallelism": f"replicas x{world}",
+                   "cold_reads": f"ids relabelled (id + step*{S['delta']}) mod E every step; 8 consecutive steps "
+                                 "touch disjoint experts",
+                   "algorithmic_bytes_per_step": S["bytes"], "timing": f"CUDA graph of {GRAPH_STEPS} steps, "
+                                                                       "CUDA events on the launch stream"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "traffic": None, "peak_kind": peak_kind},
+        "gpu_launches": steps,
+        "clocks": ck.summary(),
+    }
+    if rank == 0:
+        # null-dequant ceiling (same bytes, no math) on the same schedule
+        gn, stn = capture(S, null=True)
+        ms_null = time_graph(gn, stn, max(1, reps // 4), 2)
+        out["null_dequant"] = {"us_per_step": ms_null * 1e3, "GB/s": S["bytes"] / (ms_null * 1e-3) / 1e9}
+        ms_e2e, h2d, d2h = time_e2e(S, min(steps, 2000))
+        out["e2e"] = {"value": S["bytes"] / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "us_per_step": ms_e2e * 1e3,
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        if not args.no_sweep and args.workload == "decode":
+            sweep = {}
+            for name in ("spec_verify", "upper_decode"):
+                del S
+                torch.cuda.empty_cache()
+                S = setup(name, device)
+                g2, st2 = capture(S)
+                ms2 = time_graph(g2, st2, max(1, 4000 // GRAPH_STEPS // (4 if name == "upper_decode" else 2)), 3)
+                assert S["plan"].check(S["ws"]) == 0
+                b2 = S["bytes"] / (ms2 * 1e-3) / 1e9
+                sweep[name] = {"T": S["wl"].T, "us_per_step": ms2 * 1e3, "GB/s": b2, "frac": b2 / hbm,
+                               "algorithmic_bytes_per_step": S["bytes"]}
+            out["decode_sweep"] = sweep
+            del S
+            S = setup(args.workload, device)
+        if not args.no_cpu:
+            out["cpu_baseline"] = cpu_baseline(S)
+        print(json.dumps(out))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
