@@ -5,6 +5,8 @@
 #include "moe_internal.h"
 #include "moe_nvfp4.h"
 
+#include <cudaTypedefs.h>
+
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -46,8 +48,11 @@ struct moe_plan {
     int device = 0, num_sms = 0, smem_optin = 0;
     // tiling
     int KA = 0, nPA = 0, KB = 0, nPB = 0, nHt = 0;
-    int strideA = 0, sstrideA = 0, strideB = 0, sstrideB = 0, blockScaleA = 0, blockScaleB = 0;
+    int nib_mode = 0;
+    int scale_tmaA = 0, spA = 0, shA = 0, mkA = 0, scale_tmaB = 0, spB = 0, shB = 0, mkB = 0;
+    int offGq = 0, offUq = 0, offGs = 0, offUs = 0, offDq = 0, offDs = 0;
     int stage_bytes = 0;
+    CUtensorMap tm[6];
     int Tc = 0;  // tokens per launch chunk
     long long timeout_ns = 1000000000LL;
     bool strict = false, pdl = false;
@@ -60,38 +65,88 @@ struct moe_plan {
 
 namespace {
 
-// Part size along K (a multiple of 128 dividing K, at most cap) and the smem
-// strides that make the consumer's shared-memory reads conflict-free:
-// nibble rows at a stride = 64 (mod 128); scale rows at an odd multiple of 16
-// (per-row copies, 16-byte aligned destinations) or the natural K/16 when that
-// is an odd multiple of 8 or 16 (one block copy, only when a part spans the
-// whole row).
-bool choose_part(int K, int cap, int *KP, int *stride, int *sstride, int *block)
+// Part size along K (a multiple of 128 dividing K, at most cap) and how its
+// scale rows reach shared memory.  When K is a multiple of 256 the scale rows
+// have a 16-byte pitch and come by a 2-D tensor map whose box is KP/16 bytes
+// wide (16, 32, 64 or 128), swizzled so the consumers' reads of eight rows hit
+// eight different bank groups; otherwise (K an odd multiple of 128, at most
+// cap) one part spans the whole row and the scale block is one 1-D copy whose
+// natural pitch K/16 (8 x odd) is already conflict-free.
+struct PartPlan {
+    int KP, scale_tma, sp, sh, mk;
+};
+
+bool choose_part(int K, int cap, PartPlan *pp)
 {
     for (int kp = (K < cap ? K : cap) / 128 * 128; kp >= 128; kp -= 128) {
         if (K % kp) continue;
-        int s = kp / 2;
-        if ((s / 64) % 2 == 0) s += 64;
-        const int kb = kp / 16;
-        if (kb % 16 == 0 && (K / 16) % 16 == 0) {
-            *KP = kp;
-            *stride = s;
-            *sstride = ((kb / 16) % 2 == 1) ? kb : kb + 16;
-            *block = 0;
-            return true;
-        }
-        const int nat = K / 16;
-        const bool odd8 = (nat % 8 == 0) && ((nat / 8) % 2 == 1);
-        const bool odd16 = (nat % 16 == 0) && ((nat / 16) % 2 == 1);
-        if (kp == K && (odd8 || odd16)) {
-            *KP = kp;
-            *stride = s;
-            *sstride = nat;
-            *block = 1;
+        if (K % 256 == 0) {
+            const int inner = kp / 16;
+            if (inner == 16) { *pp = {kp, 1, 16, 0, 0}; return true; }
+            if (inner == 32) { *pp = {kp, 1, 32, 2, 1}; return true; }
+            if (inner == 64) { *pp = {kp, 1, 64, 1, 3}; return true; }
+            if (inner == 128) { *pp = {kp, 1, 128, 0, 7}; return true; }
+        } else if (kp == K) {
+            *pp = {kp, 0, K / 16, 0, 0};
             return true;
         }
     }
     return false;
+}
+
+int up1024(int v) { return (v + 1023) / 1024 * 1024; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// E2M1 rows [rows_total, K/2 bytes].  Mode 0: a 3-D view {64 B, rows, K/128
+// spans} whose box {64, BR, KP/128} lands span-major ([span][row][64 B]);
+// mode 1: 2-D boxes {128 B, BR} with the 128-byte swizzle.
+CUresult encode_nib(CUtensorMap *m, int mode, const void *base, uint64_t rows_total, int K, int BR, int KP)
+{
+    const cuuint32_t es[3] = {1, 1, 1};
+    if (mode == 0) {
+        const cuuint64_t dims[3] = {64, rows_total, static_cast<cuuint64_t>(K / 128)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 2), 64};
+        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BR), static_cast<cuuint32_t>(KP / 128)};
+        return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), rows_total};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(BR)};
+    return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// E4M3 scale rows [rows_total, K/16 bytes], box {KP/16, BR}.
+CUresult encode_scale(CUtensorMap *m, const void *base, uint64_t rows_total, int K, int BR, const PartPlan &pp)
+{
+    const cuuint32_t es[2] = {1, 1};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 16), rows_total};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 16)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(pp.KP / 16), static_cast<cuuint32_t>(BR)};
+    const CUtensorMapSwizzle sw = pp.sp == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : pp.sp == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                  : pp.sp == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                : CU_TENSOR_MAP_SWIZZLE_NONE;
+    return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 moe::SmemLayout layout_for(const moe_plan *pl, int T)
@@ -106,13 +161,13 @@ moe::SmemLayout layout_for(const moe_plan *pl, int T)
     L.red_bytes = static_cast<int>(up(red_need > scr_need ? red_need : scr_need, 128));
     L.tab_bytes = static_cast<int>(up(512 + 4 * align16i(2 * P) + align16i(P) + align16i(T), 128));
     L.stage_bytes = pl->stage_bytes;
-    const int avail = pl->smem_optin - L.red_bytes - L.tab_bytes;
+    const int avail = pl->smem_optin - L.red_bytes - L.tab_bytes - 1024;
     int ns = avail / pl->stage_bytes;
     if (ns > moe::kMaxStages) ns = moe::kMaxStages;
     L.NS = ns;
     L.red_off = ns * pl->stage_bytes;
     L.tab_off = L.red_off + L.red_bytes;
-    L.total = L.tab_off + L.tab_bytes;
+    L.total = L.tab_off + L.tab_bytes + 1024;  // + slack to align the ring to 1024 bytes
     return L;
 }
 
@@ -200,12 +255,22 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
     p.KB = pl->KB;
     p.nPB = pl->nPB;
     p.nHt = pl->nHt;
-    p.strideA = pl->strideA;
-    p.sstrideA = pl->sstrideA;
-    p.strideB = pl->strideB;
-    p.sstrideB = pl->sstrideB;
-    p.blockScaleA = pl->blockScaleA;
-    p.blockScaleB = pl->blockScaleB;
+    for (int i = 0; i < 6; ++i) p.tm[i] = pl->tm[i];
+    p.nib_mode = pl->nib_mode;
+    p.scale_tmaA = pl->scale_tmaA;
+    p.spA = pl->spA;
+    p.shA = pl->shA;
+    p.mkA = pl->mkA;
+    p.scale_tmaB = pl->scale_tmaB;
+    p.spB = pl->spB;
+    p.shB = pl->shB;
+    p.mkB = pl->mkB;
+    p.offGq = pl->offGq;
+    p.offUq = pl->offUq;
+    p.offGs = pl->offGs;
+    p.offUs = pl->offUs;
+    p.offDq = pl->offDq;
+    p.offDs = pl->offDs;
     p.stage_bytes = pl->stage_bytes;
     p.timeout_ns = pl->timeout_ns;
     p.null_mode = path == Path::Null ? 1 : 0;
@@ -326,17 +391,66 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
         const long long ms = std::atoll(t);
         if (ms > 0) pl->timeout_ns = ms * 1000000LL;
     }
-    if (!choose_part(d.H, 2048, &pl->KA, &pl->strideA, &pl->sstrideA, &pl->blockScaleA) ||
-        !choose_part(d.I, 1024, &pl->KB, &pl->strideB, &pl->sstrideB, &pl->blockScaleB)) {
+    PartPlan pa{}, pb{};
+    if (!choose_part(d.H, 2048, &pa) || !choose_part(d.I, 1024, &pb)) {
         delete pl;
-        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "no stage tiling for H=%d, I=%d", d.H, d.I);
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE,
+                    "no stage tiling for H=%d, I=%d (an odd multiple of 128 must be <= 2048 for H, <= 1024 for I)",
+                    d.H, d.I);
     }
+    pl->KA = pa.KP;
+    pl->KB = pb.KP;
+    pl->scale_tmaA = pa.scale_tma;
+    pl->spA = pa.sp;
+    pl->shA = pa.sh;
+    pl->mkA = pa.mk;
+    pl->scale_tmaB = pb.scale_tma;
+    pl->spB = pb.sp;
+    pl->shB = pb.sh;
+    pl->mkB = pb.mk;
     pl->nPA = d.H / pl->KA;
     pl->nPB = d.I / pl->KB;
     pl->nHt = d.H / moe::kMB;
-    const int stA = 32 * pl->strideA + 32 * pl->sstrideA;
-    const int stB = moe::kMB * pl->strideB + moe::kMB * pl->sstrideB;
-    pl->stage_bytes = static_cast<int>(up(stA > stB ? stA : stB, 128));
+    pl->offGq = 0;
+    pl->offUq = 8 * pl->KA;
+    pl->offGs = 16 * pl->KA;
+    pl->offUs = pl->offGs + up1024(16 * pl->spA);
+    const int stA = pl->offUs + up1024(16 * pl->spA);
+    pl->offDq = 0;
+    pl->offDs = 32 * pl->KB;
+    const int stB = pl->offDs + up1024(moe::kMB * pl->spB);
+    pl->stage_bytes = up1024(stA > stB ? stA : stB);
+    // tensor maps (host-only encoding; no device memory involved)
+    if (!encoder()) {
+        delete pl;
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    }
+    const uint64_t rowsGU = static_cast<uint64_t>(d.E) * d.I, rowsD = static_cast<uint64_t>(d.E) * d.H;
+    CUresult cr = CUDA_SUCCESS;
+    int mode = 0;
+    for (; mode < 2; ++mode) {
+        if (mode == 1 && (d.H % 256 || d.I % 256)) break;
+        cr = encode_nib(&pl->tm[0], mode, d.gate_q_dev, rowsGU, d.H, 16, pl->KA);
+        if (cr == CUDA_SUCCESS) cr = encode_nib(&pl->tm[1], mode, d.up_q_dev, rowsGU, d.H, 16, pl->KA);
+        if (cr == CUDA_SUCCESS) cr = encode_nib(&pl->tm[2], mode, d.down_q_dev, rowsD, d.I, moe::kMB, pl->KB);
+        if (cr == CUDA_SUCCESS) break;
+    }
+    if (cr != CUDA_SUCCESS || mode >= 2) {
+        delete pl;
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "tensor-map encoding of the E2M1 rows failed (CUresult %d)",
+                    static_cast<int>(cr));
+    }
+    pl->nib_mode = mode;
+    if (pl->scale_tmaA) {
+        cr = encode_scale(&pl->tm[3], d.gate_s_dev, rowsGU, d.H, 16, pa);
+        if (cr == CUDA_SUCCESS) cr = encode_scale(&pl->tm[4], d.up_s_dev, rowsGU, d.H, 16, pa);
+    }
+    if (cr == CUDA_SUCCESS && pl->scale_tmaB) cr = encode_scale(&pl->tm[5], d.down_s_dev, rowsD, d.I, moe::kMB, pb);
+    if (cr != CUDA_SUCCESS) {
+        delete pl;
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "tensor-map encoding of the E4M3 scale rows failed (CUresult %d)",
+                    static_cast<int>(cr));
+    }
     const int tc = moe::kMaxPairs / d.top_k;
     pl->Tc = d.T_max < tc ? d.T_max : tc;
     const moe::SmemLayout L = layout_for(pl, pl->Tc);

@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace moe {
@@ -29,6 +30,10 @@ constexpr uint32_t kErrRange = 4u;
 constexpr size_t kCtrlBytes = 256;
 
 struct KernelParams {
+    // TMA descriptors of the packed weights (encoded by the plan on the host):
+    //   0 gate_q, 1 up_q, 2 down_q  (E2M1 rows; layout per nib_mode)
+    //   3 gate_s, 4 up_s, 5 down_s  (E4M3 scale rows; 2-D box, swizzled)
+    CUtensorMap tm[6];
     // weights (NVFP4, layouts as in moe_nvfp4.h)
     const uint8_t *gq, *uq, *dq;
     const uint8_t *gs, *us, *ds;
@@ -50,8 +55,11 @@ struct KernelParams {
     int KA, nPA;        // gate/up: K elements per stage part, parts per ticket
     int KB, nPB;        // down: K elements per stage part, parts per ticket
     int nHt;            // H / kMB
-    int strideA, sstrideA, strideB, sstrideB;  // smem row strides (bytes)
-    int blockScaleA, blockScaleB;               // 1: scale rows copied as one block
+    int nib_mode;        // 0: 3-D span-major boxes [span][row][64 B]; 1: 2-D boxes [row][128 B], 128B swizzle
+    int scale_tmaA, scale_tmaB;  // 1: scale rows by 2-D tensor map; 0: one 1-D bulk copy (natural layout)
+    int spA, shA, mkA, spB, shB, mkB;  // scale smem row pitch, swizzle shift and mask
+    int offGq, offUq, offGs, offUs;    // phase-A stage sub-buffers (bytes, 1024-aligned)
+    int offDq, offDs;                  // phase-B stage sub-buffers
     int stage_bytes, NS;
     int red_off, red_bytes, tab_off;            // smem layout (bytes)
     int ntmax;                                  // MMA n-tiles needed (1..4)

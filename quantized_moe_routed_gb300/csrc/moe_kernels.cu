@@ -21,9 +21,11 @@
 //    is guaranteed to fill, and no grid barrier is needed (the pages' barrier
 //    version F1 was correct but not faster, "LNA-CANON.md", "含めないもの").
 //  * A producer warp streams each ticket's packed E2M1 rows and E4M3 scale
-//    rows HBM -> shared memory with cp.async.bulk (one row per lane, L2
-//    evict-first), into a ring of stages guarded by mbarriers; it keeps
-//    prefetching while consumers wait on a dependency.
+//    rows HBM -> shared memory with TMA tensor copies (cp.async.bulk.tensor:
+//    one 16-32 KB box per projection and stage, L2 evict-first) into a ring of
+//    stages guarded by mbarriers; it keeps prefetching while consumers wait on
+//    a dependency.  Box shapes are chosen so the consumers' 16-byte reads are
+//    bank-conflict-free without padding.
 //  * Eight consumer warps dequantise in registers -- cvt e2m1x2 -> f16x2, times
 //    the block scale (E2M1 x E4M3 is exact in fp16) -- and run mma.sync
 //    m16n8k16 (fp16 operands, fp32 accumulate) with weight rows as M and the
@@ -97,6 +99,25 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma2d(void *dst, const CUtensorMap *tm, int c0, int c1, uint64_t *bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *tm, int c0, int c1, int c2, uint64_t *bar,
+                                      uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(pol)
         : "memory");
 }
 
@@ -199,7 +220,9 @@ struct SmemHdr {
     uint64_t empty[kMaxStages];
     int4 stage_hdr[kMaxStages];  // {kind, group, tile, part}
     int n_groups, n_valid, n_bad, abort_flag;  // abort_flag: any role gave up (read by waits)
-    int n_comb, fill_cnt, cons_cnt, cflag;     // fills issued / fills seen complete / consumer verdict
+    int n_comb, fill_cnt, cons_cnt, pad0;      // fills issued / fills seen complete
+    int verdict[2];                            // consumer verdicts, alternating slots
+    int pad1[2];
     int comb_tok[kGroupPairs];
 };
 static_assert(sizeof(SmemHdr) <= 512, "header too large");
@@ -353,34 +376,55 @@ __device__ bool wait_count(const uint32_t *ctr, uint32_t target, const KernelPar
     }
 }
 
-// ------------------------------------------------------------------ MMA over one 128-element chunk
-// rows0/srows0: first nibble/scale row of this warp's m-group in the stage,
-// already offset to the chunk (64 bytes / 8 bytes per chunk).  bq: the chunk's
-// B operand for this thread (elements 32t .. 32t+31 of the chunk for the pair
-// of n-tile nt, column g), bf16 (x) or fp16 (h).
-//
-// K order inside a k16 step: thread t holds elements 4s..4s+3 of its 32-element
-// slice at k-step s; A register 0/1 (rows g, g+8) and B register 0 take
-// elements 4s, 4s+1; A register 2/3 and B register 1 take 4s+2, 4s+3.  Both
-// operands follow the same order, so the dot products are the plain ones.
-template <int MT, int NT, bool BF16B, bool NULLM>
-__device__ __forceinline__ void chunk_mma(const uint8_t *rows0, int stride, const uint8_t *srows0, int sstride,
-                                          const uint4 (&bq)[NT][4], float (&acc)[MT][NT][4], int g, int t)
+// ------------------------------------------------------------------ one 128-element chunk
+// Shared-memory placement of a weight row's 16 bytes that thread t consumes in
+// chunk q, and the first K element of those 32 values.  Layout 0 (span-major
+// boxes [span][row][64 B]): rows g and g+1 sit 64 bytes apart, so the eight
+// threads of a quarter-warp hit eight different 16-byte bank groups.  Layout 1
+// (rows of 128 bytes, 128-byte swizzle: granule ^= row % 8): thread t takes
+// granule 2t + (q & 1), which again spreads every quarter-warp over eight
+// groups.  The B operand follows the same K order (koff), so every dot
+// product is the plain one.
+__device__ __forceinline__ int nib_off(int mode, int BR, int row, int q, int t)
 {
-    uint4 ra[MT], rb[MT];
+    return mode == 0 ? q * (BR * 64) + row * 64 + t * 16
+                     : (q >> 1) * (BR * 128) + row * 128 + ((((t << 1) | (q & 1)) ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ int k_off(int mode, int q, int t)
+{
+    return mode == 0 ? q * 128 + t * 32 : (q >> 1) * 256 + t * 64 + (q & 1) * 32;
+}
+
+// The two E4M3 scale bytes of elements koff .. koff+31 of `row` (blocks
+// koff/16 and koff/16 + 1), in a [row][pitch] layout whose 16-byte granules
+// are XOR-swizzled by (row >> shift) & mask (the TMA swizzle of the box).
+__device__ __forceinline__ uint16_t scale_pair(const uint8_t *sb, int pitch, int shift, int mask, int row, int koff)
+{
+    const int j = koff >> 4;
+    const int gran = (j >> 4) ^ ((row >> shift) & mask);
+    return *reinterpret_cast<const uint16_t *>(sb + row * pitch + (gran << 4) + (j & 15));
+}
+
+// K order inside a k16 step: thread t holds elements 4s..4s+3 of its 32-element
+// slice at k-step s; A registers 0/1 (rows g, g+8) and B register 0 take
+// elements 4s, 4s+1; A registers 2/3 and B register 1 take 4s+2, 4s+3.
+// ra/rb: 16 bytes of E2M1 of rows g and g+8 per m-tile; s_a/s_b: their two
+// block-scale bytes; bq: the B operand (bf16 x or fp16 h), 32 elements.
+template <int MT, int NT, bool BF16B, bool NULLM>
+__device__ __forceinline__ void chunk_math(const uint4 (&ra)[MT], const uint4 (&rb)[MT], const uint16_t (&s_a)[MT],
+                                           const uint16_t (&s_b)[MT], const uint4 (&bq)[NT][4],
+                                           float (&acc)[MT][NT][4])
+{
     uint32_t sa[MT][2], sb[MT][2];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-        const uint8_t *r0 = rows0 + (mt * 16 + g) * stride + t * 16;
-        ra[mt] = *reinterpret_cast<const uint4 *>(r0);
-        rb[mt] = *reinterpret_cast<const uint4 *>(r0 + 8 * stride);
-        const uint8_t *s0 = srows0 + (mt * 16 + g) * sstride + t * 2;
-        const uint32_t s_a = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(s0));
-        const uint32_t s_b = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(s0 + 8 * sstride));
-        sa[mt][0] = __byte_perm(s_a, 0, 0x1010);
-        sa[mt][1] = __byte_perm(s_a, 0, 0x3232);
-        sb[mt][0] = __byte_perm(s_b, 0, 0x1010);
-        sb[mt][1] = __byte_perm(s_b, 0, 0x3232);
+        const uint32_t f_a = e4m3x2_to_f16x2(s_a[mt]);
+        const uint32_t f_b = e4m3x2_to_f16x2(s_b[mt]);
+        sa[mt][0] = __byte_perm(f_a, 0, 0x1010);
+        sa[mt][1] = __byte_perm(f_a, 0, 0x3232);
+        sb[mt][0] = __byte_perm(f_b, 0, 0x1010);
+        sb[mt][1] = __byte_perm(f_b, 0, 0x3232);
     }
     if constexpr (NULLM) {
         // measurement variant: keep the loads live, no dequant, no MMA
@@ -430,8 +474,24 @@ struct Cons {
     int warp, lane, g, t, tid;
     int s;          // ring stage
     uint32_t ph;    // parity of the ring pass
+    uint32_t nv;    // verdicts published so far (same value in every consumer thread)
     volatile int *abort_flag;
 };
+
+// Consumer thread 0 decides, every consumer thread gets the same answer.  The
+// slot alternates, so thread 0 cannot overwrite a verdict another thread has
+// not read yet: rewriting a slot needs the next verdict's barrier, which every
+// thread reaches only after its read.
+__device__ __forceinline__ bool publish_verdict(Cons &c, bool ok_in_thread0)
+{
+    SmemHdr *hd = c.tb.hdr;
+    const int slot = static_cast<int>(c.nv & 1u);
+    if (c.tid == 0) hd->verdict[slot] = ok_in_thread0 ? 1 : 0;
+    consumer_sync();
+    const bool ok = hd->verdict[slot] != 0;
+    ++c.nv;
+    return ok;
+}
 
 __device__ __forceinline__ void cons_release_stage(Cons &c)
 {
@@ -450,19 +510,18 @@ __device__ __forceinline__ void cons_release_stage(Cons &c)
 __device__ __forceinline__ int4 cons_next_stage(Cons &c)
 {
     SmemHdr *hd = c.tb.hdr;
+    bool ok = false;
     if (c.tid == 0) {
-        const bool ok = wait_bar(&hd->full[c.s], c.ph, *c.p, c.abort_flag);
-        hd->cflag = ok ? 1 : 0;
+        ok = wait_bar(&hd->full[c.s], c.ph, *c.p, c.abort_flag);
         if (ok) hd->cons_cnt += 1;
     }
-    consumer_sync();
-    if (!hd->cflag) return make_int4(KIND_END, 0, 0, 0);
+    if (!publish_verdict(c, ok)) return make_int4(KIND_END, 0, 0, 0);
     for (int i = 0; i < 64 && !mbar_test(&hd->full[c.s], c.ph); ++i) {
     }
     return hd->stage_hdr[c.s];
 }
 
-// B-operand loads for one chunk: 4 x 16 bytes per n-tile.
+// B-operand loads for one chunk: 4 x 16 bytes per n-tile (elements kglob .. kglob+31).
 template <int NT, bool CG>
 __device__ __forceinline__ void load_bq(uint4 (&bq)[NT][4], const uint16_t *const (&bptr)[NT], int kglob)
 {
@@ -493,7 +552,7 @@ __device__ __noinline__ bool ticket_A(Cons &c, int grp, int tile)
         bptr[nt] = nullptr;
         if (n < gcnt) {
             const int pr = c.tb.perm[gbeg + n];
-            bptr[nt] = p.x + static_cast<size_t>(pr / p.k) * p.H + c.t * 32;
+            bptr[nt] = p.x + static_cast<size_t>(pr / p.k) * p.H;
         }
     }
     float acc[2][NT][4];
@@ -512,16 +571,29 @@ __device__ __noinline__ bool ticket_A(Cons &c, int grp, int tile)
             if (h.x == KIND_END) return false;
         }
         const uint8_t *st = c.smem + c.s * p.stage_bytes;
-        const uint8_t *srows = st + 32 * p.strideA;
         constexpr bool DB = NT <= 2;  // prefetch the next chunk's B operand (register budget)
         int q = ks;
         uint4 bq[NT][4], bn[NT][4];
-        if (DB && q < chunks) load_bq<NT, false>(bq, bptr, part * p.KA + q * 128);
+        if (DB && q < chunks) load_bq<NT, false>(bq, bptr, part * p.KA + k_off(p.nib_mode, q, c.t));
         for (; q < chunks; q += kConsumerWarps) {
             const int qn = q + kConsumerWarps;
-            if (!DB) load_bq<NT, false>(bq, bptr, part * p.KA + q * 128);
-            if (DB && qn < chunks) load_bq<NT, false>(bn, bptr, part * p.KA + qn * 128);
-            chunk_mma<2, NT, true, NULLM>(st + q * 64, p.strideA, srows + q * 8, p.sstrideA, bq, acc, c.g, c.t);
+            if (!DB) load_bq<NT, false>(bq, bptr, part * p.KA + k_off(p.nib_mode, q, c.t));
+            if (DB && qn < chunks) load_bq<NT, false>(bn, bptr, part * p.KA + k_off(p.nib_mode, qn, c.t));
+            {
+                uint4 ra[2], rb[2];
+                uint16_t s_a[2], s_b[2];
+                const int ko = k_off(p.nib_mode, q, c.t);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {  // m-tile 0: gate rows, 1: up rows
+                    const uint8_t *nb = st + (mt ? p.offUq : p.offGq);
+                    ra[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, 16, c.g, q, c.t));
+                    rb[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, 16, c.g + 8, q, c.t));
+                    const uint8_t *sb = st + (mt ? p.offUs : p.offGs);
+                    s_a[mt] = scale_pair(sb, p.spA, p.shA, p.mkA, c.g, ko);
+                    s_b[mt] = scale_pair(sb, p.spA, p.shA, p.mkA, c.g + 8, ko);
+                }
+                chunk_math<2, NT, true, NULLM>(ra, rb, s_a, s_b, bq, acc);
+            }
             if (DB && qn < chunks) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
@@ -578,18 +650,17 @@ __device__ __noinline__ bool ticket_B(Cons &c, int grp, int tile)
     const int h0 = tile * kMB;
     // the group's h rows must be complete: one thread waits (acquire), the
     // verdict is published before the barrier so every consumer agrees
+    bool ok = false;
     if (c.tid == 0) {
-        const bool ok = wait_count(p.doneA + grp, static_cast<uint32_t>(p.I / 16), p, c.abort_flag);
-        c.tb.hdr->cflag = ok ? 1 : 0;
+        ok = wait_count(p.doneA + grp, static_cast<uint32_t>(p.I / 16), p, c.abort_flag);
         if (!ok) *c.abort_flag = 1;
     }
-    consumer_sync();
-    if (!c.tb.hdr->cflag) return false;
+    if (!publish_verdict(c, ok)) return false;
     const uint16_t *bptr[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int n = nt * 8 + c.g;
-        bptr[nt] = (n < gcnt) ? p.hbuf + static_cast<size_t>(gbeg + n) * p.I + c.t * 32 : nullptr;
+        bptr[nt] = (n < gcnt) ? p.hbuf + static_cast<size_t>(gbeg + n) * p.I : nullptr;
     }
     float acc[2][NT][4];
 #pragma unroll
@@ -607,17 +678,30 @@ __device__ __noinline__ bool ticket_B(Cons &c, int grp, int tile)
             if (h.x == KIND_END) return false;
         }
         const uint8_t *st = c.smem + c.s * p.stage_bytes;
-        const uint8_t *rows = st + mg * 32 * p.strideB;
-        const uint8_t *srows = st + kMB * p.strideB + mg * 32 * p.sstrideB;
+        const uint8_t *nb = st + p.offDq;
+        const uint8_t *sb = st + p.offDs;
         constexpr bool DB = NT <= 2;
         int q = ks;
         uint4 bq[NT][4], bn[NT][4];
-        if (DB && q < chunks) load_bq<NT, true>(bq, bptr, part * p.KB + q * 128);
+        if (DB && q < chunks) load_bq<NT, true>(bq, bptr, part * p.KB + k_off(p.nib_mode, q, c.t));
         for (; q < chunks; q += 4) {
             const int qn = q + 4;
-            if (!DB) load_bq<NT, true>(bq, bptr, part * p.KB + q * 128);
-            if (DB && qn < chunks) load_bq<NT, true>(bn, bptr, part * p.KB + qn * 128);
-            chunk_mma<2, NT, false, NULLM>(rows + q * 64, p.strideB, srows + q * 8, p.sstrideB, bq, acc, c.g, c.t);
+            if (!DB) load_bq<NT, true>(bq, bptr, part * p.KB + k_off(p.nib_mode, q, c.t));
+            if (DB && qn < chunks) load_bq<NT, true>(bn, bptr, part * p.KB + k_off(p.nib_mode, qn, c.t));
+            {
+                uint4 ra[2], rb[2];
+                uint16_t s_a[2], s_b[2];
+                const int ko = k_off(p.nib_mode, q, c.t);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const int r0 = mg * 32 + mt * 16 + c.g;
+                    ra[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, kMB, r0, q, c.t));
+                    rb[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, kMB, r0 + 8, q, c.t));
+                    s_a[mt] = scale_pair(sb, p.spB, p.shB, p.mkB, r0, ko);
+                    s_b[mt] = scale_pair(sb, p.spB, p.shB, p.mkB, r0 + 8, ko);
+                }
+                chunk_math<2, NT, false, NULLM>(ra, rb, s_a, s_b, bq, acc);
+            }
             if (DB && qn < chunks) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
@@ -743,42 +827,47 @@ __device__ __noinline__ void producer_loop(const KernelParams &p, uint8_t *smem,
             }
             uint8_t *st = smem + s * p.stage_bytes;
             if (lane == 0) {
+                uint64_t *bar = &hd->full[s];
                 hd->stage_hdr[s] = make_int4(isA ? KIND_A : KIND_B, grp, tile, part);
-                mbar_expect_tx(&hd->full[s], isA ? bytesA : bytesB);
-            }
-            __syncwarp();
-            if (isA) {
-                // 32 rows: 0..15 gate rows i0.., 16..31 up rows i0..
-                const int r = lane;
-                const size_t row = static_cast<size_t>(e) * p.I + tile * 16 + (r & 15);
-                const uint8_t *q = (r < 16 ? p.gq : p.uq) + row * (p.H / 2) + part * (p.KA / 2);
-                bulk_g2s(st + r * p.strideA, q, p.KA / 2, &hd->full[s], pol);
-                uint8_t *sdst = st + 32 * p.strideA;
-                if (p.blockScaleA) {
-                    if (lane < 2) {
-                        const uint8_t *sc =
-                            (lane == 0 ? p.gs : p.us) + (static_cast<size_t>(e) * p.I + tile * 16) * (p.H / 16);
-                        bulk_g2s(sdst + lane * 16 * p.sstrideA, sc, 16 * (p.H / 16), &hd->full[s], pol);
+                mbar_expect_tx(bar, isA ? bytesA : bytesB);
+                if (isA) {
+                    // gate rows i0..i0+15 and up rows i0..i0+15, K elements part*KA ..
+                    const int row = e * p.I + tile * 16;
+                    const int nsp = p.KA / 128;
+                    for (int m = 0; m < 2; ++m) {
+                        uint8_t *nd = st + (m ? p.offUq : p.offGq);
+                        const CUtensorMap *tq = &p.tm[m];
+                        if (p.nib_mode == 0) {
+                            tma3d(nd, tq, 0, row, part * nsp, bar, pol);
+                        } else {
+                            for (int b2 = 0; b2 < p.KA / 256; ++b2)
+                                tma2d(nd + b2 * 16 * 128, tq, part * (p.KA / 2) + b2 * 128, row, bar, pol);
+                        }
+                        uint8_t *sd = st + (m ? p.offUs : p.offGs);
+                        if (p.scale_tmaA)
+                            tma2d(sd, &p.tm[3 + m], part * (p.KA / 16), row, bar, pol);
+                        else
+                            bulk_g2s(sd, (m ? p.us : p.gs) + static_cast<size_t>(row) * (p.H / 16), 16 * (p.H / 16),
+                                     bar, pol);
                     }
                 } else {
-                    const uint8_t *sc = (r < 16 ? p.gs : p.us) + row * (p.H / 16) + part * (p.KA / 16);
-                    bulk_g2s(sdst + r * p.sstrideA, sc, p.KA / 16, &hd->full[s], pol);
-                }
-            } else {
-                uint8_t *sdst = st + kMB * p.strideB;
-                for (int r = lane; r < kMB; r += 32) {
-                    const size_t row = static_cast<size_t>(e) * p.H + tile * kMB + r;
-                    bulk_g2s(st + r * p.strideB, p.dq + row * (p.I / 2) + part * (p.KB / 2), p.KB / 2, &hd->full[s],
-                             pol);
-                    if (!p.blockScaleB)
-                        bulk_g2s(sdst + r * p.sstrideB, p.ds + row * (p.I / 16) + part * (p.KB / 16), p.KB / 16,
-                                 &hd->full[s], pol);
-                }
-                if (p.blockScaleB && lane == 0) {
-                    const uint8_t *sc = p.ds + (static_cast<size_t>(e) * p.H + tile * kMB) * (p.I / 16);
-                    bulk_g2s(sdst, sc, kMB * (p.I / 16), &hd->full[s], pol);
+                    // down rows h0..h0+63, K elements part*KB ..
+                    const int row = e * p.H + tile * kMB;
+                    if (p.nib_mode == 0) {
+                        tma3d(st + p.offDq, &p.tm[2], 0, row, part * (p.KB / 128), bar, pol);
+                    } else {
+                        for (int b2 = 0; b2 < p.KB / 256; ++b2)
+                            tma2d(st + p.offDq + b2 * kMB * 128, &p.tm[2], part * (p.KB / 2) + b2 * 128, row, bar,
+                                  pol);
+                    }
+                    if (p.scale_tmaB)
+                        tma2d(st + p.offDs, &p.tm[5], part * (p.KB / 16), row, bar, pol);
+                    else
+                        bulk_g2s(st + p.offDs, p.ds + static_cast<size_t>(row) * (p.I / 16), kMB * (p.I / 16), bar,
+                                 pol);
                 }
             }
+            __syncwarp();
             if (lane == 0) hd->fill_cnt += 1;
             if (++s == p.NS) {
                 s = 0;
@@ -804,7 +893,10 @@ __device__ __noinline__ void producer_loop(const KernelParams &p, uint8_t *smem,
 template <bool NULLM>
 __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_constant__ KernelParams p)
 {
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // swizzled TMA boxes want 1024-byte aligned destinations; the launch adds
+    // 1024 bytes of slack for this
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x;
     const int P = p.T * p.k;
     Tabs tb = make_tabs(smem, p.tab_off, P);
@@ -822,7 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
         hd->abort_flag = 0;
         hd->fill_cnt = 0;
         hd->cons_cnt = 0;
-        hd->cflag = 1;
+        hd->verdict[0] = hd->verdict[1] = 1;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     // grouping (every CTA, redundantly; scratch aliases the reduction buffer)
@@ -887,6 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
         c.t = c.lane & 3;
         c.s = 0;
         c.ph = 0;
+        c.nv = 0;
         c.abort_flag = abort_flag;
         consumer_loop<NULLM>(c);
     }
