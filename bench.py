@@ -251,6 +251,8 @@ def main():
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="direct launches only (W warm-up + K steps), for running under a profiler")
     args = ap.parse_args()
     if args.impl == "reference":
         if args.steps > 50:
@@ -271,6 +273,16 @@ def main():
     __graft_entry__.build()
 
     S = setup(args.workload, device)
+    if args.profile:
+        from quantized_moe_routed_gb300 import binding
+        n = len(S["ids_rot"])
+        for i in range(args.warmup + args.steps):
+            binding.moe_decode(S["plan"].handle, S["xd"], S["ids_rot"][i % n], S["wd"], S["y"], S["ws"])
+        torch.cuda.synchronize()
+        st_code = S["plan"].check(S["ws"])
+        print(json.dumps({"profile_run": True, "workload": S["wl"].name, "steps": args.steps,
+                          "warmup": args.warmup, "status": st_code}))
+        return
     g, st = capture(S)
     reps = max(1, args.steps // GRAPH_STEPS)
     steps = reps * GRAPH_STEPS
