@@ -51,7 +51,9 @@ struct moe_plan {
     int nib_mode = 0;
     int scale_tmaA = 0, spA = 0, shA = 0, mkA = 0, scale_tmaB = 0, spB = 0, shB = 0, mkB = 0;
     int offGq = 0, offUq = 0, offGs = 0, offUs = 0, offDq = 0, offDs = 0;
-    int stage_bytes = 0;
+    int offX = 0, xpitch = 0, offH = 0, hpitch = 0;
+    int stage_bytes_nt[3] = {0, 0, 0};  // stage bytes of the 1- and 2-n-tile variants
+    int stage_bytes = 0;                // of the 2-n-tile variant (the largest)
     CUtensorMap tm[6];
     int Tc = 0;  // tokens per launch chunk
     long long timeout_ns = 1000000000LL;
@@ -76,8 +78,9 @@ struct PartPlan {
     int KP, scale_tma, sp, sh, mk;
 };
 
-bool choose_part(int K, int cap, PartPlan *pp)
+bool choose_part(int K, int cap, int cap_odd, PartPlan *pp)
 {
+    if (K % 256 != 0) cap = cap_odd;
     for (int kp = (K < cap ? K : cap) / 128 * 128; kp >= 128; kp -= 128) {
         if (K % kp) continue;
         if (K % 256 == 0) {
@@ -149,23 +152,25 @@ CUresult encode_scale(CUtensorMap *m, const void *base, uint64_t rows_total, int
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// Kernel variant for a launch of T tokens: groups of at most 8 pairs (one MMA
+// n-tile) when T*k <= 8, else at most 16 pairs (two n-tiles).
+int ntiles_for(const moe_plan *pl, int T) { return T * pl->d.top_k <= 8 ? 1 : 2; }
+
 moe::SmemLayout layout_for(const moe_plan *pl, int T)
 {
     moe::SmemLayout L{};
     const int P = T * pl->d.top_k;
-    const int pc = P < moe::kGroupPairs ? P : moe::kGroupPairs;
-    int ntmax = (pc + 7) / 8;
-    if (ntmax < 1) ntmax = 1;
-    const int red_need = 8192 * ntmax;
+    const int nt = ntiles_for(pl, T);
+    const int red_need = 8192 * nt;
     const int scr_need = align16i(2 * P) + 8 * pl->d.E + 4 + 16;
     L.red_bytes = static_cast<int>(up(red_need > scr_need ? red_need : scr_need, 128));
     L.tab_bytes = static_cast<int>(up(512 + 4 * align16i(2 * P) + align16i(P) + align16i(T), 128));
-    L.stage_bytes = pl->stage_bytes;
+    L.stage_bytes = pl->stage_bytes_nt[nt];
     const int avail = pl->smem_optin - L.red_bytes - L.tab_bytes - 1024;
-    int ns = avail / pl->stage_bytes;
+    int ns = avail / L.stage_bytes;
     if (ns > moe::kMaxStages) ns = moe::kMaxStages;
     L.NS = ns;
-    L.red_off = ns * pl->stage_bytes;
+    L.red_off = ns * L.stage_bytes;
     L.tab_off = L.red_off + L.red_bytes;
     L.total = L.tab_off + L.tab_bytes + 1024;  // + slack to align the ring to 1024 bytes
     return L;
@@ -271,7 +276,10 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
     p.offUs = pl->offUs;
     p.offDq = pl->offDq;
     p.offDs = pl->offDs;
-    p.stage_bytes = pl->stage_bytes;
+    p.offX = pl->offX;
+    p.xpitch = pl->xpitch;
+    p.offH = pl->offH;
+    p.hpitch = pl->hpitch;
     p.timeout_ns = pl->timeout_ns;
     p.null_mode = path == Path::Null ? 1 : 0;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -294,9 +302,7 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
         p.red_off = L.red_off;
         p.red_bytes = L.red_bytes;
         p.tab_off = L.tab_off;
-        const int P = Tn * pl->d.top_k;
-        const int pc = P < moe::kGroupPairs ? P : moe::kGroupPairs;
-        p.ntmax = (pc + 7) / 8;
+        p.ntiles = ntiles_for(pl, Tn);
         cudaError_t e = moe::launch_step(p, pl->num_sms, L.total, pl->pdl, cs);
         if (e != cudaSuccess) {
             reject(pl);
@@ -392,7 +398,7 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
         if (ms > 0) pl->timeout_ns = ms * 1000000LL;
     }
     PartPlan pa{}, pb{};
-    if (!choose_part(d.H, 2048, &pa) || !choose_part(d.I, 1024, &pb)) {
+    if (!choose_part(d.H, 1024, 2048, &pa) || !choose_part(d.I, 512, 1024, &pb)) {
         delete pl;
         return fail(MOE_ERR_UNSUPPORTED_SHAPE,
                     "no stage tiling for H=%d, I=%d (an odd multiple of 128 must be <= 2048 for H, <= 1024 for I)",
@@ -411,15 +417,24 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
     pl->nPA = d.H / pl->KA;
     pl->nPB = d.I / pl->KB;
     pl->nHt = d.H / moe::kMB;
+    // stage layouts: weights (1024-aligned sub-buffers), then the group's
+    // activation rows at a pitch of 2*KP + 16 bytes
     pl->offGq = 0;
     pl->offUq = 8 * pl->KA;
     pl->offGs = 16 * pl->KA;
     pl->offUs = pl->offGs + up1024(16 * pl->spA);
-    const int stA = pl->offUs + up1024(16 * pl->spA);
+    pl->offX = pl->offUs + up1024(16 * pl->spA);
+    pl->xpitch = 2 * pl->KA + 16;
     pl->offDq = 0;
     pl->offDs = 32 * pl->KB;
-    const int stB = pl->offDs + up1024(moe::kMB * pl->spB);
-    pl->stage_bytes = up1024(stA > stB ? stA : stB);
+    pl->offH = pl->offDs + up1024(moe::kMB * pl->spB);
+    pl->hpitch = 2 * pl->KB + 16;
+    for (int nt = 1; nt <= 2; ++nt) {
+        const int stA = pl->offX + 8 * nt * pl->xpitch;
+        const int stB = pl->offH + 8 * nt * pl->hpitch;
+        pl->stage_bytes_nt[nt] = up1024(stA > stB ? stA : stB);
+    }
+    pl->stage_bytes = pl->stage_bytes_nt[2];
     // tensor maps (host-only encoding; no device memory involved)
     if (!encoder()) {
         delete pl;

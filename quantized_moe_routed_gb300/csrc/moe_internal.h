@@ -13,7 +13,7 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;
 constexpr int kMaxPairs = 4096;     // T*k per launch (prefill is chunked to this)
-constexpr int kGroupPairs = 32;     // pairs per expert group = 4 MMA n-tiles of 8
+constexpr int kGroupPairs = 16;     // pairs per expert group, at most 2 MMA n-tiles of 8
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxStages = 8;
@@ -59,10 +59,12 @@ struct KernelParams {
     int scale_tmaA, scale_tmaB;  // 1: scale rows by 2-D tensor map; 0: one 1-D bulk copy (natural layout)
     int spA, shA, mkA, spB, shB, mkB;  // scale smem row pitch, swizzle shift and mask
     int offGq, offUq, offGs, offUs;    // phase-A stage sub-buffers (bytes, 1024-aligned)
+    int offX, xpitch;                  // phase-A x slice: row n of the group at offX + n*xpitch
     int offDq, offDs;                  // phase-B stage sub-buffers
+    int offH, hpitch;                  // phase-B h slice
     int stage_bytes, NS;
     int red_off, red_bytes, tab_off;            // smem layout (bytes)
-    int ntmax;                                  // MMA n-tiles needed (1..4)
+    int ntiles;                                 // kernel variant: n-tiles per group (1 or 2)
     long long timeout_ns;
     int null_mode;      // 1: measurement variant (no dequant / math)
 };

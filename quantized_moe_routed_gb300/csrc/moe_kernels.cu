@@ -10,8 +10,8 @@
 //
 //  * One persistent CTA per SM.  Every CTA groups the T*k (token, slot) pairs
 //    by expert in shared memory (a stable counting sort; no separate launch),
-//    splitting an expert's pairs into groups of at most 32 (four 8-wide MMA
-//    n-tiles).
+//    splitting an expert's pairs into groups of at most 8 or 16 pairs (one or
+//    two 8-wide MMA n-tiles, fixed per launch from T*k).
 //  * Tickets come from one atomic counter (the first one is the CTA index, so
 //    the first weight loads need no atomic).  Phase-A tickets (group, 16
 //    intermediate rows of gate and up) come first, then phase-B tickets
@@ -22,9 +22,10 @@
 //    version F1 was correct but not faster, "LNA-CANON.md", "含めないもの").
 //  * A producer warp streams each ticket's packed E2M1 rows and E4M3 scale
 //    rows HBM -> shared memory with TMA tensor copies (cp.async.bulk.tensor:
-//    one 16-32 KB box per projection and stage, L2 evict-first) into a ring of
-//    stages guarded by mbarriers; it keeps prefetching while consumers wait on
-//    a dependency.  Box shapes are chosen so the consumers' 16-byte reads are
+//    one box per projection and stage, L2 evict-first), plus the group's
+//    activation rows (x for gate/up, h for down) with bulk copies, into a ring
+//    of stages guarded by mbarriers.  Consumers read shared memory only.  Box
+//    shapes are chosen so the consumers' 16-byte weight reads are
 //    bank-conflict-free without padding.
 //  * Eight consumer warps dequantise in registers -- cvt e2m1x2 -> f16x2, times
 //    the block scale (E2M1 x E4M3 is exact in fp16) -- and run mma.sync
@@ -32,6 +33,9 @@
 //    group's pairs as N.  Activations (x for gate/up, h for down) are the
 //    B operand; the K order inside each thread is permuted identically on both
 //    operands, so every thread reads 16 contiguous bytes of a weight row.
+//  * A down ticket's h rows exist once all 16-row gate/up tickets of its group
+//    are done: the producer waits (bounded) on the group's counter before it
+//    copies them, so the consumers never wait on global memory.
 //  * h = SiLU(g) * u goes to a workspace buffer (fp16) after a fixed-order
 //    cross-warp reduction; down outputs go to per-pair fp32 partials; the last
 //    CTA to finish a (token, 64-row tile) sums its k partials in slot order.
@@ -414,8 +418,9 @@ __device__ __forceinline__ uint16_t scale_pair(const uint8_t *sb, int pitch, int
 template <int MT, int NT, bool BF16B, bool NULLM>
 __device__ __forceinline__ void chunk_math(const uint4 (&ra)[MT], const uint4 (&rb)[MT], const uint16_t (&s_a)[MT],
                                            const uint16_t (&s_b)[MT], const uint4 (&bq)[NT][4],
-                                           float (&acc)[MT][NT][4])
+                                           float (&acc)[MT][NT][4], int gcnt)
 {
+    const int ntv = (gcnt + 7) >> 3;  // n-tiles holding at least one pair (warp-uniform)
     uint32_t sa[MT][2], sb[MT][2];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
@@ -445,7 +450,7 @@ __device__ __forceinline__ void chunk_math(const uint4 (&ra)[MT], const uint4 (&
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint32_t u = u4w(bq[nt][v], i);
-                    bf[nt][i] = BF16B ? bf16x2_to_f16x2(u) : u;
+                    bf[nt][i] = (BF16B && nt < ntv) ? bf16x2_to_f16x2(u) : u;
                 }
             }
 #pragma unroll
@@ -457,9 +462,11 @@ __device__ __forceinline__ void chunk_math(const uint4 (&ra)[MT], const uint4 (&
                 fa0 = hmul2(fa0, sA); fa1 = hmul2(fa1, sA); fa2 = hmul2(fa2, sA); fa3 = hmul2(fa3, sA);
                 fb0 = hmul2(fb0, sB); fb1 = hmul2(fb1, sB); fb2 = hmul2(fb2, sB); fb3 = hmul2(fb3, sB);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma16816(acc[mt][nt], fa0, fb0, fa1, fb1, bf[nt][0], bf[nt][1]);
+                for (int nt = 0; nt < NT; ++nt)
+                    if (nt < ntv) mma16816(acc[mt][nt], fa0, fb0, fa1, fb1, bf[nt][0], bf[nt][1]);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma16816(acc[mt][nt], fa2, fb2, fa3, fb3, bf[nt][2], bf[nt][3]);
+                for (int nt = 0; nt < NT; ++nt)
+                    if (nt < ntv) mma16816(acc[mt][nt], fa2, fb2, fa3, fb3, bf[nt][2], bf[nt][3]);
             }
         }
     }
@@ -467,7 +474,6 @@ __device__ __forceinline__ void chunk_math(const uint4 (&ra)[MT], const uint4 (&
 
 // ------------------------------------------------------------------ consumer context
 struct Cons {
-    const KernelParams *p;
     uint8_t *smem;
     Tabs tb;
     float4 *red;
@@ -493,11 +499,11 @@ __device__ __forceinline__ bool publish_verdict(Cons &c, bool ok_in_thread0)
     return ok;
 }
 
-__device__ __forceinline__ void cons_release_stage(Cons &c)
+__device__ __forceinline__ void cons_release_stage(const KernelParams &p, Cons &c)
 {
     __syncwarp();
     if (c.lane == 0) mbar_arrive(&c.tb.hdr->empty[c.s]);
-    if (++c.s == c.p->NS) {
+    if (++c.s == p.NS) {
         c.s = 0;
         c.ph ^= 1u;
     }
@@ -507,12 +513,12 @@ __device__ __forceinline__ void cons_release_stage(Cons &c)
 // thread 0 takes the bounded wait and publishes the verdict before a named
 // barrier, so all 256 consumer threads take the same branch; every thread then
 // observes the completed phase itself (acquire) before reading the stage.
-__device__ __forceinline__ int4 cons_next_stage(Cons &c)
+__device__ __forceinline__ int4 cons_next_stage(const KernelParams &p, Cons &c)
 {
     SmemHdr *hd = c.tb.hdr;
     bool ok = false;
     if (c.tid == 0) {
-        ok = wait_bar(&hd->full[c.s], c.ph, *c.p, c.abort_flag);
+        ok = wait_bar(&hd->full[c.s], c.ph, p, c.abort_flag);
         if (ok) hd->cons_cnt += 1;
     }
     if (!publish_verdict(c, ok)) return make_int4(KIND_END, 0, 0, 0);
@@ -521,16 +527,20 @@ __device__ __forceinline__ int4 cons_next_stage(Cons &c)
     return hd->stage_hdr[c.s];
 }
 
-// B-operand loads for one chunk: 4 x 16 bytes per n-tile (elements kglob .. kglob+31).
-template <int NT, bool CG>
-__device__ __forceinline__ void load_bq(uint4 (&bq)[NT][4], const uint16_t *const (&bptr)[NT], int kglob)
+// B operand of one chunk from the stage's activation slice: pair n of the
+// group (n = nt*8 + g) at row n of the slice, elements koff .. koff+31
+// (16 bytes per v).  Pairs past the group's end read as zero.
+template <int NT>
+__device__ __forceinline__ void load_bq_smem(uint4 (&bq)[NT][4], const uint8_t *slice, int pitch, int koff, int g,
+                                             int gcnt)
 {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        if (bptr[nt]) {
-            const uint16_t *src = bptr[nt] + kglob;
+        const int n = nt * 8 + g;
+        if (n < gcnt) {
+            const uint8_t *src = slice + n * pitch + koff * 2;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) bq[nt][v] = CG ? ldg_cg16(src + 8 * v) : ldg_nc16(src + 8 * v);
+            for (int v = 0; v < 4; ++v) bq[nt][v] = *reinterpret_cast<const uint4 *>(src + 16 * v);
         } else {
 #pragma unroll
             for (int v = 0; v < 4; ++v) bq[nt][v] = make_uint4(0, 0, 0, 0);
@@ -540,21 +550,10 @@ __device__ __forceinline__ void load_bq(uint4 (&bq)[NT][4], const uint16_t *cons
 
 // ---- phase A: gate/up rows i0..i0+15 for one group -> h (fp16)
 template <int NT, bool NULLM>
-__device__ __noinline__ bool ticket_A(Cons &c, int grp, int tile)
+__device__ __forceinline__ bool ticket_A(const KernelParams &p, Cons &c, int grp, int tile)
 {
-    const KernelParams &p = *c.p;
     const int e = c.tb.gexp[grp], gbeg = c.tb.gbeg[grp], gcnt = c.tb.gcnt[grp];
     const int i0 = tile * 16;
-    const uint16_t *bptr[NT];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int n = nt * 8 + c.g;
-        bptr[nt] = nullptr;
-        if (n < gcnt) {
-            const int pr = c.tb.perm[gbeg + n];
-            bptr[nt] = p.x + static_cast<size_t>(pr / p.k) * p.H;
-        }
-    }
     float acc[2][NT][4];
 #pragma unroll
     for (int a = 0; a < 2; ++a)
@@ -564,44 +563,30 @@ __device__ __noinline__ bool ticket_A(Cons &c, int grp, int tile)
             for (int r = 0; r < 4; ++r) acc[a][b][r] = 0.f;
 
     const int chunks = p.KA / 128;
-    const int ks = c.warp;  // K-slices = 8 consumer warps
+    const int ks = c.warp;  // K-slices = 8 consumer warps, both m-tiles per warp
     for (int part = 0; part < p.nPA; ++part) {
         if (part > 0) {
-            const int4 h = cons_next_stage(c);
+            const int4 h = cons_next_stage(p, c);
             if (h.x == KIND_END) return false;
         }
         const uint8_t *st = c.smem + c.s * p.stage_bytes;
-        constexpr bool DB = NT <= 2;  // prefetch the next chunk's B operand (register budget)
-        int q = ks;
-        uint4 bq[NT][4], bn[NT][4];
-        if (DB && q < chunks) load_bq<NT, false>(bq, bptr, part * p.KA + k_off(p.nib_mode, q, c.t));
-        for (; q < chunks; q += kConsumerWarps) {
-            const int qn = q + kConsumerWarps;
-            if (!DB) load_bq<NT, false>(bq, bptr, part * p.KA + k_off(p.nib_mode, q, c.t));
-            if (DB && qn < chunks) load_bq<NT, false>(bn, bptr, part * p.KA + k_off(p.nib_mode, qn, c.t));
-            {
-                uint4 ra[2], rb[2];
-                uint16_t s_a[2], s_b[2];
-                const int ko = k_off(p.nib_mode, q, c.t);
+        for (int q = ks; q < chunks; q += kConsumerWarps) {
+            uint4 ra[2], rb[2], bq[NT][4];
+            uint16_t s_a[2], s_b[2];
+            const int ko = k_off(p.nib_mode, q, c.t);
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {  // m-tile 0: gate rows, 1: up rows
-                    const uint8_t *nb = st + (mt ? p.offUq : p.offGq);
-                    ra[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, 16, c.g, q, c.t));
-                    rb[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, 16, c.g + 8, q, c.t));
-                    const uint8_t *sb = st + (mt ? p.offUs : p.offGs);
-                    s_a[mt] = scale_pair(sb, p.spA, p.shA, p.mkA, c.g, ko);
-                    s_b[mt] = scale_pair(sb, p.spA, p.shA, p.mkA, c.g + 8, ko);
-                }
-                chunk_math<2, NT, true, NULLM>(ra, rb, s_a, s_b, bq, acc);
+            for (int mt = 0; mt < 2; ++mt) {  // m-tile 0: gate rows, 1: up rows
+                const uint8_t *nb = st + (mt ? p.offUq : p.offGq);
+                ra[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, 16, c.g, q, c.t));
+                rb[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, 16, c.g + 8, q, c.t));
+                const uint8_t *sb = st + (mt ? p.offUs : p.offGs);
+                s_a[mt] = scale_pair(sb, p.spA, p.shA, p.mkA, c.g, ko);
+                s_b[mt] = scale_pair(sb, p.spA, p.shA, p.mkA, c.g + 8, ko);
             }
-            if (DB && qn < chunks) {
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) bq[nt][v] = bn[nt][v];
-            }
+            load_bq_smem<NT>(bq, st + p.offX, p.xpitch, ko, c.g, gcnt);
+            chunk_math<2, NT, true, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
         }
-        cons_release_stage(c);
+        cons_release_stage(p, c);
     }
     // cross-warp reduction (fixed order) -> g, u -> h
 #pragma unroll
@@ -616,15 +601,15 @@ __device__ __noinline__ bool ticket_A(Cons &c, int grp, int tile)
     bool range_bad = false;
     for (int idx = c.tid; idx < NT * 128; idx += kConsumerThreads) {
         const int nt = idx >> 7, ls = (idx >> 2) & 31, r = idx & 3;
-        float sg = 0.f, su = 0.f;
-#pragma unroll
-        for (int k2 = 0; k2 < kConsumerWarps; ++k2) {
-            sg += redf[(((k2 * 2 + 0) * NT + nt) * 32 + ls) * 4 + r];
-            su += redf[(((k2 * 2 + 1) * NT + nt) * 32 + ls) * 4 + r];
-        }
         const int row = (ls >> 2) + 8 * (r >> 1);
         const int n = nt * 8 + 2 * (ls & 3) + (r & 1);
         if (n < gcnt) {
+            float sg = 0.f, su = 0.f;
+#pragma unroll
+            for (int k2 = 0; k2 < kConsumerWarps; ++k2) {
+                sg += redf[(((k2 * 2 + 0) * NT + nt) * 32 + ls) * 4 + r];
+                su += redf[(((k2 * 2 + 1) * NT + nt) * 32 + ls) * 4 + r];
+            }
             const float gv = sg * tsg, uv = su * tsu;
             float hv = gv / (1.0f + __expf(-gv)) * uv;
             if (NULLM) hv = 0.f;
@@ -633,6 +618,8 @@ __device__ __noinline__ bool ticket_A(Cons &c, int grp, int tile)
         }
     }
     if (range_bad) atomicOr(p.ctrl + 2, kErrRange);
+    // h is read back through the async proxy (bulk copies) by other CTAs
+    asm volatile("fence.proxy.async.global;" ::: "memory");
     consumer_sync();
     if (c.tid == 0) {
         __threadfence();
@@ -643,25 +630,10 @@ __device__ __noinline__ bool ticket_A(Cons &c, int grp, int tile)
 
 // ---- phase B: down rows h0..h0+63 for one group -> partials, then combine
 template <int NT, bool NULLM>
-__device__ __noinline__ bool ticket_B(Cons &c, int grp, int tile)
+__device__ __forceinline__ bool ticket_B(const KernelParams &p, Cons &c, int grp, int tile)
 {
-    const KernelParams &p = *c.p;
     const int e = c.tb.gexp[grp], gbeg = c.tb.gbeg[grp], gcnt = c.tb.gcnt[grp];
     const int h0 = tile * kMB;
-    // the group's h rows must be complete: one thread waits (acquire), the
-    // verdict is published before the barrier so every consumer agrees
-    bool ok = false;
-    if (c.tid == 0) {
-        ok = wait_count(p.doneA + grp, static_cast<uint32_t>(p.I / 16), p, c.abort_flag);
-        if (!ok) *c.abort_flag = 1;
-    }
-    if (!publish_verdict(c, ok)) return false;
-    const uint16_t *bptr[NT];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int n = nt * 8 + c.g;
-        bptr[nt] = (n < gcnt) ? p.hbuf + static_cast<size_t>(gbeg + n) * p.I : nullptr;
-    }
     float acc[2][NT][4];
 #pragma unroll
     for (int a = 0; a < 2; ++a)
@@ -674,42 +646,28 @@ __device__ __noinline__ bool ticket_B(Cons &c, int grp, int tile)
     const int ks = c.warp & 3, mg = c.warp >> 2;  // 4 K-slices x 2 m-groups of 2 m-tiles
     for (int part = 0; part < p.nPB; ++part) {
         if (part > 0) {
-            const int4 h = cons_next_stage(c);
+            const int4 h = cons_next_stage(p, c);
             if (h.x == KIND_END) return false;
         }
         const uint8_t *st = c.smem + c.s * p.stage_bytes;
         const uint8_t *nb = st + p.offDq;
         const uint8_t *sb = st + p.offDs;
-        constexpr bool DB = NT <= 2;
-        int q = ks;
-        uint4 bq[NT][4], bn[NT][4];
-        if (DB && q < chunks) load_bq<NT, true>(bq, bptr, part * p.KB + k_off(p.nib_mode, q, c.t));
-        for (; q < chunks; q += 4) {
-            const int qn = q + 4;
-            if (!DB) load_bq<NT, true>(bq, bptr, part * p.KB + k_off(p.nib_mode, q, c.t));
-            if (DB && qn < chunks) load_bq<NT, true>(bn, bptr, part * p.KB + k_off(p.nib_mode, qn, c.t));
-            {
-                uint4 ra[2], rb[2];
-                uint16_t s_a[2], s_b[2];
-                const int ko = k_off(p.nib_mode, q, c.t);
+        for (int q = ks; q < chunks; q += 4) {
+            uint4 ra[2], rb[2], bq[NT][4];
+            uint16_t s_a[2], s_b[2];
+            const int ko = k_off(p.nib_mode, q, c.t);
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    const int r0 = mg * 32 + mt * 16 + c.g;
-                    ra[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, kMB, r0, q, c.t));
-                    rb[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, kMB, r0 + 8, q, c.t));
-                    s_a[mt] = scale_pair(sb, p.spB, p.shB, p.mkB, r0, ko);
-                    s_b[mt] = scale_pair(sb, p.spB, p.shB, p.mkB, r0 + 8, ko);
-                }
-                chunk_math<2, NT, false, NULLM>(ra, rb, s_a, s_b, bq, acc);
+            for (int mt = 0; mt < 2; ++mt) {
+                const int r0 = mg * 32 + mt * 16 + c.g;
+                ra[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, kMB, r0, q, c.t));
+                rb[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, kMB, r0 + 8, q, c.t));
+                s_a[mt] = scale_pair(sb, p.spB, p.shB, p.mkB, r0, ko);
+                s_b[mt] = scale_pair(sb, p.spB, p.shB, p.mkB, r0 + 8, ko);
             }
-            if (DB && qn < chunks) {
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) bq[nt][v] = bn[nt][v];
-            }
+            load_bq_smem<NT>(bq, st + p.offH, p.hpitch, ko, c.g, gcnt);
+            chunk_math<2, NT, false, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
         }
-        cons_release_stage(c);
+        cons_release_stage(p, c);
     }
     // cross-warp reduction over the 4 K-slices -> o -> per-pair partials
 #pragma unroll
@@ -725,12 +683,14 @@ __device__ __noinline__ bool ticket_B(Cons &c, int grp, int tile)
     for (int idx = c.tid; idx < 4 * NT * 128; idx += kConsumerThreads) {
         const int mm = idx / (NT * 128), rem = idx - mm * (NT * 128);
         const int nt = rem >> 7, ls = (rem >> 2) & 31, r = rem & 3;
-        float so = 0.f;
-#pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) so += redf[(((k2 * 4 + mm) * NT + nt) * 32 + ls) * 4 + r];
         const int row = mm * 16 + (ls >> 2) + 8 * (r >> 1);
         const int n = nt * 8 + 2 * (ls & 3) + (r & 1);
-        if (n < gcnt) p.part[static_cast<size_t>(gbeg + n) * p.H + h0 + row] = so * tsd;
+        if (n < gcnt) {
+            float so = 0.f;
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) so += redf[(((k2 * 4 + mm) * NT + nt) * 32 + ls) * 4 + r];
+            p.part[static_cast<size_t>(gbeg + n) * p.H + h0 + row] = so * tsd;
+        }
     }
     consumer_sync();
     // count arrivals per (token, tile); the last arriver combines that token
@@ -763,36 +723,25 @@ __device__ __noinline__ bool ticket_B(Cons &c, int grp, int tile)
     return true;
 }
 
-template <bool NULLM>
-__device__ __forceinline__ void consumer_loop(Cons &c)
+template <int NT, bool NULLM>
+__device__ __forceinline__ void consumer_loop(const KernelParams &p, Cons &c)
 {
     for (;;) {
-        const int4 h = cons_next_stage(c);
+        const int4 h = cons_next_stage(p, c);
         if (h.x == KIND_END) break;
-        const int grp = h.y, tile = h.z;
-        const int nt = (c.tb.gcnt[grp] + 7) >> 3;
-        bool ok;
-        if (h.x == KIND_A) {
-            switch (nt) {
-                case 1: ok = ticket_A<1, NULLM>(c, grp, tile); break;
-                case 2: ok = ticket_A<2, NULLM>(c, grp, tile); break;
-                case 3: ok = ticket_A<3, NULLM>(c, grp, tile); break;
-                default: ok = ticket_A<4, NULLM>(c, grp, tile); break;
-            }
-        } else {
-            switch (nt) {
-                case 1: ok = ticket_B<1, NULLM>(c, grp, tile); break;
-                case 2: ok = ticket_B<2, NULLM>(c, grp, tile); break;
-                case 3: ok = ticket_B<3, NULLM>(c, grp, tile); break;
-                default: ok = ticket_B<4, NULLM>(c, grp, tile); break;
-            }
-        }
+        const bool ok = (h.x == KIND_A) ? ticket_A<NT, NULLM>(p, c, h.y, h.z) : ticket_B<NT, NULLM>(p, c, h.y, h.z);
         if (!ok) break;  // uniform: decided from a flag published before a barrier
     }
 }
 
 // ------------------------------------------------------------------ producer
-__device__ __noinline__ void producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, volatile int *abort_flag)
+// Lane 0 takes tickets, waits (bounded) for free stages and issues the weight
+// boxes; lanes 0..gcnt-1 then copy the group's activation rows (x rows for a
+// gate/up part, h rows for a down part) into the same stage.  A down part's h
+// rows exist only once the group's 16-row gate/up tickets are all finished:
+// lane 0 waits (bounded) for that count before the first part of the ticket.
+__device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb,
+                                              volatile int *abort_flag)
 {
     const int lane = threadIdx.x & 31;
     SmemHdr *hd = tb.hdr;
@@ -801,8 +750,8 @@ __device__ __noinline__ void producer_loop(const KernelParams &p, uint8_t *smem,
     const int TA = p.I / 16;
     const int nA = ng * TA;
     const int total = nA + ng * p.nHt;
-    const uint32_t bytesA = 32u * (p.KA / 2) + 32u * (p.KA / 16);
-    const uint32_t bytesB = kMB * (p.KB / 2) + kMB * (p.KB / 16);
+    const uint32_t wbytesA = 32u * (p.KA / 2) + 32u * (p.KA / 16);
+    const uint32_t wbytesB = kMB * (p.KB / 2) + kMB * (p.KB / 16);
     int s = 0;
     uint32_t ph = 0;
     int ticket = blockIdx.x;
@@ -814,10 +763,25 @@ __device__ __noinline__ void producer_loop(const KernelParams &p, uint8_t *smem,
         const int tt = isA ? ticket : ticket - nA;
         const int grp = isA ? tt / TA : tt / p.nHt;
         const int tile = isA ? tt % TA : tt % p.nHt;
-        const int e = tb.gexp[grp];
+        const int e = tb.gexp[grp], gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
         const int nparts = isA ? p.nPA : p.nPB;
+        // activation row of this lane's pair (x row for gate/up, h row for down)
+        const uint16_t *arow = nullptr;
+        if (lane < gcnt)
+            arow = isA ? p.x + static_cast<size_t>(tb.perm[gbeg + lane] / p.k) * p.H
+                       : p.hbuf + static_cast<size_t>(gbeg + lane) * p.I;
         bool ok = true;
-        for (int part = 0; part < nparts; ++part) {
+        if (!isA) {
+            int got = 1;
+            if (lane == 0) {
+                got = wait_count(p.doneA + grp, static_cast<uint32_t>(TA), p, abort_flag) ? 1 : 0;
+                // the h rows were written through the generic proxy; the bulk
+                // copies below read them through the async proxy
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            ok = __shfl_sync(0xffffffffu, got, 0) != 0;
+        }
+        for (int part = 0; ok && part < nparts; ++part) {
             int got = 0;
             if (lane == 0) got = wait_bar(&hd->empty[s], ph ^ 1u, p, abort_flag) ? 1 : 0;
             got = __shfl_sync(0xffffffffu, got, 0);
@@ -826,10 +790,11 @@ __device__ __noinline__ void producer_loop(const KernelParams &p, uint8_t *smem,
                 break;
             }
             uint8_t *st = smem + s * p.stage_bytes;
+            uint64_t *bar = &hd->full[s];
+            const int KP = isA ? p.KA : p.KB;
             if (lane == 0) {
-                uint64_t *bar = &hd->full[s];
                 hd->stage_hdr[s] = make_int4(isA ? KIND_A : KIND_B, grp, tile, part);
-                mbar_expect_tx(bar, isA ? bytesA : bytesB);
+                mbar_expect_tx(bar, (isA ? wbytesA : wbytesB) + static_cast<uint32_t>(gcnt) * 2u * KP);
                 if (isA) {
                     // gate rows i0..i0+15 and up rows i0..i0+15, K elements part*KA ..
                     const int row = e * p.I + tile * 16;
@@ -868,6 +833,10 @@ __device__ __noinline__ void producer_loop(const KernelParams &p, uint8_t *smem,
                 }
             }
             __syncwarp();
+            if (arow) {
+                uint8_t *dst = st + (isA ? p.offX + lane * p.xpitch : p.offH + lane * p.hpitch);
+                bulk_g2s(dst, arow + static_cast<size_t>(part) * KP, 2u * KP, bar, pol);
+            }
             if (lane == 0) hd->fill_cnt += 1;
             if (++s == p.NS) {
                 s = 0;
@@ -875,11 +844,14 @@ __device__ __noinline__ void producer_loop(const KernelParams &p, uint8_t *smem,
             }
         }
         ticket = __shfl_sync(0xffffffffu, next, 0);
-        if (!ok) break;
+        if (!ok) {
+            if (lane == 0) *abort_flag = 1;
+            break;
+        }
     }
     // end marker (the consumers' waits also end on the abort flag)
     if (lane == 0) {
-        if (wait_bar(&hd->empty[s], ph ^ 1u, p, abort_flag)) {
+        if (!*abort_flag && wait_bar(&hd->empty[s], ph ^ 1u, p, abort_flag)) {
             hd->stage_hdr[s] = make_int4(KIND_END, 0, 0, 0);
             mbar_arrive(&hd->full[s]);
         } else {
@@ -890,7 +862,7 @@ __device__ __noinline__ void producer_loop(const KernelParams &p, uint8_t *smem,
 }
 
 // ------------------------------------------------------------------ the persistent step kernel
-template <bool NULLM>
+template <int NT, bool NULLM>
 __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_constant__ KernelParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -924,13 +896,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
         int32_t *ecnt = reinterpret_cast<int32_t *>(scr + align16(2 * P));
         int32_t *eoff = ecnt + p.E;
         group_pairs(p.ids, P, p.E, ids16, ecnt, eoff, tb.perm, tb.pos, &hd->n_valid, &hd->n_bad);
-        // split each expert's pairs into groups of <= 32
+        // split each expert's pairs into groups of at most G = 8*NT pairs
+        constexpr int G = 8 * NT;
         if (tid < 32) {
             const int lane = tid;
             const int per = (p.E + 31) / 32;
             const int lo = min(p.E, lane * per), hi = min(p.E, lo + per);
             int s = 0;
-            for (int e2 = lo; e2 < hi; ++e2) s += (ecnt[e2] + kGroupPairs - 1) / kGroupPairs;
+            for (int e2 = lo; e2 < hi; ++e2) s += (ecnt[e2] + G - 1) / G;
             int incl = s;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
@@ -940,10 +913,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
             int gi = incl - s;
             for (int e2 = lo; e2 < hi; ++e2) {
                 const int cnt = ecnt[e2];
-                for (int b = 0; b < cnt; b += kGroupPairs) {
+                for (int b = 0; b < cnt; b += G) {
                     tb.gexp[gi] = static_cast<uint16_t>(e2);
                     tb.gbeg[gi] = static_cast<uint16_t>(eoff[e2] + b);
-                    tb.gcnt[gi] = static_cast<uint8_t>(min(kGroupPairs, cnt - b));
+                    tb.gcnt[gi] = static_cast<uint8_t>(min(G, cnt - b));
                     ++gi;
                 }
             }
@@ -968,7 +941,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
         producer_loop(p, smem, tb, abort_flag);
     } else {
         Cons c;
-        c.p = &p;
         c.smem = smem;
         c.tb = tb;
         c.red = reinterpret_cast<float4 *>(smem + p.red_off);
@@ -981,7 +953,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
         c.ph = 0;
         c.nv = 0;
         c.abort_flag = abort_flag;
-        consumer_loop<NULLM>(c);
+        consumer_loop<NT, NULLM>(p, c);
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
@@ -1055,9 +1027,15 @@ int group_smem_bytes(int P, int E)
 
 cudaError_t set_step_smem_limit(int bytes)
 {
-    cudaError_t e = cudaFuncSetAttribute(moe_step_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(moe_step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const void *fns[] = {reinterpret_cast<const void *>(moe_step_kernel<1, false>),
+                         reinterpret_cast<const void *>(moe_step_kernel<2, false>),
+                         reinterpret_cast<const void *>(moe_step_kernel<1, true>),
+                         reinterpret_cast<const void *>(moe_step_kernel<2, true>)};
+    for (const void *f : fns) {
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_step(const KernelParams &p, int grid, int smem_bytes, bool pdl, cudaStream_t st)
@@ -1072,8 +1050,11 @@ cudaError_t launch_step(const KernelParams &p, int grid, int smem_bytes, bool pd
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (p.null_mode) return cudaLaunchKernelEx(&cfg, moe_step_kernel<true>, p);
-    return cudaLaunchKernelEx(&cfg, moe_step_kernel<false>, p);
+    if (p.ntiles == 1)
+        return p.null_mode ? cudaLaunchKernelEx(&cfg, moe_step_kernel<1, true>, p)
+                           : cudaLaunchKernelEx(&cfg, moe_step_kernel<1, false>, p);
+    return p.null_mode ? cudaLaunchKernelEx(&cfg, moe_step_kernel<2, true>, p)
+                       : cudaLaunchKernelEx(&cfg, moe_step_kernel<2, false>, p);
 }
 
 cudaError_t launch_group(const int32_t *ids, int P, int E, uint32_t *ctrl, int32_t *counts, int32_t *offsets,
