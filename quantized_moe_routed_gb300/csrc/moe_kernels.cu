@@ -228,6 +228,7 @@ struct SmemHdr {
     int verdict[2];                            // consumer verdicts, alternating slots
     int pad1[2];
     int comb_tok[kGroupPairs];
+    int pend_stage[kMaxStages], pend_grp[kMaxStages], pend_part[kMaxStages];  // producer's queued h copies
 };
 static_assert(sizeof(SmemHdr) <= 512, "header too large");
 
@@ -735,11 +736,96 @@ __device__ __forceinline__ void consumer_loop(const KernelParams &p, Cons &c)
 }
 
 // ------------------------------------------------------------------ producer
-// Lane 0 takes tickets, waits (bounded) for free stages and issues the weight
-// boxes; lanes 0..gcnt-1 then copy the group's activation rows (x rows for a
-// gate/up part, h rows for a down part) into the same stage.  A down part's h
-// rows exist only once the group's 16-row gate/up tickets are all finished:
-// lane 0 waits (bounded) for that count before the first part of the ticket.
+// Ticket order.  With n groups, TA gate/up tickets and nHt down tickets per
+// group, and a lookahead of L = min(2, n) groups, the sequence is
+//   A_0 .. A_{L-1}, then (A_j, B_{j-L}) for j = L .. n-1, then B_{n-L} .. B_{n-1}
+// (A_j = the TA gate/up tickets of group j, B_j = its nHt down tickets).  Every
+// gate/up ticket of a group precedes all its down tickets, which is all the
+// dependency waits need; the lookahead lets a group's h rows be ready (or
+// nearly) by the time its down stages reach the consumers.
+struct TicketInfo {
+    int isA, grp, tile;
+};
+
+__device__ __forceinline__ TicketInfo decode_ticket(int t, int n, int TA, int nB)
+{
+    const int L = n < 2 ? n : 2;
+    TicketInfo r;
+    if (t < L * TA) {
+        r.isA = 1; r.grp = t / TA; r.tile = t % TA;
+        return r;
+    }
+    int t2 = t - L * TA;
+    const int pairs = (n - L) * (TA + nB);
+    if (t2 < pairs) {
+        const int j = L + t2 / (TA + nB), q = t2 % (TA + nB);
+        if (q < TA) { r.isA = 1; r.grp = j; r.tile = q; }
+        else { r.isA = 0; r.grp = j - L; r.tile = q - TA; }
+        return r;
+    }
+    t2 -= pairs;
+    r.isA = 0; r.grp = n - L + t2 / nB; r.tile = t2 % nB;
+    return r;
+}
+
+// Lane 0 takes tickets, finds free stages and issues the weight boxes; the
+// lanes 0..gcnt-1 copy the group's activation rows into the same stage.  For a
+// gate/up part those are x rows, copied at once.  For a down part they are h
+// rows, which exist only once all 16-row gate/up tickets of the group are done:
+// the part is queued and its h rows are copied when the group's counter is
+// complete (polled, never waited on, while the producer keeps streaming
+// weights).  The stage's barrier expects both, so consumers see it complete
+// only with its h rows.
+struct Pending {
+    int head, tail;
+};
+
+__device__ __forceinline__ void issue_h(const KernelParams &p, uint8_t *smem, Tabs tb, int s, int grp, int part,
+                                        uint64_t pol, int lane)
+{
+    SmemHdr *hd = tb.hdr;
+    const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
+    if (lane < gcnt) {
+        uint8_t *dst = smem + s * p.stage_bytes + p.offH + lane * p.hpitch;
+        const uint16_t *src = p.hbuf + static_cast<size_t>(gbeg + lane) * p.I + static_cast<size_t>(part) * p.KB;
+        bulk_g2s(dst, src, 2u * p.KB, &hd->full[s], pol);
+    }
+}
+
+// Copy the h rows of every queued down part whose group is complete, oldest
+// first.  Returns false when the oldest entry has waited past the limit.
+__device__ __forceinline__ bool service_pending(const KernelParams &p, uint8_t *smem, Tabs tb, Pending &q,
+                                                uint64_t &since, uint64_t pol, int lane, volatile int *abort_flag)
+{
+    SmemHdr *hd = tb.hdr;
+    const uint32_t TA = static_cast<uint32_t>(p.I / 16);
+    while (q.head != q.tail) {
+        const int slot = q.head % kMaxStages;
+        const int grp = hd->pend_grp[slot];
+        int ready = 0;
+        if (lane == 0) {
+            ready = ld_acquire(p.doneA + grp) == TA ? 1 : 0;
+            // the h rows were written through the generic proxy; the bulk
+            // copies read them through the async proxy
+            if (ready) asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        if (!ready) {
+            if (since == 0) since = gtimer();
+            if (static_cast<long long>(gtimer() - since) > p.timeout_ns) {
+                if (lane == 0) raise_error(p, abort_flag, kErrTimeout);
+                return false;
+            }
+            return true;
+        }
+        __syncwarp();
+        issue_h(p, smem, tb, hd->pend_stage[slot], grp, hd->pend_part[slot], pol, lane);
+        ++q.head;
+        since = 0;
+    }
+    return true;
+}
+
 __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb,
                                               volatile int *abort_flag)
 {
@@ -748,44 +834,49 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
     const uint64_t pol = policy_evict_first();
     const int ng = hd->n_groups;
     const int TA = p.I / 16;
-    const int nA = ng * TA;
-    const int total = nA + ng * p.nHt;
+    const int total = ng * (TA + p.nHt);
     const uint32_t wbytesA = 32u * (p.KA / 2) + 32u * (p.KA / 16);
     const uint32_t wbytesB = kMB * (p.KB / 2) + kMB * (p.KB / 16);
+    Pending q{0, 0};
+    uint64_t since = 0;
+    bool ok = true;
     int s = 0;
     uint32_t ph = 0;
     int ticket = blockIdx.x;
-    while (ticket < total) {
-        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+    // wait for a free stage while servicing queued h copies; false on abort/timeout
+    auto acquire_stage = [&]() -> bool {
+        const uint64_t t0 = gtimer();
+        for (uint32_t it = 0;; ++it) {
+            int freed = 0;
+            if (lane == 0) freed = mbar_test(&hd->empty[s], ph ^ 1u) ? 1 : 0;
+            if (__shfl_sync(0xffffffffu, freed, 0)) return true;
+            if (!service_pending(p, smem, tb, q, since, pol, lane, abort_flag)) return false;
+            if ((it & 15u) == 15u) {
+                int bad = 0;
+                if (lane == 0) {
+                    bad = *abort_flag || (static_cast<long long>(gtimer() - t0) > p.timeout_ns);
+                    if (bad && !*abort_flag) raise_error(p, abort_flag, kErrTimeout);
+                }
+                if (__shfl_sync(0xffffffffu, bad, 0)) return false;
+            }
+        }
+    };
+    while (ok && ticket < total) {
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) {
+            ok = false;
+            break;
+        }
         int next = 0;
         if (lane == 0) next = static_cast<int>(gridDim.x + atomicAdd(p.ctrl, 1u));
-        const bool isA = ticket < nA;
-        const int tt = isA ? ticket : ticket - nA;
-        const int grp = isA ? tt / TA : tt / p.nHt;
-        const int tile = isA ? tt % TA : tt % p.nHt;
+        const TicketInfo ti = decode_ticket(ticket, ng, TA, p.nHt);
+        const bool isA = ti.isA != 0;
+        const int grp = ti.grp, tile = ti.tile;
         const int e = tb.gexp[grp], gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
         const int nparts = isA ? p.nPA : p.nPB;
-        // activation row of this lane's pair (x row for gate/up, h row for down)
-        const uint16_t *arow = nullptr;
-        if (lane < gcnt)
-            arow = isA ? p.x + static_cast<size_t>(tb.perm[gbeg + lane] / p.k) * p.H
-                       : p.hbuf + static_cast<size_t>(gbeg + lane) * p.I;
-        bool ok = true;
-        if (!isA) {
-            int got = 1;
-            if (lane == 0) {
-                got = wait_count(p.doneA + grp, static_cast<uint32_t>(TA), p, abort_flag) ? 1 : 0;
-                // the h rows were written through the generic proxy; the bulk
-                // copies below read them through the async proxy
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-            }
-            ok = __shfl_sync(0xffffffffu, got, 0) != 0;
-        }
-        for (int part = 0; ok && part < nparts; ++part) {
-            int got = 0;
-            if (lane == 0) got = wait_bar(&hd->empty[s], ph ^ 1u, p, abort_flag) ? 1 : 0;
-            got = __shfl_sync(0xffffffffu, got, 0);
-            if (!got) {
+        const uint16_t *xrow = nullptr;  // x row of this lane's pair (gate/up)
+        if (isA && lane < gcnt) xrow = p.x + static_cast<size_t>(tb.perm[gbeg + lane] / p.k) * p.H;
+        for (int part = 0; part < nparts; ++part) {
+            if (!acquire_stage()) {
                 ok = false;
                 break;
             }
@@ -830,12 +921,20 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
                     else
                         bulk_g2s(st + p.offDs, p.ds + static_cast<size_t>(row) * (p.I / 16), kMB * (p.I / 16), bar,
                                  pol);
+                    const int slot = q.tail % kMaxStages;
+                    hd->pend_stage[slot] = s;
+                    hd->pend_grp[slot] = grp;
+                    hd->pend_part[slot] = part;
                 }
             }
             __syncwarp();
-            if (arow) {
-                uint8_t *dst = st + (isA ? p.offX + lane * p.xpitch : p.offH + lane * p.hpitch);
-                bulk_g2s(dst, arow + static_cast<size_t>(part) * KP, 2u * KP, bar, pol);
+            if (xrow) bulk_g2s(st + p.offX + lane * p.xpitch, xrow + static_cast<size_t>(part) * KP, 2u * KP, bar, pol);
+            if (!isA) {
+                ++q.tail;
+                if (!service_pending(p, smem, tb, q, since, pol, lane, abort_flag)) {
+                    ok = false;
+                    break;
+                }
             }
             if (lane == 0) hd->fill_cnt += 1;
             if (++s == p.NS) {
@@ -844,19 +943,21 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
             }
         }
         ticket = __shfl_sync(0xffffffffu, next, 0);
-        if (!ok) {
-            if (lane == 0) *abort_flag = 1;
-            break;
-        }
+    }
+    // copy the h rows still queued (bounded)
+    while (ok && q.head != q.tail) {
+        if (!service_pending(p, smem, tb, q, since, pol, lane, abort_flag)) ok = false;
+        else if (q.head != q.tail) __nanosleep(128);
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) ok = false;
     }
     // end marker (the consumers' waits also end on the abort flag)
-    if (lane == 0) {
-        if (!*abort_flag && wait_bar(&hd->empty[s], ph ^ 1u, p, abort_flag)) {
+    if (ok && acquire_stage()) {
+        if (lane == 0) {
             hd->stage_hdr[s] = make_int4(KIND_END, 0, 0, 0);
             mbar_arrive(&hd->full[s]);
-        } else {
-            *abort_flag = 1;
         }
+    } else if (lane == 0) {
+        *abort_flag = 1;
     }
     __syncwarp();
 }
@@ -962,8 +1063,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
         if (*abort_flag) {
             // drain: wait (bounded) for the copies of every stage filled but not
             // yet seen complete, so no bulk copy lands after the CTA exits
+            const uint64_t t0 = gtimer();
             for (int i = hd->cons_cnt; i < hd->fill_cnt; ++i) {
-                const uint64_t t0 = gtimer();
                 while (!mbar_test(&hd->full[i % p.NS], static_cast<uint32_t>((i / p.NS) & 1))) {
                     if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) break;
                 }
