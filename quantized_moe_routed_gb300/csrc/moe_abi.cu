@@ -164,7 +164,7 @@ moe::SmemLayout layout_for(const moe_plan *pl, int T)
     const int red_need = 8192 * nt;
     const int scr_need = align16i(2 * P) + 8 * pl->d.E + 4 + 16;
     L.red_bytes = static_cast<int>(up(red_need > scr_need ? red_need : scr_need, 128));
-    L.tab_bytes = static_cast<int>(up(512 + 4 * align16i(2 * P) + align16i(P) + align16i(T), 128));
+    L.tab_bytes = static_cast<int>(up(1024 + 4 * align16i(2 * P) + align16i(P) + align16i(T), 128));
     L.stage_bytes = pl->stage_bytes_nt[nt];
     const int avail = pl->smem_optin - L.red_bytes - L.tab_bytes - 1024;
     int ns = avail / L.stage_bytes;

@@ -8,10 +8,11 @@
 
 namespace moe {
 
-// CTA shape of the persistent ticket kernel: 8 consumer warps + 1 producer warp.
+// CTA shape of the persistent ticket kernel: 8 consumer warps, 1 producer warp
+// (copy issue), 1 helper warp (cross-CTA counters, h-row copies, combine).
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;
+constexpr int kThreads = kConsumerThreads + 64;
 constexpr int kMaxPairs = 4096;     // T*k per launch (prefill is chunked to this)
 constexpr int kGroupPairs = 16;     // pairs per expert group, at most 2 MMA n-tiles of 8
 constexpr int kMaxTopK = 16;

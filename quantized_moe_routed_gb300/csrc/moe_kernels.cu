@@ -139,24 +139,6 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p)
     return v;
 }
 
-__device__ __forceinline__ uint4 ldg_nc16(const void *p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ uint4 ldg_cg16(const void *p)
-{
-    uint4 v;
-    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 __device__ __forceinline__ float ldg_cg_f32(const float *p)
 {
     float v;
@@ -168,6 +150,9 @@ __device__ __forceinline__ void consumer_sync()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
+
+__device__ __forceinline__ int vload(const int *a) { return *reinterpret_cast<const volatile int *>(a); }
+__device__ __forceinline__ void vstore(int *a, int v) { *reinterpret_cast<volatile int *>(a) = v; }
 
 // Four E2M1 pairs (one 32-bit word, element 2i in the low nibble of byte i)
 // -> four f16x2 {element 2i (low half), element 2i+1 (high half)}.
@@ -219,18 +204,26 @@ __device__ __forceinline__ uint32_t u4w(const uint4 &v, int i)
 }
 
 // ------------------------------------------------------------------ shared state
+constexpr int kDoneQ = 32;
+
+// CTA-shared control block.  Three single-writer queues connect the roles:
+//   tq  helper -> producer   next ticket (one fetched ahead)
+//   pq  producer -> helper   down parts whose h rows still have to be copied
+//   dq  consumers -> helper  finished tickets (counters to release, tokens to combine)
 struct SmemHdr {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     int4 stage_hdr[kMaxStages];  // {kind, group, tile, part}
     int n_groups, n_valid, n_bad, abort_flag;  // abort_flag: any role gave up (read by waits)
-    int n_comb, fill_cnt, cons_cnt, pad0;      // fills issued / fills seen complete
+    int fill_cnt, cons_cnt, cons_done, pad0;   // fills issued / fills seen complete / consumers finished
     int verdict[2];                            // consumer verdicts, alternating slots
-    int pad1[2];
-    int comb_tok[kGroupPairs];
-    int pend_stage[kMaxStages], pend_grp[kMaxStages], pend_part[kMaxStages];  // producer's queued h copies
+    int tq_head, tq_tail, tq_buf[2];
+    int pq_head, pq_tail, pad1[2];
+    int pq_stage[kMaxStages], pq_grp[kMaxStages], pq_part[kMaxStages];
+    int dq_head, dq_tail, pad2[2];
+    int dq_kind[kDoneQ], dq_grp[kDoneQ], dq_tile[kDoneQ];
 };
-static_assert(sizeof(SmemHdr) <= 512, "header too large");
+static_assert(sizeof(SmemHdr) <= 1024, "header too large");
 
 enum { KIND_A = 0, KIND_B = 1, KIND_END = 2 };
 
@@ -251,7 +244,7 @@ __device__ Tabs make_tabs(uint8_t *smem, int tab_off, int P)
     Tabs t;
     uint8_t *b = smem + tab_off;
     t.hdr = reinterpret_cast<SmemHdr *>(b);
-    int o = 512;
+    int o = 1024;
     t.perm = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
     t.pos = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
     t.gexp = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
@@ -352,28 +345,6 @@ __device__ bool wait_bar(uint64_t *bar, uint32_t parity, const KernelParams &p, 
                 return false;
             }
             if ((it & 1023u) == 0 && (ld_relaxed(p.ctrl + 2) & kErrTimeout)) {
-                *abort_flag = 1;
-                return false;
-            }
-        }
-    }
-}
-
-// Wait until *ctr == target (acquire); false on abort / timeout.
-__device__ bool wait_count(const uint32_t *ctr, uint32_t target, const KernelParams &p, volatile int *abort_flag)
-{
-    if (ld_acquire(ctr) == target) return true;
-    const uint64_t t0 = gtimer();
-    for (uint32_t it = 1;; ++it) {
-        __nanosleep(64);
-        if (ld_acquire(ctr) == target) return true;
-        if ((it & 15u) == 0) {
-            if (*abort_flag) return false;
-            if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
-                raise_error(p, abort_flag, kErrTimeout);
-                return false;
-            }
-            if (ld_relaxed(p.ctrl + 2) & kErrTimeout) {
                 *abort_flag = 1;
                 return false;
             }
@@ -500,6 +471,33 @@ __device__ __forceinline__ bool publish_verdict(Cons &c, bool ok_in_thread0)
     return ok;
 }
 
+// Consumer thread 0 hands a finished ticket to the helper warp (bounded wait
+// for queue space).  The consumers' global stores of the ticket precede this
+// through the barrier the caller passed; the helper releases them at gpu scope.
+__device__ __forceinline__ void cons_push_done(const KernelParams &p, Cons &c, int kind, int grp, int tile)
+{
+    if (c.tid != 0) return;
+    SmemHdr *hd = c.tb.hdr;
+    const int tail = hd->dq_tail;  // only this thread writes it
+    if (tail - vload(&hd->dq_head) >= kDoneQ) {
+        const uint64_t t0 = gtimer();
+        while (tail - vload(&hd->dq_head) >= kDoneQ) {
+            if (*c.abort_flag) return;
+            if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
+                raise_error(p, c.abort_flag, kErrTimeout);
+                return;
+            }
+            __nanosleep(64);
+        }
+    }
+    const int slot = tail % kDoneQ;
+    hd->dq_kind[slot] = kind;
+    hd->dq_grp[slot] = grp;
+    hd->dq_tile[slot] = tile;
+    __threadfence_block();
+    vstore(&hd->dq_tail, tail + 1);
+}
+
 __device__ __forceinline__ void cons_release_stage(const KernelParams &p, Cons &c)
 {
     __syncwarp();
@@ -619,13 +617,8 @@ __device__ __forceinline__ bool ticket_A(const KernelParams &p, Cons &c, int grp
         }
     }
     if (range_bad) atomicOr(p.ctrl + 2, kErrRange);
-    // h is read back through the async proxy (bulk copies) by other CTAs
-    asm volatile("fence.proxy.async.global;" ::: "memory");
     consumer_sync();
-    if (c.tid == 0) {
-        __threadfence();
-        atomicAdd(p.doneA + grp, 1u);
-    }
+    cons_push_done(p, c, KIND_A, grp, tile);
     return true;
 }
 
@@ -677,7 +670,6 @@ __device__ __forceinline__ bool ticket_B(const KernelParams &p, Cons &c, int grp
         for (int nt = 0; nt < NT; ++nt)
             c.red[((ks * 4 + mg * 2 + mt) * NT + nt) * 32 + c.lane] =
                 make_float4(acc[mt][nt][0], acc[mt][nt][1], acc[mt][nt][2], acc[mt][nt][3]);
-    if (c.tid == 0) c.tb.hdr->n_comb = 0;
     consumer_sync();
     const float tsd = p.dts[e];
     const float *redf = reinterpret_cast<const float *>(c.red);
@@ -694,33 +686,7 @@ __device__ __forceinline__ bool ticket_B(const KernelParams &p, Cons &c, int grp
         }
     }
     consumer_sync();
-    // count arrivals per (token, tile); the last arriver combines that token
-    if (c.tid < gcnt) {
-        const int pr = c.tb.perm[gbeg + c.tid];
-        const int tok = pr / p.k;
-        uint32_t *ctr = p.cnt + static_cast<size_t>(tok) * p.nHt + tile;
-        __threadfence();
-        const uint32_t old = atomicAdd(ctr, 1u);
-        if (old + 1u == static_cast<uint32_t>(c.tb.kvalid[tok])) {
-            *ctr = 0u;  // last arrival: reset for the next launch
-            __threadfence();
-            const int slot = atomicAdd(&c.tb.hdr->n_comb, 1);
-            c.tb.hdr->comb_tok[slot] = tok;
-        }
-    }
-    consumer_sync();
-    const int ncomb = c.tb.hdr->n_comb;
-    for (int idx = c.tid; idx < ncomb * kMB; idx += kConsumerThreads) {
-        const int tok = c.tb.hdr->comb_tok[idx / kMB];
-        const int row = idx % kMB;
-        float yv = 0.f;
-        for (int j = 0; j < p.k; ++j) {
-            const int ps = c.tb.pos[tok * p.k + j];
-            if (ps != 0xFFFF) yv += p.w[tok * p.k + j] * ldg_cg_f32(p.part + static_cast<size_t>(ps) * p.H + h0 + row);
-        }
-        p.y[static_cast<size_t>(tok) * p.H + h0 + row] = yv;
-    }
-    consumer_sync();
+    cons_push_done(p, c, KIND_B, grp, tile);
     return true;
 }
 
@@ -733,6 +699,7 @@ __device__ __forceinline__ void consumer_loop(const KernelParams &p, Cons &c)
         const bool ok = (h.x == KIND_A) ? ticket_A<NT, NULLM>(p, c, h.y, h.z) : ticket_B<NT, NULLM>(p, c, h.y, h.z);
         if (!ok) break;  // uniform: decided from a flag published before a barrier
     }
+    if (c.tid == 0) vstore(&c.tb.hdr->cons_done, 1);
 }
 
 // ------------------------------------------------------------------ producer
@@ -768,64 +735,12 @@ __device__ __forceinline__ TicketInfo decode_ticket(int t, int n, int TA, int nB
     return r;
 }
 
-// Lane 0 takes tickets, finds free stages and issues the weight boxes; the
-// lanes 0..gcnt-1 copy the group's activation rows into the same stage.  For a
-// gate/up part those are x rows, copied at once.  For a down part they are h
-// rows, which exist only once all 16-row gate/up tickets of the group are done:
-// the part is queued and its h rows are copied when the group's counter is
-// complete (polled, never waited on, while the producer keeps streaming
-// weights).  The stage's barrier expects both, so consumers see it complete
-// only with its h rows.
-struct Pending {
-    int head, tail;
-};
-
-__device__ __forceinline__ void issue_h(const KernelParams &p, uint8_t *smem, Tabs tb, int s, int grp, int part,
-                                        uint64_t pol, int lane)
-{
-    SmemHdr *hd = tb.hdr;
-    const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
-    if (lane < gcnt) {
-        uint8_t *dst = smem + s * p.stage_bytes + p.offH + lane * p.hpitch;
-        const uint16_t *src = p.hbuf + static_cast<size_t>(gbeg + lane) * p.I + static_cast<size_t>(part) * p.KB;
-        bulk_g2s(dst, src, 2u * p.KB, &hd->full[s], pol);
-    }
-}
-
-// Copy the h rows of every queued down part whose group is complete, oldest
-// first.  Returns false when the oldest entry has waited past the limit.
-__device__ __forceinline__ bool service_pending(const KernelParams &p, uint8_t *smem, Tabs tb, Pending &q,
-                                                uint64_t &since, uint64_t pol, int lane, volatile int *abort_flag)
-{
-    SmemHdr *hd = tb.hdr;
-    const uint32_t TA = static_cast<uint32_t>(p.I / 16);
-    while (q.head != q.tail) {
-        const int slot = q.head % kMaxStages;
-        const int grp = hd->pend_grp[slot];
-        int ready = 0;
-        if (lane == 0) {
-            ready = ld_acquire(p.doneA + grp) == TA ? 1 : 0;
-            // the h rows were written through the generic proxy; the bulk
-            // copies read them through the async proxy
-            if (ready) asm volatile("fence.proxy.async.global;" ::: "memory");
-        }
-        ready = __shfl_sync(0xffffffffu, ready, 0);
-        if (!ready) {
-            if (since == 0) since = gtimer();
-            if (static_cast<long long>(gtimer() - since) > p.timeout_ns) {
-                if (lane == 0) raise_error(p, abort_flag, kErrTimeout);
-                return false;
-            }
-            return true;
-        }
-        __syncwarp();
-        issue_h(p, smem, tb, hd->pend_stage[slot], grp, hd->pend_part[slot], pol, lane);
-        ++q.head;
-        since = 0;
-    }
-    return true;
-}
-
+// Lane 0 of the producer warp finds free stages and issues the weight boxes;
+// lanes 0..gcnt-1 copy a gate/up part's x rows into the same stage.  A down
+// part's h rows exist only once all 16-row gate/up tickets of its group are
+// done, so the part goes to the helper's queue and the helper copies them;
+// the stage's barrier expects both.  The producer never waits on global
+// memory: its next ticket comes from the helper too.
 __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb,
                                               volatile int *abort_flag)
 {
@@ -837,37 +752,31 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
     const int total = ng * (TA + p.nHt);
     const uint32_t wbytesA = 32u * (p.KA / 2) + 32u * (p.KA / 16);
     const uint32_t wbytesB = kMB * (p.KB / 2) + kMB * (p.KB / 16);
-    Pending q{0, 0};
-    uint64_t since = 0;
     bool ok = true;
     int s = 0;
     uint32_t ph = 0;
     int ticket = blockIdx.x;
-    // wait for a free stage while servicing queued h copies; false on abort/timeout
-    auto acquire_stage = [&]() -> bool {
-        const uint64_t t0 = gtimer();
-        for (uint32_t it = 0;; ++it) {
-            int freed = 0;
-            if (lane == 0) freed = mbar_test(&hd->empty[s], ph ^ 1u) ? 1 : 0;
-            if (__shfl_sync(0xffffffffu, freed, 0)) return true;
-            if (!service_pending(p, smem, tb, q, since, pol, lane, abort_flag)) return false;
-            if ((it & 15u) == 15u) {
-                int bad = 0;
-                if (lane == 0) {
-                    bad = *abort_flag || (static_cast<long long>(gtimer() - t0) > p.timeout_ns);
-                    if (bad && !*abort_flag) raise_error(p, abort_flag, kErrTimeout);
+    // a bounded wait for a condition polled by lane 0; false on abort/timeout
+    auto lane0_wait = [&](auto &&cond) -> bool {
+        int got = 0;
+        if (lane == 0) {
+            const uint64_t t0 = gtimer();
+            for (uint32_t it = 0;; ++it) {
+                if (cond()) { got = 1; break; }
+                if ((it & 15u) == 15u) {
+                    if (*abort_flag) break;
+                    if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
+                        raise_error(p, abort_flag, kErrTimeout);
+                        break;
+                    }
                 }
-                if (__shfl_sync(0xffffffffu, bad, 0)) return false;
             }
         }
+        return __shfl_sync(0xffffffffu, got, 0) != 0;
     };
-    while (ok && ticket < total) {
-        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) {
-            ok = false;
-            break;
-        }
-        int next = 0;
-        if (lane == 0) next = static_cast<int>(gridDim.x + atomicAdd(p.ctrl, 1u));
+    int tq_head = 0;
+    while (ok) {
+        if (ticket >= total) break;
         const TicketInfo ti = decode_ticket(ticket, ng, TA, p.nHt);
         const bool isA = ti.isA != 0;
         const int grp = ti.grp, tile = ti.tile;
@@ -876,7 +785,7 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
         const uint16_t *xrow = nullptr;  // x row of this lane's pair (gate/up)
         if (isA && lane < gcnt) xrow = p.x + static_cast<size_t>(tb.perm[gbeg + lane] / p.k) * p.H;
         for (int part = 0; part < nparts; ++part) {
-            if (!acquire_stage()) {
+            if (!lane0_wait([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
                 ok = false;
                 break;
             }
@@ -921,37 +830,41 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
                     else
                         bulk_g2s(st + p.offDs, p.ds + static_cast<size_t>(row) * (p.I / 16), kMB * (p.I / 16), bar,
                                  pol);
-                    const int slot = q.tail % kMaxStages;
-                    hd->pend_stage[slot] = s;
-                    hd->pend_grp[slot] = grp;
-                    hd->pend_part[slot] = part;
+                    // the h rows: queued for the helper (at most one entry per stage in flight)
+                    const int tail = hd->pq_tail;
+                    const int slot = tail % kMaxStages;
+                    hd->pq_stage[slot] = s;
+                    hd->pq_grp[slot] = grp;
+                    hd->pq_part[slot] = part;
+                    __threadfence_block();
+                    vstore(&hd->pq_tail, tail + 1);
                 }
+                hd->fill_cnt += 1;
             }
             __syncwarp();
             if (xrow) bulk_g2s(st + p.offX + lane * p.xpitch, xrow + static_cast<size_t>(part) * KP, 2u * KP, bar, pol);
-            if (!isA) {
-                ++q.tail;
-                if (!service_pending(p, smem, tb, q, since, pol, lane, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-            }
-            if (lane == 0) hd->fill_cnt += 1;
             if (++s == p.NS) {
                 s = 0;
                 ph ^= 1u;
             }
         }
-        ticket = __shfl_sync(0xffffffffu, next, 0);
-    }
-    // copy the h rows still queued (bounded)
-    while (ok && q.head != q.tail) {
-        if (!service_pending(p, smem, tb, q, since, pol, lane, abort_flag)) ok = false;
-        else if (q.head != q.tail) __nanosleep(128);
-        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) ok = false;
+        if (!ok) break;
+        // next ticket from the helper
+        if (!lane0_wait([&] { return vload(&hd->tq_tail) > tq_head; })) {
+            ok = false;
+            break;
+        }
+        int t = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            t = hd->tq_buf[tq_head & 1];
+            vstore(&hd->tq_head, tq_head + 1);
+        }
+        ++tq_head;
+        ticket = __shfl_sync(0xffffffffu, t, 0);
     }
     // end marker (the consumers' waits also end on the abort flag)
-    if (ok && acquire_stage()) {
+    if (ok && lane0_wait([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
         if (lane == 0) {
             hd->stage_hdr[s] = make_int4(KIND_END, 0, 0, 0);
             mbar_arrive(&hd->full[s]);
@@ -960,6 +873,137 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
         *abort_flag = 1;
     }
     __syncwarp();
+}
+
+// ------------------------------------------------------------------ helper warp
+// Everything that waits on or publishes to other CTAs runs here, so that
+// neither the producer's copy issue nor the consumers' math ever stalls on a
+// global round trip:
+//   * fetch the next ticket from the global counter (one ahead);
+//   * copy queued down parts' h rows once the group's gate/up counter is full
+//     (acquire, then an async-proxy fence: the rows were written through the
+//     generic proxy and are read by bulk copies);
+//   * release finished work: a gpu-scope fence, then bump the group's gate/up
+//     counter (gate/up ticket) or the per-(token, 64-row tile) arrival counters
+//     (down ticket); the CTA that completes a token's tile sums its k per-pair
+//     outputs in slot order and writes y -- no floating-point atomics, so the
+//     result is the same bits every run.
+__device__ __forceinline__ void helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, volatile int *abort_flag)
+{
+    const int lane = threadIdx.x & 31;
+    SmemHdr *hd = tb.hdr;
+    const uint64_t pol = policy_evict_first();
+    const int ng = hd->n_groups;
+    const uint32_t TA = static_cast<uint32_t>(p.I / 16);
+    const int total = ng * (static_cast<int>(TA) + p.nHt);
+    bool tick_done = false;
+    int tq_tail = 0, pq_head = 0, dq_head = 0;
+    uint64_t idle_since = 0;
+    for (;;) {
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        bool progress = false;
+        // 1) keep one ticket ready for the producer
+        if (!tick_done && tq_tail - vload(&hd->tq_head) < 1) {
+            int t = 0;
+            if (lane == 0) {
+                t = static_cast<int>(gridDim.x + atomicAdd(p.ctrl, 1u));
+                hd->tq_buf[tq_tail & 1] = t;
+                __threadfence_block();
+                vstore(&hd->tq_tail, tq_tail + 1);
+            }
+            ++tq_tail;
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (t >= total) tick_done = true;
+            progress = true;
+        }
+        // 2) h rows of queued down parts whose group is complete
+        while (pq_head != vload(&hd->pq_tail)) {
+            __threadfence_block();
+            const int slot = pq_head % kMaxStages;
+            const int grp = hd->pq_grp[slot];
+            int ready = 0;
+            if (lane == 0) ready = ld_acquire(p.doneA + grp) == TA ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, ready, 0)) break;
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            const int st = hd->pq_stage[slot], part = hd->pq_part[slot];
+            const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
+            if (lane < gcnt) {
+                uint8_t *dst = smem + st * p.stage_bytes + p.offH + lane * p.hpitch;
+                const uint16_t *src =
+                    p.hbuf + static_cast<size_t>(gbeg + lane) * p.I + static_cast<size_t>(part) * p.KB;
+                bulk_g2s(dst, src, 2u * p.KB, &hd->full[st], pol);
+            }
+            ++pq_head;
+            __syncwarp();
+            if (lane == 0) vstore(&hd->pq_head, pq_head);
+            progress = true;
+        }
+        // 3) release finished tickets
+        const int dq_tail = vload(&hd->dq_tail);
+        if (dq_head != dq_tail) {
+            __threadfence_block();
+            __threadfence();  // the consumers' h / partial stores become visible first (cumulative)
+            for (; dq_head != dq_tail; ++dq_head) {
+                const int slot = dq_head % kDoneQ;
+                const int kind = hd->dq_kind[slot], grp = hd->dq_grp[slot], tile = hd->dq_tile[slot];
+                if (kind == KIND_A) {
+                    if (lane == 0) atomicAdd(p.doneA + grp, 1u);
+                    continue;
+                }
+                const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
+                int tok = -1;
+                bool last = false;
+                if (lane < gcnt) {
+                    tok = tb.perm[gbeg + lane] / p.k;
+                    uint32_t *ctr = p.cnt + static_cast<size_t>(tok) * p.nHt + tile;
+                    const uint32_t old = atomicAdd(ctr, 1u);
+                    last = old + 1u == static_cast<uint32_t>(tb.kvalid[tok]);
+                    if (last) *ctr = 0u;  // last arrival: reset for the next launch
+                }
+                uint32_t mask = __ballot_sync(0xffffffffu, last);
+                if (mask) {
+                    __threadfence();  // see the other CTAs' per-pair outputs
+                    const int h0 = tile * kMB;
+                    while (mask) {
+                        const int src = __ffs(mask) - 1;
+                        mask &= mask - 1;
+                        const int t2 = __shfl_sync(0xffffffffu, tok, src);
+                        for (int row = lane; row < kMB; row += 32) {
+                            float yv = 0.f;
+                            for (int j = 0; j < p.k; ++j) {
+                                const int ps = tb.pos[t2 * p.k + j];
+                                if (ps != 0xFFFF)
+                                    yv += p.w[t2 * p.k + j] *
+                                          ldg_cg_f32(p.part + static_cast<size_t>(ps) * p.H + h0 + row);
+                            }
+                            p.y[static_cast<size_t>(t2) * p.H + h0 + row] = yv;
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) vstore(&hd->dq_head, dq_head);
+            progress = true;
+        }
+        // 4) done when the consumers are, with nothing left queued
+        if (vload(&hd->cons_done) && dq_head == vload(&hd->dq_tail) && pq_head == vload(&hd->pq_tail)) break;
+        // 5) bounded idleness
+        if (progress) {
+            idle_since = 0;
+        } else {
+            int bad = 0;
+            if (lane == 0) {
+                const uint64_t now = gtimer();
+                if (idle_since == 0) idle_since = now;
+                else if (static_cast<long long>(now - idle_since) > p.timeout_ns) {
+                    raise_error(p, abort_flag, kErrTimeout);
+                    bad = 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, bad, 0)) break;
+            __nanosleep(32);
+        }
+    }
 }
 
 // ------------------------------------------------------------------ the persistent step kernel
@@ -987,6 +1031,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
         hd->abort_flag = 0;
         hd->fill_cnt = 0;
         hd->cons_cnt = 0;
+        hd->cons_done = 0;
+        hd->tq_head = hd->tq_tail = 0;
+        hd->pq_head = hd->pq_tail = 0;
+        hd->dq_head = hd->dq_tail = 0;
         hd->verdict[0] = hd->verdict[1] = 1;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1038,7 +1086,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
         __syncthreads();
     }
 
-    if (tid >= kConsumerThreads) {
+    if (tid >= kConsumerThreads + 32) {
+        helper_loop(p, smem, tb, abort_flag);
+    } else if (tid >= kConsumerThreads) {
         producer_loop(p, smem, tb, abort_flag);
     } else {
         Cons c;
