@@ -140,6 +140,30 @@ moe_status_t moe_group(moe_plan_t plan, const int32_t *ids_dev, int T, void *ws_
 moe_status_t moe_decode(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
                         float *y_dev, int T, void *ws_dev, void *stream);
 
+/* moe_decode without a caller-supplied workspace, for callers that cannot
+ * allocate one: a host runtime whose device memory is fully reserved by its
+ * own pool, or code being captured into a CUDA graph where cudaMalloc is not
+ * allowed.  The pages have no counterpart: their kernels always take scratch
+ * from the caller.
+ * Same x_dev, ids_dev, w_dev, y_dev, T and stream as moe_decode
+ * (0 <= T <= min(24, T_max)).  The scratch is one library-owned buffer per
+ * device of 16 MiB in this library's global memory; a call needs
+ * 256 + 16384 + 4*T*(H/64) + 2*T*top_k*I + 4*T*top_k*H bytes (each piece
+ * rounded up to 256) and is refused with MOE_ERR_UNSUPPORTED_SHAPE when that
+ * exceeds 16 MiB.  Nothing is allocated or freed: each call zeroes the
+ * scratch's control block and counters (one memset on `stream`) and launches
+ * the decode kernel on it.
+ * The first call on each device does the set-up (it looks up the scratch's
+ * device address, which may load the module); make that first call before
+ * any stream capture.  Every call on a device shares the one buffer, so calls
+ * that overlap in time (other streams, other threads, other plans on the
+ * same device) race and corrupt each other: order them on one stream.
+ * check == 0: asynchronous, no synchronisation.  check != 0: synchronise
+ * `stream` after the launch and return the device error status (MOE_OK,
+ * MOE_ERR_TIMEOUT, MOE_ERR_BAD_EXPERT_ID or MOE_ERR_RANGE, as moe_check). */
+moe_status_t moe_decode_static(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
+                               float *y_dev, int T, int check, void *stream);
+
 /* The same step for 1 <= T <= T_max (prefill chunks), same arguments.  Runs
  * the persistent ticket kernel over chunks of at most 4096 / top_k tokens. */
 moe_status_t moe_prefill(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,

@@ -48,6 +48,7 @@ SIGNATURES = {
     "moe_workspace_init": (_I, [_P, _P, _S, _P]),
     "moe_group": (_I, [_P, _P, _I, _P, _P, _P, _P, _P]),
     "moe_decode": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
+    "moe_decode_static": (_I, [_P, _P, _P, _P, _P, _I, _I, _P]),
     "moe_prefill": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
     "moe_null_step": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
     "moe_check": (_I, [_P, _P, _P]),
@@ -159,6 +160,18 @@ def _step(fn, plan, x, ids, w, y, ws, stream):
 
 def moe_decode(plan, x, ids, w, y, ws, stream=None):
     _step(load_library().moe_decode, plan, x, ids, w, y, ws, stream)
+
+
+def moe_decode_static(plan, x, ids, w, y, check: bool = False, stream=None):
+    """moe_decode on the library's own per-device scratch (no workspace
+    argument, nothing allocated).  check=True synchronises and raises on a
+    device-recorded error."""
+    _need(x, torch.bfloat16, "x")
+    _need(ids, torch.int32, "ids")
+    _need(w, torch.float32, "w")
+    _need(y, torch.float32, "y")
+    _check(load_library().moe_decode_static(plan, _ptr(x), _ptr(ids), _ptr(w), _ptr(y), x.shape[0], int(check),
+                                            _stream(stream)))
 
 
 def moe_prefill(plan, x, ids, w, y, ws, stream=None):

@@ -194,8 +194,13 @@ void reject(moe_plan *pl)
 
 enum class Path { Decode, Prefill, Null };
 
+// Byte offsets of the workspace pieces from the workspace base.
+struct WsOffsets {
+    size_t off_done, off_cnt, off_h, off_part, total;
+};
+
 moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, int T, void *ws,
-                      void *stream, Path path)
+                      void *stream, Path path, const WsOffsets *wo = nullptr)
 {
     if (!pl) return fail(MOE_ERR_INVALID_ARG, "null plan");
     if (T < 0 || T > pl->d.T_max) {
@@ -247,10 +252,10 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
     p.uts = pl->d.up_ts_dev;
     p.dts = pl->d.down_ts_dev;
     p.ctrl = reinterpret_cast<uint32_t *>(wsb);
-    p.doneA = reinterpret_cast<uint32_t *>(wsb + pl->off_done);
-    p.cnt = reinterpret_cast<uint32_t *>(wsb + pl->off_cnt);
-    p.hbuf = reinterpret_cast<uint16_t *>(wsb + pl->off_h);
-    p.part = reinterpret_cast<float *>(wsb + pl->off_part);
+    p.doneA = reinterpret_cast<uint32_t *>(wsb + (wo ? wo->off_done : pl->off_done));
+    p.cnt = reinterpret_cast<uint32_t *>(wsb + (wo ? wo->off_cnt : pl->off_cnt));
+    p.hbuf = reinterpret_cast<uint16_t *>(wsb + (wo ? wo->off_h : pl->off_h));
+    p.part = reinterpret_cast<float *>(wsb + (wo ? wo->off_part : pl->off_part));
     p.H = pl->d.H;
     p.I = pl->d.I;
     p.E = pl->d.E;
@@ -322,6 +327,55 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
                          pl->num_sms, pl->stage_bytes);
         });
     return MOE_OK;
+}
+
+// ---- library-owned scratch for moe_decode_static
+//
+// Some callers cannot hand the library a workspace: a host runtime whose
+// device memory is entirely reserved by its own pool, or code being captured
+// into a CUDA graph where a fresh cudaMalloc is not allowed.  For them the
+// decode path can run on this fixed per-device buffer instead.  It lives in
+// this module's global memory (no cudaMalloc, no cudaFree, no allocation of
+// any kind per call), so its size is a compile-time maximum.
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_ptr[kMaxDevices] = {};
+
+// Set-up, once per device, with that device current: the device address of
+// the scratch (the first query may load this module onto the device, which
+// is why the first call should come before any stream capture).
+moe_status_t static_scratch(int dev, void **out)
+{
+    if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_INVALID_ARG, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        if (!ptr || !aligned(ptr, 256)) return fail(MOE_ERR_CUDA, "static scratch has no usable device address");
+        g_static_ptr[dev] = ptr;
+    }
+    *out = g_static_ptr[dev];
+    return MOE_OK;
+}
+
+// The workspace pieces for a decode call of T tokens, packed for T (the
+// plan's own layout is sized for T_max tokens).  The control block, the
+// gate/up completion counters and the tile arrival counters come first, so
+// the bytes that must start at zero are [0, off_h).
+WsOffsets static_layout(const moe_plan *pl, int T)
+{
+    WsOffsets o{};
+    const size_t P = static_cast<size_t>(T) * pl->d.top_k;
+    o.off_done = moe::kCtrlBytes;
+    o.off_cnt = up(o.off_done + 4 * static_cast<size_t>(moe::kMaxPairs), 256);
+    o.off_h = up(o.off_cnt + 4 * static_cast<size_t>(T) * pl->nHt, 256);
+    o.off_part = up(o.off_h + 2 * P * pl->d.I, 256);
+    o.total = up(o.off_part + 4 * P * pl->d.H, 256);
+    return o;
 }
 
 }  // namespace
@@ -553,6 +607,55 @@ moe_status_t moe_decode(moe_plan_t plan, const void *x_dev, const int32_t *ids_d
                         float *y_dev, int T, void *ws_dev, void *stream)
 {
     return run_step(plan, x_dev, ids_dev, w_dev, y_dev, T, ws_dev, stream, Path::Decode);
+}
+
+moe_status_t moe_decode_static(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
+                               float *y_dev, int T, int check, void *stream)
+{
+    if (!plan) return fail(MOE_ERR_INVALID_ARG, "null plan");
+    if (T < 0 || T > moe::kDecodeMaxT || T > plan->d.T_max) {
+        reject(plan);
+        return fail(MOE_ERR_INVALID_ARG, "moe_decode_static takes 0 <= T <= min(%d, T_max=%d), got %d",
+                    moe::kDecodeMaxT, plan->d.T_max, T);
+    }
+    if (T == 0) return MOE_OK;
+    moe_status_t st = check_device(plan);
+    if (st != MOE_OK) {
+        reject(plan);
+        return st;
+    }
+    const WsOffsets wo = static_layout(plan, T);
+    if (wo.total > kStaticScratchBytes) {
+        reject(plan);
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE,
+                    "T=%d, top_k=%d, H=%d, I=%d need %zu bytes of scratch; the static scratch holds %zu", T,
+                    plan->d.top_k, plan->d.H, plan->d.I, wo.total, kStaticScratchBytes);
+    }
+    void *scr = nullptr;
+    st = static_scratch(plan->device, &scr);
+    if (st != MOE_OK) {
+        reject(plan);
+        return st;
+    }
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // the control block and the counters must start at zero
+    cudaError_t e = cudaMemsetAsync(scr, 0, wo.off_h, cs);
+    if (e != cudaSuccess) {
+        reject(plan);
+        return fail(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+    }
+    st = run_step(plan, x_dev, ids_dev, w_dev, y_dev, T, scr, stream, Path::Decode, &wo);
+    if (st != MOE_OK || !check) return st;
+    // check: wait for the step and report what the device recorded
+    uint32_t word = 0;
+    e = cudaStreamSynchronize(cs);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&word, static_cast<uint8_t *>(scr) + 8, 4, cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "moe_decode_static check: %s", cudaGetErrorString(e));
+    if (word & moe::kErrTimeout) return fail(MOE_ERR_TIMEOUT, "a device-side wait timed out");
+    if (word & moe::kErrBadId) return fail(MOE_ERR_BAD_EXPERT_ID, "an expert id >= E was seen and skipped");
+    if (word & moe::kErrRange) return fail(MOE_ERR_RANGE, "an fp16 intermediate (h) overflowed");
+    return MOE_OK;
 }
 
 moe_status_t moe_prefill(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
