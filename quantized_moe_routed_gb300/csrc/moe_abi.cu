@@ -51,9 +51,7 @@ struct moe_plan {
     int nib_mode = 0;
     int scale_tmaA = 0, spA = 0, shA = 0, mkA = 0, scale_tmaB = 0, spB = 0, shB = 0, mkB = 0;
     int offGq = 0, offUq = 0, offGs = 0, offUs = 0, offDq = 0, offDs = 0;
-    int offX = 0, xpitch = 0, offH = 0, hpitch = 0;
-    int stage_bytes_nt[3] = {0, 0, 0};  // stage bytes of the 1- and 2-n-tile variants
-    int stage_bytes = 0;                // of the 2-n-tile variant (the largest)
+    int stage_bytes = 0;  // one ring stage: the larger of a gate/up and a down part's weights
     CUtensorMap tm[6];
     int Tc = 0;  // tokens per launch chunk
     long long timeout_ns = 1000000000LL;
@@ -161,11 +159,11 @@ moe::SmemLayout layout_for(const moe_plan *pl, int T)
     moe::SmemLayout L{};
     const int P = T * pl->d.top_k;
     const int nt = ntiles_for(pl, T);
-    const int red_need = 8192 * nt;
+    const int red_need = 2 * 8192 * nt;  // two ticket-end reduction buffers
     const int scr_need = align16i(2 * P) + 8 * pl->d.E + 4 + 16;
     L.red_bytes = static_cast<int>(up(red_need > scr_need ? red_need : scr_need, 128));
-    L.tab_bytes = static_cast<int>(up(1024 + 4 * align16i(2 * P) + align16i(P) + align16i(T), 128));
-    L.stage_bytes = pl->stage_bytes_nt[nt];
+    L.tab_bytes = moe::tab_bytes_for(P, T);
+    L.stage_bytes = pl->stage_bytes;
     const int avail = pl->smem_optin - L.red_bytes - L.tab_bytes - 1024;
     int ns = avail / L.stage_bytes;
     if (ns > moe::kMaxStages) ns = moe::kMaxStages;
@@ -281,10 +279,6 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
     p.offUs = pl->offUs;
     p.offDq = pl->offDq;
     p.offDs = pl->offDs;
-    p.offX = pl->offX;
-    p.xpitch = pl->xpitch;
-    p.offH = pl->offH;
-    p.hpitch = pl->hpitch;
     p.timeout_ns = pl->timeout_ns;
     p.null_mode = path == Path::Null ? 1 : 0;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -471,24 +465,19 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
     pl->nPA = d.H / pl->KA;
     pl->nPB = d.I / pl->KB;
     pl->nHt = d.H / moe::kMB;
-    // stage layouts: weights (1024-aligned sub-buffers), then the group's
-    // activation rows at a pitch of 2*KP + 16 bytes
+    // stage layouts: weights only, in 1024-aligned sub-buffers (the
+    // activations are read from global memory by the consumers)
     pl->offGq = 0;
     pl->offUq = 8 * pl->KA;
     pl->offGs = 16 * pl->KA;
     pl->offUs = pl->offGs + up1024(16 * pl->spA);
-    pl->offX = pl->offUs + up1024(16 * pl->spA);
-    pl->xpitch = 2 * pl->KA + 16;
     pl->offDq = 0;
     pl->offDs = 32 * pl->KB;
-    pl->offH = pl->offDs + up1024(moe::kMB * pl->spB);
-    pl->hpitch = 2 * pl->KB + 16;
-    for (int nt = 1; nt <= 2; ++nt) {
-        const int stA = pl->offX + 8 * nt * pl->xpitch;
-        const int stB = pl->offH + 8 * nt * pl->hpitch;
-        pl->stage_bytes_nt[nt] = up1024(stA > stB ? stA : stB);
+    {
+        const int stA = pl->offUs + up1024(16 * pl->spA);
+        const int stB = pl->offDs + up1024(moe::kMB * pl->spB);
+        pl->stage_bytes = stA > stB ? stA : stB;
     }
-    pl->stage_bytes = pl->stage_bytes_nt[2];
     // tensor maps (host-only encoding; no device memory involved)
     if (!encoder()) {
         delete pl;

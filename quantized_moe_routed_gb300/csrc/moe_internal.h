@@ -9,7 +9,7 @@
 namespace moe {
 
 // CTA shape of the persistent ticket kernel: 8 consumer warps, 1 producer warp
-// (copy issue), 1 helper warp (cross-CTA counters, h-row copies, combine).
+// (weight copy issue), 1 helper warp (tickets, cross-CTA counters, combine).
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 64;
@@ -17,7 +17,7 @@ constexpr int kMaxPairs = 4096;     // T*k per launch (prefill is chunked to thi
 constexpr int kGroupPairs = 16;     // pairs per expert group, at most 2 MMA n-tiles of 8
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 16;
 constexpr int kDecodeMaxT = 24;     // the pages' m <= 24 decode bound
 constexpr int kMB = 64;             // down-projection rows per phase-B ticket
 
@@ -25,6 +25,16 @@ constexpr int kMB = 64;             // down-projection rows per phase-B ticket
 constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrBadId = 2u;
 constexpr uint32_t kErrRange = 4u;
+
+// Shared-memory tables of the step kernel: a 1024-byte control block, then
+// five uint16 arrays of P entries, two uint8 arrays of P and one of T, each
+// padded to 16 bytes; the whole rounded up to 128 bytes.
+constexpr int kTabHdrBytes = 1024;
+inline int tab_bytes_for(int P, int T)
+{
+    const int a2 = (2 * P + 15) & ~15, a1 = (P + 15) & ~15, aT = (T + 15) & ~15;
+    return (kTabHdrBytes + 5 * a2 + 2 * a1 + aT + 127) / 128 * 128;
+}
 
 // Workspace control block (first 256 bytes of the workspace).
 //   word 0: ticket counter   word 1: CTAs finished   word 2: error bits
@@ -48,7 +58,7 @@ struct KernelParams {
     uint32_t *ctrl;     // control block
     uint32_t *doneA;    // [kMaxPairs] per-group count of finished gate/up tickets
     uint32_t *cnt;      // [T * nHt] per (token, H-tile) arrivals
-    uint16_t *hbuf;     // [P, I] fp16 h, rows in sorted pair order
+    uint16_t *hbuf;     // [P, I] fp16 h, rows in sorted pair order, 128-element blocks permuted (see kernels)
     float *part;        // [P, H] fp32 per-pair down-projection outputs
     // shape
     int H, I, E, k, T;
@@ -60,9 +70,7 @@ struct KernelParams {
     int scale_tmaA, scale_tmaB;  // 1: scale rows by 2-D tensor map; 0: one 1-D bulk copy (natural layout)
     int spA, shA, mkA, spB, shB, mkB;  // scale smem row pitch, swizzle shift and mask
     int offGq, offUq, offGs, offUs;    // phase-A stage sub-buffers (bytes, 1024-aligned)
-    int offX, xpitch;                  // phase-A x slice: row n of the group at offX + n*xpitch
     int offDq, offDs;                  // phase-B stage sub-buffers
-    int offH, hpitch;                  // phase-B h slice
     int stage_bytes, NS;
     int red_off, red_bytes, tab_off;            // smem layout (bytes)
     int ntiles;                                 // kernel variant: n-tiles per group (1 or 2)

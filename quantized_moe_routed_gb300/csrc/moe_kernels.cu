@@ -13,36 +13,39 @@
 //    splitting an expert's pairs into groups of at most 8 or 16 pairs (one or
 //    two 8-wide MMA n-tiles, fixed per launch from T*k).
 //  * Tickets come from one atomic counter (the first one is the CTA index, so
-//    the first weight loads need no atomic).  Phase-A tickets (group, 16
-//    intermediate rows of gate and up) come first, then phase-B tickets
-//    (group, 64 rows of down).  Each CTA takes tickets in increasing order, so
-//    every phase-A ticket is held by a running CTA before any phase-B ticket
-//    is handed out: the per-group completion counter a phase-B ticket waits on
-//    is guaranteed to fill, and no grid barrier is needed (the pages' barrier
+//    the first weight loads need no atomic).  Gate/up tickets (group, 16
+//    intermediate rows of gate and up) all precede the down tickets (group,
+//    64 rows of down); each CTA takes tickets in increasing order, so every
+//    gate/up ticket is held by a running CTA before any down ticket is handed
+//    out: the per-group completion counter a down ticket waits on is
+//    guaranteed to fill, and no grid barrier is needed (the pages' barrier
 //    version F1 was correct but not faster, "LNA-CANON.md", "含めないもの").
-//  * A producer warp streams each ticket's packed E2M1 rows and E4M3 scale
-//    rows HBM -> shared memory with TMA tensor copies (cp.async.bulk.tensor:
-//    one box per projection and stage, L2 evict-first), plus the group's
-//    activation rows (x for gate/up, h for down) with bulk copies, into a ring
-//    of stages guarded by mbarriers.  Consumers read shared memory only.  Box
-//    shapes are chosen so the consumers' 16-byte weight reads are
-//    bank-conflict-free without padding.
-//  * Eight consumer warps dequantise in registers -- cvt e2m1x2 -> f16x2, times
-//    the block scale (E2M1 x E4M3 is exact in fp16) -- and run mma.sync
-//    m16n8k16 (fp16 operands, fp32 accumulate) with weight rows as M and the
-//    group's pairs as N.  Activations (x for gate/up, h for down) are the
-//    B operand; the K order inside each thread is permuted identically on both
-//    operands, so every thread reads 16 contiguous bytes of a weight row.
-//  * A down ticket's h rows exist once all 16-row gate/up tickets of its group
-//    are done: the producer waits (bounded) on the group's counter before it
-//    copies them, so the consumers never wait on global memory.
+//  * A producer warp streams only weights: each ticket part's packed E2M1 rows
+//    and E4M3 scale rows go HBM -> shared memory as a few large TMA tensor
+//    boxes (cp.async.bulk.tensor, L2 evict-first) into a ring of equal stages
+//    guarded by mbarriers.  Box shapes make the consumers' 16-byte weight
+//    reads bank-conflict-free without padding.
+//  * Eight consumer warps each walk the ring on their own (no CTA barrier per
+//    stage).  They dequantise in registers -- cvt e2m1x2 -> f16x2, times the
+//    block scale (E2M1 x E4M3 is exact in fp16) -- and run mma.sync m16n8k16
+//    (fp16 operands, fp32 accumulate) with weight rows as M and the group's
+//    pairs as N.  The activations (x for gate/up, h for down) are the
+//    B operand and come straight from global memory (L2): a warp starts the
+//    next stage's activation loads from the published stage header while it
+//    computes the current one.  The K order inside each thread is permuted
+//    identically on both operands, so every thread reads 16 contiguous bytes
+//    of a weight row.
+//  * A down ticket's h rows exist once all gate/up tickets of its group are
+//    done: the helper warp polls the group's counter and flags the group in
+//    shared memory; consumers never poll global memory.
 //  * h = SiLU(g) * u goes to a workspace buffer (fp16) after a fixed-order
-//    cross-warp reduction; down outputs go to per-pair fp32 partials; the last
-//    CTA to finish a (token, 64-row tile) sums its k partials in slot order.
-//    No floating-point atomics anywhere: results are bitwise reproducible.
+//    cross-warp reduction done by the last warp to finish the ticket; down
+//    outputs go to per-pair fp32 partials; the last CTA to finish a (token,
+//    64-row tile) sums its k partials in slot order.  No floating-point
+//    atomics anywhere: results are bitwise reproducible.
 //  * Every wait is bounded (globaltimer); a timeout sets the workspace error
-//    word and the CTA drains and returns.  The last CTA out resets the
-//    workspace counters, so a workspace needs zeroing only once.
+//    word and the CTA drains its copies and returns.  The last CTA out resets
+//    the workspace counters, so a workspace needs zeroing only once.
 #include "moe_internal.h"
 
 #include <cuda_fp16.h>
@@ -146,13 +149,40 @@ __device__ __forceinline__ float ldg_cg_f32(const float *p)
     return v;
 }
 
-__device__ __forceinline__ void consumer_sync()
+
+// CTA-scope acquire / release on shared memory: order this thread's later
+// (earlier) accesses after (before) the flag, without the full fence that
+// would also wait for this thread's unrelated global loads in flight.
+__device__ __forceinline__ int ld_acq_cta(const int *a)
 {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(a)) : "memory");
+    return v;
 }
 
-__device__ __forceinline__ int vload(const int *a) { return *reinterpret_cast<const volatile int *>(a); }
-__device__ __forceinline__ void vstore(int *a, int v) { *reinterpret_cast<volatile int *>(a) = v; }
+__device__ __forceinline__ void st_rel_cta(int *a, int v)
+{
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(a)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acq_cta_u8(const uint8_t *a)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u8 %0, [%1];" : "=r"(v) : "r"(smem_u32(a)) : "memory");
+    return static_cast<int>(v);
+}
+
+__device__ __forceinline__ void st_rel_cta_u8(uint8_t *a, int v)
+{
+    asm volatile("st.release.cta.shared::cta.u8 [%0], %1;" ::"r"(smem_u32(a)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int atom_add_acqrel_cta(int *a, int v)
+{
+    int old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(a)), "r"(v) : "memory");
+    return old;
+}
 
 // Four E2M1 pairs (one 32-bit word, element 2i in the low nibble of byte i)
 // -> four f16x2 {element 2i (low half), element 2i+1 (high half)}.
@@ -192,7 +222,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u)
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1)
 {
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
                  "{%0,%1,%2,%3};"
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -204,26 +234,27 @@ __device__ __forceinline__ uint32_t u4w(const uint4 &v, int i)
 }
 
 // ------------------------------------------------------------------ shared state
-constexpr int kDoneQ = 32;
+constexpr int kDoneQ = 16;  // finished tickets in flight from the consumers to the helper
+constexpr int kTq = 4;      // tickets fetched ahead (helper -> producer)
 
-// CTA-shared control block.  Three single-writer queues connect the roles:
-//   tq  helper -> producer   next ticket (one fetched ahead)
-//   pq  producer -> helper   down parts whose h rows still have to be copied
-//   dq  consumers -> helper  finished tickets (counters to release, tokens to combine)
+// CTA-shared control block.  The roles talk through single-writer fields:
+//   tq       helper -> producer     tickets fetched ahead
+//   hdr_seq  producer -> consumers  1 + the fill number whose header stage_hdr[s] holds
+//   red_*    consumers -> consumers the cross-warp reduction buffer's arrivals / release
+//   dq       consumers -> helper    finished tickets, slot = ticket sequence number % kDoneQ
 struct SmemHdr {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     int4 stage_hdr[kMaxStages];  // {kind, group, tile, part}
-    int n_groups, n_valid, n_bad, abort_flag;  // abort_flag: any role gave up (read by waits)
-    int fill_cnt, cons_cnt, cons_done, pad0;   // fills issued / fills seen complete / consumers finished
-    int verdict[2];                            // consumer verdicts, alternating slots
-    int tq_head, tq_tail, tq_buf[2];
-    int pq_head, pq_tail, pad1[2];
-    int pq_stage[kMaxStages], pq_grp[kMaxStages], pq_part[kMaxStages];
-    int dq_head, dq_tail, pad2[2];
-    int dq_kind[kDoneQ], dq_grp[kDoneQ], dq_tile[kDoneQ];
+    int hdr_seq[kMaxStages];
+    int n_groups, n_valid, n_bad, abort_flag;  // abort_flag: any role gave up (read by every wait)
+    uint64_t redbar[2];                        // ticket-end arrivals of the 8 consumer warps, per buffer
+    int fill_cnt, cons_exited, red_cnt, pad1;
+    int tq_head, tq_tail, dq_head, pad0;
+    int tq_buf[kTq];
+    int dq_seq[kDoneQ], dq_kind[kDoneQ], dq_grp[kDoneQ], dq_tile[kDoneQ];
 };
-static_assert(sizeof(SmemHdr) <= 1024, "header too large");
+static_assert(sizeof(SmemHdr) <= kTabHdrBytes, "header too large");
 
 enum { KIND_A = 0, KIND_B = 1, KIND_END = 2 };
 
@@ -233,7 +264,9 @@ struct Tabs {
     uint16_t *pos;    // [P] inverse: sorted position of pair p, 0xFFFF if invalid
     uint16_t *gexp;   // [P] group -> expert
     uint16_t *gbeg;   // [P] group -> first sorted position
-    uint8_t *gcnt;    // [P] group -> number of pairs (1..32)
+    uint16_t *stok;   // [P] sorted position -> token
+    uint8_t *gcnt;    // [P] group -> number of pairs (1..16)
+    uint8_t *hready;  // [P] group -> 0 unknown, 1 polled by the helper, 2 h rows complete
     uint8_t *kvalid;  // [T] valid slots per token
 };
 
@@ -244,12 +277,14 @@ __device__ Tabs make_tabs(uint8_t *smem, int tab_off, int P)
     Tabs t;
     uint8_t *b = smem + tab_off;
     t.hdr = reinterpret_cast<SmemHdr *>(b);
-    int o = 1024;
+    int o = kTabHdrBytes;
     t.perm = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
     t.pos = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
     t.gexp = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
     t.gbeg = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
+    t.stok = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
     t.gcnt = b + o; o += align16(P);
+    t.hready = b + o; o += align16(P);
     t.kvalid = b + o;
     return t;
 }
@@ -444,115 +479,251 @@ __device__ __forceinline__ void chunk_math(const uint4 (&ra)[MT], const uint4 (&
     }
 }
 
-// ------------------------------------------------------------------ consumer context
-struct Cons {
-    uint8_t *smem;
-    Tabs tb;
-    float4 *red;
-    int warp, lane, g, t, tid;
-    int s;          // ring stage
-    uint32_t ph;    // parity of the ring pass
-    uint32_t nv;    // verdicts published so far (same value in every consumer thread)
-    volatile int *abort_flag;
-};
-
-// Consumer thread 0 decides, every consumer thread gets the same answer.  The
-// slot alternates, so thread 0 cannot overwrite a verdict another thread has
-// not read yet: rewriting a slot needs the next verdict's barrier, which every
-// thread reaches only after its read.
-__device__ __forceinline__ bool publish_verdict(Cons &c, bool ok_in_thread0)
+// ------------------------------------------------------------------ activation operands
+// The B operand of one 128-element chunk comes straight from global memory,
+// not through the stage ring: pair n = nt*8 + g of the group, the 32 elements
+// this thread owns in the chunk, as four 16-byte pieces (piece v = elements
+// koff + 8v .. koff + 8v + 7).  Pairs past the group's end read as zero.
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *ptr)
 {
-    SmemHdr *hd = c.tb.hdr;
-    const int slot = static_cast<int>(c.nv & 1u);
-    if (c.tid == 0) hd->verdict[slot] = ok_in_thread0 ? 1 : 0;
-    consumer_sync();
-    const bool ok = hd->verdict[slot] != 0;
-    ++c.nv;
-    return ok;
+    uint4 v;
+    asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr));
+    return v;
 }
 
-// Consumer thread 0 hands a finished ticket to the helper warp (bounded wait
-// for queue space).  The consumers' global stores of the ticket precede this
-// through the barrier the caller passed; the helper releases them at gpu scope.
-__device__ __forceinline__ void cons_push_done(const KernelParams &p, Cons &c, int kind, int grp, int tile)
+__device__ __forceinline__ uint4 ldg_cg_v4(const void *ptr)
 {
-    if (c.tid != 0) return;
-    SmemHdr *hd = c.tb.hdr;
-    const int tail = hd->dq_tail;  // only this thread writes it
-    if (tail - vload(&hd->dq_head) >= kDoneQ) {
-        const uint64_t t0 = gtimer();
-        while (tail - vload(&hd->dq_head) >= kDoneQ) {
-            if (*c.abort_flag) return;
-            if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
-                raise_error(p, c.abort_flag, kErrTimeout);
-                return;
-            }
-            __nanosleep(64);
-        }
-    }
-    const int slot = tail % kDoneQ;
-    hd->dq_kind[slot] = kind;
-    hd->dq_grp[slot] = grp;
-    hd->dq_tile[slot] = tile;
-    __threadfence_block();
-    vstore(&hd->dq_tail, tail + 1);
+    uint4 v;
+    asm("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr));
+    return v;
 }
 
-__device__ __forceinline__ void cons_release_stage(const KernelParams &p, Cons &c)
-{
-    __syncwarp();
-    if (c.lane == 0) mbar_arrive(&c.tb.hdr->empty[c.s]);
-    if (++c.s == p.NS) {
-        c.s = 0;
-        c.ph ^= 1u;
-    }
-}
-
-// Wait for the next stage; returns its header (KIND_END on abort).  Consumer
-// thread 0 takes the bounded wait and publishes the verdict before a named
-// barrier, so all 256 consumer threads take the same branch; every thread then
-// observes the completed phase itself (acquire) before reading the stage.
-__device__ __forceinline__ int4 cons_next_stage(const KernelParams &p, Cons &c)
-{
-    SmemHdr *hd = c.tb.hdr;
-    bool ok = false;
-    if (c.tid == 0) {
-        ok = wait_bar(&hd->full[c.s], c.ph, p, c.abort_flag);
-        if (ok) hd->cons_cnt += 1;
-    }
-    if (!publish_verdict(c, ok)) return make_int4(KIND_END, 0, 0, 0);
-    for (int i = 0; i < 64 && !mbar_test(&hd->full[c.s], c.ph); ++i) {
-    }
-    return hd->stage_hdr[c.s];
-}
-
-// B operand of one chunk from the stage's activation slice: pair n of the
-// group (n = nt*8 + g) at row n of the slice, elements koff .. koff+31
-// (16 bytes per v).  Pairs past the group's end read as zero.
+// x (gate/up): the caller's bf16 rows, read-only for the whole step, through
+// the non-coherent path.  A thread's four pieces share sectors, so after the
+// first one the rest hit L1.
 template <int NT>
-__device__ __forceinline__ void load_bq_smem(uint4 (&bq)[NT][4], const uint8_t *slice, int pitch, int koff, int g,
-                                             int gcnt)
+__device__ __forceinline__ void load_x(uint4 (&b)[NT][4], const KernelParams &p, const Tabs &tb, int gbeg, int gcnt,
+                                       int kglob, int g)
 {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int n = nt * 8 + g;
         if (n < gcnt) {
-            const uint8_t *src = slice + n * pitch + koff * 2;
+            const uint16_t *src = p.x + static_cast<size_t>(tb.stok[gbeg + n]) * p.H + kglob;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) bq[nt][v] = *reinterpret_cast<const uint4 *>(src + 16 * v);
+            for (int v = 0; v < 4; ++v) b[nt][v] = ldg_nc_v4(src + 8 * v);
         } else {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) bq[nt][v] = make_uint4(0, 0, 0, 0);
+            for (int v = 0; v < 4; ++v) b[nt][v] = make_uint4(0, 0, 0, 0);
         }
     }
 }
 
-// ---- phase A: gate/up rows i0..i0+15 for one group -> h (fp16)
-template <int NT, bool NULLM>
-__device__ __forceinline__ bool ticket_A(const KernelParams &p, Cons &c, int grp, int tile)
+// Position of intermediate element k inside a row of h.  Each 128-element
+// block qg (the K chunk the down consumers read) is stored as [v][t][8]:
+// the 8 elements a thread t takes as piece v sit next to those of t +- 1, so
+// one 16-byte load of eight pairs x four threads reads eight 64-byte runs.
+// k -> (qg, t, v, e) follows the chunk K order of the weight layout (k_off).
+__device__ __forceinline__ int h_index(int mode, int k)
 {
-    const int e = c.tb.gexp[grp], gbeg = c.tb.gbeg[grp], gcnt = c.tb.gcnt[grp];
-    const int i0 = tile * 16;
+    const int e = k & 7, v = (k >> 3) & 3;
+    int qg, t;
+    if (mode == 0) {
+        qg = k >> 7;
+        t = (k >> 5) & 3;
+    } else {
+        qg = ((k >> 8) << 1) | ((k >> 5) & 1);
+        t = (k >> 6) & 3;
+    }
+    return qg * 128 + v * 32 + t * 8 + e;
+}
+
+// h (down): rows written during this step by other CTAs, read at L2 (.cg).
+template <int NT>
+__device__ __forceinline__ void load_h(uint4 (&b)[NT][4], const KernelParams &p, int gbeg, int gcnt, int qg, int g,
+                                       int t)
+{
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int n = nt * 8 + g;
+        if (n < gcnt) {
+            const uint16_t *src = p.hbuf + static_cast<size_t>(gbeg + n) * p.I + qg * 128 + t * 8;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) b[nt][v] = ldg_cg_v4(src + 32 * v);
+        } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) b[nt][v] = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ consumer warps
+// Each of the eight consumer warps walks the stage ring on its own: it waits
+// for a stage's weights (bounded), computes its share of the ticket, and
+// releases the stage with one arrival.  No barrier spans warps; the only
+// cross-warp step is the reduction at the end of a ticket, done by whichever
+// warp arrives last while the others move on.
+
+// Bounded wait on an mbarrier phase.  Every lane polls the barrier itself
+// (acquire); the verdict is made warp-uniform with a vote, so a lane that
+// gave up (abort flag, timeout) takes the whole warp out.
+__device__ __forceinline__ bool warp_wait_bar(const KernelParams &p, uint64_t *bar, uint32_t ph,
+                                              volatile int *abort_flag)
+{
+    bool ok = mbar_test(bar, ph);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if (!ok) ok = wait_bar(bar, ph, p, abort_flag);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded per-lane spin until pred() (a CTA-shared flag read with acquire);
+// warp-uniform verdict.
+template <class Pred>
+__device__ __forceinline__ bool warp_spin(const KernelParams &p, Pred pred, volatile int *abort_flag)
+{
+    bool ok = pred();
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if (!ok) {
+        const uint64_t t0 = gtimer();
+        for (uint32_t it = 1;; ++it) {
+            if (pred()) { ok = true; break; }
+            if ((it & 15u) == 0) {
+                if (*abort_flag) break;
+                if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
+                    raise_error(p, abort_flag, kErrTimeout);
+                    break;
+                }
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Header of fill n_next if the producer has published it already (uniform).
+__device__ __forceinline__ bool peek_header(SmemHdr *hd, int s_next, int n_next, int4 &h)
+{
+    const bool ok = ld_acq_cta(&hd->hdr_seq[s_next]) == n_next + 1;
+    if (!__all_sync(0xffffffffu, ok)) return false;
+    h = hd->stage_hdr[s_next];
+    return true;
+}
+
+// Hand a finished ticket to the helper: slot = ticket sequence number.  The
+// warp's global stores precede the release through __syncwarp; the helper
+// releases them at gpu scope.
+__device__ __forceinline__ bool push_done(const KernelParams &p, SmemHdr *hd, int tick, int kind, int grp, int tile,
+                                          int lane, volatile int *abort_flag)
+{
+    __syncwarp();
+    const int need = tick - kDoneQ + 1;
+    if (!warp_spin(p, [&] { return ld_acq_cta(&hd->dq_head) >= need; }, abort_flag)) return false;
+    if (lane == 0) {
+        const int slot = tick % kDoneQ;
+        hd->dq_kind[slot] = kind;
+        hd->dq_grp[slot] = grp;
+        hd->dq_tile[slot] = tile;
+        st_rel_cta(&hd->dq_seq[slot], tick + 1);
+    }
+    __syncwarp();
+    return true;
+}
+
+// End of a ticket.  Every warp leaves its fp32 partial sums (its K-slice of
+// the ticket's rows) in one of two reduction buffers and arrives on that
+// buffer's mbarrier; once all eight have arrived (bounded wait), each warp
+// reduces one eighth of the outputs in a fixed order (warp 0 first), applies
+// the tensor scales (ts0, ts1: gate and up, or down and unused) and writes
+// its share of h (gate/up ticket) or of the per-pair down outputs (down
+// ticket).  The last warp to finish queues the ticket for the helper.  A
+// buffer is rewritten two tickets later, by which time every warp has passed
+// the other buffer's barrier, i.e. has finished reading this one.
+template <int NT, bool NULLM>
+__device__ __forceinline__ bool finish_ticket(const KernelParams &p, const Tabs &tb, float4 *red,
+                                              const float (&acc)[2][NT][4], bool isA, int grp, int tile, int tick,
+                                              float ts0, float ts1, int warp, int lane, volatile int *abort_flag)
+{
+    SmemHdr *hd = tb.hdr;
+    const int b = tick & 1;
+    float4 *rb = red + b * (16 * NT * 32);
+    const int base = isA ? warp * 2 : (warp & 3) * 4 + (warp >> 2) * 2;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            rb[((base + mt) * NT + nt) * 32 + lane] =
+                make_float4(acc[mt][nt][0], acc[mt][nt][1], acc[mt][nt][2], acc[mt][nt][3]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&hd->redbar[b]);
+    if (!warp_wait_bar(p, &hd->redbar[b], static_cast<uint32_t>((tick >> 1) & 1), abort_flag)) return false;
+    const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
+    const float *redf = reinterpret_cast<const float *>(rb);
+    if (isA) {
+        // h[n][i0 + row] = SiLU(g) * u: this warp's 16*NT of the 16 rows x 8*NT pairs
+        const int idx = warp * (16 * NT) + lane;
+        if (lane < 16 * NT) {
+            const int nt = idx >> 7, ls = (idx >> 2) & 31, r = idx & 3;
+            const int row = (ls >> 2) + 8 * (r >> 1);
+            const int n = nt * 8 + 2 * (ls & 3) + (r & 1);
+            if (n < gcnt) {
+                float sg = 0.f, su = 0.f;
+#pragma unroll
+                for (int k2 = 0; k2 < kConsumerWarps; ++k2) {
+                    sg += redf[(((k2 * 2 + 0) * NT + nt) * 32 + ls) * 4 + r];
+                    su += redf[(((k2 * 2 + 1) * NT + nt) * 32 + ls) * 4 + r];
+                }
+                const float gv = sg * ts0, uv = su * ts1;
+                float v = gv / (1.0f + __expf(-gv)) * uv;
+                if (NULLM) v = 0.f;
+                if (!(fabsf(v) <= 65504.0f)) atomicOr(p.ctrl + 2, kErrRange);
+                p.hbuf[static_cast<size_t>(gbeg + n) * p.I + h_index(p.nib_mode, tile * 16 + row)] =
+                    __half_as_ushort(__float2half_rn(v));
+            }
+        }
+    } else {
+        // per-pair down outputs of rows h0 .. h0+63: this warp's 64*NT, sum of the 4 K-slices
+        const int h0 = tile * kMB;
+#pragma unroll
+        for (int j = 0; j < 2 * NT; ++j) {
+            const int idx = warp * (64 * NT) + j * 32 + lane;
+            const int mm = idx / (NT * 128), rem = idx - mm * (NT * 128);
+            const int nt = rem >> 7, ls = (rem >> 2) & 31, r = rem & 3;
+            const int row = mm * 16 + (ls >> 2) + 8 * (r >> 1);
+            const int n = nt * 8 + 2 * (ls & 3) + (r & 1);
+            if (n < gcnt) {
+                float so = 0.f;
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2) so += redf[(((k2 * 4 + mm) * NT + nt) * 32 + ls) * 4 + r];
+                p.part[static_cast<size_t>(gbeg + n) * p.H + h0 + row] = so * ts0;
+            }
+        }
+    }
+    // the last warp done queues the ticket (acq_rel: the other warps' stores come first)
+    __syncwarp();
+    int last = 0;
+    if (lane == 0)
+        last = atom_add_acqrel_cta(&hd->red_cnt, 1) == kConsumerWarps * tick + (kConsumerWarps - 1);
+    if (!__shfl_sync(0xffffffffu, last, 0)) return true;
+    return push_done(p, hd, tick, isA ? KIND_A : KIND_B, grp, tile, lane, abort_flag);
+}
+
+template <int NT, bool NULLM>
+__device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *smem, const Tabs &tb,
+                                              volatile int *abort_flag)
+{
+    SmemHdr *hd = tb.hdr;
+    float4 *red = reinterpret_cast<float4 *>(smem + p.red_off);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int chunksA = p.KA / 128, chunksB = p.KB / 128;
+    const int ksB = warp & 3, mgB = warp >> 2;  // down: 4 K-slices x 2 groups of 32 rows
+    int s = 0, n = 0, tick = 0;
+    uint32_t ph = 0;
+    uint4 nb[NT][4];     // B operand of this warp's first task in fill n, if loaded ahead
+    bool have_nb = false;
+    float ts0 = 0.f, ts1 = 0.f;  // the ticket's tensor scales, loaded at its first part
     float acc[2][NT][4];
 #pragma unroll
     for (int a = 0; a < 2; ++a)
@@ -561,186 +732,148 @@ __device__ __forceinline__ bool ticket_A(const KernelParams &p, Cons &c, int grp
 #pragma unroll
             for (int r = 0; r < 4; ++r) acc[a][b][r] = 0.f;
 
-    const int chunks = p.KA / 128;
-    const int ks = c.warp;  // K-slices = 8 consumer warps, both m-tiles per warp
-    for (int part = 0; part < p.nPA; ++part) {
-        if (part > 0) {
-            const int4 h = cons_next_stage(p, c);
-            if (h.x == KIND_END) return false;
-        }
-        const uint8_t *st = c.smem + c.s * p.stage_bytes;
-        for (int q = ks; q < chunks; q += kConsumerWarps) {
-            uint4 ra[2], rb[2], bq[NT][4];
-            uint16_t s_a[2], s_b[2];
-            const int ko = k_off(p.nib_mode, q, c.t);
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {  // m-tile 0: gate rows, 1: up rows
-                const uint8_t *nb = st + (mt ? p.offUq : p.offGq);
-                ra[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, 16, c.g, q, c.t));
-                rb[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, 16, c.g + 8, q, c.t));
-                const uint8_t *sb = st + (mt ? p.offUs : p.offGs);
-                s_a[mt] = scale_pair(sb, p.spA, p.shA, p.mkA, c.g, ko);
-                s_b[mt] = scale_pair(sb, p.spA, p.shA, p.mkA, c.g + 8, ko);
-            }
-            load_bq_smem<NT>(bq, st + p.offX, p.xpitch, ko, c.g, gcnt);
-            chunk_math<2, NT, true, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
-        }
-        cons_release_stage(p, c);
-    }
-    // cross-warp reduction (fixed order) -> g, u -> h
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-            c.red[((ks * 2 + mt) * NT + nt) * 32 + c.lane] =
-                make_float4(acc[mt][nt][0], acc[mt][nt][1], acc[mt][nt][2], acc[mt][nt][3]);
-    consumer_sync();
-    const float tsg = p.gts[e], tsu = p.uts[e];
-    const float *redf = reinterpret_cast<const float *>(c.red);
-    bool range_bad = false;
-    for (int idx = c.tid; idx < NT * 128; idx += kConsumerThreads) {
-        const int nt = idx >> 7, ls = (idx >> 2) & 31, r = idx & 3;
-        const int row = (ls >> 2) + 8 * (r >> 1);
-        const int n = nt * 8 + 2 * (ls & 3) + (r & 1);
-        if (n < gcnt) {
-            float sg = 0.f, su = 0.f;
-#pragma unroll
-            for (int k2 = 0; k2 < kConsumerWarps; ++k2) {
-                sg += redf[(((k2 * 2 + 0) * NT + nt) * 32 + ls) * 4 + r];
-                su += redf[(((k2 * 2 + 1) * NT + nt) * 32 + ls) * 4 + r];
-            }
-            const float gv = sg * tsg, uv = su * tsu;
-            float hv = gv / (1.0f + __expf(-gv)) * uv;
-            if (NULLM) hv = 0.f;
-            if (!(fabsf(hv) <= 65504.0f)) range_bad = true;
-            p.hbuf[static_cast<size_t>(gbeg + n) * p.I + i0 + row] = __half_as_ushort(__float2half_rn(hv));
-        }
-    }
-    if (range_bad) atomicOr(p.ctrl + 2, kErrRange);
-    consumer_sync();
-    cons_push_done(p, c, KIND_A, grp, tile);
-    return true;
-}
-
-// ---- phase B: down rows h0..h0+63 for one group -> partials, then combine
-template <int NT, bool NULLM>
-__device__ __forceinline__ bool ticket_B(const KernelParams &p, Cons &c, int grp, int tile)
-{
-    const int e = c.tb.gexp[grp], gbeg = c.tb.gbeg[grp], gcnt = c.tb.gcnt[grp];
-    const int h0 = tile * kMB;
-    float acc[2][NT][4];
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int b = 0; b < NT; ++b)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) acc[a][b][r] = 0.f;
-
-    const int chunks = p.KB / 128;
-    const int ks = c.warp & 3, mg = c.warp >> 2;  // 4 K-slices x 2 m-groups of 2 m-tiles
-    for (int part = 0; part < p.nPB; ++part) {
-        if (part > 0) {
-            const int4 h = cons_next_stage(p, c);
-            if (h.x == KIND_END) return false;
-        }
-        const uint8_t *st = c.smem + c.s * p.stage_bytes;
-        const uint8_t *nb = st + p.offDq;
-        const uint8_t *sb = st + p.offDs;
-        for (int q = ks; q < chunks; q += 4) {
-            uint4 ra[2], rb[2], bq[NT][4];
-            uint16_t s_a[2], s_b[2];
-            const int ko = k_off(p.nib_mode, q, c.t);
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                const int r0 = mg * 32 + mt * 16 + c.g;
-                ra[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, kMB, r0, q, c.t));
-                rb[mt] = *reinterpret_cast<const uint4 *>(nb + nib_off(p.nib_mode, kMB, r0 + 8, q, c.t));
-                s_a[mt] = scale_pair(sb, p.spB, p.shB, p.mkB, r0, ko);
-                s_b[mt] = scale_pair(sb, p.spB, p.shB, p.mkB, r0 + 8, ko);
-            }
-            load_bq_smem<NT>(bq, st + p.offH, p.hpitch, ko, c.g, gcnt);
-            chunk_math<2, NT, false, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
-        }
-        cons_release_stage(p, c);
-    }
-    // cross-warp reduction over the 4 K-slices -> o -> per-pair partials
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-            c.red[((ks * 4 + mg * 2 + mt) * NT + nt) * 32 + c.lane] =
-                make_float4(acc[mt][nt][0], acc[mt][nt][1], acc[mt][nt][2], acc[mt][nt][3]);
-    consumer_sync();
-    const float tsd = p.dts[e];
-    const float *redf = reinterpret_cast<const float *>(c.red);
-    for (int idx = c.tid; idx < 4 * NT * 128; idx += kConsumerThreads) {
-        const int mm = idx / (NT * 128), rem = idx - mm * (NT * 128);
-        const int nt = rem >> 7, ls = (rem >> 2) & 31, r = rem & 3;
-        const int row = mm * 16 + (ls >> 2) + 8 * (r >> 1);
-        const int n = nt * 8 + 2 * (ls & 3) + (r & 1);
-        if (n < gcnt) {
-            float so = 0.f;
-#pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2) so += redf[(((k2 * 4 + mm) * NT + nt) * 32 + ls) * 4 + r];
-            p.part[static_cast<size_t>(gbeg + n) * p.H + h0 + row] = so * tsd;
-        }
-    }
-    consumer_sync();
-    cons_push_done(p, c, KIND_B, grp, tile);
-    return true;
-}
-
-template <int NT, bool NULLM>
-__device__ __forceinline__ void consumer_loop(const KernelParams &p, Cons &c)
-{
     for (;;) {
-        const int4 h = cons_next_stage(p, c);
+        if (!warp_wait_bar(p, &hd->full[s], ph, abort_flag)) break;
+        const int4 h = hd->stage_hdr[s];
         if (h.x == KIND_END) break;
-        const bool ok = (h.x == KIND_A) ? ticket_A<NT, NULLM>(p, c, h.y, h.z) : ticket_B<NT, NULLM>(p, c, h.y, h.z);
-        if (!ok) break;  // uniform: decided from a flag published before a barrier
+        const bool isA = h.x == KIND_A;
+        const int grp = h.y, tile = h.z, part = h.w;
+        const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
+        if (part == 0) {
+            const int e = tb.gexp[grp];
+            ts0 = __ldg(isA ? p.gts + e : p.dts + e);
+            ts1 = isA ? __ldg(p.uts + e) : 0.f;
+        }
+        if (!isA && !have_nb &&
+            !warp_spin(p, [&] { return ld_acq_cta_u8(tb.hready + grp) == 2; }, abort_flag))
+            break;
+        const uint8_t *st = smem + s * p.stage_bytes;
+        // this warp's tasks: gate/up chunk q (rows g, g+8 of gate and of up),
+        // or down chunk q of the 32 rows mgB*32 .. +31
+        auto load_w = [&](int q, uint4 (&ra)[2], uint4 (&rb)[2], uint16_t (&s_a)[2], uint16_t (&s_b)[2]) {
+            const int ko = k_off(p.nib_mode, q, t);
+            if (isA) {
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {  // m-tile 0: gate rows, 1: up rows
+                    const uint8_t *nbp = st + (mt ? p.offUq : p.offGq);
+                    ra[mt] = *reinterpret_cast<const uint4 *>(nbp + nib_off(p.nib_mode, 16, g, q, t));
+                    rb[mt] = *reinterpret_cast<const uint4 *>(nbp + nib_off(p.nib_mode, 16, g + 8, q, t));
+                    const uint8_t *sbp = st + (mt ? p.offUs : p.offGs);
+                    s_a[mt] = scale_pair(sbp, p.spA, p.shA, p.mkA, g, ko);
+                    s_b[mt] = scale_pair(sbp, p.spA, p.shA, p.mkA, g + 8, ko);
+                }
+            } else {
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const int r0 = mgB * 32 + mt * 16 + g;
+                    ra[mt] = *reinterpret_cast<const uint4 *>(st + p.offDq + nib_off(p.nib_mode, kMB, r0, q, t));
+                    rb[mt] = *reinterpret_cast<const uint4 *>(st + p.offDq + nib_off(p.nib_mode, kMB, r0 + 8, q, t));
+                    s_a[mt] = scale_pair(st + p.offDs, p.spB, p.shB, p.mkB, r0, ko);
+                    s_b[mt] = scale_pair(st + p.offDs, p.spB, p.shB, p.mkB, r0 + 8, ko);
+                }
+            }
+        };
+        const int q0 = isA ? warp : ksB, qstep = isA ? kConsumerWarps : 4, qend = isA ? chunksA : chunksB;
+        uint4 ra[2], rb[2], bq[NT][4];
+        uint16_t s_a[2], s_b[2];
+        // (one n-tile: the first task's weight reads go out before the
+        // look-ahead below and overlap it; two n-tiles: after it, which keeps
+        // the live registers within the 168 three warps per SMSP allow)
+        if (q0 < qend) {
+            if (NT == 1) load_w(q0, ra, rb, s_a, s_b);
+            if (have_nb) {
+#pragma unroll
+                for (int a = 0; a < NT; ++a)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) bq[a][v] = nb[a][v];
+            } else if (isA) {
+                load_x<NT>(bq, p, tb, gbeg, gcnt, part * p.KA + k_off(p.nib_mode, q0, t), g);
+            } else {
+                load_h<NT>(bq, p, gbeg, gcnt, part * chunksB + q0, g, t);
+            }
+        }
+        // look one fill ahead and start its B-operand loads now
+        {
+            const int s2 = s + 1 == p.NS ? 0 : s + 1;
+            int4 h2;
+            have_nb = false;
+            if (peek_header(hd, s2, n + 1, h2) && h2.x != KIND_END) {
+                const bool a2 = h2.x == KIND_A;
+                const int gb2 = tb.gbeg[h2.y], gc2 = tb.gcnt[h2.y];
+                if (a2 && warp < chunksA) {
+                    load_x<NT>(nb, p, tb, gb2, gc2, h2.w * p.KA + k_off(p.nib_mode, warp, t), g);
+                    have_nb = true;
+                } else if (!a2 && ksB < chunksB &&
+                           __all_sync(0xffffffffu, ld_acq_cta_u8(tb.hready + h2.y) == 2)) {
+                    load_h<NT>(nb, p, gb2, gc2, h2.w * chunksB + ksB, g, t);
+                    have_nb = true;
+                }
+            }
+        }
+        if (NT != 1 && q0 < qend) load_w(q0, ra, rb, s_a, s_b);
+        for (int q = q0; q < qend; q += qstep) {
+            if (q != q0) {
+                load_w(q, ra, rb, s_a, s_b);
+                if (isA) load_x<NT>(bq, p, tb, gbeg, gcnt, part * p.KA + k_off(p.nib_mode, q, t), g);
+                else load_h<NT>(bq, p, gbeg, gcnt, part * chunksB + q, g, t);
+            }
+            if (isA) chunk_math<2, NT, true, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
+            else chunk_math<2, NT, false, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
+        }
+        // release the stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hd->empty[s]);
+        if (++s == p.NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+        ++n;
+        if (part == (isA ? p.nPA : p.nPB) - 1) {
+            if (!finish_ticket<NT, NULLM>(p, tb, red, acc, isA, grp, tile, tick, ts0, ts1, warp, lane, abort_flag))
+                break;
+            ++tick;
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int b = 0; b < NT; ++b)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) acc[a][b][r] = 0.f;
+        }
     }
-    if (c.tid == 0) vstore(&c.tb.hdr->cons_done, 1);
+    __syncwarp();
+    if (lane == 0) atom_add_acqrel_cta(&hd->cons_exited, 1);  // after this warp's queue entries
 }
 
-// ------------------------------------------------------------------ producer
-// Ticket order.  With n groups, TA gate/up tickets and nHt down tickets per
-// group, and a lookahead of L = min(2, n) groups, the sequence is
-//   A_0 .. A_{L-1}, then (A_j, B_{j-L}) for j = L .. n-1, then B_{n-L} .. B_{n-1}
-// (A_j = the TA gate/up tickets of group j, B_j = its nHt down tickets).  Every
-// gate/up ticket of a group precedes all its down tickets, which is all the
-// dependency waits need; the lookahead lets a group's h rows be ready (or
-// nearly) by the time its down stages reach the consumers.
+// ------------------------------------------------------------------ tickets
+// Ticket order: all gate/up tickets (group-major: the TA 16-row tiles of group
+// 0, then group 1, ...), then all down tickets (group-major: the nB 64-row
+// tiles of each group).  Every gate/up ticket precedes every down ticket, so
+// each down ticket's dependency is held by a running CTA when it is handed
+// out, and by then most groups' h rows are long complete: the down phase
+// starts while the last gate/up tickets finish, with no idle dependency wait
+// in the steady state.
 struct TicketInfo {
     int isA, grp, tile;
 };
 
 __device__ __forceinline__ TicketInfo decode_ticket(int t, int n, int TA, int nB)
 {
-    const int L = n < 2 ? n : 2;
     TicketInfo r;
-    if (t < L * TA) {
+    if (t < n * TA) {
         r.isA = 1; r.grp = t / TA; r.tile = t % TA;
-        return r;
+    } else {
+        const int t2 = t - n * TA;
+        r.isA = 0; r.grp = t2 / nB; r.tile = t2 % nB;
     }
-    int t2 = t - L * TA;
-    const int pairs = (n - L) * (TA + nB);
-    if (t2 < pairs) {
-        const int j = L + t2 / (TA + nB), q = t2 % (TA + nB);
-        if (q < TA) { r.isA = 1; r.grp = j; r.tile = q; }
-        else { r.isA = 0; r.grp = j - L; r.tile = q - TA; }
-        return r;
-    }
-    t2 -= pairs;
-    r.isA = 0; r.grp = n - L + t2 / nB; r.tile = t2 % nB;
     return r;
 }
 
-// Lane 0 of the producer warp finds free stages and issues the weight boxes;
-// lanes 0..gcnt-1 copy a gate/up part's x rows into the same stage.  A down
-// part's h rows exist only once all 16-row gate/up tickets of its group are
-// done, so the part goes to the helper's queue and the helper copies them;
-// the stage's barrier expects both.  The producer never waits on global
-// memory: its next ticket comes from the helper too.
+// ------------------------------------------------------------------ producer warp
+// Lane 0 finds free stages and issues each part's weight boxes: for a gate/up
+// part the 16 gate rows and 16 up rows (E2M1 and E4M3), for a down part 64
+// down rows.  The stage header is published (hdr_seq) before the copies, so
+// the consumers can start the part's activation loads while the weights are
+// still in flight.  Tickets come from the helper, which fetches them ahead.
 __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb,
                                               volatile int *abort_flag)
 {
@@ -753,7 +886,7 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
     const uint32_t wbytesA = 32u * (p.KA / 2) + 32u * (p.KA / 16);
     const uint32_t wbytesB = kMB * (p.KB / 2) + kMB * (p.KB / 16);
     bool ok = true;
-    int s = 0;
+    int s = 0, fill = 0;
     uint32_t ph = 0;
     int ticket = blockIdx.x;
     // a bounded wait for a condition polled by lane 0; false on abort/timeout
@@ -775,26 +908,23 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
         return __shfl_sync(0xffffffffu, got, 0) != 0;
     };
     int tq_head = 0;
-    while (ok) {
-        if (ticket >= total) break;
+    while (ok && ticket < total) {
         const TicketInfo ti = decode_ticket(ticket, ng, TA, p.nHt);
         const bool isA = ti.isA != 0;
         const int grp = ti.grp, tile = ti.tile;
-        const int e = tb.gexp[grp], gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
+        const int e = tb.gexp[grp];
         const int nparts = isA ? p.nPA : p.nPB;
-        const uint16_t *xrow = nullptr;  // x row of this lane's pair (gate/up)
-        if (isA && lane < gcnt) xrow = p.x + static_cast<size_t>(tb.perm[gbeg + lane] / p.k) * p.H;
         for (int part = 0; part < nparts; ++part) {
             if (!lane0_wait([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
                 ok = false;
                 break;
             }
-            uint8_t *st = smem + s * p.stage_bytes;
-            uint64_t *bar = &hd->full[s];
-            const int KP = isA ? p.KA : p.KB;
             if (lane == 0) {
+                uint8_t *st = smem + s * p.stage_bytes;
+                uint64_t *bar = &hd->full[s];
                 hd->stage_hdr[s] = make_int4(isA ? KIND_A : KIND_B, grp, tile, part);
-                mbar_expect_tx(bar, (isA ? wbytesA : wbytesB) + static_cast<uint32_t>(gcnt) * 2u * KP);
+                st_rel_cta(&hd->hdr_seq[s], fill + 1);
+                mbar_expect_tx(bar, isA ? wbytesA : wbytesB);
                 if (isA) {
                     // gate rows i0..i0+15 and up rows i0..i0+15, K elements part*KA ..
                     const int row = e * p.I + tile * 16;
@@ -830,19 +960,10 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
                     else
                         bulk_g2s(st + p.offDs, p.ds + static_cast<size_t>(row) * (p.I / 16), kMB * (p.I / 16), bar,
                                  pol);
-                    // the h rows: queued for the helper (at most one entry per stage in flight)
-                    const int tail = hd->pq_tail;
-                    const int slot = tail % kMaxStages;
-                    hd->pq_stage[slot] = s;
-                    hd->pq_grp[slot] = grp;
-                    hd->pq_part[slot] = part;
-                    __threadfence_block();
-                    vstore(&hd->pq_tail, tail + 1);
                 }
-                hd->fill_cnt += 1;
             }
             __syncwarp();
-            if (xrow) bulk_g2s(st + p.offX + lane * p.xpitch, xrow + static_cast<size_t>(part) * KP, 2u * KP, bar, pol);
+            ++fill;
             if (++s == p.NS) {
                 s = 0;
                 ph ^= 1u;
@@ -850,15 +971,14 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
         }
         if (!ok) break;
         // next ticket from the helper
-        if (!lane0_wait([&] { return vload(&hd->tq_tail) > tq_head; })) {
+        if (!lane0_wait([&] { return ld_acq_cta(&hd->tq_tail) > tq_head; })) {
             ok = false;
             break;
         }
         int t = 0;
         if (lane == 0) {
-            __threadfence_block();
-            t = hd->tq_buf[tq_head & 1];
-            vstore(&hd->tq_head, tq_head + 1);
+            t = hd->tq_buf[tq_head % kTq];
+            st_rel_cta(&hd->tq_head, tq_head + 1);
         }
         ++tq_head;
         ticket = __shfl_sync(0xffffffffu, t, 0);
@@ -867,11 +987,14 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
     if (ok && lane0_wait([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
         if (lane == 0) {
             hd->stage_hdr[s] = make_int4(KIND_END, 0, 0, 0);
+            st_rel_cta(&hd->hdr_seq[s], fill + 1);
             mbar_arrive(&hd->full[s]);
         }
+        ++fill;
     } else if (lane == 0) {
         *abort_flag = 1;
     }
+    if (lane == 0) hd->fill_cnt = fill;
     __syncwarp();
 }
 
@@ -879,82 +1002,80 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
 // Everything that waits on or publishes to other CTAs runs here, so that
 // neither the producer's copy issue nor the consumers' math ever stalls on a
 // global round trip:
-//   * fetch the next ticket from the global counter (one ahead);
-//   * copy queued down parts' h rows once the group's gate/up counter is full
-//     (acquire, then an async-proxy fence: the rows were written through the
-//     generic proxy and are read by bulk copies);
-//   * release finished work: a gpu-scope fence, then bump the group's gate/up
-//     counter (gate/up ticket) or the per-(token, 64-row tile) arrival counters
-//     (down ticket); the CTA that completes a token's tile sums its k per-pair
-//     outputs in slot order and writes y -- no floating-point atomics, so the
-//     result is the same bits every run.
-__device__ __forceinline__ void helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, volatile int *abort_flag)
+//   * fetch tickets from the global counter, up to kTq ahead of the producer;
+//   * for every down ticket this CTA will run, poll its group's gate/up
+//     counter (acquire, gpu scope) and flag the group's h rows complete in
+//     shared memory (each lane watches one group);
+//   * release finished work in ticket order: a gpu-scope fence, then bump the
+//     group's gate/up counter (gate/up ticket) or the per-(token, 64-row tile)
+//     arrival counters (down ticket); the CTA that completes a token's tile
+//     sums its k per-pair outputs in slot order and writes y -- no
+//     floating-point atomics, so the result is the same bits every run.
+__device__ __forceinline__ void helper_loop(const KernelParams &p, Tabs tb, volatile int *abort_flag)
 {
     const int lane = threadIdx.x & 31;
     SmemHdr *hd = tb.hdr;
-    const uint64_t pol = policy_evict_first();
     const int ng = hd->n_groups;
-    const uint32_t TA = static_cast<uint32_t>(p.I / 16);
-    const int total = ng * (static_cast<int>(TA) + p.nHt);
-    bool tick_done = false;
-    int tq_tail = 0, pq_head = 0, dq_head = 0;
+    const int TA = p.I / 16;
+    const int total = ng * (TA + p.nHt);
+    bool fetch_done = false;
+    int tq_tail = 0, dq_head = 0;
+    int watch = -1;  // the group this lane polls (-1: none)
     uint64_t idle_since = 0;
+    // a down ticket's group goes on the watch list once (hready 0 -> 1)
+    auto note_ticket = [&](int tk) {
+        if (tk >= total) return;
+        const TicketInfo ti = decode_ticket(tk, ng, TA, p.nHt);
+        if (ti.isA) return;
+        // only this warp writes hready, and lane 0's view is the one that counts
+        if (__shfl_sync(0xffffffffu, ld_acq_cta_u8(tb.hready + ti.grp), 0) != 0) return;
+        const uint32_t free_lanes = __ballot_sync(0xffffffffu, watch < 0);
+        const int l = __ffs(free_lanes) - 1;  // a free lane exists: checked before the fetch
+        if (lane == l) watch = ti.grp;
+        if (lane == 0) st_rel_cta_u8(tb.hready + ti.grp, 1);
+        __syncwarp();
+    };
+    note_ticket(blockIdx.x);
     for (;;) {
         if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
         bool progress = false;
-        // 1) keep one ticket ready for the producer
-        if (!tick_done && tq_tail - vload(&hd->tq_head) < 1) {
-            int t = 0;
+        // 1) keep tickets queued for the producer (and a free watch lane for the next one)
+        const int tq_head = __shfl_sync(0xffffffffu, ld_acq_cta(&hd->tq_head), 0);
+        if (!fetch_done && tq_tail - tq_head < kTq && __ballot_sync(0xffffffffu, watch < 0) != 0) {
+            int tk = 0;
             if (lane == 0) {
-                t = static_cast<int>(gridDim.x + atomicAdd(p.ctrl, 1u));
-                hd->tq_buf[tq_tail & 1] = t;
-                __threadfence_block();
-                vstore(&hd->tq_tail, tq_tail + 1);
+                tk = static_cast<int>(gridDim.x + atomicAdd(p.ctrl, 1u));
+                hd->tq_buf[tq_tail % kTq] = tk;
+                st_rel_cta(&hd->tq_tail, tq_tail + 1);
             }
             ++tq_tail;
-            t = __shfl_sync(0xffffffffu, t, 0);
-            if (t >= total) tick_done = true;
+            tk = __shfl_sync(0xffffffffu, tk, 0);
+            if (tk >= total) fetch_done = true;
+            else note_ticket(tk);
             progress = true;
         }
-        // 2) h rows of queued down parts whose group is complete
-        while (pq_head != vload(&hd->pq_tail)) {
-            __threadfence_block();
-            const int slot = pq_head % kMaxStages;
-            const int grp = hd->pq_grp[slot];
-            int ready = 0;
-            if (lane == 0) ready = ld_acquire(p.doneA + grp) == TA ? 1 : 0;
-            if (!__shfl_sync(0xffffffffu, ready, 0)) break;
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            const int st = hd->pq_stage[slot], part = hd->pq_part[slot];
-            const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
-            if (lane < gcnt) {
-                uint8_t *dst = smem + st * p.stage_bytes + p.offH + lane * p.hpitch;
-                const uint16_t *src =
-                    p.hbuf + static_cast<size_t>(gbeg + lane) * p.I + static_cast<size_t>(part) * p.KB;
-                bulk_g2s(dst, src, 2u * p.KB, &hd->full[st], pol);
-            }
-            ++pq_head;
-            __syncwarp();
-            if (lane == 0) vstore(&hd->pq_head, pq_head);
+        // 2) groups whose gate/up tickets are all done: their h rows may be read
+        if (watch >= 0 && ld_acquire(p.doneA + watch) == static_cast<uint32_t>(TA)) {
+            st_rel_cta_u8(tb.hready + watch, 2);
+            watch = -1;
             progress = true;
         }
-        // 3) release finished tickets
-        const int dq_tail = vload(&hd->dq_tail);
-        if (dq_head != dq_tail) {
-            __threadfence_block();
+        progress = __any_sync(0xffffffffu, progress);
+        // 3) release finished tickets, in ticket order
+        const int exited = __shfl_sync(0xffffffffu, ld_acq_cta(&hd->cons_exited), 0);
+        for (;;) {
+            const int slot = dq_head % kDoneQ;
+            if (__shfl_sync(0xffffffffu, ld_acq_cta(&hd->dq_seq[slot]), 0) != dq_head + 1) break;
             __threadfence();  // the consumers' h / partial stores become visible first (cumulative)
-            for (; dq_head != dq_tail; ++dq_head) {
-                const int slot = dq_head % kDoneQ;
-                const int kind = hd->dq_kind[slot], grp = hd->dq_grp[slot], tile = hd->dq_tile[slot];
-                if (kind == KIND_A) {
-                    if (lane == 0) atomicAdd(p.doneA + grp, 1u);
-                    continue;
-                }
+            const int kind = hd->dq_kind[slot], grp = hd->dq_grp[slot], tile = hd->dq_tile[slot];
+            if (kind == KIND_A) {
+                if (lane == 0) atomicAdd(p.doneA + grp, 1u);
+            } else {
                 const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
                 int tok = -1;
                 bool last = false;
                 if (lane < gcnt) {
-                    tok = tb.perm[gbeg + lane] / p.k;
+                    tok = tb.stok[gbeg + lane];
                     uint32_t *ctr = p.cnt + static_cast<size_t>(tok) * p.nHt + tile;
                     const uint32_t old = atomicAdd(ctr, 1u);
                     last = old + 1u == static_cast<uint32_t>(tb.kvalid[tok]);
@@ -981,12 +1102,13 @@ __device__ __forceinline__ void helper_loop(const KernelParams &p, uint8_t *smem
                     }
                 }
             }
+            ++dq_head;
             __syncwarp();
-            if (lane == 0) vstore(&hd->dq_head, dq_head);
+            if (lane == 0) st_rel_cta(&hd->dq_head, dq_head);
             progress = true;
         }
-        // 4) done when the consumers are, with nothing left queued
-        if (vload(&hd->cons_done) && dq_head == vload(&hd->dq_tail) && pq_head == vload(&hd->pq_tail)) break;
+        // 4) done when every consumer warp has left and its last ticket is released
+        if (exited == kConsumerWarps) break;
         // 5) bounded idleness
         if (progress) {
             idle_since = 0;
@@ -1027,17 +1149,20 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
         for (int i = 0; i < p.NS; ++i) {
             mbar_init(&hd->full[i], 1);
             mbar_init(&hd->empty[i], kConsumerWarps);
+            hd->hdr_seq[i] = 0;
         }
         hd->abort_flag = 0;
         hd->fill_cnt = 0;
-        hd->cons_cnt = 0;
-        hd->cons_done = 0;
+        hd->cons_exited = 0;
+        hd->red_cnt = 0;
+        mbar_init(&hd->redbar[0], kConsumerWarps);
+        mbar_init(&hd->redbar[1], kConsumerWarps);
         hd->tq_head = hd->tq_tail = 0;
-        hd->pq_head = hd->pq_tail = 0;
-        hd->dq_head = hd->dq_tail = 0;
-        hd->verdict[0] = hd->verdict[1] = 1;
+        hd->dq_head = 0;
+        for (int i = 0; i < kDoneQ; ++i) hd->dq_seq[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    for (int i = tid; i < P; i += blockDim.x) tb.hready[i] = 0;
     // grouping (every CTA, redundantly; scratch aliases the reduction buffer)
     {
         uint8_t *scr = smem + p.red_off;
@@ -1076,6 +1201,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
             for (int j = 0; j < p.k; ++j) v += (tb.pos[t * p.k + j] != 0xFFFFu);
             tb.kvalid[t] = static_cast<uint8_t>(v);
         }
+        const int nv = hd->n_valid;
+        for (int r = tid; r < nv; r += blockDim.x) tb.stok[r] = static_cast<uint16_t>(tb.perm[r] / p.k);
         __syncthreads();
         if (blockIdx.x == 0 && tid == 0 && hd->n_bad) atomicOr(p.ctrl + 2, kErrBadId);
         // tokens without a valid slot: y = 0 (nobody else writes them)
@@ -1087,35 +1214,26 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
     }
 
     if (tid >= kConsumerThreads + 32) {
-        helper_loop(p, smem, tb, abort_flag);
+        helper_loop(p, tb, abort_flag);
     } else if (tid >= kConsumerThreads) {
         producer_loop(p, smem, tb, abort_flag);
     } else {
-        Cons c;
-        c.smem = smem;
-        c.tb = tb;
-        c.red = reinterpret_cast<float4 *>(smem + p.red_off);
-        c.tid = tid;
-        c.warp = tid >> 5;
-        c.lane = tid & 31;
-        c.g = c.lane >> 2;
-        c.t = c.lane & 3;
-        c.s = 0;
-        c.ph = 0;
-        c.nv = 0;
-        c.abort_flag = abort_flag;
-        consumer_loop<NT, NULLM>(p, c);
+        consumer_warp<NT, NULLM>(p, smem, tb, abort_flag);
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
 
     if (tid == 0) {
         if (*abort_flag) {
-            // drain: wait (bounded) for the copies of every stage filled but not
-            // yet seen complete, so no bulk copy lands after the CTA exits
+            // drain: wait (bounded) for the last fill of every stage, so no
+            // copy lands after the CTA exits (earlier fills of a stage were
+            // all consumed, hence complete)
             const uint64_t t0 = gtimer();
-            for (int i = hd->cons_cnt; i < hd->fill_cnt; ++i) {
-                while (!mbar_test(&hd->full[i % p.NS], static_cast<uint32_t>((i / p.NS) & 1))) {
+            const int F = hd->fill_cnt;
+            for (int i = 0; i < p.NS; ++i) {
+                const int fi = F / p.NS + (i < F % p.NS ? 1 : 0);
+                if (fi == 0) continue;
+                while (!mbar_test(&hd->full[i], static_cast<uint32_t>((fi - 1) & 1))) {
                     if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) break;
                 }
             }
