@@ -148,7 +148,7 @@ moe_status_t moe_decode(moe_plan_t plan, const void *x_dev, const int32_t *ids_d
  * Same x_dev, ids_dev, w_dev, y_dev, T and stream as moe_decode
  * (0 <= T <= min(24, T_max)).  The scratch is one library-owned buffer per
  * device of 16 MiB in this library's global memory; a call needs
- * 256 + 16384 + 4*T*(H/64) + 2*T*top_k*I + 4*T*top_k*H bytes (each piece
+ * 256 + 16384 + 4*T*(H/64) + 2*T*top_k*I + 6*T*top_k*H bytes (each piece
  * rounded up to 256) and is refused with MOE_ERR_UNSUPPORTED_SHAPE when that
  * exceeds 16 MiB.  Nothing is allocated or freed: each call zeroes the
  * scratch's control block and counters (one memset on `stream`) and launches

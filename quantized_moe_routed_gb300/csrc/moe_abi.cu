@@ -50,15 +50,16 @@ struct moe_plan {
     int KA = 0, nPA = 0, KB = 0, nPB = 0, nHt = 0;
     int nib_mode = 0;
     int scale_tmaA = 0, spA = 0, shA = 0, mkA = 0, scale_tmaB = 0, spB = 0, shB = 0, mkB = 0;
-    int offGq = 0, offUq = 0, offGs = 0, offUs = 0, offDq = 0, offDs = 0;
-    int stage_bytes = 0;  // one ring stage: the larger of a gate/up and a down part's weights
+    int offGq = 0, offUq = 0, offGs = 0, offUs = 0, offAa = 0, offDq = 0, offDs = 0, offAb = 0;
+    int stage_bytes_nt[3] = {0, 0, 0};  // one ring stage of the 1- and 2-n-tile variants
+    int stage_bytes = 0;                // of the 2-n-tile variant (the largest)
     CUtensorMap tm[6];
     int Tc = 0;  // tokens per launch chunk
     long long timeout_ns = 1000000000LL;
     bool strict = false, pdl = false;
     int smem_attr = 0;  // dynamic smem the kernel attribute currently allows
     // workspace layout (bytes from the base)
-    size_t off_done = 0, off_cnt = 0, off_h = 0, off_part = 0, ws_bytes = 0;
+    size_t off_done = 0, off_cnt = 0, off_h = 0, off_part = 0, off_xs = 0, ws_bytes = 0;
     std::mutex mu;
     moe_stats_t stats{};
 };
@@ -163,7 +164,7 @@ moe::SmemLayout layout_for(const moe_plan *pl, int T)
     const int scr_need = align16i(2 * P) + 8 * pl->d.E + 4 + 16;
     L.red_bytes = static_cast<int>(up(red_need > scr_need ? red_need : scr_need, 128));
     L.tab_bytes = moe::tab_bytes_for(P, T);
-    L.stage_bytes = pl->stage_bytes;
+    L.stage_bytes = pl->stage_bytes_nt[nt];
     const int avail = pl->smem_optin - L.red_bytes - L.tab_bytes - 1024;
     int ns = avail / L.stage_bytes;
     if (ns > moe::kMaxStages) ns = moe::kMaxStages;
@@ -194,7 +195,8 @@ enum class Path { Decode, Prefill, Null };
 
 // Byte offsets of the workspace pieces from the workspace base.
 struct WsOffsets {
-    size_t off_done, off_cnt, off_h, off_part, total;
+    size_t off_done, off_cnt, off_h, off_part, off_xs, total;
+    int Pmax;  // rows of each part block of xs / hbuf
 };
 
 moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, int T, void *ws,
@@ -253,6 +255,8 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
     p.doneA = reinterpret_cast<uint32_t *>(wsb + (wo ? wo->off_done : pl->off_done));
     p.cnt = reinterpret_cast<uint32_t *>(wsb + (wo ? wo->off_cnt : pl->off_cnt));
     p.hbuf = reinterpret_cast<uint16_t *>(wsb + (wo ? wo->off_h : pl->off_h));
+    p.xs = reinterpret_cast<uint16_t *>(wsb + (wo ? wo->off_xs : pl->off_xs));
+    p.Pmax = wo ? wo->Pmax : pl->Tc * pl->d.top_k;
     p.part = reinterpret_cast<float *>(wsb + (wo ? wo->off_part : pl->off_part));
     p.H = pl->d.H;
     p.I = pl->d.I;
@@ -277,8 +281,10 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
     p.offUq = pl->offUq;
     p.offGs = pl->offGs;
     p.offUs = pl->offUs;
+    p.offAa = pl->offAa;
     p.offDq = pl->offDq;
     p.offDs = pl->offDs;
+    p.offAb = pl->offAb;
     p.timeout_ns = pl->timeout_ns;
     p.null_mode = path == Path::Null ? 1 : 0;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -368,7 +374,9 @@ WsOffsets static_layout(const moe_plan *pl, int T)
     o.off_cnt = up(o.off_done + 4 * static_cast<size_t>(moe::kMaxPairs), 256);
     o.off_h = up(o.off_cnt + 4 * static_cast<size_t>(T) * pl->nHt, 256);
     o.off_part = up(o.off_h + 2 * P * pl->d.I, 256);
-    o.total = up(o.off_part + 4 * P * pl->d.H, 256);
+    o.off_xs = up(o.off_part + 4 * P * pl->d.H, 256);
+    o.total = up(o.off_xs + 2 * P * pl->d.H, 256);
+    o.Pmax = static_cast<int>(P);
     return o;
 }
 
@@ -446,7 +454,7 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
         if (ms > 0) pl->timeout_ns = ms * 1000000LL;
     }
     PartPlan pa{}, pb{};
-    if (!choose_part(d.H, 1024, 2048, &pa) || !choose_part(d.I, 512, 1024, &pb)) {
+    if (!choose_part(d.H, 512, 2048, &pa) || !choose_part(d.I, 512, 1024, &pb)) {
         delete pl;
         return fail(MOE_ERR_UNSUPPORTED_SHAPE,
                     "no stage tiling for H=%d, I=%d (an odd multiple of 128 must be <= 2048 for H, <= 1024 for I)",
@@ -468,16 +476,20 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
     // stage layouts: weights only, in 1024-aligned sub-buffers (the
     // activations are read from global memory by the consumers)
     pl->offGq = 0;
-    pl->offUq = 8 * pl->KA;
-    pl->offGs = 16 * pl->KA;
-    pl->offUs = pl->offGs + up1024(16 * pl->spA);
+    pl->offUq = moe::kRA * pl->KA / 2;
+    pl->offGs = moe::kRA * pl->KA;
+    pl->offUs = pl->offGs + up1024(moe::kRA * pl->spA);
+    pl->offAa = pl->offUs + up1024(moe::kRA * pl->spA);
     pl->offDq = 0;
-    pl->offDs = 32 * pl->KB;
-    {
-        const int stA = pl->offUs + up1024(16 * pl->spA);
-        const int stB = pl->offDs + up1024(moe::kMB * pl->spB);
-        pl->stage_bytes = stA > stB ? stA : stB;
+    pl->offDs = moe::kMB * pl->KB / 2;
+    pl->offAb = pl->offDs + up1024(moe::kMB * pl->spB);
+    for (int nt = 1; nt <= 2; ++nt) {
+        // weights, then the group's activation rows (8*nt rows of 2*KP bytes)
+        const int stA = pl->offAa + 8 * nt * 2 * pl->KA;
+        const int stB = pl->offAb + 8 * nt * 2 * pl->KB;
+        pl->stage_bytes_nt[nt] = up1024(stA > stB ? stA : stB);
     }
+    pl->stage_bytes = pl->stage_bytes_nt[2];
     // tensor maps (host-only encoding; no device memory involved)
     if (!encoder()) {
         delete pl;
@@ -488,8 +500,8 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
     int mode = 0;
     for (; mode < 2; ++mode) {
         if (mode == 1 && (d.H % 256 || d.I % 256)) break;
-        cr = encode_nib(&pl->tm[0], mode, d.gate_q_dev, rowsGU, d.H, 16, pl->KA);
-        if (cr == CUDA_SUCCESS) cr = encode_nib(&pl->tm[1], mode, d.up_q_dev, rowsGU, d.H, 16, pl->KA);
+        cr = encode_nib(&pl->tm[0], mode, d.gate_q_dev, rowsGU, d.H, moe::kRA, pl->KA);
+        if (cr == CUDA_SUCCESS) cr = encode_nib(&pl->tm[1], mode, d.up_q_dev, rowsGU, d.H, moe::kRA, pl->KA);
         if (cr == CUDA_SUCCESS) cr = encode_nib(&pl->tm[2], mode, d.down_q_dev, rowsD, d.I, moe::kMB, pl->KB);
         if (cr == CUDA_SUCCESS) break;
     }
@@ -500,8 +512,8 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
     }
     pl->nib_mode = mode;
     if (pl->scale_tmaA) {
-        cr = encode_scale(&pl->tm[3], d.gate_s_dev, rowsGU, d.H, 16, pa);
-        if (cr == CUDA_SUCCESS) cr = encode_scale(&pl->tm[4], d.up_s_dev, rowsGU, d.H, 16, pa);
+        cr = encode_scale(&pl->tm[3], d.gate_s_dev, rowsGU, d.H, moe::kRA, pa);
+        if (cr == CUDA_SUCCESS) cr = encode_scale(&pl->tm[4], d.up_s_dev, rowsGU, d.H, moe::kRA, pa);
     }
     if (cr == CUDA_SUCCESS && pl->scale_tmaB) cr = encode_scale(&pl->tm[5], d.down_s_dev, rowsD, d.I, moe::kMB, pb);
     if (cr != CUDA_SUCCESS) {
@@ -528,6 +540,8 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
     o = up(o + 2 * Pc * d.I, 256);
     pl->off_part = o;
     o = up(o + 4 * Pc * d.H, 256);
+    pl->off_xs = o;
+    o = up(o + 2 * Pc * d.H, 256);
     pl->ws_bytes = o;
     pl->stats.num_sms = sms;
     pl->stats.stages = L.NS;

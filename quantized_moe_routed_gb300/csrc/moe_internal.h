@@ -21,15 +21,18 @@ constexpr int kMaxStages = 16;
 constexpr int kDecodeMaxT = 24;     // the pages' m <= 24 decode bound
 constexpr int kMB = 64;             // down-projection rows per phase-B ticket
 
+// Rows of a gate/up ticket: 32 intermediate rows of gate and the same 32 of up.
+constexpr int kRA = 32;
+
 // Device error word bits (workspace control block, word 2).
 constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrBadId = 2u;
 constexpr uint32_t kErrRange = 4u;
 
-// Shared-memory tables of the step kernel: a 1024-byte control block, then
+// Shared-memory tables of the step kernel: a 2048-byte control block, then
 // five uint16 arrays of P entries, two uint8 arrays of P and one of T, each
 // padded to 16 bytes; the whole rounded up to 128 bytes.
-constexpr int kTabHdrBytes = 1024;
+constexpr int kTabHdrBytes = 2048;
 inline int tab_bytes_for(int P, int T)
 {
     const int a2 = (2 * P + 15) & ~15, a1 = (P + 15) & ~15, aT = (T + 15) & ~15;
@@ -38,6 +41,8 @@ inline int tab_bytes_for(int P, int T)
 
 // Workspace control block (first 256 bytes of the workspace).
 //   word 0: ticket counter   word 1: CTAs finished   word 2: error bits
+//   word 3: activation rows gathered (x, fp16) so far in this launch
+//   word 4: activation rows claimed for gathering so far in this launch
 constexpr size_t kCtrlBytes = 256;
 
 struct KernelParams {
@@ -58,10 +63,12 @@ struct KernelParams {
     uint32_t *ctrl;     // control block
     uint32_t *doneA;    // [kMaxPairs] per-group count of finished gate/up tickets
     uint32_t *cnt;      // [T * nHt] per (token, H-tile) arrivals
-    uint16_t *hbuf;     // [P, I] fp16 h, rows in sorted pair order, 128-element blocks permuted (see kernels)
+    uint16_t *xs;       // [nPA][Pmax][KA] fp16 x, rows in sorted pair order (layout: see kernels)
+    uint16_t *hbuf;     // [nPB][Pmax][KB] fp16 h, same row order and layout
     float *part;        // [P, H] fp32 per-pair down-projection outputs
     // shape
     int H, I, E, k, T;
+    int Pmax;           // rows of each part block of xs / hbuf
     // tiling (chosen on the host)
     int KA, nPA;        // gate/up: K elements per stage part, parts per ticket
     int KB, nPB;        // down: K elements per stage part, parts per ticket
@@ -69,8 +76,8 @@ struct KernelParams {
     int nib_mode;        // 0: 3-D span-major boxes [span][row][64 B]; 1: 2-D boxes [row][128 B], 128B swizzle
     int scale_tmaA, scale_tmaB;  // 1: scale rows by 2-D tensor map; 0: one 1-D bulk copy (natural layout)
     int spA, shA, mkA, spB, shB, mkB;  // scale smem row pitch, swizzle shift and mask
-    int offGq, offUq, offGs, offUs;    // phase-A stage sub-buffers (bytes, 1024-aligned)
-    int offDq, offDs;                  // phase-B stage sub-buffers
+    int offGq, offUq, offGs, offUs, offAa;  // gate/up stage sub-buffers (weights 1024-aligned; offAa: x rows)
+    int offDq, offDs, offAb;                // down stage sub-buffers (offAb: h rows)
     int stage_bytes, NS;
     int red_off, red_bytes, tab_off;            // smem layout (bytes)
     int ntiles;                                 // kernel variant: n-tiles per group (1 or 2)

@@ -238,20 +238,22 @@ constexpr int kDoneQ = 16;  // finished tickets in flight from the consumers to 
 constexpr int kTq = 4;      // tickets fetched ahead (helper -> producer)
 
 // CTA-shared control block.  The roles talk through single-writer fields:
-//   tq       helper -> producer     tickets fetched ahead
-//   hdr_seq  producer -> consumers  1 + the fill number whose header stage_hdr[s] holds
-//   red_*    consumers -> consumers the cross-warp reduction buffer's arrivals / release
-//   dq       consumers -> helper    finished tickets, slot = ticket sequence number % kDoneQ
+//   tq       helper -> producer    tickets fetched ahead
+//   pq       producer -> helper    stages whose activation rows the helper copies
+//                                  (x before it is gathered, h of every down part)
+//   redbar   consumers             ticket-end arrivals of the 8 consumer warps
+//   dq       consumers -> helper   finished tickets, slot = ticket sequence number % kDoneQ
 struct SmemHdr {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     int4 stage_hdr[kMaxStages];  // {kind, group, tile, part}
-    int hdr_seq[kMaxStages];
+    uint64_t redbar[2];
     int n_groups, n_valid, n_bad, abort_flag;  // abort_flag: any role gave up (read by every wait)
-    uint64_t redbar[2];                        // ticket-end arrivals of the 8 consumer warps, per buffer
-    int fill_cnt, cons_exited, red_cnt, pad1;
-    int tq_head, tq_tail, dq_head, pad0;
+    int fill_cnt, cons_exited, red_cnt, xready;
+    int tq_head, tq_tail, dq_head, pq_tail;
+    int pq_head, claim, pad1, pad2;
     int tq_buf[kTq];
+    int pq_stage[kMaxStages], pq_grp[kMaxStages], pq_part[kMaxStages], pq_kind[kMaxStages];
     int dq_seq[kDoneQ], dq_kind[kDoneQ], dq_grp[kDoneQ], dq_tile[kDoneQ];
 };
 static_assert(sizeof(SmemHdr) <= kTabHdrBytes, "header too large");
@@ -479,94 +481,67 @@ __device__ __forceinline__ void chunk_math(const uint4 (&ra)[MT], const uint4 (&
     }
 }
 
-// ------------------------------------------------------------------ activation operands
-// The B operand of one 128-element chunk comes straight from global memory,
-// not through the stage ring: pair n = nt*8 + g of the group, the 32 elements
-// this thread owns in the chunk, as four 16-byte pieces (piece v = elements
-// koff + 8v .. koff + 8v + 7).  Pairs past the group's end read as zero.
-__device__ __forceinline__ uint4 ldg_nc_v4(const void *ptr)
+// ------------------------------------------------------------------ activation rows
+// x (gathered into sorted pair order and converted to fp16 in the prologue)
+// and h live in the workspace as [part][Pmax][KP] fp16 blocks: the K slice a
+// stage needs for a group's rows gbeg .. gbeg+gcnt-1 is one contiguous run,
+// moved into the stage by a single bulk copy.  Inside each 128-element chunk
+// of a row, the 16-byte granule with the 8 elements thread t takes as piece v
+// (elements koff + 8v .. +7 in the chunk K order of k_off) sits at granule
+//   8*(v >> 1) + ((2t + (v & 1)) ^ (r & 1))      (r: the row's pair position)
+// so the eight threads of a quarter-warp (rows of both parities, t = 0..3)
+// read eight different bank groups; rows are a multiple of 128 bytes apart.
+__device__ __forceinline__ int act_granule(int v, int t, int rpar)
 {
-    uint4 v;
-    asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(ptr));
-    return v;
+    return 8 * (v >> 1) + ((2 * t + (v & 1)) ^ rpar);
 }
 
-__device__ __forceinline__ uint4 ldg_cg_v4(const void *ptr)
+// Element position of element kk (0 <= kk < KP) within its row of a part
+// block, for a row of parity rpar (inverse of the chunk K order of k_off).
+__device__ __forceinline__ int act_index(int mode, int kk, int rpar)
 {
-    uint4 v;
-    asm("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(ptr));
-    return v;
-}
-
-// x (gate/up): the caller's bf16 rows, read-only for the whole step, through
-// the non-coherent path.  A thread's four pieces share sectors, so after the
-// first one the rest hit L1.
-template <int NT>
-__device__ __forceinline__ void load_x(uint4 (&b)[NT][4], const KernelParams &p, const Tabs &tb, int gbeg, int gcnt,
-                                       int kglob, int g)
-{
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int n = nt * 8 + g;
-        if (n < gcnt) {
-            const uint16_t *src = p.x + static_cast<size_t>(tb.stok[gbeg + n]) * p.H + kglob;
-#pragma unroll
-            for (int v = 0; v < 4; ++v) b[nt][v] = ldg_nc_v4(src + 8 * v);
-        } else {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) b[nt][v] = make_uint4(0, 0, 0, 0);
-        }
-    }
-}
-
-// Position of intermediate element k inside a row of h.  Each 128-element
-// block qg (the K chunk the down consumers read) is stored as [v][t][8]:
-// the 8 elements a thread t takes as piece v sit next to those of t +- 1, so
-// one 16-byte load of eight pairs x four threads reads eight 64-byte runs.
-// k -> (qg, t, v, e) follows the chunk K order of the weight layout (k_off).
-__device__ __forceinline__ int h_index(int mode, int k)
-{
-    const int e = k & 7, v = (k >> 3) & 3;
-    int qg, t;
+    const int e = kk & 7, v = (kk >> 3) & 3;
+    int q, t;
     if (mode == 0) {
-        qg = k >> 7;
-        t = (k >> 5) & 3;
+        q = kk >> 7;
+        t = (kk >> 5) & 3;
     } else {
-        qg = ((k >> 8) << 1) | ((k >> 5) & 1);
-        t = (k >> 6) & 3;
+        q = ((kk >> 8) << 1) | ((kk >> 5) & 1);
+        t = (kk >> 6) & 3;
     }
-    return qg * 128 + v * 32 + t * 8 + e;
+    return q * 128 + act_granule(v, t, rpar) * 8 + e;
 }
 
-// h (down): rows written during this step by other CTAs, read at L2 (.cg).
+// The B operand of chunk q for pair n = nt*8 + g of the group, from the
+// stage's copy of the group's rows (row pitch `pitch` bytes).  Rows past the
+// group's end hold stale data: they only feed MMA columns nobody reads.
 template <int NT>
-__device__ __forceinline__ void load_h(uint4 (&b)[NT][4], const KernelParams &p, int gbeg, int gcnt, int qg, int g,
-                                       int t)
+__device__ __forceinline__ void load_act(uint4 (&b)[NT][4], const uint8_t *act, int pitch, int q, int gbeg, int g,
+                                         int t)
 {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int n = nt * 8 + g;
-        if (n < gcnt) {
-            const uint16_t *src = p.hbuf + static_cast<size_t>(gbeg + n) * p.I + qg * 128 + t * 8;
+        const uint8_t *row = act + n * pitch + q * 256;
+        const int rpar = (gbeg + n) & 1;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) b[nt][v] = ldg_cg_v4(src + 32 * v);
-        } else {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) b[nt][v] = make_uint4(0, 0, 0, 0);
-        }
+        for (int v = 0; v < 4; ++v) b[nt][v] = *reinterpret_cast<const uint4 *>(row + act_granule(v, t, rpar) * 16);
     }
+}
+
+// bf16 -> fp16 of 8 values (exact inside the fp16 range).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u)
+{
+    return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
 }
 
 // ------------------------------------------------------------------ consumer warps
 // Each of the eight consumer warps walks the stage ring on its own: it waits
-// for a stage's weights (bounded), computes its share of the ticket, and
-// releases the stage with one arrival.  No barrier spans warps; the only
-// cross-warp step is the reduction at the end of a ticket, done by whichever
-// warp arrives last while the others move on.
+// for a stage (bounded), computes its share -- K chunk ks = warp % 4 of rows
+// half = warp / 4 (gate/up: 16 gate and the same 16 up rows; down: 32 rows)
+// -- and releases the stage with one arrival.  Weights and activation rows
+// are both in the stage; no barrier spans warps except the reduction at the
+// end of each ticket.
 
 // Bounded wait on an mbarrier phase.  Every lane polls the barrier itself
 // (acquire); the verdict is made warp-uniform with a vote, so a lane that
@@ -603,18 +578,10 @@ __device__ __forceinline__ bool warp_spin(const KernelParams &p, Pred pred, vola
     return __all_sync(0xffffffffu, ok);
 }
 
-// Header of fill n_next if the producer has published it already (uniform).
-__device__ __forceinline__ bool peek_header(SmemHdr *hd, int s_next, int n_next, int4 &h)
-{
-    const bool ok = ld_acq_cta(&hd->hdr_seq[s_next]) == n_next + 1;
-    if (!__all_sync(0xffffffffu, ok)) return false;
-    h = hd->stage_hdr[s_next];
-    return true;
-}
-
 // Hand a finished ticket to the helper: slot = ticket sequence number.  The
-// warp's global stores precede the release through __syncwarp; the helper
-// releases them at gpu scope.
+// warp's global stores (and, through the acq_rel ticket counter, those of the
+// other seven warps) precede the release; the helper releases them at gpu
+// scope.
 __device__ __forceinline__ bool push_done(const KernelParams &p, SmemHdr *hd, int tick, int kind, int grp, int tile,
                                           int lane, volatile int *abort_flag)
 {
@@ -632,15 +599,15 @@ __device__ __forceinline__ bool push_done(const KernelParams &p, SmemHdr *hd, in
     return true;
 }
 
-// End of a ticket.  Every warp leaves its fp32 partial sums (its K-slice of
-// the ticket's rows) in one of two reduction buffers and arrives on that
-// buffer's mbarrier; once all eight have arrived (bounded wait), each warp
-// reduces one eighth of the outputs in a fixed order (warp 0 first), applies
-// the tensor scales (ts0, ts1: gate and up, or down and unused) and writes
-// its share of h (gate/up ticket) or of the per-pair down outputs (down
-// ticket).  The last warp to finish queues the ticket for the helper.  A
-// buffer is rewritten two tickets later, by which time every warp has passed
-// the other buffer's barrier, i.e. has finished reading this one.
+// End of a ticket.  Every warp leaves its fp32 partial sums (its K chunk of
+// its rows) in one of two reduction buffers and arrives on that buffer's
+// mbarrier; once all eight have arrived (bounded wait), each warp reduces one
+// eighth of the outputs over the four K chunks in a fixed order, applies the
+// tensor scales (ts0, ts1: gate and up, or down and unused) and writes its
+// share of h (gate/up ticket) or of the per-pair down outputs (down ticket).
+// The last warp to finish queues the ticket for the helper.  A buffer is
+// rewritten two tickets later, by which time every warp has passed the other
+// buffer's barrier, i.e. has finished reading this one.
 template <int NT, bool NULLM>
 __device__ __forceinline__ bool finish_ticket(const KernelParams &p, const Tabs &tb, float4 *red,
                                               const float (&acc)[2][NT][4], bool isA, int grp, int tile, int tick,
@@ -649,7 +616,7 @@ __device__ __forceinline__ bool finish_ticket(const KernelParams &p, const Tabs 
     SmemHdr *hd = tb.hdr;
     const int b = tick & 1;
     float4 *rb = red + b * (16 * NT * 32);
-    const int base = isA ? warp * 2 : (warp & 3) * 4 + (warp >> 2) * 2;
+    const int base = (warp & 3) * 4 + (warp >> 2) * 2;  // slot (ks, half, mt) = ks*4 + half*2 + mt
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -662,29 +629,33 @@ __device__ __forceinline__ bool finish_ticket(const KernelParams &p, const Tabs 
     const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
     const float *redf = reinterpret_cast<const float *>(rb);
     if (isA) {
-        // h[n][i0 + row] = SiLU(g) * u: this warp's 16*NT of the 16 rows x 8*NT pairs
-        const int idx = warp * (16 * NT) + lane;
-        if (lane < 16 * NT) {
-            const int nt = idx >> 7, ls = (idx >> 2) & 31, r = idx & 3;
-            const int row = (ls >> 2) + 8 * (r >> 1);
+        // h[n][i0 + half*16 + row] = SiLU(g) * u: this warp's NT*32 of the 32 rows x 8*NT pairs
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const int idx = warp * (32 * NT) + j * 32 + lane;
+            const int half = idx / (NT * 128), rem = idx - half * (NT * 128);
+            const int nt = rem >> 7, ls = (rem >> 2) & 31, r = rem & 3;
+            const int row = half * 16 + (ls >> 2) + 8 * (r >> 1);
             const int n = nt * 8 + 2 * (ls & 3) + (r & 1);
             if (n < gcnt) {
                 float sg = 0.f, su = 0.f;
 #pragma unroll
-                for (int k2 = 0; k2 < kConsumerWarps; ++k2) {
-                    sg += redf[(((k2 * 2 + 0) * NT + nt) * 32 + ls) * 4 + r];
-                    su += redf[(((k2 * 2 + 1) * NT + nt) * 32 + ls) * 4 + r];
+                for (int k2 = 0; k2 < 4; ++k2) {
+                    sg += redf[(((k2 * 4 + half * 2 + 0) * NT + nt) * 32 + ls) * 4 + r];
+                    su += redf[(((k2 * 4 + half * 2 + 1) * NT + nt) * 32 + ls) * 4 + r];
                 }
                 const float gv = sg * ts0, uv = su * ts1;
                 float v = gv / (1.0f + __expf(-gv)) * uv;
                 if (NULLM) v = 0.f;
                 if (!(fabsf(v) <= 65504.0f)) atomicOr(p.ctrl + 2, kErrRange);
-                p.hbuf[static_cast<size_t>(gbeg + n) * p.I + h_index(p.nib_mode, tile * 16 + row)] =
+                const int kh = tile * kRA + row, pb = kh / p.KB, kk = kh - pb * p.KB;
+                const int rr = gbeg + n;
+                p.hbuf[(static_cast<size_t>(pb) * p.Pmax + rr) * p.KB + act_index(p.nib_mode, kk, rr & 1)] =
                     __half_as_ushort(__float2half_rn(v));
             }
         }
     } else {
-        // per-pair down outputs of rows h0 .. h0+63: this warp's 64*NT, sum of the 4 K-slices
+        // per-pair down outputs of rows h0 .. h0+63: this warp's 64*NT, sum of the 4 K chunks
         const int h0 = tile * kMB;
 #pragma unroll
         for (int j = 0; j < 2 * NT; ++j) {
@@ -710,19 +681,59 @@ __device__ __forceinline__ bool finish_ticket(const KernelParams &p, const Tabs 
     return push_done(p, hd, tick, isA ? KIND_A : KIND_B, grp, tile, lane, abort_flag);
 }
 
+__device__ __forceinline__ void consumer_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+}
+
+// Gather x into sorted pair order as fp16 in the activation layout.  Rows
+// are claimed in batches from a global counter, so whichever CTAs run first
+// do the work and no CTA depends on another being resident; the rows written
+// are then published with a gpu-scope release (counter word 3).  Run by the
+// eight consumer warps while the first weight copies are in flight.
+__device__ __forceinline__ void gather_x(const KernelParams &p, const Tabs &tb)
+{
+    SmemHdr *hd = tb.hdr;
+    const int nv = hd->n_valid, tid = threadIdx.x;
+    const int batch = (nv + gridDim.x - 1) / gridDim.x;
+    int mine = 0;
+    for (;;) {
+        if (tid == 0) hd->claim = nv ? static_cast<int>(atomicAdd(p.ctrl + 4, static_cast<uint32_t>(batch))) : 0;
+        consumer_sync();
+        const int c = hd->claim;
+        consumer_sync();
+        if (c >= nv) break;
+        const int c_end = min(c + batch, nv);
+        for (int r = c; r < c_end; ++r) {
+            const uint16_t *src = p.x + static_cast<size_t>(tb.stok[r]) * p.H;
+            for (int k8 = tid * 8; k8 < p.H; k8 += kConsumerThreads * 8) {
+                const int pa = k8 / p.KA, kk = k8 - pa * p.KA;
+                const uint4 v = bf16x8_to_f16x8(*reinterpret_cast<const uint4 *>(src + k8));
+                *reinterpret_cast<uint4 *>(p.xs + (static_cast<size_t>(pa) * p.Pmax + r) * p.KA +
+                                           act_index(p.nib_mode, kk, r & 1)) = v;
+            }
+        }
+        mine += c_end - c;
+    }
+    if (mine) {
+        __threadfence();
+        consumer_sync();
+        if (tid == 0) atomicAdd(p.ctrl + 3, static_cast<uint32_t>(mine));
+    }
+}
+
 template <int NT, bool NULLM>
 __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *smem, const Tabs &tb,
                                               volatile int *abort_flag)
 {
+    gather_x(p, tb);
     SmemHdr *hd = tb.hdr;
     float4 *red = reinterpret_cast<float4 *>(smem + p.red_off);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int ks = warp & 3, half = warp >> 2;
     const int chunksA = p.KA / 128, chunksB = p.KB / 128;
-    const int ksB = warp & 3, mgB = warp >> 2;  // down: 4 K-slices x 2 groups of 32 rows
-    int s = 0, n = 0, tick = 0;
+    int s = 0, tick = 0;
     uint32_t ph = 0;
-    uint4 nb[NT][4];     // B operand of this warp's first task in fill n, if loaded ahead
-    bool have_nb = false;
     float ts0 = 0.f, ts1 = 0.f;  // the ticket's tensor scales, loaded at its first part
     float acc[2][NT][4];
 #pragma unroll
@@ -744,81 +755,41 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
             ts0 = __ldg(isA ? p.gts + e : p.dts + e);
             ts1 = isA ? __ldg(p.uts + e) : 0.f;
         }
-        if (!isA && !have_nb &&
-            !warp_spin(p, [&] { return ld_acq_cta_u8(tb.hready + grp) == 2; }, abort_flag))
-            break;
         const uint8_t *st = smem + s * p.stage_bytes;
-        // this warp's tasks: gate/up chunk q (rows g, g+8 of gate and of up),
-        // or down chunk q of the 32 rows mgB*32 .. +31
-        auto load_w = [&](int q, uint4 (&ra)[2], uint4 (&rb)[2], uint16_t (&s_a)[2], uint16_t (&s_b)[2]) {
-            const int ko = k_off(p.nib_mode, q, t);
-            if (isA) {
+        if (isA) {
+            for (int q = ks; q < chunksA; q += 4) {
+                uint4 ra[2], rb[2], bq[NT][4];
+                uint16_t s_a[2], s_b[2];
+                const int ko = k_off(p.nib_mode, q, t);
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {  // m-tile 0: gate rows, 1: up rows
+                for (int mt = 0; mt < 2; ++mt) {  // m-tile 0: gate rows, 1: up rows (same 16 rows)
                     const uint8_t *nbp = st + (mt ? p.offUq : p.offGq);
-                    ra[mt] = *reinterpret_cast<const uint4 *>(nbp + nib_off(p.nib_mode, 16, g, q, t));
-                    rb[mt] = *reinterpret_cast<const uint4 *>(nbp + nib_off(p.nib_mode, 16, g + 8, q, t));
+                    const int r0 = half * 16 + g;
+                    ra[mt] = *reinterpret_cast<const uint4 *>(nbp + nib_off(p.nib_mode, kRA, r0, q, t));
+                    rb[mt] = *reinterpret_cast<const uint4 *>(nbp + nib_off(p.nib_mode, kRA, r0 + 8, q, t));
                     const uint8_t *sbp = st + (mt ? p.offUs : p.offGs);
-                    s_a[mt] = scale_pair(sbp, p.spA, p.shA, p.mkA, g, ko);
-                    s_b[mt] = scale_pair(sbp, p.spA, p.shA, p.mkA, g + 8, ko);
+                    s_a[mt] = scale_pair(sbp, p.spA, p.shA, p.mkA, r0, ko);
+                    s_b[mt] = scale_pair(sbp, p.spA, p.shA, p.mkA, r0 + 8, ko);
                 }
-            } else {
+                load_act<NT>(bq, st + p.offAa, 2 * p.KA, q, gbeg, g, t);
+                chunk_math<2, NT, false, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
+            }
+        } else {
+            for (int q = ks; q < chunksB; q += 4) {
+                uint4 ra[2], rb[2], bq[NT][4];
+                uint16_t s_a[2], s_b[2];
+                const int ko = k_off(p.nib_mode, q, t);
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
-                    const int r0 = mgB * 32 + mt * 16 + g;
+                    const int r0 = half * 32 + mt * 16 + g;
                     ra[mt] = *reinterpret_cast<const uint4 *>(st + p.offDq + nib_off(p.nib_mode, kMB, r0, q, t));
                     rb[mt] = *reinterpret_cast<const uint4 *>(st + p.offDq + nib_off(p.nib_mode, kMB, r0 + 8, q, t));
                     s_a[mt] = scale_pair(st + p.offDs, p.spB, p.shB, p.mkB, r0, ko);
                     s_b[mt] = scale_pair(st + p.offDs, p.spB, p.shB, p.mkB, r0 + 8, ko);
                 }
+                load_act<NT>(bq, st + p.offAb, 2 * p.KB, q, gbeg, g, t);
+                chunk_math<2, NT, false, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
             }
-        };
-        const int q0 = isA ? warp : ksB, qstep = isA ? kConsumerWarps : 4, qend = isA ? chunksA : chunksB;
-        uint4 ra[2], rb[2], bq[NT][4];
-        uint16_t s_a[2], s_b[2];
-        // (one n-tile: the first task's weight reads go out before the
-        // look-ahead below and overlap it; two n-tiles: after it, which keeps
-        // the live registers within the 168 three warps per SMSP allow)
-        if (q0 < qend) {
-            if (NT == 1) load_w(q0, ra, rb, s_a, s_b);
-            if (have_nb) {
-#pragma unroll
-                for (int a = 0; a < NT; ++a)
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) bq[a][v] = nb[a][v];
-            } else if (isA) {
-                load_x<NT>(bq, p, tb, gbeg, gcnt, part * p.KA + k_off(p.nib_mode, q0, t), g);
-            } else {
-                load_h<NT>(bq, p, gbeg, gcnt, part * chunksB + q0, g, t);
-            }
-        }
-        // look one fill ahead and start its B-operand loads now
-        {
-            const int s2 = s + 1 == p.NS ? 0 : s + 1;
-            int4 h2;
-            have_nb = false;
-            if (peek_header(hd, s2, n + 1, h2) && h2.x != KIND_END) {
-                const bool a2 = h2.x == KIND_A;
-                const int gb2 = tb.gbeg[h2.y], gc2 = tb.gcnt[h2.y];
-                if (a2 && warp < chunksA) {
-                    load_x<NT>(nb, p, tb, gb2, gc2, h2.w * p.KA + k_off(p.nib_mode, warp, t), g);
-                    have_nb = true;
-                } else if (!a2 && ksB < chunksB &&
-                           __all_sync(0xffffffffu, ld_acq_cta_u8(tb.hready + h2.y) == 2)) {
-                    load_h<NT>(nb, p, gb2, gc2, h2.w * chunksB + ksB, g, t);
-                    have_nb = true;
-                }
-            }
-        }
-        if (NT != 1 && q0 < qend) load_w(q0, ra, rb, s_a, s_b);
-        for (int q = q0; q < qend; q += qstep) {
-            if (q != q0) {
-                load_w(q, ra, rb, s_a, s_b);
-                if (isA) load_x<NT>(bq, p, tb, gbeg, gcnt, part * p.KA + k_off(p.nib_mode, q, t), g);
-                else load_h<NT>(bq, p, gbeg, gcnt, part * chunksB + q, g, t);
-            }
-            if (isA) chunk_math<2, NT, true, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
-            else chunk_math<2, NT, false, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
         }
         // release the stage
         __syncwarp();
@@ -827,7 +798,6 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
             s = 0;
             ph ^= 1u;
         }
-        ++n;
         if (part == (isA ? p.nPA : p.nPB) - 1) {
             if (!finish_ticket<NT, NULLM>(p, tb, red, acc, isA, grp, tile, tick, ts0, ts1, warp, lane, abort_flag))
                 break;
@@ -845,13 +815,11 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
 }
 
 // ------------------------------------------------------------------ tickets
-// Ticket order: all gate/up tickets (group-major: the TA 16-row tiles of group
+// Ticket order: all gate/up tickets (group-major: the TA 32-row tiles of group
 // 0, then group 1, ...), then all down tickets (group-major: the nB 64-row
 // tiles of each group).  Every gate/up ticket precedes every down ticket, so
 // each down ticket's dependency is held by a running CTA when it is handed
-// out, and by then most groups' h rows are long complete: the down phase
-// starts while the last gate/up tickets finish, with no idle dependency wait
-// in the steady state.
+// out, and by then most groups' h rows are long complete.
 struct TicketInfo {
     int isA, grp, tile;
 };
@@ -869,11 +837,12 @@ __device__ __forceinline__ TicketInfo decode_ticket(int t, int n, int TA, int nB
 }
 
 // ------------------------------------------------------------------ producer warp
-// Lane 0 finds free stages and issues each part's weight boxes: for a gate/up
-// part the 16 gate rows and 16 up rows (E2M1 and E4M3), for a down part 64
-// down rows.  The stage header is published (hdr_seq) before the copies, so
-// the consumers can start the part's activation loads while the weights are
-// still in flight.  Tickets come from the helper, which fetches them ahead.
+// Lane 0 finds free stages and issues each part's copies: the weight boxes
+// (gate/up part: 32 gate rows and the same 32 up rows, E2M1 and E4M3; down
+// part: 64 down rows), and for a gate/up part the group's x rows once the
+// gathered x is complete.  The other activation copies (x before that, h of
+// every down part, which exists only once all gate/up tickets of its group
+// are done) go to the helper's queue.  The stage barrier expects them all.
 __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb,
                                               volatile int *abort_flag)
 {
@@ -881,12 +850,13 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
     SmemHdr *hd = tb.hdr;
     const uint64_t pol = policy_evict_first();
     const int ng = hd->n_groups;
-    const int TA = p.I / 16;
+    const int TA = p.I / kRA;
     const int total = ng * (TA + p.nHt);
-    const uint32_t wbytesA = 32u * (p.KA / 2) + 32u * (p.KA / 16);
+    const uint32_t wbytesA = 2u * kRA * (p.KA / 2) + 2u * kRA * (p.KA / 16);
     const uint32_t wbytesB = kMB * (p.KB / 2) + kMB * (p.KB / 16);
     bool ok = true;
-    int s = 0, fill = 0;
+    bool x_ok = false;  // gathered x seen complete (and ordered before our bulk copies)
+    int s = 0, fill = 0, pq_tail = 0;
     uint32_t ph = 0;
     int ticket = blockIdx.x;
     // a bounded wait for a condition polled by lane 0; false on abort/timeout
@@ -912,7 +882,7 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
         const TicketInfo ti = decode_ticket(ticket, ng, TA, p.nHt);
         const bool isA = ti.isA != 0;
         const int grp = ti.grp, tile = ti.tile;
-        const int e = tb.gexp[grp];
+        const int e = tb.gexp[grp], gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
         const int nparts = isA ? p.nPA : p.nPB;
         for (int part = 0; part < nparts; ++part) {
             if (!lane0_wait([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
@@ -922,12 +892,13 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
             if (lane == 0) {
                 uint8_t *st = smem + s * p.stage_bytes;
                 uint64_t *bar = &hd->full[s];
+                const int KP = isA ? p.KA : p.KB;
+                const uint32_t abytes = static_cast<uint32_t>(gcnt) * 2u * KP;
                 hd->stage_hdr[s] = make_int4(isA ? KIND_A : KIND_B, grp, tile, part);
-                st_rel_cta(&hd->hdr_seq[s], fill + 1);
-                mbar_expect_tx(bar, isA ? wbytesA : wbytesB);
+                mbar_expect_tx(bar, (isA ? wbytesA : wbytesB) + abytes);
                 if (isA) {
-                    // gate rows i0..i0+15 and up rows i0..i0+15, K elements part*KA ..
-                    const int row = e * p.I + tile * 16;
+                    // gate rows i0..i0+31 and up rows i0..i0+31, K elements part*KA ..
+                    const int row = e * p.I + tile * kRA;
                     const int nsp = p.KA / 128;
                     for (int m = 0; m < 2; ++m) {
                         uint8_t *nd = st + (m ? p.offUq : p.offGq);
@@ -936,14 +907,24 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
                             tma3d(nd, tq, 0, row, part * nsp, bar, pol);
                         } else {
                             for (int b2 = 0; b2 < p.KA / 256; ++b2)
-                                tma2d(nd + b2 * 16 * 128, tq, part * (p.KA / 2) + b2 * 128, row, bar, pol);
+                                tma2d(nd + b2 * kRA * 128, tq, part * (p.KA / 2) + b2 * 128, row, bar, pol);
                         }
                         uint8_t *sd = st + (m ? p.offUs : p.offGs);
                         if (p.scale_tmaA)
                             tma2d(sd, &p.tm[3 + m], part * (p.KA / 16), row, bar, pol);
                         else
-                            bulk_g2s(sd, (m ? p.us : p.gs) + static_cast<size_t>(row) * (p.H / 16), 16 * (p.H / 16),
-                                     bar, pol);
+                            bulk_g2s(sd, (m ? p.us : p.gs) + static_cast<size_t>(row) * (p.H / 16),
+                                     kRA * (p.H / 16), bar, pol);
+                    }
+                    if (!x_ok && ld_acq_cta(&hd->xready)) {
+                        // x was gathered by other CTAs' generic stores: order them
+                        // before this thread's async-proxy reads
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        x_ok = true;
+                    }
+                    if (x_ok) {
+                        bulk_g2s(st + p.offAa, p.xs + (static_cast<size_t>(part) * p.Pmax + gbeg) * p.KA, abytes, bar,
+                                 pol);
                     }
                 } else {
                     // down rows h0..h0+63, K elements part*KB ..
@@ -961,8 +942,18 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
                         bulk_g2s(st + p.offDs, p.ds + static_cast<size_t>(row) * (p.I / 16), kMB * (p.I / 16), bar,
                                  pol);
                 }
+                if (!isA || !x_ok) {
+                    // activation rows: the helper copies them when they exist
+                    const int slot = pq_tail % kMaxStages;
+                    hd->pq_stage[slot] = s;
+                    hd->pq_grp[slot] = grp;
+                    hd->pq_part[slot] = part;
+                    hd->pq_kind[slot] = isA ? KIND_A : KIND_B;
+                    st_rel_cta(&hd->pq_tail, pq_tail + 1);
+                    ++pq_tail;
+                }
             }
-            __syncwarp();
+            pq_tail = __shfl_sync(0xffffffffu, pq_tail, 0);
             ++fill;
             if (++s == p.NS) {
                 s = 0;
@@ -975,19 +966,18 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
             ok = false;
             break;
         }
-        int t = 0;
+        int tn = 0;
         if (lane == 0) {
-            t = hd->tq_buf[tq_head % kTq];
+            tn = hd->tq_buf[tq_head % kTq];
             st_rel_cta(&hd->tq_head, tq_head + 1);
         }
         ++tq_head;
-        ticket = __shfl_sync(0xffffffffu, t, 0);
+        ticket = __shfl_sync(0xffffffffu, tn, 0);
     }
     // end marker (the consumers' waits also end on the abort flag)
     if (ok && lane0_wait([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
         if (lane == 0) {
             hd->stage_hdr[s] = make_int4(KIND_END, 0, 0, 0);
-            st_rel_cta(&hd->hdr_seq[s], fill + 1);
             mbar_arrive(&hd->full[s]);
         }
         ++fill;
@@ -1003,23 +993,26 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
 // neither the producer's copy issue nor the consumers' math ever stalls on a
 // global round trip:
 //   * fetch tickets from the global counter, up to kTq ahead of the producer;
-//   * for every down ticket this CTA will run, poll its group's gate/up
-//     counter (acquire, gpu scope) and flag the group's h rows complete in
-//     shared memory (each lane watches one group);
+//   * watch the gathered-x counter, and for every down ticket this CTA will
+//     run its group's gate/up counter (acquire, gpu scope; each lane watches
+//     one group), flagging completion in shared memory;
+//   * copy the queued stages' activation rows once they exist (after an
+//     async-proxy fence: the rows were written through the generic proxy);
 //   * release finished work in ticket order: a gpu-scope fence, then bump the
 //     group's gate/up counter (gate/up ticket) or the per-(token, 64-row tile)
 //     arrival counters (down ticket); the CTA that completes a token's tile
 //     sums its k per-pair outputs in slot order and writes y -- no
 //     floating-point atomics, so the result is the same bits every run.
-__device__ __forceinline__ void helper_loop(const KernelParams &p, Tabs tb, volatile int *abort_flag)
+__device__ __forceinline__ void helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, volatile int *abort_flag)
 {
     const int lane = threadIdx.x & 31;
     SmemHdr *hd = tb.hdr;
-    const int ng = hd->n_groups;
-    const int TA = p.I / 16;
+    const uint64_t pol = policy_evict_first();
+    const int ng = hd->n_groups, nvalid = hd->n_valid;
+    const int TA = p.I / kRA;
     const int total = ng * (TA + p.nHt);
-    bool fetch_done = false;
-    int tq_tail = 0, dq_head = 0;
+    bool fetch_done = false, xr = false;
+    int tq_tail = 0, dq_head = 0, pq_head = 0;
     int watch = -1;  // the group this lane polls (-1: none)
     uint64_t idle_since = 0;
     // a down ticket's group goes on the watch list once (hready 0 -> 1)
@@ -1054,14 +1047,43 @@ __device__ __forceinline__ void helper_loop(const KernelParams &p, Tabs tb, vola
             else note_ticket(tk);
             progress = true;
         }
-        // 2) groups whose gate/up tickets are all done: their h rows may be read
+        // 2) the gathered x, and groups whose gate/up tickets are all done
+        if (!xr) {
+            int done = 0;
+            if (lane == 0) done = ld_acquire(p.ctrl + 3) >= static_cast<uint32_t>(nvalid);
+            if (__shfl_sync(0xffffffffu, done, 0)) {
+                xr = true;
+                if (lane == 0) st_rel_cta(&hd->xready, 1);
+                progress = true;
+            }
+        }
         if (watch >= 0 && ld_acquire(p.doneA + watch) == static_cast<uint32_t>(TA)) {
             st_rel_cta_u8(tb.hready + watch, 2);
             watch = -1;
             progress = true;
         }
         progress = __any_sync(0xffffffffu, progress);
-        // 3) release finished tickets, in ticket order
+        // 3) queued activation copies, in order, as soon as their rows exist
+        for (;;) {
+            const int pq_tail = __shfl_sync(0xffffffffu, ld_acq_cta(&hd->pq_tail), 0);
+            if (pq_head == pq_tail) break;
+            const int slot = pq_head % kMaxStages;
+            const int kind = hd->pq_kind[slot], grp = hd->pq_grp[slot];
+            const bool ready = kind == KIND_A ? xr : (ld_acq_cta_u8(tb.hready + grp) == 2);
+            if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                const int st = hd->pq_stage[slot], part = hd->pq_part[slot];
+                const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
+                uint8_t *dst = smem + st * p.stage_bytes + (kind == KIND_A ? p.offAa : p.offAb);
+                const int KP = kind == KIND_A ? p.KA : p.KB;
+                const uint16_t *src = (kind == KIND_A ? p.xs : p.hbuf) + (static_cast<size_t>(part) * p.Pmax + gbeg) * KP;
+                bulk_g2s(dst, src, static_cast<uint32_t>(gcnt) * 2u * KP, &hd->full[st], pol);
+            }
+            ++pq_head;
+            progress = true;
+        }
+        // 4) release finished tickets, in ticket order
         const int exited = __shfl_sync(0xffffffffu, ld_acq_cta(&hd->cons_exited), 0);
         for (;;) {
             const int slot = dq_head % kDoneQ;
@@ -1107,9 +1129,9 @@ __device__ __forceinline__ void helper_loop(const KernelParams &p, Tabs tb, vola
             if (lane == 0) st_rel_cta(&hd->dq_head, dq_head);
             progress = true;
         }
-        // 4) done when every consumer warp has left and its last ticket is released
+        // 5) done when every consumer warp has left and its last ticket is released
         if (exited == kConsumerWarps) break;
-        // 5) bounded idleness
+        // 6) bounded idleness
         if (progress) {
             idle_since = 0;
         } else {
@@ -1149,16 +1171,18 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
         for (int i = 0; i < p.NS; ++i) {
             mbar_init(&hd->full[i], 1);
             mbar_init(&hd->empty[i], kConsumerWarps);
-            hd->hdr_seq[i] = 0;
         }
+        mbar_init(&hd->redbar[0], kConsumerWarps);
+        mbar_init(&hd->redbar[1], kConsumerWarps);
         hd->abort_flag = 0;
         hd->fill_cnt = 0;
         hd->cons_exited = 0;
         hd->red_cnt = 0;
-        mbar_init(&hd->redbar[0], kConsumerWarps);
-        mbar_init(&hd->redbar[1], kConsumerWarps);
+        hd->xready = 0;
         hd->tq_head = hd->tq_tail = 0;
         hd->dq_head = 0;
+        hd->pq_head = hd->pq_tail = 0;
+        hd->claim = 0;
         for (int i = 0; i < kDoneQ; ++i) hd->dq_seq[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1214,7 +1238,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
     }
 
     if (tid >= kConsumerThreads + 32) {
-        helper_loop(p, tb, abort_flag);
+        helper_loop(p, smem, tb, abort_flag);
     } else if (tid >= kConsumerThreads) {
         producer_loop(p, smem, tb, abort_flag);
     } else {
@@ -1252,6 +1276,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
             }
             p.ctrl[0] = 0u;
             p.ctrl[1] = 0u;
+            p.ctrl[3] = 0u;
+            p.ctrl[4] = 0u;
             __threadfence();
         }
     }
