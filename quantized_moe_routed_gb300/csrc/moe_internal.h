@@ -9,10 +9,11 @@
 namespace moe {
 
 // CTA shape of the persistent ticket kernel: 8 consumer warps, 1 producer warp
-// (weight copy issue), 1 helper warp (tickets, cross-CTA counters, combine).
+// (copy issue), 1 helper warp (tickets, dependency watch, activation copies),
+// 1 release warp (cross-CTA counters, combine).
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 64;
+constexpr int kThreads = kConsumerThreads + 96;
 constexpr int kMaxPairs = 4096;     // T*k per launch (prefill is chunked to this)
 constexpr int kGroupPairs = 16;     // pairs per expert group, at most 2 MMA n-tiles of 8
 constexpr int kMaxTopK = 16;

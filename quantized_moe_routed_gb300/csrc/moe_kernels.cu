@@ -258,7 +258,10 @@ struct SmemHdr {
 };
 static_assert(sizeof(SmemHdr) <= kTabHdrBytes, "header too large");
 
-enum { KIND_A = 0, KIND_B = 1, KIND_END = 2 };
+// KIND_AX: a gate/up part whose x rows are not in the stage (the gathered x
+// was not yet published when it was issued): the consumers read them from
+// the caller's bf16 x instead.
+enum { KIND_A = 0, KIND_B = 1, KIND_END = 2, KIND_AX = 3 };
 
 struct Tabs {
     SmemHdr *hdr;
@@ -529,6 +532,34 @@ __device__ __forceinline__ void load_act(uint4 (&b)[NT][4], const uint8_t *act, 
     }
 }
 
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *ptr)
+{
+    uint4 v;
+    asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(ptr));
+    return v;
+}
+
+// The B operand of a gate/up chunk straight from the caller's bf16 x (read
+// only for the whole step): pair n = nt*8 + g of the group, the 32 elements
+// of this thread from K position kglob.  Pairs past the group's end are 0.
+template <int NT>
+__device__ __forceinline__ void load_x_direct(uint4 (&b)[NT][4], const KernelParams &p, const Tabs &tb, int gbeg,
+                                              int gcnt, int kglob, int g)
+{
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int n = nt * 8 + g;
+        if (n < gcnt) {
+            const uint16_t *src = p.x + static_cast<size_t>(tb.stok[gbeg + n]) * p.H + kglob;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) b[nt][v] = ldg_nc_v4(src + 8 * v);
+        } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) b[nt][v] = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
 // bf16 -> fp16 of 8 values (exact inside the fp16 range).
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u)
 {
@@ -747,7 +778,7 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
         if (!warp_wait_bar(p, &hd->full[s], ph, abort_flag)) break;
         const int4 h = hd->stage_hdr[s];
         if (h.x == KIND_END) break;
-        const bool isA = h.x == KIND_A;
+        const bool isA = h.x != KIND_B, xdirect = h.x == KIND_AX;
         const int grp = h.y, tile = h.z, part = h.w;
         const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
         if (part == 0) {
@@ -771,8 +802,13 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
                     s_a[mt] = scale_pair(sbp, p.spA, p.shA, p.mkA, r0, ko);
                     s_b[mt] = scale_pair(sbp, p.spA, p.shA, p.mkA, r0 + 8, ko);
                 }
-                load_act<NT>(bq, st + p.offAa, 2 * p.KA, q, gbeg, g, t);
-                chunk_math<2, NT, false, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
+                if (xdirect) {
+                    load_x_direct<NT>(bq, p, tb, gbeg, gcnt, part * p.KA + ko, g);
+                    chunk_math<2, NT, true, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
+                } else {
+                    load_act<NT>(bq, st + p.offAa, 2 * p.KA, q, gbeg, g, t);
+                    chunk_math<2, NT, false, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
+                }
             }
         } else {
             for (int q = ks; q < chunksB; q += 4) {
@@ -837,16 +873,17 @@ __device__ __forceinline__ TicketInfo decode_ticket(int t, int n, int TA, int nB
 }
 
 // ------------------------------------------------------------------ producer warp
-// Lane 0 finds free stages and issues each part's copies: the weight boxes
-// (gate/up part: 32 gate rows and the same 32 up rows, E2M1 and E4M3; down
-// part: 64 down rows), and for a gate/up part the group's x rows once the
-// gathered x is complete.  The other activation copies (x before that, h of
-// every down part, which exists only once all gate/up tickets of its group
-// are done) go to the helper's queue.  The stage barrier expects them all.
+// Lane 0 alone finds free stages and issues each part's copies: the weight
+// boxes (gate/up part: 32 gate rows and the same 32 up rows, E2M1 and E4M3;
+// down part: 64 down rows), and for a gate/up part the group's x rows from the
+// gathered x.  Until that gather is published, gate/up parts go out without
+// their x rows (KIND_AX) and the consumers read x directly.  A down part's h
+// rows exist only once all gate/up tickets of its group are done: those
+// copies go to the helper's queue.  The stage barrier expects every byte.
 __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb,
                                               volatile int *abort_flag)
 {
-    const int lane = threadIdx.x & 31;
+    if ((threadIdx.x & 31) != 0) return;
     SmemHdr *hd = tb.hdr;
     const uint64_t pol = policy_evict_first();
     const int ng = hd->n_groups;
@@ -854,106 +891,94 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
     const int total = ng * (TA + p.nHt);
     const uint32_t wbytesA = 2u * kRA * (p.KA / 2) + 2u * kRA * (p.KA / 16);
     const uint32_t wbytesB = kMB * (p.KB / 2) + kMB * (p.KB / 16);
+    const int nspA = p.KA / 128, nspB = p.KB / 128;
     bool ok = true;
     bool x_ok = false;  // gathered x seen complete (and ordered before our bulk copies)
-    int s = 0, fill = 0, pq_tail = 0;
+    int s = 0, fill = 0, pq_tail = 0, tq_head = 0;
     uint32_t ph = 0;
     int ticket = blockIdx.x;
-    // a bounded wait for a condition polled by lane 0; false on abort/timeout
-    auto lane0_wait = [&](auto &&cond) -> bool {
-        int got = 0;
-        if (lane == 0) {
-            const uint64_t t0 = gtimer();
-            for (uint32_t it = 0;; ++it) {
-                if (cond()) { got = 1; break; }
-                if ((it & 15u) == 15u) {
-                    if (*abort_flag) break;
-                    if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
-                        raise_error(p, abort_flag, kErrTimeout);
-                        break;
-                    }
+    // a bounded wait for cond(); false on abort/timeout
+    auto wait_for = [&](auto &&cond) -> bool {
+        if (cond()) return true;  // the common case: no timer read
+        const uint64_t t0 = gtimer();
+        for (uint32_t it = 0;; ++it) {
+            if (cond()) return true;
+            if ((it & 15u) == 15u) {
+                if (*abort_flag) return false;
+                if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
+                    raise_error(p, abort_flag, kErrTimeout);
+                    return false;
                 }
             }
         }
-        return __shfl_sync(0xffffffffu, got, 0) != 0;
     };
-    int tq_head = 0;
     while (ok && ticket < total) {
         const TicketInfo ti = decode_ticket(ticket, ng, TA, p.nHt);
         const bool isA = ti.isA != 0;
         const int grp = ti.grp, tile = ti.tile;
         const int e = tb.gexp[grp], gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
         const int nparts = isA ? p.nPA : p.nPB;
+        const int KP = isA ? p.KA : p.KB;
+        const uint32_t abytes = static_cast<uint32_t>(gcnt) * 2u * KP;
+        const int row = isA ? e * p.I + tile * kRA : e * p.H + tile * kMB;
         for (int part = 0; part < nparts; ++part) {
-            if (!lane0_wait([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
+            if (!wait_for([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
                 ok = false;
                 break;
             }
-            if (lane == 0) {
-                uint8_t *st = smem + s * p.stage_bytes;
-                uint64_t *bar = &hd->full[s];
-                const int KP = isA ? p.KA : p.KB;
-                const uint32_t abytes = static_cast<uint32_t>(gcnt) * 2u * KP;
-                hd->stage_hdr[s] = make_int4(isA ? KIND_A : KIND_B, grp, tile, part);
-                mbar_expect_tx(bar, (isA ? wbytesA : wbytesB) + abytes);
-                if (isA) {
-                    // gate rows i0..i0+31 and up rows i0..i0+31, K elements part*KA ..
-                    const int row = e * p.I + tile * kRA;
-                    const int nsp = p.KA / 128;
-                    for (int m = 0; m < 2; ++m) {
-                        uint8_t *nd = st + (m ? p.offUq : p.offGq);
-                        const CUtensorMap *tq = &p.tm[m];
-                        if (p.nib_mode == 0) {
-                            tma3d(nd, tq, 0, row, part * nsp, bar, pol);
-                        } else {
-                            for (int b2 = 0; b2 < p.KA / 256; ++b2)
-                                tma2d(nd + b2 * kRA * 128, tq, part * (p.KA / 2) + b2 * 128, row, bar, pol);
-                        }
-                        uint8_t *sd = st + (m ? p.offUs : p.offGs);
-                        if (p.scale_tmaA)
-                            tma2d(sd, &p.tm[3 + m], part * (p.KA / 16), row, bar, pol);
-                        else
-                            bulk_g2s(sd, (m ? p.us : p.gs) + static_cast<size_t>(row) * (p.H / 16),
-                                     kRA * (p.H / 16), bar, pol);
-                    }
-                    if (!x_ok && ld_acq_cta(&hd->xready)) {
-                        // x was gathered by other CTAs' generic stores: order them
-                        // before this thread's async-proxy reads
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
-                        x_ok = true;
-                    }
-                    if (x_ok) {
-                        bulk_g2s(st + p.offAa, p.xs + (static_cast<size_t>(part) * p.Pmax + gbeg) * p.KA, abytes, bar,
-                                 pol);
-                    }
+            uint8_t *st = smem + s * p.stage_bytes;
+            uint64_t *bar = &hd->full[s];
+            if (isA) {
+                if (!x_ok && ld_acq_cta(&hd->xready)) {
+                    // x was gathered by other CTAs' generic stores: order them
+                    // before this thread's async-proxy reads
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    x_ok = true;
+                }
+                hd->stage_hdr[s] = make_int4(x_ok ? KIND_A : KIND_AX, grp, tile, part);
+                mbar_expect_tx(bar, wbytesA + (x_ok ? abytes : 0u));
+                // gate rows i0..i0+31 and up rows i0..i0+31, K elements part*KA ..
+                if (p.nib_mode == 0) {
+                    tma3d(st + p.offGq, &p.tm[0], 0, row, part * nspA, bar, pol);
+                    tma3d(st + p.offUq, &p.tm[1], 0, row, part * nspA, bar, pol);
                 } else {
-                    // down rows h0..h0+63, K elements part*KB ..
-                    const int row = e * p.H + tile * kMB;
-                    if (p.nib_mode == 0) {
-                        tma3d(st + p.offDq, &p.tm[2], 0, row, part * (p.KB / 128), bar, pol);
-                    } else {
-                        for (int b2 = 0; b2 < p.KB / 256; ++b2)
-                            tma2d(st + p.offDq + b2 * kMB * 128, &p.tm[2], part * (p.KB / 2) + b2 * 128, row, bar,
-                                  pol);
+                    for (int b2 = 0; b2 < p.KA / 256; ++b2) {
+                        tma2d(st + p.offGq + b2 * kRA * 128, &p.tm[0], part * (p.KA / 2) + b2 * 128, row, bar, pol);
+                        tma2d(st + p.offUq + b2 * kRA * 128, &p.tm[1], part * (p.KA / 2) + b2 * 128, row, bar, pol);
                     }
-                    if (p.scale_tmaB)
-                        tma2d(st + p.offDs, &p.tm[5], part * (p.KB / 16), row, bar, pol);
-                    else
-                        bulk_g2s(st + p.offDs, p.ds + static_cast<size_t>(row) * (p.I / 16), kMB * (p.I / 16), bar,
-                                 pol);
                 }
-                if (!isA || !x_ok) {
-                    // activation rows: the helper copies them when they exist
-                    const int slot = pq_tail % kMaxStages;
-                    hd->pq_stage[slot] = s;
-                    hd->pq_grp[slot] = grp;
-                    hd->pq_part[slot] = part;
-                    hd->pq_kind[slot] = isA ? KIND_A : KIND_B;
-                    st_rel_cta(&hd->pq_tail, pq_tail + 1);
-                    ++pq_tail;
+                if (p.scale_tmaA) {
+                    tma2d(st + p.offGs, &p.tm[3], part * (p.KA / 16), row, bar, pol);
+                    tma2d(st + p.offUs, &p.tm[4], part * (p.KA / 16), row, bar, pol);
+                } else {
+                    bulk_g2s(st + p.offGs, p.gs + static_cast<size_t>(row) * (p.H / 16), kRA * (p.H / 16), bar, pol);
+                    bulk_g2s(st + p.offUs, p.us + static_cast<size_t>(row) * (p.H / 16), kRA * (p.H / 16), bar, pol);
                 }
+                if (x_ok)
+                    bulk_g2s(st + p.offAa, p.xs + (static_cast<size_t>(part) * p.Pmax + gbeg) * p.KA, abytes, bar,
+                             pol);
+            } else {
+                hd->stage_hdr[s] = make_int4(KIND_B, grp, tile, part);
+                mbar_expect_tx(bar, wbytesB + abytes);
+                // down rows h0..h0+63, K elements part*KB ..
+                if (p.nib_mode == 0) {
+                    tma3d(st + p.offDq, &p.tm[2], 0, row, part * nspB, bar, pol);
+                } else {
+                    for (int b2 = 0; b2 < p.KB / 256; ++b2)
+                        tma2d(st + p.offDq + b2 * kMB * 128, &p.tm[2], part * (p.KB / 2) + b2 * 128, row, bar, pol);
+                }
+                if (p.scale_tmaB)
+                    tma2d(st + p.offDs, &p.tm[5], part * (p.KB / 16), row, bar, pol);
+                else
+                    bulk_g2s(st + p.offDs, p.ds + static_cast<size_t>(row) * (p.I / 16), kMB * (p.I / 16), bar, pol);
+                // the h rows: the helper copies them once they exist
+                const int slot = pq_tail % kMaxStages;
+                hd->pq_stage[slot] = s;
+                hd->pq_grp[slot] = grp;
+                hd->pq_part[slot] = part;
+                hd->pq_kind[slot] = KIND_B;
+                st_rel_cta(&hd->pq_tail, ++pq_tail);
             }
-            pq_tail = __shfl_sync(0xffffffffu, pq_tail, 0);
             ++fill;
             if (++s == p.NS) {
                 s = 0;
@@ -962,47 +987,33 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
         }
         if (!ok) break;
         // next ticket from the helper
-        if (!lane0_wait([&] { return ld_acq_cta(&hd->tq_tail) > tq_head; })) {
+        if (!wait_for([&] { return ld_acq_cta(&hd->tq_tail) > tq_head; })) {
             ok = false;
             break;
         }
-        int tn = 0;
-        if (lane == 0) {
-            tn = hd->tq_buf[tq_head % kTq];
-            st_rel_cta(&hd->tq_head, tq_head + 1);
-        }
-        ++tq_head;
-        ticket = __shfl_sync(0xffffffffu, tn, 0);
+        ticket = hd->tq_buf[tq_head % kTq];
+        st_rel_cta(&hd->tq_head, ++tq_head);
     }
     // end marker (the consumers' waits also end on the abort flag)
-    if (ok && lane0_wait([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
-        if (lane == 0) {
-            hd->stage_hdr[s] = make_int4(KIND_END, 0, 0, 0);
-            mbar_arrive(&hd->full[s]);
-        }
+    if (ok && wait_for([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
+        hd->stage_hdr[s] = make_int4(KIND_END, 0, 0, 0);
+        mbar_arrive(&hd->full[s]);
         ++fill;
-    } else if (lane == 0) {
+    } else {
         *abort_flag = 1;
     }
-    if (lane == 0) hd->fill_cnt = fill;
-    __syncwarp();
+    hd->fill_cnt = fill;
 }
 
 // ------------------------------------------------------------------ helper warp
-// Everything that waits on or publishes to other CTAs runs here, so that
-// neither the producer's copy issue nor the consumers' math ever stalls on a
-// global round trip:
+// Waits on other CTAs' progress so that neither the producer's copy issue nor
+// the consumers' math ever stalls on a global round trip:
 //   * fetch tickets from the global counter, up to kTq ahead of the producer;
 //   * watch the gathered-x counter, and for every down ticket this CTA will
 //     run its group's gate/up counter (acquire, gpu scope; each lane watches
 //     one group), flagging completion in shared memory;
-//   * copy the queued stages' activation rows once they exist (after an
-//     async-proxy fence: the rows were written through the generic proxy);
-//   * release finished work in ticket order: a gpu-scope fence, then bump the
-//     group's gate/up counter (gate/up ticket) or the per-(token, 64-row tile)
-//     arrival counters (down ticket); the CTA that completes a token's tile
-//     sums its k per-pair outputs in slot order and writes y -- no
-//     floating-point atomics, so the result is the same bits every run.
+//   * copy the queued down parts' h rows once they exist (after an
+//     async-proxy fence: the rows were written through the generic proxy).
 __device__ __forceinline__ void helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, volatile int *abort_flag)
 {
     const int lane = threadIdx.x & 31;
@@ -1012,7 +1023,7 @@ __device__ __forceinline__ void helper_loop(const KernelParams &p, uint8_t *smem
     const int TA = p.I / kRA;
     const int total = ng * (TA + p.nHt);
     bool fetch_done = false, xr = false;
-    int tq_tail = 0, dq_head = 0, pq_head = 0;
+    int tq_tail = 0, pq_head = 0;
     int watch = -1;  // the group this lane polls (-1: none)
     uint64_t idle_since = 0;
     // a down ticket's group goes on the watch list once (hready 0 -> 1)
@@ -1063,34 +1074,68 @@ __device__ __forceinline__ void helper_loop(const KernelParams &p, uint8_t *smem
             progress = true;
         }
         progress = __any_sync(0xffffffffu, progress);
-        // 3) queued activation copies, in order, as soon as their rows exist
+        // 3) queued h copies, in order, as soon as their rows exist
         for (;;) {
             const int pq_tail = __shfl_sync(0xffffffffu, ld_acq_cta(&hd->pq_tail), 0);
             if (pq_head == pq_tail) break;
             const int slot = pq_head % kMaxStages;
-            const int kind = hd->pq_kind[slot], grp = hd->pq_grp[slot];
-            const bool ready = kind == KIND_A ? xr : (ld_acq_cta_u8(tb.hready + grp) == 2);
-            if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;
+            const int grp = hd->pq_grp[slot];
+            if (!__shfl_sync(0xffffffffu, ld_acq_cta_u8(tb.hready + grp) == 2 ? 1 : 0, 0)) break;
             if (lane == 0) {
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 const int st = hd->pq_stage[slot], part = hd->pq_part[slot];
                 const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
-                uint8_t *dst = smem + st * p.stage_bytes + (kind == KIND_A ? p.offAa : p.offAb);
-                const int KP = kind == KIND_A ? p.KA : p.KB;
-                const uint16_t *src = (kind == KIND_A ? p.xs : p.hbuf) + (static_cast<size_t>(part) * p.Pmax + gbeg) * KP;
-                bulk_g2s(dst, src, static_cast<uint32_t>(gcnt) * 2u * KP, &hd->full[st], pol);
+                bulk_g2s(smem + st * p.stage_bytes + p.offAb,
+                         p.hbuf + (static_cast<size_t>(part) * p.Pmax + gbeg) * p.KB,
+                         static_cast<uint32_t>(gcnt) * 2u * p.KB, &hd->full[st], pol);
             }
             ++pq_head;
             progress = true;
         }
-        // 4) release finished tickets, in ticket order
+        // 4) done when every consumer warp has left
+        if (__shfl_sync(0xffffffffu, ld_acq_cta(&hd->cons_exited), 0) == kConsumerWarps) break;
+        // 5) bounded idleness
+        if (progress) {
+            idle_since = 0;
+        } else {
+            int bad = 0;
+            if (lane == 0) {
+                const uint64_t now = gtimer();
+                if (idle_since == 0) idle_since = now;
+                else if (static_cast<long long>(now - idle_since) > p.timeout_ns) {
+                    raise_error(p, abort_flag, kErrTimeout);
+                    bad = 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, bad, 0)) break;
+            __nanosleep(32);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ release warp
+// Publishes finished work to the other CTAs, in ticket order: a gpu-scope
+// fence, then bump the group's gate/up counter (gate/up ticket) or the
+// per-(token, 64-row tile) arrival counters (down ticket).  The CTA that
+// completes a token's tile sums its k per-pair outputs in slot order and
+// writes y -- no floating-point atomics, so the result is the same bits every
+// run.  The k partial loads of a row are all issued before the sum.
+__device__ __forceinline__ void release_loop(const KernelParams &p, Tabs tb, volatile int *abort_flag)
+{
+    const int lane = threadIdx.x & 31;
+    SmemHdr *hd = tb.hdr;
+    int dq_head = 0;
+    uint64_t idle_since = 0;
+    for (;;) {
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        bool progress = false;
         const int exited = __shfl_sync(0xffffffffu, ld_acq_cta(&hd->cons_exited), 0);
         for (;;) {
             const int slot = dq_head % kDoneQ;
             if (__shfl_sync(0xffffffffu, ld_acq_cta(&hd->dq_seq[slot]), 0) != dq_head + 1) break;
             __threadfence();  // the consumers' h / partial stores become visible first (cumulative)
             const int kind = hd->dq_kind[slot], grp = hd->dq_grp[slot], tile = hd->dq_tile[slot];
-            if (kind == KIND_A) {
+            if (kind != KIND_B) {
                 if (lane == 0) atomicAdd(p.doneA + grp, 1u);
             } else {
                 const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
@@ -1111,14 +1156,26 @@ __device__ __forceinline__ void helper_loop(const KernelParams &p, uint8_t *smem
                         const int src = __ffs(mask) - 1;
                         mask &= mask - 1;
                         const int t2 = __shfl_sync(0xffffffffu, tok, src);
-                        for (int row = lane; row < kMB; row += 32) {
-                            float yv = 0.f;
-                            for (int j = 0; j < p.k; ++j) {
-                                const int ps = tb.pos[t2 * p.k + j];
-                                if (ps != 0xFFFF)
-                                    yv += p.w[t2 * p.k + j] *
-                                          ldg_cg_f32(p.part + static_cast<size_t>(ps) * p.H + h0 + row);
+#pragma unroll
+                        for (int rr = 0; rr < kMB / 32; ++rr) {
+                            const int row = rr * 32 + lane;
+                            float pv[kMaxTopK], wv[kMaxTopK];
+#pragma unroll
+                            for (int j = 0; j < kMaxTopK; ++j) {
+                                pv[j] = 0.f;
+                                wv[j] = 0.f;
+                                if (j < p.k) {
+                                    const int ps = tb.pos[t2 * p.k + j];
+                                    if (ps != 0xFFFF) {
+                                        pv[j] = __ldcg(p.part + static_cast<size_t>(ps) * p.H + h0 + row);
+                                        wv[j] = p.w[t2 * p.k + j];
+                                    }
+                                }
                             }
+                            float yv = 0.f;
+#pragma unroll
+                            for (int j = 0; j < kMaxTopK; ++j)
+                                if (j < p.k && tb.pos[t2 * p.k + j] != 0xFFFF) yv += wv[j] * pv[j];
                             p.y[static_cast<size_t>(t2) * p.H + h0 + row] = yv;
                         }
                     }
@@ -1129,9 +1186,8 @@ __device__ __forceinline__ void helper_loop(const KernelParams &p, uint8_t *smem
             if (lane == 0) st_rel_cta(&hd->dq_head, dq_head);
             progress = true;
         }
-        // 5) done when every consumer warp has left and its last ticket is released
+        // done when every consumer warp has left and its last ticket is released
         if (exited == kConsumerWarps) break;
-        // 6) bounded idleness
         if (progress) {
             idle_since = 0;
         } else {
@@ -1237,7 +1293,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
         __syncthreads();
     }
 
-    if (tid >= kConsumerThreads + 32) {
+    if (tid >= kConsumerThreads + 64) {
+        release_loop(p, tb, abort_flag);
+    } else if (tid >= kConsumerThreads + 32) {
         helper_loop(p, smem, tb, abort_flag);
     } else if (tid >= kConsumerThreads) {
         producer_loop(p, smem, tb, abort_flag);

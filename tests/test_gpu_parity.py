@@ -282,3 +282,21 @@ def test_poisoned_workspace_times_out_and_recovers():
     assert plan.check(ws) == 0
     y_ref, _ = oracle.moe_forward(x, ids, w, {k: v.cpu() for k, v in W.items()})
     assert rel_err(y.cpu().numpy(), y_ref) <= TOL
+
+
+# ------------------------------------------------------------------ programmatic dependent launch
+def test_pdl_back_to_back_matches(cache):
+    """Steps launched with programmatic dependent launch, back to back on one
+    stream over a shared workspace, give the same bits as plain launches."""
+    wl, x, ids, w, W = workload_inputs("spec_verify", cache)
+    ref_plan, ref_ws, y_ref, st = run_case(wl, x, ids, w, W)
+    assert st == 0
+    plan = MoePlan(W, wl.H, wl.I, wl.E, wl.k, T_max=wl.T, strict=True, pdl=True)
+    ws = plan.new_workspace()
+    xd, idsd, wd = x.to(DEV), ids.to(DEV), w.to(DEV)
+    ys = [torch.empty((wl.T, wl.H), dtype=torch.float32, device=DEV) for _ in range(4)]
+    for y in ys:
+        plan.step(xd, idsd, wd, ws, y=y)
+    assert plan.check(ws) == 0
+    for y in ys:
+        assert torch.equal(y, y_ref)
