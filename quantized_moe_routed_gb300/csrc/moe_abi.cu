@@ -164,7 +164,14 @@ moe::SmemLayout layout_for(const moe_plan *pl, int T)
     const int scr_need = align16i(2 * P) + 8 * pl->d.E + 4 + 16;
     L.red_bytes = static_cast<int>(up(red_need > scr_need ? red_need : scr_need, 128));
     L.tab_bytes = moe::tab_bytes_for(P, T);
-    L.stage_bytes = pl->stage_bytes_nt[nt];
+    {
+        // weights, then the group's activation rows: groups hold at most
+        // min(8*nt, T) pairs (the kernel's group cap), 2*KP bytes each
+        const int rows = 8 * nt < T ? 8 * nt : T;
+        const int stA = pl->offAa + rows * 2 * pl->KA;
+        const int stB = pl->offAb + rows * 2 * pl->KB;
+        L.stage_bytes = up1024(stA > stB ? stA : stB);
+    }
     const int avail = pl->smem_optin - L.red_bytes - L.tab_bytes - 1024;
     int ns = avail / L.stage_bytes;
     if (ns > moe::kMaxStages) ns = moe::kMaxStages;

@@ -364,6 +364,54 @@ __device__ void group_pairs(const int32_t *__restrict__ ids, int P, int E, int16
     __syncthreads();
 }
 
+// Grouping of at most 32 pairs by one warp, in registers: lane p holds pair p;
+// its rank in the (expert, pair index) order is counted against every other
+// lane, which gives the same stable order as the counting sort.  Groups are
+// the runs of equal experts in that order, cut every G pairs.  Writes perm,
+// pos, stok, gexp/gbeg/gcnt and the header counts; the caller syncs.
+__device__ void group_pairs_warp(const KernelParams &p, int P, int G, Tabs tb)
+{
+    SmemHdr *hd = tb.hdr;
+    const int lane = threadIdx.x & 31;
+    int e = -1;
+    if (lane < P) e = p.ids[lane];
+    const bool valid = lane < P && e >= 0 && e < p.E;
+    const uint32_t badm = __ballot_sync(0xffffffffu, lane < P && e >= p.E);
+    const int key = valid ? e : 0x7fffffff;  // invalid pairs sort last
+    int rank = 0;
+    for (int j = 0; j < P; ++j) {
+        const int kj = __shfl_sync(0xffffffffu, key, j);
+        rank += (kj < key || (kj == key && j < lane)) ? 1 : 0;
+    }
+    const int nv = __popc(__ballot_sync(0xffffffffu, valid));
+    if (lane < P) tb.pos[lane] = valid ? static_cast<uint16_t>(rank) : 0xFFFFu;
+    if (valid) tb.perm[rank] = static_cast<uint16_t>(lane);
+    __syncwarp();
+    // sorted position r = lane: its pair, expert, token
+    const int pr = lane < nv ? tb.perm[lane] : 0;
+    const int er = __shfl_sync(0xffffffffu, e, pr);
+    if (lane < nv) tb.stok[lane] = static_cast<uint16_t>(pr / p.k);
+    const int eprev = __shfl_up_sync(0xffffffffu, er, 1);
+    const uint32_t runm = __ballot_sync(0xffffffffu, lane < nv && (lane == 0 || eprev != er));
+    const int rs = 31 - __clz(runm & (0xffffffffu >> (31 - lane)));  // start of this lane's run
+    const uint32_t above = runm & ~(0xffffffffu >> (31 - lane));        // run starts after this lane
+    const int re = above ? __ffs(above) - 1 : nv;                      // end of the run
+    const int off = lane - rs;
+    const bool head = lane < nv && off % G == 0;
+    const uint32_t headm = __ballot_sync(0xffffffffu, head);
+    if (head) {
+        const int gi = __popc(headm & (0xffffffffu >> (31 - lane))) - 1;
+        tb.gexp[gi] = static_cast<uint16_t>(er);
+        tb.gbeg[gi] = static_cast<uint16_t>(lane);
+        tb.gcnt[gi] = static_cast<uint8_t>(min(G, re - lane));
+    }
+    if (lane == 0) {
+        hd->n_valid = nv;
+        hd->n_bad = __popc(badm);
+        hd->n_groups = __popc(headm);
+    }
+}
+
 // ------------------------------------------------------------------ bounded waits
 __device__ __noinline__ void raise_error(const KernelParams &p, volatile int *abort_flag, uint32_t bits)
 {
@@ -1249,9 +1297,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
         int16_t *ids16 = reinterpret_cast<int16_t *>(scr);
         int32_t *ecnt = reinterpret_cast<int32_t *>(scr + align16(2 * P));
         int32_t *eoff = ecnt + p.E;
+        // groups of at most G pairs: one or two MMA n-tiles, and never more
+        // pairs than tokens (so a stage's activation rows fit; a token that
+        // names one expert in several slots gets several groups)
+        const int G = min(8 * NT, p.T);
+        if (P <= 32) {
+            if (tid < 32) group_pairs_warp(p, P, G, tb);
+            __syncthreads();
+        } else {
         group_pairs(p.ids, P, p.E, ids16, ecnt, eoff, tb.perm, tb.pos, &hd->n_valid, &hd->n_bad);
-        // split each expert's pairs into groups of at most G = 8*NT pairs
-        constexpr int G = 8 * NT;
         if (tid < 32) {
             const int lane = tid;
             const int per = (p.E + 31) / 32;
@@ -1276,13 +1330,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
             }
             if (lane == 31) hd->n_groups = incl;
         }
+        const int nv0 = hd->n_valid;
+        for (int r = tid; r < nv0; r += blockDim.x) tb.stok[r] = static_cast<uint16_t>(tb.perm[r] / p.k);
+        __syncthreads();
+        }
         for (int t = tid; t < p.T; t += blockDim.x) {
             int v = 0;
             for (int j = 0; j < p.k; ++j) v += (tb.pos[t * p.k + j] != 0xFFFFu);
             tb.kvalid[t] = static_cast<uint8_t>(v);
         }
-        const int nv = hd->n_valid;
-        for (int r = tid; r < nv; r += blockDim.x) tb.stok[r] = static_cast<uint16_t>(tb.perm[r] / p.k);
         __syncthreads();
         if (blockIdx.x == 0 && tid == 0 && hd->n_bad) atomicOr(p.ctrl + 2, kErrBadId);
         // tokens without a valid slot: y = 0 (nobody else writes them)
