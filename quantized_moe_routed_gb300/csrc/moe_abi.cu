@@ -43,17 +43,23 @@ std::once_flag g_active_once;
 
 }  // namespace
 
+// One tiling of the step kernel: gate/up tiles of RA rows and K parts of KA
+// elements, down parts of KB elements, the stage sub-buffer offsets and the
+// tensor maps of the six weight arrays for those box shapes.
+struct Tiling {
+    int RA = 0, KA = 0, KB = 0, nPA = 0, nPB = 0, nib_mode = 0;
+    int scale_tmaA = 0, spA = 0, shA = 0, mkA = 0, scale_tmaB = 0, spB = 0, shB = 0, mkB = 0;
+    int offGq = 0, offUq = 0, offGs = 0, offUs = 0, offAa = 0, offDq = 0, offDs = 0, offAb = 0;
+    CUtensorMap tm[6];
+};
+
 struct moe_plan {
     moe_plan_desc d;
     int device = 0, num_sms = 0, smem_optin = 0;
-    // tiling
-    int KA = 0, nPA = 0, KB = 0, nPB = 0, nHt = 0;
-    int nib_mode = 0;
-    int scale_tmaA = 0, spA = 0, shA = 0, mkA = 0, scale_tmaB = 0, spB = 0, shB = 0, mkB = 0;
-    int offGq = 0, offUq = 0, offGs = 0, offUs = 0, offAa = 0, offDq = 0, offDs = 0, offAb = 0;
-    int stage_bytes_nt[3] = {0, 0, 0};  // one ring stage of the 1- and 2-n-tile variants
-    int stage_bytes = 0;                // of the 2-n-tile variant (the largest)
-    CUtensorMap tm[6];
+    // tilings of the one- and two-n-tile kernel variants (tl[1], tl[2])
+    Tiling tl[3];
+    int nHt = 0;
+    int stage_bytes = 0;  // largest stage at T_max (for messages)
     int Tc = 0;  // tokens per launch chunk
     long long timeout_ns = 1000000000LL;
     bool strict = false, pdl = false;
@@ -167,9 +173,10 @@ moe::SmemLayout layout_for(const moe_plan *pl, int T)
     {
         // weights, then the group's activation rows: groups hold at most
         // min(8*nt, T) pairs (the kernel's group cap), 2*KP bytes each
+        const Tiling &tl = pl->tl[nt];
         const int rows = 8 * nt < T ? 8 * nt : T;
-        const int stA = pl->offAa + rows * 2 * pl->KA;
-        const int stB = pl->offAb + rows * 2 * pl->KB;
+        const int stA = tl.offAa + rows * 2 * tl.KA;
+        const int stB = tl.offAb + rows * 2 * tl.KB;
         L.stage_bytes = up1024(stA > stB ? stA : stB);
     }
     const int avail = pl->smem_optin - L.red_bytes - L.tab_bytes - 1024;
@@ -180,6 +187,69 @@ moe::SmemLayout layout_for(const moe_plan *pl, int T)
     L.tab_off = L.red_off + L.red_bytes;
     L.total = L.tab_off + L.tab_bytes + 1024;  // + slack to align the ring to 1024 bytes
     return L;
+}
+
+// The tiling of the n-tile variant nt: gate/up tiles of 32 rows and K parts
+// of up to 512 elements, down parts of up to 512, so every consumer warp
+// takes one 128-element chunk of 32 rows per stage and a stage's activation
+// rows (up to 16 pairs) stay small next to its weights.  (Measured on the
+// T=1 decode workload: 16-row tiles with 2048/1024-element parts, two chunks
+// per warp, were about 3% slower.)
+moe_status_t build_tiling(const moe_plan_desc &d, int nt, Tiling &tl)
+{
+    PartPlan pa{}, pb{};
+    const int capA = 512, capB = 512;
+    (void)nt;
+    if (!choose_part(d.H, capA, 2048, &pa) || !choose_part(d.I, capB, 1024, &pb))
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE,
+                    "no stage tiling for H=%d, I=%d (an odd multiple of 128 must be <= 2048 for H, <= 1024 for I)",
+                    d.H, d.I);
+    tl.RA = 32;
+    tl.KA = pa.KP;
+    tl.KB = pb.KP;
+    tl.scale_tmaA = pa.scale_tma;
+    tl.spA = pa.sp;
+    tl.shA = pa.sh;
+    tl.mkA = pa.mk;
+    tl.scale_tmaB = pb.scale_tma;
+    tl.spB = pb.sp;
+    tl.shB = pb.sh;
+    tl.mkB = pb.mk;
+    tl.nPA = d.H / tl.KA;
+    tl.nPB = d.I / tl.KB;
+    // stage sub-buffers: weights (1024-aligned), then the group's activation rows
+    tl.offGq = 0;
+    tl.offUq = tl.RA * tl.KA / 2;
+    tl.offGs = tl.RA * tl.KA;
+    tl.offUs = tl.offGs + up1024(tl.RA * tl.spA);
+    tl.offAa = tl.offUs + up1024(tl.RA * tl.spA);
+    tl.offDq = 0;
+    tl.offDs = moe::kMB * tl.KB / 2;
+    tl.offAb = tl.offDs + up1024(moe::kMB * tl.spB);
+    // tensor maps (host-only encoding; no device memory involved)
+    const uint64_t rowsGU = static_cast<uint64_t>(d.E) * d.I, rowsD = static_cast<uint64_t>(d.E) * d.H;
+    CUresult cr = CUDA_SUCCESS;
+    int mode = 0;
+    for (; mode < 2; ++mode) {
+        if (mode == 1 && (d.H % 256 || d.I % 256)) break;
+        cr = encode_nib(&tl.tm[0], mode, d.gate_q_dev, rowsGU, d.H, tl.RA, tl.KA);
+        if (cr == CUDA_SUCCESS) cr = encode_nib(&tl.tm[1], mode, d.up_q_dev, rowsGU, d.H, tl.RA, tl.KA);
+        if (cr == CUDA_SUCCESS) cr = encode_nib(&tl.tm[2], mode, d.down_q_dev, rowsD, d.I, moe::kMB, tl.KB);
+        if (cr == CUDA_SUCCESS) break;
+    }
+    if (cr != CUDA_SUCCESS || mode >= 2)
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "tensor-map encoding of the E2M1 rows failed (CUresult %d)",
+                    static_cast<int>(cr));
+    tl.nib_mode = mode;
+    if (tl.scale_tmaA) {
+        cr = encode_scale(&tl.tm[3], d.gate_s_dev, rowsGU, d.H, tl.RA, pa);
+        if (cr == CUDA_SUCCESS) cr = encode_scale(&tl.tm[4], d.up_s_dev, rowsGU, d.H, tl.RA, pa);
+    }
+    if (cr == CUDA_SUCCESS && tl.scale_tmaB) cr = encode_scale(&tl.tm[5], d.down_s_dev, rowsD, d.I, moe::kMB, pb);
+    if (cr != CUDA_SUCCESS)
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "tensor-map encoding of the E4M3 scale rows failed (CUresult %d)",
+                    static_cast<int>(cr));
+    return MOE_OK;
 }
 
 moe_status_t check_device(const moe_plan *pl)
@@ -269,29 +339,7 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
     p.I = pl->d.I;
     p.E = pl->d.E;
     p.k = pl->d.top_k;
-    p.KA = pl->KA;
-    p.nPA = pl->nPA;
-    p.KB = pl->KB;
-    p.nPB = pl->nPB;
     p.nHt = pl->nHt;
-    for (int i = 0; i < 6; ++i) p.tm[i] = pl->tm[i];
-    p.nib_mode = pl->nib_mode;
-    p.scale_tmaA = pl->scale_tmaA;
-    p.spA = pl->spA;
-    p.shA = pl->shA;
-    p.mkA = pl->mkA;
-    p.scale_tmaB = pl->scale_tmaB;
-    p.spB = pl->spB;
-    p.shB = pl->shB;
-    p.mkB = pl->mkB;
-    p.offGq = pl->offGq;
-    p.offUq = pl->offUq;
-    p.offGs = pl->offGs;
-    p.offUs = pl->offUs;
-    p.offAa = pl->offAa;
-    p.offDq = pl->offDq;
-    p.offDs = pl->offDs;
-    p.offAb = pl->offAb;
     p.timeout_ns = pl->timeout_ns;
     p.null_mode = path == Path::Null ? 1 : 0;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -315,6 +363,32 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
         p.red_bytes = L.red_bytes;
         p.tab_off = L.tab_off;
         p.ntiles = ntiles_for(pl, Tn);
+        {
+            const Tiling &tl = pl->tl[p.ntiles];
+            p.RA = tl.RA;
+            p.KA = tl.KA;
+            p.nPA = tl.nPA;
+            p.KB = tl.KB;
+            p.nPB = tl.nPB;
+            for (int i = 0; i < 6; ++i) p.tm[i] = tl.tm[i];
+            p.nib_mode = tl.nib_mode;
+            p.scale_tmaA = tl.scale_tmaA;
+            p.spA = tl.spA;
+            p.shA = tl.shA;
+            p.mkA = tl.mkA;
+            p.scale_tmaB = tl.scale_tmaB;
+            p.spB = tl.spB;
+            p.shB = tl.shB;
+            p.mkB = tl.mkB;
+            p.offGq = tl.offGq;
+            p.offUq = tl.offUq;
+            p.offGs = tl.offGs;
+            p.offUs = tl.offUs;
+            p.offAa = tl.offAa;
+            p.offDq = tl.offDq;
+            p.offDs = tl.offDs;
+            p.offAb = tl.offAb;
+        }
         cudaError_t e = moe::launch_step(p, pl->num_sms, L.total, pl->pdl, cs);
         if (e != cudaSuccess) {
             reject(pl);
@@ -460,73 +534,17 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
         const long long ms = std::atoll(t);
         if (ms > 0) pl->timeout_ns = ms * 1000000LL;
     }
-    PartPlan pa{}, pb{};
-    if (!choose_part(d.H, 512, 2048, &pa) || !choose_part(d.I, 512, 1024, &pb)) {
-        delete pl;
-        return fail(MOE_ERR_UNSUPPORTED_SHAPE,
-                    "no stage tiling for H=%d, I=%d (an odd multiple of 128 must be <= 2048 for H, <= 1024 for I)",
-                    d.H, d.I);
-    }
-    pl->KA = pa.KP;
-    pl->KB = pb.KP;
-    pl->scale_tmaA = pa.scale_tma;
-    pl->spA = pa.sp;
-    pl->shA = pa.sh;
-    pl->mkA = pa.mk;
-    pl->scale_tmaB = pb.scale_tma;
-    pl->spB = pb.sp;
-    pl->shB = pb.sh;
-    pl->mkB = pb.mk;
-    pl->nPA = d.H / pl->KA;
-    pl->nPB = d.I / pl->KB;
-    pl->nHt = d.H / moe::kMB;
-    // stage layouts: weights only, in 1024-aligned sub-buffers (the
-    // activations are read from global memory by the consumers)
-    pl->offGq = 0;
-    pl->offUq = moe::kRA * pl->KA / 2;
-    pl->offGs = moe::kRA * pl->KA;
-    pl->offUs = pl->offGs + up1024(moe::kRA * pl->spA);
-    pl->offAa = pl->offUs + up1024(moe::kRA * pl->spA);
-    pl->offDq = 0;
-    pl->offDs = moe::kMB * pl->KB / 2;
-    pl->offAb = pl->offDs + up1024(moe::kMB * pl->spB);
-    for (int nt = 1; nt <= 2; ++nt) {
-        // weights, then the group's activation rows (8*nt rows of 2*KP bytes)
-        const int stA = pl->offAa + 8 * nt * 2 * pl->KA;
-        const int stB = pl->offAb + 8 * nt * 2 * pl->KB;
-        pl->stage_bytes_nt[nt] = up1024(stA > stB ? stA : stB);
-    }
-    pl->stage_bytes = pl->stage_bytes_nt[2];
-    // tensor maps (host-only encoding; no device memory involved)
     if (!encoder()) {
         delete pl;
         return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     }
-    const uint64_t rowsGU = static_cast<uint64_t>(d.E) * d.I, rowsD = static_cast<uint64_t>(d.E) * d.H;
-    CUresult cr = CUDA_SUCCESS;
-    int mode = 0;
-    for (; mode < 2; ++mode) {
-        if (mode == 1 && (d.H % 256 || d.I % 256)) break;
-        cr = encode_nib(&pl->tm[0], mode, d.gate_q_dev, rowsGU, d.H, moe::kRA, pl->KA);
-        if (cr == CUDA_SUCCESS) cr = encode_nib(&pl->tm[1], mode, d.up_q_dev, rowsGU, d.H, moe::kRA, pl->KA);
-        if (cr == CUDA_SUCCESS) cr = encode_nib(&pl->tm[2], mode, d.down_q_dev, rowsD, d.I, moe::kMB, pl->KB);
-        if (cr == CUDA_SUCCESS) break;
-    }
-    if (cr != CUDA_SUCCESS || mode >= 2) {
-        delete pl;
-        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "tensor-map encoding of the E2M1 rows failed (CUresult %d)",
-                    static_cast<int>(cr));
-    }
-    pl->nib_mode = mode;
-    if (pl->scale_tmaA) {
-        cr = encode_scale(&pl->tm[3], d.gate_s_dev, rowsGU, d.H, moe::kRA, pa);
-        if (cr == CUDA_SUCCESS) cr = encode_scale(&pl->tm[4], d.up_s_dev, rowsGU, d.H, moe::kRA, pa);
-    }
-    if (cr == CUDA_SUCCESS && pl->scale_tmaB) cr = encode_scale(&pl->tm[5], d.down_s_dev, rowsD, d.I, moe::kMB, pb);
-    if (cr != CUDA_SUCCESS) {
-        delete pl;
-        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "tensor-map encoding of the E4M3 scale rows failed (CUresult %d)",
-                    static_cast<int>(cr));
+    pl->nHt = d.H / moe::kMB;
+    for (int nt = 1; nt <= 2; ++nt) {
+        const moe_status_t ts = build_tiling(d, nt, pl->tl[nt]);
+        if (ts != MOE_OK) {
+            delete pl;
+            return ts;
+        }
     }
     const int tc = moe::kMaxPairs / d.top_k;
     pl->Tc = d.T_max < tc ? d.T_max : tc;
@@ -534,8 +552,9 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
     if (L.NS < 2 || L.total > optin) {
         delete pl;
         return fail(MOE_ERR_UNSUPPORTED_SHAPE, "shared memory: %d stages of %d bytes do not fit", L.NS,
-                    pl->stage_bytes);
+                    L.stage_bytes);
     }
+    pl->stage_bytes = L.stage_bytes;
     // workspace layout (fixed per plan)
     size_t o = moe::kCtrlBytes;
     pl->off_done = o;

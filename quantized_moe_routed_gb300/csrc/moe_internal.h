@@ -22,9 +22,6 @@ constexpr int kMaxStages = 16;
 constexpr int kDecodeMaxT = 24;     // the pages' m <= 24 decode bound
 constexpr int kMB = 64;             // down-projection rows per phase-B ticket
 
-// Rows of a gate/up ticket: 32 intermediate rows of gate and the same 32 of up.
-constexpr int kRA = 32;
-
 // Device error word bits (workspace control block, word 2).
 constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrBadId = 2u;
@@ -71,6 +68,7 @@ struct KernelParams {
     int H, I, E, k, T;
     int Pmax;           // rows of each part block of xs / hbuf
     // tiling (chosen on the host)
+    int RA;             // gate/up: rows of gate (and of up) per ticket (16 or 32)
     int KA, nPA;        // gate/up: K elements per stage part, parts per ticket
     int KB, nPB;        // down: K elements per stage part, parts per ticket
     int nHt;            // H / kMB

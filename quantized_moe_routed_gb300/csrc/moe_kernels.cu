@@ -13,7 +13,7 @@
 //    splitting an expert's pairs into groups of at most 8 or 16 pairs (one or
 //    two 8-wide MMA n-tiles, fixed per launch from T*k).
 //  * Tickets come from one atomic counter (the first one is the CTA index, so
-//    the first weight loads need no atomic).  Gate/up tickets (group, 16
+//    the first weight loads need no atomic).  Gate/up tickets (group, 16 or 32
 //    intermediate rows of gate and up) all precede the down tickets (group,
 //    64 rows of down); each CTA takes tickets in increasing order, so every
 //    gate/up ticket is held by a running CTA before any down ticket is handed
@@ -142,12 +142,6 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p)
     return v;
 }
 
-__device__ __forceinline__ float ldg_cg_f32(const float *p)
-{
-    float v;
-    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
-    return v;
-}
 
 
 // CTA-scope acquire / release on shared memory: order this thread's later
@@ -564,19 +558,25 @@ __device__ __forceinline__ int act_index(int mode, int kk, int rpar)
 }
 
 // The B operand of chunk q for pair n = nt*8 + g of the group, from the
-// stage's copy of the group's rows (row pitch `pitch` bytes).  Rows past the
-// group's end hold stale data: they only feed MMA columns nobody reads.
+// stage's copy of the group's gcnt rows (row pitch `pitch` bytes).  The stage
+// holds only those rows: pairs past the group's end read as zero.
 template <int NT>
-__device__ __forceinline__ void load_act(uint4 (&b)[NT][4], const uint8_t *act, int pitch, int q, int gbeg, int g,
-                                         int t)
+__device__ __forceinline__ void load_act(uint4 (&b)[NT][4], const uint8_t *act, int pitch, int q, int gbeg, int gcnt,
+                                         int g, int t)
 {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int n = nt * 8 + g;
-        const uint8_t *row = act + n * pitch + q * 256;
-        const int rpar = (gbeg + n) & 1;
+        if (n < gcnt) {
+            const uint8_t *row = act + n * pitch + q * 256;
+            const int rpar = (gbeg + n) & 1;
 #pragma unroll
-        for (int v = 0; v < 4; ++v) b[nt][v] = *reinterpret_cast<const uint4 *>(row + act_granule(v, t, rpar) * 16);
+            for (int v = 0; v < 4; ++v)
+                b[nt][v] = *reinterpret_cast<const uint4 *>(row + act_granule(v, t, rpar) * 16);
+        } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) b[nt][v] = make_uint4(0, 0, 0, 0);
+        }
     }
 }
 
@@ -613,6 +613,22 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u)
 {
     return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
 }
+
+// Rows of a gate/up tile in the n-tile variant NT (the host's tiling uses the
+// same rule; the code also handles 16).
+template <int NT>
+struct TileRows {
+    static constexpr int RA = 32;
+};
+
+// The operands of one chunk task: E2M1 rows g and g+8 of both m-tiles, their
+// scale pairs, and the B operand.
+template <int NT>
+struct TaskOps {
+    uint4 ra[2], rb[2];
+    uint16_t s_a[2], s_b[2];
+    uint4 bq[NT][4];
+};
 
 // ------------------------------------------------------------------ consumer warps
 // Each of the eight consumer warps walks the stage ring on its own: it waits
@@ -695,7 +711,10 @@ __device__ __forceinline__ bool finish_ticket(const KernelParams &p, const Tabs 
     SmemHdr *hd = tb.hdr;
     const int b = tick & 1;
     float4 *rb = red + b * (16 * NT * 32);
-    const int base = (warp & 3) * 4 + (warp >> 2) * 2;  // slot (ks, half, mt) = ks*4 + half*2 + mt
+    // reduction slots: gate/up (k-slice, row half, m-tile) = (ks*nhalf + half)*2 + mt;
+    // down (k-slice, 32-row group, m-tile) = ks*4 + mg*2 + mt
+    constexpr int RA = TileRows<NT>::RA, nhalf = RA / 16, nks = kConsumerWarps / nhalf;
+    const int base = isA ? (warp % nks * nhalf + warp / nks) * 2 : (warp & 3) * 4 + (warp >> 2) * 2;
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -708,10 +727,11 @@ __device__ __forceinline__ bool finish_ticket(const KernelParams &p, const Tabs 
     const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
     const float *redf = reinterpret_cast<const float *>(rb);
     if (isA) {
-        // h[n][i0 + half*16 + row] = SiLU(g) * u: this warp's NT*32 of the 32 rows x 8*NT pairs
+        // h[n][i0 + half*16 + row] = SiLU(g) * u: this warp's RA*NT of the RA rows x 8*NT pairs
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int idx = warp * (32 * NT) + j * 32 + lane;
+        for (int j = 0; j < (RA * NT + 31) / 32; ++j) {
+            const int idx = warp * (RA * NT) + j * 32 + lane;
+            if (j * 32 + lane >= RA * NT) break;
             const int half = idx / (NT * 128), rem = idx - half * (NT * 128);
             const int nt = rem >> 7, ls = (rem >> 2) & 31, r = rem & 3;
             const int row = half * 16 + (ls >> 2) + 8 * (r >> 1);
@@ -719,15 +739,15 @@ __device__ __forceinline__ bool finish_ticket(const KernelParams &p, const Tabs 
             if (n < gcnt) {
                 float sg = 0.f, su = 0.f;
 #pragma unroll
-                for (int k2 = 0; k2 < 4; ++k2) {
-                    sg += redf[(((k2 * 4 + half * 2 + 0) * NT + nt) * 32 + ls) * 4 + r];
-                    su += redf[(((k2 * 4 + half * 2 + 1) * NT + nt) * 32 + ls) * 4 + r];
+                for (int k2 = 0; k2 < nks; ++k2) {
+                    sg += redf[((((k2 * nhalf + half) * 2 + 0) * NT + nt) * 32 + ls) * 4 + r];
+                    su += redf[((((k2 * nhalf + half) * 2 + 1) * NT + nt) * 32 + ls) * 4 + r];
                 }
                 const float gv = sg * ts0, uv = su * ts1;
                 float v = gv / (1.0f + __expf(-gv)) * uv;
                 if (NULLM) v = 0.f;
                 if (!(fabsf(v) <= 65504.0f)) atomicOr(p.ctrl + 2, kErrRange);
-                const int kh = tile * kRA + row, pb = kh / p.KB, kk = kh - pb * p.KB;
+                const int kh = tile * RA + row, pb = kh / p.KB, kk = kh - pb * p.KB;
                 const int rr = gbeg + n;
                 p.hbuf[(static_cast<size_t>(pb) * p.Pmax + rr) * p.KB + act_index(p.nib_mode, kk, rr & 1)] =
                     __half_as_ushort(__float2half_rn(v));
@@ -809,7 +829,9 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
     SmemHdr *hd = tb.hdr;
     float4 *red = reinterpret_cast<float4 *>(smem + p.red_off);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int ks = warp & 3, half = warp >> 2;
+    constexpr int RA = TileRows<NT>::RA, nhalf = RA / 16, nks = kConsumerWarps / nhalf;
+    const int ks = warp & 3, half = warp >> 2;          // down: K chunk, 32-row group
+    const int ksA = warp % nks, halfA = warp / nks;    // gate/up: K chunk, 16-row half
     const int chunksA = p.KA / 128, chunksB = p.KB / 128;
     int s = 0, tick = 0;
     uint32_t ph = 0;
@@ -835,45 +857,49 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
             ts1 = isA ? __ldg(p.uts + e) : 0.f;
         }
         const uint8_t *st = smem + s * p.stage_bytes;
-        if (isA) {
-            for (int q = ks; q < chunksA; q += 4) {
-                uint4 ra[2], rb[2], bq[NT][4];
-                uint16_t s_a[2], s_b[2];
-                const int ko = k_off(p.nib_mode, q, t);
+        // this warp's tasks in the stage: gate/up chunks q = ksA, ksA + nks, ..
+        // (16 gate and the same 16 up rows), or down chunks q = ks, ks + 4, ..
+        // (32 rows)
+        const int q0 = isA ? ksA : ks, qstep = isA ? nks : 4, qend = isA ? chunksA : chunksB;
+        auto load_task = [&](int q, TaskOps<NT> &o) {
+            const int ko = k_off(p.nib_mode, q, t);
+            if (isA) {
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {  // m-tile 0: gate rows, 1: up rows (same 16 rows)
                     const uint8_t *nbp = st + (mt ? p.offUq : p.offGq);
-                    const int r0 = half * 16 + g;
-                    ra[mt] = *reinterpret_cast<const uint4 *>(nbp + nib_off(p.nib_mode, kRA, r0, q, t));
-                    rb[mt] = *reinterpret_cast<const uint4 *>(nbp + nib_off(p.nib_mode, kRA, r0 + 8, q, t));
+                    const int r0 = halfA * 16 + g;
+                    o.ra[mt] = *reinterpret_cast<const uint4 *>(nbp + nib_off(p.nib_mode, RA, r0, q, t));
+                    o.rb[mt] = *reinterpret_cast<const uint4 *>(nbp + nib_off(p.nib_mode, RA, r0 + 8, q, t));
                     const uint8_t *sbp = st + (mt ? p.offUs : p.offGs);
-                    s_a[mt] = scale_pair(sbp, p.spA, p.shA, p.mkA, r0, ko);
-                    s_b[mt] = scale_pair(sbp, p.spA, p.shA, p.mkA, r0 + 8, ko);
+                    o.s_a[mt] = scale_pair(sbp, p.spA, p.shA, p.mkA, r0, ko);
+                    o.s_b[mt] = scale_pair(sbp, p.spA, p.shA, p.mkA, r0 + 8, ko);
                 }
                 if (xdirect) {
-                    load_x_direct<NT>(bq, p, tb, gbeg, gcnt, part * p.KA + ko, g);
-                    chunk_math<2, NT, true, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
+                    load_x_direct<NT>(o.bq, p, tb, gbeg, gcnt, part * p.KA + ko, g);
+#pragma unroll
+                    for (int a = 0; a < NT; ++a)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) o.bq[a][v] = bf16x8_to_f16x8(o.bq[a][v]);
                 } else {
-                    load_act<NT>(bq, st + p.offAa, 2 * p.KA, q, gbeg, g, t);
-                    chunk_math<2, NT, false, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
+                    load_act<NT>(o.bq, st + p.offAa, 2 * p.KA, q, gbeg, gcnt, g, t);
                 }
-            }
-        } else {
-            for (int q = ks; q < chunksB; q += 4) {
-                uint4 ra[2], rb[2], bq[NT][4];
-                uint16_t s_a[2], s_b[2];
-                const int ko = k_off(p.nib_mode, q, t);
+            } else {
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
                     const int r0 = half * 32 + mt * 16 + g;
-                    ra[mt] = *reinterpret_cast<const uint4 *>(st + p.offDq + nib_off(p.nib_mode, kMB, r0, q, t));
-                    rb[mt] = *reinterpret_cast<const uint4 *>(st + p.offDq + nib_off(p.nib_mode, kMB, r0 + 8, q, t));
-                    s_a[mt] = scale_pair(st + p.offDs, p.spB, p.shB, p.mkB, r0, ko);
-                    s_b[mt] = scale_pair(st + p.offDs, p.spB, p.shB, p.mkB, r0 + 8, ko);
+                    o.ra[mt] = *reinterpret_cast<const uint4 *>(st + p.offDq + nib_off(p.nib_mode, kMB, r0, q, t));
+                    o.rb[mt] = *reinterpret_cast<const uint4 *>(st + p.offDq + nib_off(p.nib_mode, kMB, r0 + 8, q, t));
+                    o.s_a[mt] = scale_pair(st + p.offDs, p.spB, p.shB, p.mkB, r0, ko);
+                    o.s_b[mt] = scale_pair(st + p.offDs, p.spB, p.shB, p.mkB, r0 + 8, ko);
                 }
-                load_act<NT>(bq, st + p.offAb, 2 * p.KB, q, gbeg, g, t);
-                chunk_math<2, NT, false, NULLM>(ra, rb, s_a, s_b, bq, acc, gcnt);
+                load_act<NT>(o.bq, st + p.offAb, 2 * p.KB, q, gbeg, gcnt, g, t);
             }
+        };
+        // one copy of the chunk math in the loop keeps the hot code small
+        for (int q = q0; q < qend; q += qstep) {
+            TaskOps<NT> o;
+            load_task(q, o);
+            chunk_math<2, NT, false, NULLM>(o.ra, o.rb, o.s_a, o.s_b, o.bq, acc, gcnt);
         }
         // release the stage
         __syncwarp();
@@ -899,7 +925,7 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
 }
 
 // ------------------------------------------------------------------ tickets
-// Ticket order: all gate/up tickets (group-major: the TA 32-row tiles of group
+// Ticket order: all gate/up tickets (group-major: the TA row tiles of group
 // 0, then group 1, ...), then all down tickets (group-major: the nB 64-row
 // tiles of each group).  Every gate/up ticket precedes every down ticket, so
 // each down ticket's dependency is held by a running CTA when it is handed
@@ -935,9 +961,9 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
     SmemHdr *hd = tb.hdr;
     const uint64_t pol = policy_evict_first();
     const int ng = hd->n_groups;
-    const int TA = p.I / kRA;
+    const int TA = p.I / p.RA;
     const int total = ng * (TA + p.nHt);
-    const uint32_t wbytesA = 2u * kRA * (p.KA / 2) + 2u * kRA * (p.KA / 16);
+    const uint32_t wbytesA = 2u * p.RA * (p.KA / 2) + 2u * p.RA * (p.KA / 16);
     const uint32_t wbytesB = kMB * (p.KB / 2) + kMB * (p.KB / 16);
     const int nspA = p.KA / 128, nspB = p.KB / 128;
     bool ok = true;
@@ -968,7 +994,7 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
         const int nparts = isA ? p.nPA : p.nPB;
         const int KP = isA ? p.KA : p.KB;
         const uint32_t abytes = static_cast<uint32_t>(gcnt) * 2u * KP;
-        const int row = isA ? e * p.I + tile * kRA : e * p.H + tile * kMB;
+        const int row = isA ? e * p.I + tile * p.RA : e * p.H + tile * kMB;
         for (int part = 0; part < nparts; ++part) {
             if (!wait_for([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
                 ok = false;
@@ -991,16 +1017,16 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
                     tma3d(st + p.offUq, &p.tm[1], 0, row, part * nspA, bar, pol);
                 } else {
                     for (int b2 = 0; b2 < p.KA / 256; ++b2) {
-                        tma2d(st + p.offGq + b2 * kRA * 128, &p.tm[0], part * (p.KA / 2) + b2 * 128, row, bar, pol);
-                        tma2d(st + p.offUq + b2 * kRA * 128, &p.tm[1], part * (p.KA / 2) + b2 * 128, row, bar, pol);
+                        tma2d(st + p.offGq + b2 * p.RA * 128, &p.tm[0], part * (p.KA / 2) + b2 * 128, row, bar, pol);
+                        tma2d(st + p.offUq + b2 * p.RA * 128, &p.tm[1], part * (p.KA / 2) + b2 * 128, row, bar, pol);
                     }
                 }
                 if (p.scale_tmaA) {
                     tma2d(st + p.offGs, &p.tm[3], part * (p.KA / 16), row, bar, pol);
                     tma2d(st + p.offUs, &p.tm[4], part * (p.KA / 16), row, bar, pol);
                 } else {
-                    bulk_g2s(st + p.offGs, p.gs + static_cast<size_t>(row) * (p.H / 16), kRA * (p.H / 16), bar, pol);
-                    bulk_g2s(st + p.offUs, p.us + static_cast<size_t>(row) * (p.H / 16), kRA * (p.H / 16), bar, pol);
+                    bulk_g2s(st + p.offGs, p.gs + static_cast<size_t>(row) * (p.H / 16), p.RA * (p.H / 16), bar, pol);
+                    bulk_g2s(st + p.offUs, p.us + static_cast<size_t>(row) * (p.H / 16), p.RA * (p.H / 16), bar, pol);
                 }
                 if (x_ok)
                     bulk_g2s(st + p.offAa, p.xs + (static_cast<size_t>(part) * p.Pmax + gbeg) * p.KA, abytes, bar,
@@ -1068,7 +1094,7 @@ __device__ __forceinline__ void helper_loop(const KernelParams &p, uint8_t *smem
     SmemHdr *hd = tb.hdr;
     const uint64_t pol = policy_evict_first();
     const int ng = hd->n_groups, nvalid = hd->n_valid;
-    const int TA = p.I / kRA;
+    const int TA = p.I / p.RA;
     const int total = ng * (TA + p.nHt);
     bool fetch_done = false, xr = false;
     int tq_tail = 0, pq_head = 0;
