@@ -43,6 +43,25 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def measured_traffic():
+    """DRAM bytes per launch of the decode step from the committed ncu summary,
+    if that capture was taken of the kernel source as it is now; else None."""
+    import hashlib
+    try:
+        src = open(os.path.join(ROOT, "quantized_moe_routed_gb300", "csrc", "moe_kernels.cu"), "rb").read()
+        sha = hashlib.sha256(src).hexdigest()
+        fields = {}
+        for line in open(os.path.join(ROOT, "profiles", "moe_step_kernel_decode.md")):
+            if ":" in line:
+                key, val = line.split(":", 1)
+                fields[key.strip()] = val.strip()
+        if fields.get("kernel_source_sha256") == sha:
+            return int(fields["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
@@ -319,7 +338,8 @@ def main():
                    "algorithmic_bytes_per_step": S["bytes"], "timing": f"CUDA graph of {GRAPH_STEPS} steps (programmatic dependent launch), "
                                                                        "CUDA events on the launch stream"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                     "traffic": None, "peak_kind": peak_kind},
+                     "traffic": measured_traffic() if S["wl"].name == "decode" else None,
+                     "peak_kind": peak_kind},
         "gpu_launches": steps,
         "clocks": ck.summary(),
     }
