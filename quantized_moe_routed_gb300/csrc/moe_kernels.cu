@@ -252,9 +252,9 @@ struct SmemHdr {
 };
 static_assert(sizeof(SmemHdr) <= kTabHdrBytes, "header too large");
 
-// KIND_AX: a gate/up part whose x rows are not in the stage (the gathered x
-// was not yet published when it was issued): the consumers read them from
-// the caller's bf16 x instead.
+// KIND_AX: a gate/up part issued before the gathered x was published: its
+// stage holds the group's x rows copied straight from the caller's bf16 x
+// (natural element order, one row per pair), which the consumers convert.
 enum { KIND_A = 0, KIND_B = 1, KIND_END = 2, KIND_AX = 3 };
 
 struct Tabs {
@@ -580,27 +580,27 @@ __device__ __forceinline__ void load_act(uint4 (&b)[NT][4], const uint8_t *act, 
     }
 }
 
-__device__ __forceinline__ uint4 ldg_nc_v4(const void *ptr)
+// bf16 -> fp16 of 8 values (exact inside the fp16 range).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u)
 {
-    uint4 v;
-    asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(ptr));
-    return v;
+    return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
 }
 
-// The B operand of a gate/up chunk straight from the caller's bf16 x (read
-// only for the whole step): pair n = nt*8 + g of the group, the 32 elements
-// of this thread from K position kglob.  Pairs past the group's end are 0.
+// The B operand of a gate/up chunk from a KIND_AX stage: the group's x rows
+// as copied from the caller's bf16 x (row n at n*pitch, natural order), the
+// 32 elements of this thread from chunk offset koff, converted to fp16.
+// Pairs past the group's end are 0.
 template <int NT>
-__device__ __forceinline__ void load_x_direct(uint4 (&b)[NT][4], const KernelParams &p, const Tabs &tb, int gbeg,
-                                              int gcnt, int kglob, int g)
+__device__ __forceinline__ void load_x_raw(uint4 (&b)[NT][4], const uint8_t *act, int pitch, int koff, int gcnt,
+                                           int g)
 {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int n = nt * 8 + g;
         if (n < gcnt) {
-            const uint16_t *src = p.x + static_cast<size_t>(tb.stok[gbeg + n]) * p.H + kglob;
+            const uint8_t *src = act + n * pitch + koff * 2;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) b[nt][v] = ldg_nc_v4(src + 8 * v);
+            for (int v = 0; v < 4; ++v) b[nt][v] = bf16x8_to_f16x8(*reinterpret_cast<const uint4 *>(src + 16 * v));
         } else {
 #pragma unroll
             for (int v = 0; v < 4; ++v) b[nt][v] = make_uint4(0, 0, 0, 0);
@@ -608,11 +608,6 @@ __device__ __forceinline__ void load_x_direct(uint4 (&b)[NT][4], const KernelPar
     }
 }
 
-// bf16 -> fp16 of 8 values (exact inside the fp16 range).
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u)
-{
-    return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
-}
 
 // Rows of a gate/up tile in the n-tile variant NT (the host's tiling uses the
 // same rule; the code also handles 16).
@@ -875,11 +870,7 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
                     o.s_b[mt] = scale_pair(sbp, p.spA, p.shA, p.mkA, r0 + 8, ko);
                 }
                 if (xdirect) {
-                    load_x_direct<NT>(o.bq, p, tb, gbeg, gcnt, part * p.KA + ko, g);
-#pragma unroll
-                    for (int a = 0; a < NT; ++a)
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) o.bq[a][v] = bf16x8_to_f16x8(o.bq[a][v]);
+                    load_x_raw<NT>(o.bq, st + p.offAa, 2 * p.KA, ko, gcnt, g);
                 } else {
                     load_act<NT>(o.bq, st + p.offAa, 2 * p.KA, q, gbeg, gcnt, g, t);
                 }
@@ -1010,7 +1001,7 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
                     x_ok = true;
                 }
                 hd->stage_hdr[s] = make_int4(x_ok ? KIND_A : KIND_AX, grp, tile, part);
-                mbar_expect_tx(bar, wbytesA + (x_ok ? abytes : 0u));
+                mbar_expect_tx(bar, wbytesA + abytes);
                 // gate rows i0..i0+31 and up rows i0..i0+31, K elements part*KA ..
                 if (p.nib_mode == 0) {
                     tma3d(st + p.offGq, &p.tm[0], 0, row, part * nspA, bar, pol);
@@ -1028,9 +1019,16 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
                     bulk_g2s(st + p.offGs, p.gs + static_cast<size_t>(row) * (p.H / 16), p.RA * (p.H / 16), bar, pol);
                     bulk_g2s(st + p.offUs, p.us + static_cast<size_t>(row) * (p.H / 16), p.RA * (p.H / 16), bar, pol);
                 }
-                if (x_ok)
+                if (x_ok) {
                     bulk_g2s(st + p.offAa, p.xs + (static_cast<size_t>(part) * p.Pmax + gbeg) * p.KA, abytes, bar,
                              pol);
+                } else {
+                    // the caller's bf16 rows of the group's tokens, K slice of this part
+                    for (int n = 0; n < gcnt; ++n)
+                        bulk_g2s(st + p.offAa + n * 2 * p.KA,
+                                 p.x + static_cast<size_t>(tb.stok[gbeg + n]) * p.H + static_cast<size_t>(part) * p.KA,
+                                 2u * p.KA, bar, pol);
+                }
             } else {
                 hd->stage_hdr[s] = make_int4(KIND_B, grp, tile, part);
                 mbar_expect_tx(bar, wbytesB + abytes);
