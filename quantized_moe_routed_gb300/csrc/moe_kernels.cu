@@ -856,7 +856,7 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
         // (16 gate and the same 16 up rows), or down chunks q = ks, ks + 4, ..
         // (32 rows)
         const int q0 = isA ? ksA : ks, qstep = isA ? nks : 4, qend = isA ? chunksA : chunksB;
-        auto load_task = [&](int q, TaskOps<NT> &o) {
+        auto load_task = [&](const uint8_t *st, bool xdirect, int q, TaskOps<NT> &o) {
             const int ko = k_off(p.nib_mode, q, t);
             if (isA) {
 #pragma unroll
@@ -886,11 +886,39 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
                 load_act<NT>(o.bq, st + p.offAb, 2 * p.KB, q, gbeg, gcnt, g, t);
             }
         };
-        // one copy of the chunk math in the loop keeps the hot code small
-        for (int q = q0; q < qend; q += qstep) {
-            TaskOps<NT> o;
-            load_task(q, o);
-            chunk_math<2, NT, false, NULLM>(o.ra, o.rb, o.s_a, o.s_b, o.bq, acc, gcnt);
+        const int nparts = isA ? p.nPA : p.nPB;
+        int last_part = part;
+        bool paired = false;
+        if constexpr (NT == 1) {
+            // one n-tile, one task per warp: take this part and the next part of
+            // the same ticket together (the producer issues a ticket's parts in
+            // consecutive stages), so waits, releases and load latencies are paid
+            // once per pair and the two chunks' dequantisation overlaps
+            if (q0 < qend && q0 + qstep >= qend && part + 1 < nparts) {
+                const int s2 = s + 1 == p.NS ? 0 : s + 1;
+                const uint32_t ph2 = s + 1 == p.NS ? ph ^ 1u : ph;
+                if (!warp_wait_bar(p, &hd->full[s2], ph2, abort_flag)) break;
+                const bool xd2 = hd->stage_hdr[s2].x == KIND_AX;
+                TaskOps<NT> o1, o2;
+                load_task(st, xdirect, q0, o1);
+                load_task(smem + s2 * p.stage_bytes, xd2, q0, o2);
+                chunk_math<2, NT, false, NULLM>(o1.ra, o1.rb, o1.s_a, o1.s_b, o1.bq, acc, gcnt);
+                chunk_math<2, NT, false, NULLM>(o2.ra, o2.rb, o2.s_a, o2.s_b, o2.bq, acc, gcnt);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&hd->empty[s]);
+                s = s2;
+                ph = ph2;
+                last_part = part + 1;
+                paired = true;
+            }
+        }
+        if (!paired) {
+            // one copy of the chunk math in the loop keeps the hot code small
+            for (int q = q0; q < qend; q += qstep) {
+                TaskOps<NT> o;
+                load_task(st, xdirect, q, o);
+                chunk_math<2, NT, false, NULLM>(o.ra, o.rb, o.s_a, o.s_b, o.bq, acc, gcnt);
+            }
         }
         // release the stage
         __syncwarp();
@@ -899,7 +927,7 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
             s = 0;
             ph ^= 1u;
         }
-        if (part == (isA ? p.nPA : p.nPB) - 1) {
+        if (last_part == nparts - 1) {
             if (!finish_ticket<NT, NULLM>(p, tb, red, acc, isA, grp, tile, tick, ts0, ts1, warp, lane, abort_flag))
                 break;
             ++tick;
