@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define MOE_NVFP4_ABI_VERSION 1
+#define MOE_NVFP4_ABI_VERSION 2
 
 typedef enum {
     MOE_OK = 0,
@@ -77,7 +77,21 @@ typedef struct {
     int strict; /* 1: refuse (MOE_ERR_NOT_FAST_PATH) anything but the named path; */
                 /*    the environment variable MOE_STRICT=1 forces it on          */
     int pdl;    /* 1: launch with programmatic dependent launch allowed          */
+    int kernel; /* which step kernel runs moe_decode / moe_prefill:               */
+                /*   MOE_KERNEL_AUTO: the library's choice (currently the         */
+                /*     register kernel, the faster of the two on the decode       */
+                /*     workloads measured);                                       */
+                /*   MOE_KERNEL_REGISTER: E2M1 x E4M3 dequantised in registers,   */
+                /*     fp16 mma.sync (any shape the plan accepts);                */
+                /*   MOE_KERNEL_TENSOR: tcgen05 block-scaled FP4 MMA on the        */
+                /*     NVFP4 bytes, activations as four FP4 digit rows (the plan  */
+                /*     is refused with UNSUPPORTED_SHAPE where the shape does not */
+                /*     allow it).  Its block scales must be non-negative E4M3     */
+                /*     codes (the MMA reads them unsigned), as an NVFP4 quantiser */
+                /*     writes them.                                               */
 } moe_plan_desc;
+
+enum { MOE_KERNEL_AUTO = 0, MOE_KERNEL_REGISTER = 1, MOE_KERNEL_TENSOR = 2 };
 
 /* Per-plan launch counters (host side; how many times each path ran). */
 typedef struct {
@@ -86,6 +100,7 @@ typedef struct {
     uint64_t null_launches;    /* measurement variant (no dequant, no math)     */
     uint64_t group_launches;   /* stand-alone grouping kernel                   */
     uint64_t rejected_calls;   /* calls that returned an error status           */
+    uint64_t tensor_launches;  /* of decode + prefill: tensor-core kernel       */
     int num_sms;               /* SMs on the plan's device (grid size)          */
     int stages;                /* shared-memory ring stages at the largest T    */
     int smem_bytes;            /* dynamic shared memory per CTA at the largest T */

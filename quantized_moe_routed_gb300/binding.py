@@ -32,12 +32,16 @@ class moe_plan_desc(C.Structure):
                 ("gate_q_dev", C.c_void_p), ("up_q_dev", C.c_void_p), ("down_q_dev", C.c_void_p),
                 ("gate_s_dev", C.c_void_p), ("up_s_dev", C.c_void_p), ("down_s_dev", C.c_void_p),
                 ("gate_ts_dev", C.c_void_p), ("up_ts_dev", C.c_void_p), ("down_ts_dev", C.c_void_p),
-                ("device", C.c_int), ("strict", C.c_int), ("pdl", C.c_int)]
+                ("device", C.c_int), ("strict", C.c_int), ("pdl", C.c_int), ("kernel", C.c_int)]
+
+
+MOE_KERNEL_AUTO, MOE_KERNEL_REGISTER, MOE_KERNEL_TENSOR = 0, 1, 2
 
 
 class moe_stats_t(C.Structure):
     _fields_ = [("decode_launches", C.c_uint64), ("prefill_launches", C.c_uint64), ("null_launches", C.c_uint64),
-                ("group_launches", C.c_uint64), ("rejected_calls", C.c_uint64), ("num_sms", C.c_int),
+                ("group_launches", C.c_uint64), ("rejected_calls", C.c_uint64),
+                ("tensor_launches", C.c_uint64), ("num_sms", C.c_int),
                 ("stages", C.c_int), ("smem_bytes", C.c_int)]
 
 
@@ -115,7 +119,7 @@ def _need(t, dtype, name):
 
 # ----------------------------------------------------------------------------- ABI functions
 def moe_plan_create(weights: dict, H: int, I: int, E: int, top_k: int, T_max: int, device: int = -1,
-                    strict: bool = False, pdl: bool = False):
+                    strict: bool = False, pdl: bool = False, kernel: int = MOE_KERNEL_AUTO):
     """weights: dict with gate_q/up_q/down_q/gate_s/up_s/down_s (uint8) and
     gate_ts/up_ts/down_ts (float32) CUDA tensors in the ABI layout."""
     lib = load_library()
@@ -126,7 +130,7 @@ def moe_plan_create(weights: dict, H: int, I: int, E: int, top_k: int, T_max: in
     d = moe_plan_desc(H, I, E, top_k, T_max,
                       *[weights[n].data_ptr() for n in ("gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s",
                                                         "gate_ts", "up_ts", "down_ts")],
-                      device, int(strict), int(pdl))
+                      device, int(strict), int(pdl), int(kernel))
     out = C.c_void_p()
     _check(lib.moe_plan_create(C.byref(d), C.byref(out)))
     return out
@@ -214,11 +218,12 @@ class MoePlan:
     """Owns a plan handle and keeps the weight tensors alive."""
 
     def __init__(self, weights: dict, H: int, I: int, E: int, top_k: int, T_max: int, device=None,
-                 strict: bool = False, pdl: bool = False):
+                 strict: bool = False, pdl: bool = False, kernel: int = MOE_KERNEL_AUTO):
         self.weights = weights
         self.H, self.I, self.E, self.top_k, self.T_max = H, I, E, top_k, T_max
         dev = weights["gate_q"].device.index if device is None else device
-        self.handle = moe_plan_create(weights, H, I, E, top_k, T_max, device=dev, strict=strict, pdl=pdl)
+        self.handle = moe_plan_create(weights, H, I, E, top_k, T_max, device=dev, strict=strict, pdl=pdl,
+                                      kernel=kernel)
 
     def __del__(self):
         h = getattr(self, "handle", None)

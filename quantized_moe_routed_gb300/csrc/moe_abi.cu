@@ -66,6 +66,13 @@ struct moe_plan {
     int smem_attr = 0;  // dynamic smem the kernel attribute currently allows
     // workspace layout (bytes from the base)
     size_t off_done = 0, off_cnt = 0, off_h = 0, off_part = 0, off_xs = 0, ws_bytes = 0;
+    // tensor-core kernel: weight tensor maps (128-row boxes), workspace pieces
+    bool use_tc = false;
+    CUtensorMap tmw[6];
+    int tc_smem_attr = 0;
+    int tc_rows = 0;  // digit rows of xq / hq (4 per pair, at least 64)
+    int Ipad = 0;     // I rounded up to 512
+    size_t off_xq = 0, off_xsf = 0, off_xmul = 0, off_hq = 0, off_hsf = 0, off_hexp = 0, off_apart = 0, off_acnt = 0;
     std::mutex mu;
     moe_stats_t stats{};
 };
@@ -252,6 +259,43 @@ moe_status_t build_tiling(const moe_plan_desc &d, int nt, Tiling &tl)
     return MOE_OK;
 }
 
+// Shapes the tensor-core kernel takes: 256-element K tiles of H and I (whose
+// scale rows are then a whole number of 16-byte TMA units) and at most 32
+// slices of 128 rows in I (the per-pair slice exponent row).
+bool tc_shape_ok(const moe_plan_desc &d) { return d.H % 256 == 0 && d.I % 256 == 0 && d.I <= 4096; }
+
+moe_status_t build_tc_maps(const moe_plan_desc &d, CUtensorMap (&m)[6])
+{
+    const uint64_t rowsGU = static_cast<uint64_t>(d.E) * d.I, rowsD = static_cast<uint64_t>(d.E) * d.H;
+    const PartPlan sp{256, 1, 16, 0, 0};  // scale box: 16 bytes (one 256-element tile) x 128 rows, no swizzle
+    CUresult cr = encode_nib(&m[0], 1, d.gate_q_dev, rowsGU, d.H, moe::kTcRows, 256);
+    if (cr == CUDA_SUCCESS) cr = encode_nib(&m[1], 1, d.up_q_dev, rowsGU, d.H, moe::kTcRows, 256);
+    if (cr == CUDA_SUCCESS) cr = encode_nib(&m[2], 1, d.down_q_dev, rowsD, d.I, moe::kTcRows, 256);
+    if (cr == CUDA_SUCCESS) cr = encode_scale(&m[3], d.gate_s_dev, rowsGU, d.H, moe::kTcRows, sp);
+    if (cr == CUDA_SUCCESS) cr = encode_scale(&m[4], d.up_s_dev, rowsGU, d.H, moe::kTcRows, sp);
+    if (cr == CUDA_SUCCESS) cr = encode_scale(&m[5], d.down_s_dev, rowsD, d.I, moe::kTcRows, sp);
+    if (cr != CUDA_SUCCESS)
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "tensor-map encoding for the tensor-core kernel failed (CUresult %d)",
+                    static_cast<int>(cr));
+    return MOE_OK;
+}
+
+// Row-major uint8 [rows, cols] with a {box_c, box_r} box.
+CUresult encode_rows(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, int box_c, int box_r, bool sw128)
+{
+    const cuuint32_t es[2] = {1, 1};
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_c), static_cast<cuuint32_t>(box_r)};
+    return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// MMA N (digit rows per group) for a launch of T tokens: a group holds at
+// most N/4 pairs, and one expert takes at most T pairs of a launch.
+int tc_n_for(int T) { return T <= 4 ? 16 : (T <= 8 ? 32 : 64); }
+
 moe_status_t check_device(const moe_plan *pl)
 {
     int cur = -1;
@@ -275,6 +319,128 @@ struct WsOffsets {
     size_t off_done, off_cnt, off_h, off_part, off_xs, total;
     int Pmax;  // rows of each part block of xs / hbuf
 };
+
+// The tensor-core kernel over T tokens, in launches of at most Tc tokens.
+moe_status_t run_tc(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, int T, void *ws,
+                    cudaStream_t cs, Path path)
+{
+    {
+        std::lock_guard<std::mutex> lk(pl->mu);
+        if (pl->tc_smem_attr == 0) {
+            cudaError_t e = moe::set_tc_smem_limit(pl->smem_optin);
+            if (e != cudaSuccess) {
+                pl->stats.rejected_calls++;
+                return fail(MOE_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            }
+            pl->tc_smem_attr = pl->smem_optin;
+        }
+    }
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    const moe_plan_desc &d = pl->d;
+    moe::KernelParams p{};
+    p.gq = d.gate_q_dev;
+    p.uq = d.up_q_dev;
+    p.dq = d.down_q_dev;
+    p.gs = d.gate_s_dev;
+    p.us = d.up_s_dev;
+    p.ds = d.down_s_dev;
+    p.gts = d.gate_ts_dev;
+    p.uts = d.up_ts_dev;
+    p.dts = d.down_ts_dev;
+    p.ctrl = reinterpret_cast<uint32_t *>(wsb);
+    p.doneA = reinterpret_cast<uint32_t *>(wsb + pl->off_done);
+    p.cnt = reinterpret_cast<uint32_t *>(wsb + pl->off_cnt);
+    p.part = reinterpret_cast<float *>(wsb + pl->off_part);
+    p.xq = wsb + pl->off_xq;
+    p.xsf = wsb + pl->off_xsf;
+    p.xmul = reinterpret_cast<float *>(wsb + pl->off_xmul);
+    p.hq = wsb + pl->off_hq;
+    p.hsf = wsb + pl->off_hsf;
+    p.hexp = reinterpret_cast<int8_t *>(wsb + pl->off_hexp);
+    p.apart = reinterpret_cast<float *>(wsb + pl->off_apart);
+    p.acnt = reinterpret_cast<uint32_t *>(wsb + pl->off_acnt);
+    p.Pmax = pl->Tc * d.top_k;
+    p.H = d.H;
+    p.I = d.I;
+    p.E = d.E;
+    p.k = d.top_k;
+    p.nHt = d.H / moe::kTcRows;
+    p.Ipad = pl->Ipad;
+    p.timeout_ns = pl->timeout_ns;
+    for (int i = 0; i < 6; ++i) p.tmt[i] = pl->tmw[i];
+    int launches = 0;
+    for (int t0 = 0; t0 < T; t0 += pl->Tc) {
+        const int Tn = (T - t0) < pl->Tc ? (T - t0) : pl->Tc;
+        const int N = tc_n_for(Tn), G = N / 4;
+        const int P = Tn * d.top_k;
+        const int tab = moe::tab_bytes_for(P, Tn);
+        const int stage = moe::tc_stage_bytes(N);
+        const int ep_scratch = 16 * moe::kTcRows * 4;  // the epilogue's h rows, [pair][128] fp32
+        int ns = (pl->tc_smem_attr - tab - ep_scratch - 1024) / stage;
+        if (ns > moe::kTcMaxStages) ns = moe::kTcMaxStages;
+        if (ns > (512 - 4 * N) / 64) ns = (512 - 4 * N) / 64;  // tensor-memory columns: 4N + 64 per stage
+        const int scr = align16i(2 * P) + 8 * d.E + 16;  // grouping scratch, aliases the ring
+        if (ns < 2 || scr > ns * stage) {
+            reject(pl);
+            return fail(MOE_ERR_UNSUPPORTED_SHAPE, "tensor-core kernel: shared memory does not fit (%d stages)", ns);
+        }
+        // K splits of the gate/up units: enough tickets for two per SM while
+        // every split keeps >= 2 stages and the partial buffer holds them
+        const int TA = d.I / moe::kTcRows;
+        int ngmax = d.E + P / G;
+        if (ngmax > P) ngmax = P;
+        const long units = static_cast<long>(ngmax) * TA;
+        int KS = 1;
+        while (KS < 8 && units * KS < 2L * pl->num_sms && (d.H / (2 * KS)) % 256 == 0 && d.H / (2 * KS) >= 512 &&
+               units * 2 * KS <= moe::kTcApartUnits)
+            KS *= 2;
+        if (const char *ks = std::getenv("MOE_TC_KSPLIT")) {  // tuning override: 1, 2, 4 or 8
+            const int v = std::atoi(ks);
+            if ((v == 1 || v == 2 || v == 4 || v == 8) && d.H % (256 * v) == 0 && units * v <= moe::kTcApartUnits) KS = v;
+        }
+        // x digit rows per token when every token's rows fit one MMA (N = 4T
+        // rounded up to 16, T <= 16); else per sorted pair
+        p.xtok = Tn <= 16 ? 1 : 0;
+        const uint64_t xrows = p.xtok ? static_cast<uint64_t>(4 * Tn) : static_cast<uint64_t>(pl->tc_rows);
+        CUresult cr = encode_rows(&p.tmt[6], p.xq, xrows, d.H / 2, 128, N, true);
+        if (cr == CUDA_SUCCESS) cr = encode_rows(&p.tmt[7], p.xsf, xrows, d.H / 16, 16, N, false);
+        if (cr == CUDA_SUCCESS) cr = encode_rows(&p.tmt[8], p.hq, pl->tc_rows, pl->Ipad / 2, 128, N, true);
+        if (cr == CUDA_SUCCESS) cr = encode_rows(&p.tmt[9], p.hsf, pl->tc_rows, pl->Ipad / 16, 16, N, false);
+        if (cr != CUDA_SUCCESS) {
+            reject(pl);
+            return fail(MOE_ERR_CUDA, "tensor-map encoding of the workspace failed (CUresult %d)", static_cast<int>(cr));
+        }
+        p.T = Tn;
+        p.x = static_cast<const uint16_t *>(x) + static_cast<size_t>(t0) * d.H;
+        p.ids = ids + static_cast<size_t>(t0) * d.top_k;
+        p.w = w + static_cast<size_t>(t0) * d.top_k;
+        p.y = y + static_cast<size_t>(t0) * d.H;
+        p.NS = ns;
+        p.stage_bytes = stage;
+        p.tab_off = ns * stage;
+        p.red_off = p.tab_off + (tab + 15) / 16 * 16;
+        p.tcN = N;
+        p.KS = KS;
+        const int total = p.red_off + ep_scratch + 1024;
+        cudaError_t e = moe::launch_tc(p, pl->num_sms, total, pl->pdl, cs);
+        if (e != cudaSuccess) {
+            reject(pl);
+            return fail(MOE_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+        }
+        ++launches;
+    }
+    {
+        std::lock_guard<std::mutex> lk(pl->mu);
+        if (path == Path::Prefill) pl->stats.prefill_launches += launches;
+        else pl->stats.decode_launches += launches;
+        pl->stats.tensor_launches += launches;
+    }
+    if (!env_flag("MOE_QUIET"))
+        std::call_once(g_active_once, [&] {
+            std::fprintf(stderr, "moe_nvfp4: sm_103a routed-experts tensor-core kernel ACTIVE (%d SMs)\n", pl->num_sms);
+        });
+    return MOE_OK;
+}
 
 moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, int T, void *ws,
                       void *stream, Path path, const WsOffsets *wo = nullptr)
@@ -305,6 +471,8 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
         reject(pl);
         return st;
     }
+    if (pl->use_tc && path != Path::Null && !wo)
+        return run_tc(pl, x, ids, w, y, T, ws, static_cast<cudaStream_t>(stream), path);
     // kernel smem attribute: allow up to the device's opt-in limit (once per plan)
     {
         std::lock_guard<std::mutex> lk(pl->mu);
@@ -546,6 +714,25 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
             return ts;
         }
     }
+    if (d.kernel < MOE_KERNEL_AUTO || d.kernel > MOE_KERNEL_TENSOR) {
+        delete pl;
+        return fail(MOE_ERR_INVALID_ARG, "kernel=%d is not a MOE_KERNEL_* value", d.kernel);
+    }
+    if (d.kernel == MOE_KERNEL_TENSOR && !tc_shape_ok(d)) {
+        delete pl;
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE,
+                    "the tensor-core kernel takes H and I multiples of 256 and I <= 4096 (H=%d, I=%d)", d.H, d.I);
+    }
+    // automatic choice: the register kernel (measured faster on the decode
+    // workloads so far); the tensor-core kernel on request
+    pl->use_tc = d.kernel == MOE_KERNEL_TENSOR;
+    if (pl->use_tc) {
+        const moe_status_t ts = build_tc_maps(d, pl->tmw);
+        if (ts != MOE_OK) {
+            delete pl;
+            return ts;
+        }
+    }
     const int tc = moe::kMaxPairs / d.top_k;
     pl->Tc = d.T_max < tc ? d.T_max : tc;
     const moe::SmemLayout L = layout_for(pl, pl->Tc);
@@ -568,6 +755,27 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
     o = up(o + 4 * Pc * d.H, 256);
     pl->off_xs = o;
     o = up(o + 2 * Pc * d.H, 256);
+    if (pl->use_tc) {
+        const size_t rows = 4 * Pc < 64 ? 64 : 4 * Pc;
+        pl->tc_rows = static_cast<int>(rows);
+        pl->Ipad = (d.I + 511) / 512 * 512;
+        pl->off_xq = o;
+        o = up(o + rows * (d.H / 2), 256);
+        pl->off_xsf = o;
+        o = up(o + rows * (d.H / 16), 256);
+        pl->off_xmul = o;
+        o = up(o + rows * 4, 256);
+        pl->off_hq = o;
+        o = up(o + rows * (pl->Ipad / 2), 256);
+        pl->off_hsf = o;
+        o = up(o + rows * (pl->Ipad / 16), 256);
+        pl->off_hexp = o;
+        o = up(o + rows * 16, 256);
+        pl->off_apart = o;
+        o = up(o + static_cast<size_t>(moe::kTcApartUnits) * 2 * 16 * moe::kTcRows * 4, 256);
+        pl->off_acnt = o;
+        o = up(o + static_cast<size_t>(moe::kTcApartUnits) * 4, 256);
+    }
     pl->ws_bytes = o;
     pl->stats.num_sms = sms;
     pl->stats.stages = L.NS;

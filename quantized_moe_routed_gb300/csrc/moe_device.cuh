@@ -1,0 +1,458 @@
+// moe_device.cuh -- device-side pieces shared by the two step kernels
+// (moe_kernels.cu: dequantise-in-registers path; moe_tc.cu: tensor-core
+// block-scaled path): PTX wrappers (mbarrier, TMA, acquire/release), the
+// CTA control block, the in-CTA grouping of the T*k pairs and the bounded
+// waits.  Included inside namespace moe { namespace { ... } }.
+#pragma once
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t gtimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma2d(void *dst, const CUtensorMap *tm, int c0, int c1, uint64_t *bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *tm, int c0, int c1, int c2, uint64_t *bar,
+                                      uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+
+
+// CTA-scope acquire / release on shared memory: order this thread's later
+// (earlier) accesses after (before) the flag, without the full fence that
+// would also wait for this thread's unrelated global loads in flight.
+__device__ __forceinline__ int ld_acq_cta(const int *a)
+{
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(a)) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_rel_cta(int *a, int v)
+{
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(a)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acq_cta_u8(const uint8_t *a)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u8 %0, [%1];" : "=r"(v) : "r"(smem_u32(a)) : "memory");
+    return static_cast<int>(v);
+}
+
+__device__ __forceinline__ void st_rel_cta_u8(uint8_t *a, int v)
+{
+    asm volatile("st.release.cta.shared::cta.u8 [%0], %1;" ::"r"(smem_u32(a)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int atom_add_acqrel_cta(int *a, int v)
+{
+    int old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(a)), "r"(v) : "memory");
+    return old;
+}
+
+// Four E2M1 pairs (one 32-bit word, element 2i in the low nibble of byte i)
+// -> four f16x2 {element 2i (low half), element 2i+1 (high half)}.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t &o0, uint32_t &o1, uint32_t &o2, uint32_t &o3)
+{
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+        : "r"(w));
+}
+
+// Two E4M3 scale bytes (low byte first) -> f16x2 {low, high}; exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v)
+{
+    uint32_t o;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o) : "h"(v));
+    return o;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Two bf16 (element 2i low) -> f16x2 (round to nearest even; exact in range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u)
+{
+    float lo = __uint_as_float(u << 16), hi = __uint_as_float(u & 0xffff0000u);
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t u4w(const uint4 &v, int i)
+{
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// ------------------------------------------------------------------ shared state
+constexpr int kDoneQ = 16;  // finished tickets in flight from the consumers to the helper
+constexpr int kTq = 4;      // tickets fetched ahead (helper -> producer)
+
+// CTA-shared control block.  The roles talk through single-writer fields:
+//   tq       helper -> producer    tickets fetched ahead
+//   pq       producer -> helper    stages whose activation rows the helper copies
+//                                  (x before it is gathered, h of every down part)
+//   redbar   consumers             ticket-end arrivals of the 8 consumer warps
+//   dq       consumers -> helper   finished tickets, slot = ticket sequence number % kDoneQ
+struct SmemHdr {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    int4 stage_hdr[kMaxStages];  // {kind, group, tile, part}
+    uint64_t redbar[2];
+    int n_groups, n_valid, n_bad, abort_flag;  // abort_flag: any role gave up (read by every wait)
+    int fill_cnt, cons_exited, red_cnt, xready;
+    int tq_head, tq_tail, dq_head, pq_tail;
+    int pq_head, claim, pad1, pad2;
+    int tq_buf[kTq];
+    int pq_stage[kMaxStages], pq_grp[kMaxStages], pq_part[kMaxStages], pq_kind[kMaxStages];
+    int dq_seq[kDoneQ], dq_kind[kDoneQ], dq_grp[kDoneQ], dq_tile[kDoneQ];
+    // tensor-core kernel only: stage scale factors in tensor memory (scale
+    // warps -> MMA thread), accumulator buffers (MMA thread <-> epilogue),
+    // the ticket each accumulator buffer holds, the tensor-memory base and
+    // the epilogue's cross-warp scratch
+    uint64_t sfready[kMaxStages];
+    uint64_t accfull[2], accempty[2];
+    int4 tinfo[2];  // {kind, group, tile, k-split}
+    uint64_t mma_done;
+    uint64_t epibar;  // the four epilogue warps' meeting point (bounded waits)
+    int tseq[2];    // accumulator buffer use published with tinfo (release/acquire)
+    uint32_t tmem_base;
+    int ep_last;
+    float ep_amax[4][16];
+    int ep_exp[16];  // h prescale exponents of the epilogue's pairs
+    int grouped;     // grouping tables complete (warps 8-11 -> warps 0-7)
+};
+static_assert(sizeof(SmemHdr) <= kTabHdrBytes, "header too large");
+
+// KIND_AX: a gate/up part issued before the gathered x was published: its
+// stage holds the group's x rows copied straight from the caller's bf16 x
+// (natural element order, one row per pair), which the consumers convert.
+enum { KIND_A = 0, KIND_B = 1, KIND_END = 2, KIND_AX = 3 };
+
+struct Tabs {
+    SmemHdr *hdr;
+    uint16_t *perm;   // [P] sorted pair list (flat pair index t*k+j)
+    uint16_t *pos;    // [P] inverse: sorted position of pair p, 0xFFFF if invalid
+    uint16_t *gexp;   // [P] group -> expert
+    uint16_t *gbeg;   // [P] group -> first sorted position
+    uint16_t *stok;   // [P] sorted position -> token
+    uint8_t *gcnt;    // [P] group -> number of pairs (1..16)
+    uint8_t *hready;  // [P] group -> 0 unknown, 1 polled by the helper, 2 h rows complete
+    uint8_t *kvalid;  // [T] valid slots per token
+};
+
+__host__ __device__ inline int align16(int v) { return (v + 15) & ~15; }
+
+__device__ Tabs make_tabs(uint8_t *smem, int tab_off, int P)
+{
+    Tabs t;
+    uint8_t *b = smem + tab_off;
+    t.hdr = reinterpret_cast<SmemHdr *>(b);
+    int o = kTabHdrBytes;
+    t.perm = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
+    t.pos = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
+    t.gexp = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
+    t.gbeg = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
+    t.stok = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
+    t.gcnt = b + o; o += align16(P);
+    t.hready = b + o; o += align16(P);
+    t.kvalid = b + o;
+    return t;
+}
+
+// ------------------------------------------------------------------ grouping
+// Stable counting sort of the P flat pairs p = t*k + j by expert id, run by all
+// threads of the CTA.  Scratch (ids16 [P], ecnt [E], eoff [E+1]) may alias
+// anything not otherwise live.  Results: perm/pos (see Tabs), *n_valid, *n_bad,
+// eoff (exclusive offsets, eoff[E] = n_valid) and ecnt (counts).
+__device__ void group_pairs(const int32_t *__restrict__ ids, int P, int E, int16_t *ids16, int32_t *ecnt,
+                            int32_t *eoff, uint16_t *perm, uint16_t *pos, int *n_valid, int *n_bad)
+{
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) *n_bad = 0;
+    for (int e = tid; e < E; e += nthr) ecnt[e] = 0;
+    __syncthreads();
+    int bad = 0;
+    for (int p = tid; p < P; p += nthr) {
+        int e = ids[p];
+        if (e >= E) ++bad;
+        ids16[p] = (e >= 0 && e < E) ? static_cast<int16_t>(e) : static_cast<int16_t>(-1);
+    }
+    if (bad) atomicAdd(n_bad, bad);
+    __syncthreads();
+    for (int p = tid; p < P; p += nthr) {
+        int e = ids16[p];
+        if (e >= 0) atomicAdd(&ecnt[e], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive scan of ecnt over E entries, lanes own contiguous ranges
+        const int per = (E + 31) / 32;
+        const int lo = min(E, lane * per), hi = min(E, lo + per);
+        int s = 0;
+        for (int e = lo; e < hi; ++e) s += ecnt[e];
+        int incl = s;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        int run = incl - s;
+        for (int e = lo; e < hi; ++e) {
+            eoff[e] = run;
+            run += ecnt[e];
+        }
+        if (lane == 31) eoff[E] = incl;
+        __syncwarp();
+        // stable scatter: pairs in index order, 32 at a time
+        for (int base = 0; base < P; base += 32) {
+            const int p = base + lane;
+            const int e = (p < P) ? ids16[p] : -2;
+            const uint32_t peers = __match_any_sync(0xffffffffu, e);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            int dst = 0;
+            if (e >= 0) dst = eoff[e] + rank;  // eoff doubles as the running cursor
+            __syncwarp();
+            if (e >= 0) {
+                perm[dst] = static_cast<uint16_t>(p);
+                pos[p] = static_cast<uint16_t>(dst);
+                if (rank == 0) eoff[e] += __popc(peers);
+            } else if (p < P) {
+                pos[p] = 0xFFFFu;
+            }
+            __syncwarp();
+        }
+        // restore exclusive offsets (the cursor now points one past each range)
+        for (int e = lo; e < hi; ++e) eoff[e] -= ecnt[e];
+        __syncwarp();
+        if (lane == 0) *n_valid = eoff[E];
+    }
+    __syncthreads();
+}
+
+// Grouping of at most 32 pairs by one warp, in registers: lane p holds pair p;
+// its rank in the (expert, pair index) order is counted against every other
+// lane, which gives the same stable order as the counting sort.  Groups are
+// the runs of equal experts in that order, cut every G pairs.  Writes perm,
+// pos, stok, gexp/gbeg/gcnt and the header counts; the caller syncs.
+__device__ void group_pairs_warp(const KernelParams &p, int P, int G, Tabs tb)
+{
+    SmemHdr *hd = tb.hdr;
+    const int lane = threadIdx.x & 31;
+    int e = -1;
+    if (lane < P) e = p.ids[lane];
+    const bool valid = lane < P && e >= 0 && e < p.E;
+    const uint32_t badm = __ballot_sync(0xffffffffu, lane < P && e >= p.E);
+    const int key = valid ? e : 0x7fffffff;  // invalid pairs sort last
+    int rank = 0;
+    for (int j = 0; j < P; ++j) {
+        const int kj = __shfl_sync(0xffffffffu, key, j);
+        rank += (kj < key || (kj == key && j < lane)) ? 1 : 0;
+    }
+    const int nv = __popc(__ballot_sync(0xffffffffu, valid));
+    if (lane < P) tb.pos[lane] = valid ? static_cast<uint16_t>(rank) : 0xFFFFu;
+    if (valid) tb.perm[rank] = static_cast<uint16_t>(lane);
+    __syncwarp();
+    // sorted position r = lane: its pair, expert, token
+    const int pr = lane < nv ? tb.perm[lane] : 0;
+    const int er = __shfl_sync(0xffffffffu, e, pr);
+    if (lane < nv) tb.stok[lane] = static_cast<uint16_t>(pr / p.k);
+    const int eprev = __shfl_up_sync(0xffffffffu, er, 1);
+    const uint32_t runm = __ballot_sync(0xffffffffu, lane < nv && (lane == 0 || eprev != er));
+    const int rs = 31 - __clz(runm & (0xffffffffu >> (31 - lane)));  // start of this lane's run
+    const uint32_t above = runm & ~(0xffffffffu >> (31 - lane));        // run starts after this lane
+    const int re = above ? __ffs(above) - 1 : nv;                      // end of the run
+    const int off = lane - rs;
+    const bool head = lane < nv && off % G == 0;
+    const uint32_t headm = __ballot_sync(0xffffffffu, head);
+    if (head) {
+        const int gi = __popc(headm & (0xffffffffu >> (31 - lane))) - 1;
+        tb.gexp[gi] = static_cast<uint16_t>(er);
+        tb.gbeg[gi] = static_cast<uint16_t>(lane);
+        tb.gcnt[gi] = static_cast<uint8_t>(min(G, re - lane));
+    }
+    if (lane == 0) {
+        hd->n_valid = nv;
+        hd->n_bad = __popc(badm);
+        hd->n_groups = __popc(headm);
+    }
+}
+
+// ------------------------------------------------------------------ bounded waits
+__device__ __noinline__ void raise_error(const KernelParams &p, volatile int *abort_flag, uint32_t bits)
+{
+    atomicOr(p.ctrl + 2, bits);
+    if (abort_flag) *abort_flag = 1;
+}
+
+// Wait for an mbarrier phase; false if the CTA aborted or the wait timed out.
+__device__ bool wait_bar(uint64_t *bar, uint32_t parity, const KernelParams &p, volatile int *abort_flag)
+{
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_test(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
+                raise_error(p, abort_flag, kErrTimeout);
+                return false;
+            }
+            if ((it & 1023u) == 0 && (ld_relaxed(p.ctrl + 2) & kErrTimeout)) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait on an mbarrier phase.  Every lane polls the barrier itself
+// (acquire); the verdict is made warp-uniform with a vote, so a lane that
+// gave up (abort flag, timeout) takes the whole warp out.
+__device__ __forceinline__ bool warp_wait_bar(const KernelParams &p, uint64_t *bar, uint32_t ph,
+                                              volatile int *abort_flag)
+{
+    bool ok = mbar_test(bar, ph);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if (!ok) ok = wait_bar(bar, ph, p, abort_flag);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded per-lane spin until pred() (a CTA-shared flag read with acquire);
+// warp-uniform verdict.
+template <class Pred>
+__device__ __forceinline__ bool warp_spin(const KernelParams &p, Pred pred, volatile int *abort_flag)
+{
+    bool ok = pred();
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if (!ok) {
+        const uint64_t t0 = gtimer();
+        for (uint32_t it = 1;; ++it) {
+            if (pred()) { ok = true; break; }
+            if ((it & 15u) == 0) {
+                if (*abort_flag) break;
+                if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
+                    raise_error(p, abort_flag, kErrTimeout);
+                    break;
+                }
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Hand a finished ticket to the helper: slot = ticket sequence number.  The
+// warp's global stores (and, through the acq_rel ticket counter, those of the
+// other seven warps) precede the release; the helper releases them at gpu
+// scope.
+__device__ __forceinline__ bool push_done(const KernelParams &p, SmemHdr *hd, int tick, int kind, int grp, int tile,
+                                          int lane, volatile int *abort_flag)
+{
+    __syncwarp();
+    const int need = tick - kDoneQ + 1;
+    if (!warp_spin(p, [&] { return ld_acq_cta(&hd->dq_head) >= need; }, abort_flag)) return false;
+    if (lane == 0) {
+        const int slot = tick % kDoneQ;
+        hd->dq_kind[slot] = kind;
+        hd->dq_grp[slot] = grp;
+        hd->dq_tile[slot] = tile;
+        st_rel_cta(&hd->dq_seq[slot], tick + 1);
+    }
+    __syncwarp();
+    return true;
+}

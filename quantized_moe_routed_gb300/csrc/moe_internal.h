@@ -27,10 +27,10 @@ constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrBadId = 2u;
 constexpr uint32_t kErrRange = 4u;
 
-// Shared-memory tables of the step kernel: a 2048-byte control block, then
+// Shared-memory tables of the step kernel: a 3072-byte control block, then
 // five uint16 arrays of P entries, two uint8 arrays of P and one of T, each
 // padded to 16 bytes; the whole rounded up to 128 bytes.
-constexpr int kTabHdrBytes = 2048;
+constexpr int kTabHdrBytes = 3072;
 inline int tab_bytes_for(int P, int T)
 {
     const int a2 = (2 * P + 15) & ~15, a1 = (P + 15) & ~15, aT = (T + 15) & ~15;
@@ -82,6 +82,22 @@ struct KernelParams {
     int ntiles;                                 // kernel variant: n-tiles per group (1 or 2)
     long long timeout_ns;
     int null_mode;      // 1: measurement variant (no dequant / math)
+
+    // ---- tensor-core path (moe_tc.cu) ----
+    // TMA descriptors: 0 gate_q, 1 up_q, 2 down_q (box 128 B x 128 rows, 128-byte
+    // swizzle); 3 gate_s, 4 up_s, 5 down_s (box 16 B x 128 rows); 6 xq, 8 hq
+    // (box 128 B x tcN rows, 128-byte swizzle); 7 xsf, 9 hsf (box 16 B x tcN rows)
+    CUtensorMap tmt[10];
+    uint8_t *xq, *xsf;  // [Pmax*4][H/2], [Pmax*4][H/16]: each sorted pair's x as 4 FP4 digit rows
+    float *xmul;        // [Pmax*4] multiplier of each x digit row
+    uint8_t *hq, *hsf;  // [Pmax*4][Ipad/2], [Pmax*4][Ipad/16]: h digit rows
+    int8_t *hexp;       // [Pmax][32]: prescale exponent of each 128-row slice of h
+    float *apart;       // split-K partial gate/up sums
+    uint32_t *acnt;     // split-K arrivals per gate/up unit
+    int tcN;            // MMA N: digit rows per group (16, 32 or 64; a group has <= tcN/4 pairs)
+    int KS;             // K splits of a gate/up unit (1, 2, 4 or 8)
+    int Ipad;           // I rounded up to 512
+    int xtok;           // 1: x digit rows per token (gate/up MMAs take all tokens, T <= 16); 0: per sorted pair
 };
 
 // Dynamic shared memory layout of the persistent kernel for P pairs.
@@ -95,6 +111,18 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, uint32_t *ctrl, int32
                          int32_t *offsets, int32_t *perm, cudaStream_t st);
 cudaError_t launch_poison(uint32_t *doneA, int n, cudaStream_t st);
 cudaError_t set_step_smem_limit(int bytes);
+// Tensor-core path (moe_tc.cu).
+constexpr int kTcThreads = 384;    // 12 warps: 4 scale, 4 epilogue, producer, MMA, helper, release
+constexpr int kTcRows = 128;       // weight rows per tile (MMA M) and per ticket
+constexpr int kTcMaxStages = 8;
+constexpr int kTcApartUnits = 1024;  // split-K (unit, split) slots of the partial buffer
+inline int tc_stage_bytes(int N)
+{
+    const int end = 36864 + 2 * N * 128 + 2 * N * 16 + 16 * 32;
+    return (end + 1023) / 1024 * 1024;
+}
+cudaError_t launch_tc(const KernelParams &p, int grid, int smem_bytes, bool pdl, cudaStream_t st);
+cudaError_t set_tc_smem_limit(int bytes);
 int group_smem_bytes(int P, int E);
 
 }  // namespace moe

@@ -1,0 +1,1399 @@
+// moe_tc.cu -- sm_103a tensor-core path of the routed-experts MoE step:
+//   y_t = sum_j w_tj * W_down[e_tj] ( SiLU(W_gate[e_tj] x_t) (.) (W_up[e_tj] x_t) )
+// with every weight byte consumed by the 5th-generation tensor cores straight
+// from its NVFP4 encoding (tcgen05.mma kind::mxf4nvf4, block_scale,
+// scale_vec::4X: E2M1 operands, one E4M3 scale per 16 elements).
+//
+// The block-scaled MMA takes FP4 on both sides, so each activation row (x for
+// gate/up, h for down) enters as the sum of four NVFP4 "digit" rows: digit j
+// holds 4^j times the residual left by digits 0..j-1, quantised per 16-element
+// block with an E4M3 scale rounded up (so no element saturates) and E2M1
+// round-to-nearest-even, after one power-of-two prescale that puts the row's
+// largest magnitude in (1344, 2688].  Each digit is one MMA column; the fp32
+// epilogue sums a pair's four columns with weights 4^-j * 2^-prescale.  The
+// representation error after four digits is about 2^-9 of a block's
+// magnitude, far inside the step's 2e-3 tolerance (it sits near 1.5e-4 on the
+// synthetic NVFP4 experts).  h is produced 128 rows at a time, before its
+// whole row is known, so each 128-row slice gets its own prescale; the
+// scale-factor pass of a down stage rebases every slice's block scales to the
+// row's largest slice (an exact exponent shift unless a scale leaves the
+// E4M3 normal range, which only happens 2^14 below the row's largest slice).
+//
+// Work is split into tickets exactly as in the register path (moe_kernels.cu):
+// gate/up units of 128 intermediate rows (optionally split along K into KS
+// tickets whose fp32 partials the last arriver sums in split order), then
+// down tickets of 128 output rows, all on one atomic counter, no grid barrier.
+// A CTA (one per SM) runs twelve warps:
+//   warps 0-3   scale warps: per stage, move the weight and activation block
+//               scales from shared memory into tensor memory (tcgen05.st) in
+//               the layout the MMA reads (row r: lane r, column + r/32),
+//               rebasing h slice exponents on the way
+//   warps 4-7   epilogue: read the accumulators (tcgen05.ld), combine digits,
+//               split-K partials, SiLU * up, quantise h into digits (gate/up)
+//               or write per-pair down outputs
+//   warp 8      producer: TMA copies of weight tiles, their scales and x digits
+//   warp 9      MMA issue (one thread) and tensor-memory allocation
+//   warp 10     helper: tickets, dependency watch, h digit copies
+//   warp 11     release: cross-CTA counters and the slot-ordered combine
+// Warps 0-7 first quantise the gathered x rows into digits (rows claimed in
+// batches from a global counter, as in the register path).
+#include "moe_internal.h"
+
+#include <cuda_fp16.h>
+
+namespace moe {
+namespace {
+
+#include "moe_device.cuh"
+
+// ------------------------------------------------------------------ constants
+constexpr int kTcWarps = kTcThreads / 32;
+constexpr int kTile = 128 * 128;  // bytes of an E2M1 tile: 128 rows x 256 elements
+constexpr int kSfTile = 128 * 16; // bytes of its block scales
+constexpr int kOffW0 = 0, kOffW1 = kTile, kOffS0 = 2 * kTile, kOffS1 = 2 * kTile + kSfTile;
+constexpr int kOffB0 = 36864;     // activation digit rows (1024-aligned)
+constexpr int kTmemCols = 512;
+// Tensor memory: accumulators in columns [0, 4N) (two buffers of gate + up, or
+// of down), then 64 columns of scale factors per stage from column 4N: four
+// sets of 16 (gate or first tile, up or second tile, activation first K
+// range, activation second K range), K step kk of a set at +4kk.  Every
+// tensor-memory address used is a multiple of 4 columns.
+constexpr float kPreMax = 2688.f; // largest prescaled magnitude: 6 * 448
+
+
+__device__ __forceinline__ int offB1(int N) { return kOffB0 + N * 128; }
+__device__ __forceinline__ int offSB0(int N) { return kOffB0 + 2 * N * 128; }
+__device__ __forceinline__ int offSB1(int N) { return kOffB0 + 2 * N * 128 + N * 16; }
+__device__ __forceinline__ int offHX(int N) { return kOffB0 + 2 * N * 128 + 2 * N * 16; }
+
+// ------------------------------------------------------------------ tcgen05 wrappers
+__device__ __forceinline__ void tc_alloc(uint32_t *dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+// D[128 x N] (+)= A[128 x 64] * B[N x 64]^T, E2M1 operands, E4M3 block scales per 16 along K
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t acc)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+        : "memory");
+}
+// Row data w[0..3] (K steps 0..3 of a set) to 16 columns of this warp's lanes,
+// each word repeated over its 4 columns: lane quarter q reads column 4kk + q.
+__device__ __forceinline__ void tc_st_set(uint32_t taddr, uint4 w)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %1, %1, %1, %2, %2, %2, %2, %3, %3, %3, %3, %4, %4, %4, %4};" ::"r"(taddr),
+                 "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w)
+                 : "memory");
+}
+// Activation scale set: the MMA's datapath for each lane quarter reads the B
+// scales from its own quarter's lanes (lane 32q + n%32, column 4kk + n/32), so
+// every warp writes rows lo = lane (column 4kk) and hi = 32 + lane (column
+// 4kk + 1; only read when N = 64).
+__device__ __forceinline__ void tc_st_bset(uint32_t taddr, uint4 lo, uint4 hi)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %5, %1, %5, %2, %6, %2, %6, %3, %7, %3, %7, %4, %8, %4, %8};" ::"r"(taddr),
+                 "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&r)[16])
+{
+    uint32_t u[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]), "=r"(u[8]),
+          "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = __uint_as_float(u[i]);
+}
+__device__ __forceinline__ void tc_ld4(uint32_t taddr, float4 &r)
+{
+    uint32_t a, b, c, d;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "r"(taddr)
+                 : "memory");
+    r = make_float4(__uint_as_float(a), __uint_as_float(b), __uint_as_float(c), __uint_as_float(d));
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major rows of 128 bytes, 128-byte swizzle,
+// 8-row groups 1024 bytes apart (tcgen05 descriptor version 1).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
+}
+// Instruction descriptor, kind::mxf4nvf4: E2M1 A and B (format 1), K-major both,
+// E4M3 scales, M = 128, N = n.
+__device__ __forceinline__ uint32_t fp4_idesc(int n)
+{
+    return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ FP4 digits
+// Value of a non-negative E4M3 code (0 .. 0x7E).
+__device__ __forceinline__ float e4m3_value(uint32_t c)
+{
+    const uint32_t E = c >> 3, m = c & 7u;
+    return E ? __uint_as_float(((E + 120u) << 23) | (m << 20)) : static_cast<float>(m) * 0.001953125f;
+}
+// Smallest E4M3 value >= a (a >= 0), saturating at 448: its code, and the value in s.
+__device__ __forceinline__ uint32_t e4m3_ceil(float a, float &s)
+{
+    uint32_t c;
+    asm("{\n .reg .b16 t;\n cvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n cvt.u32.u16 %0, t;\n}" : "=r"(c) : "f"(0.f), "f"(a));
+    c &= 0x7Fu;
+    float v = e4m3_value(c);
+    if (v < a && c < 0x7Eu) {
+        ++c;
+        v = e4m3_value(c);
+    }
+    s = v;
+    return c;
+}
+// Two values -> one byte of E2M1 codes (lo in the low nibble), RNE, saturating.
+__device__ __forceinline__ uint32_t e2m1_pack2(float lo, float hi)
+{
+    uint32_t r;
+    asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// Values of the two E2M1 codes of a byte (element 2i low nibble).
+__device__ __forceinline__ float2 e2m1_unpack2(uint32_t b)
+{
+    uint32_t o;
+    asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(o) : "r"(b));
+    return __half22float2(*reinterpret_cast<const __half2 *>(&o));
+}
+
+// Quantise one 16-element block, prescaled, into four digits: digit j encodes
+// 4^j times the residual r_j, E4M3 scale rounded up, E2M1 RNE.  r is consumed
+// (left as the final residual); pk[j] = the 8 code bytes, sc[j] = scale code.
+__device__ __forceinline__ void quant_block4(float (&r)[16], uint2 (&pk)[4], uint32_t (&sc)[4])
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float f = static_cast<float>(1 << (2 * j));
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(r[i]));
+        float s;
+        sc[j] = e4m3_ceil(amax * f * (1.0f / 6.0f), s);
+        uint32_t w[2] = {0u, 0u};
+        if (s > 0.f) {
+            const float inv = f / s, back = s / f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t b = e2m1_pack2(r[2 * i] * inv, r[2 * i + 1] * inv);
+                w[i >> 2] |= b << (8 * (i & 3));
+                const float2 d = e2m1_unpack2(b);
+                r[2 * i] -= d.x * back;
+                r[2 * i + 1] -= d.y * back;
+            }
+        }
+        pk[j] = make_uint2(w[0], w[1]);
+    }
+}
+
+// Prescale exponent e of a row (or slice) with largest magnitude a > 0:
+// a * 2^e in (1344, 2688]; 100 for a == 0 (no data), clamped to [-100, 100].
+__device__ __forceinline__ int prescale_exp(float a)
+{
+    if (!(a > 0.f)) return 100;
+    if (!(a < 3.0e38f)) return -100;
+    const uint32_t u = __float_as_uint(a);
+    int E = static_cast<int>((u >> 23) & 0xFFu) - 127;
+    float m = __uint_as_float((u & 0x007FFFFFu) | 0x3F800000u);
+    if (E == -127) {  // subnormal a: normalise
+        const float an = a * 8388608.f;  // 2^23
+        const uint32_t un = __float_as_uint(an);
+        E = static_cast<int>((un >> 23) & 0xFFu) - 127 - 23;
+        m = __uint_as_float((un & 0x007FFFFFu) | 0x3F800000u);
+    }
+    const int e = (m <= 1.3125f ? 11 : 10) - E;
+    return max(-100, min(100, e));
+}
+__device__ __forceinline__ float exp2i(int e)  // 2^e for -126 <= e <= 127
+{
+    return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+__device__ __forceinline__ float mul_pow2(float v, int e)  // v * 2^e, e in [-200, 200]
+{
+    const int e1 = e / 2, e2 = e - e1;
+    return v * exp2i(max(-126, min(127, e1))) * exp2i(max(-126, min(127, e2)));
+}
+
+// An E4M3 scale code (0 .. 0x7E) times 2^-d (d >= 0), rounded to nearest even.
+__device__ __forceinline__ uint32_t e4m3_shift_down(uint32_t c, int d)
+{
+    if (d <= 0 || c == 0u) return c;
+    const uint32_t E = c >> 3, m = c & 7u;
+    if (static_cast<int>(E) - d >= 1) return c - (static_cast<uint32_t>(d) << 3);
+    // result is subnormal: significand S at exponent position, shifted right by k
+    const uint32_t S = E ? (8u | m) : m;
+    const int k = (E ? 1 - (static_cast<int>(E) - d) : d);  // >= 1
+    if (k > 8) return 0u;
+    const uint32_t q = S >> k, rem = S & ((1u << k) - 1u), half = 1u << (k - 1);
+    return q + ((rem > half || (rem == half && (q & 1u))) ? 1u : 0u);
+}
+
+// ------------------------------------------------------------------ prologue
+__device__ __forceinline__ void grp_sync()  // warps 8-11
+{
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// Stable counting sort of the P pairs by expert on warps 8-11 (128 threads),
+// the same order as the register kernel's grouping: counts, exclusive scan and
+// a stable scatter by the first of these warps.
+__device__ void tc_group_pairs(const KernelParams &p, int P, int16_t *ids16, int32_t *ecnt, int32_t *eoff, Tabs tb)
+{
+    SmemHdr *hd = tb.hdr;
+    const int lt = threadIdx.x - 256, lane = lt & 31, E = p.E;
+    if (lt == 0) hd->n_bad = 0;
+    for (int e = lt; e < E; e += 128) ecnt[e] = 0;
+    grp_sync();
+    int bad = 0;
+    for (int q = lt; q < P; q += 128) {
+        const int e = p.ids[q];
+        if (e >= E) ++bad;
+        ids16[q] = (e >= 0 && e < E) ? static_cast<int16_t>(e) : static_cast<int16_t>(-1);
+    }
+    if (bad) atomicAdd(&hd->n_bad, bad);
+    grp_sync();
+    for (int q = lt; q < P; q += 128) {
+        const int e = ids16[q];
+        if (e >= 0) atomicAdd(&ecnt[e], 1);
+    }
+    grp_sync();
+    if (lt < 32) {
+        const int per = (E + 31) / 32;
+        const int lo = min(E, lane * per), hi = min(E, lo + per);
+        int sum = 0;
+        for (int e = lo; e < hi; ++e) sum += ecnt[e];
+        int incl = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        int run = incl - sum;
+        for (int e = lo; e < hi; ++e) {
+            eoff[e] = run;
+            run += ecnt[e];
+        }
+        if (lane == 31) eoff[E] = incl;
+        __syncwarp();
+        for (int base = 0; base < P; base += 32) {
+            const int q = base + lane;
+            const int e = (q < P) ? ids16[q] : -2;
+            const uint32_t peers = __match_any_sync(0xffffffffu, e);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            int dst = 0;
+            if (e >= 0) dst = eoff[e] + rank;
+            __syncwarp();
+            if (e >= 0) {
+                tb.perm[dst] = static_cast<uint16_t>(q);
+                tb.pos[q] = static_cast<uint16_t>(dst);
+                if (rank == 0) eoff[e] += __popc(peers);
+            } else if (q < P) {
+                tb.pos[q] = 0xFFFFu;
+            }
+            __syncwarp();
+        }
+        for (int e = lo; e < hi; ++e) eoff[e] -= ecnt[e];
+        __syncwarp();
+        if (lane == 0) hd->n_valid = eoff[E];
+    }
+    grp_sync();
+}
+
+// Group the T*k pairs (every CTA, redundantly) into groups of at most G pairs
+// on warps 8-11, while warps 0-7 quantise x; tokens without a valid slot get
+// y = 0.  The counting sort's scratch aliases the stage ring, which is not in
+// use yet.  Publishes hd->grouped when the tables are complete.
+__device__ void tc_group(const KernelParams &p, uint8_t *smem, Tabs tb, int G)
+{
+    SmemHdr *hd = tb.hdr;
+    const int lt = threadIdx.x - 256, P = p.T * p.k;
+    if (P <= 32) {
+        if (lt < 32) group_pairs_warp(p, P, G, tb);
+        grp_sync();
+    } else {
+        int16_t *ids16 = reinterpret_cast<int16_t *>(smem);
+        int32_t *ecnt = reinterpret_cast<int32_t *>(smem + align16(2 * P));
+        int32_t *eoff = ecnt + p.E;
+        tc_group_pairs(p, P, ids16, ecnt, eoff, tb);
+        if (lt < 32) {
+            const int lane = lt;
+            const int per = (p.E + 31) / 32;
+            const int lo = min(p.E, lane * per), hi = min(p.E, lo + per);
+            int sum = 0;
+            for (int e2 = lo; e2 < hi; ++e2) sum += (ecnt[e2] + G - 1) / G;
+            int incl = sum;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += v;
+            }
+            int gi = incl - sum;
+            for (int e2 = lo; e2 < hi; ++e2) {
+                const int cnt = ecnt[e2];
+                for (int b = 0; b < cnt; b += G) {
+                    tb.gexp[gi] = static_cast<uint16_t>(e2);
+                    tb.gbeg[gi] = static_cast<uint16_t>(eoff[e2] + b);
+                    tb.gcnt[gi] = static_cast<uint8_t>(min(G, cnt - b));
+                    ++gi;
+                }
+            }
+            if (lane == 31) hd->n_groups = incl;
+        }
+        const int nv0 = hd->n_valid;
+        for (int r = lt; r < nv0; r += 128) tb.stok[r] = static_cast<uint16_t>(tb.perm[r] / p.k);
+        grp_sync();
+    }
+    for (int t = lt; t < p.T; t += 128) {
+        int v = 0;
+        for (int j = 0; j < p.k; ++j) v += (tb.pos[t * p.k + j] != 0xFFFFu);
+        tb.kvalid[t] = static_cast<uint8_t>(v);
+    }
+    grp_sync();
+    if (blockIdx.x == 0 && lt == 0 && hd->n_bad) atomicOr(p.ctrl + 2, kErrBadId);
+    for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
+        if (tb.kvalid[t] == 0)
+            for (int r = lt; r < p.H; r += 128) p.y[static_cast<size_t>(t) * p.H + r] = 0.f;
+    }
+    grp_sync();
+    if (lt == 0) st_rel_cta(&hd->grouped, 1);
+}
+
+// x -> four FP4 digit rows (xq, xsf) and their multipliers (xmul), either one
+// set per token (p.xtok: the gate/up MMAs take every token's rows, N = 4T
+// rounded up) or one per sorted pair (one group's rows in one box).  Work
+// items are (token, 512-element chunk), claimed one at a time by warps 0-7 of
+// whichever CTAs get there (global counter, control word 4): a warp reads the
+// token's whole row for its prescale (largest magnitude), then lane l
+// quantises block 32c + l of the chunk.  Per-token rows need nothing from the
+// grouping, so this runs while warps 8-11 group; per-pair rows wait for it.
+// Items done are published with a gpu-scope release (control word 3); x is
+// complete when all T * ceil(H/512) items are.
+__device__ void tc_quantize_x(const KernelParams &p, const Tabs &tb, volatile int *abort_flag)
+{
+    SmemHdr *hd = tb.hdr;
+    const int lane = threadIdx.x & 31;
+    const int nchunk = (p.H + 511) / 512, nitems = p.T * nchunk, nblk = p.H / 16;
+    int mine = 0;
+    bool grouped = p.xtok != 0;
+    for (;;) {
+        int it = 0;
+        if (lane == 0) it = static_cast<int>(atomicAdd(p.ctrl + 4, 1u));
+        it = __shfl_sync(0xffffffffu, it, 0);
+        if (it >= nitems) break;
+        ++mine;
+        const int t = it / nchunk, c = it - t * nchunk;
+        const uint16_t *src = p.x + static_cast<size_t>(t) * p.H;
+        float amax = 0.f;
+        for (int e8 = 8 * lane; e8 < p.H; e8 += 256) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(src + e8);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xffff0000u))));
+        }
+#pragma unroll
+        for (int d = 16; d; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+        const int e = prescale_exp(amax);
+        const float P = mul_pow2(1.f, e);
+        const int b = 32 * c + lane;  // this lane's 16-element block
+        uint2 pk[4] = {};
+        uint32_t sc[4] = {};
+        if (b < nblk) {
+            const uint4 u0 = *reinterpret_cast<const uint4 *>(src + 16 * b);
+            const uint4 u1 = *reinterpret_cast<const uint4 *>(src + 16 * b + 8);
+            const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                v[2 * i] = __uint_as_float(w[i] << 16) * P;
+                v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u) * P;
+            }
+            quant_block4(v, pk, sc);
+        }
+        auto put = [&](int r) {
+            if (b < nblk) {
+#pragma unroll
+                for (int d = 0; d < 4; ++d) {
+                    const size_t row = static_cast<size_t>(r) * 4 + d;
+                    *reinterpret_cast<uint2 *>(p.xq + row * (p.H / 2) + 8 * b) = pk[d];
+                    p.xsf[row * (p.H / 16) + b] = static_cast<uint8_t>(sc[d]);
+                }
+            }
+            if (c == 0 && lane < 4) p.xmul[static_cast<size_t>(r) * 4 + lane] = mul_pow2(1.f, -e - 2 * lane);
+        };
+        if (p.xtok) {
+            put(t);
+        } else {
+            if (!grouped) {
+                if (!warp_spin(p, [&] { return ld_acq_cta(&hd->grouped) != 0; }, abort_flag)) break;
+                grouped = true;
+            }
+            for (int j = 0; j < p.k; ++j) {
+                const int r = tb.pos[t * p.k + j];
+                if (r != 0xFFFF) put(r);
+            }
+        }
+    }
+    if (mine) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.ctrl + 3, static_cast<uint32_t>(mine));
+    }
+}
+
+// ------------------------------------------------------------------ scale warps
+// E4M3 scales of four blocks (one word) times 2^-d.  Fast path: every byte
+// keeps a normal exponent, so the shift is a subtraction from each exponent.
+__device__ __forceinline__ uint32_t rebase4(uint32_t w, int d)
+{
+    if (d <= 0) return w;
+    if (d < 15) {
+        const uint32_t dd = 0x01010101u * static_cast<uint32_t>(d);
+        const uint32_t nz = __vcmpne4(w, 0u);  // zero scales stay zero
+        if ((__vcmpgtu4((w >> 3) & 0x0F0F0F0Fu, dd) | ~nz) == 0xFFFFFFFFu) return w - ((dd << 3) & nz);
+    }
+    uint32_t o = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o |= e4m3_shift_down((w >> (8 * i)) & 0xFFu, d) << (8 * i);
+    return o;
+}
+
+// Smallest of a pair's nsl slice exponents (signed bytes, 32-byte row).
+__device__ __forceinline__ int row_eref(const int8_t *hx, int nsl)
+{
+    const uint4 v0 = *reinterpret_cast<const uint4 *>(hx), v1 = *reinterpret_cast<const uint4 *>(hx + 16);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    int e = 127;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (i < nsl) e = min(e, static_cast<int>(static_cast<int8_t>(w[i >> 2] >> (8 * (i & 3)))));
+    return e;
+}
+// The block scales of one h digit row over a down stage's 512 elements (slices
+// e4[0..3] of 128, two per K range) rebased to the pair's reference exponent.
+__device__ __forceinline__ void rebase_row(uint4 &x0, uint4 &x1, const int8_t *e4p, int eref)
+{
+    const uint32_t e4 = *reinterpret_cast<const uint32_t *>(e4p);
+    const int d0 = static_cast<int8_t>(e4) - eref, d1 = static_cast<int8_t>(e4 >> 8) - eref;
+    const int d2 = static_cast<int8_t>(e4 >> 16) - eref, d3 = static_cast<int8_t>(e4 >> 24) - eref;
+    if ((d0 | d1 | d2 | d3) == 0) return;
+    x0 = make_uint4(rebase4(x0.x, d0), rebase4(x0.y, d0), rebase4(x0.z, d1), rebase4(x0.w, d1));
+    x1 = make_uint4(rebase4(x1.x, d2), rebase4(x1.y, d2), rebase4(x1.z, d3), rebase4(x1.w, d3));
+}
+
+// Per stage: the weight tiles' block scales (row r of the 128) and the
+// activation digit rows' block scales (row n < N) go to tensor memory in the
+// layout the block-scaled MMA reads.  Its scale address names column set + 4kk
+// (K step kk); the datapath of lane quarter q reads the scales of weight row r
+// (r in quarter q) at lane r, column set + 4kk + q, and those of activation
+// row n at lane 32q + n%32, column set + 4kk + n/32.  So warp q writes, in its
+// own lanes, weight row 32q + lane repeated over the four columns of each K
+// step, and activation rows lane and 32 + lane in columns +0 and +1.  For a
+// down stage the h digit scales are first rebased from their 128-row slice's
+// prescale to the pair's reference (its largest slice).  One arrival per warp
+// on the stage's sfready barrier.
+template <int N>
+__device__ void tc_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb, volatile int *abort_flag)
+{
+    SmemHdr *hd = tb.hdr;
+    const int q = threadIdx.x >> 5, lane = threadIdx.x & 31, r = 32 * q + lane;
+    const uint32_t lanebase = hd->tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+    constexpr int nhi = N > 32 ? 32 : 0;  // second activation row of this lane (N = 64)
+    const int nsl = p.I / kTcRows;
+    int s = 0, eref_lo = 0, eref_hi = 0;
+    uint32_t ph = 0;
+    for (;;) {
+        if (!warp_wait_bar(p, &hd->full[s], ph, abort_flag)) break;
+        const int4 h = hd->stage_hdr[s];
+        const uint8_t *st = smem + s * p.stage_bytes;
+        if (h.x != KIND_END) {
+            const uint32_t col = lanebase + 4 * N + 64 * s;
+            tc_st_set(col + 0, *reinterpret_cast<const uint4 *>(st + kOffS0 + 16 * r));
+            tc_st_set(col + 16, *reinterpret_cast<const uint4 *>(st + kOffS1 + 16 * r));
+            // activation rows lane and lane + nhi (K ranges 0 and, for down, 1)
+            uint4 a0 = *reinterpret_cast<const uint4 *>(st + offSB0(N) + 16 * lane);
+            uint4 c0 = *reinterpret_cast<const uint4 *>(st + offSB0(N) + 16 * (lane + nhi));
+            if (h.x == KIND_B) {
+                uint4 a1 = *reinterpret_cast<const uint4 *>(st + offSB1(N) + 16 * lane);
+                uint4 c1 = *reinterpret_cast<const uint4 *>(st + offSB1(N) + 16 * (lane + nhi));
+                const int gcnt = tb.gcnt[h.y], part = h.w & 0xFFFF;
+                const int8_t *hxb = reinterpret_cast<const int8_t *>(st + offHX(N));
+                const int pl_lo = lane >> 2, pl_hi = (lane + nhi) >> 2;
+                if (part == 0) {
+                    // a new down ticket: each row's reference (its pair's smallest slice exponent)
+                    eref_lo = pl_lo < gcnt ? row_eref(hxb + 32 * pl_lo, nsl) : 0;
+                    eref_hi = pl_hi < gcnt ? row_eref(hxb + 32 * pl_hi, nsl) : 0;
+                }
+                if (pl_lo < gcnt) rebase_row(a0, a1, hxb + 32 * pl_lo + 4 * part, eref_lo);
+                if (nhi && pl_hi < gcnt) rebase_row(c0, c1, hxb + 32 * pl_hi + 4 * part, eref_hi);
+                tc_st_bset(col + 48, a1, c1);
+            }
+            tc_st_bset(col + 32, a0, c0);
+            tc_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hd->sfready[s]);
+        if (h.x == KIND_END) break;
+        if (++s == p.NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ MMA thread
+// One thread issues every MMA of the CTA.  A gate/up stage: four K steps of
+// 64 into the gate and the up accumulators (same B operand); a down stage:
+// eight K steps (two tiles) into one accumulator.  The stage is released by a
+// commit on its empty barrier; a ticket's accumulator buffer is handed to the
+// epilogue by a commit on accfull, after its ticket is published in tinfo.
+template <int N>
+__device__ void tc_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb, volatile int *abort_flag)
+{
+    SmemHdr *hd = tb.hdr;
+    const uint32_t tbase = hd->tmem_base;
+    const uint32_t idesc = fp4_idesc(N);
+    const int nPA = (p.H / p.KS) / 256, nPB = (p.I + 511) / 512;
+    int s = 0, buf = 0;
+    uint32_t ph = 0;
+    int uses[2] = {0, 0};
+    bool ok = true;
+    for (;;) {
+        if (!wait_bar(&hd->sfready[s], ph, p, abort_flag)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        const int4 h = hd->stage_hdr[s];
+        if (h.x == KIND_END) break;
+        const bool isA = h.x != KIND_B;
+        const int part = h.w & 0xFFFF;
+        const int nparts = isA ? nPA : nPB;
+        if (part == 0 && uses[buf] > 0) {
+            if (!wait_bar(&hd->accempty[buf], static_cast<uint32_t>((uses[buf] - 1) & 1), p, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+        }
+        const uint32_t sa = smem_u32(smem + s * p.stage_bytes);
+        const uint32_t sfc = tbase + 4 * N + 64 * s;
+        const uint32_t dcol = tbase + static_cast<uint32_t>(buf * 2 * N);
+        if (isA) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t acc = (part > 0 || kk > 0) ? 1u : 0u;
+                const uint64_t bd = sw128_desc(sa + kOffB0 + 32 * kk);
+                tc_mma(dcol, sw128_desc(sa + kOffW0 + 32 * kk), bd, idesc, sfc + 4 * kk, sfc + 32 + 4 * kk, acc);
+                tc_mma(dcol + N, sw128_desc(sa + kOffW1 + 32 * kk), bd, idesc, sfc + 16 + 4 * kk, sfc + 32 + 4 * kk,
+                       acc);
+            }
+        } else {
+#pragma unroll
+            for (int kr = 0; kr < 2; ++kr)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t acc = (part > 0 || kr > 0 || kk > 0) ? 1u : 0u;
+                    tc_mma(dcol, sw128_desc(sa + (kr ? kOffW1 : kOffW0) + 32 * kk),
+                           sw128_desc(sa + (kr ? offB1(N) : kOffB0) + 32 * kk), idesc, sfc + 16 * kr + 4 * kk,
+                           sfc + 32 + 16 * kr + 4 * kk, acc);
+                }
+        }
+        tc_commit(&hd->empty[s]);
+        if (part == nparts - 1) {
+            hd->tinfo[buf] = h;
+            st_rel_cta(&hd->tseq[buf], uses[buf] + 1);
+            tc_commit(&hd->accfull[buf]);
+            ++uses[buf];
+            buf ^= 1;
+        }
+        if (++s == p.NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+    // end of work for the epilogue (it also leaves on the abort flag), in the
+    // next buffer once the epilogue has read that buffer's previous ticket
+    if (ok && uses[buf] > 0)
+        ok = wait_bar(&hd->accempty[buf], static_cast<uint32_t>((uses[buf] - 1) & 1), p, abort_flag);
+    if (ok) {
+        hd->tinfo[buf] = make_int4(KIND_END, 0, 0, 0);
+        st_rel_cta(&hd->tseq[buf], uses[buf] + 1);
+        mbar_arrive(&hd->accfull[buf]);
+    }
+    // every MMA issued must complete before the CTA frees tensor memory
+    tc_commit(&hd->mma_done);
+    int no_abort = 0;
+    wait_bar(&hd->mma_done, 0u, p, &no_abort);
+}
+
+// ------------------------------------------------------------------ epilogue warps
+// Warp 4+q owns accumulator lanes 32q .. 32q+31, i.e. rows 32q .. 32q+31 of the
+// ticket's 128.  Gate/up ticket: digit columns -> g, u per pair (times the
+// tensor scales); split-K partials go through the workspace and the last
+// arriver sums the KS splits in split order; then h = SiLU(g) * u, quantised
+// into four digit rows per pair (prescale per 128-row slice, blocks of 16
+// rows = 16 lanes, two rows per byte = lane pairs).  Down ticket: digit
+// columns -> per-pair output rows (fp32) for the combine.
+template <int N>
+__device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb, volatile int *abort_flag)
+{
+    constexpr int GP = N / 4;  // pairs per group at most
+    SmemHdr *hd = tb.hdr;
+    const int q = (threadIdx.x >> 5) - 4, lane = threadIdx.x & 31, r = 32 * q + lane;
+    const uint32_t lanebase = hd->tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+    const int TA = p.I / kTcRows, nsl = p.I / kTcRows;
+    const size_t hrow = static_cast<size_t>(p.Ipad / 2), srow = static_cast<size_t>(p.Ipad / 16);
+    int buf = 0, npush = 0, nsync = 0;
+    int uses[2] = {0, 0};
+    // the four epilogue warps meet on an mbarrier (bounded wait: a warp that
+    // gave up cannot leave the others blocked)
+    auto epi_sync = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hd->epibar);
+        const bool ok = warp_wait_bar(p, &hd->epibar, static_cast<uint32_t>(nsync & 1), abort_flag);
+        ++nsync;
+        return ok;
+    };
+    for (;;) {
+        if (!warp_wait_bar(p, &hd->accfull[buf], static_cast<uint32_t>(uses[buf] & 1), abort_flag)) break;
+        const int want = uses[buf] + 1;
+        if (!warp_spin(p, [&] { return ld_acq_cta(&hd->tseq[buf]) == want; }, abort_flag)) break;
+        const int4 ti = hd->tinfo[buf];
+        if (ti.x == KIND_END) break;
+        tc_fence_after();
+        const bool isA = ti.x != KIND_B;
+        const int grp = ti.y, tile = ti.z, ks = ti.w >> 16;
+        const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp], e = tb.gexp[grp];
+        const uint32_t dcol = lanebase + static_cast<uint32_t>(buf * 2 * N);
+        float g[GP], u[GP];
+#pragma unroll
+        for (int i = 0; i < GP; ++i) g[i] = u[i] = 0.f;
+        if (isA && p.xtok) {
+            // every token's four digit columns: pair i reads token stok[gbeg+i]'s
+            // four columns (gate and up), four pairs at a time
+#pragma unroll
+            for (int c = 0; c < GP; c += 4) {
+                if (c >= gcnt) break;
+                float4 dg[4], du[4], xm[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (c + i < gcnt) {
+                        const int tok = tb.stok[gbeg + c + i];
+                        xm[i] = __ldcg(reinterpret_cast<const float4 *>(p.xmul) + tok);
+                        tc_ld4(dcol + 4 * tok, dg[i]);
+                        tc_ld4(dcol + N + 4 * tok, du[i]);
+                    }
+                }
+                tc_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (c + i < gcnt) {
+                        g[c + i] = dg[i].x * xm[i].x + dg[i].y * xm[i].y + dg[i].z * xm[i].z + dg[i].w * xm[i].w;
+                        u[c + i] = du[i].x * xm[i].x + du[i].y * xm[i].y + du[i].z * xm[i].z + du[i].w * xm[i].w;
+                    }
+                }
+            }
+        } else if (isA) {
+            float4 xm[GP];
+#pragma unroll
+            for (int i = 0; i < GP; ++i)
+                xm[i] = i < gcnt ? __ldcg(reinterpret_cast<const float4 *>(p.xmul) + gbeg + i) : make_float4(0, 0, 0, 0);
+#pragma unroll
+            for (int c = 0; c < GP; c += 4) {
+                if (c < gcnt) {
+                    float dg[16], du[16];
+                    tc_ld16(dcol + 4 * c, dg);
+                    tc_ld16(dcol + N + 4 * c, du);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 m = xm[c + i];
+                        g[c + i] = dg[4 * i] * m.x + dg[4 * i + 1] * m.y + dg[4 * i + 2] * m.z + dg[4 * i + 3] * m.w;
+                        u[c + i] = du[4 * i] * m.x + du[4 * i + 1] * m.y + du[4 * i + 2] * m.z + du[4 * i + 3] * m.w;
+                    }
+                }
+            }
+        } else {
+            int eref[GP];  // each pair's h reference exponent: its largest slice's (the smallest exponent)
+#pragma unroll
+            for (int i = 0; i < GP; ++i) {
+                int v = 127;
+                if (i < gcnt && lane < nsl) v = __ldcg(p.hexp + static_cast<size_t>(gbeg + i) * 32 + lane);
+#pragma unroll
+                for (int d = 16; d; d >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, d));
+                eref[i] = v;
+            }
+#pragma unroll
+            for (int c = 0; c < GP; c += 4) {
+                if (c < gcnt) {
+                    float dd[16];
+                    tc_ld16(dcol + 4 * c, dd);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float m0 = mul_pow2(1.f, -eref[c + i]);
+                        g[c + i] = (dd[4 * i] + dd[4 * i + 1] * 0.25f + dd[4 * i + 2] * 0.0625f +
+                                    dd[4 * i + 3] * 0.015625f) * m0;
+                    }
+                }
+            }
+        }
+        // the accumulator buffer is free again
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hd->accempty[buf]);
+        ++uses[buf];
+        buf ^= 1;
+
+        if (!isA) {
+            const float ts = __ldg(p.dts + e);
+            const int h0 = tile * kTcRows;
+#pragma unroll
+            for (int i = 0; i < GP; ++i)
+                if (i < gcnt) p.part[static_cast<size_t>(gbeg + i) * p.H + h0 + r] = g[i] * ts;
+        } else {
+            const float tg = __ldg(p.gts + e), tu = __ldg(p.uts + e);
+#pragma unroll
+            for (int i = 0; i < GP; ++i) {
+                g[i] *= tg;
+                u[i] *= tu;
+            }
+            bool last = true;
+            if (p.KS > 1) {
+                const int unit = grp * TA + tile;
+                float *pb = p.apart + static_cast<size_t>(unit) * p.KS * (2 * GP * kTcRows);
+#pragma unroll
+                for (int i = 0; i < GP; ++i)
+                    if (i < gcnt) {
+                        pb[static_cast<size_t>(ks) * (2 * GP * kTcRows) + (2 * i) * kTcRows + r] = g[i];
+                        pb[static_cast<size_t>(ks) * (2 * GP * kTcRows) + (2 * i + 1) * kTcRows + r] = u[i];
+                    }
+                __threadfence();
+                if (!epi_sync()) break;
+                if (q == 0 && lane == 0) {
+                    const uint32_t old = atomicAdd(p.acnt + unit, 1u);
+                    const int l = old + 1u == static_cast<uint32_t>(p.KS);
+                    if (l) p.acnt[unit] = 0u;  // reset for the next launch
+                    hd->ep_last = l;
+                }
+                if (!epi_sync()) break;
+                last = hd->ep_last != 0;
+                if (last) {
+                    __threadfence();
+#pragma unroll
+                    for (int i = 0; i < GP; ++i)
+                        if (i < gcnt) {
+                            // all partial loads in flight, then the sum in split order
+                            float pg[8], pu[8];
+#pragma unroll
+                            for (int k2 = 0; k2 < 8; ++k2) {
+                                const float *pk = pb + static_cast<size_t>(k2) * (2 * GP * kTcRows);
+                                const bool other = k2 < p.KS && k2 != ks;
+                                pg[k2] = other ? __ldcg(pk + (2 * i) * kTcRows + r) : g[i];
+                                pu[k2] = other ? __ldcg(pk + (2 * i + 1) * kTcRows + r) : u[i];
+                            }
+                            float sg = 0.f, su = 0.f;
+#pragma unroll
+                            for (int k2 = 0; k2 < 8; ++k2)
+                                if (k2 < p.KS) {
+                                    sg += pg[k2];
+                                    su += pu[k2];
+                                }
+                            g[i] = sg;
+                            u[i] = su;
+                        }
+                }
+            }
+            if (last) {
+                // h = SiLU(g) * u, then four digit rows per pair
+                // h rows -> shared memory [pair][128], then thread t quantises pair
+                // t/8's 16-element block t%8 into four digits (no shuffles)
+                float *hs = reinterpret_cast<float *>(smem + p.red_off);
+#pragma unroll
+                for (int i = 0; i < GP; ++i) {
+                    if (i < gcnt) {
+                        const float hv = g[i] / (1.0f + __expf(-g[i])) * u[i];
+                        if (!(fabsf(hv) < 3.0e38f)) atomicOr(p.ctrl + 2, kErrRange);
+                        hs[i * kTcRows + r] = hv;
+                    }
+                }
+                if (!epi_sync()) break;
+                {
+                    const int t = threadIdx.x - 128, pi = t >> 3, blk = t & 7;
+                    float v[16];
+                    float a = 0.f;
+#pragma unroll
+                    for (int i4 = 0; i4 < 4; ++i4) {
+                        const float4 x4 = pi < gcnt ? *reinterpret_cast<const float4 *>(hs + pi * kTcRows + 16 * blk + 4 * i4)
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                        v[4 * i4] = x4.x;
+                        v[4 * i4 + 1] = x4.y;
+                        v[4 * i4 + 2] = x4.z;
+                        v[4 * i4 + 3] = x4.w;
+                        a = fmaxf(a, fmaxf(fmaxf(fabsf(x4.x), fabsf(x4.y)), fmaxf(fabsf(x4.z), fabsf(x4.w))));
+                    }
+                    // the 128-row slice's largest magnitude: the pair's eight threads
+#pragma unroll
+                    for (int d = 1; d < 8; d <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
+                    // each 128-row slice of h gets its own prescale; the scale warps of a
+                    // down stage rebase the slices' block scales to the pair's largest
+                    const int es = prescale_exp(a);
+                    if (pi < gcnt) {
+                        const float P = mul_pow2(1.f, es);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= P;
+                        uint2 pk[4];
+                        uint32_t sc[4];
+                        quant_block4(v, pk, sc);
+                        const int k0 = tile * kTcRows + 16 * blk;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const size_t row = static_cast<size_t>(gbeg + pi) * 4 + j;
+                            *reinterpret_cast<uint2 *>(p.hq + row * hrow + k0 / 2) = pk[j];
+                            p.hsf[row * srow + k0 / 16] = static_cast<uint8_t>(sc[j]);
+                        }
+                        if (blk == 0) p.hexp[static_cast<size_t>(gbeg + pi) * 32 + tile] = static_cast<int8_t>(es);
+                    }
+                }
+            }
+            if (!last) continue;
+            // this unit's h is written: count it for the group (complete at TA)
+            __threadfence();
+            if (!epi_sync()) break;
+            if (q == 0 && lane == 0) atomicAdd(p.doneA + grp, 1u);
+            continue;
+        }
+        // all four warps' stores precede the hand-over to the release warp
+        if (!epi_sync()) break;
+        if (q == 0) {
+            if (!push_done(p, hd, npush, isA ? KIND_A : KIND_B, grp, tile, lane, abort_flag)) break;
+        }
+        ++npush;
+    }
+    __syncwarp();
+    if (lane == 0) atom_add_acqrel_cta(&hd->cons_exited, 1);
+}
+
+// ------------------------------------------------------------------ tickets
+// Gate/up tickets (group, 128-row tile, K split; the split fastest), then down
+// tickets (group, 128-row tile); group-major both.
+struct TcTicket {
+    int isA, grp, tile, ks;
+};
+__device__ __forceinline__ TcTicket tc_decode_ticket(int t, int ng, int TA, int KS, int nHt)
+{
+    TcTicket r;
+    const int nA = ng * TA * KS;
+    if (t < nA) {
+        r.isA = 1;
+        r.grp = t / (TA * KS);
+        const int rem = t - r.grp * TA * KS;
+        r.tile = rem / KS;
+        r.ks = rem - r.tile * KS;
+    } else {
+        const int t2 = t - nA;
+        r.isA = 0;
+        r.grp = t2 / nHt;
+        r.tile = t2 - r.grp * nHt;
+        r.ks = 0;
+    }
+    return r;
+}
+
+// ------------------------------------------------------------------ producer warp
+// Lane 0 issues each stage's copies: gate/up stage = the gate and up tiles (128
+// rows x 256 elements, E2M1 and E4M3) and the group's x digit rows for those
+// 256 elements; down stage = two 256-element tiles of 128 down rows and their
+// scales, the h digit rows (two tiles), their scales and the group's h slice
+// exponents coming from the helper once the group's h exists.  x digit rows
+// of stages issued before the x digits are published also come from the helper.
+template <int N>
+__device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, volatile int *abort_flag)
+{
+    if ((threadIdx.x & 31) != 0) return;
+    SmemHdr *hd = tb.hdr;
+    const uint64_t pol = policy_evict_first();
+    const int ng = hd->n_groups, TA = p.I / kTcRows, nHt = p.H / kTcRows, KS = p.KS;
+    const int nPA = (p.H / KS) / 256, nPB = (p.I + 511) / 512;
+    const int total = ng * (TA * KS + nHt);
+    bool ok = true, x_ok = false;
+    int s = 0, fill = 0, pq_tail = 0, tq_head = 0;
+    uint32_t ph = 0;
+    int ticket = blockIdx.x;
+    // gate/up stages issued before x is complete: their x copies wait here
+    int pend_s[kTcMaxStages], pend_kc[kTcMaxStages], npend = 0;
+    const uint32_t x_items = static_cast<uint32_t>(p.T * ((p.H + 511) / 512));
+    auto flush_x = [&]() {
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        x_ok = true;
+        for (int i = 0; i < npend; ++i) {
+            uint8_t *st = smem + pend_s[i] * p.stage_bytes;
+            uint64_t *bar = &hd->full[pend_s[i]];
+            const int gb = tb.gbeg[hd->stage_hdr[pend_s[i]].y];
+            tma2d(st + kOffB0, &p.tmt[6], pend_kc[i] * 128, p.xtok ? 0 : gb * 4, bar, pol);
+            tma2d(st + offSB0(N), &p.tmt[7], pend_kc[i] * 16, p.xtok ? 0 : gb * 4, bar, pol);
+        }
+        npend = 0;
+    };
+    auto poll_x = [&]() {
+        if (!x_ok && npend > 0 && ld_acquire(p.ctrl + 3) >= x_items) flush_x();
+    };
+    auto wait_for = [&](auto &&cond) -> bool {
+        if (cond()) return true;
+        const uint64_t t0 = gtimer();
+        for (uint32_t it = 0;; ++it) {
+            if (cond()) return true;
+            if ((it & 15u) == 15u) poll_x();
+            if ((it & 15u) == 15u) {
+                if (*abort_flag) return false;
+                if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
+                    raise_error(p, abort_flag, kErrTimeout);
+                    return false;
+                }
+            }
+        }
+    };
+    auto queue_copy = [&](int st_idx, int grp, int part, int kind) {
+        const int slot = pq_tail % kMaxStages;
+        hd->pq_stage[slot] = st_idx;
+        hd->pq_grp[slot] = grp;
+        hd->pq_part[slot] = part;
+        hd->pq_kind[slot] = kind;
+        st_rel_cta(&hd->pq_tail, ++pq_tail);
+    };
+    while (ok && ticket < total) {
+        const TcTicket ti = tc_decode_ticket(ticket, ng, TA, KS, nHt);
+        const int e = tb.gexp[ti.grp], gbeg = tb.gbeg[ti.grp], gcnt = tb.gcnt[ti.grp];
+        const int nparts = ti.isA ? nPA : nPB;
+        for (int part = 0; part < nparts; ++part) {
+            if (!wait_for([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
+                ok = false;
+                break;
+            }
+            uint8_t *st = smem + s * p.stage_bytes;
+            uint64_t *bar = &hd->full[s];
+            if (ti.isA) {
+                if (!x_ok && ld_acq_cta(&hd->xready)) flush_x();
+                const int kc = ti.ks * nPA + part;  // 256-element chunk of H
+                const int row = e * p.I + ti.tile * kTcRows;
+                hd->stage_hdr[s] = make_int4(KIND_A, ti.grp, ti.tile, part | (ti.ks << 16));
+                mbar_expect_tx(bar, static_cast<uint32_t>(2 * kTile + 2 * kSfTile + N * 128 + N * 16));
+                tma2d(st + kOffW0, &p.tmt[0], kc * 128, row, bar, pol);
+                tma2d(st + kOffW1, &p.tmt[1], kc * 128, row, bar, pol);
+                tma2d(st + kOffS0, &p.tmt[3], kc * 16, row, bar, pol);
+                tma2d(st + kOffS1, &p.tmt[4], kc * 16, row, bar, pol);
+                if (x_ok) {
+                    tma2d(st + kOffB0, &p.tmt[6], kc * 128, p.xtok ? 0 : gbeg * 4, bar, pol);
+                    tma2d(st + offSB0(N), &p.tmt[7], kc * 16, p.xtok ? 0 : gbeg * 4, bar, pol);
+                } else {
+                    pend_s[npend] = s;
+                    pend_kc[npend] = kc;
+                    ++npend;
+                }
+            } else {
+                const int kc0 = 2 * part;  // 256-element chunks of I
+                const int row = e * p.H + ti.tile * kTcRows;
+                hd->stage_hdr[s] = make_int4(KIND_B, ti.grp, ti.tile, part);
+                mbar_expect_tx(bar, static_cast<uint32_t>(2 * kTile + 2 * kSfTile + 2 * N * 128 + 2 * N * 16 + gcnt * 32));
+                tma2d(st + kOffW0, &p.tmt[2], kc0 * 128, row, bar, pol);
+                tma2d(st + kOffW1, &p.tmt[2], (kc0 + 1) * 128, row, bar, pol);
+                tma2d(st + kOffS0, &p.tmt[5], kc0 * 16, row, bar, pol);
+                tma2d(st + kOffS1, &p.tmt[5], (kc0 + 1) * 16, row, bar, pol);
+                queue_copy(s, ti.grp, part, KIND_B);
+            }
+            ++fill;
+            if (++s == p.NS) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+        if (!ok) break;
+        if (!wait_for([&] { return ld_acq_cta(&hd->tq_tail) > tq_head; })) {
+            ok = false;
+            break;
+        }
+        ticket = hd->tq_buf[tq_head % kTq];
+        st_rel_cta(&hd->tq_head, ++tq_head);
+    }
+    // x copies still pending: wait for x (bounded), then issue them
+    if (ok && npend > 0 && !wait_for([&] { poll_x(); return npend == 0; })) ok = false;
+    if (ok && wait_for([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
+        hd->stage_hdr[s] = make_int4(KIND_END, 0, 0, 0);
+        mbar_arrive(&hd->full[s]);
+        ++fill;
+    } else {
+        *abort_flag = 1;
+    }
+    hd->fill_cnt = fill;
+}
+
+// ------------------------------------------------------------------ helper warp
+// Tickets ahead of the producer, the published-x watch, per-group gate/up
+// completion watch (one group per lane) and the queued activation copies.
+template <int N>
+__device__ void tc_helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, volatile int *abort_flag)
+{
+    const int lane = threadIdx.x & 31;
+    SmemHdr *hd = tb.hdr;
+    const uint64_t pol = policy_evict_first();
+    const int ng = hd->n_groups;
+    const int TA = p.I / kTcRows, nHt = p.H / kTcRows, KS = p.KS;
+    const int total = ng * (TA * KS + nHt);
+    bool fetch_done = false, xr = false;
+    int tq_tail = 0, pq_head = 0;
+    int watch = -1;
+    uint64_t idle_since = 0;
+    auto note_ticket = [&](int tk) {
+        if (tk >= total) return;
+        const TcTicket ti = tc_decode_ticket(tk, ng, TA, KS, nHt);
+        if (ti.isA) return;
+        if (__shfl_sync(0xffffffffu, ld_acq_cta_u8(tb.hready + ti.grp), 0) != 0) return;
+        const uint32_t free_lanes = __ballot_sync(0xffffffffu, watch < 0);
+        const int l = __ffs(free_lanes) - 1;
+        if (lane == l) watch = ti.grp;
+        if (lane == 0) st_rel_cta_u8(tb.hready + ti.grp, 1);
+        __syncwarp();
+    };
+    note_ticket(blockIdx.x);
+    for (;;) {
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        bool progress = false;
+        const int tq_head = __shfl_sync(0xffffffffu, ld_acq_cta(&hd->tq_head), 0);
+        if (!fetch_done && tq_tail - tq_head < kTq && __ballot_sync(0xffffffffu, watch < 0) != 0) {
+            int tk = 0;
+            if (lane == 0) {
+                tk = static_cast<int>(gridDim.x + atomicAdd(p.ctrl, 1u));
+                hd->tq_buf[tq_tail % kTq] = tk;
+                st_rel_cta(&hd->tq_tail, tq_tail + 1);
+            }
+            ++tq_tail;
+            tk = __shfl_sync(0xffffffffu, tk, 0);
+            if (tk >= total) fetch_done = true;
+            else note_ticket(tk);
+            progress = true;
+        }
+        if (!xr) {
+            int done = 0;
+            if (lane == 0) done = ld_acquire(p.ctrl + 3) >= static_cast<uint32_t>(p.T * ((p.H + 511) / 512));
+            if (__shfl_sync(0xffffffffu, done, 0)) {
+                xr = true;
+                if (lane == 0) st_rel_cta(&hd->xready, 1);
+                progress = true;
+            }
+        }
+        if (watch >= 0 && ld_acquire(p.doneA + watch) == static_cast<uint32_t>(TA)) {
+            st_rel_cta_u8(tb.hready + watch, 2);
+            watch = -1;
+            progress = true;
+        }
+        progress = __any_sync(0xffffffffu, progress);
+        for (;;) {
+            const int pq_tail = __shfl_sync(0xffffffffu, ld_acq_cta(&hd->pq_tail), 0);
+            if (pq_head == pq_tail) break;
+            const int slot = pq_head % kMaxStages;
+            const int grp = hd->pq_grp[slot], kind = hd->pq_kind[slot];
+            const bool ready = kind == KIND_A ? xr : ld_acq_cta_u8(tb.hready + grp) == 2;
+            if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) break;
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                const int si = hd->pq_stage[slot], part = hd->pq_part[slot];
+                uint8_t *st = smem + si * p.stage_bytes;
+                uint64_t *bar = &hd->full[si];
+                const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
+                if (kind == KIND_A) {
+                    tma2d(st + kOffB0, &p.tmt[6], part * 128, p.xtok ? 0 : gbeg * 4, bar, pol);
+                    tma2d(st + offSB0(N), &p.tmt[7], part * 16, p.xtok ? 0 : gbeg * 4, bar, pol);
+                } else {
+                    const int kc0 = 2 * part;
+                    tma2d(st + kOffB0, &p.tmt[8], kc0 * 128, gbeg * 4, bar, pol);
+                    tma2d(st + offB1(N), &p.tmt[8], (kc0 + 1) * 128, gbeg * 4, bar, pol);
+                    tma2d(st + offSB0(N), &p.tmt[9], kc0 * 16, gbeg * 4, bar, pol);
+                    tma2d(st + offSB1(N), &p.tmt[9], (kc0 + 1) * 16, gbeg * 4, bar, pol);
+                    bulk_g2s(st + offHX(N), p.hexp + static_cast<size_t>(gbeg) * 32, static_cast<uint32_t>(gcnt) * 32u,
+                             bar, pol);
+                }
+            }
+            ++pq_head;
+            progress = true;
+        }
+        if (__shfl_sync(0xffffffffu, ld_acq_cta(&hd->cons_exited), 0) == 4) break;
+        if (progress) {
+            idle_since = 0;
+        } else {
+            int bad = 0;
+            if (lane == 0) {
+                const uint64_t now = gtimer();
+                if (idle_since == 0) idle_since = now;
+                else if (static_cast<long long>(now - idle_since) > p.timeout_ns) {
+                    raise_error(p, abort_flag, kErrTimeout);
+                    bad = 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, bad, 0)) break;
+            __nanosleep(32);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ release warp
+// As in the register path: a gpu-scope fence, then the group's gate/up unit
+// counter, or the (token, 128-row tile) arrival counters of a down ticket; the
+// last arrival for a (token, tile) sums the token's k per-pair outputs in slot
+// order (bitwise reproducible) and writes y.
+__device__ void tc_release_loop(const KernelParams &p, Tabs tb, volatile int *abort_flag)
+{
+    const int lane = threadIdx.x & 31;
+    SmemHdr *hd = tb.hdr;
+    const int nHt = p.H / kTcRows;
+    int dq_head = 0;
+    uint64_t idle_since = 0;
+    for (;;) {
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        bool progress = false;
+        const int exited = __shfl_sync(0xffffffffu, ld_acq_cta(&hd->cons_exited), 0);
+        for (;;) {
+            const int slot = dq_head % kDoneQ;
+            if (__shfl_sync(0xffffffffu, ld_acq_cta(&hd->dq_seq[slot]), 0) != dq_head + 1) break;
+            __threadfence();
+            const int kind = hd->dq_kind[slot], grp = hd->dq_grp[slot], tile = hd->dq_tile[slot];
+            if (kind != KIND_B) {
+                if (lane == 0) atomicAdd(p.doneA + grp, 1u);
+            } else {
+                const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
+                int tok = -1;
+                bool last = false;
+                if (lane < gcnt) {
+                    tok = tb.stok[gbeg + lane];
+                    uint32_t *ctr = p.cnt + static_cast<size_t>(tok) * nHt + tile;
+                    const uint32_t old = atomicAdd(ctr, 1u);
+                    last = old + 1u == static_cast<uint32_t>(tb.kvalid[tok]);
+                    if (last) *ctr = 0u;
+                }
+                uint32_t mask = __ballot_sync(0xffffffffu, last);
+                if (mask) {
+                    __threadfence();
+                    const int h0 = tile * kTcRows;
+                    while (mask) {
+                        const int src = __ffs(mask) - 1;
+                        mask &= mask - 1;
+                        const int t2 = __shfl_sync(0xffffffffu, tok, src);
+#pragma unroll
+                        for (int rr = 0; rr < kTcRows / 32; ++rr) {
+                            const int row = rr * 32 + lane;
+                            float pv[kMaxTopK], wv[kMaxTopK];
+#pragma unroll
+                            for (int j = 0; j < kMaxTopK; ++j) {
+                                pv[j] = 0.f;
+                                wv[j] = 0.f;
+                                if (j < p.k) {
+                                    const int ps = tb.pos[t2 * p.k + j];
+                                    if (ps != 0xFFFF) {
+                                        pv[j] = __ldcg(p.part + static_cast<size_t>(ps) * p.H + h0 + row);
+                                        wv[j] = p.w[t2 * p.k + j];
+                                    }
+                                }
+                            }
+                            float yv = 0.f;
+#pragma unroll
+                            for (int j = 0; j < kMaxTopK; ++j)
+                                if (j < p.k && tb.pos[t2 * p.k + j] != 0xFFFF) yv += wv[j] * pv[j];
+                            p.y[static_cast<size_t>(t2) * p.H + h0 + row] = yv;
+                        }
+                    }
+                }
+            }
+            ++dq_head;
+            __syncwarp();
+            if (lane == 0) st_rel_cta(&hd->dq_head, dq_head);
+            progress = true;
+        }
+        if (exited == 4) break;
+        if (progress) {
+            idle_since = 0;
+        } else {
+            int bad = 0;
+            if (lane == 0) {
+                const uint64_t now = gtimer();
+                if (idle_since == 0) idle_since = now;
+                else if (static_cast<long long>(now - idle_since) > p.timeout_ns) {
+                    raise_error(p, abort_flag, kErrTimeout);
+                    bad = 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, bad, 0)) break;
+            __nanosleep(32);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int N>
+__global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const __grid_constant__ KernelParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int P = p.T * p.k;
+    Tabs tb = make_tabs(smem, p.tab_off, P);
+    SmemHdr *hd = tb.hdr;
+    volatile int *abort_flag = &hd->abort_flag;
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    if (tid == 0) {
+        for (int i = 0; i < p.NS; ++i) {
+            mbar_init(&hd->full[i], 1);
+            mbar_init(&hd->empty[i], 1);
+            mbar_init(&hd->sfready[i], 4);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&hd->accfull[b], 1);
+            mbar_init(&hd->accempty[b], 4);
+            hd->tseq[b] = 0;
+        }
+        mbar_init(&hd->mma_done, 1);
+        mbar_init(&hd->epibar, 4);
+        hd->grouped = 0;
+        hd->abort_flag = 0;
+        hd->fill_cnt = 0;
+        hd->cons_exited = 0;
+        hd->xready = 0;
+        hd->tq_head = hd->tq_tail = 0;
+        hd->dq_head = 0;
+        hd->pq_head = hd->pq_tail = 0;
+        hd->claim = 0;
+        for (int i = 0; i < kDoneQ; ++i) hd->dq_seq[i] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    for (int i = tid; i < P; i += blockDim.x) tb.hready[i] = 0;
+    if (warp == 9) tc_alloc(&hd->tmem_base, kTmemCols);
+    if (tid == 256)
+        for (int i = 0; i < 10; ++i)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmt[i])) : "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    if (warp < 8) {
+        // x digits (per token: concurrently with the grouping), then the loops,
+        // which read the grouping tables
+        tc_quantize_x(p, tb, abort_flag);
+        if (warp_spin(p, [&] { return ld_acq_cta(&hd->grouped) != 0; }, abort_flag)) {
+            if (warp < 4) tc_scale_loop<N>(p, smem, tb, abort_flag);
+            else tc_epilogue_loop<N>(p, smem, tb, abort_flag);
+        }
+    } else {
+        tc_group(p, smem, tb, N / 4);
+        if (warp == 8) {
+            tc_producer_loop<N>(p, smem, tb, abort_flag);
+        } else if (warp == 9) {
+            if ((tid & 31) == 0) tc_mma_loop<N>(p, smem, tb, abort_flag);
+        } else if (warp == 10) {
+            tc_helper_loop<N>(p, smem, tb, abort_flag);
+        } else {
+            tc_release_loop(p, tb, abort_flag);
+        }
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tc_dealloc(hd->tmem_base, kTmemCols);
+    }
+    if (tid == 0) {
+        if (*abort_flag) {
+            const uint64_t t0 = gtimer();
+            const int F = hd->fill_cnt;
+            for (int i = 0; i < p.NS; ++i) {
+                const int fi = F / p.NS + (i < F % p.NS ? 1 : 0);
+                if (fi == 0) continue;
+                while (!mbar_test(&hd->full[i], static_cast<uint32_t>((fi - 1) & 1))) {
+                    if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) break;
+                }
+            }
+        }
+        __threadfence();
+        const uint32_t done = atomicAdd(p.ctrl + 1, 1u);
+        if (done == gridDim.x - 1) {
+            __threadfence();
+            const bool err = (ld_relaxed(p.ctrl + 2) & kErrTimeout) != 0;
+            const int ng = hd->n_groups;
+            for (int i = 0; i < ng; ++i) p.doneA[i] = 0u;
+            if (err) {
+                for (int i = 0; i < kMaxPairs; ++i) p.doneA[i] = 0u;
+                for (int i = 0; i < p.T * (p.H / kTcRows); ++i) p.cnt[i] = 0u;
+                for (int i = 0; i < kTcApartUnits; ++i) p.acnt[i] = 0u;
+            }
+            p.ctrl[0] = 0u;
+            p.ctrl[1] = 0u;
+            p.ctrl[3] = 0u;
+            p.ctrl[4] = 0u;
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t set_tc_smem_limit(int bytes)
+{
+    const void *fns[] = {reinterpret_cast<const void *>(moe_tc_kernel<16>),
+                         reinterpret_cast<const void *>(moe_tc_kernel<32>),
+                         reinterpret_cast<const void *>(moe_tc_kernel<64>)};
+    for (const void *f : fns) {
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_tc(const KernelParams &p, int grid, int smem_bytes, bool pdl, cudaStream_t st)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (p.tcN == 16) return cudaLaunchKernelEx(&cfg, moe_tc_kernel<16>, p);
+    if (p.tcN == 32) return cudaLaunchKernelEx(&cfg, moe_tc_kernel<32>, p);
+    return cudaLaunchKernelEx(&cfg, moe_tc_kernel<64>, p);
+}
+
+}  // namespace moe

@@ -23,9 +23,21 @@ def test_library_exports_every_declared_symbol():
     for name in decl:
         assert hasattr(lib, name), name
     lib.moe_abi_version.restype = ctypes.c_int
-    assert lib.moe_abi_version() == 1
+    assert lib.moe_abi_version() == 2
     lib.moe_status_string.restype = ctypes.c_char_p
     assert lib.moe_status_string(6) == b"MOE_ERR_TIMEOUT"
+
+
+def test_plan_desc_and_stats_match_the_header():
+    # the ctypes mirrors of moe_plan_desc / moe_stats_t list the header's fields in order
+    from quantized_moe_routed_gb300 import binding
+    src = open(os.path.join(ROOT, "include", "moe_nvfp4.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    for struct, py in (("moe_plan_desc", binding.moe_plan_desc), ("moe_stats_t", binding.moe_stats_t)):
+        body = re.search(r"typedef struct \{([^{}]*)\}\s*" + struct + ";", src).group(1)
+        names = re.findall(r"\*?\s*(\w+)\s*[,;]", body)
+        assert names == [f for f, _ in py._fields_], (struct, names)
+    assert (binding.MOE_KERNEL_AUTO, binding.MOE_KERNEL_REGISTER, binding.MOE_KERNEL_TENSOR) == (0, 1, 2)
 
 
 def test_binding_loads_and_rejects_without_plan():

@@ -39,8 +39,8 @@ def weights_cpu(W, experts):
     return out
 
 
-def run_case(wl, x, ids, w, W, *, strict=True, T_max=None, pdl=False):
-    plan = MoePlan(W, wl.H, wl.I, wl.E, wl.k, T_max=T_max or max(wl.T, 1), strict=strict, pdl=pdl)
+def run_case(wl, x, ids, w, W, *, strict=True, T_max=None, pdl=False, kernel=binding.MOE_KERNEL_AUTO):
+    plan = MoePlan(W, wl.H, wl.I, wl.E, wl.k, T_max=T_max or max(wl.T, 1), strict=strict, pdl=pdl, kernel=kernel)
     ws = plan.new_workspace()
     y = plan.step(x.to(DEV), ids.to(DEV), w.to(DEV), ws)
     st = plan.check(ws)
@@ -81,6 +81,56 @@ def test_workload_parity(name, sample, cache):
     assert err <= TOL
     s = plan.stats()
     assert s["decode_launches" if wl.T <= 24 else "prefill_launches"] >= 1 and s["rejected_calls"] == 0
+
+
+# ------------------------------------------------------------------ the tensor-core kernel
+@pytest.mark.parametrize("name,sample", [("decode", None), ("spec_verify", None), ("upper_decode", None),
+                                         ("prefill", 24)])
+def test_tensor_kernel_workload_parity(name, sample, cache):
+    wl, x, ids, w, W = workload_inputs(name, cache)
+    plan, ws, y, st = run_case(wl, x, ids, w, W, kernel=binding.MOE_KERNEL_TENSOR)
+    assert st == 0, binding.STATUS_NAMES.get(st)
+    tokens = list(range(wl.T)) if sample is None else sorted(
+        np.random.default_rng(7).choice(wl.T, size=sample, replace=False).tolist())
+    y_ref, _ = oracle.moe_forward(x, ids, w, weights_cpu(W, touched_experts(ids[tokens], wl.E)), tokens=tokens)
+    err = rel_err(y.cpu().numpy()[tokens], y_ref)
+    print(f"{name} (tensor-core kernel): rel err {err:.3e}")
+    assert err <= TOL
+    s = plan.stats()
+    assert s["tensor_launches"] >= 1 and s["rejected_calls"] == 0
+
+
+@pytest.mark.parametrize("name", ["decode", "spec_verify"])
+def test_tensor_kernel_bitwise_reproducible(name, cache):
+    wl, x, ids, w, W = workload_inputs(name, cache)
+    plan = MoePlan(W, wl.H, wl.I, wl.E, wl.k, T_max=wl.T, strict=True, kernel=binding.MOE_KERNEL_TENSOR)
+    ws = plan.new_workspace()
+    xd, idd, wd = x.to(DEV), ids.to(DEV), w.to(DEV)
+    y1 = plan.step(xd, idd, wd, ws).clone()
+    y2 = plan.step(xd, idd, wd, ws).clone()
+    assert plan.check(ws) == 0
+    assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [(1, 512, 256, 6, 3), (5, 512, 512, 6, 3), (12, 768, 768, 9, 4),
+                                       (24, 512, 256, 16, 8)])
+def test_tensor_kernel_small_shapes(T, H, I, E, k):
+    wl = Workload("tc-small", T=T, H=H, I=I, E=E, k=k, routing="uniform", seed=11)
+    ids = make_topk_ids(wl)
+    x, w = make_x(wl), make_topk_w(wl)
+    W = small_weights(wl)
+    plan, ws, y, st = run_case(wl, x, ids, w, W, strict=False, kernel=binding.MOE_KERNEL_TENSOR)
+    assert st == 0, binding.STATUS_NAMES.get(st)
+    y_ref, _ = oracle.moe_forward(x, ids, w, {kk: v.cpu() for kk, v in W.items()})
+    assert rel_err(y.cpu().numpy(), y_ref) <= TOL
+
+
+def test_tensor_kernel_refuses_shapes_it_cannot_take():
+    wl = Workload("tc-refuse", T=2, H=256, I=128, E=4, k=2, routing="uniform", seed=12)
+    W = small_weights(wl)
+    with pytest.raises(MoeError) as ei:
+        MoePlan(W, wl.H, wl.I, wl.E, wl.k, T_max=2, kernel=binding.MOE_KERNEL_TENSOR)
+    assert ei.value.status == binding.MOE_ERR_UNSUPPORTED_SHAPE
 
 
 def test_bitwise_reproducible(cache):
