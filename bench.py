@@ -117,7 +117,7 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def setup(wl_name, device):
+def setup(wl_name, device, kernel=None):
     from quantized_moe_routed_gb300 import MoePlan
     from quantized_moe_routed_gb300.inputs import (WORKLOADS, algorithmic_bytes, make_expert_weights,
                                                    make_topk_ids, make_topk_w, make_x, rotate_ids, rotation_delta)
@@ -127,7 +127,10 @@ def setup(wl_name, device):
     delta = rotation_delta(ids, wl.E, window=8)
     # programmatic dependent launch: each step's grid is launched while the
     # previous one drains (its first instruction still waits for it)
-    plan = MoePlan(W, wl.H, wl.I, wl.E, wl.k, T_max=wl.T, strict=True, pdl=True)
+    from quantized_moe_routed_gb300 import binding
+    kern = {"auto": binding.MOE_KERNEL_AUTO, "register": binding.MOE_KERNEL_REGISTER,
+            "tensor": binding.MOE_KERNEL_TENSOR}[kernel or os.environ.get("MOE_BENCH_KERNEL", "auto")]
+    plan = MoePlan(W, wl.H, wl.I, wl.E, wl.k, T_max=wl.T, strict=True, pdl=True, kernel=kern)
     ws = plan.new_workspace()
     nrot = max(8, GRAPH_STEPS)
     ids_rot = [rotate_ids(ids, s, delta, wl.E).to(device) for s in range(nrot)]
@@ -139,7 +142,7 @@ def setup(wl_name, device):
 def capture(S, null=False):
     """One CUDA graph of GRAPH_STEPS consecutive steps over rotated ids."""
     from quantized_moe_routed_gb300 import binding
-    fn = binding.moe_null_step if null else binding.moe_decode
+    fn = binding.moe_null_step if null else (binding.moe_decode if S["wl"].T <= 24 else binding.moe_prefill)
     st = torch.cuda.Stream()
     st.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(st):

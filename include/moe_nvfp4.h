@@ -78,9 +78,9 @@ typedef struct {
                 /*    the environment variable MOE_STRICT=1 forces it on          */
     int pdl;    /* 1: launch with programmatic dependent launch allowed          */
     int kernel; /* which step kernel runs moe_decode / moe_prefill:               */
-                /*   MOE_KERNEL_AUTO: the library's choice (currently the         */
-                /*     register kernel, the faster of the two on the decode       */
-                /*     workloads measured);                                       */
+                /*   MOE_KERNEL_AUTO: per launch, the tensor-core kernel for more */
+                /*     than 8 (token, slot) pairs when the shape allows it (H and */
+                /*     I multiples of 256, I <= 4096), else the register kernel;  */
                 /*   MOE_KERNEL_REGISTER: E2M1 x E4M3 dequantised in registers,   */
                 /*     fp16 mma.sync (any shape the plan accepts);                */
                 /*   MOE_KERNEL_TENSOR: tcgen05 block-scaled FP4 MMA on the        */

@@ -471,7 +471,13 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
         reject(pl);
         return st;
     }
-    if (pl->use_tc && path != Path::Null && !wo)
+    // kernel choice: the tensor-core kernel when asked for, or (automatic) for
+    // more than 8 pairs per launch; a single token's 8 pairs stream too few
+    // bytes per expert for the tensor-core pipeline's fixed latencies, and the
+    // register kernel is faster there (measured: 30.6 vs 52.7 us at T = 1,
+    // 192 vs 154 us at T = 16, 330 vs 226 us at T = 24)
+    if (pl->use_tc && path != Path::Null && !wo &&
+        (pl->d.kernel == MOE_KERNEL_TENSOR || T * pl->d.top_k > 8))
         return run_tc(pl, x, ids, w, y, T, ws, static_cast<cudaStream_t>(stream), path);
     // kernel smem attribute: allow up to the device's opt-in limit (once per plan)
     {
@@ -723,9 +729,9 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
         return fail(MOE_ERR_UNSUPPORTED_SHAPE,
                     "the tensor-core kernel takes H and I multiples of 256 and I <= 4096 (H=%d, I=%d)", d.H, d.I);
     }
-    // automatic choice: the register kernel (measured faster on the decode
-    // workloads so far); the tensor-core kernel on request
-    pl->use_tc = d.kernel == MOE_KERNEL_TENSOR;
+    // the tensor-core kernel is available when the shape allows it and it was
+    // not excluded; which kernel a launch takes is decided per launch (run_step)
+    pl->use_tc = d.kernel != MOE_KERNEL_REGISTER && tc_shape_ok(d);
     if (pl->use_tc) {
         const moe_status_t ts = build_tc_maps(d, pl->tmw);
         if (ts != MOE_OK) {

@@ -91,7 +91,7 @@ struct KernelParams {
     uint8_t *xq, *xsf;  // [Pmax*4][H/2], [Pmax*4][H/16]: each sorted pair's x as 4 FP4 digit rows
     float *xmul;        // [Pmax*4] multiplier of each x digit row
     uint8_t *hq, *hsf;  // [Pmax*4][Ipad/2], [Pmax*4][Ipad/16]: h digit rows
-    int8_t *hexp;       // [Pmax][32]: prescale exponent of each 128-row slice of h
+    int8_t *hexp;       // [Pmax][64]: prescale exponent of each 128-row slice of h; [32] the pair's reference
     float *apart;       // split-K partial gate/up sums
     uint32_t *acnt;     // split-K arrivals per gate/up unit
     int tcN;            // MMA N: digit rows per group (16, 32 or 64; a group has <= tcN/4 pairs)
@@ -118,7 +118,7 @@ constexpr int kTcMaxStages = 8;
 constexpr int kTcApartUnits = 1024;  // split-K (unit, split) slots of the partial buffer
 inline int tc_stage_bytes(int N)
 {
-    const int end = 36864 + 2 * N * 128 + 2 * N * 16 + 16 * 32;
+    const int end = 36864 + 2 * N * 128 + 2 * N * 16;
     return (end + 1023) / 1024 * 1024;
 }
 cudaError_t launch_tc(const KernelParams &p, int grid, int smem_bytes, bool pdl, cudaStream_t st);

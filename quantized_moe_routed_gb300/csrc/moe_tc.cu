@@ -498,18 +498,6 @@ __device__ __forceinline__ int row_eref(const int8_t *hx, int nsl)
         if (i < nsl) e = min(e, static_cast<int>(static_cast<int8_t>(w[i >> 2] >> (8 * (i & 3)))));
     return e;
 }
-// The block scales of one h digit row over a down stage's 512 elements (slices
-// e4[0..3] of 128, two per K range) rebased to the pair's reference exponent.
-__device__ __forceinline__ void rebase_row(uint4 &x0, uint4 &x1, const int8_t *e4p, int eref)
-{
-    const uint32_t e4 = *reinterpret_cast<const uint32_t *>(e4p);
-    const int d0 = static_cast<int8_t>(e4) - eref, d1 = static_cast<int8_t>(e4 >> 8) - eref;
-    const int d2 = static_cast<int8_t>(e4 >> 16) - eref, d3 = static_cast<int8_t>(e4 >> 24) - eref;
-    if ((d0 | d1 | d2 | d3) == 0) return;
-    x0 = make_uint4(rebase4(x0.x, d0), rebase4(x0.y, d0), rebase4(x0.z, d1), rebase4(x0.w, d1));
-    x1 = make_uint4(rebase4(x1.x, d2), rebase4(x1.y, d2), rebase4(x1.z, d3), rebase4(x1.w, d3));
-}
-
 // Per stage: the weight tiles' block scales (row r of the 128) and the
 // activation digit rows' block scales (row n < N) go to tensor memory in the
 // layout the block-scaled MMA reads.  Its scale address names column set + 4kk
@@ -517,10 +505,8 @@ __device__ __forceinline__ void rebase_row(uint4 &x0, uint4 &x1, const int8_t *e
 // (r in quarter q) at lane r, column set + 4kk + q, and those of activation
 // row n at lane 32q + n%32, column set + 4kk + n/32.  So warp q writes, in its
 // own lanes, weight row 32q + lane repeated over the four columns of each K
-// step, and activation rows lane and 32 + lane in columns +0 and +1.  For a
-// down stage the h digit scales are first rebased from their 128-row slice's
-// prescale to the pair's reference (its largest slice).  One arrival per warp
-// on the stage's sfready barrier.
+// step, and activation rows lane and 32 + lane in columns +0 and +1.  One
+// arrival per warp on the stage's sfready barrier.
 template <int N>
 __device__ void tc_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb, volatile int *abort_flag)
 {
@@ -528,8 +514,7 @@ __device__ void tc_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
     const int q = threadIdx.x >> 5, lane = threadIdx.x & 31, r = 32 * q + lane;
     const uint32_t lanebase = hd->tmem_base + (static_cast<uint32_t>(32 * q) << 16);
     constexpr int nhi = N > 32 ? 32 : 0;  // second activation row of this lane (N = 64)
-    const int nsl = p.I / kTcRows;
-    int s = 0, eref_lo = 0, eref_hi = 0;
+    int s = 0;
     uint32_t ph = 0;
     for (;;) {
         if (!warp_wait_bar(p, &hd->full[s], ph, abort_flag)) break;
@@ -540,21 +525,11 @@ __device__ void tc_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
             tc_st_set(col + 0, *reinterpret_cast<const uint4 *>(st + kOffS0 + 16 * r));
             tc_st_set(col + 16, *reinterpret_cast<const uint4 *>(st + kOffS1 + 16 * r));
             // activation rows lane and lane + nhi (K ranges 0 and, for down, 1)
-            uint4 a0 = *reinterpret_cast<const uint4 *>(st + offSB0(N) + 16 * lane);
-            uint4 c0 = *reinterpret_cast<const uint4 *>(st + offSB0(N) + 16 * (lane + nhi));
+            const uint4 a0 = *reinterpret_cast<const uint4 *>(st + offSB0(N) + 16 * lane);
+            const uint4 c0 = *reinterpret_cast<const uint4 *>(st + offSB0(N) + 16 * (lane + nhi));
             if (h.x == KIND_B) {
-                uint4 a1 = *reinterpret_cast<const uint4 *>(st + offSB1(N) + 16 * lane);
-                uint4 c1 = *reinterpret_cast<const uint4 *>(st + offSB1(N) + 16 * (lane + nhi));
-                const int gcnt = tb.gcnt[h.y], part = h.w & 0xFFFF;
-                const int8_t *hxb = reinterpret_cast<const int8_t *>(st + offHX(N));
-                const int pl_lo = lane >> 2, pl_hi = (lane + nhi) >> 2;
-                if (part == 0) {
-                    // a new down ticket: each row's reference (its pair's smallest slice exponent)
-                    eref_lo = pl_lo < gcnt ? row_eref(hxb + 32 * pl_lo, nsl) : 0;
-                    eref_hi = pl_hi < gcnt ? row_eref(hxb + 32 * pl_hi, nsl) : 0;
-                }
-                if (pl_lo < gcnt) rebase_row(a0, a1, hxb + 32 * pl_lo + 4 * part, eref_lo);
-                if (nhi && pl_hi < gcnt) rebase_row(c0, c1, hxb + 32 * pl_hi + 4 * part, eref_hi);
+                const uint4 a1 = *reinterpret_cast<const uint4 *>(st + offSB1(N) + 16 * lane);
+                const uint4 c1 = *reinterpret_cast<const uint4 *>(st + offSB1(N) + 16 * (lane + nhi));
                 tc_st_bset(col + 48, a1, c1);
             }
             tc_st_bset(col + 32, a0, c0);
@@ -745,15 +720,9 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
                 }
             }
         } else {
-            int eref[GP];  // each pair's h reference exponent: its largest slice's (the smallest exponent)
+            int eref[GP];  // each pair's h reference exponent (its largest slice's), set by the group's finisher
 #pragma unroll
-            for (int i = 0; i < GP; ++i) {
-                int v = 127;
-                if (i < gcnt && lane < nsl) v = __ldcg(p.hexp + static_cast<size_t>(gbeg + i) * 32 + lane);
-#pragma unroll
-                for (int d = 16; d; d >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, d));
-                eref[i] = v;
-            }
+            for (int i = 0; i < GP; ++i) eref[i] = i < gcnt ? __ldcg(p.hexp + static_cast<size_t>(gbeg + i) * 64 + 32) : 0;
 #pragma unroll
             for (int c = 0; c < GP; c += 4) {
                 if (c < gcnt) {
@@ -883,15 +852,48 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
                             *reinterpret_cast<uint2 *>(p.hq + row * hrow + k0 / 2) = pk[j];
                             p.hsf[row * srow + k0 / 16] = static_cast<uint8_t>(sc[j]);
                         }
-                        if (blk == 0) p.hexp[static_cast<size_t>(gbeg + pi) * 32 + tile] = static_cast<int8_t>(es);
+                        if (blk == 0) p.hexp[static_cast<size_t>(gbeg + pi) * 64 + tile] = static_cast<int8_t>(es);
                     }
                 }
             }
             if (!last) continue;
-            // this unit's h is written: count it for the group (complete at TA)
+            // this unit's h is written: count it for the group; the CTA that
+            // completes the group (count TA) rebases the group's h block scales from
+            // each slice's prescale to the pair's reference (its largest slice, the
+            // smallest exponent) and publishes the group with one more count
             __threadfence();
             if (!epi_sync()) break;
-            if (q == 0 && lane == 0) atomicAdd(p.doneA + grp, 1u);
+            if (q == 0 && lane == 0)
+                hd->ep_last = atomicAdd(p.doneA + grp, 1u) + 1u == static_cast<uint32_t>(TA);
+            if (!epi_sync()) break;
+            if (hd->ep_last) {
+                __threadfence();
+                int8_t *ex = reinterpret_cast<int8_t *>(smem + p.red_off);  // [pair][33]: slices, reference
+                const int t = threadIdx.x - 128;
+                if (t < gcnt) {
+                    const int8_t *hx = p.hexp + static_cast<size_t>(gbeg + t) * 64;
+                    int e = 127;
+                    for (int i = 0; i < nsl; ++i) {
+                        const int v = __ldcg(hx + i);
+                        ex[t * 33 + i] = static_cast<int8_t>(v);
+                        e = min(e, v);
+                    }
+                    ex[t * 33 + 32] = static_cast<int8_t>(e);
+                    p.hexp[static_cast<size_t>(gbeg + t) * 64 + 32] = static_cast<int8_t>(e);
+                }
+                if (!epi_sync()) break;
+                const int wpr = p.I / 64;  // scale words (four 16-element blocks) per digit row
+                for (int wd = t; wd < gcnt * 4 * wpr; wd += 128) {
+                    const int row = wd / wpr, wi = wd - row * wpr, pl = row >> 2;
+                    const int d = ex[pl * 33 + (wi >> 1)] - ex[pl * 33 + 32];
+                    if (d <= 0) continue;
+                    uint32_t *sw = reinterpret_cast<uint32_t *>(p.hsf + (static_cast<size_t>(gbeg) * 4 + row) * srow) + wi;
+                    *sw = rebase4(__ldcg(sw), d);
+                }
+                __threadfence();
+                if (!epi_sync()) break;
+                if (q == 0 && lane == 0) atomicAdd(p.doneA + grp, 1u);
+            }
             continue;
         }
         // all four warps' stores precede the hand-over to the release warp
@@ -1025,7 +1027,7 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
                 const int kc0 = 2 * part;  // 256-element chunks of I
                 const int row = e * p.H + ti.tile * kTcRows;
                 hd->stage_hdr[s] = make_int4(KIND_B, ti.grp, ti.tile, part);
-                mbar_expect_tx(bar, static_cast<uint32_t>(2 * kTile + 2 * kSfTile + 2 * N * 128 + 2 * N * 16 + gcnt * 32));
+                mbar_expect_tx(bar, static_cast<uint32_t>(2 * kTile + 2 * kSfTile + 2 * N * 128 + 2 * N * 16));
                 tma2d(st + kOffW0, &p.tmt[2], kc0 * 128, row, bar, pol);
                 tma2d(st + kOffW1, &p.tmt[2], (kc0 + 1) * 128, row, bar, pol);
                 tma2d(st + kOffS0, &p.tmt[5], kc0 * 16, row, bar, pol);
@@ -1112,7 +1114,7 @@ __device__ void tc_helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, vo
                 progress = true;
             }
         }
-        if (watch >= 0 && ld_acquire(p.doneA + watch) == static_cast<uint32_t>(TA)) {
+        if (watch >= 0 && ld_acquire(p.doneA + watch) == static_cast<uint32_t>(TA) + 1u) {
             st_rel_cta_u8(tb.hready + watch, 2);
             watch = -1;
             progress = true;
@@ -1140,8 +1142,6 @@ __device__ void tc_helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, vo
                     tma2d(st + offB1(N), &p.tmt[8], (kc0 + 1) * 128, gbeg * 4, bar, pol);
                     tma2d(st + offSB0(N), &p.tmt[9], kc0 * 16, gbeg * 4, bar, pol);
                     tma2d(st + offSB1(N), &p.tmt[9], (kc0 + 1) * 16, gbeg * 4, bar, pol);
-                    bulk_g2s(st + offHX(N), p.hexp + static_cast<size_t>(gbeg) * 32, static_cast<uint32_t>(gcnt) * 32u,
-                             bar, pol);
                 }
             }
             ++pq_head;

@@ -63,11 +63,12 @@ def workload_inputs(name, cache):
 
 
 # ------------------------------------------------------------------ the five workloads at full size
+@pytest.mark.parametrize("kernel", [binding.MOE_KERNEL_AUTO, binding.MOE_KERNEL_REGISTER])
 @pytest.mark.parametrize("name,sample", [("tiny", None), ("decode", None), ("spec_verify", None),
                                          ("upper_decode", None), ("prefill", 24)])
-def test_workload_parity(name, sample, cache):
+def test_workload_parity(name, sample, kernel, cache):
     wl, x, ids, w, W = workload_inputs(name, cache)
-    plan, ws, y, st = run_case(wl, x, ids, w, W)
+    plan, ws, y, st = run_case(wl, x, ids, w, W, kernel=kernel)
     assert st == 0, binding.STATUS_NAMES.get(st)
     if sample is None:
         tokens = list(range(wl.T))
@@ -81,6 +82,8 @@ def test_workload_parity(name, sample, cache):
     assert err <= TOL
     s = plan.stats()
     assert s["decode_launches" if wl.T <= 24 else "prefill_launches"] >= 1 and s["rejected_calls"] == 0
+    if kernel == binding.MOE_KERNEL_REGISTER:
+        assert s["tensor_launches"] == 0
 
 
 # ------------------------------------------------------------------ the tensor-core kernel
