@@ -421,6 +421,16 @@ moe_status_t run_tc(moe_plan *pl, const void *x, const int32_t *ids, const float
         p.red_off = p.tab_off + (tab + 15) / 16 * 16;
         p.tcN = N;
         p.KS = KS;
+        // the last wave of gate/up units in 4-way K splits (each still >= 2
+        // stages), when the units are not split already
+        p.KSt = 1;
+        p.tail_units = 0;
+        p.tq_depth = 1;
+        if (const char *q = std::getenv("MOE_TC_TQ")) p.tq_depth = std::atoi(q) < 1 ? 1 : (std::atoi(q) > 4 ? 4 : std::atoi(q));
+        if (KS == 1 && d.H % (4 * 512) == 0 && std::getenv("MOE_TC_TAIL")) {
+            p.KSt = 4;
+            p.tail_units = pl->num_sms < moe::kTcApartUnits / 4 ? pl->num_sms : moe::kTcApartUnits / 4;
+        }
         const int total = p.red_off + ep_scratch + 1024;
         cudaError_t e = moe::launch_tc(p, pl->num_sms, total, pl->pdl, cs);
         if (e != cudaSuccess) {

@@ -95,7 +95,9 @@ struct KernelParams {
     float *apart;       // split-K partial gate/up sums
     uint32_t *acnt;     // split-K arrivals per gate/up unit
     int tcN;            // MMA N: digit rows per group (16, 32 or 64; a group has <= tcN/4 pairs)
-    int KS;             // K splits of a gate/up unit (1, 2, 4 or 8)
+    int KS;             // K splits of a gate/up unit (1, 2, 4 or 8) ...
+    int KSt, tail_units;  // ... except the last tail_units units: KSt splits
+    int tq_depth;       // tickets the helper fetches ahead of the producer (1 .. 4)
     int Ipad;           // I rounded up to 512
     int xtok;           // 1: x digit rows per token (gate/up MMAs take all tokens, T <= 16); 0: per sorted pair
 };

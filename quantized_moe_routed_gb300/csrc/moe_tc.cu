@@ -66,6 +66,28 @@ __device__ __forceinline__ int offSB0(int N) { return kOffB0 + 2 * N * 128; }
 __device__ __forceinline__ int offSB1(int N) { return kOffB0 + 2 * N * 128 + N * 16; }
 __device__ __forceinline__ int offHX(int N) { return kOffB0 + 2 * N * 128 + 2 * N * 16; }
 
+// Gate/up unit splitting along K (see the ticket order below).
+struct TcSplit {
+    int units, tstart, nhead, ntail;  // tail units start at unit tstart
+};
+__device__ __forceinline__ TcSplit tc_split(const KernelParams &p, int ng)
+{
+    TcSplit sp;
+    sp.units = ng * (p.I / kTcRows);
+    sp.tstart = max(0, sp.units - p.tail_units);
+    sp.nhead = sp.tstart * p.KS;
+    sp.ntail = (sp.units - sp.tstart) * p.KSt;
+    return sp;
+}
+// Slot of a split unit in the partial-sum buffer (and its arrival counter):
+// head units use slots only when they are split (KS > 1, then there is no
+// tail), tail units follow them.  Slots stay below kTcApartUnits (the host's
+// choice of KS, KSt and tail_units).
+__device__ __forceinline__ int tc_unit_slot(const KernelParams &p, const TcSplit &sp, int u)
+{
+    const int head_slots = p.KS > 1 ? sp.tstart * p.KS : 0;
+    return u < sp.tstart ? u * p.KS : head_slots + (u - sp.tstart) * p.KSt;
+}
 // ------------------------------------------------------------------ tcgen05 wrappers
 __device__ __forceinline__ void tc_alloc(uint32_t *dst, uint32_t ncols)
 {
@@ -558,7 +580,7 @@ __device__ void tc_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
     SmemHdr *hd = tb.hdr;
     const uint32_t tbase = hd->tmem_base;
     const uint32_t idesc = fp4_idesc(N);
-    const int nPA = (p.H / p.KS) / 256, nPB = (p.I + 511) / 512;
+    const int nPB = (p.I + 511) / 512;
     int s = 0, buf = 0;
     uint32_t ph = 0;
     int uses[2] = {0, 0};
@@ -573,7 +595,7 @@ __device__ void tc_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
         if (h.x == KIND_END) break;
         const bool isA = h.x != KIND_B;
         const int part = h.w & 0xFFFF;
-        const int nparts = isA ? nPA : nPB;
+        const int nparts = isA ? (p.H >> ((h.w >> 20) & 3)) / 256 : nPB;
         if (part == 0 && uses[buf] > 0) {
             if (!wait_bar(&hd->accempty[buf], static_cast<uint32_t>((uses[buf] - 1) & 1), p, abort_flag)) {
                 ok = false;
@@ -668,7 +690,7 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
         if (ti.x == KIND_END) break;
         tc_fence_after();
         const bool isA = ti.x != KIND_B;
-        const int grp = ti.y, tile = ti.z, ks = ti.w >> 16;
+        const int grp = ti.y, tile = ti.z, ks = (ti.w >> 16) & 15, nks = 1 << ((ti.w >> 20) & 3);
         const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp], e = tb.gexp[grp];
         const uint32_t dcol = lanebase + static_cast<uint32_t>(buf * 2 * N);
         float g[GP], u[GP];
@@ -759,9 +781,9 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
                 u[i] *= tu;
             }
             bool last = true;
-            if (p.KS > 1) {
-                const int unit = grp * TA + tile;
-                float *pb = p.apart + static_cast<size_t>(unit) * p.KS * (2 * GP * kTcRows);
+            if (nks > 1) {
+                const int slot = tc_unit_slot(p, tc_split(p, hd->n_groups), grp * TA + tile);
+                float *pb = p.apart + static_cast<size_t>(slot) * (2 * GP * kTcRows);
 #pragma unroll
                 for (int i = 0; i < GP; ++i)
                     if (i < gcnt) {
@@ -771,9 +793,9 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
                 __threadfence();
                 if (!epi_sync()) break;
                 if (q == 0 && lane == 0) {
-                    const uint32_t old = atomicAdd(p.acnt + unit, 1u);
-                    const int l = old + 1u == static_cast<uint32_t>(p.KS);
-                    if (l) p.acnt[unit] = 0u;  // reset for the next launch
+                    const uint32_t old = atomicAdd(p.acnt + slot, 1u);
+                    const int l = old + 1u == static_cast<uint32_t>(nks);
+                    if (l) p.acnt[slot] = 0u;  // reset for the next launch
                     hd->ep_last = l;
                 }
                 if (!epi_sync()) break;
@@ -788,14 +810,14 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
 #pragma unroll
                             for (int k2 = 0; k2 < 8; ++k2) {
                                 const float *pk = pb + static_cast<size_t>(k2) * (2 * GP * kTcRows);
-                                const bool other = k2 < p.KS && k2 != ks;
+                                const bool other = k2 < nks && k2 != ks;
                                 pg[k2] = other ? __ldcg(pk + (2 * i) * kTcRows + r) : g[i];
                                 pu[k2] = other ? __ldcg(pk + (2 * i + 1) * kTcRows + r) : u[i];
                             }
                             float sg = 0.f, su = 0.f;
 #pragma unroll
                             for (int k2 = 0; k2 < 8; ++k2)
-                                if (k2 < p.KS) {
+                                if (k2 < nks) {
                                     sg += pg[k2];
                                     su += pu[k2];
                                 }
@@ -908,30 +930,46 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
 }
 
 // ------------------------------------------------------------------ tickets
-// Gate/up tickets (group, 128-row tile, K split; the split fastest), then down
-// tickets (group, 128-row tile); group-major both.
+// Gate/up tickets (unit = group x 128-row tile, group-major; a unit's K splits
+// consecutive), then down tickets (group, 128-row tile), group-major.  Units
+// are split KS ways along K, except the last p.tail_units units, split KSt
+// ways: the final wave of gate/up work comes in smaller pieces, so the groups
+// it completes (whose down tickets end the launch) are ready sooner.
 struct TcTicket {
-    int isA, grp, tile, ks;
+    int isA, grp, tile, ks, nks;
 };
-__device__ __forceinline__ TcTicket tc_decode_ticket(int t, int ng, int TA, int KS, int nHt)
+__device__ __forceinline__ TcTicket tc_decode_ticket(const KernelParams &p, const TcSplit &sp, int t, int nHt)
 {
     TcTicket r;
-    const int nA = ng * TA * KS;
-    if (t < nA) {
+    const int TA = p.I / kTcRows;
+    if (t < sp.nhead + sp.ntail) {
+        int u;
+        if (t < sp.nhead) {
+            u = t / p.KS;
+            r.ks = t - u * p.KS;
+            r.nks = p.KS;
+        } else {
+            const int t2 = t - sp.nhead;
+            const int v = t2 / p.KSt;
+            u = sp.tstart + v;
+            r.ks = t2 - v * p.KSt;
+            r.nks = p.KSt;
+        }
         r.isA = 1;
-        r.grp = t / (TA * KS);
-        const int rem = t - r.grp * TA * KS;
-        r.tile = rem / KS;
-        r.ks = rem - r.tile * KS;
+        r.grp = u / TA;
+        r.tile = u - r.grp * TA;
     } else {
-        const int t2 = t - nA;
+        const int t2 = t - sp.nhead - sp.ntail;
         r.isA = 0;
         r.grp = t2 / nHt;
         r.tile = t2 - r.grp * nHt;
         r.ks = 0;
+        r.nks = 1;
     }
     return r;
 }
+// log2 of a split count in {1, 2, 4, 8}
+__device__ __forceinline__ int tc_lg(int v) { return v >= 8 ? 3 : (v >= 4 ? 2 : (v >= 2 ? 1 : 0)); }
 
 // ------------------------------------------------------------------ producer warp
 // Lane 0 issues each stage's copies: gate/up stage = the gate and up tiles (128
@@ -946,9 +984,10 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
     if ((threadIdx.x & 31) != 0) return;
     SmemHdr *hd = tb.hdr;
     const uint64_t pol = policy_evict_first();
-    const int ng = hd->n_groups, TA = p.I / kTcRows, nHt = p.H / kTcRows, KS = p.KS;
-    const int nPA = (p.H / KS) / 256, nPB = (p.I + 511) / 512;
-    const int total = ng * (TA * KS + nHt);
+    const int ng = hd->n_groups, nHt = p.H / kTcRows;
+    const TcSplit sp = tc_split(p, ng);
+    const int nPB = (p.I + 511) / 512;
+    const int total = sp.nhead + sp.ntail + ng * nHt;
     bool ok = true, x_ok = false;
     int s = 0, fill = 0, pq_tail = 0, tq_head = 0;
     uint32_t ph = 0;
@@ -995,8 +1034,9 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
         st_rel_cta(&hd->pq_tail, ++pq_tail);
     };
     while (ok && ticket < total) {
-        const TcTicket ti = tc_decode_ticket(ticket, ng, TA, KS, nHt);
+        const TcTicket ti = tc_decode_ticket(p, sp, ticket, nHt);
         const int e = tb.gexp[ti.grp], gbeg = tb.gbeg[ti.grp], gcnt = tb.gcnt[ti.grp];
+        const int nPA = (p.H / ti.nks) / 256;
         const int nparts = ti.isA ? nPA : nPB;
         for (int part = 0; part < nparts; ++part) {
             if (!wait_for([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
@@ -1009,7 +1049,7 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
                 if (!x_ok && ld_acq_cta(&hd->xready)) flush_x();
                 const int kc = ti.ks * nPA + part;  // 256-element chunk of H
                 const int row = e * p.I + ti.tile * kTcRows;
-                hd->stage_hdr[s] = make_int4(KIND_A, ti.grp, ti.tile, part | (ti.ks << 16));
+                hd->stage_hdr[s] = make_int4(KIND_A, ti.grp, ti.tile, part | (ti.ks << 16) | (tc_lg(ti.nks) << 20));
                 mbar_expect_tx(bar, static_cast<uint32_t>(2 * kTile + 2 * kSfTile + N * 128 + N * 16));
                 tma2d(st + kOffW0, &p.tmt[0], kc * 128, row, bar, pol);
                 tma2d(st + kOffW1, &p.tmt[1], kc * 128, row, bar, pol);
@@ -1070,15 +1110,16 @@ __device__ void tc_helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, vo
     SmemHdr *hd = tb.hdr;
     const uint64_t pol = policy_evict_first();
     const int ng = hd->n_groups;
-    const int TA = p.I / kTcRows, nHt = p.H / kTcRows, KS = p.KS;
-    const int total = ng * (TA * KS + nHt);
+    const int TA = p.I / kTcRows, nHt = p.H / kTcRows;
+    const TcSplit sp = tc_split(p, ng);
+    const int total = sp.nhead + sp.ntail + ng * nHt;
     bool fetch_done = false, xr = false;
     int tq_tail = 0, pq_head = 0;
     int watch = -1;
     uint64_t idle_since = 0;
     auto note_ticket = [&](int tk) {
         if (tk >= total) return;
-        const TcTicket ti = tc_decode_ticket(tk, ng, TA, KS, nHt);
+        const TcTicket ti = tc_decode_ticket(p, sp, tk, nHt);
         if (ti.isA) return;
         if (__shfl_sync(0xffffffffu, ld_acq_cta_u8(tb.hready + ti.grp), 0) != 0) return;
         const uint32_t free_lanes = __ballot_sync(0xffffffffu, watch < 0);
@@ -1092,7 +1133,9 @@ __device__ void tc_helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, vo
         if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
         bool progress = false;
         const int tq_head = __shfl_sync(0xffffffffu, ld_acq_cta(&hd->tq_head), 0);
-        if (!fetch_done && tq_tail - tq_head < kTq && __ballot_sync(0xffffffffu, watch < 0) != 0) {
+        // one ticket ahead of the producer: a gate/up ticket is up to sixteen
+        // stages, so a deeper queue lets early CTAs hoard work the others need
+        if (!fetch_done && tq_tail - tq_head < p.tq_depth && __ballot_sync(0xffffffffu, watch < 0) != 0) {
             int tk = 0;
             if (lane == 0) {
                 tk = static_cast<int>(gridDim.x + atomicAdd(p.ctrl, 1u));
