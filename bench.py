@@ -45,10 +45,12 @@ def peaks():
 
 def measured_traffic():
     """DRAM bytes per launch of the decode step from the committed ncu summary,
-    if that capture was taken of the kernel source as it is now; else None."""
+    if that capture was taken of the kernel sources as they are now (the hash
+    of moe_kernels.cu followed by moe_device.cuh); else None."""
     import hashlib
     try:
-        src = open(os.path.join(ROOT, "quantized_moe_routed_gb300", "csrc", "moe_kernels.cu"), "rb").read()
+        csrc = os.path.join(ROOT, "quantized_moe_routed_gb300", "csrc")
+        src = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ("moe_kernels.cu", "moe_device.cuh"))
         sha = hashlib.sha256(src).hexdigest()
         fields = {}
         for line in open(os.path.join(ROOT, "profiles", "moe_step_kernel_decode.md")):
