@@ -182,6 +182,7 @@ __device__ __forceinline__ uint32_t u4w(const uint4 &v, int i)
 // ------------------------------------------------------------------ shared state
 constexpr int kDoneQ = 16;  // finished tickets in flight from the consumers to the helper
 constexpr int kTq = 4;      // tickets fetched ahead (helper -> producer)
+constexpr int kCombJobs = 256;  // combine jobs a CTA can list per launch (more are summed in place)
 
 // CTA-shared control block.  The roles talk through single-writer fields:
 //   tq       helper -> producer    tickets fetched ahead
@@ -213,9 +214,11 @@ struct SmemHdr {
     int tseq[2];    // accumulator buffer use published with tinfo (release/acquire)
     uint32_t tmem_base;
     int ep_last;
-    float ep_amax[4][16];
-    int ep_exp[16];  // h prescale exponents of the epilogue's pairs
     int grouped;     // grouping tables complete (warps 8-11 -> warps 0-7)
+    // combine jobs (token << 16 | tile) listed by the release warp: cj_count
+    // listed (release-published), cj_claim taken (CAS), cj_closed: no more
+    int cj_count, cj_claim, cj_closed;
+    uint32_t cj[kCombJobs];
 };
 static_assert(sizeof(SmemHdr) <= kTabHdrBytes, "header too large");
 
@@ -436,10 +439,10 @@ __device__ __forceinline__ bool warp_spin(const KernelParams &p, Pred pred, vola
     return __all_sync(0xffffffffu, ok);
 }
 
-// Hand a finished ticket to the helper: slot = ticket sequence number.  The
-// warp's global stores (and, through the acq_rel ticket counter, those of the
-// other seven warps) precede the release; the helper releases them at gpu
-// scope.
+// Hand a finished ticket to the release warp: slot = ticket sequence number.
+// The warp's global stores (and, through the acq_rel ticket counter or the
+// epilogue's barrier, those of the other warps) precede the release; the
+// release warp publishes them at gpu scope.
 __device__ __forceinline__ bool push_done(const KernelParams &p, SmemHdr *hd, int tick, int kind, int grp, int tile,
                                           int lane, volatile int *abort_flag)
 {
@@ -455,4 +458,187 @@ __device__ __forceinline__ bool push_done(const KernelParams &p, SmemHdr *hd, in
     }
     __syncwarp();
     return true;
+}
+
+// ------------------------------------------------------------------ release and combine
+// A (token, tile) whose k per-pair output rows are all written is combined:
+// y rows = sum over the token's valid slots, in slot order, of w * the pair's
+// output row -- no floating-point atomics, so the same bits every run.  The
+// release warp lists these jobs in shared memory and takes them between
+// finished tickets; every other warp helps once its own loop is over
+// (combine_assist), which spreads the burst of last arrivals at the end of a
+// step over the whole CTA.
+
+// One job, warp-wide: ROWS rows, all loads of a batch of eight slots in flight
+// before the sums.
+template <int ROWS>
+__device__ __forceinline__ void combine_tile(const KernelParams &p, const Tabs &tb, int tok, int tile, int lane)
+{
+    constexpr int R = ROWS / 32;
+    const size_t h0 = static_cast<size_t>(tile) * ROWS + lane;
+    __threadfence();  // the other CTAs' output rows, seen through the arrival counter
+    float yv[R];
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) yv[rr] = 0.f;
+    for (int j0 = 0; j0 < p.k; j0 += 8) {
+        float pv[R][8], wv[8];
+        bool ok[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int s = j0 + j;
+            const int ps = s < p.k ? tb.pos[tok * p.k + s] : 0xFFFF;
+            ok[j] = ps != 0xFFFF;
+            wv[j] = ok[j] ? p.w[tok * p.k + s] : 0.f;
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr)
+                pv[rr][j] = ok[j] ? __ldcg(p.part + static_cast<size_t>(ps) * p.H + h0 + rr * 32) : 0.f;
+        }
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (ok[j]) yv[rr] += wv[j] * pv[rr][j];
+    }
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) p.y[static_cast<size_t>(tok) * p.H + h0 + rr * 32] = yv[rr];
+}
+
+// Take the next listed job and run it (warp-wide); false if none is listed.
+template <int ROWS>
+__device__ __forceinline__ bool run_one_combine(const KernelParams &p, const Tabs &tb, int lane)
+{
+    SmemHdr *hd = tb.hdr;
+    uint32_t job = 0;
+    int found = 0;
+    if (lane == 0) {
+        int c = ld_acq_cta(&hd->cj_claim);
+        for (;;) {
+            if (c >= ld_acq_cta(&hd->cj_count)) break;
+            const int prev = atomicCAS(&hd->cj_claim, c, c + 1);
+            if (prev == c) {
+                job = hd->cj[c];
+                found = 1;
+                break;
+            }
+            c = prev;
+        }
+    }
+    if (!__shfl_sync(0xffffffffu, found, 0)) return false;
+    job = __shfl_sync(0xffffffffu, job, 0);
+    combine_tile<ROWS>(p, tb, static_cast<int>(job >> 16), static_cast<int>(job & 0xFFFFu), lane);
+    return true;
+}
+
+// A warp whose own loop is over: run listed jobs until the release warp has
+// closed the list and none is left (bounded by the abort flag and the timeout).
+template <int ROWS>
+__device__ void combine_assist(const KernelParams &p, const Tabs &tb, volatile int *abort_flag)
+{
+    const int lane = threadIdx.x & 31;
+    SmemHdr *hd = tb.hdr;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (run_one_combine<ROWS>(p, tb, lane)) {
+            t0 = 0;
+            continue;
+        }
+        if (__shfl_sync(0xffffffffu, ld_acq_cta(&hd->cj_closed), 0)) {
+            // closed: whatever was listed before closing is visible now
+            if (!run_one_combine<ROWS>(p, tb, lane)) return;
+            continue;
+        }
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) return;
+        int bad = 0;
+        if (lane == 0 && (it & 15u) == 15u) {
+            const uint64_t now = gtimer();
+            if (t0 == 0) t0 = now;
+            else if (static_cast<long long>(now - t0) > p.timeout_ns) {
+                raise_error(p, abort_flag, kErrTimeout);
+                bad = 1;
+            }
+        }
+        if (__shfl_sync(0xffffffffu, bad, 0)) return;
+        __nanosleep(64);
+    }
+}
+
+// Release warp: publishes finished work to the other CTAs in ticket order -- a
+// gpu-scope fence, then the group's gate/up counter (gate/up ticket) or the
+// (token, ROWS-row tile) arrival counters (down ticket).  The arrival that
+// completes a token's tile lists the combine job (or, with the list full,
+// runs it in place).  Leaves once nexit warps have left their loops and every
+// ticket they pushed is released, closing the job list.
+template <int ROWS>
+__device__ void release_loop_common(const KernelParams &p, Tabs tb, int nHt, int nexit, volatile int *abort_flag)
+{
+    const int lane = threadIdx.x & 31;
+    SmemHdr *hd = tb.hdr;
+    int dq_head = 0;
+    uint64_t idle_since = 0;
+    for (;;) {
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        bool progress = false;
+        const int exited = __shfl_sync(0xffffffffu, ld_acq_cta(&hd->cons_exited), 0);
+        for (;;) {
+            const int slot = dq_head % kDoneQ;
+            if (__shfl_sync(0xffffffffu, ld_acq_cta(&hd->dq_seq[slot]), 0) != dq_head + 1) break;
+            __threadfence();  // the ticket's global stores become visible first (cumulative)
+            const int kind = hd->dq_kind[slot], grp = hd->dq_grp[slot], tile = hd->dq_tile[slot];
+            if (kind != KIND_B) {
+                if (lane == 0) atomicAdd(p.doneA + grp, 1u);
+            } else {
+                const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
+                int tok = -1;
+                bool last = false;
+                if (lane < gcnt) {
+                    tok = tb.stok[gbeg + lane];
+                    uint32_t *ctr = p.cnt + static_cast<size_t>(tok) * nHt + tile;
+                    const uint32_t old = atomicAdd(ctr, 1u);
+                    last = old + 1u == static_cast<uint32_t>(tb.kvalid[tok]);
+                    if (last) *ctr = 0u;  // last arrival: reset for the next launch
+                }
+                uint32_t mask = __ballot_sync(0xffffffffu, last);
+                if (mask) {
+                    const int n = hd->cj_count, m = __popc(mask);
+                    if (n + m <= kCombJobs) {
+                        if (last) hd->cj[n + __popc(mask & ((1u << lane) - 1u))] = static_cast<uint32_t>(tok) << 16 | static_cast<uint32_t>(tile);
+                        __syncwarp();
+                        if (lane == 0) st_rel_cta(&hd->cj_count, n + m);
+                    } else {
+                        while (mask) {
+                            const int src = __ffs(mask) - 1;
+                            mask &= mask - 1;
+                            combine_tile<ROWS>(p, tb, __shfl_sync(0xffffffffu, tok, src), tile, lane);
+                        }
+                    }
+                }
+            }
+            ++dq_head;
+            __syncwarp();
+            if (lane == 0) st_rel_cta(&hd->dq_head, dq_head);
+            progress = true;
+        }
+        if (exited == nexit) {
+            __syncwarp();
+            if (lane == 0) st_rel_cta(&hd->cj_closed, 1);
+            break;
+        }
+        // between finished tickets: one listed job
+        if (run_one_combine<ROWS>(p, tb, lane)) progress = true;
+        if (progress) {
+            idle_since = 0;
+        } else {
+            int bad = 0;
+            if (lane == 0) {
+                const uint64_t now = gtimer();
+                if (idle_since == 0) idle_since = now;
+                else if (static_cast<long long>(now - idle_since) > p.timeout_ns) {
+                    raise_error(p, abort_flag, kErrTimeout);
+                    bad = 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, bad, 0)) break;
+            __nanosleep(32);
+        }
+    }
 }

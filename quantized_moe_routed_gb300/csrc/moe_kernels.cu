@@ -778,99 +778,6 @@ __device__ __forceinline__ void helper_loop(const KernelParams &p, uint8_t *smem
     }
 }
 
-// ------------------------------------------------------------------ release warp
-// Publishes finished work to the other CTAs, in ticket order: a gpu-scope
-// fence, then bump the group's gate/up counter (gate/up ticket) or the
-// per-(token, 64-row tile) arrival counters (down ticket).  The CTA that
-// completes a token's tile sums its k per-pair outputs in slot order and
-// writes y -- no floating-point atomics, so the result is the same bits every
-// run.  The k partial loads of a row are all issued before the sum.
-__device__ __forceinline__ void release_loop(const KernelParams &p, Tabs tb, volatile int *abort_flag)
-{
-    const int lane = threadIdx.x & 31;
-    SmemHdr *hd = tb.hdr;
-    int dq_head = 0;
-    uint64_t idle_since = 0;
-    for (;;) {
-        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-        bool progress = false;
-        const int exited = __shfl_sync(0xffffffffu, ld_acq_cta(&hd->cons_exited), 0);
-        for (;;) {
-            const int slot = dq_head % kDoneQ;
-            if (__shfl_sync(0xffffffffu, ld_acq_cta(&hd->dq_seq[slot]), 0) != dq_head + 1) break;
-            __threadfence();  // the consumers' h / partial stores become visible first (cumulative)
-            const int kind = hd->dq_kind[slot], grp = hd->dq_grp[slot], tile = hd->dq_tile[slot];
-            if (kind != KIND_B) {
-                if (lane == 0) atomicAdd(p.doneA + grp, 1u);
-            } else {
-                const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
-                int tok = -1;
-                bool last = false;
-                if (lane < gcnt) {
-                    tok = tb.stok[gbeg + lane];
-                    uint32_t *ctr = p.cnt + static_cast<size_t>(tok) * p.nHt + tile;
-                    const uint32_t old = atomicAdd(ctr, 1u);
-                    last = old + 1u == static_cast<uint32_t>(tb.kvalid[tok]);
-                    if (last) *ctr = 0u;  // last arrival: reset for the next launch
-                }
-                uint32_t mask = __ballot_sync(0xffffffffu, last);
-                if (mask) {
-                    __threadfence();  // see the other CTAs' per-pair outputs
-                    const int h0 = tile * kMB;
-                    while (mask) {
-                        const int src = __ffs(mask) - 1;
-                        mask &= mask - 1;
-                        const int t2 = __shfl_sync(0xffffffffu, tok, src);
-#pragma unroll
-                        for (int rr = 0; rr < kMB / 32; ++rr) {
-                            const int row = rr * 32 + lane;
-                            float pv[kMaxTopK], wv[kMaxTopK];
-#pragma unroll
-                            for (int j = 0; j < kMaxTopK; ++j) {
-                                pv[j] = 0.f;
-                                wv[j] = 0.f;
-                                if (j < p.k) {
-                                    const int ps = tb.pos[t2 * p.k + j];
-                                    if (ps != 0xFFFF) {
-                                        pv[j] = __ldcg(p.part + static_cast<size_t>(ps) * p.H + h0 + row);
-                                        wv[j] = p.w[t2 * p.k + j];
-                                    }
-                                }
-                            }
-                            float yv = 0.f;
-#pragma unroll
-                            for (int j = 0; j < kMaxTopK; ++j)
-                                if (j < p.k && tb.pos[t2 * p.k + j] != 0xFFFF) yv += wv[j] * pv[j];
-                            p.y[static_cast<size_t>(t2) * p.H + h0 + row] = yv;
-                        }
-                    }
-                }
-            }
-            ++dq_head;
-            __syncwarp();
-            if (lane == 0) st_rel_cta(&hd->dq_head, dq_head);
-            progress = true;
-        }
-        // done when every consumer warp has left and its last ticket is released
-        if (exited == kConsumerWarps) break;
-        if (progress) {
-            idle_since = 0;
-        } else {
-            int bad = 0;
-            if (lane == 0) {
-                const uint64_t now = gtimer();
-                if (idle_since == 0) idle_since = now;
-                else if (static_cast<long long>(now - idle_since) > p.timeout_ns) {
-                    raise_error(p, abort_flag, kErrTimeout);
-                    bad = 1;
-                }
-            }
-            if (__shfl_sync(0xffffffffu, bad, 0)) break;
-            __nanosleep(32);
-        }
-    }
-}
-
 // ------------------------------------------------------------------ the persistent step kernel
 template <int NT, bool NULLM>
 __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_constant__ KernelParams p)
@@ -904,6 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
         hd->dq_head = 0;
         hd->pq_head = hd->pq_tail = 0;
         hd->claim = 0;
+        hd->cj_count = hd->cj_claim = hd->cj_closed = 0;
         for (int i = 0; i < kDoneQ; ++i) hd->dq_seq[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -967,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
     }
 
     if (tid >= kConsumerThreads + 64) {
-        release_loop(p, tb, abort_flag);
+        release_loop_common<kMB>(p, tb, p.nHt, kConsumerWarps, abort_flag);
     } else if (tid >= kConsumerThreads + 32) {
         helper_loop(p, smem, tb, abort_flag);
     } else if (tid >= kConsumerThreads) {
@@ -975,6 +883,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
     } else {
         consumer_warp<NT, NULLM>(p, smem, tb, abort_flag);
     }
+    // every warp, its own loop over, helps with the remaining combine jobs
+    __syncwarp();
+    combine_assist<kMB>(p, tb, abort_flag);
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
 

@@ -14,10 +14,11 @@
 // representation error after four digits is about 2^-9 of a block's
 // magnitude, far inside the step's 2e-3 tolerance (it sits near 1.5e-4 on the
 // synthetic NVFP4 experts).  h is produced 128 rows at a time, before its
-// whole row is known, so each 128-row slice gets its own prescale; the
-// scale-factor pass of a down stage rebases every slice's block scales to the
-// row's largest slice (an exact exponent shift unless a scale leaves the
-// E4M3 normal range, which only happens 2^14 below the row's largest slice).
+// whole row is known, so each 128-row slice gets its own prescale; the CTA
+// that completes a group's gate/up work rebases every slice's block scales to
+// the row's largest slice before the group's down tickets may read h (an
+// exact exponent shift unless a scale leaves the E4M3 normal range, which
+// only happens 2^14 below the row's largest slice).
 //
 // Work is split into tickets exactly as in the register path (moe_kernels.cu):
 // gate/up units of 128 intermediate rows (optionally split along K into KS
@@ -26,15 +27,15 @@
 // A CTA (one per SM) runs twelve warps:
 //   warps 0-3   scale warps: per stage, move the weight and activation block
 //               scales from shared memory into tensor memory (tcgen05.st) in
-//               the layout the MMA reads (row r: lane r, column + r/32),
-//               rebasing h slice exponents on the way
+//               the layout the MMA reads (row r: lane r, column + r/32)
 //   warps 4-7   epilogue: read the accumulators (tcgen05.ld), combine digits,
 //               split-K partials, SiLU * up, quantise h into digits (gate/up)
 //               or write per-pair down outputs
 //   warp 8      producer: TMA copies of weight tiles, their scales and x digits
 //   warp 9      MMA issue (one thread) and tensor-memory allocation
 //   warp 10     helper: tickets, dependency watch, h digit copies
-//   warp 11     release: cross-CTA counters and the slot-ordered combine
+//   warp 11     release: cross-CTA counters; lists the slot-ordered combines,
+//               which every warp helps to run once its own loop is over
 // Warps 0-7 first quantise the gathered x rows into digits (rows claimed in
 // batches from a global counter, as in the register path).
 #include "moe_internal.h"
@@ -509,17 +510,6 @@ __device__ __forceinline__ uint32_t rebase4(uint32_t w, int d)
     return o;
 }
 
-// Smallest of a pair's nsl slice exponents (signed bytes, 32-byte row).
-__device__ __forceinline__ int row_eref(const int8_t *hx, int nsl)
-{
-    const uint4 v0 = *reinterpret_cast<const uint4 *>(hx), v1 = *reinterpret_cast<const uint4 *>(hx + 16);
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    int e = 127;
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-        if (i < nsl) e = min(e, static_cast<int>(static_cast<int8_t>(w[i >> 2] >> (8 * (i & 3)))));
-    return e;
-}
 // Per stage: the weight tiles' block scales (row r of the 128) and the
 // activation digit rows' block scales (row n < N) go to tensor memory in the
 // layout the block-scaled MMA reads.  Its scale address names column set + 4kk
@@ -581,9 +571,10 @@ __device__ void tc_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
     const uint32_t tbase = hd->tmem_base;
     const uint32_t idesc = fp4_idesc(N);
     const int nPB = (p.I + 511) / 512;
-    int s = 0, buf = 0;
+    // tickets alternate between the two accumulator buffers: after n tickets
+    // the next one uses buffer n & 1, which has held n >> 1 tickets before
+    int s = 0, nt = 0;
     uint32_t ph = 0;
-    int uses[2] = {0, 0};
     bool ok = true;
     for (;;) {
         if (!wait_bar(&hd->sfready[s], ph, p, abort_flag)) {
@@ -596,8 +587,9 @@ __device__ void tc_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
         const bool isA = h.x != KIND_B;
         const int part = h.w & 0xFFFF;
         const int nparts = isA ? (p.H >> ((h.w >> 20) & 3)) / 256 : nPB;
-        if (part == 0 && uses[buf] > 0) {
-            if (!wait_bar(&hd->accempty[buf], static_cast<uint32_t>((uses[buf] - 1) & 1), p, abort_flag)) {
+        const int buf = nt & 1, used = nt >> 1;
+        if (part == 0 && used > 0) {
+            if (!wait_bar(&hd->accempty[buf], static_cast<uint32_t>((used - 1) & 1), p, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -629,10 +621,9 @@ __device__ void tc_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
         tc_commit(&hd->empty[s]);
         if (part == nparts - 1) {
             hd->tinfo[buf] = h;
-            st_rel_cta(&hd->tseq[buf], uses[buf] + 1);
+            st_rel_cta(&hd->tseq[buf], used + 1);
             tc_commit(&hd->accfull[buf]);
-            ++uses[buf];
-            buf ^= 1;
+            ++nt;
         }
         if (++s == p.NS) {
             s = 0;
@@ -641,11 +632,12 @@ __device__ void tc_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
     }
     // end of work for the epilogue (it also leaves on the abort flag), in the
     // next buffer once the epilogue has read that buffer's previous ticket
-    if (ok && uses[buf] > 0)
-        ok = wait_bar(&hd->accempty[buf], static_cast<uint32_t>((uses[buf] - 1) & 1), p, abort_flag);
+    const int buf = nt & 1, used = nt >> 1;
+    if (ok && used > 0)
+        ok = wait_bar(&hd->accempty[buf], static_cast<uint32_t>((used - 1) & 1), p, abort_flag);
     if (ok) {
         hd->tinfo[buf] = make_int4(KIND_END, 0, 0, 0);
-        st_rel_cta(&hd->tseq[buf], uses[buf] + 1);
+        st_rel_cta(&hd->tseq[buf], used + 1);
         mbar_arrive(&hd->accfull[buf]);
     }
     // every MMA issued must complete before the CTA frees tensor memory
@@ -671,8 +663,7 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
     const uint32_t lanebase = hd->tmem_base + (static_cast<uint32_t>(32 * q) << 16);
     const int TA = p.I / kTcRows, nsl = p.I / kTcRows;
     const size_t hrow = static_cast<size_t>(p.Ipad / 2), srow = static_cast<size_t>(p.Ipad / 16);
-    int buf = 0, npush = 0, nsync = 0;
-    int uses[2] = {0, 0};
+    int nt = 0, npush = 0, nsync = 0;  // tickets read: buffer nt & 1, used nt >> 1 times before
     // the four epilogue warps meet on an mbarrier (bounded wait: a warp that
     // gave up cannot leave the others blocked)
     auto epi_sync = [&]() -> bool {
@@ -683,8 +674,9 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
         return ok;
     };
     for (;;) {
-        if (!warp_wait_bar(p, &hd->accfull[buf], static_cast<uint32_t>(uses[buf] & 1), abort_flag)) break;
-        const int want = uses[buf] + 1;
+        const int buf = nt & 1, used = nt >> 1;
+        if (!warp_wait_bar(p, &hd->accfull[buf], static_cast<uint32_t>(used & 1), abort_flag)) break;
+        const int want = used + 1;
         if (!warp_spin(p, [&] { return ld_acq_cta(&hd->tseq[buf]) == want; }, abort_flag)) break;
         const int4 ti = hd->tinfo[buf];
         if (ti.x == KIND_END) break;
@@ -722,20 +714,21 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
                 }
             }
         } else if (isA) {
-            float4 xm[GP];
-#pragma unroll
-            for (int i = 0; i < GP; ++i)
-                xm[i] = i < gcnt ? __ldcg(reinterpret_cast<const float4 *>(p.xmul) + gbeg + i) : make_float4(0, 0, 0, 0);
 #pragma unroll
             for (int c = 0; c < GP; c += 4) {
                 if (c < gcnt) {
+                    float4 xm[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        xm[i] = c + i < gcnt ? __ldcg(reinterpret_cast<const float4 *>(p.xmul) + gbeg + c + i)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
                     float dg[16], du[16];
                     tc_ld16(dcol + 4 * c, dg);
                     tc_ld16(dcol + N + 4 * c, du);
                     tc_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float4 m = xm[c + i];
+                        const float4 m = xm[i];
                         g[c + i] = dg[4 * i] * m.x + dg[4 * i + 1] * m.y + dg[4 * i + 2] * m.z + dg[4 * i + 3] * m.w;
                         u[c + i] = du[4 * i] * m.x + du[4 * i + 1] * m.y + du[4 * i + 2] * m.z + du[4 * i + 3] * m.w;
                     }
@@ -764,8 +757,7 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&hd->accempty[buf]);
-        ++uses[buf];
-        buf ^= 1;
+        ++nt;
 
         if (!isA) {
             const float ts = __ldg(p.dts + e);
@@ -857,8 +849,8 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
                     // the 128-row slice's largest magnitude: the pair's eight threads
 #pragma unroll
                     for (int d = 1; d < 8; d <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
-                    // each 128-row slice of h gets its own prescale; the scale warps of a
-                    // down stage rebase the slices' block scales to the pair's largest
+                    // each 128-row slice of h gets its own prescale; the group's finisher
+                    // (below) rebases the slices' block scales to the pair's largest
                     const int es = prescale_exp(a);
                     if (pi < gcnt) {
                         const float P = mul_pow2(1.f, es);
@@ -992,18 +984,26 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
     int s = 0, fill = 0, pq_tail = 0, tq_head = 0;
     uint32_t ph = 0;
     int ticket = blockIdx.x;
-    // gate/up stages issued before x is complete: their x copies wait here
-    int pend_s[kTcMaxStages], pend_kc[kTcMaxStages], npend = 0;
+    // gate/up stages issued before x is complete wait for their x copies: they
+    // are npend consecutive ring stages from pend0 (a CTA's gate/up tickets
+    // precede its down tickets, and a stage cannot come round again before its
+    // x has arrived); each one's chunk of H follows from its stage header
+    int pend0 = 0, npend = 0;
     const uint32_t x_items = static_cast<uint32_t>(p.T * ((p.H + 511) / 512));
     auto flush_x = [&]() {
         asm volatile("fence.proxy.async.global;" ::: "memory");
         x_ok = true;
+        int ps = pend0;
         for (int i = 0; i < npend; ++i) {
-            uint8_t *st = smem + pend_s[i] * p.stage_bytes;
-            uint64_t *bar = &hd->full[pend_s[i]];
-            const int gb = tb.gbeg[hd->stage_hdr[pend_s[i]].y];
-            tma2d(st + kOffB0, &p.tmt[6], pend_kc[i] * 128, p.xtok ? 0 : gb * 4, bar, pol);
-            tma2d(st + offSB0(N), &p.tmt[7], pend_kc[i] * 16, p.xtok ? 0 : gb * 4, bar, pol);
+            uint8_t *st = smem + ps * p.stage_bytes;
+            uint64_t *bar = &hd->full[ps];
+            const int4 sh = hd->stage_hdr[ps];
+            const int lg = (sh.w >> 20) & 3;
+            const int kc = ((sh.w >> 16) & 15) * ((p.H >> lg) / 256) + (sh.w & 0xFFFF);
+            const int gb = tb.gbeg[sh.y];
+            tma2d(st + kOffB0, &p.tmt[6], kc * 128, p.xtok ? 0 : gb * 4, bar, pol);
+            tma2d(st + offSB0(N), &p.tmt[7], kc * 16, p.xtok ? 0 : gb * 4, bar, pol);
+            if (++ps == p.NS) ps = 0;
         }
         npend = 0;
     };
@@ -1059,9 +1059,7 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
                     tma2d(st + kOffB0, &p.tmt[6], kc * 128, p.xtok ? 0 : gbeg * 4, bar, pol);
                     tma2d(st + offSB0(N), &p.tmt[7], kc * 16, p.xtok ? 0 : gbeg * 4, bar, pol);
                 } else {
-                    pend_s[npend] = s;
-                    pend_kc[npend] = kc;
-                    ++npend;
+                    if (npend++ == 0) pend0 = s;
                 }
             } else {
                 const int kc0 = 2 * part;  // 256-element chunks of I
@@ -1209,97 +1207,6 @@ __device__ void tc_helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, vo
     }
 }
 
-// ------------------------------------------------------------------ release warp
-// As in the register path: a gpu-scope fence, then the group's gate/up unit
-// counter, or the (token, 128-row tile) arrival counters of a down ticket; the
-// last arrival for a (token, tile) sums the token's k per-pair outputs in slot
-// order (bitwise reproducible) and writes y.
-__device__ void tc_release_loop(const KernelParams &p, Tabs tb, volatile int *abort_flag)
-{
-    const int lane = threadIdx.x & 31;
-    SmemHdr *hd = tb.hdr;
-    const int nHt = p.H / kTcRows;
-    int dq_head = 0;
-    uint64_t idle_since = 0;
-    for (;;) {
-        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-        bool progress = false;
-        const int exited = __shfl_sync(0xffffffffu, ld_acq_cta(&hd->cons_exited), 0);
-        for (;;) {
-            const int slot = dq_head % kDoneQ;
-            if (__shfl_sync(0xffffffffu, ld_acq_cta(&hd->dq_seq[slot]), 0) != dq_head + 1) break;
-            __threadfence();
-            const int kind = hd->dq_kind[slot], grp = hd->dq_grp[slot], tile = hd->dq_tile[slot];
-            if (kind != KIND_B) {
-                if (lane == 0) atomicAdd(p.doneA + grp, 1u);
-            } else {
-                const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
-                int tok = -1;
-                bool last = false;
-                if (lane < gcnt) {
-                    tok = tb.stok[gbeg + lane];
-                    uint32_t *ctr = p.cnt + static_cast<size_t>(tok) * nHt + tile;
-                    const uint32_t old = atomicAdd(ctr, 1u);
-                    last = old + 1u == static_cast<uint32_t>(tb.kvalid[tok]);
-                    if (last) *ctr = 0u;
-                }
-                uint32_t mask = __ballot_sync(0xffffffffu, last);
-                if (mask) {
-                    __threadfence();
-                    const int h0 = tile * kTcRows;
-                    while (mask) {
-                        const int src = __ffs(mask) - 1;
-                        mask &= mask - 1;
-                        const int t2 = __shfl_sync(0xffffffffu, tok, src);
-#pragma unroll
-                        for (int rr = 0; rr < kTcRows / 32; ++rr) {
-                            const int row = rr * 32 + lane;
-                            float pv[kMaxTopK], wv[kMaxTopK];
-#pragma unroll
-                            for (int j = 0; j < kMaxTopK; ++j) {
-                                pv[j] = 0.f;
-                                wv[j] = 0.f;
-                                if (j < p.k) {
-                                    const int ps = tb.pos[t2 * p.k + j];
-                                    if (ps != 0xFFFF) {
-                                        pv[j] = __ldcg(p.part + static_cast<size_t>(ps) * p.H + h0 + row);
-                                        wv[j] = p.w[t2 * p.k + j];
-                                    }
-                                }
-                            }
-                            float yv = 0.f;
-#pragma unroll
-                            for (int j = 0; j < kMaxTopK; ++j)
-                                if (j < p.k && tb.pos[t2 * p.k + j] != 0xFFFF) yv += wv[j] * pv[j];
-                            p.y[static_cast<size_t>(t2) * p.H + h0 + row] = yv;
-                        }
-                    }
-                }
-            }
-            ++dq_head;
-            __syncwarp();
-            if (lane == 0) st_rel_cta(&hd->dq_head, dq_head);
-            progress = true;
-        }
-        if (exited == 4) break;
-        if (progress) {
-            idle_since = 0;
-        } else {
-            int bad = 0;
-            if (lane == 0) {
-                const uint64_t now = gtimer();
-                if (idle_since == 0) idle_since = now;
-                else if (static_cast<long long>(now - idle_since) > p.timeout_ns) {
-                    raise_error(p, abort_flag, kErrTimeout);
-                    bad = 1;
-                }
-            }
-            if (__shfl_sync(0xffffffffu, bad, 0)) break;
-            __nanosleep(32);
-        }
-    }
-}
-
 // ------------------------------------------------------------------ the kernel
 template <int N>
 __global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const __grid_constant__ KernelParams p)
@@ -1336,6 +1243,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const __grid_cons
         hd->dq_head = 0;
         hd->pq_head = hd->pq_tail = 0;
         hd->claim = 0;
+        hd->cj_count = hd->cj_claim = hd->cj_closed = 0;
         for (int i = 0; i < kDoneQ; ++i) hd->dq_seq[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1365,9 +1273,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const __grid_cons
         } else if (warp == 10) {
             tc_helper_loop<N>(p, smem, tb, abort_flag);
         } else {
-            tc_release_loop(p, tb, abort_flag);
+            release_loop_common<kTcRows>(p, tb, p.H / kTcRows, 4, abort_flag);
         }
     }
+    // every warp, its own loop over, helps with the remaining combine jobs
+    __syncwarp();
+    combine_assist<kTcRows>(p, tb, abort_flag);
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     tc_fence_before();
     __syncthreads();
