@@ -6,6 +6,7 @@
 #include "moe_nvfp4.h"
 
 #include <cudaTypedefs.h>
+#include <algorithm>
 
 #include <cstdarg>
 #include <cstdio>
@@ -375,12 +376,21 @@ moe_status_t run_tc(moe_plan *pl, const void *x, const int32_t *ids, const float
         const int P = Tn * d.top_k;
         const int tab = moe::tab_bytes_for(P, Tn);
         const int stage = moe::tc_stage_bytes(N);
-        const int ep_scratch = 16 * moe::kTcRows * 4;  // the epilogue's h rows, [pair][128] fp32
+        const int ep_scratch = 4 * moe::kTcRows * 4;  // the epilogue's h rows, four pairs at a time, fp32
+        // x digit rows per token when the gate/up MMA's N can take every token's
+        // four rows (4T rounded up to 16, at most 2N: T <= 24); else per sorted pair
+        const bool xtok = Tn <= 24;
+        const int NA = xtok ? (4 * Tn + 15) / 16 * 16 : N;
         int ns = (pl->tc_smem_attr - tab - ep_scratch - 1024) / stage;
         if (ns > moe::kTcMaxStages) ns = moe::kTcMaxStages;
-        if (ns > (512 - 4 * N) / 64) ns = (512 - 4 * N) / 64;  // tensor-memory columns: 4N + 64 per stage
-        const int scr = align16i(2 * P) + 8 * d.E + 16;  // grouping scratch, aliases the ring
-        if (ns < 2 || scr > ns * stage) {
+        // tensor memory: two accumulator buffers of gate + up (4 NA columns), then
+        // 64 columns per scale-factor slot
+        int nsf = (512 - 4 * NA) / 64;
+        if (nsf > ns) nsf = ns;
+        // grouping scratch, aliases the ring: the counting sort's or (P <= 256) the
+        // rank sort's ([4][256] u16 tables, 8 ints, the per-expert offsets)
+        const int scr = std::max(align16i(2 * P) + 8 * d.E + 16, 2048 + 32 + 4 * d.E);
+        if (ns < 2 || nsf < 2 || scr > ns * stage) {
             reject(pl);
             return fail(MOE_ERR_UNSUPPORTED_SHAPE, "tensor-core kernel: shared memory does not fit (%d stages)", ns);
         }
@@ -398,12 +408,10 @@ moe_status_t run_tc(moe_plan *pl, const void *x, const int32_t *ids, const float
             const int v = std::atoi(ks);
             if ((v == 1 || v == 2 || v == 4 || v == 8) && d.H % (256 * v) == 0 && units * v <= moe::kTcApartUnits) KS = v;
         }
-        // x digit rows per token when every token's rows fit one MMA (N = 4T
-        // rounded up to 16, T <= 16); else per sorted pair
-        p.xtok = Tn <= 16 ? 1 : 0;
+        p.xtok = xtok ? 1 : 0;
         const uint64_t xrows = p.xtok ? static_cast<uint64_t>(4 * Tn) : static_cast<uint64_t>(pl->tc_rows);
-        CUresult cr = encode_rows(&p.tmt[6], p.xq, xrows, d.H / 2, 128, N, true);
-        if (cr == CUDA_SUCCESS) cr = encode_rows(&p.tmt[7], p.xsf, xrows, d.H / 16, 16, N, false);
+        CUresult cr = encode_rows(&p.tmt[6], p.xq, xrows, d.H / 2, 128, NA, true);
+        if (cr == CUDA_SUCCESS) cr = encode_rows(&p.tmt[7], p.xsf, xrows, d.H / 16, 16, NA, false);
         if (cr == CUDA_SUCCESS) cr = encode_rows(&p.tmt[8], p.hq, pl->tc_rows, pl->Ipad / 2, 128, N, true);
         if (cr == CUDA_SUCCESS) cr = encode_rows(&p.tmt[9], p.hsf, pl->tc_rows, pl->Ipad / 16, 16, N, false);
         if (cr != CUDA_SUCCESS) {
@@ -420,6 +428,8 @@ moe_status_t run_tc(moe_plan *pl, const void *x, const int32_t *ids, const float
         p.tab_off = ns * stage;
         p.red_off = p.tab_off + (tab + 15) / 16 * 16;
         p.tcN = N;
+        p.tcNA = NA;
+        p.NSF = nsf;
         p.KS = KS;
         // the last wave of gate/up units in 4-way K splits (each still >= 2
         // stages), when the units are not split already

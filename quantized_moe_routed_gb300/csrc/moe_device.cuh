@@ -418,8 +418,12 @@ __device__ __forceinline__ bool warp_wait_bar(const KernelParams &p, uint64_t *b
 
 // Bounded per-lane spin until pred() (a CTA-shared flag read with acquire);
 // warp-uniform verdict.
+// pause_ns > 0: sleep between polls, for waits whose end is not
+// latency-critical, so that the waiting warps leave the issue slots to the
+// warps doing the work being waited for.
 template <class Pred>
-__device__ __forceinline__ bool warp_spin(const KernelParams &p, Pred pred, volatile int *abort_flag)
+__device__ __forceinline__ bool warp_spin(const KernelParams &p, Pred pred, volatile int *abort_flag,
+                                          unsigned pause_ns = 0)
 {
     bool ok = pred();
     if (__all_sync(0xffffffffu, ok)) return true;
@@ -427,6 +431,7 @@ __device__ __forceinline__ bool warp_spin(const KernelParams &p, Pred pred, vola
         const uint64_t t0 = gtimer();
         for (uint32_t it = 1;; ++it) {
             if (pred()) { ok = true; break; }
+            if (pause_ns) __nanosleep(pause_ns);
             if ((it & 15u) == 0) {
                 if (*abort_flag) break;
                 if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {

@@ -95,6 +95,8 @@ struct KernelParams {
     float *apart;       // split-K partial gate/up sums
     uint32_t *acnt;     // split-K arrivals per gate/up unit
     int tcN;            // MMA N: digit rows per group (16, 32 or 64; a group has <= tcN/4 pairs)
+    int tcNA;           // gate/up MMA N: tcN, or with per-token x rows 4T rounded up to 16 (<= 2 tcN)
+    int NSF;            // tensor-memory scale-factor slots (<= NS): stage n uses slot n % NSF
     int KS;             // K splits of a gate/up unit (1, 2, 4 or 8) ...
     int KSt, tail_units;  // ... except the last tail_units units: KSt splits
     int tq_depth;       // tickets the helper fetches ahead of the producer (1 .. 4)

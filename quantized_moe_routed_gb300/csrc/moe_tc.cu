@@ -54,10 +54,12 @@ constexpr int kSfTile = 128 * 16; // bytes of its block scales
 constexpr int kOffW0 = 0, kOffW1 = kTile, kOffS0 = 2 * kTile, kOffS1 = 2 * kTile + kSfTile;
 constexpr int kOffB0 = 36864;     // activation digit rows (1024-aligned)
 constexpr int kTmemCols = 512;
-// Tensor memory: accumulators in columns [0, 4N) (two buffers of gate + up, or
-// of down), then 64 columns of scale factors per stage from column 4N: four
-// sets of 16 (gate or first tile, up or second tile, activation first K
-// range, activation second K range), K step kk of a set at +4kk.  Every
+// Tensor memory: two accumulator buffers in columns [0, 4 NA), each gate
+// (NA columns) then up (NA columns), or down (N columns); then NSF slots of 64
+// scale-factor columns from column 4 NA, stage n in slot n % NSF: four sets of
+// 16 (gate or first tile, up or second tile, activation first K range,
+// activation second K range), K step kk of a set at +4kk.  NA is the gate/up
+// MMA's N (all tokens' x digit rows, or the group's), N the down MMA's.  Every
 // tensor-memory address used is a multiple of 4 columns.
 constexpr float kPreMax = 2688.f; // largest prescaled magnitude: 6 * 448
 
@@ -65,7 +67,6 @@ constexpr float kPreMax = 2688.f; // largest prescaled magnitude: 6 * 448
 __device__ __forceinline__ int offB1(int N) { return kOffB0 + N * 128; }
 __device__ __forceinline__ int offSB0(int N) { return kOffB0 + 2 * N * 128; }
 __device__ __forceinline__ int offSB1(int N) { return kOffB0 + 2 * N * 128 + N * 16; }
-__device__ __forceinline__ int offHX(int N) { return kOffB0 + 2 * N * 128 + 2 * N * 16; }
 
 // Gate/up unit splitting along K (see the ticket order below).
 struct TcSplit {
@@ -127,12 +128,13 @@ __device__ __forceinline__ void tc_st_set(uint32_t taddr, uint4 w)
 }
 // Activation scale set: the MMA's datapath for each lane quarter reads the B
 // scales from its own quarter's lanes (lane 32q + n%32, column 4kk + n/32), so
-// every warp writes rows lo = lane (column 4kk) and hi = 32 + lane (column
-// 4kk + 1; only read when N = 64).
-__device__ __forceinline__ void tc_st_bset(uint32_t taddr, uint4 lo, uint4 hi)
+// every warp writes rows r0 = lane, r1 = 32 + lane, r2 = 64 + lane and
+// r3 = 96 + lane in columns 4kk + 0 .. 3 (rows past the MMA's N are not read).
+__device__ __forceinline__ void tc_st_bset(uint32_t taddr, uint4 r0, uint4 r1, uint4 r2, uint4 r3)
 {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %5, %1, %5, %2, %6, %2, %6, %3, %7, %3, %7, %4, %8, %4, %8};" ::"r"(taddr),
-                 "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %5, %9, %13, %2, %6, %10, %14, %3, %7, %11, %15, %4, %8, %12, %16};" ::"r"(taddr),
+                 "r"(r0.x), "r"(r0.y), "r"(r0.z), "r"(r0.w), "r"(r1.x), "r"(r1.y), "r"(r1.z), "r"(r1.w),
+                 "r"(r2.x), "r"(r2.y), "r"(r2.z), "r"(r2.w), "r"(r3.x), "r"(r3.y), "r"(r3.z), "r"(r3.w)
                  : "memory");
 }
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -235,6 +237,37 @@ __device__ __forceinline__ void quant_block4(float (&r)[16], uint2 (&pk)[4], uin
             }
         }
         pk[j] = make_uint2(w[0], w[1]);
+    }
+}
+
+// quant_block4 spread over a quad of lanes (lanes 4b .. 4b+3 hold the block's
+// elements 4(lane & 3) .. +3): the same arithmetic per element, the block's
+// largest magnitude of each digit's residual by two shuffles.  pk[j] = this
+// lane's two code bytes of digit j (elements in order, low nibble first),
+// sc[j] = the digit's scale code (the same in all four lanes).
+__device__ __forceinline__ void quant_block4_quad(float (&r)[4], uint32_t (&pk)[4], uint32_t (&sc)[4])
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float f = static_cast<float>(1 << (2 * j));
+        float amax = fmaxf(fmaxf(fabsf(r[0]), fabsf(r[1])), fmaxf(fabsf(r[2]), fabsf(r[3])));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        float s;
+        sc[j] = e4m3_ceil(amax * f * (1.0f / 6.0f), s);
+        uint32_t w = 0u;
+        if (s > 0.f) {
+            const float inv = f / s, back = s / f;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const uint32_t b = e2m1_pack2(r[2 * i] * inv, r[2 * i + 1] * inv);
+                w |= b << (8 * i);
+                const float2 d = e2m1_unpack2(b);
+                r[2 * i] -= d.x * back;
+                r[2 * i + 1] -= d.y * back;
+            }
+        }
+        pk[j] = w;
     }
 }
 
@@ -351,6 +384,134 @@ __device__ void tc_group_pairs(const KernelParams &p, int P, int16_t *ids16, int
     grp_sync();
 }
 
+// Stable sort of 32 < P <= 256 pairs by expert (ties by pair index, the
+// counting sort's order) and the group tables, every step spread over warps
+// 8-11: per-expert counts (shared atomics), a block scan of the counts, then
+// pair q goes to its expert's offset plus the number of earlier pairs of the
+// same expert (a packed 16-bit compare over the earlier ids), and every
+// sorted position whose offset in its expert's run is a multiple of G opens a
+// group, numbered by a block scan.  scr: ring memory not yet in use.
+__device__ void tc_group_small(const KernelParams &p, int P, int G, uint8_t *scr, Tabs tb)
+{
+    SmemHdr *hd = tb.hdr;
+    const int lt = threadIdx.x - 256, lane = lt & 31, wq = lt >> 5, E = p.E;
+    uint16_t *ids16 = reinterpret_cast<uint16_t *>(scr);  // [256] expert or 0xFFFF
+    uint16_t *sexp = ids16 + 256;                         // [256] expert at a sorted position
+    uint16_t *srun = sexp + 256;                          // [256] first position of its expert's run
+    uint16_t *send = srun + 256;                          // [256] one past the run's last
+    int *wsum = reinterpret_cast<int *>(send + 256);      // [4] warp totals; [4] invalid pairs
+    int *ecnt = wsum + 8;                                 // [E] pairs per expert, then exclusive offsets
+    if (lt == 0) {
+        hd->n_bad = 0;
+        wsum[4] = 0;
+    }
+    for (int e = lt; e < E; e += 128) ecnt[e] = 0;
+    int bad = 0, inval = 0;
+    for (int q = lt; q < 256; q += 128) {
+        int e = -1;
+        if (q < P) {
+            e = p.ids[q];
+            bad += e >= E;
+            if (e < 0 || e >= E) e = -1;
+            inval += q < P && e < 0;
+        }
+        ids16[q] = static_cast<uint16_t>(e);  // 0xFFFF: invalid or past P
+    }
+    grp_sync();
+    if (bad) atomicAdd(&hd->n_bad, bad);
+    if (inval) atomicAdd(&wsum[4], inval);
+    for (int q = lt; q < P; q += 128)
+        if (ids16[q] != 0xFFFFu) atomicAdd(&ecnt[ids16[q]], 1);
+    grp_sync();
+    // exclusive scan of the counts: thread lt owns experts [lt*per, lt*per + per)
+    {
+        const int per = (E + 127) / 128, lo = min(E, lt * per), hi = min(E, lo + per);
+        int sum = 0;
+        for (int e = lo; e < hi; ++e) sum += ecnt[e];
+        int incl = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        if (lane == 31) wsum[wq] = incl;
+        grp_sync();
+        int run = incl - sum;
+        for (int i = 0; i < wq; ++i) run += wsum[i];
+        grp_sync();  // wsum is reused below
+        for (int e = lo; e < hi; ++e) {
+            const int c = ecnt[e];
+            ecnt[e] = run;
+            run += c;
+        }
+    }
+    // ecnt holds offsets now: expert e's run is [ecnt[e], ecnt[e + 1]) (nv for the last)
+    grp_sync();
+    const int nv = P - wsum[4];
+    const uint32_t *ids32 = reinterpret_cast<const uint32_t *>(ids16);
+    for (int q = lt; q < P; q += 128) {
+        const uint32_t e = ids16[q];
+        if (e == 0xFFFFu) {
+            tb.pos[q] = 0xFFFFu;
+            continue;
+        }
+        const uint32_t ee = e | (e << 16);
+        int before = 0;
+        const int nw = q >> 1;  // words wholly before q
+        int w = 0;
+        for (; w + 8 <= nw; w += 8) {
+            uint32_t v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = ids32[w + i];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) before += __popc(__vcmpeq2(v[i], ee));
+        }
+        for (; w < nw; ++w) before += __popc(__vcmpeq2(ids32[w], ee));
+        before >>= 4;
+        if (q & 1) before += ids16[q - 1] == e;
+        const int off = ecnt[e], s = off + before;
+        tb.perm[s] = static_cast<uint16_t>(q);
+        tb.pos[q] = static_cast<uint16_t>(s);
+        sexp[s] = static_cast<uint16_t>(e);
+        srun[s] = static_cast<uint16_t>(off);
+        send[s] = static_cast<uint16_t>(static_cast<int>(e) + 1 < E ? ecnt[e + 1] : nv);  // e's count is >= 1
+    }
+    grp_sync();
+    // group starts over the sorted positions, two per thread
+    const int s0 = 2 * lt, s1 = s0 + 1;
+    const int f0 = s0 < nv && (s0 - srun[s0]) % G == 0;
+    const int f1 = s1 < nv && (s1 - srun[s1]) % G == 0;
+    const int c = f0 + f1;
+    int incl = c;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    if (lane == 31) wsum[wq] = incl;
+    grp_sync();
+    int g = incl - c;
+    for (int i = 0; i < wq; ++i) g += wsum[i];
+    if (f0) {
+        tb.gexp[g] = sexp[s0];
+        tb.gbeg[g] = static_cast<uint16_t>(s0);
+        tb.gcnt[g] = static_cast<uint8_t>(min(G, send[s0] - s0));
+        ++g;
+    }
+    if (f1) {
+        tb.gexp[g] = sexp[s1];
+        tb.gbeg[g] = static_cast<uint16_t>(s1);
+        tb.gcnt[g] = static_cast<uint8_t>(min(G, send[s1] - s1));
+    }
+    if (s0 < nv) tb.stok[s0] = static_cast<uint16_t>(tb.perm[s0] / p.k);
+    if (s1 < nv) tb.stok[s1] = static_cast<uint16_t>(tb.perm[s1] / p.k);
+    if (lt == 0) {
+        hd->n_groups = wsum[0] + wsum[1] + wsum[2] + wsum[3];
+        hd->n_valid = nv;
+    }
+    grp_sync();
+}
+
 // Group the T*k pairs (every CTA, redundantly) into groups of at most G pairs
 // on warps 8-11, while warps 0-7 quantise x; tokens without a valid slot get
 // y = 0.  The counting sort's scratch aliases the stage ring, which is not in
@@ -362,6 +523,8 @@ __device__ void tc_group(const KernelParams &p, uint8_t *smem, Tabs tb, int G)
     if (P <= 32) {
         if (lt < 32) group_pairs_warp(p, P, G, tb);
         grp_sync();
+    } else if (P <= 256) {
+        tc_group_small(p, P, G, smem, tb);
     } else {
         int16_t *ids16 = reinterpret_cast<int16_t *>(smem);
         int32_t *ecnt = reinterpret_cast<int32_t *>(smem + align16(2 * P));
@@ -436,12 +599,22 @@ __device__ void tc_quantize_x(const KernelParams &p, const Tabs &tb, volatile in
         const int t = it / nchunk, c = it - t * nchunk;
         const uint16_t *src = p.x + static_cast<size_t>(t) * p.H;
         float amax = 0.f;
-        for (int e8 = 8 * lane; e8 < p.H; e8 += 256) {
-            const uint4 u = *reinterpret_cast<const uint4 *>(src + e8);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        // the whole row for its largest magnitude: sixteen 16-byte loads per
+        // lane in flight at once (one round trip for H <= 4096)
+        for (int v0 = lane; v0 < p.H / 8; v0 += 512) {
+            uint4 u[16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xffff0000u))));
+            for (int i = 0; i < 16; ++i) {
+                const int v = v0 + 32 * i;
+                u[i] = v < p.H / 8 ? __ldg(reinterpret_cast<const uint4 *>(src) + v) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xffff0000u))));
+            }
         }
 #pragma unroll
         for (int d = 16; d; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
@@ -477,7 +650,7 @@ __device__ void tc_quantize_x(const KernelParams &p, const Tabs &tb, volatile in
             put(t);
         } else {
             if (!grouped) {
-                if (!warp_spin(p, [&] { return ld_acq_cta(&hd->grouped) != 0; }, abort_flag)) break;
+                if (!warp_spin(p, [&] { return ld_acq_cta(&hd->grouped) != 0; }, abort_flag, 128)) break;
                 grouped = true;
             }
             for (int j = 0; j < p.k; ++j) {
@@ -525,32 +698,53 @@ __device__ void tc_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
     SmemHdr *hd = tb.hdr;
     const int q = threadIdx.x >> 5, lane = threadIdx.x & 31, r = 32 * q + lane;
     const uint32_t lanebase = hd->tmem_base + (static_cast<uint32_t>(32 * q) << 16);
-    constexpr int nhi = N > 32 ? 32 : 0;  // second activation row of this lane (N = 64)
-    int s = 0;
-    uint32_t ph = 0;
+    const int NA = p.tcNA;
+    auto row = [&](const uint8_t *b, int i) { return *reinterpret_cast<const uint4 *>(b + 16 * i); };
+    // ring stage s (parity ph) of stage sequence number n; its scale slot
+    // n % NSF; ring stage ms (parity mph) of stage n - NSF, the slot's last user
+    int s = 0, n = 0, slot = 0, ms = 0;
+    uint32_t ph = 0, mph = 0;
+    const uint32_t sfbase = lanebase + 4 * NA;
     for (;;) {
         if (!warp_wait_bar(p, &hd->full[s], ph, abort_flag)) break;
         const int4 h = hd->stage_hdr[s];
         const uint8_t *st = smem + s * p.stage_bytes;
         if (h.x != KIND_END) {
-            const uint32_t col = lanebase + 4 * N + 64 * s;
-            tc_st_set(col + 0, *reinterpret_cast<const uint4 *>(st + kOffS0 + 16 * r));
-            tc_st_set(col + 16, *reinterpret_cast<const uint4 *>(st + kOffS1 + 16 * r));
-            // activation rows lane and lane + nhi (K ranges 0 and, for down, 1)
-            const uint4 a0 = *reinterpret_cast<const uint4 *>(st + offSB0(N) + 16 * lane);
-            const uint4 c0 = *reinterpret_cast<const uint4 *>(st + offSB0(N) + 16 * (lane + nhi));
-            if (h.x == KIND_B) {
-                const uint4 a1 = *reinterpret_cast<const uint4 *>(st + offSB1(N) + 16 * lane);
-                const uint4 c1 = *reinterpret_cast<const uint4 *>(st + offSB1(N) + 16 * (lane + nhi));
-                tc_st_bset(col + 48, a1, c1);
+            // this stage's scale slot was last read by the MMAs of stage n - NSF
+            if (n >= p.NSF) {
+                if (!warp_wait_bar(p, &hd->empty[ms], mph, abort_flag)) break;
+                if (++ms == p.NS) {
+                    ms = 0;
+                    mph ^= 1u;
+                }
             }
-            tc_st_bset(col + 32, a0, c0);
+            const uint32_t col = sfbase + 64u * static_cast<uint32_t>(slot);
+            tc_st_set(col + 0, row(st + kOffS0, r));
+            tc_st_set(col + 16, row(st + kOffS1, r));
+            const uint8_t *sb0 = st + offSB0(N);
+            if (h.x == KIND_B) {
+                // h rows lane and 32 + lane, K ranges 0 and 1
+                const uint8_t *sb1 = st + offSB1(N);
+                const uint4 a0 = row(sb0, lane), a1 = row(sb1, lane);
+                const uint4 c0 = N > 32 ? row(sb0, lane + 32) : a0, c1 = N > 32 ? row(sb1, lane + 32) : a1;
+                tc_st_bset(col + 48, a1, c1, a1, c1);
+                tc_st_bset(col + 32, a0, c0, a0, c0);
+            } else {
+                // the NA x rows (up to 128)
+                const uint4 b0 = row(sb0, lane);
+                const uint4 b1 = NA > 32 ? row(sb0, lane + 32) : b0;
+                const uint4 b2 = NA > 64 ? row(sb0, lane + 64) : b0;
+                const uint4 b3 = NA > 96 ? row(sb0, lane + 96) : b0;
+                tc_st_bset(col + 32, b0, b1, b2, b3);
+            }
             tc_wait_st();
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&hd->sfready[s]);
         if (h.x == KIND_END) break;
+        ++n;
+        if (++slot == p.NSF) slot = 0;
         if (++s == p.NS) {
             s = 0;
             ph ^= 1u;
@@ -569,12 +763,15 @@ __device__ void tc_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
 {
     SmemHdr *hd = tb.hdr;
     const uint32_t tbase = hd->tmem_base;
-    const uint32_t idesc = fp4_idesc(N);
+    const int NA = p.tcNA;
+    const uint32_t idescA = fp4_idesc(NA), idescB = fp4_idesc(N);
     const int nPB = (p.I + 511) / 512;
-    // tickets alternate between the two accumulator buffers: after n tickets
-    // the next one uses buffer n & 1, which has held n >> 1 tickets before
-    int s = 0, nt = 0;
+    // tickets alternate between the two accumulator buffers: after nt tickets
+    // the next one uses buffer nt & 1, which has held nt >> 1 tickets before;
+    // the stage with sequence number n takes scale slot n % NSF (kept as slot)
+    int s = 0, nt = 0, slot = 0;
     uint32_t ph = 0;
+    const uint32_t sfbase = tbase + 4 * NA, nsf = static_cast<uint32_t>(p.NSF);
     bool ok = true;
     for (;;) {
         if (!wait_bar(&hd->sfready[s], ph, p, abort_flag)) {
@@ -595,27 +792,29 @@ __device__ void tc_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
             }
             tc_fence_after();
         }
-        const uint32_t sa = smem_u32(smem + s * p.stage_bytes);
-        const uint32_t sfc = tbase + 4 * N + 64 * s;
-        const uint32_t dcol = tbase + static_cast<uint32_t>(buf * 2 * N);
+        // descriptors of the stage's operands: the start-address field is the
+        // byte address / 16, so a K step of 32 bytes adds 2 (no carry: shared
+        // addresses stay below 2^18)
+        const uint64_t d0 = sw128_desc(smem_u32(smem + s * p.stage_bytes));
+        const uint32_t sfc = sfbase + 64u * static_cast<uint32_t>(slot);
+        const uint32_t dcol = tbase + static_cast<uint32_t>(buf * 2 * NA);
         if (isA) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t acc = (part > 0 || kk > 0) ? 1u : 0u;
-                const uint64_t bd = sw128_desc(sa + kOffB0 + 32 * kk);
-                tc_mma(dcol, sw128_desc(sa + kOffW0 + 32 * kk), bd, idesc, sfc + 4 * kk, sfc + 32 + 4 * kk, acc);
-                tc_mma(dcol + N, sw128_desc(sa + kOffW1 + 32 * kk), bd, idesc, sfc + 16 + 4 * kk, sfc + 32 + 4 * kk,
-                       acc);
+                const uint64_t bd = d0 + (kOffB0 + 32 * kk) / 16;
+                tc_mma(dcol, d0 + (kOffW0 + 32 * kk) / 16, bd, idescA, sfc + 4 * kk, sfc + 32 + 4 * kk, acc);
+                tc_mma(dcol + NA, d0 + (kOffW1 + 32 * kk) / 16, bd, idescA, sfc + 16 + 4 * kk, sfc + 32 + 4 * kk, acc);
             }
         } else {
+            const uint64_t b1 = d0 + static_cast<uint64_t>(offB1(N) / 16);
 #pragma unroll
             for (int kr = 0; kr < 2; ++kr)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint32_t acc = (part > 0 || kr > 0 || kk > 0) ? 1u : 0u;
-                    tc_mma(dcol, sw128_desc(sa + (kr ? kOffW1 : kOffW0) + 32 * kk),
-                           sw128_desc(sa + (kr ? offB1(N) : kOffB0) + 32 * kk), idesc, sfc + 16 * kr + 4 * kk,
-                           sfc + 32 + 16 * kr + 4 * kk, acc);
+                    tc_mma(dcol, d0 + ((kr ? kOffW1 : kOffW0) + 32 * kk) / 16, (kr ? b1 : d0 + kOffB0 / 16) + 2 * kk,
+                           idescB, sfc + 16 * kr + 4 * kk, sfc + 32 + 16 * kr + 4 * kk, acc);
                 }
         }
         tc_commit(&hd->empty[s]);
@@ -625,6 +824,7 @@ __device__ void tc_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
             tc_commit(&hd->accfull[buf]);
             ++nt;
         }
+        if (++slot == static_cast<int>(nsf)) slot = 0;
         if (++s == p.NS) {
             s = 0;
             ph ^= 1u;
@@ -684,7 +884,7 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
         const bool isA = ti.x != KIND_B;
         const int grp = ti.y, tile = ti.z, ks = (ti.w >> 16) & 15, nks = 1 << ((ti.w >> 20) & 3);
         const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp], e = tb.gexp[grp];
-        const uint32_t dcol = lanebase + static_cast<uint32_t>(buf * 2 * N);
+        const uint32_t dcol = lanebase + static_cast<uint32_t>(buf * 2 * p.tcNA);  // gate, then up at + tcNA
         float g[GP], u[GP];
 #pragma unroll
         for (int i = 0; i < GP; ++i) g[i] = u[i] = 0.f;
@@ -701,7 +901,7 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
                         const int tok = tb.stok[gbeg + c + i];
                         xm[i] = __ldcg(reinterpret_cast<const float4 *>(p.xmul) + tok);
                         tc_ld4(dcol + 4 * tok, dg[i]);
-                        tc_ld4(dcol + N + 4 * tok, du[i]);
+                        tc_ld4(dcol + p.tcNA + 4 * tok, du[i]);
                     }
                 }
                 tc_wait_ld();
@@ -724,7 +924,7 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
                                              : make_float4(0.f, 0.f, 0.f, 0.f);
                     float dg[16], du[16];
                     tc_ld16(dcol + 4 * c, dg);
-                    tc_ld16(dcol + N + 4 * c, du);
+                    tc_ld16(dcol + p.tcNA + 4 * c, du);
                     tc_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -819,56 +1019,58 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
                 }
             }
             if (last) {
-                // h = SiLU(g) * u, then four digit rows per pair
-                // h rows -> shared memory [pair][128], then thread t quantises pair
-                // t/8's 16-element block t%8 into four digits (no shuffles)
+                // h = SiLU(g) * u, then four digit rows per pair, four pairs per
+                // round: the rows go through shared memory ([4][128] floats), then
+                // warp q takes pair i0 + q (its 128-row slice gets one prescale;
+                // the group's finisher below rebases the slices' block scales to
+                // the pair's largest), lane l its rows 4l .. 4l+3, a quad of lanes
+                // one 16-row block
                 float *hs = reinterpret_cast<float *>(smem + p.red_off);
+                bool bad = false;
 #pragma unroll
-                for (int i = 0; i < GP; ++i) {
-                    if (i < gcnt) {
-                        const float hv = g[i] / (1.0f + __expf(-g[i])) * u[i];
-                        if (!(fabsf(hv) < 3.0e38f)) atomicOr(p.ctrl + 2, kErrRange);
-                        hs[i * kTcRows + r] = hv;
+                for (int i0 = 0; i0 < GP; i0 += 4) {
+                    if (i0 >= gcnt) break;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (i0 + i < gcnt) {
+                            const float hv = g[i0 + i] / (1.0f + __expf(-g[i0 + i])) * u[i0 + i];
+                            if (!(fabsf(hv) < 3.0e38f)) atomicOr(p.ctrl + 2, kErrRange);
+                            hs[i * kTcRows + r] = hv;
+                        }
                     }
-                }
-                if (!epi_sync()) break;
-                {
-                    const int t = threadIdx.x - 128, pi = t >> 3, blk = t & 7;
-                    float v[16];
-                    float a = 0.f;
-#pragma unroll
-                    for (int i4 = 0; i4 < 4; ++i4) {
-                        const float4 x4 = pi < gcnt ? *reinterpret_cast<const float4 *>(hs + pi * kTcRows + 16 * blk + 4 * i4)
-                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-                        v[4 * i4] = x4.x;
-                        v[4 * i4 + 1] = x4.y;
-                        v[4 * i4 + 2] = x4.z;
-                        v[4 * i4 + 3] = x4.w;
-                        a = fmaxf(a, fmaxf(fmaxf(fabsf(x4.x), fabsf(x4.y)), fmaxf(fabsf(x4.z), fabsf(x4.w))));
+                    if (!epi_sync()) {
+                        bad = true;
+                        break;
                     }
-                    // the 128-row slice's largest magnitude: the pair's eight threads
-#pragma unroll
-                    for (int d = 1; d < 8; d <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
-                    // each 128-row slice of h gets its own prescale; the group's finisher
-                    // (below) rebases the slices' block scales to the pair's largest
-                    const int es = prescale_exp(a);
+                    const int pi = i0 + q;
                     if (pi < gcnt) {
+                        const float4 x4 = *reinterpret_cast<const float4 *>(hs + q * kTcRows + 4 * lane);
+                        float v[4] = {x4.x, x4.y, x4.z, x4.w};
+                        float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+                        for (int d = 1; d < 32; d <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
+                        const int es = prescale_exp(a);
                         const float P = mul_pow2(1.f, es);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] *= P;
-                        uint2 pk[4];
-                        uint32_t sc[4];
-                        quant_block4(v, pk, sc);
-                        const int k0 = tile * kTcRows + 16 * blk;
+                        for (int e4 = 0; e4 < 4; ++e4) v[e4] *= P;
+                        uint32_t pk[4], sc[4];
+                        quant_block4_quad(v, pk, sc);
+                        const int k0 = tile * kTcRows + 4 * lane;  // this lane's first row of h
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const size_t row = static_cast<size_t>(gbeg + pi) * 4 + j;
-                            *reinterpret_cast<uint2 *>(p.hq + row * hrow + k0 / 2) = pk[j];
-                            p.hsf[row * srow + k0 / 16] = static_cast<uint8_t>(sc[j]);
+                            *reinterpret_cast<uint16_t *>(p.hq + row * hrow + k0 / 2) = static_cast<uint16_t>(pk[j]);
+                            if ((lane & 3) == 0) p.hsf[row * srow + k0 / 16] = static_cast<uint8_t>(sc[j]);
                         }
-                        if (blk == 0) p.hexp[static_cast<size_t>(gbeg + pi) * 64 + tile] = static_cast<int8_t>(es);
+                        if (lane == 0) p.hexp[static_cast<size_t>(gbeg + pi) * 64 + tile] = static_cast<int8_t>(es);
+                    }
+                    // every warp has read the round's rows before the next round writes
+                    if (!epi_sync()) {
+                        bad = true;
+                        break;
                     }
                 }
+                if (bad) break;
             }
             if (!last) continue;
             // this unit's h is written: count it for the group; the CTA that
@@ -1046,11 +1248,13 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
             uint8_t *st = smem + s * p.stage_bytes;
             uint64_t *bar = &hd->full[s];
             if (ti.isA) {
-                if (!x_ok && ld_acq_cta(&hd->xready)) flush_x();
+                // x complete: the helper's flag, or (before the helper runs) the
+                // published count itself
+                if (!x_ok && (ld_acq_cta(&hd->xready) || ld_acquire(p.ctrl + 3) >= x_items)) flush_x();
                 const int kc = ti.ks * nPA + part;  // 256-element chunk of H
                 const int row = e * p.I + ti.tile * kTcRows;
                 hd->stage_hdr[s] = make_int4(KIND_A, ti.grp, ti.tile, part | (ti.ks << 16) | (tc_lg(ti.nks) << 20));
-                mbar_expect_tx(bar, static_cast<uint32_t>(2 * kTile + 2 * kSfTile + N * 128 + N * 16));
+                mbar_expect_tx(bar, static_cast<uint32_t>(2 * kTile + 2 * kSfTile + p.tcNA * 128 + p.tcNA * 16));
                 tma2d(st + kOffW0, &p.tmt[0], kc * 128, row, bar, pol);
                 tma2d(st + kOffW1, &p.tmt[1], kc * 128, row, bar, pol);
                 tma2d(st + kOffS0, &p.tmt[3], kc * 16, row, bar, pol);
@@ -1260,7 +1464,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const __grid_cons
         // x digits (per token: concurrently with the grouping), then the loops,
         // which read the grouping tables
         tc_quantize_x(p, tb, abort_flag);
-        if (warp_spin(p, [&] { return ld_acq_cta(&hd->grouped) != 0; }, abort_flag)) {
+        if (warp_spin(p, [&] { return ld_acq_cta(&hd->grouped) != 0; }, abort_flag, 128)) {
             if (warp < 4) tc_scale_loop<N>(p, smem, tb, abort_flag);
             else tc_epilogue_loop<N>(p, smem, tb, abort_flag);
         }
