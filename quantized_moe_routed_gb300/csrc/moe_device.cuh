@@ -237,6 +237,8 @@ struct Tabs {
     uint8_t *gcnt;    // [P] group -> number of pairs (1..16)
     uint8_t *hready;  // [P] group -> 0 unknown, 1 polled by the helper, 2 h rows complete
     uint8_t *kvalid;  // [T] valid slots per token
+    int8_t *eref;     // [P] sorted position -> h reference exponent of the pair (tensor-core
+                      //     kernel: set by the helper before it marks the group's h complete)
 };
 
 __host__ __device__ inline int align16(int v) { return (v + 15) & ~15; }
@@ -254,6 +256,7 @@ __device__ Tabs make_tabs(uint8_t *smem, int tab_off, int P)
     t.stok = reinterpret_cast<uint16_t *>(b + o); o += align16(2 * P);
     t.gcnt = b + o; o += align16(P);
     t.hready = b + o; o += align16(P);
+    t.eref = reinterpret_cast<int8_t *>(b + o); o += align16(P);
     t.kvalid = b + o;
     return t;
 }

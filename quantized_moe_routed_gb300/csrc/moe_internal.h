@@ -34,7 +34,7 @@ constexpr int kTabHdrBytes = 3072;
 inline int tab_bytes_for(int P, int T)
 {
     const int a2 = (2 * P + 15) & ~15, a1 = (P + 15) & ~15, aT = (T + 15) & ~15;
-    return (kTabHdrBytes + 5 * a2 + 2 * a1 + aT + 127) / 128 * 128;
+    return (kTabHdrBytes + 5 * a2 + 3 * a1 + aT + 127) / 128 * 128;
 }
 
 // Workspace control block (first 256 bytes of the workspace).

@@ -586,16 +586,18 @@ __device__ void tc_group(const KernelParams &p, uint8_t *smem, Tabs tb, int G)
 __device__ void tc_quantize_x(const KernelParams &p, const Tabs &tb, volatile int *abort_flag)
 {
     SmemHdr *hd = tb.hdr;
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nchunk = (p.H + 511) / 512, nitems = p.T * nchunk, nblk = p.H / 16;
-    int mine = 0;
     bool grouped = p.xtok != 0;
-    for (;;) {
-        int it = 0;
-        if (lane == 0) it = static_cast<int>(atomicAdd(p.ctrl + 4, 1u));
-        it = __shfl_sync(0xffffffffu, it, 0);
-        if (it >= nitems) break;
-        ++mine;
+    // one claim of eight items for the CTA (warp w takes base + w), published
+    // in shared memory; only if items remain after that batch do warps go on
+    // claiming one at a time
+    if (threadIdx.x == 0) st_rel_cta(&hd->claim, static_cast<int>(atomicAdd(p.ctrl + 4, 8u)));
+    if (!warp_spin(p, [&] { return ld_acq_cta(&hd->claim) >= 0; }, abort_flag)) return;
+    const int base = ld_acq_cta(&hd->claim);
+    const bool more = base + 8 < nitems;
+    int it = base + warp;
+    while (it < nitems) {
         const int t = it / nchunk, c = it - t * nchunk;
         const uint16_t *src = p.x + static_cast<size_t>(t) * p.H;
         float amax = 0.f;
@@ -658,12 +660,40 @@ __device__ void tc_quantize_x(const KernelParams &p, const Tabs &tb, volatile in
                 if (r != 0xFFFF) put(r);
             }
         }
-    }
-    if (mine) {
+        // publish the item at once (gpu-scope release of the warp's stores)
         __threadfence();
         __syncwarp();
-        if (lane == 0) atomicAdd(p.ctrl + 3, static_cast<uint32_t>(mine));
+        if (lane == 0) atomicAdd(p.ctrl + 3, 1u);
+        if (!more) break;
+        int nx = 0;
+        if (lane == 0) nx = static_cast<int>(atomicAdd(p.ctrl + 4, 1u));
+        it = __shfl_sync(0xffffffffu, nx, 0);
     }
+}
+
+// Epilogue warp 4, before its loop (it has nothing to do until the first MMA,
+// which needs x): watch the published x count in a tight bounded loop and
+// raise the CTA's xready flag the moment x is complete.
+__device__ void tc_watch_x(const KernelParams &p, SmemHdr *hd, volatile int *abort_flag)
+{
+    if ((threadIdx.x & 31) == 0) {
+        const uint32_t x_items = static_cast<uint32_t>(p.T * ((p.H + 511) / 512));
+        const uint64_t t0 = gtimer();
+        for (uint32_t it = 0;; ++it) {
+            if (ld_acquire(p.ctrl + 3) >= x_items) {
+                st_rel_cta(&hd->xready, 1);
+                break;
+            }
+            if ((it & 15u) == 15u) {
+                if (*abort_flag) break;
+                if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
+                    raise_error(p, abort_flag, kErrTimeout);
+                    break;
+                }
+            }
+        }
+    }
+    __syncwarp();
 }
 
 // ------------------------------------------------------------------ scale warps
@@ -935,9 +965,13 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
                 }
             }
         } else {
-            int eref[GP];  // each pair's h reference exponent (its largest slice's), set by the group's finisher
+            // each pair's h reference exponent (its largest slice's, set by the
+            // group's finisher), copied to shared memory by the helper before it
+            // marked the group complete (acquire that mark first)
+            (void)ld_acq_cta_u8(tb.hready + grp);
+            int eref[GP];
 #pragma unroll
-            for (int i = 0; i < GP; ++i) eref[i] = i < gcnt ? __ldcg(p.hexp + static_cast<size_t>(gbeg + i) * 64 + 32) : 0;
+            for (int i = 0; i < GP; ++i) eref[i] = i < gcnt ? tb.eref[gbeg + i] : 0;
 #pragma unroll
             for (int c = 0; c < GP; c += 4) {
                 if (c < gcnt) {
@@ -1191,7 +1225,6 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
     // precede its down tickets, and a stage cannot come round again before its
     // x has arrived); each one's chunk of H follows from its stage header
     int pend0 = 0, npend = 0;
-    const uint32_t x_items = static_cast<uint32_t>(p.T * ((p.H + 511) / 512));
     auto flush_x = [&]() {
         asm volatile("fence.proxy.async.global;" ::: "memory");
         x_ok = true;
@@ -1210,7 +1243,7 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
         npend = 0;
     };
     auto poll_x = [&]() {
-        if (!x_ok && npend > 0 && ld_acquire(p.ctrl + 3) >= x_items) flush_x();
+        if (!x_ok && npend > 0 && ld_acq_cta(&hd->xready)) flush_x();
     };
     auto wait_for = [&](auto &&cond) -> bool {
         if (cond()) return true;
@@ -1248,9 +1281,6 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
             uint8_t *st = smem + s * p.stage_bytes;
             uint64_t *bar = &hd->full[s];
             if (ti.isA) {
-                // x complete: the helper's flag, or (before the helper runs) the
-                // published count itself
-                if (!x_ok && (ld_acq_cta(&hd->xready) || ld_acquire(p.ctrl + 3) >= x_items)) flush_x();
                 const int kc = ti.ks * nPA + part;  // 256-element chunk of H
                 const int row = e * p.I + ti.tile * kTcRows;
                 hd->stage_hdr[s] = make_int4(KIND_A, ti.grp, ti.tile, part | (ti.ks << 16) | (tc_lg(ti.nks) << 20));
@@ -1259,6 +1289,8 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
                 tma2d(st + kOffW1, &p.tmt[1], kc * 128, row, bar, pol);
                 tma2d(st + kOffS0, &p.tmt[3], kc * 16, row, bar, pol);
                 tma2d(st + kOffS1, &p.tmt[4], kc * 16, row, bar, pol);
+                // x complete (the flag epilogue warp 4 raises; a shared-memory read)
+                if (!x_ok && ld_acq_cta(&hd->xready)) flush_x();
                 if (x_ok) {
                     tma2d(st + kOffB0, &p.tmt[6], kc * 128, p.xtok ? 0 : gbeg * 4, bar, pol);
                     tma2d(st + offSB0(N), &p.tmt[7], kc * 16, p.xtok ? 0 : gbeg * 4, bar, pol);
@@ -1303,7 +1335,7 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
 }
 
 // ------------------------------------------------------------------ helper warp
-// Tickets ahead of the producer, the published-x watch, per-group gate/up
+// Tickets ahead of the producer, the CTA's x-ready flag, per-group gate/up
 // completion watch (one group per lane) and the queued activation copies.
 template <int N>
 __device__ void tc_helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, volatile int *abort_flag)
@@ -1350,16 +1382,21 @@ __device__ void tc_helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, vo
             else note_ticket(tk);
             progress = true;
         }
-        if (!xr) {
-            int done = 0;
-            if (lane == 0) done = ld_acquire(p.ctrl + 3) >= static_cast<uint32_t>(p.T * ((p.H + 511) / 512));
-            if (__shfl_sync(0xffffffffu, done, 0)) {
-                xr = true;
-                if (lane == 0) st_rel_cta(&hd->xready, 1);
-                progress = true;
-            }
+        if (!xr && __shfl_sync(0xffffffffu, ld_acq_cta(&hd->xready), 0)) {
+            xr = true;
+            progress = true;
         }
         if (watch >= 0 && ld_acquire(p.doneA + watch) == static_cast<uint32_t>(TA) + 1u) {
+            // the group's h reference exponents (its finisher's) for the epilogue,
+            // then the group is marked complete (release)
+            const int gb = tb.gbeg[watch], gc = tb.gcnt[watch];
+            int8_t ev[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                ev[i] = i < gc ? __ldcg(p.hexp + static_cast<size_t>(gb + i) * 64 + 32) : 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (i < gc) tb.eref[gb + i] = ev[i];
             st_rel_cta_u8(tb.hready + watch, 2);
             watch = -1;
             progress = true;
@@ -1446,7 +1483,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const __grid_cons
         hd->tq_head = hd->tq_tail = 0;
         hd->dq_head = 0;
         hd->pq_head = hd->pq_tail = 0;
-        hd->claim = 0;
+        hd->claim = -1;  // x items: the CTA's batch, claimed by thread 0
         hd->cj_count = hd->cj_claim = hd->cj_closed = 0;
         for (int i = 0; i < kDoneQ; ++i) hd->dq_seq[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1464,6 +1501,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_tc_kernel(const __grid_cons
         // x digits (per token: concurrently with the grouping), then the loops,
         // which read the grouping tables
         tc_quantize_x(p, tb, abort_flag);
+        if (warp == 4) tc_watch_x(p, hd, abort_flag);
         if (warp_spin(p, [&] { return ld_acq_cta(&hd->grouped) != 0; }, abort_flag, 128)) {
             if (warp < 4) tc_scale_loop<N>(p, smem, tb, abort_flag);
             else tc_epilogue_loop<N>(p, smem, tb, abort_flag);
