@@ -1,0 +1,118 @@
+"""The tensor-core path's activation operand, restated and bounded on the CPU.
+
+The block-scaled FP4 MMA takes FP4 on both sides, so the tensor-core kernel
+feeds each activation row as the sum of four NVFP4 "digit" rows: after one
+power-of-two prescale of the row (largest magnitude into (1344, 2688]), digit j
+holds 4^j times the residual left by digits 0..j-1, per 16-element block an
+E4M3 scale rounded up and E2M1 round-to-nearest-even.  This module writes that
+decomposition out from its definition (numpy, float64, no code shared with the
+kernel) and pins the error bound the design relies on: after four digits every
+element is within (9/8 / 6)^4 of its block's largest magnitude, i.e. about
+1.24e-3, well inside the step's 2e-3 tolerance on max |y|.
+"""
+import numpy as np
+import pytest
+
+E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def e4m3_values():
+    """All non-negative finite E4M3 values (codes 0x00..0x7E), ascending."""
+    out = []
+    for c in range(0x7F):
+        e, m = c >> 3, c & 7
+        out.append(m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    return np.array(out)
+
+
+E4M3 = e4m3_values()
+
+
+def e4m3_ceil(a):
+    """Smallest E4M3 value >= a (a >= 0), saturating at 448."""
+    i = np.searchsorted(E4M3, a, side="left")
+    return E4M3[np.minimum(i, len(E4M3) - 1)]
+
+
+def e2m1_rne(v):
+    """Round to the E2M1 grid, ties to the even code, saturating at 6."""
+    s = np.sign(v)
+    a = np.minimum(np.abs(v), 6.0)
+    i = np.searchsorted(E2M1, a)  # first grid point >= a
+    i = np.clip(i, 1, len(E2M1) - 1)
+    lo, hi = E2M1[i - 1], E2M1[i]
+    pick_hi = (a - lo > hi - a) | ((a - lo == hi - a) & ((i % 2) == 0))
+    return s * np.where(pick_hi, hi, lo)
+
+
+def prescale_exponent(amax):
+    """e with amax * 2^e in (1344, 2688]."""
+    e = int(np.floor(np.log2(2688.0 / amax)))
+    while amax * 2.0 ** e > 2688.0:
+        e -= 1
+    while amax * 2.0 ** (e + 1) <= 2688.0:
+        e += 1
+    return e
+
+
+def digits(row, ndig=4):
+    """(prescale exponent, list of digit rows as values) of one activation row."""
+    e = prescale_exponent(np.max(np.abs(row)))
+    r = row * 2.0 ** e
+    out = []
+    for j in range(ndig):
+        f = 4.0 ** j
+        blocks = (r * f).reshape(-1, 16)
+        s = e4m3_ceil(np.max(np.abs(blocks), axis=1) / 6.0)[:, None]
+        q = np.where(s > 0, e2m1_rne(np.divide(blocks, s, out=np.zeros_like(blocks), where=s > 0)), 0.0) * s
+        out.append(q.reshape(-1) / f)
+        r = r - q.reshape(-1) / f
+    return e, out
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_four_digits_stay_within_the_bound(seed):
+    rng = np.random.default_rng(seed)
+    row = rng.standard_normal(4096) * rng.choice([1e-3, 1.0, 37.0])
+    row[rng.integers(0, 4096, 8)] *= 50.0  # a few outliers, as activations have
+    e, ds = digits(row)
+    recon = sum(ds) * 2.0 ** -e
+    blocks = np.abs(row.reshape(-1, 16)).max(axis=1).repeat(16)
+    bound = (9.0 / 8.0 / 6.0) ** 4
+    err = np.abs(recon - row)
+    assert np.all(err <= bound * blocks * (1 + 1e-12))
+    # far inside the bound on average
+    assert np.mean(err / np.maximum(blocks, 1e-300)) < bound / 4
+
+
+def test_each_digit_shrinks_the_residual_by_the_stated_factor():
+    rng = np.random.default_rng(7)
+    row = rng.standard_normal(4096)
+    e, ds = digits(row, ndig=4)
+    r = row * 2.0 ** e
+    amax = np.abs(r.reshape(-1, 16)).max(axis=1)
+    for j in range(4):
+        r = r - ds[j]
+        left = np.abs(r.reshape(-1, 16)).max(axis=1)
+        assert np.all(left <= amax * (9.0 / 8.0 / 6.0) ** (j + 1) * (1 + 1e-12))
+
+
+def test_digit_codes_never_saturate_and_zero_stays_zero():
+    rng = np.random.default_rng(3)
+    row = rng.standard_normal(512)
+    row[:16] = 0.0  # an all-zero block: every digit and scale is zero
+    e, ds = digits(row)
+    assert all(np.all(d[:16] == 0.0) for d in ds)
+    # scales are rounded up, so no element of any digit exceeds 6 x its scale
+    r = row * 2.0 ** e
+    for j in range(4):
+        f = 4.0 ** j
+        b = (r * f).reshape(-1, 16)
+        s = e4m3_ceil(np.abs(b).max(axis=1) / 6.0)
+        assert np.all(np.abs(b).max(axis=1) <= 6.0 * s + 1e-12)
+        r = r - ds[j]
+
+
+def test_e2m1_ties_go_to_the_even_code():
+    v = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -5.0, 7.0])
+    assert e2m1_rne(v).tolist() == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, -0.0, -4.0, 6.0]
