@@ -123,6 +123,18 @@ __device__ __forceinline__ void st_rel_cta_u8(uint8_t *a, int v)
     asm volatile("st.release.cta.shared::cta.u8 [%0], %1;" ::"r"(smem_u32(a)), "r"(v) : "memory");
 }
 
+// Global counters at gpu scope: an arrival that also publishes (release) what
+// the arriving thread has observed, and (acq_rel) sees what earlier arrivals published.
+__device__ __forceinline__ uint32_t atom_add_acqrel_gpu(uint32_t *a, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void red_add_release_gpu(uint32_t *a, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
 __device__ __forceinline__ int atom_add_acqrel_cta(int *a, int v)
 {
     int old;
@@ -589,11 +601,12 @@ __device__ void release_loop_common(const KernelParams &p, Tabs tb, int nHt, int
         const int exited = __shfl_sync(0xffffffffu, ld_acq_cta(&hd->cons_exited), 0);
         for (;;) {
             const int slot = dq_head % kDoneQ;
+            // every lane acquires the entry (CTA scope), so its gpu-scope release
+            // below also publishes the ticket's global stores (cumulativity)
             if (__shfl_sync(0xffffffffu, ld_acq_cta(&hd->dq_seq[slot]), 0) != dq_head + 1) break;
-            __threadfence();  // the ticket's global stores become visible first (cumulative)
             const int kind = hd->dq_kind[slot], grp = hd->dq_grp[slot], tile = hd->dq_tile[slot];
             if (kind != KIND_B) {
-                if (lane == 0) atomicAdd(p.doneA + grp, 1u);
+                if (lane == 0) red_add_release_gpu(p.doneA + grp, 1u);
             } else {
                 const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
                 int tok = -1;
@@ -601,7 +614,7 @@ __device__ void release_loop_common(const KernelParams &p, Tabs tb, int nHt, int
                 if (lane < gcnt) {
                     tok = tb.stok[gbeg + lane];
                     uint32_t *ctr = p.cnt + static_cast<size_t>(tok) * nHt + tile;
-                    const uint32_t old = atomicAdd(ctr, 1u);
+                    const uint32_t old = atom_add_acqrel_gpu(ctr, 1u);
                     last = old + 1u == static_cast<uint32_t>(tb.kvalid[tok]);
                     if (last) *ctr = 0u;  // last arrival: reset for the next launch
                 }
