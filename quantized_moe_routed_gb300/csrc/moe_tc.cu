@@ -48,7 +48,6 @@ namespace {
 #include "moe_device.cuh"
 
 // ------------------------------------------------------------------ constants
-constexpr int kTcWarps = kTcThreads / 32;
 constexpr int kTile = 128 * 128;  // bytes of an E2M1 tile: 128 rows x 256 elements
 constexpr int kSfTile = 128 * 16; // bytes of its block scales
 constexpr int kOffW0 = 0, kOffW1 = kTile, kOffS0 = 2 * kTile, kOffS1 = 2 * kTile + kSfTile;
@@ -61,7 +60,6 @@ constexpr int kTmemCols = 512;
 // activation second K range), K step kk of a set at +4kk.  NA is the gate/up
 // MMA's N (all tokens' x digit rows, or the group's), N the down MMA's.  Every
 // tensor-memory address used is a multiple of 4 columns.
-constexpr float kPreMax = 2688.f; // largest prescaled magnitude: 6 * 448
 
 
 __device__ __forceinline__ int offB1(int N) { return kOffB0 + N * 128; }
@@ -1270,7 +1268,7 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
     };
     while (ok && ticket < total) {
         const TcTicket ti = tc_decode_ticket(p, sp, ticket, nHt);
-        const int e = tb.gexp[ti.grp], gbeg = tb.gbeg[ti.grp], gcnt = tb.gcnt[ti.grp];
+        const int e = tb.gexp[ti.grp], gbeg = tb.gbeg[ti.grp];
         const int nPA = (p.H / ti.nks) / 256;
         const int nparts = ti.isA ? nPA : nPB;
         for (int part = 0; part < nparts; ++part) {
@@ -1414,7 +1412,7 @@ __device__ void tc_helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, vo
                 const int si = hd->pq_stage[slot], part = hd->pq_part[slot];
                 uint8_t *st = smem + si * p.stage_bytes;
                 uint64_t *bar = &hd->full[si];
-                const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
+                const int gbeg = tb.gbeg[grp];
                 if (kind == KIND_A) {
                     tma2d(st + kOffB0, &p.tmt[6], part * 128, p.xtok ? 0 : gbeg * 4, bar, pol);
                     tma2d(st + offSB0(N), &p.tmt[7], part * 16, p.xtok ? 0 : gbeg * 4, bar, pol);
