@@ -64,6 +64,17 @@ def measured_traffic():
     return None
 
 
+def aggregate_ranks(ms, nbytes, world, device):
+    """Whole-job numbers of `world` independent replicas: the slowest rank's ms per
+    step (max over ranks) and the GB/s of the bytes all ranks processed in it."""
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t)
+    return ms, nbytes * world / (ms * 1e-3) / 1e9
+
+
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
@@ -330,10 +341,7 @@ def main():
     with Clocks(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) as ck:
         ms, per_rep = time_graph(g, st, reps, 0, per_replay=True)
     torch.cuda.synchronize()
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t)
+    ms, job_gbs = aggregate_ranks(ms, S["bytes"], world, device)
     st_code = S["plan"].check(S["ws"])
     if st_code != 0:
         raise SystemExit(f"device status {st_code} after the timed region")
@@ -341,7 +349,7 @@ def main():
     hbm, peak_kind = peaks()
     gbs = S["bytes"] / (ms * 1e-3) / 1e9
     out = {
-        "metric": METRIC, "value": gbs * world, "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "metric": METRIC, "value": job_gbs, "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": warm * GRAPH_STEPS, "ms_per_step": ms, "us_per_step": ms * 1e3, "higher_is_better": True,
         # spread over the timed graph replays (each the mean of GRAPH_STEPS steps)
         "us_per_step_p10_p50_p90": [float(np.percentile(per_rep, q)) * 1e3 for q in (10, 50, 90)],
