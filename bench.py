@@ -334,11 +334,12 @@ def main():
     steps = reps * GRAPH_STEPS
     warm = max(args.warmup, 3)
     time_graph(g, st, 1, warm)  # warm-up replays (untimed)
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    out_dir = os.environ.get("MOE_BENCH_OUT", os.path.join(ROOT, "bench_out"))  # the clock samples
+    os.makedirs(out_dir, exist_ok=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with Clocks(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) as ck:
+    with Clocks(os.path.join(out_dir, f"clocks_rank{rank}.csv")) as ck:
         ms, per_rep = time_graph(g, st, reps, 0, per_replay=True)
     torch.cuda.synchronize()
     ms, job_gbs = aggregate_ranks(ms, S["bytes"], world, device)
