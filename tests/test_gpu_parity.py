@@ -204,13 +204,18 @@ def test_ragged_shapes(H, I):
     check_small(wl, make_topk_ids(wl))
 
 
-def test_empty_duplicate_and_bad_slots():
-    wl = Workload("slots", T=6, H=256, I=256, E=7, k=4, routing="uniform", seed=3)
+# the pairs of a launch are grouped by one warp (P <= 32), by the rank sort of
+# 32 < P <= 256 (tensor-core kernel) or by the counting sort above; T = 40 is a
+# prefill launch
+@pytest.mark.parametrize("T,k", [(6, 4), (12, 4), (24, 8), (40, 8)])
+def test_empty_duplicate_and_bad_slots(T, k):
+    wl = Workload("slots", T=T, H=256, I=256, E=11, k=k, routing="uniform", seed=3)
     ids = make_topk_ids(wl).clone()
     ids[0, 1] = -1            # empty slot
     ids[1, 2] = ids[1, 0]     # duplicate expert within a token
     ids[2, :] = -1            # token with no valid slot -> y == 0
     ids[3, 3] = wl.E + 2      # out of range: skipped and flagged
+    ids[T - 1, 0] = -5        # another empty slot, in the last token
     y, _ = check_small(wl, ids, expect_status=binding.MOE_ERR_BAD_EXPERT_ID)
     assert bool((y[2] == 0).all())
 
