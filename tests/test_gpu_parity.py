@@ -116,10 +116,12 @@ def test_tensor_kernel_bitwise_reproducible(name, cache):
 
 
 # T = 17, 20: gate/up MMA N = 80 (per-token x rows); T = 33: per-pair x rows in
-# one launch; E = 2: 24 pairs per expert, several groups of one expert
+# one launch; E = 2: 24 pairs per expert, several groups of one expert;
+# I = 4096: the largest I, 32 h slices per pair; H = 8192: two rounds of x loads
 @pytest.mark.parametrize("T,H,I,E,k", [(1, 512, 256, 6, 3), (5, 512, 512, 6, 3), (12, 768, 768, 9, 4),
                                        (24, 512, 256, 16, 8), (17, 512, 512, 8, 4), (20, 768, 256, 12, 6),
-                                       (33, 512, 256, 16, 8), (24, 512, 256, 2, 2)])
+                                       (33, 512, 256, 16, 8), (24, 512, 256, 2, 2), (12, 256, 4096, 4, 2),
+                                       (4, 8192, 256, 4, 4)])
 def test_tensor_kernel_small_shapes(T, H, I, E, k):
     wl = Workload("tc-small", T=T, H=H, I=I, E=E, k=k, routing="uniform", seed=11)
     ids = make_topk_ids(wl)
