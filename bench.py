@@ -193,37 +193,33 @@ def time_graph(g, st, reps, warm, per_replay=False):
 
 
 def time_e2e(S, steps):
-    """Per step through the public binding with host buffers: pinned host ->
-    device copies of x, ids, w; the step; the device -> host copy of y."""
-    from quantized_moe_routed_gb300 import binding
-    wl = S["wl"]
-    hx = S["x"].pin_memory()
-    hids = [r.cpu().pin_memory() for r in S["ids_rot"][:8]]
-    hw = S["w"].pin_memory()
-    hy = torch.empty((wl.T, wl.H), dtype=torch.float32).pin_memory()
-    dx, dids, dw = torch.empty_like(S["xd"]), torch.empty_like(S["ids_rot"][0]), torch.empty_like(S["wd"])
+    """Per step through the C ABI's host-buffer entry (moe_step_host, via
+    MoePlan.step_host): one copy of the step's packed x / ids / w block from
+    pinned host memory, then the step, whose kernels store y into pinned host
+    memory.  Eight blocks, each filled once with a different relabelling of the
+    ids, take turns, so no block is rewritten while a copy from it may be in
+    flight."""
+    from quantized_moe_routed_gb300 import HostIO
+    wl, plan = S["wl"], S["plan"]
+    ios = []
+    for r in S["ids_rot"][:8]:
+        io = HostIO(plan, wl.T, y_from=ios[0] if ios else None)
+        io.x.copy_(S["x"])
+        io.ids.copy_(r.cpu())
+        io.w.copy_(S["w"])
+        ios.append(io)
     st = torch.cuda.current_stream()
-    step = binding.moe_decode if wl.T <= 24 else binding.moe_prefill
     for i in range(3):
-        dx.copy_(hx, non_blocking=True)
-        step(S["plan"].handle, dx, dids.copy_(hids[i], non_blocking=True),
-             dw.copy_(hw, non_blocking=True), S["y"], S["ws"])
-        hy.copy_(S["y"], non_blocking=True)
+        plan.step_host(ios[i % len(ios)], S["ws"])
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(st)
     for i in range(steps):
-        dx.copy_(hx, non_blocking=True)
-        dids.copy_(hids[i % 8], non_blocking=True)
-        dw.copy_(hw, non_blocking=True)
-        step(S["plan"].handle, dx, dids, dw, S["y"], S["ws"])
-        hy.copy_(S["y"], non_blocking=True)
+        plan.step_host(ios[i % len(ios)], S["ws"])
     e1.record(st)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    h2d = hx.numel() * 2 + hids[0].numel() * 4 + hw.numel() * 4
-    d2h = hy.numel() * 4
-    return ms, h2d, d2h
+    return ms, ios[0].nbytes, ios[0].y.numel() * 4
 
 
 def cpu_baseline(S, seconds=10.0):
@@ -376,7 +372,9 @@ def main():
         out["null_dequant"] = {"us_per_step": ms_null * 1e3, "GB/s": S["bytes"] / (ms_null * 1e-3) / 1e9}
         ms_e2e, h2d, d2h = time_e2e(S, min(steps, 2000))
         out["e2e"] = {"value": S["bytes"] / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "us_per_step": ms_e2e * 1e3,
-                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "api": "moe_step_host, one call per step from Python: one host->device copy of the packed "
+                             "x/ids/w block, the step storing y into pinned host memory"}
         if not args.no_sweep and args.workload == "decode":
             sweep = {}
             for name in ("spec_verify", "upper_decode"):

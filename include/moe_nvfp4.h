@@ -20,7 +20,8 @@
  *  - Pointers named *_dev are CUDA device pointers on the plan's device; the
  *    caller owns them (allocates, frees, keeps them alive while work that
  *    uses them is in flight).  The library never frees caller memory and
- *    allocates no device memory.
+ *    allocates no device memory.  Pointers named *_host are host pointers,
+ *    also owned by the caller.
  *  - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
  *    stream.  Work is enqueued asynchronously; no entry point below
  *    synchronises except moe_check.
@@ -39,7 +40,7 @@
 extern "C" {
 #endif
 
-#define MOE_NVFP4_ABI_VERSION 2
+#define MOE_NVFP4_ABI_VERSION 3
 
 typedef enum {
     MOE_OK = 0,
@@ -178,6 +179,48 @@ moe_status_t moe_decode(moe_plan_t plan, const void *x_dev, const int32_t *ids_d
  * MOE_ERR_TIMEOUT, MOE_ERR_BAD_EXPERT_ID or MOE_ERR_RANGE, as moe_check). */
 moe_status_t moe_decode_static(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
                                float *y_dev, int T, int check, void *stream);
+
+/* Layout of the packed input block that moe_step_host copies in one piece,
+ * for T tokens: x (bf16 [T, H]) at offset 0, ids (int32 [T, top_k]) at
+ * *off_ids, w (float [T, top_k]) at *off_w, each piece starting on a 256-byte
+ * boundary.  Returns the block's size in bytes (a multiple of 256), or 0 for
+ * a null plan or T outside [1, T_max] (the offsets are then not written).
+ * off_ids and off_w may be null.  Host arithmetic only, no CUDA call.  The
+ * pages have no counterpart: their step is always called on device buffers. */
+size_t moe_io_bytes(moe_plan_t plan, int T, size_t *off_ids, size_t *off_w);
+
+/* The step from host buffers to a host buffer, in one call: one host->device
+ * copy of the packed input block, then the step (moe_decode for T <= 24,
+ * moe_prefill above), which writes y.  If y_host is page-locked memory that
+ * the device can address (cudaHostAlloc, or cudaHostRegister with mapping, on a
+ * system with unified addressing), the step's kernels store y into it
+ * directly and y_dev is not written.  Otherwise the step writes y_dev, and one
+ * device->host copy brings it to y_host.  Everything goes on `stream`, in
+ * that order.  There is no synchronisation: y_host holds the result once the
+ * stream has passed the step (cudaStreamSynchronize or an event).
+ *   io_host  host block of moe_io_bytes(plan, T) bytes, laid out as
+ *            moe_io_bytes states.  It should be pinned (cudaHostAlloc or
+ *            cudaHostRegister): the copies are then asynchronous.  From
+ *            pageable memory they still work, but the runtime stages them
+ *            and the call returns later.
+ *   io_dev   device block of the same size, 256-byte aligned; after the call,
+ *            it holds the copied x, ids and w
+ *   y_dev    device float [T, H], 16-byte aligned: the step's output when
+ *            y_host is not device-addressable
+ *   y_host   host float [T, H], receives y (pinned, like io_host)
+ *   T        0 <= T <= T_max (T == 0 is a no-op)
+ *   ws_dev   workspace, as for moe_decode
+ * Both paths are named paths, so strict mode refuses neither.  The arguments
+ * are checked before anything is queued.  A call rejected for its arguments
+ * copies nothing and returns the status moe_decode would return.  If the
+ * step cannot be launched once the input copy is queued (MOE_ERR_CUDA or
+ * MOE_ERR_UNSUPPORTED_SHAPE), that copy stands and y_host is not written.
+ * MOE_ERR_CUDA also means a copy could not be queued.  Device-side errors
+ * (timeouts, bad ids) go to the workspace error word, as for moe_decode.
+ * The caller owns every buffer.  io_host must not be rewritten, and y_host
+ * must not be read, before the stream has passed the step. */
+moe_status_t moe_step_host(moe_plan_t plan, const void *io_host, void *io_dev, float *y_dev, float *y_host,
+                           int T, void *ws_dev, void *stream);
 
 /* The same step for 1 <= T <= T_max (prefill chunks), same arguments.  Runs
  * the persistent ticket kernel over chunks of at most 4096 / top_k tokens. */

@@ -53,6 +53,8 @@ SIGNATURES = {
     "moe_group": (_I, [_P, _P, _I, _P, _P, _P, _P, _P]),
     "moe_decode": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
     "moe_decode_static": (_I, [_P, _P, _P, _P, _P, _I, _I, _P]),
+    "moe_io_bytes": (_S, [_P, _I, C.POINTER(C.c_size_t), C.POINTER(C.c_size_t)]),
+    "moe_step_host": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
     "moe_prefill": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
     "moe_null_step": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
     "moe_check": (_I, [_P, _P, _P]),
@@ -178,6 +180,44 @@ def moe_decode_static(plan, x, ids, w, y, check: bool = False, stream=None):
                                             _stream(stream)))
 
 
+def moe_io_bytes(plan, T: int):
+    """(size, off_ids, off_w) of the packed input block of moe_step_host for
+    T tokens: x at 0, ids at off_ids, w at off_w; size 0 for an invalid T."""
+    oi, ow = C.c_size_t(0), C.c_size_t(0)
+    n = load_library().moe_io_bytes(plan, T, C.byref(oi), C.byref(ow))
+    return int(n), int(oi.value), int(ow.value)
+
+
+def _need_host(t, dtype, nbytes, name):
+    if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise MoeError(MOE_ERR_INVALID_ARG, f"{name} must be a contiguous {dtype} host tensor")
+    if t.numel() * t.element_size() < nbytes:
+        raise MoeError(MOE_ERR_INVALID_ARG, f"{name} holds {t.numel() * t.element_size()} bytes, needs {nbytes}")
+
+
+def moe_step_host(plan, io_host, io_dev, y_dev, y_host, T: int, ws, stream=None):
+    """The step from a packed host block (x, ids, w at the offsets of
+    moe_io_bytes) to a host y: one copy in, then the step, which stores y
+    straight into y_host when that is pinned (else into y_dev, followed by one
+    copy out); all on `stream` and asynchronous.  io_host / y_host are host
+    tensors (pinned for asynchronous copies), io_dev / ws CUDA tensors, y_dev a
+    CUDA [>= T, H] tensor."""
+    n, _, _ = moe_io_bytes(plan, T) if T > 0 else (0, 0, 0)
+    _need_host(io_host, torch.uint8, n, "io_host")
+    _need(io_dev, torch.uint8, "io_dev")
+    _need(y_dev, torch.float32, "y_dev")
+    if io_dev.numel() < n:
+        raise MoeError(MOE_ERR_INVALID_ARG, f"io_dev holds {io_dev.numel()} bytes, needs {n}")
+    if y_dev.dim() != 2:
+        raise MoeError(MOE_ERR_INVALID_ARG, "y_dev must be [T, H]")
+    ny = T * y_dev.shape[1] * 4
+    if y_dev.numel() * 4 < ny:
+        raise MoeError(MOE_ERR_INVALID_ARG, f"y_dev holds {y_dev.numel() * 4} bytes, needs {ny}")
+    _need_host(y_host, torch.float32, ny, "y_host")
+    _check(load_library().moe_step_host(plan, _ptr(io_host), _ptr(io_dev), _ptr(y_dev), _ptr(y_host), T,
+                                          _ptr(ws), _stream(stream)))
+
+
 def moe_prefill(plan, x, ids, w, y, ws, stream=None):
     _step(load_library().moe_prefill, plan, x, ids, w, y, ws, stream)
 
@@ -248,6 +288,15 @@ class MoePlan:
             moe_prefill(self.handle, x, ids, w, y, ws, stream)
         return y
 
+    def step_host(self, io: "HostIO", ws, stream=None):
+        """moe_step_host on a HostIO block: copy io.x / io.ids / io.w in and
+        run the step, which stores y into the pinned io.y.  Asynchronous: io.y
+        is valid once the stream has been synchronised."""
+        lib = load_library()
+        _check(lib.moe_step_host(self.handle, io._host_p, io._dev_p, io._ydev_p, io._yhost_p, io.T, _ptr(ws),
+                                   _stream(stream)))
+        return io.y
+
     def group(self, ids, ws, stream=None):
         dev = ids.device
         counts = torch.empty(self.E, dtype=torch.int32, device=dev)
@@ -261,3 +310,35 @@ class MoePlan:
 
     def stats(self) -> dict:
         return moe_stats(self.handle)
+
+
+class HostIO:
+    """Pinned host staging for MoePlan.step_host.  `x` (bf16 [T, H]), `ids`
+    (int32 [T, top_k]) and `w` (float [T, top_k]) are views of one pinned block
+    that a step copies to the device in one piece; the step's kernels store the
+    result straight into `y` (float [T, H], pinned).  `y_dev` is the device
+    buffer the library falls back to if the device cannot address `y`.  Write the inputs in place; do not rewrite them while
+    an earlier step on this block may still be copying (use one block per step
+    in flight).  `y_from` shares another HostIO's y buffers."""
+
+    def __init__(self, plan: MoePlan, T: int, y_from: "HostIO" = None):
+        n, oi, ow = moe_io_bytes(plan.handle, T)
+        if n == 0:
+            raise MoeError(MOE_ERR_INVALID_ARG, f"T={T} outside [1, T_max={plan.T_max}]")
+        dev = plan.weights["gate_q"].device
+        H, k = plan.H, plan.top_k
+        self.T, self.nbytes = T, n
+        self.host = torch.zeros(n, dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.x = self.host[:T * H * 2].view(torch.bfloat16).view(T, H)
+        self.ids = self.host[oi:oi + T * k * 4].view(torch.int32).view(T, k)
+        self.w = self.host[ow:ow + T * k * 4].view(torch.float32).view(T, k)
+        if y_from is not None:
+            if y_from.T < T or y_from.y.shape[1] != H:
+                raise MoeError(MOE_ERR_INVALID_ARG, "y_from's y is smaller than this block's")
+            self.y, self.y_dev = y_from.y[:T], y_from.y_dev[:T]
+        else:
+            self.y = torch.zeros((T, H), dtype=torch.float32).pin_memory()
+            self.y_dev = torch.empty((T, H), dtype=torch.float32, device=dev)
+        self._host_p, self._dev_p = _ptr(self.host), _ptr(self.dev)
+        self._ydev_p, self._yhost_p = _ptr(self.y_dev), _ptr(self.y)

@@ -921,6 +921,74 @@ moe_status_t moe_decode_static(moe_plan_t plan, const void *x_dev, const int32_t
     return MOE_OK;
 }
 
+size_t moe_io_bytes(moe_plan_t plan, int T, size_t *off_ids, size_t *off_w)
+{
+    if (!plan || T < 1 || T > plan->d.T_max) return 0;
+    auto up256 = [](size_t n) { return (n + 255) / 256 * 256; };
+    const size_t x_bytes = static_cast<size_t>(T) * plan->d.H * 2;
+    const size_t sel_bytes = static_cast<size_t>(T) * plan->d.top_k * 4;
+    const size_t oi = up256(x_bytes), ow = oi + up256(sel_bytes);
+    if (off_ids) *off_ids = oi;
+    if (off_w) *off_w = ow;
+    return ow + up256(sel_bytes);
+}
+
+moe_status_t moe_step_host(moe_plan_t plan, const void *io_host, void *io_dev, float *y_dev, float *y_host,
+                           int T, void *ws_dev, void *stream)
+{
+    if (!plan) return fail(MOE_ERR_INVALID_ARG, "null plan");
+    if (T < 0 || T > plan->d.T_max) {
+        reject(plan);
+        return fail(MOE_ERR_INVALID_ARG, "T=%d outside [0, T_max=%d]", T, plan->d.T_max);
+    }
+    if (T == 0) return MOE_OK;
+    if (!io_host || !io_dev || !y_dev || !y_host || !ws_dev) {
+        reject(plan);
+        return fail(MOE_ERR_INVALID_ARG, "null io_host/io_dev/y_dev/y_host/workspace pointer");
+    }
+    if (!aligned(io_dev, 256) || !aligned(y_dev, 16) || !aligned(ws_dev, 256)) {
+        reject(plan);
+        return fail(MOE_ERR_MISALIGNED, "io_dev and the workspace need 256-byte, y_dev 16-byte alignment");
+    }
+    moe_status_t st = check_device(plan);
+    if (st != MOE_OK) {
+        reject(plan);
+        return st;
+    }
+    // y goes straight into y_host when the device can address it (page-locked
+    // and mapped; the kernels write y with plain stores and never read it back),
+    // else into y_dev and one copy brings it over
+    float *y_out = y_dev;
+    {
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, y_host) == cudaSuccess) {
+            if (a.type == cudaMemoryTypeHost && a.devicePointer && aligned(a.devicePointer, 16))
+                y_out = static_cast<float *>(a.devicePointer);
+        } else {
+            (void)cudaGetLastError();  // not an address CUDA knows: take the copy
+        }
+    }
+    size_t oi = 0, ow = 0;
+    const size_t in_bytes = moe_io_bytes(plan, T, &oi, &ow);
+    uint8_t *dev = static_cast<uint8_t *>(io_dev);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(io_dev, io_host, in_bytes, cudaMemcpyHostToDevice, cs);
+    if (e != cudaSuccess) {
+        reject(plan);
+        return fail(MOE_ERR_CUDA, "input copy: %s", cudaGetErrorString(e));
+    }
+    st = run_step(plan, dev, reinterpret_cast<const int32_t *>(dev + oi), reinterpret_cast<const float *>(dev + ow),
+                  y_out, T, ws_dev, stream, T <= moe::kDecodeMaxT ? Path::Decode : Path::Prefill);
+    if (st != MOE_OK || y_out != y_dev) return st;
+    e = cudaMemcpyAsync(y_host, y_dev, static_cast<size_t>(T) * plan->d.H * sizeof(float), cudaMemcpyDeviceToHost,
+                        cs);
+    if (e != cudaSuccess) {
+        reject(plan);
+        return fail(MOE_ERR_CUDA, "result copy: %s", cudaGetErrorString(e));
+    }
+    return MOE_OK;
+}
+
 moe_status_t moe_prefill(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
                          float *y_dev, int T, void *ws_dev, void *stream)
 {

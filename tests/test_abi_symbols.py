@@ -23,7 +23,7 @@ def test_library_exports_every_declared_symbol():
     for name in decl:
         assert hasattr(lib, name), name
     lib.moe_abi_version.restype = ctypes.c_int
-    assert lib.moe_abi_version() == 2
+    assert lib.moe_abi_version() == 3
     lib.moe_status_string.restype = ctypes.c_char_p
     assert lib.moe_status_string(6) == b"MOE_ERR_TIMEOUT"
 
@@ -47,3 +47,5 @@ def test_binding_loads_and_rejects_without_plan():
     assert lib.moe_check(None, None, None) == q.binding.MOE_ERR_INVALID_ARG
     assert "null" in q.moe_last_error()
     assert q.moe_workspace_bytes(None, 1) == 0
+    assert q.moe_io_bytes(None, 1) == (0, 0, 0)
+    assert lib.moe_step_host(None, None, None, None, None, 1, None, None) == q.binding.MOE_ERR_INVALID_ARG
