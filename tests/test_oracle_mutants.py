@@ -1,0 +1,124 @@
+"""The oracle's pins catch plausible mistakes in the oracle.
+
+Each case copies oracle/moe_oracle.c, plants one mistake (a wrong exponent
+bias, a swapped nibble, a dropped term, a wrong sign, index or stride, a
+transposed operand, an unstable sort), compiles the copy, points the oracle
+package at it and runs the pins of tests/test_oracle_pins.py until one fails.
+A mutant that passes every pin would be a mistake the pins cannot see.  The
+unmutated copy must pass them all.  Every planted index stays inside its array
+for the pins' shapes (I <= H, ids inside [0, E) where they index), so a mutant
+computes wrong numbers and never reads out of bounds.  CPU only.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(os.path.abspath(oracle.__file__)), "moe_oracle.c")
+
+# name -> (text in moe_oracle.c, replacement); each text occurs exactly once
+MUTANTS = {
+    "e2m1_exponent_bias": ("(int)e - 1)", "(int)e - 2)"),
+    "e2m1_subnormal": ("(e == 0) ? 0.5 * (double)m", "(e == 0) ? 1.0 * (double)m"),
+    "e2m1_sign_bit": ("s = (code >> 3) & 1u", "s = (code >> 2) & 1u"),
+    "e4m3_exponent_bias": ("(int)e - 7)", "(int)e - 6)"),
+    "e4m3_subnormal": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    "e4m3_nan_code": ("if (e == 15u && m == 7u)", "if (e == 15u && m == 6u)"),
+    "nibble_order": ("(c & 1) ? (byte >> 4) : (byte & 15u)", "(c & 1) ? (byte & 15u) : (byte >> 4)"),
+    "scale_block_of_32": ("(size_t)(c / 16)]", "(size_t)(c / 32)]"),
+    "scale_row_pitch": ("s[r * (size_t)(K / 16)", "s[r * (size_t)(K / 32)"),
+    "packed_row_pitch": ("q[r * (size_t)(K / 2)", "q[r * (size_t)(K / 4)"),
+    "tensor_scale_dropped": ("tab_e2m1[nib] * tab_e4m3[sc] * ts;", "tab_e2m1[nib] * tab_e4m3[sc] + 0.0 * ts;"),
+    "bf16_shift": ("(uint32_t)b << 16", "(uint32_t)b << 15"),
+    "gate_up_tensor_scales_swapped": ("double tg = (double)gate_ts[e], tu = (double)up_ts[e]",
+                                      "double tg = (double)up_ts[e], tu = (double)gate_ts[e]"),
+    "gate_reads_up_weights": ("sg += weight_at(gq, gs, tg,", "sg += weight_at(uq, us, tg,"),
+    "up_reads_gate_scales": ("su += weight_at(uq, us, tu,", "su += weight_at(uq, gs, tu,"),
+    "gate_sum_half_row": ("for (int c = 0; c < H; ++c) {\n            sg +=",
+                          "for (int c = 0; c < H / 2; ++c) {\n            sg +="),
+    "silu_sign": ("exp(-sg)", "exp(sg)"),
+    "silu_on_up": ("hbuf[i] = sg / (1.0 + exp(-sg)) * su;", "hbuf[i] = su / (1.0 + exp(-su)) * sg;"),
+    "sigmoid_not_silu": ("hbuf[i] = sg / (1.0 + exp(-sg)) * su;", "hbuf[i] = 1.0 / (1.0 + exp(-sg)) * su;"),
+    "down_rows_reversed": ("weight_at(dq, ds, td, I, (size_t)r, i)", "weight_at(dq, ds, td, I, (size_t)(H - 1 - r), i)"),
+    "down_sum_not_accumulated": ("acc += weight_at(dq, ds, td, I, (size_t)r, i) * hbuf[i];",
+                                 "acc = weight_at(dq, ds, td, I, (size_t)r, i) * hbuf[i];"),
+    "down_expert_stride": ("*dq = down_q + (size_t)e * H * (I / 2)", "*dq = down_q + (size_t)e * I * (I / 2)"),
+    "x_row_stride": ("x[(size_t)t * H + (size_t)c]", "x[(size_t)t * I + (size_t)c]"),
+    "ids_transposed": ("int e = ids[(size_t)t * k + (size_t)j];", "int e = ids[(size_t)j * T + (size_t)t];"),
+    "last_slot_dropped": ("for (int j = 0; j < k; ++j) {", "for (int j = 0; j < k - 1; ++j) {"),
+    "routing_weight_dropped": ("yt[r] += wj * o[r];", "yt[r] += o[r];"),
+    "routing_weight_of_slot0": ("w[(size_t)t * k + (size_t)j]", "w[(size_t)t * k]"),
+    "bad_id_not_counted": ("++bad;\n                continue;", "continue;"),
+    "group_unstable": ("for (int p = 0; p < P; ++p) {\n        int e = ids[p];\n        if (e >= 0 && e < E)",
+                       "for (int p = P - 1; p >= 0; --p) {\n        int e = ids[p];\n        if (e >= 0 && e < E)"),
+    "group_offsets_not_prefix_sum": ("offsets[e + 1] = offsets[e] + counts[e];", "offsets[e + 1] = counts[e];"),
+    "group_negative_ids_counted_bad": ("if (e >= E)\n            ++bad;\n        else if (e >= 0)",
+                                       "if (e >= E || e < 0)\n            ++bad;\n        else if (e >= 0)"),
+    "group_padding_not_minus_one": ("perm[p] = -1;", "perm[p] = 0;"),
+}
+
+
+def _pin_checks():
+    """The pins, cheapest first, as (name, callable) pairs."""
+    small = pins.make_small_case()
+    checks = [
+        ("e2m1_table", pins.test_e2m1_table_matches_spec),
+        ("e4m3_table", pins.test_e4m3_golden_and_library),
+        ("dequant_library_route", pins.test_dequant_matches_library_route),
+        ("quantizer_roundtrip", pins.test_quantizer_grid_roundtrip_exact),
+        ("quantizer_ties", pins.test_quantizer_e2m1_ties_to_even),
+        ("group_sorted_16x8", lambda: pins.test_group_against_sorted(16, 8, 256, 1)),
+        ("group_sorted_7x4", lambda: pins.test_group_against_sorted(7, 4, 5, 5)),
+        ("gate_up_fractions", pins.test_gate_up_exact_against_fractions),
+        ("silu_down_torch", pins.test_silu_mul_and_down_against_torch),
+        ("dense_mlp", pins.test_dense_mlp_special_case),
+        ("combine_torch", pins.test_combine_against_torch),
+    ]
+    for name in ("zero_weights_give_zero", "token_permutation_permutes_output", "power_of_two_scaling",
+                 "slot_linearity", "empty_and_bad_slots", "duplicate_slots_add", "token_subset_matches_full",
+                 "thread_count_does_not_change_result"):
+        fn = getattr(pins, "test_" + name)
+        checks.append((name, lambda fn=fn: fn(small)))
+    return checks
+
+
+def _build(src_text, out_dir, name):
+    src = os.path.join(out_dir, name + ".c")
+    lib = os.path.join(out_dir, "lib" + name + ".so")
+    with open(src, "w") as f:
+        f.write(src_text)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", lib, src, "-lm"],
+                   check=True, capture_output=True)
+    return lib
+
+
+def _first_failing_pin(lib, monkeypatch):
+    """Load `lib` as the oracle and return the name of the first pin that fails
+    (None if all pass)."""
+    monkeypatch.setattr(oracle, "build", lambda force=False: lib)
+    monkeypatch.setattr(oracle, "_lib", None)
+    for name, check in _pin_checks():
+        try:
+            check()
+        except (AssertionError, ValueError):
+            return name
+    return None
+
+
+def test_unmutated_copy_passes_every_pin(tmp_path, monkeypatch):
+    src = open(SRC).read()
+    lib = _build(src, str(tmp_path), "control")
+    assert _first_failing_pin(lib, monkeypatch) is None
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_mutant_fails_a_pin(mutant, tmp_path, monkeypatch):
+    old, new = MUTANTS[mutant]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"{mutant}: the text to mutate must occur exactly once"
+    lib = _build(src.replace(old, new), str(tmp_path), mutant)
+    killed_by = _first_failing_pin(lib, monkeypatch)
+    assert killed_by is not None, f"no pin catches the mutant {mutant}"

@@ -190,10 +190,14 @@ def test_combine_against_torch():
 
 
 # ------------------------------------------------------------------ invariants
-@pytest.fixture(scope="module")
-def small_case():
+def make_small_case():
     wl = Workload("t", T=5, H=128, I=64, E=8, k=3, routing="uniform", seed=21)
     return wl, make_inputs(wl, experts="all")
+
+
+@pytest.fixture(scope="module")
+def small_case():
+    return make_small_case()
 
 
 def test_zero_weights_give_zero(small_case):
