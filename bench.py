@@ -318,8 +318,9 @@ def main():
     if args.profile:
         from quantized_moe_routed_gb300 import binding
         n = len(S["ids_rot"])
+        fn = binding.moe_decode if S["wl"].T <= 24 else binding.moe_prefill
         for i in range(args.warmup + args.steps):
-            binding.moe_decode(S["plan"].handle, S["xd"], S["ids_rot"][i % n], S["wd"], S["y"], S["ws"])
+            fn(S["plan"].handle, S["xd"], S["ids_rot"][i % n], S["wd"], S["y"], S["ws"])
         torch.cuda.synchronize()
         st_code = S["plan"].check(S["ws"])
         print(json.dumps({"profile_run": True, "workload": S["wl"].name, "steps": args.steps,
