@@ -222,10 +222,25 @@ def time_e2e(S, steps):
     return ms, ios[0].nbytes, ios[0].y.numel() * 4
 
 
+def _time_oracle(S, Wc, threads, seconds, max_steps):
+    """Whole oracle steps on `threads` host threads, bounded to about `seconds`
+    (at least one step): (steps run, seconds per step)."""
+    import oracle
+    toks = list(range(S["wl"].T))
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.moe_forward(S["x"], S["ids"], S["w"], Wc, tokens=toks, n_threads=threads)
+        n += 1
+        if time.perf_counter() - t0 > seconds or n >= max_steps:
+            break
+    return n, (time.perf_counter() - t0) / n
+
+
 def cpu_baseline(S, seconds=10.0):
     """The oracle, as it is, on the host cores, over whole steps of the same
-    workload (bounded to about `seconds`)."""
-    import oracle
+    workload: on all cores (OpenMP over output rows; the reported value), then
+    on one thread, each bounded to about half of `seconds`."""
     from quantized_moe_routed_gb300.inputs import touched_experts
     wl = S["wl"]
     used = touched_experts(S["ids"], wl.E)
@@ -236,18 +251,13 @@ def cpu_baseline(S, seconds=10.0):
             c[e] = v[e].cpu()
         Wc[k] = c
     cores = os.cpu_count() or 1
-    toks = list(range(wl.T))
-    t0 = time.perf_counter()
-    n = 0
-    while True:
-        oracle.moe_forward(S["x"], S["ids"], S["w"], Wc, tokens=toks, n_threads=cores)
-        n += 1
-        if time.perf_counter() - t0 > seconds or n >= 20:
-            break
-    dt = (time.perf_counter() - t0) / n
+    n, dt = _time_oracle(S, Wc, cores, seconds / 2, 20)
+    n1, dt1 = _time_oracle(S, Wc, 1, seconds / 2, 20)
     return {"value": S["bytes"] / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} whole step(s) of the {wl.name} workload (T={wl.T}, all touched experts), "
-                      f"{dt * 1e3:.1f} ms per step, OpenMP over output rows"}
+                      f"{dt * 1e3:.1f} ms per step, OpenMP over output rows",
+            "single_thread": {"value": S["bytes"] / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"{n1} whole step(s), {dt1 * 1e3:.1f} ms per step"}}
 
 
 def run_reference(args):
