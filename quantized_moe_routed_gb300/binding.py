@@ -156,11 +156,22 @@ def moe_group(plan, ids, ws, counts, offsets, perm, stream=None):
                                     _ptr(perm), _stream(stream)))
 
 
+def _need_step_shapes(x, ids, w, y):
+    """x [T, H], ids and w [T, k], y [>= T, H]: the kernels read T*k ids and
+    weights and write T rows of y, so the tensors must agree."""
+    T = x.shape[0] if x.dim() == 2 else -1
+    if (T < 0 or ids.dim() != 2 or ids.shape[0] != T or tuple(w.shape) != tuple(ids.shape) or y.dim() != 2 or
+            y.shape[0] < T or y.shape[1] != x.shape[1]):
+        raise MoeError(MOE_ERR_INVALID_ARG, f"shapes x {tuple(x.shape)}, ids {tuple(ids.shape)}, w {tuple(w.shape)}, "
+                                            f"y {tuple(y.shape)} are not x [T, H], ids and w [T, k], y [T, H]")
+
+
 def _step(fn, plan, x, ids, w, y, ws, stream):
     _need(x, torch.bfloat16, "x")
     _need(ids, torch.int32, "ids")
     _need(w, torch.float32, "w")
     _need(y, torch.float32, "y")
+    _need_step_shapes(x, ids, w, y)
     _check(fn(plan, _ptr(x), _ptr(ids), _ptr(w), _ptr(y), x.shape[0], _ptr(ws), _stream(stream)))
 
 
@@ -176,6 +187,7 @@ def moe_decode_static(plan, x, ids, w, y, check: bool = False, stream=None):
     _need(ids, torch.int32, "ids")
     _need(w, torch.float32, "w")
     _need(y, torch.float32, "y")
+    _need_step_shapes(x, ids, w, y)
     _check(load_library().moe_decode_static(plan, _ptr(x), _ptr(ids), _ptr(w), _ptr(y), x.shape[0], int(check),
                                             _stream(stream)))
 
@@ -278,6 +290,9 @@ class MoePlan:
         return ws
 
     def step(self, x, ids, w, ws, y=None, stream=None, null: bool = False):
+        if x.dim() != 2 or x.shape[1] != self.H or ids.dim() != 2 or ids.shape[1] != self.top_k:
+            raise MoeError(MOE_ERR_INVALID_ARG, f"x {tuple(x.shape)} and ids {tuple(ids.shape)} are not "
+                                                f"[T, {self.H}] and [T, {self.top_k}]")
         if y is None:
             y = torch.empty((x.shape[0], self.H), dtype=torch.float32, device=x.device)
         if null:
@@ -298,6 +313,8 @@ class MoePlan:
         return io.y
 
     def group(self, ids, ws, stream=None):
+        if ids.dim() != 2 or ids.shape[1] != self.top_k:
+            raise MoeError(MOE_ERR_INVALID_ARG, f"ids {tuple(ids.shape)} is not [T, {self.top_k}]")
         dev = ids.device
         counts = torch.empty(self.E, dtype=torch.int32, device=dev)
         offsets = torch.empty(self.E + 1, dtype=torch.int32, device=dev)

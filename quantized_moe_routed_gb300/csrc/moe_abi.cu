@@ -13,6 +13,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <string>
 
 namespace {
@@ -717,7 +718,8 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
         return fail(MOE_ERR_UNSUPPORTED_SHAPE, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
                     major, minor);
 
-    moe_plan *pl = new moe_plan();
+    moe_plan *pl = new (std::nothrow) moe_plan();  // no exception may cross the C ABI
+    if (!pl) return fail(MOE_ERR_INVALID_ARG, "out of host memory for the plan");
     pl->d = d;
     pl->device = dev;
     pl->num_sms = sms;
@@ -836,11 +838,12 @@ moe_status_t moe_group(moe_plan_t plan, const int32_t *ids_dev, int T, void *ws_
                        int32_t *offsets_dev, int32_t *perm_dev, void *stream)
 {
     if (!plan) return fail(MOE_ERR_INVALID_ARG, "null plan");
-    const int P = T * plan->d.top_k;
-    if (T < 1 || P > moe::kMaxPairs) {
+    // range check before the product, which would overflow for huge T
+    if (T < 1 || T > moe::kMaxPairs / plan->d.top_k) {
         reject(plan);
         return fail(MOE_ERR_INVALID_ARG, "moe_group takes 1 <= T and T*top_k <= %d (T=%d)", moe::kMaxPairs, T);
     }
+    const int P = T * plan->d.top_k;
     if (!ids_dev || !counts_dev || !offsets_dev || !perm_dev || !ws_dev) {
         reject(plan);
         return fail(MOE_ERR_INVALID_ARG, "null pointer");

@@ -49,3 +49,21 @@ def test_binding_loads_and_rejects_without_plan():
     assert q.moe_workspace_bytes(None, 1) == 0
     assert q.moe_io_bytes(None, 1) == (0, 0, 0)
     assert lib.moe_step_host(None, None, None, None, None, 1, None, None) == q.binding.MOE_ERR_INVALID_ARG
+
+
+def test_step_shapes_must_agree():
+    # the binding refuses tensors that disagree about T, top_k or H before any call
+    import pytest
+    import torch
+    from quantized_moe_routed_gb300 import MoeError, binding
+    T, H, k = 3, 256, 4
+    x, ids, w, y = (torch.zeros((T, H)), torch.zeros((T, k)), torch.zeros((T, k)), torch.zeros((T, H)))
+    binding._need_step_shapes(x, ids, w, y)
+    binding._need_step_shapes(x, ids, w, torch.zeros((T + 2, H)))          # a taller y is fine
+    binding._need_step_shapes(torch.zeros((0, H)), torch.zeros((0, k)), torch.zeros((0, k)), torch.zeros((0, H)))
+    bad = [(x, ids[:1], w[:1], y), (x, ids, w[:, :2], y), (x, ids, w, y[:1]), (x, ids, w, torch.zeros((T, H + 1))),
+           (x.reshape(-1), ids, w, y), (x, ids.reshape(-1), w.reshape(-1), y)]
+    for args in bad:
+        with pytest.raises(MoeError) as ei:
+            binding._need_step_shapes(*args)
+        assert ei.value.status == binding.MOE_ERR_INVALID_ARG

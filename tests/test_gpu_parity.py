@@ -293,6 +293,21 @@ def test_invalid_arguments_rejected_on_host():
     with pytest.raises(MoeError) as ei:
         MoePlan(W, 200, wl.I, wl.E, wl.k, T_max=4)             # H not a multiple of 128
     assert ei.value.status == binding.MOE_ERR_UNSUPPORTED_SHAPE
+    # tensors that disagree about T or top_k are refused before the call
+    x_ok = torch.zeros((wl.T, wl.H), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(MoeError) as ei:
+        plan.step(x_ok, ids[:, :1].contiguous(), w[:, :1].contiguous(), ws)   # ids not [T, top_k]
+    assert ei.value.status == binding.MOE_ERR_INVALID_ARG
+    with pytest.raises(MoeError) as ei:
+        binding.moe_decode(plan.handle, x_ok, ids[:1].contiguous(), w[:1].contiguous(), y, ws)   # 1 row of ids
+    assert ei.value.status == binding.MOE_ERR_INVALID_ARG
+    # moe_group with T * top_k beyond int range: refused before any launch
+    i32 = dict(dtype=torch.int32, device=DEV)
+    lib = binding.load_library()
+    assert lib.moe_group(plan.handle, binding._ptr(ids), 1 << 30, binding._ptr(ws),
+                         binding._ptr(torch.zeros(wl.E, **i32)), binding._ptr(torch.zeros(wl.E + 1, **i32)),
+                         binding._ptr(torch.zeros(wl.T * wl.k, **i32)), None) == binding.MOE_ERR_INVALID_ARG
+    assert plan.check(ws) == 0
 
 
 # ------------------------------------------------------------------ grouping kernel, bit-exact
