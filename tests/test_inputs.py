@@ -25,19 +25,25 @@ def test_workload_shapes_and_determinism():
 
 
 def test_class_routing_hits_exact_classes():
+    """12 experts in each class R_e = 8, 4, 2, 1 (180 picks), then 12 filler
+    picks over the other experts: here each filler lands on its own expert."""
     wl = WORKLOADS["upper_decode"]
     ids = make_topk_ids(wl).numpy().reshape(-1)
     vals, cnt = np.unique(ids, return_counts=True)
     hist = {r: int((cnt == r).sum()) for r in set(cnt.tolist())}
-    assert hist[8] == 12 and hist[4] == 12 and hist[2] >= 12 and hist[1] >= 12 - 12
-    assert cnt.sum() == wl.T * wl.k
+    assert hist == {8: 12, 4: 12, 2: 12, 1: 24}
+    assert int(cnt[(cnt != 8) & (cnt != 4)].sum()) == 12 * 2 + 12 * 1 + 12
+    assert cnt.sum() == wl.T * wl.k and len(vals) == 60
 
 
 def test_zipf_routing_is_skewed():
+    """Zipf(1) ranks, drawn without replacement per token: the hottest expert
+    takes 13 of the 16 tokens (R_e up to 13, not 1-8), 62 experts touched."""
     wl = WORKLOADS["spec_verify"]
     ids = make_topk_ids(wl).numpy().reshape(-1)
     _, cnt = np.unique(ids, return_counts=True)
-    assert cnt.max() >= 8 and len(cnt) < wl.T * wl.k
+    assert int(cnt.max()) == 13 and len(cnt) == 62
+    assert int((cnt == 1).sum()) == 39     # a long tail of single-pair experts
 
 
 def test_quantizer_random_error_bound():
@@ -78,3 +84,28 @@ def test_algorithmic_bytes_decode():
     assert per_expert == 7_077_900
     assert algorithmic_bytes(wl, ids) == 8 * per_expert + 4096 * 2 + 8 * 8 + 4096 * 4
     assert touched_experts(torch.tensor([[3, -1, 9, 3]]), 8) == [3]
+
+
+def test_zipf_draws_follow_one_over_rank_without_replacement():
+    """Reading c12 (sequential draws without replacement, p(rank r) ~ 1/r,
+    rank -> expert through a seeded permutation): over many tokens the first
+    pick's rank frequency is p_r, and the (first, second) pair frequency is
+    p_r1 * p_r2 / (1 - p_r1), each within 5 binomial standard deviations."""
+    from quantized_moe_routed_gb300.inputs import _ids_zipf, _np_rng
+    E, n = 4, 40000
+    ids = _ids_zipf(_np_rng(5, 3), n, 2, E)
+    perm = _np_rng(5, 3).permutation(E)        # the first thing the draw takes from its stream
+    rank_of = np.empty(E, np.int64)
+    rank_of[perm] = np.arange(E)
+    r1, r2 = rank_of[ids[:, 0]], rank_of[ids[:, 1]]
+    assert np.all(r1 != r2)
+    p = 1.0 / np.arange(1, E + 1)
+    p /= p.sum()
+    f1 = np.bincount(r1, minlength=E) / n
+    assert np.all(np.abs(f1 - p) < 5 * np.sqrt(p * (1 - p) / n))
+    joint = np.zeros((E, E))
+    np.add.at(joint, (r1, r2), 1.0 / n)
+    for a in range(E):
+        for b in range(E):
+            q = 0.0 if a == b else p[a] * p[b] / (1 - p[a])
+            assert abs(joint[a, b] - q) <= 5 * np.sqrt(q * (1 - q) / n) + 1e-12, (a, b, joint[a, b], q)
