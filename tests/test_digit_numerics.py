@@ -116,3 +116,26 @@ def test_digit_codes_never_saturate_and_zero_stays_zero():
 def test_e2m1_ties_go_to_the_even_code():
     v = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -5.0, 7.0])
     assert e2m1_rne(v).tolist() == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, -0.0, -4.0, 6.0]
+
+
+def test_blocks_far_below_the_row_max_lose_relative_not_absolute_precision():
+    """Blocks far below the row's largest magnitude reach subnormal E4M3
+    scales (the prescale is shared by the row).  Relative to their own block
+    their error grows past the bound (a block 2^26 down is mostly lost), but
+    every element's error stays below 2^-24 of the row's largest magnitude, so
+    such blocks carry no weight in a dot product."""
+    rng = np.random.default_rng(11)
+    row = rng.standard_normal(4096)
+    shifts = [14, 17, 20, 26, 40]
+    for k, sh in enumerate(shifts):
+        row[16 * (k + 1):16 * (k + 2)] = rng.standard_normal(16) * 2.0 ** -sh
+    e, ds = digits(row)
+    err = np.abs(sum(ds) * 2.0 ** -e - row)
+    rmax = np.abs(row).max()
+    bound = (9.0 / 8.0 / 6.0) ** 4
+    assert err.max() <= bound * rmax
+    for k in range(len(shifts)):
+        b = slice(16 * (k + 1), 16 * (k + 2))
+        assert err[b].max() <= 2.0 ** -24 * rmax
+    far = slice(16 * 4, 16 * 5)                 # the block 2^26 below
+    assert err[far].max() > bound * np.abs(row[far]).max()
