@@ -144,7 +144,8 @@ moe_status_t moe_group(moe_plan_t plan, const int32_t *ids_dev, int T, void *ws_
 
 /* The routed-experts step for 0 <= T <= 24 tokens (decode; T == 0 is a no-op).
  *   x_dev    bf16 [T, H] row-major, 16-byte aligned; values must fit fp16
- *            (|x| <= 65504) because the tensor-core operands are fp16
+ *            (|x| <= 65504) because the register kernel's mma.sync operands
+ *            are fp16 (the tensor-core kernel prescales each row itself)
  *   ids_dev  int32 [T, top_k]: id < 0 = empty slot, id >= E = skipped + flagged
  *   w_dev    float [T, top_k] routing weights, used as given
  *   y_dev    float [T, H] row-major, 16-byte aligned; fully written
@@ -222,8 +223,10 @@ size_t moe_io_bytes(moe_plan_t plan, int T, size_t *off_ids, size_t *off_w);
 moe_status_t moe_step_host(moe_plan_t plan, const void *io_host, void *io_dev, float *y_dev, float *y_host,
                            int T, void *ws_dev, void *stream);
 
-/* The same step for 1 <= T <= T_max (prefill chunks), same arguments.  Runs
- * the persistent ticket kernel over chunks of at most 4096 / top_k tokens. */
+/* The same step for 1 <= T <= T_max (prefill chunks), same arguments.  One
+ * launch of the kernel the plan chooses per chunk of at most 4096 / top_k
+ * tokens (the tensor-core kernel when the shape allows it and a chunk has
+ * more than 8 pairs, else the register kernel). */
 moe_status_t moe_prefill(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
                          float *y_dev, int T, void *ws_dev, void *stream);
 
