@@ -1,7 +1,8 @@
 """GPU parity of the sm_103a routed-MoE step against the CPU oracle, through
-the C ABI.  Tolerance: max|y - y_ref| / max|y_ref| <= 2e-3 (fp32 output,
-fp16 tensor-core operands, fp32 accumulation); grouping bit-exact; repeated
-runs bitwise identical."""
+the C ABI.  Tolerance: max|y - y_ref| / max|y_ref| <= 2e-3 (fp32 output; fp16
+mma.sync operands on the register kernel, four FP4 digit rows per activation
+row on the tensor-core kernel; fp32 accumulation); grouping bit-exact;
+repeated runs bitwise identical."""
 import os
 
 import numpy as np
