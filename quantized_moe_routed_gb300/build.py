@@ -1,7 +1,9 @@
 """Build the sm_103a C-ABI library libmoe_nvfp4.so in-tree (nvcc, no cmake).
 
 The three translation units compile in parallel, then link into
-quantized_moe_routed_gb300/_build/libmoe_nvfp4.so (static cudart).
+quantized_moe_routed_gb300/_build/libmoe_nvfp4.so (static cudart).  The
+compiler's output for each unit (the kernels' ptxas register and spill report)
+is kept beside the objects as <unit>.log.
 """
 from __future__ import annotations
 
@@ -53,6 +55,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     failed = []
     for src, pr in procs:
         out, _ = pr.communicate()
+        with open(os.path.join(BUILD, src + ".log"), "w") as f:
+            f.write(out)
         if verbose or pr.returncode:
             sys.stderr.write(out)
         if pr.returncode:
