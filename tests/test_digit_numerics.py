@@ -8,7 +8,9 @@ E4M3 scale rounded up and E2M1 round-to-nearest-even.  This module writes that
 decomposition out from its definition (numpy, float64, no code shared with the
 kernel) and pins the error bound the design relies on: after four digits every
 element is within (9/8 / 6)^4 of its block's largest magnitude, i.e. about
-1.24e-3, well inside the step's 2e-3 tolerance on max |y|.
+1.24e-3, well inside the step's 2e-3 tolerance on max |y|.  It also restates
+how h's per-slice digits are moved to one reference exponent per pair, and
+bounds what that move costs.
 """
 import numpy as np
 import pytest
@@ -139,3 +141,64 @@ def test_blocks_far_below_the_row_max_lose_relative_not_absolute_precision():
         assert err[b].max() <= 2.0 ** -24 * rmax
     far = slice(16 * 4, 16 * 5)                 # the block 2^26 below
     assert err[far].max() > bound * np.abs(row[far]).max()
+
+
+def e4m3_rne(a):
+    """Nearest E4M3 value to a >= 0 (ties to the even code), saturating at 448."""
+    i = np.clip(np.searchsorted(E4M3, a), 1, len(E4M3) - 1)
+    lo, hi = E4M3[i - 1], E4M3[i]
+    up = (a - lo > hi - a) | ((a - lo == hi - a) & (i % 2 == 0))
+    return np.where(a >= 448.0, 448.0, np.where(up, hi, lo))
+
+
+def slice_digits(sl):
+    """Prescale exponent, E2M1 values [16-blocks, 16] and E4M3 scales [16-blocks]
+    of the four digit rows of one slice, from the decomposition's definition."""
+    e = prescale_exponent(np.max(np.abs(sl)))
+    r = sl * 2.0 ** e
+    vals, scales = [], []
+    for j in range(4):
+        f = 4.0 ** j
+        b = (r * f).reshape(-1, 16)
+        s = e4m3_ceil(np.max(np.abs(b), axis=1) / 6.0)
+        v = np.where(s[:, None] > 0, e2m1_rne(np.divide(b, s[:, None], out=np.zeros_like(b), where=s[:, None] > 0)), 0.0)
+        vals.append(v)
+        scales.append(s)
+        r = r - (v * s[:, None]).reshape(-1) / f
+    return e, vals, scales
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_h_slices_rebased_to_the_pair_reference(seed):
+    """Reading r19: each 128-row slice of a pair's h is decomposed with its own
+    prescale, then every digit's block scales are moved to the pair's reference
+    exponent (its largest slice) by an E4M3 round-to-nearest-even of
+    scale x 2^-d.  The move is exact while a scale stays normal; below that a
+    scale changes by at most half a subnormal step (2^-10), so with E2M1 values
+    <= 6 and digit weights 4^-j the element error grows by at most
+    6 * 2^-10 * 85/64 in reference units, under 2^-17 of the pair's largest |h|
+    (which sits above 1344 there)."""
+    rng = np.random.default_rng(100 + seed)
+    I = 1024
+    h = rng.standard_normal(I) * np.exp(rng.uniform(-3, 3))
+    h *= np.where(rng.random(I) < 0.02, 30.0, 1.0)
+    shifts = rng.integers(0, 30, I // 128)
+    shifts[rng.integers(I // 128)] = 0
+    for i in range(I // 128):
+        h[128 * i:128 * (i + 1)] *= 2.0 ** -float(shifts[i])
+    per = [slice_digits(h[128 * i:128 * (i + 1)]) for i in range(I // 128)]
+    eref = min(p[0] for p in per)
+    rec = np.zeros(I)
+    for i, (e, vals, scales) in enumerate(per):
+        d = e - eref
+        out = np.zeros(128)
+        for j in range(4):
+            moved = e4m3_rne(scales[j] * 2.0 ** -d)
+            if np.all((scales[j] == 0) | (scales[j] * 2.0 ** -d >= 2.0 ** -6)):
+                assert np.array_equal(moved, scales[j] * 2.0 ** -d)     # normal: an exact shift
+            out += (vals[j] * moved[:, None]).reshape(-1) / 4.0 ** j
+        rec[128 * i:128 * (i + 1)] = out * 2.0 ** -eref
+    err = np.abs(rec - h)
+    blk = np.abs(h).reshape(-1, 16).max(axis=1).repeat(16)
+    bound = (9.0 / 8.0 / 6.0) ** 4
+    assert np.all(err <= bound * blk + 2.0 ** -17 * np.abs(h).max())
