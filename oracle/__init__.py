@@ -12,6 +12,7 @@ Functions:
   expert_pair(...)                 -- g, u, h, o for one (token, expert) pair
   moe_forward(...)                 -- y (float64) for all or selected tokens
   group(ids, E)                    -- counts, offsets, perm (stable) + bad count
+  route(logits, k)                 -- top-k ids and softmax weights per token
 """
 from __future__ import annotations
 
@@ -61,6 +62,8 @@ def _load():
             lib.oracle_moe_forward.restype = C.c_int
             lib.oracle_group.argtypes = [P, i, i, P, P, P]
             lib.oracle_group.restype = C.c_int
+            lib.oracle_route.argtypes = [P, i, i, i, P, P]
+            lib.oracle_route.restype = C.c_int
             _lib = lib
     return _lib
 
@@ -172,3 +175,15 @@ def group(ids, E: int):
     perm = np.empty(max(P, 1), np.int32)
     bad = _load().oracle_group(_p(idsa), P, E, _p(counts), _p(offsets), _p(perm))
     return counts, offsets, perm[:P], bad
+
+
+def route(logits, k: int):
+    """Top-k experts per token by logit (ties: smaller index; NaN as -inf) and
+    the softmax of the selected logits: (ids int32 [T, k], w float32 [T, k])."""
+    lg = _np(logits, np.float32)
+    T, E = lg.shape
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float32)
+    if _load().oracle_route(_p(lg), T, E, int(k), _p(ids), _p(w)) != 0:
+        raise ValueError("oracle_route rejected its arguments")
+    return ids, w

@@ -34,6 +34,11 @@
  * p = t*k + j of valid pairs sorted by (expert, p) -- a stable counting sort,
  * the unique answer.
  *
+ * Routing (the step in front of the path, which the pages do not describe):
+ * per token the k largest router logits in descending order, equal logits by
+ * the smaller expert index, NaN as -infinity, and the softmax of the selected
+ * logits in double -- the plain definition of top-k gating.
+ *
  * Parallelism: optional OpenMP over independent output rows only; every
  * individual sum keeps its sequential order, so the result does not depend on
  * the thread count.
@@ -253,4 +258,51 @@ int oracle_group(const int32_t *ids, int P, int E, int32_t *counts, int32_t *off
     }
     free(cursor);
     return bad;
+}
+
+/* ---------------------------------------------------------------- routing */
+
+/* Top-k routing in front of the step: for each token t, the k experts with the
+ * largest router logits, in descending order of logit (equal logits: the
+ * smaller expert index first; NaN counts as -infinity), and their weights, the
+ * softmax over those k logits (in double, then rounded to float).  If the
+ * largest selected logit is -infinity the weights are 0.  This is the router
+ * output the input recipe draws at random (k logits, softmax over them); the
+ * pages do not describe the router, so it is the plain definition.
+ * logits float [T, E]; ids int32 [T, k]; w float [T, k].  Returns -1 on a
+ * bad argument (k < 1, k > E, T < 0), else 0. */
+int oracle_route(const float *logits, int T, int E, int k, int32_t *ids, float *w)
+{
+    if (T < 0 || E < 1 || k < 1 || k > E)
+        return -1;
+    char *taken = (char *)malloc((size_t)E);
+    double *sel = (double *)malloc(sizeof(double) * (size_t)k);
+    for (int t = 0; t < T; ++t) {
+        const float *lt = logits + (size_t)t * E;
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            double bv = 0.0;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e])
+                    continue;
+                double v = isnan(lt[e]) ? -INFINITY : (double)lt[e];
+                if (best < 0 || v > bv) {   /* strict: an equal logit keeps the smaller index */
+                    best = e;
+                    bv = v;
+                }
+            }
+            taken[best] = 1;
+            ids[(size_t)t * k + j] = best;
+            sel[j] = bv;
+        }
+        double m = sel[0], sum = 0.0;
+        for (int j = 0; j < k; ++j)
+            sum += (m == -INFINITY) ? 0.0 : exp(sel[j] - m);
+        for (int j = 0; j < k; ++j)
+            w[(size_t)t * k + j] = (m == -INFINITY) ? 0.0f : (float)(exp(sel[j] - m) / sum);
+    }
+    free(taken);
+    free(sel);
+    return 0;
 }

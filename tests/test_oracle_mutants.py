@@ -2,8 +2,9 @@
 
 Each case copies oracle/moe_oracle.c, plants one mistake (a wrong exponent
 bias, a swapped nibble, a dropped term, a wrong sign, index or stride, a
-transposed operand, an unstable sort), compiles the copy, points the oracle
-package at it and runs the pins of tests/test_oracle_pins.py until one fails.
+transposed operand, an unstable sort, a wrong tie or NaN rule in the routing),
+compiles the copy, points the oracle package at it and runs the pins of
+tests/test_oracle_pins.py until one fails.
 A mutant that passes every pin would be a mistake the pins cannot see.  The
 unmutated copy must pass them all.  Every planted index stays inside its array
 for the pins' shapes (I <= H, ids inside [0, E) where they index), so a mutant
@@ -48,7 +49,8 @@ MUTANTS = {
     "down_expert_stride": ("*dq = down_q + (size_t)e * H * (I / 2)", "*dq = down_q + (size_t)e * I * (I / 2)"),
     "x_row_stride": ("x[(size_t)t * H + (size_t)c]", "x[(size_t)t * I + (size_t)c]"),
     "ids_transposed": ("int e = ids[(size_t)t * k + (size_t)j];", "int e = ids[(size_t)j * T + (size_t)t];"),
-    "last_slot_dropped": ("for (int j = 0; j < k; ++j) {", "for (int j = 0; j < k - 1; ++j) {"),
+    "last_slot_dropped": ("for (int j = 0; j < k; ++j) {\n            int e = ids[",
+                          "for (int j = 0; j < k - 1; ++j) {\n            int e = ids["),
     "routing_weight_dropped": ("yt[r] += wj * o[r];", "yt[r] += o[r];"),
     "routing_weight_of_slot0": ("w[(size_t)t * k + (size_t)j]", "w[(size_t)t * k]"),
     "bad_id_not_counted": ("++bad;\n                continue;", "continue;"),
@@ -58,6 +60,12 @@ MUTANTS = {
     "group_negative_ids_counted_bad": ("if (e >= E)\n            ++bad;\n        else if (e >= 0)",
                                        "if (e >= E || e < 0)\n            ++bad;\n        else if (e >= 0)"),
     "group_padding_not_minus_one": ("perm[p] = -1;", "perm[p] = 0;"),
+    "route_ties_to_larger_index": ("if (best < 0 || v > bv) {", "if (best < 0 || v >= bv) {"),
+    "route_nan_compared_as_a_value": ("double v = isnan(lt[e]) ? -INFINITY : (double)lt[e];", "double v = (double)lt[e];"),
+    "route_sum_without_max_shift": ("sum += (m == -INFINITY) ? 0.0 : exp(sel[j] - m);",
+                                    "sum += (m == -INFINITY) ? 0.0 : exp(sel[j]);"),
+    "route_weights_not_normalised": ("(float)(exp(sel[j] - m) / sum)", "(float)(exp(sel[j] - m))"),
+    "route_ids_of_token_0": ("const float *lt = logits + (size_t)t * E;", "const float *lt = logits;"),
 }
 
 
@@ -76,6 +84,9 @@ def _pin_checks():
         ("silu_down_torch", pins.test_silu_mul_and_down_against_torch),
         ("dense_mlp", pins.test_dense_mlp_special_case),
         ("combine_torch", pins.test_combine_against_torch),
+        ("route_brute_force", lambda: pins.test_route_against_brute_force(16, 256, 8, 1)),
+        ("route_ties_nan_extremes", pins.test_route_ties_nan_and_extremes),
+        ("route_invariants", pins.test_route_invariants),
     ]
     for name in ("zero_weights_give_zero", "token_permutation_permutes_output", "power_of_two_scaling",
                  "slot_linearity", "empty_and_bad_slots", "duplicate_slots_add", "token_subset_matches_full",

@@ -296,3 +296,52 @@ def test_group_against_sorted(T, k, E, seed):
     for e in range(E):
         assert counts[e] == sum(1 for v in flat if v == e)
     assert offsets[0] == 0 and list(np.diff(offsets)) == list(counts)
+
+
+# ------------------------------------------------------------------ routing (top-k + softmax in front of the step)
+def _route_brute(logits, k):
+    """numpy: stable sort by descending logit (NaN as -inf), softmax in float64."""
+    lg = np.where(np.isnan(logits), -np.inf, logits.astype(np.float64))
+    order = np.argsort(-lg, axis=1, kind="stable")[:, :k]
+    sel = np.take_along_axis(lg, order, axis=1)
+    z = np.exp(sel - sel[:, :1])
+    return order.astype(np.int32), (z / z.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
+@pytest.mark.parametrize("T,E,k,seed", [(1, 256, 8, 0), (16, 256, 8, 1), (5, 7, 7, 2), (3, 1024, 16, 3), (0, 8, 2, 4)])
+def test_route_against_brute_force(T, E, k, seed):
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    ids, w = oracle.route(logits, k)
+    ref_ids, ref_w = _route_brute(logits, k)
+    assert np.array_equal(ids, ref_ids)
+    assert np.allclose(w, ref_w, rtol=2.5e-7, atol=0)
+
+
+def test_route_ties_nan_and_extremes():
+    lg = np.array([[0.5, 2.0, 2.0, -1.0, np.nan, 3.0],
+                   [1.0, 1.0, 1.0, 1.0, 1.0, 1.0],
+                   [1000.0, 999.0, -1000.0, 998.0, 0.0, 0.0],
+                   [-np.inf] * 6,
+                   [np.nan, -5.0, 0.25, np.nan, 0.5, -5.0]], np.float32)
+    ids, w = oracle.route(lg, 3)
+    assert ids.tolist() == [[5, 1, 2], [0, 1, 2], [0, 1, 3], [0, 1, 2], [4, 2, 1]]
+    assert np.allclose(w[1], 1 / 3, rtol=1e-7)                     # equal logits, equal weights
+    e = np.exp([0.0, -1.0, -2.0])
+    assert np.allclose(w[2], e / e.sum(), rtol=2.5e-7)             # large logits: no overflow
+    assert np.all(w[3] == 0.0)                                       # nothing finite to weigh
+    assert np.allclose(w[:3].astype(np.float64).sum(axis=1), 1.0, atol=1e-6)
+
+
+def test_route_invariants():
+    rng = np.random.default_rng(9)
+    lg = rng.standard_normal((6, 64)).astype(np.float32)
+    ids, w = oracle.route(lg, 8)
+    ids2, w2 = oracle.route(lg + np.float32(4.0), 8)                # softmax is shift-invariant
+    assert np.array_equal(ids, ids2) and np.allclose(w, w2, rtol=1e-6)
+    perm = rng.permutation(64)                                       # relabelling experts relabels ids
+    ids3, w3 = oracle.route(lg[:, perm], 8)
+    assert np.array_equal(perm[ids3], ids) and np.array_equal(w3, w)
+    full, wf = oracle.route(lg, 64)                                  # k = E: the whole descending order
+    assert np.array_equal(full, np.argsort(-lg, axis=1, kind="stable"))
+    assert np.all(np.diff(wf, axis=1) <= 0)
