@@ -237,6 +237,45 @@ def _time_oracle(S, Wc, threads, seconds, max_steps):
     return n, (time.perf_counter() - t0) / n
 
 
+def time_routed(S, reps):
+    """The step with top-k routing in front (moe_route, then the step, on one
+    stream, in a CUDA graph of GRAPH_STEPS steps): ms per routed step and ms
+    per routing launch alone.  Each step's logits are the seeded logits rolled
+    along the expert axis by step*delta, so the routing picks the same number
+    of experts and consecutive steps touch disjoint ones (cold reads)."""
+    from quantized_moe_routed_gb300 import binding
+    from quantized_moe_routed_gb300.inputs import make_router_logits, rotation_delta
+    wl, plan, dev = S["wl"], S["plan"], S["xd"].device
+    base = make_router_logits(wl)
+    delta = rotation_delta(torch.topk(base, wl.k, dim=1).indices.to(torch.int32), wl.E, window=8)
+    lgs = [torch.roll(base, shifts=s * delta, dims=1).contiguous().to(dev) for s in range(GRAPH_STEPS)]
+    ids = torch.empty((wl.T, wl.k), dtype=torch.int32, device=dev)
+    w = torch.empty((wl.T, wl.k), dtype=torch.float32, device=dev)
+    step = binding.moe_decode if wl.T <= 24 else binding.moe_prefill
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        for i in range(3):
+            binding.moe_route(plan.handle, lgs[i], ids, w, st)
+            step(plan.handle, S["xd"], ids, w, S["y"], S["ws"], st)
+    st.synchronize()
+    graphs = []
+    for with_step in (True, False):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            for i in range(GRAPH_STEPS):
+                binding.moe_route(plan.handle, lgs[i], ids, w, st)
+                if with_step:
+                    step(plan.handle, S["xd"], ids, w, S["y"], S["ws"], st)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    ms = time_graph(graphs[0], st, reps, 3)
+    ms_route = time_graph(graphs[1], st, reps, 3)
+    if plan.check(S["ws"]) != 0:
+        raise RuntimeError("device status after the routed steps")
+    return ms, ms_route, wl.T * wl.E * 4
+
+
 def cpu_baseline(S, seconds=10.0):
     """The oracle, as it is, on the host cores, over whole steps of the same
     workload: on all cores (OpenMP over output rows; the reported value), then
@@ -403,6 +442,18 @@ def main():
             S = setup(args.workload, device)
         if not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline(S)
+        # routing in front of the step, the last GPU work: every other key of
+        # the line is complete whatever happens here
+        try:
+            ms_r, ms_route, lbytes = time_routed(S, max(1, 2000 // GRAPH_STEPS))
+            rb = S["bytes"] + lbytes
+            out["routed_step"] = {"us_per_step": ms_r * 1e3, "GB/s": rb / (ms_r * 1e-3) / 1e9,
+                                  "frac": rb / (ms_r * 1e-3) / 1e9 / hbm, "route_us": ms_route * 1e3,
+                                  "algorithmic_bytes_per_step": rb,
+                                  "form": "moe_route (logits [T, E] -> ids, w) then the step, one stream, "
+                                          f"CUDA graph of {GRAPH_STEPS} steps; route_us: the routing launch alone"}
+        except Exception as exc:  # noqa: BLE001 -- reported, never fatal to the line
+            out["routed_step"] = {"unavailable": str(exc).splitlines()[0][:200] if str(exc) else type(exc).__name__}
         print(json.dumps(out))
     if world > 1:
         dist.barrier()

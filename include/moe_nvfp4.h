@@ -102,6 +102,7 @@ typedef struct {
     uint64_t group_launches;   /* stand-alone grouping kernel                   */
     uint64_t rejected_calls;   /* calls that returned an error status           */
     uint64_t tensor_launches;  /* of decode + prefill: tensor-core kernel       */
+    uint64_t route_launches;   /* top-k routing kernel (moe_route)              */
     int num_sms;               /* SMs on the plan's device (grid size)          */
     int stages;                /* shared-memory ring stages at the largest T    */
     int smem_bytes;            /* dynamic shared memory per CTA at the largest T */
@@ -236,6 +237,25 @@ moe_status_t moe_prefill(moe_plan_t plan, const void *x_dev, const int32_t *ids_
  * "null-decode" variant, "LNA-CANON.md", section "lna2 とは"). */
 moe_status_t moe_null_step(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
                            float *y_dev, int T, void *ws_dev, void *stream);
+
+/* Top-k routing in front of the step.  The pages do not describe the router;
+ * this is the plain definition of top-k gating.  For each of the T tokens,
+ * ids_dev receives the top_k experts with the largest router logits, in
+ * descending order of logit.  Equal logits put the smaller expert index first,
+ * and NaN counts as -infinity.  w_dev receives the softmax of those top_k
+ * logits (fp32, expf); when the largest selected logit is -infinity the
+ * weights are 0.  These are the ids_dev / w_dev that a following moe_decode
+ * or moe_prefill on the same stream takes, so routing needs no trip through
+ * the host.
+ *   logits_dev  float [T, E] row-major, 4-byte aligned
+ *   ids_dev     int32 [T, top_k]; w_dev float [T, top_k]; 4-byte aligned
+ *   T           0 <= T <= T_max (T == 0 is a no-op)
+ * top_k > E is refused with MOE_ERR_UNSUPPORTED_SHAPE.  One launch, one warp
+ * per token, asynchronous on `stream`.  With the plan's pdl flag it may start
+ * while the previous kernel on the stream drains; it waits for that kernel
+ * before it reads or writes anything.  Bitwise reproducible. */
+moe_status_t moe_route(moe_plan_t plan, const float *logits_dev, int T, int32_t *ids_dev, float *w_dev,
+                       void *stream);
 
 /* Synchronise `stream`, read and clear the workspace's device error word.
  * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_BAD_EXPERT_ID or MOE_ERR_RANGE

@@ -41,7 +41,7 @@ MOE_KERNEL_AUTO, MOE_KERNEL_REGISTER, MOE_KERNEL_TENSOR = 0, 1, 2
 class moe_stats_t(C.Structure):
     _fields_ = [("decode_launches", C.c_uint64), ("prefill_launches", C.c_uint64), ("null_launches", C.c_uint64),
                 ("group_launches", C.c_uint64), ("rejected_calls", C.c_uint64),
-                ("tensor_launches", C.c_uint64), ("num_sms", C.c_int),
+                ("tensor_launches", C.c_uint64), ("route_launches", C.c_uint64), ("num_sms", C.c_int),
                 ("stages", C.c_int), ("smem_bytes", C.c_int)]
 
 
@@ -57,6 +57,7 @@ SIGNATURES = {
     "moe_step_host": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
     "moe_prefill": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
     "moe_null_step": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
+    "moe_route": (_I, [_P, _P, _I, _P, _P, _P]),
     "moe_check": (_I, [_P, _P, _P]),
     "moe_debug_poison_workspace": (_I, [_P, _P, _P]),
     "moe_stats": (_I, [_P, C.POINTER(moe_stats_t)]),
@@ -238,6 +239,19 @@ def moe_null_step(plan, x, ids, w, y, ws, stream=None):
     _step(load_library().moe_null_step, plan, x, ids, w, y, ws, stream)
 
 
+def moe_route(plan, logits, ids, w, stream=None):
+    """Top-k routing: logits float [T, E] -> ids int32 [T, top_k] and softmax
+    weights float [T, top_k] on the device (the ids / w a step then takes)."""
+    _need(logits, torch.float32, "logits")
+    _need(ids, torch.int32, "ids")
+    _need(w, torch.float32, "w")
+    T = logits.shape[0] if logits.dim() == 2 else -1
+    if T < 0 or ids.dim() != 2 or ids.shape[0] != T or tuple(w.shape) != tuple(ids.shape):
+        raise MoeError(MOE_ERR_INVALID_ARG, f"shapes logits {tuple(logits.shape)}, ids {tuple(ids.shape)}, "
+                                            f"w {tuple(w.shape)} are not logits [T, E], ids and w [T, k]")
+    _check(load_library().moe_route(plan, _ptr(logits), T, _ptr(ids), _ptr(w), _stream(stream)))
+
+
 def moe_check(plan, ws, stream=None) -> int:
     """Synchronise and return the device status code (0 = MOE_OK); clears it."""
     return int(load_library().moe_check(plan, _ptr(ws), _stream(stream)))
@@ -311,6 +325,23 @@ class MoePlan:
         _check(lib.moe_step_host(self.handle, io._host_p, io._dev_p, io._ydev_p, io._yhost_p, io.T, _ptr(ws),
                                    _stream(stream)))
         return io.y
+
+    def route(self, logits, stream=None, ids=None, w=None):
+        """Top-k routing of logits [T, E] (float32, on the device): (ids, w)."""
+        if logits.dim() != 2 or logits.shape[1] != self.E:
+            raise MoeError(MOE_ERR_INVALID_ARG, f"logits {tuple(logits.shape)} is not [T, {self.E}]")
+        T = logits.shape[0]
+        if ids is None:
+            ids = torch.empty((T, self.top_k), dtype=torch.int32, device=logits.device)
+        if w is None:
+            w = torch.empty((T, self.top_k), dtype=torch.float32, device=logits.device)
+        moe_route(self.handle, logits, ids, w, stream)
+        return ids, w
+
+    def step_logits(self, x, logits, ws, y=None, stream=None):
+        """Routing, then the step, on one stream: no trip through the host."""
+        ids, w = self.route(logits, stream)
+        return self.step(x, ids, w, ws, y=y, stream=stream)
 
     def group(self, ids, ws, stream=None):
         if ids.dim() != 2 or ids.shape[1] != self.top_k:

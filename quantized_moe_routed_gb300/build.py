@@ -1,6 +1,6 @@
 """Build the sm_103a C-ABI library libmoe_nvfp4.so in-tree (nvcc, no cmake).
 
-The three translation units compile in parallel, then link into
+The four translation units compile in parallel, then link into
 quantized_moe_routed_gb300/_build/libmoe_nvfp4.so (static cudart).  The
 compiler's output for each unit (the kernels' ptxas register and spill report)
 is kept beside the objects as <unit>.log.
@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe_nvfp4.so")
-SOURCES = ("moe_kernels.cu", "moe_tc.cu", "moe_abi.cu")
+SOURCES = ("moe_kernels.cu", "moe_tc.cu", "moe_route.cu", "moe_abi.cu")
 HEADERS = ("moe_internal.h", "moe_device.cuh")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -48,7 +48,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     for src in SOURCES:
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
         cmd = [cc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
-        if src in ("moe_kernels.cu", "moe_tc.cu"):
+        if src in ("moe_kernels.cu", "moe_tc.cu", "moe_route.cu"):
             cmd += ["-Xptxas", "-v"]
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
         objs.append(obj)

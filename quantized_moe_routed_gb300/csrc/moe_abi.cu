@@ -1,7 +1,7 @@
 // moe_abi.cu -- host side of the C ABI declared in include/moe_nvfp4.h:
 // argument validation, tile choice, workspace layout, launches, counters.
-// Every step of the routed-experts computation runs in moe_kernels.cu; this
-// file only checks, plans and enqueues.
+// Every step of the computation runs in the kernels (moe_kernels.cu,
+// moe_tc.cu, moe_route.cu); this file only checks, plans and enqueues.
 #include "moe_internal.h"
 #include "moe_nvfp4.h"
 
@@ -1006,6 +1006,44 @@ moe_status_t moe_null_step(moe_plan_t plan, const void *x_dev, const int32_t *id
                            float *y_dev, int T, void *ws_dev, void *stream)
 {
     return run_step(plan, x_dev, ids_dev, w_dev, y_dev, T, ws_dev, stream, Path::Null);
+}
+
+moe_status_t moe_route(moe_plan_t plan, const float *logits_dev, int T, int32_t *ids_dev, float *w_dev,
+                       void *stream)
+{
+    if (!plan) return fail(MOE_ERR_INVALID_ARG, "null plan");
+    if (T < 0 || T > plan->d.T_max) {
+        reject(plan);
+        return fail(MOE_ERR_INVALID_ARG, "T=%d outside [0, T_max=%d]", T, plan->d.T_max);
+    }
+    if (plan->d.top_k > plan->d.E) {
+        reject(plan);
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "routing needs top_k <= E (top_k=%d, E=%d)", plan->d.top_k,
+                    plan->d.E);
+    }
+    if (T == 0) return MOE_OK;
+    if (!logits_dev || !ids_dev || !w_dev) {
+        reject(plan);
+        return fail(MOE_ERR_INVALID_ARG, "null logits/ids/w pointer");
+    }
+    if (!aligned(logits_dev, 4) || !aligned(ids_dev, 4) || !aligned(w_dev, 4)) {
+        reject(plan);
+        return fail(MOE_ERR_MISALIGNED, "logits, ids and w need 4-byte alignment");
+    }
+    moe_status_t st = check_device(plan);
+    if (st != MOE_OK) {
+        reject(plan);
+        return st;
+    }
+    cudaError_t e = moe::launch_route(logits_dev, T, plan->d.E, plan->d.top_k, ids_dev, w_dev, plan->pdl,
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        reject(plan);
+        return fail(MOE_ERR_CUDA, "routing launch: %s", cudaGetErrorString(e));
+    }
+    std::lock_guard<std::mutex> lk(plan->mu);
+    plan->stats.route_launches++;
+    return MOE_OK;
 }
 
 moe_status_t moe_check(moe_plan_t plan, void *ws_dev, void *stream)

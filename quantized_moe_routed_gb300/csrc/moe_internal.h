@@ -127,6 +127,10 @@ inline int tc_stage_bytes(int N)
 }
 cudaError_t launch_tc(const KernelParams &p, int grid, int smem_bytes, bool pdl, cudaStream_t st);
 cudaError_t set_tc_smem_limit(int bytes);
+
+// moe_route.cu: top-k routing, one warp per token (E <= 1024, k <= min(16, E))
+cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w, bool pdl,
+                         cudaStream_t st);
 int group_smem_bytes(int P, int E);
 
 }  // namespace moe

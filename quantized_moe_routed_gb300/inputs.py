@@ -38,7 +38,7 @@ import torch
 
 __all__ = [
     "Workload", "WORKLOADS", "quantize_nvfp4", "make_x", "make_topk_w",
-    "make_topk_ids", "make_expert_weights", "make_inputs", "rotate_ids",
+    "make_topk_ids", "make_router_logits", "make_expert_weights", "make_inputs", "rotate_ids",
     "rotation_delta", "touched_experts", "algorithmic_bytes",
 ]
 
@@ -123,6 +123,13 @@ def make_topk_w(wl: Workload) -> torch.Tensor:
     p = np.exp(z)
     p = p / p.sum(axis=1, keepdims=True)
     return torch.from_numpy(p.astype(np.float32))
+
+
+def make_router_logits(wl: Workload) -> torch.Tensor:
+    """Router logits for the routing step in front of the path: N(0,1) fp32
+    [T, E] from their own seeded stream (4), CPU."""
+    a = _np_rng(wl.seed, 4).standard_normal((wl.T, wl.E), dtype=np.float32)
+    return torch.from_numpy(a)
 
 
 def _ids_uniform(rng, T, k, E):
