@@ -49,6 +49,7 @@ def test_binding_loads_and_rejects_without_plan():
     assert q.moe_workspace_bytes(None, 1) == 0
     assert q.moe_io_bytes(None, 1) == (0, 0, 0)
     assert lib.moe_step_host(None, None, None, None, None, 1, None, None) == q.binding.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(None, None, 1, None, None, None) == q.binding.MOE_ERR_INVALID_ARG
 
 
 def test_step_shapes_must_agree():
