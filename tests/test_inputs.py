@@ -109,3 +109,17 @@ def test_zipf_draws_follow_one_over_rank_without_replacement():
         for b in range(E):
             q = 0.0 if a == b else p[a] * p[b] / (1 - p[a])
             assert abs(joint[a, b] - q) <= 5 * np.sqrt(q * (1 - q) / n) + 1e-12, (a, b, joint[a, b], q)
+
+
+def test_router_logits_are_seeded_and_leave_the_other_streams_alone():
+    from quantized_moe_routed_gb300.inputs import make_router_logits
+    wl = WORKLOADS["spec_verify"]
+    a = make_router_logits(wl)
+    assert a.shape == (wl.T, wl.E) and a.dtype == torch.float32
+    assert torch.equal(a, make_router_logits(wl))
+    assert not torch.equal(a, make_router_logits(wl.replace(seed=1)))
+    assert abs(float(a.std()) - 1.0) < 0.05
+    # x, the routing weights and the ids come from their own streams, as before
+    x0, w0, i0 = make_x(wl), make_topk_w(wl), make_topk_ids(wl)
+    make_router_logits(wl)
+    assert torch.equal(x0, make_x(wl)) and torch.equal(w0, make_topk_w(wl)) and torch.equal(i0, make_topk_ids(wl))
