@@ -51,7 +51,7 @@ typedef enum {
     MOE_ERR_CUDA = 5,              /* a CUDA runtime call failed (message has details) */
     MOE_ERR_TIMEOUT = 6,           /* device: a bounded wait gave up (see moe_check)   */
     MOE_ERR_BAD_EXPERT_ID = 7,     /* device: an id >= E was seen (slot skipped)       */
-    MOE_ERR_RANGE = 8              /* device: an fp16 intermediate overflowed          */
+    MOE_ERR_RANGE = 8              /* device: an intermediate (h) was not finite      */
 } moe_status_t;
 
 /* Opaque plan: host memory owned by the library (moe_plan_destroy frees it). */
@@ -144,9 +144,10 @@ moe_status_t moe_group(moe_plan_t plan, const int32_t *ids_dev, int T, void *ws_
                        int32_t *counts_dev, int32_t *offsets_dev, int32_t *perm_dev, void *stream);
 
 /* The routed-experts step for 0 <= T <= 24 tokens (decode; T == 0 is a no-op).
- *   x_dev    bf16 [T, H] row-major, 16-byte aligned; values must fit fp16
- *            (|x| <= 65504) because the register kernel's mma.sync operands
- *            are fp16 (the tensor-core kernel prescales each row itself)
+ *   x_dev    bf16 [T, H] row-major, 16-byte aligned; any finite bf16 values:
+ *            both kernels prescale each token's row by a power of two before
+ *            narrowing it (fp16 mma.sync operands, or FP4 digit rows) and undo
+ *            the prescale exactly in their fp32 epilogues
  *   ids_dev  int32 [T, top_k]: id < 0 = empty slot, id >= E = skipped + flagged
  *   w_dev    float [T, top_k] routing weights, used as given
  *   y_dev    float [T, H] row-major, 16-byte aligned; fully written
@@ -166,9 +167,10 @@ moe_status_t moe_decode(moe_plan_t plan, const void *x_dev, const int32_t *ids_d
  * Same x_dev, ids_dev, w_dev, y_dev, T and stream as moe_decode
  * (0 <= T <= min(24, T_max)).  The scratch is one library-owned buffer per
  * device of 16 MiB in this library's global memory; a call needs
- * 256 + 16384 + 4*T*(H/64) + 2*T*top_k*I + 6*T*top_k*H bytes (each piece
- * rounded up to 256) and is refused with MOE_ERR_UNSUPPORTED_SHAPE when that
- * exceeds 16 MiB.  Nothing is allocated or freed: each call zeroes the
+ * 256 + 16384 + 4*T*(H/64) + 8*T*top_k + 2*T*top_k*I + 6*T*top_k*H
+ * + 32*T*top_k*(I/KB) bytes (each piece rounded up to 256; KB = 512 when I is
+ * a multiple of 256, else I) and is refused with MOE_ERR_UNSUPPORTED_SHAPE
+ * when that exceeds 16 MiB.  Nothing is allocated or freed: each call zeroes the
  * scratch's control block and counters (one memset on `stream`) and launches
  * the decode kernel on it.
  * The first call on each device does the set-up (it looks up the scratch's
@@ -244,7 +246,8 @@ moe_status_t moe_null_step(moe_plan_t plan, const void *x_dev, const int32_t *id
  * descending order of logit.  Equal logits put the smaller expert index first,
  * and NaN counts as -infinity.  w_dev receives the softmax of those top_k
  * logits (fp32, expf); when the largest selected logit is -infinity the
- * weights are 0.  These are the ids_dev / w_dev that a following moe_decode
+ * weights are 0, and when it is +infinity the selected +infinity logits
+ * share the weight equally (1/their count) and the others get 0.  These are the ids_dev / w_dev that a following moe_decode
  * or moe_prefill on the same stream takes, so routing needs no trip through
  * the host.
  *   logits_dev  float [T, E] row-major, 4-byte aligned

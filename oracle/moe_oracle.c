@@ -266,7 +266,9 @@ int oracle_group(const int32_t *ids, int P, int E, int32_t *counts, int32_t *off
  * largest router logits, in descending order of logit (equal logits: the
  * smaller expert index first; NaN counts as -infinity), and their weights, the
  * softmax over those k logits (in double, then rounded to float).  If the
- * largest selected logit is -infinity the weights are 0.  This is the router
+ * largest selected logit is -infinity the weights are 0; if it is +infinity,
+ * the selected +infinity logits share the weight equally and the others get
+ * 0 (the softmax's limit as those logits grow together).  This is the router
  * output the input recipe draws at random (k logits, softmax over them); the
  * pages do not describe the router, so it is the plain definition.
  * logits float [T, E]; ids int32 [T, k]; w float [T, k].  Returns -1 on a
@@ -296,11 +298,15 @@ int oracle_route(const float *logits, int T, int E, int k, int32_t *ids, float *
             ids[(size_t)t * k + j] = best;
             sel[j] = bv;
         }
+        /* a +infinity winner: the softmax's limit as the infinite logits grow
+         * together, equal weights over the selected +infinity logits */
         double m = sel[0], sum = 0.0;
         for (int j = 0; j < k; ++j)
-            sum += (m == -INFINITY) ? 0.0 : exp(sel[j] - m);
-        for (int j = 0; j < k; ++j)
-            w[(size_t)t * k + j] = (m == -INFINITY) ? 0.0f : (float)(exp(sel[j] - m) / sum);
+            sum += (m == -INFINITY) ? 0.0 : (m == INFINITY ? (sel[j] == INFINITY ? 1.0 : 0.0) : exp(sel[j] - m));
+        for (int j = 0; j < k; ++j) {
+            double ej = (m == INFINITY) ? (sel[j] == INFINITY ? 1.0 : 0.0) : exp(sel[j] - m);
+            w[(size_t)t * k + j] = (m == -INFINITY) ? 0.0f : (float)(ej / sum);
+        }
     }
     free(taken);
     free(sel);

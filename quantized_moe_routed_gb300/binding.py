@@ -249,6 +249,8 @@ def moe_route(plan, logits, ids, w, stream=None):
     if T < 0 or ids.dim() != 2 or ids.shape[0] != T or tuple(w.shape) != tuple(ids.shape):
         raise MoeError(MOE_ERR_INVALID_ARG, f"shapes logits {tuple(logits.shape)}, ids {tuple(ids.shape)}, "
                                             f"w {tuple(w.shape)} are not logits [T, E], ids and w [T, k]")
+    if not (logits.device == ids.device == w.device):
+        raise MoeError(MOE_ERR_INVALID_ARG, "logits, ids and w must be on one device")
     _check(load_library().moe_route(plan, _ptr(logits), T, _ptr(ids), _ptr(w), _stream(stream)))
 
 
@@ -327,21 +329,39 @@ class MoePlan:
         return io.y
 
     def route(self, logits, stream=None, ids=None, w=None):
-        """Top-k routing of logits [T, E] (float32, on the device): (ids, w)."""
+        """Top-k routing of logits [T, E] (float32, on the plan's device): (ids, w).
+        The kernel reads T*E logits and writes T*top_k ids and weights, so
+        caller-supplied ids / w must be exactly [T, top_k].  Temporaries are
+        allocated on `stream`, so the caching allocator does not hand their
+        memory out again while the routing queued there may still use it."""
         if logits.dim() != 2 or logits.shape[1] != self.E:
             raise MoeError(MOE_ERR_INVALID_ARG, f"logits {tuple(logits.shape)} is not [T, {self.E}]")
+        dev = self.weights["gate_q"].device
+        if logits.device != dev:
+            raise MoeError(MOE_ERR_INVALID_ARG, f"logits are on {logits.device}, the plan on {dev}")
         T = logits.shape[0]
-        if ids is None:
-            ids = torch.empty((T, self.top_k), dtype=torch.int32, device=logits.device)
-        if w is None:
-            w = torch.empty((T, self.top_k), dtype=torch.float32, device=logits.device)
-        moe_route(self.handle, logits, ids, w, stream)
+        for name, t in (("ids", ids), ("w", w)):
+            if t is not None and (t.dim() != 2 or tuple(t.shape) != (T, self.top_k)):
+                raise MoeError(MOE_ERR_INVALID_ARG, f"{name} {tuple(t.shape)} is not [{T}, {self.top_k}]")
+        st = torch.cuda.current_stream(dev) if stream is None else stream
+        with torch.cuda.stream(st):
+            if ids is None:
+                ids = torch.empty((T, self.top_k), dtype=torch.int32, device=dev)
+            if w is None:
+                w = torch.empty((T, self.top_k), dtype=torch.float32, device=dev)
+        moe_route(self.handle, logits, ids, w, st)
         return ids, w
 
     def step_logits(self, x, logits, ws, y=None, stream=None):
-        """Routing, then the step, on one stream: no trip through the host."""
-        ids, w = self.route(logits, stream)
-        return self.step(x, ids, w, ws, y=y, stream=stream)
+        """Routing, then the step, on one stream: no trip through the host.
+        The routing's ids / w (and y, if not given) are allocated on that
+        stream, so they stay reserved until the work queued there has run."""
+        st = torch.cuda.current_stream(x.device) if stream is None else stream
+        ids, w = self.route(logits, st)
+        if y is None:
+            with torch.cuda.stream(st):
+                y = torch.empty((x.shape[0], self.H), dtype=torch.float32, device=x.device)
+        return self.step(x, ids, w, ws, y=y, stream=st)
 
     def group(self, ids, ws, stream=None):
         if ids.dim() != 2 or ids.shape[1] != self.top_k:

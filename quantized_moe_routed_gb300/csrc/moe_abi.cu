@@ -67,7 +67,8 @@ struct moe_plan {
     bool strict = false, pdl = false;
     int smem_attr = 0;  // dynamic smem the kernel attribute currently allows
     // workspace layout (bytes from the base)
-    size_t off_done = 0, off_cnt = 0, off_h = 0, off_part = 0, off_xs = 0, ws_bytes = 0;
+    size_t off_done = 0, off_cnt = 0, off_href = 0, off_h = 0, off_part = 0, off_xs = 0, off_xexp = 0, off_hte = 0;
+    size_t ws_bytes = 0;
     // tensor-core kernel: weight tensor maps (128-row boxes), workspace pieces
     bool use_tc = false;
     CUtensorMap tmw[6];
@@ -185,7 +186,7 @@ moe::SmemLayout layout_for(const moe_plan *pl, int T)
         const Tiling &tl = pl->tl[nt];
         const int rows = 8 * nt < T ? 8 * nt : T;
         const int stA = tl.offAa + rows * 2 * tl.KA;
-        const int stB = tl.offAb + rows * 2 * tl.KB;
+        const int stB = tl.offAb + rows * (2 * tl.KB + moe::kHteRow);
         L.stage_bytes = up1024(stA > stB ? stA : stB);
     }
     const int avail = pl->smem_optin - L.red_bytes - L.tab_bytes - 1024;
@@ -318,7 +319,7 @@ enum class Path { Decode, Prefill, Null };
 
 // Byte offsets of the workspace pieces from the workspace base.
 struct WsOffsets {
-    size_t off_done, off_cnt, off_h, off_part, off_xs, total;
+    size_t off_done, off_cnt, off_href, off_h, off_part, off_xs, off_xexp, off_hte, total;
     int Pmax;  // rows of each part block of xs / hbuf
 };
 
@@ -528,6 +529,9 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
     p.cnt = reinterpret_cast<uint32_t *>(wsb + (wo ? wo->off_cnt : pl->off_cnt));
     p.hbuf = reinterpret_cast<uint16_t *>(wsb + (wo ? wo->off_h : pl->off_h));
     p.xs = reinterpret_cast<uint16_t *>(wsb + (wo ? wo->off_xs : pl->off_xs));
+    p.href = reinterpret_cast<uint32_t *>(wsb + (wo ? wo->off_href : pl->off_href));
+    p.xexp = reinterpret_cast<int32_t *>(wsb + (wo ? wo->off_xexp : pl->off_xexp));
+    p.hte = reinterpret_cast<int8_t *>(wsb + (wo ? wo->off_hte : pl->off_hte));
     p.Pmax = wo ? wo->Pmax : pl->Tc * pl->d.top_k;
     p.part = reinterpret_cast<float *>(wsb + (wo ? wo->off_part : pl->off_part));
     p.H = pl->d.H;
@@ -648,10 +652,14 @@ WsOffsets static_layout(const moe_plan *pl, int T)
     const size_t P = static_cast<size_t>(T) * pl->d.top_k;
     o.off_done = moe::kCtrlBytes;
     o.off_cnt = up(o.off_done + 4 * static_cast<size_t>(moe::kMaxPairs), 256);
-    o.off_h = up(o.off_cnt + 4 * static_cast<size_t>(T) * pl->nHt, 256);
+    o.off_href = up(o.off_cnt + 4 * static_cast<size_t>(T) * pl->nHt, 256);
+    o.off_h = up(o.off_href + 4 * P, 256);
     o.off_part = up(o.off_h + 2 * P * pl->d.I, 256);
     o.off_xs = up(o.off_part + 4 * P * pl->d.H, 256);
-    o.total = up(o.off_xs + 2 * P * pl->d.H, 256);
+    o.off_xexp = up(o.off_xs + 2 * P * pl->d.H, 256);
+    const size_t nPB = static_cast<size_t>(pl->d.I / pl->tl[1].KB);
+    o.off_hte = up(o.off_xexp + 4 * P, 256);
+    o.total = up(o.off_hte + nPB * P * moe::kHteRow, 256);
     o.Pmax = static_cast<int>(P);
     return o;
 }
@@ -777,12 +785,18 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
     pl->off_cnt = o;
     o = up(o + 4 * static_cast<size_t>(pl->Tc) * pl->nHt, 256);
     const size_t Pc = static_cast<size_t>(pl->Tc) * d.top_k;
+    pl->off_href = o;
+    o = up(o + 4 * Pc, 256);
     pl->off_h = o;
     o = up(o + 2 * Pc * d.I, 256);
     pl->off_part = o;
     o = up(o + 4 * Pc * d.H, 256);
     pl->off_xs = o;
     o = up(o + 2 * Pc * d.H, 256);
+    pl->off_xexp = o;
+    o = up(o + 4 * Pc, 256);
+    pl->off_hte = o;
+    o = up(o + static_cast<size_t>(d.I / pl->tl[1].KB) * Pc * moe::kHteRow, 256);
     if (pl->use_tc) {
         const size_t rows = 4 * Pc < 64 ? 64 : 4 * Pc;
         pl->tc_rows = static_cast<int>(rows);
@@ -920,7 +934,7 @@ moe_status_t moe_decode_static(moe_plan_t plan, const void *x_dev, const int32_t
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "moe_decode_static check: %s", cudaGetErrorString(e));
     if (word & moe::kErrTimeout) return fail(MOE_ERR_TIMEOUT, "a device-side wait timed out");
     if (word & moe::kErrBadId) return fail(MOE_ERR_BAD_EXPERT_ID, "an expert id >= E was seen and skipped");
-    if (word & moe::kErrRange) return fail(MOE_ERR_RANGE, "an fp16 intermediate (h) overflowed");
+    if (word & moe::kErrRange) return fail(MOE_ERR_RANGE, "an intermediate (h) was not finite");
     return MOE_OK;
 }
 
@@ -1060,7 +1074,7 @@ moe_status_t moe_check(moe_plan_t plan, void *ws_dev, void *stream)
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "moe_check: %s", cudaGetErrorString(e));
     if (word & moe::kErrTimeout) return fail(MOE_ERR_TIMEOUT, "a device-side wait timed out");
     if (word & moe::kErrBadId) return fail(MOE_ERR_BAD_EXPERT_ID, "an expert id >= E was seen and skipped");
-    if (word & moe::kErrRange) return fail(MOE_ERR_RANGE, "an fp16 intermediate (h) overflowed");
+    if (word & moe::kErrRange) return fail(MOE_ERR_RANGE, "an intermediate (h) was not finite");
     return MOE_OK;
 }
 

@@ -177,6 +177,15 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u)
     return d;
 }
 
+// Two bf16 times the power of two s (exact in fp32), then -> f16x2 (RNE).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t u, float s)
+{
+    float lo = __uint_as_float(u << 16) * s, hi = __uint_as_float(u & 0xffff0000u) * s;
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1)
 {
@@ -184,6 +193,31 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
                  "{%0,%1,%2,%3};"
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float exp2i(int e)  // 2^e for -126 <= e <= 127
+{
+    return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+__device__ __forceinline__ float mul_pow2(float v, int e)  // v * 2^e, e in [-200, 200]
+{
+    const int e1 = e / 2, e2 = e - e1;
+    return v * exp2i(max(-126, min(127, e1))) * exp2i(max(-126, min(127, e2)));
+}
+// Power-of-two prescale for fp16 operands: the exponent e with a * 2^e in
+// [2^14, 2^15) for the largest magnitude a of a row or tile (every element then
+// stays below fp16's largest finite value, and the largest keeps all eleven
+// significant bits), clamped to [-126, 127]; 0 when a is 0 or not finite.
+__device__ __forceinline__ int f16_prescale_exp(float a)
+{
+    if (!(a > 0.f) || !(a < 3.0e38f)) return 0;
+    uint32_t u = __float_as_uint(a);
+    int E = static_cast<int>((u >> 23) & 0xFFu) - 127;
+    if (E == -127) {  // subnormal a: normalise
+        u = __float_as_uint(a * 8388608.f);  // 2^23
+        E = static_cast<int>((u >> 23) & 0xFFu) - 127 - 23;
+    }
+    return max(-126, min(127, 14 - E));
 }
 
 __device__ __forceinline__ uint32_t u4w(const uint4 &v, int i)
@@ -231,6 +265,7 @@ struct SmemHdr {
     // listed (release-published), cj_claim taken (CAS), cj_closed: no more
     int cj_count, cj_claim, cj_closed;
     uint32_t cj[kCombJobs];
+    int xexp[kXexpPrologueT];  // register kernel, T <= kXexpPrologueT: each token's x prescale
 };
 static_assert(sizeof(SmemHdr) <= kTabHdrBytes, "header too large");
 

@@ -21,6 +21,8 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxStages = 16;
 constexpr int kDecodeMaxT = 24;     // the pages' m <= 24 decode bound
 constexpr int kMB = 64;             // down-projection rows per phase-B ticket
+constexpr int kXexpPrologueT = 8;   // register kernel: up to this T, every CTA finds the x prescales itself
+constexpr int kHteRow = 32;         // register kernel: bytes of h tile exponents per (part, pair) row
 
 // Device error word bits (workspace control block, word 2).
 constexpr uint32_t kErrTimeout = 1u;
@@ -64,6 +66,9 @@ struct KernelParams {
     uint16_t *xs;       // [nPA][Pmax][KA] fp16 x, rows in sorted pair order (layout: see kernels)
     uint16_t *hbuf;     // [nPB][Pmax][KB] fp16 h, same row order and layout
     float *part;        // [P, H] fp32 per-pair down-projection outputs
+    int32_t *xexp;      // [Pmax] register kernel: prescale exponent of each token's x (T > kXexpPrologueT)
+    int8_t *hte;        // [nPB][Pmax][kHteRow] register kernel: prescale exponent of each 32-row tile of h
+    uint32_t *href;     // [Pmax] register kernel: per pair, 200 - (smallest tile exponent), by red.max
     // shape
     int H, I, E, k, T;
     int Pmax;           // rows of each part block of xs / hbuf

@@ -201,27 +201,32 @@ __device__ __forceinline__ void load_act(uint4 (&b)[NT][4], const uint8_t *act, 
     }
 }
 
-// bf16 -> fp16 of 8 values (exact inside the fp16 range).
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u)
+// bf16 times the power of two s -> fp16, 8 values (the prescale keeps every
+// value inside the fp16 range, see f16_prescale_exp).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u, float s)
 {
-    return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
+    return make_uint4(bf16x2_to_f16x2_scaled(u.x, s), bf16x2_to_f16x2_scaled(u.y, s),
+                      bf16x2_to_f16x2_scaled(u.z, s), bf16x2_to_f16x2_scaled(u.w, s));
 }
 
 // The B operand of a gate/up chunk from a KIND_AX stage: the group's x rows
 // as copied from the caller's bf16 x (row n at n*pitch, natural order), the
-// 32 elements of this thread from chunk offset koff, converted to fp16.
-// Pairs past the group's end are 0.
+// 32 elements of this thread from chunk offset koff, prescaled by the pair's
+// token exponent and converted to fp16 -- the same values the gathered x
+// holds.  Pairs past the group's end are 0.
 template <int NT>
 __device__ __forceinline__ void load_x_raw(uint4 (&b)[NT][4], const uint8_t *act, int pitch, int koff, int gcnt,
-                                           int g)
+                                           int g, const Tabs &tb, int gbeg)
 {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int n = nt * 8 + g;
         if (n < gcnt) {
             const uint8_t *src = act + n * pitch + koff * 2;
+            const float sc = exp2i(tb.hdr->xexp[tb.stok[gbeg + n]]);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) b[nt][v] = bf16x8_to_f16x8(*reinterpret_cast<const uint4 *>(src + 16 * v));
+            for (int v = 0; v < 4; ++v)
+                b[nt][v] = bf16x8_to_f16x8(*reinterpret_cast<const uint4 *>(src + 16 * v), sc);
         } else {
 #pragma unroll
             for (int v = 0; v < 4; ++v) b[nt][v] = make_uint4(0, 0, 0, 0);
@@ -287,34 +292,45 @@ __device__ __forceinline__ bool finish_ticket(const KernelParams &p, const Tabs 
     const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
     const float *redf = reinterpret_cast<const float *>(rb);
     if (isA) {
-        // h[n][i0 + half*16 + row] = SiLU(g) * u: this warp's RA*NT of the RA rows x 8*NT pairs
+        // warp w takes pairs w, w + 8 of the group; lane l row l of the 32-row
+        // tile: g and u summed over the K slices in a fixed order, the x
+        // prescale undone (exact), h = SiLU(g) * u in fp32; the tile's h goes
+        // to fp16 under its own power-of-two prescale (largest |h| of the tile
+        // in [2^14, 2^15)), recorded per (pair, tile); the pair's reference
+        // (its largest tile's exponent) is gathered by a max over 200 - e
+        static_assert(RA == 32, "a gate/up tile is one warp's 32 rows");
+        const int row = lane, half = row >> 4, rr = row & 15;
+        for (int n = warp; n < gcnt; n += kConsumerWarps) {
+            const int nt = n >> 3, n8 = n & 7;
+            const int ls = (rr & 7) * 4 + (n8 >> 1), r = (rr >> 3) * 2 + (n8 & 1);
+            float sg = 0.f, su = 0.f;
 #pragma unroll
-        for (int j = 0; j < (RA * NT + 31) / 32; ++j) {
-            const int idx = warp * (RA * NT) + j * 32 + lane;
-            if (j * 32 + lane >= RA * NT) break;
-            const int half = idx / (NT * 128), rem = idx - half * (NT * 128);
-            const int nt = rem >> 7, ls = (rem >> 2) & 31, r = rem & 3;
-            const int row = half * 16 + (ls >> 2) + 8 * (r >> 1);
-            const int n = nt * 8 + 2 * (ls & 3) + (r & 1);
-            if (n < gcnt) {
-                float sg = 0.f, su = 0.f;
+            for (int k2 = 0; k2 < nks; ++k2) {
+                sg += redf[((((k2 * nhalf + half) * 2 + 0) * NT + nt) * 32 + ls) * 4 + r];
+                su += redf[((((k2 * nhalf + half) * 2 + 1) * NT + nt) * 32 + ls) * 4 + r];
+            }
+            const int sr = gbeg + n;
+            const int tok = tb.stok[sr];
+            const int ex = p.T <= kXexpPrologueT ? hd->xexp[tok] : __ldcg(p.xexp + tok);
+            const float gv = mul_pow2(sg * ts0, -ex), uv = mul_pow2(su * ts1, -ex);
+            float v = gv / (1.0f + __expf(-gv)) * uv;
+            if (NULLM) v = 0.f;
+            if (!(fabsf(v) < 3.0e38f)) atomicOr(p.ctrl + 2, kErrRange);  // h not finite
+            float a = fabsf(v);
 #pragma unroll
-                for (int k2 = 0; k2 < nks; ++k2) {
-                    sg += redf[((((k2 * nhalf + half) * 2 + 0) * NT + nt) * 32 + ls) * 4 + r];
-                    su += redf[((((k2 * nhalf + half) * 2 + 1) * NT + nt) * 32 + ls) * 4 + r];
-                }
-                const float gv = sg * ts0, uv = su * ts1;
-                float v = gv / (1.0f + __expf(-gv)) * uv;
-                if (NULLM) v = 0.f;
-                if (!(fabsf(v) <= 65504.0f)) atomicOr(p.ctrl + 2, kErrRange);
-                const int kh = tile * RA + row, pb = kh / p.KB, kk = kh - pb * p.KB;
-                const int rr = gbeg + n;
-                p.hbuf[(static_cast<size_t>(pb) * p.Pmax + rr) * p.KB + act_index(p.nib_mode, kk, rr & 1)] =
-                    __half_as_ushort(__float2half_rn(v));
+            for (int d = 16; d; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
+            const int et = f16_prescale_exp(a);
+            const int kh = tile * RA + row, pb = kh / p.KB, kk = kh - pb * p.KB;
+            p.hbuf[(static_cast<size_t>(pb) * p.Pmax + sr) * p.KB + act_index(p.nib_mode, kk, sr & 1)] =
+                __half_as_ushort(__float2half_rn(v * exp2i(et)));
+            if (lane == 0) {
+                p.hte[(static_cast<size_t>(pb) * p.Pmax + sr) * kHteRow + kk / 32] = static_cast<int8_t>(et);
+                atomicMax(p.href + sr, static_cast<uint32_t>(200 - et));
             }
         }
     } else {
-        // per-pair down outputs of rows h0 .. h0+63: this warp's 64*NT, sum of the 4 K chunks
+        // per-pair down outputs of rows h0 .. h0+63: this warp's 64*NT, sum of
+        // the 4 K chunks; the pair's h reference prescale undone (exact)
         const int h0 = tile * kMB;
 #pragma unroll
         for (int j = 0; j < 2 * NT; ++j) {
@@ -327,7 +343,7 @@ __device__ __forceinline__ bool finish_ticket(const KernelParams &p, const Tabs 
                 float so = 0.f;
 #pragma unroll
                 for (int k2 = 0; k2 < 4; ++k2) so += redf[(((k2 * 4 + mm) * NT + nt) * 32 + ls) * 4 + r];
-                p.part[static_cast<size_t>(gbeg + n) * p.H + h0 + row] = so * ts0;
+                p.part[static_cast<size_t>(gbeg + n) * p.H + h0 + row] = mul_pow2(so * ts0, -tb.eref[gbeg + n]);
             }
         }
     }
@@ -345,15 +361,43 @@ __device__ __forceinline__ void consumer_sync()
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
 
-// Gather x into sorted pair order as fp16 in the activation layout.  Rows
-// are claimed in batches from a global counter, so whichever CTAs run first
-// do the work and no CTA depends on another being resident; the rows written
-// are then published with a gpu-scope release (counter word 3).  Run by the
-// eight consumer warps while the first weight copies are in flight.
+// Largest |x| of row `src` (H bf16), warp-wide.
+__device__ __forceinline__ float row_absmax(const uint16_t *src, int H, int lane)
+{
+    float amax = 0.f;
+    for (int v0 = lane; v0 < H / 8; v0 += 32 * 8) {
+        uint4 u[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int v = v0 + 32 * i;
+            u[i] = v < H / 8 ? *reinterpret_cast<const uint4 *>(src + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xffff0000u))));
+        }
+    }
+#pragma unroll
+    for (int d = 16; d; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    return amax;
+}
+
+// Gather x into sorted pair order as fp16 in the activation layout, each row
+// under its token's power-of-two prescale (f16_prescale_exp of the row's
+// largest |x|; undone exactly in the fp32 epilogue).  Rows are claimed in
+// batches from a global counter, so whichever CTAs run first do the work and
+// no CTA depends on another being resident; the rows written are then
+// published with a gpu-scope release (counter word 3).  One warp per row.
+// Up to kXexpPrologueT tokens every CTA already holds the exponents; above,
+// the warp finds its row's and records it per token for the epilogues.  Run
+// by the eight consumer warps while the first weight copies are in flight.
 __device__ __forceinline__ void gather_x(const KernelParams &p, const Tabs &tb)
 {
     SmemHdr *hd = tb.hdr;
-    const int nv = hd->n_valid, tid = threadIdx.x;
+    const int nv = hd->n_valid, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int batch = (nv + gridDim.x - 1) / gridDim.x;
     int mine = 0;
     for (;;) {
@@ -363,11 +407,20 @@ __device__ __forceinline__ void gather_x(const KernelParams &p, const Tabs &tb)
         consumer_sync();
         if (c >= nv) break;
         const int c_end = min(c + batch, nv);
-        for (int r = c; r < c_end; ++r) {
-            const uint16_t *src = p.x + static_cast<size_t>(tb.stok[r]) * p.H;
-            for (int k8 = tid * 8; k8 < p.H; k8 += kConsumerThreads * 8) {
+        for (int r = c + warp; r < c_end; r += kConsumerWarps) {
+            const int tok = tb.stok[r];
+            const uint16_t *src = p.x + static_cast<size_t>(tok) * p.H;
+            int ex;
+            if (p.T <= kXexpPrologueT) {
+                ex = hd->xexp[tok];
+            } else {
+                ex = f16_prescale_exp(row_absmax(src, p.H, lane));
+                if (lane == 0) p.xexp[tok] = ex;
+            }
+            const float sc = exp2i(ex);
+            for (int k8 = lane * 8; k8 < p.H; k8 += 32 * 8) {
                 const int pa = k8 / p.KA, kk = k8 - pa * p.KA;
-                const uint4 v = bf16x8_to_f16x8(*reinterpret_cast<const uint4 *>(src + k8));
+                const uint4 v = bf16x8_to_f16x8(*reinterpret_cast<const uint4 *>(src + k8), sc);
                 *reinterpret_cast<uint4 *>(p.xs + (static_cast<size_t>(pa) * p.Pmax + r) * p.KA +
                                            act_index(p.nib_mode, kk, r & 1)) = v;
             }
@@ -385,8 +438,18 @@ template <int NT, bool NULLM>
 __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *smem, const Tabs &tb,
                                               volatile int *abort_flag)
 {
-    gather_x(p, tb);
     SmemHdr *hd = tb.hdr;
+    if (p.T <= kXexpPrologueT) {
+        // every token's x prescale, one warp per token (the KIND_AX stages and
+        // the gather both need them)
+        const int w0 = threadIdx.x >> 5;
+        if (w0 < p.T) {
+            const int ex = f16_prescale_exp(row_absmax(p.x + static_cast<size_t>(w0) * p.H, p.H, threadIdx.x & 31));
+            if ((threadIdx.x & 31) == 0) hd->xexp[w0] = ex;
+        }
+        consumer_sync();
+    }
+    gather_x(p, tb);
     float4 *red = reinterpret_cast<float4 *>(smem + p.red_off);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     constexpr int RA = TileRows<NT>::RA, nhalf = RA / 16, nks = kConsumerWarps / nhalf;
@@ -411,6 +474,9 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
         const bool isA = h.x != KIND_B, xdirect = h.x == KIND_AX;
         const int grp = h.y, tile = h.z, part = h.w;
         const int gbeg = tb.gbeg[grp], gcnt = tb.gcnt[grp];
+        // a down stage's h was copied after the helper marked the group complete;
+        // acquire that mark for the pairs' reference exponents (tb.eref)
+        if (!isA && !warp_spin(p, [&] { return ld_acq_cta_u8(tb.hready + grp) == 2; }, abort_flag)) break;
         if (part == 0) {
             const int e = tb.gexp[grp];
             ts0 = __ldg(isA ? p.gts + e : p.dts + e);
@@ -435,7 +501,7 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
                     o.s_b[mt] = scale_pair(sbp, p.spA, p.shA, p.mkA, r0 + 8, ko);
                 }
                 if (xdirect) {
-                    load_x_raw<NT>(o.bq, st + p.offAa, 2 * p.KA, ko, gcnt, g);
+                    load_x_raw<NT>(o.bq, st + p.offAa, 2 * p.KA, ko, gcnt, g, tb, gbeg);
                 } else {
                     load_act<NT>(o.bq, st + p.offAa, 2 * p.KA, q, gbeg, gcnt, g, t);
                 }
@@ -449,6 +515,22 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
                     o.s_b[mt] = scale_pair(st + p.offDs, p.spB, p.shB, p.mkB, r0 + 8, ko);
                 }
                 load_act<NT>(o.bq, st + p.offAb, 2 * p.KB, q, gbeg, gcnt, g, t);
+                // this thread's 32 K elements are one gate/up tile of h: bring
+                // the tile's prescale to the pair's reference (a power of two
+                // <= 1, exact unless it leaves the fp16 normal range)
+                const int8_t *te = reinterpret_cast<const int8_t *>(st + p.offAb + gcnt * 2 * p.KB);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int n = nt * 8 + g;
+                    if (n < gcnt) {
+                        const int d = te[n * kHteRow + ko / 32] - tb.eref[gbeg + n];
+                        const uint32_t m = d <= 24 ? __half_as_ushort(__float2half_rn(exp2i(-d))) * 0x10001u : 0u;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            o.bq[nt][v] = make_uint4(hmul2(o.bq[nt][v].x, m), hmul2(o.bq[nt][v].y, m),
+                                                     hmul2(o.bq[nt][v].z, m), hmul2(o.bq[nt][v].w, m));
+                    }
+                }
             }
         };
         const int nparts = isA ? p.nPA : p.nPB;
@@ -587,6 +669,12 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
             uint8_t *st = smem + s * p.stage_bytes;
             uint64_t *bar = &hd->full[s];
             if (isA) {
+                // above kXexpPrologueT tokens only the gather knows the x
+                // prescales: no stage goes out with the caller's raw rows
+                if (!x_ok && p.T > kXexpPrologueT && !wait_for([&] { return ld_acq_cta(&hd->xready) != 0; })) {
+                    ok = false;
+                    break;
+                }
                 if (!x_ok && ld_acq_cta(&hd->xready)) {
                     // x was gathered by other CTAs' generic stores: order them
                     // before this thread's async-proxy reads
@@ -624,7 +712,7 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
                 }
             } else {
                 hd->stage_hdr[s] = make_int4(KIND_B, grp, tile, part);
-                mbar_expect_tx(bar, wbytesB + abytes);
+                mbar_expect_tx(bar, wbytesB + abytes + static_cast<uint32_t>(gcnt) * kHteRow);
                 // down rows h0..h0+63, K elements part*KB ..
                 if (p.nib_mode == 0) {
                     tma3d(st + p.offDq, &p.tm[2], 0, row, part * nspB, bar, pol);
@@ -734,6 +822,15 @@ __device__ __forceinline__ void helper_loop(const KernelParams &p, uint8_t *smem
             }
         }
         if (watch >= 0 && ld_acquire(p.doneA + watch) == static_cast<uint32_t>(TA)) {
+            // the pairs' h reference exponents (their largest tile's), then the
+            // group is marked complete (release: the consumers acquire the mark)
+            const int gb = tb.gbeg[watch], gc = tb.gcnt[watch];
+            uint32_t hv[kGroupPairs];
+#pragma unroll
+            for (int i = 0; i < kGroupPairs; ++i) hv[i] = i < gc ? __ldcg(p.href + gb + i) : 200u;
+#pragma unroll
+            for (int i = 0; i < kGroupPairs; ++i)
+                if (i < gc) tb.eref[gb + i] = static_cast<int8_t>(200 - static_cast<int>(hv[i]));
             st_rel_cta_u8(tb.hready + watch, 2);
             watch = -1;
             progress = true;
@@ -753,6 +850,9 @@ __device__ __forceinline__ void helper_loop(const KernelParams &p, uint8_t *smem
                 bulk_g2s(smem + st * p.stage_bytes + p.offAb,
                          p.hbuf + (static_cast<size_t>(part) * p.Pmax + gbeg) * p.KB,
                          static_cast<uint32_t>(gcnt) * 2u * p.KB, &hd->full[st], pol);
+                bulk_g2s(smem + st * p.stage_bytes + p.offAb + gcnt * 2 * p.KB,
+                         p.hte + (static_cast<size_t>(part) * p.Pmax + gbeg) * kHteRow,
+                         static_cast<uint32_t>(gcnt) * kHteRow, &hd->full[st], pol);
             }
             ++pq_head;
             progress = true;
@@ -910,11 +1010,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
             // last CTA out: reset the counters for the next launch
             __threadfence();
             const bool err = (ld_relaxed(p.ctrl + 2) & kErrTimeout) != 0;
-            const int ng = hd->n_groups;
+            const int ng = hd->n_groups, nv = hd->n_valid;
             for (int i = 0; i < ng; ++i) p.doneA[i] = 0u;
+            for (int i = 0; i < nv; ++i) p.href[i] = 0u;
             if (err) {
                 for (int i = 0; i < kMaxPairs; ++i) p.doneA[i] = 0u;
                 for (int i = 0; i < p.T * p.nHt; ++i) p.cnt[i] = 0u;
+                for (int i = 0; i < p.Pmax; ++i) p.href[i] = 0u;
             }
             p.ctrl[0] = 0u;
             p.ctrl[1] = 0u;

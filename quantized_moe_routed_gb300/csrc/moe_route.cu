@@ -3,7 +3,8 @@
 // The serving pages do not describe the router; this is the plain definition
 // of top-k gating: per token, the top_k experts with the largest router
 // logits in descending order (equal logits: the smaller expert index first;
-// NaN counts as -infinity) and the softmax of the selected logits.  Its
+// NaN counts as -infinity) and the softmax of the selected logits (when the
+// largest is +infinity, equal weights over the selected +infinity logits).  Its
 // outputs are the ids and weights the step takes, so routing needs no trip
 // through the host.
 //
@@ -56,6 +57,9 @@ __global__ void __launch_bounds__(32 * kRouteWarps)
         }
         v[s] = x;
     }
+    // the logits are in registers: the step that follows may start its
+    // prologue (its griddepcontrol.wait still waits for this whole grid)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     float my_v = -INFINITY, m = -INFINITY;
     int my_i = 0;
     for (int j = 0; j < k; ++j) {
@@ -87,8 +91,11 @@ __global__ void __launch_bounds__(32 * kRouteWarps)
             my_i = bi;
         }
     }
-    const bool none = m == -INFINITY;  // nothing finite to weigh: weights 0
-    const float ej = (lane < k && !none) ? expf(my_v - m) : 0.f;
+    // nothing finite to weigh: weights 0; a +infinity winner: the weight is
+    // shared equally by the selected +infinity logits (the limit of the
+    // softmax as those logits grow together), the others get 0
+    const bool none = m == -INFINITY, inf = m == INFINITY;
+    const float ej = (lane < k && !none) ? (inf ? (my_v == INFINITY ? 1.f : 0.f) : expf(my_v - m)) : 0.f;
     float sum = 0.f;
     for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ej, j);
     if (lane < k) {

@@ -287,15 +287,6 @@ __device__ __forceinline__ int prescale_exp(float a)
     const int e = (m <= 1.3125f ? 11 : 10) - E;
     return max(-100, min(100, e));
 }
-__device__ __forceinline__ float exp2i(int e)  // 2^e for -126 <= e <= 127
-{
-    return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-}
-__device__ __forceinline__ float mul_pow2(float v, int e)  // v * 2^e, e in [-200, 200]
-{
-    const int e1 = e / 2, e2 = e - e1;
-    return v * exp2i(max(-126, min(127, e1))) * exp2i(max(-126, min(127, e2)));
-}
 
 // An E4M3 scale code (0 .. 0x7E) times 2^-d (d >= 0), rounded to nearest even.
 __device__ __forceinline__ uint32_t e4m3_shift_down(uint32_t c, int d)

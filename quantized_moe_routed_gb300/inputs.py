@@ -37,7 +37,7 @@ import numpy as np
 import torch
 
 __all__ = [
-    "Workload", "WORKLOADS", "quantize_nvfp4", "make_x", "make_topk_w",
+    "Workload", "WORKLOADS", "quantize_nvfp4", "make_x", "make_x_variant", "make_topk_w",
     "make_topk_ids", "make_router_logits", "make_expert_weights", "make_inputs", "rotate_ids",
     "rotation_delta", "touched_experts", "algorithmic_bytes",
 ]
@@ -114,6 +114,17 @@ def make_x(wl: Workload) -> torch.Tensor:
     """Hidden states: N(0,1) fp32 rounded to bf16 (RNE), [T, H], CPU."""
     a = _np_rng(wl.seed, 1).standard_normal((wl.T, wl.H), dtype=np.float32)
     return torch.from_numpy(a).to(torch.bfloat16)
+
+
+def make_x_variant(wl: Workload, scale_log2: int = 0, outliers=(), outlier_log2: int = 8) -> torch.Tensor:
+    """The hidden states of make_x times 2^scale_log2, with the listed channels
+    (columns) further multiplied by 2^outlier_log2: the range and outlier-channel
+    stress inputs.  Powers of two keep every bf16 value exact (while it stays a
+    normal bf16 number), so the input's shape and distribution are unchanged."""
+    a = make_x(wl).to(torch.float32) * (2.0 ** scale_log2)
+    for c in outliers:
+        a[:, c] *= 2.0 ** outlier_log2
+    return a.to(torch.bfloat16)
 
 
 def make_topk_w(wl: Workload) -> torch.Tensor:

@@ -170,7 +170,7 @@ def slice_digits(sl):
 
 @pytest.mark.parametrize("seed", range(12))
 def test_h_slices_rebased_to_the_pair_reference(seed):
-    """Reading r19: each 128-row slice of a pair's h is decomposed with its own
+    """Each 128-row slice of a pair's h is decomposed with its own
     prescale, then every digit's block scales are moved to the pair's reference
     exponent (its largest slice) by an E4M3 round-to-nearest-even of
     scale x 2^-d.  The move is exact while a scale stays normal; below that a

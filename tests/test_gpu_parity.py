@@ -63,23 +63,29 @@ def workload_inputs(name, cache):
     return cache[name]
 
 
+def workload_ref(name, cache):
+    """The oracle's y over every token of the workload (computed once per module:
+    the prefill chunk's 4096 pairs take about 20 s on the host's cores)."""
+    key = name + "/ref"
+    if key not in cache:
+        wl, x, ids, w, W = workload_inputs(name, cache)
+        y_ref, bad = oracle.moe_forward(x, ids, w, weights_cpu(W, touched_experts(ids, wl.E)))
+        assert bad == 0
+        cache[key] = y_ref
+    return cache[key]
+
+
 # ------------------------------------------------------------------ the five workloads at full size
 @pytest.mark.parametrize("kernel", [binding.MOE_KERNEL_AUTO, binding.MOE_KERNEL_REGISTER])
-@pytest.mark.parametrize("name,sample", [("tiny", None), ("decode", None), ("spec_verify", None),
-                                         ("upper_decode", None), ("prefill", 24)])
-def test_workload_parity(name, sample, kernel, cache):
+@pytest.mark.parametrize("name", ["tiny", "decode", "spec_verify", "upper_decode", "prefill"])
+def test_workload_parity(name, kernel, cache):
+    """Every element of y, every token (the prefill chunk's 512 included)."""
     wl, x, ids, w, W = workload_inputs(name, cache)
     plan, ws, y, st = run_case(wl, x, ids, w, W, kernel=kernel)
     assert st == 0, binding.STATUS_NAMES.get(st)
-    if sample is None:
-        tokens = list(range(wl.T))
-    else:
-        tokens = sorted(np.random.default_rng(7).choice(wl.T, size=sample, replace=False).tolist())
-    used = touched_experts(ids[tokens], wl.E)
-    y_ref, bad = oracle.moe_forward(x, ids, w, weights_cpu(W, used), tokens=tokens)
-    assert bad == 0
-    err = rel_err(y.cpu().numpy()[tokens], y_ref)
-    print(f"{name}: rel err {err:.3e} over {len(tokens)} tokens")
+    y_ref = workload_ref(name, cache)
+    err = rel_err(y.cpu().numpy(), y_ref)
+    print(f"{name}: rel err {err:.3e} over {wl.T} tokens")
     assert err <= TOL
     s = plan.stats()
     assert s["decode_launches" if wl.T <= 24 else "prefill_launches"] >= 1 and s["rejected_calls"] == 0
@@ -88,20 +94,32 @@ def test_workload_parity(name, sample, kernel, cache):
 
 
 # ------------------------------------------------------------------ the tensor-core kernel
-@pytest.mark.parametrize("name,sample", [("decode", None), ("spec_verify", None), ("upper_decode", None),
-                                         ("prefill", 24)])
-def test_tensor_kernel_workload_parity(name, sample, cache):
+@pytest.mark.parametrize("name", ["decode", "spec_verify", "upper_decode", "prefill"])
+def test_tensor_kernel_workload_parity(name, cache):
     wl, x, ids, w, W = workload_inputs(name, cache)
     plan, ws, y, st = run_case(wl, x, ids, w, W, kernel=binding.MOE_KERNEL_TENSOR)
     assert st == 0, binding.STATUS_NAMES.get(st)
-    tokens = list(range(wl.T)) if sample is None else sorted(
-        np.random.default_rng(7).choice(wl.T, size=sample, replace=False).tolist())
-    y_ref, _ = oracle.moe_forward(x, ids, w, weights_cpu(W, touched_experts(ids[tokens], wl.E)), tokens=tokens)
-    err = rel_err(y.cpu().numpy()[tokens], y_ref)
+    err = rel_err(y.cpu().numpy(), workload_ref(name, cache))
     print(f"{name} (tensor-core kernel): rel err {err:.3e}")
     assert err <= TOL
     s = plan.stats()
     assert s["tensor_launches"] >= 1 and s["rejected_calls"] == 0
+
+
+@pytest.mark.parametrize("kernel", [binding.MOE_KERNEL_AUTO, binding.MOE_KERNEL_REGISTER])
+def test_prefill_in_two_chunks_top16(kernel):
+    """T = 512 at top_k = 16 is two launches of 256 tokens (4096 pairs each):
+    every element of y against the oracle."""
+    wl = Workload("prefill-k16", T=512, H=1024, I=512, E=64, k=16, routing="uniform", seed=21)
+    x, ids, w = make_x(wl), make_topk_ids(wl), make_topk_w(wl)
+    W = small_weights(wl)
+    plan, ws, y, st = run_case(wl, x, ids, w, W, kernel=kernel)
+    assert st == 0, binding.STATUS_NAMES.get(st)
+    assert plan.stats()["prefill_launches"] == 2
+    y_ref, _ = oracle.moe_forward(x, ids, w, {kk: v.cpu() for kk, v in W.items()})
+    err = rel_err(y.cpu().numpy(), y_ref)
+    print(f"prefill in two chunks at top_k=16: rel err {err:.3e}")
+    assert err <= TOL
 
 
 @pytest.mark.parametrize("name", ["decode", "spec_verify"])

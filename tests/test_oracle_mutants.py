@@ -62,9 +62,10 @@ MUTANTS = {
     "group_padding_not_minus_one": ("perm[p] = -1;", "perm[p] = 0;"),
     "route_ties_to_larger_index": ("if (best < 0 || v > bv) {", "if (best < 0 || v >= bv) {"),
     "route_nan_compared_as_a_value": ("double v = isnan(lt[e]) ? -INFINITY : (double)lt[e];", "double v = (double)lt[e];"),
-    "route_sum_without_max_shift": ("sum += (m == -INFINITY) ? 0.0 : exp(sel[j] - m);",
-                                    "sum += (m == -INFINITY) ? 0.0 : exp(sel[j]);"),
-    "route_weights_not_normalised": ("(float)(exp(sel[j] - m) / sum)", "(float)(exp(sel[j] - m))"),
+    "route_sum_without_max_shift": (": exp(sel[j] - m));", ": exp(sel[j]));"),
+    "route_weights_not_normalised": ("(float)(ej / sum)", "(float)(ej)"),
+    "route_inf_winner_as_softmax": ("double ej = (m == INFINITY) ? (sel[j] == INFINITY ? 1.0 : 0.0) : exp(sel[j] - m);",
+                                    "double ej = exp(sel[j] - m);"),
     "route_ids_of_token_0": ("const float *lt = logits + (size_t)t * E;", "const float *lt = logits;"),
 }
 

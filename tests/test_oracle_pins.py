@@ -323,13 +323,17 @@ def test_route_ties_nan_and_extremes():
                    [1.0, 1.0, 1.0, 1.0, 1.0, 1.0],
                    [1000.0, 999.0, -1000.0, 998.0, 0.0, 0.0],
                    [-np.inf] * 6,
-                   [np.nan, -5.0, 0.25, np.nan, 0.5, -5.0]], np.float32)
+                   [np.nan, -5.0, 0.25, np.nan, 0.5, -5.0],
+                   [1.0, np.inf, 0.0, np.inf, 5.0, np.inf],
+                   [np.inf, -np.inf, 3.0, 2.0, 1.0, 0.0]], np.float32)
     ids, w = oracle.route(lg, 3)
-    assert ids.tolist() == [[5, 1, 2], [0, 1, 2], [0, 1, 3], [0, 1, 2], [4, 2, 1]]
+    assert ids.tolist() == [[5, 1, 2], [0, 1, 2], [0, 1, 3], [0, 1, 2], [4, 2, 1], [1, 3, 5], [0, 2, 3]]
     assert np.allclose(w[1], 1 / 3, rtol=1e-7)                     # equal logits, equal weights
     e = np.exp([0.0, -1.0, -2.0])
     assert np.allclose(w[2], e / e.sum(), rtol=2.5e-7)             # large logits: no overflow
     assert np.all(w[3] == 0.0)                                       # nothing finite to weigh
+    assert np.allclose(w[5], 1 / 3, rtol=1e-7)                       # +inf winners share the weight
+    assert w[6].tolist() == [1.0, 0.0, 0.0]                          # one +inf winner takes it all
     assert np.allclose(w[:3].astype(np.float64).sum(axis=1), 1.0, atol=1e-6)
 
 

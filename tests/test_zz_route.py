@@ -52,13 +52,32 @@ def test_route_ties_nan_and_extremes():
                    [1.0, 1.0, 1.0, 1.0, 1.0, 1.0],
                    [1000.0, 999.0, -1000.0, 998.0, 0.0, 0.0],
                    [-np.inf] * 6,
-                   [np.nan, -5.0, 0.25, np.nan, 0.5, -5.0]], np.float32)
-    wl, W, plan = _plan(5, 6, 3)
+                   [np.nan, -5.0, 0.25, np.nan, 0.5, -5.0],
+                   [1.0, np.inf, 0.0, np.inf, 5.0, np.inf],
+                   [np.inf, -np.inf, 3.0, 2.0, 1.0, 0.0]], np.float32)
+    wl, W, plan = _plan(7, 6, 3)
     ids, w = plan.route(torch.from_numpy(lg).to(DEV))
     torch.cuda.synchronize()
-    assert ids.cpu().tolist() == [[5, 1, 2], [0, 1, 2], [0, 1, 3], [0, 1, 2], [4, 2, 1]]
+    assert ids.cpu().tolist() == [[5, 1, 2], [0, 1, 2], [0, 1, 3], [0, 1, 2], [4, 2, 1], [1, 3, 5], [0, 2, 3]]
     assert bool((w[3] == 0).all())
+    assert w[6].cpu().tolist() == [1.0, 0.0, 0.0]      # a +inf winner takes the whole weight
     _check(ids, w, lg, 3)
+
+
+def test_route_refuses_mismatched_outputs():
+    """The kernel writes T*top_k ids and weights: narrower caller buffers are
+    refused on the host, before any launch."""
+    wl, W, plan = _plan(4, 16, 4)
+    lg = torch.zeros((4, 16), dtype=torch.float32, device=DEV)
+    for ids, w in ((torch.empty((4, 2), dtype=torch.int32, device=DEV), None),
+                   (None, torch.empty((4, 3), dtype=torch.float32, device=DEV)),
+                   (torch.empty((3, 4), dtype=torch.int32, device=DEV), torch.empty((3, 4), device=DEV))):
+        with pytest.raises(MoeError) as ei:
+            plan.route(lg, ids=ids, w=w)
+        assert ei.value.status == binding.MOE_ERR_INVALID_ARG
+    with pytest.raises(MoeError):
+        plan.route(torch.zeros((4, 8), dtype=torch.float32, device=DEV))    # not [T, E]
+    assert plan.stats()["route_launches"] == 0
 
 
 def test_route_is_bitwise_reproducible():
