@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define MOE_NVFP4_ABI_VERSION 3
+#define MOE_NVFP4_ABI_VERSION 4
 
 typedef enum {
     MOE_OK = 0,
@@ -79,13 +79,18 @@ typedef struct {
                 /*    the environment variable MOE_STRICT=1 forces it on          */
     int pdl;    /* 1: launch with programmatic dependent launch allowed          */
     int kernel; /* which step kernel runs moe_decode / moe_prefill:               */
-                /*   MOE_KERNEL_AUTO: per launch, the tensor-core kernel for more */
-                /*     than 8 (token, slot) pairs when the shape allows it (H and */
-                /*     I multiples of 256, I <= 4096), else the register kernel;  */
+                /*   MOE_KERNEL_AUTO: per launch, where the shape allows the      */
+                /*     tensor cores (H and I multiples of 256, I <= 4096): the    */
+                /*     small-launch tensor-core kernel for at most 4 tokens and  */
+                /*     32 (token, slot) pairs, the tensor-core ticket kernel for */
+                /*     more than 8 pairs; otherwise the register kernel;          */
                 /*   MOE_KERNEL_REGISTER: E2M1 x E4M3 dequantised in registers,   */
                 /*     fp16 mma.sync (any shape the plan accepts);                */
                 /*   MOE_KERNEL_TENSOR: tcgen05 block-scaled FP4 MMA on the        */
-                /*     NVFP4 bytes, activations as four FP4 digit rows (the plan  */
+                /*     NVFP4 bytes, activations as four FP4 digit rows: the      */
+                /*     small-launch kernel for launches it takes, else the        */
+                /*     ticket kernel (the environment variable MOE_SMALL=0 at    */
+                /*     plan creation leaves the small-launch kernel out) (the plan */
                 /*     is refused with UNSUPPORTED_SHAPE where the shape does not */
                 /*     allow it).  Its block scales must be non-negative E4M3     */
                 /*     codes (the MMA reads them unsigned), as an NVFP4 quantiser */
@@ -103,6 +108,7 @@ typedef struct {
     uint64_t rejected_calls;   /* calls that returned an error status           */
     uint64_t tensor_launches;  /* of decode + prefill: tensor-core kernel       */
     uint64_t route_launches;   /* top-k routing kernel (moe_route)              */
+    uint64_t small_launches;   /* of tensor_launches: the small-launch kernel   */
     int num_sms;               /* SMs on the plan's device (grid size)          */
     int stages;                /* shared-memory ring stages at the largest T    */
     int smem_bytes;            /* dynamic shared memory per CTA at the largest T */
@@ -265,8 +271,8 @@ moe_status_t moe_route(moe_plan_t plan, const float *logits_dev, int T, int32_t 
  * (the first set, in that order), or MOE_ERR_CUDA. */
 moe_status_t moe_check(moe_plan_t plan, void *ws_dev, void *stream);
 
-/* Test support for the failure path: set every phase-A completion counter in
- * the workspace to a value no launch reaches, so the next step's bounded
+/* Test support for the failure path: set every gate/up completion counter in
+ * the workspace (of every kernel) to a value no launch reaches, so the next step's bounded
  * dependency waits expire (after the plan's wait limit, 1 s by default or
  * MOE_WAIT_TIMEOUT_MS) and it reports MOE_ERR_TIMEOUT through moe_check
  * instead of hanging.  Re-initialise the workspace afterwards. */

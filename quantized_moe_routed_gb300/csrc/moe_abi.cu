@@ -76,6 +76,10 @@ struct moe_plan {
     int tc_rows = 0;  // digit rows of xq / hq (4 per pair, at least 64)
     int Ipad = 0;     // I rounded up to 512
     size_t off_xq = 0, off_xsf = 0, off_xmul = 0, off_hq = 0, off_hsf = 0, off_hexp = 0, off_apart = 0, off_acnt = 0;
+    // small-launch tensor-core kernel (launches of at most T_small tokens)
+    bool use_small = false;
+    int T_small = 0, smaxseg = 0, shs = 0, small_smem_attr = 0;
+    size_t off_sgdone = 0, off_sapart = 0;
     std::mutex mu;
     moe_stats_t stats{};
 };
@@ -464,6 +468,112 @@ moe_status_t run_tc(moe_plan *pl, const void *x, const int32_t *ids, const float
     return MOE_OK;
 }
 
+// Shared memory of the small-launch kernel for T tokens: the stage ring, the
+// resident x digit rows and their scales, the h digit slots and their scales,
+// the kernel's tables, the common control block and tables; NS = 0 if fewer
+// than two stages fit.
+struct SmallLayout {
+    int NS = 0, xrows = 0, off_x = 0, off_xsc = 0, off_h = 0, off_hsc = 0, off_scr = 0, tab_off = 0, total = 0;
+};
+SmallLayout small_layout(const moe_plan *pl, int T)
+{
+    SmallLayout L;
+    const int KC = pl->d.H / 256, KCI = pl->d.I / 256, P = T * pl->d.top_k;
+    L.xrows = T <= 2 ? 8 : 16;
+    // rows 8-15 of the last chunk are read (and ignored) when a chunk holds 8 rows
+    const int xbytes = KC * L.xrows * 128 + (L.xrows == 8 ? 1024 : 0);
+    const int hbytes = pl->shs * KCI * 2048, hsbytes = pl->shs * KCI * 256;
+    const int rest = up1024(xbytes) + up1024(KC * 256) + hbytes + static_cast<int>(up(hsbytes, 16)) +
+                     moe::kSmScrBytes + 128 + moe::tab_bytes_for(P, T) + 1024;
+    int ns = (pl->smem_optin - rest) / moe::kSmStage;
+    if (ns > moe::kMaxStages) ns = moe::kMaxStages;
+    if (ns < 2) return L;
+    L.NS = ns;
+    L.off_x = ns * moe::kSmStage;
+    L.off_xsc = L.off_x + up1024(xbytes);
+    L.off_h = L.off_xsc + up1024(KC * 256);
+    L.off_hsc = L.off_h + hbytes;
+    L.off_scr = static_cast<int>(up(L.off_hsc + hsbytes, 16));
+    L.tab_off = static_cast<int>(up(L.off_scr + moe::kSmScrBytes, 128));
+    L.total = L.tab_off + moe::tab_bytes_for(P, T) + 1024;
+    return L;
+}
+
+// The small-launch tensor-core kernel over T <= T_small tokens (one launch).
+moe_status_t run_small(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, int T, void *ws,
+                       cudaStream_t cs, Path path)
+{
+    {
+        std::lock_guard<std::mutex> lk(pl->mu);
+        if (pl->small_smem_attr == 0) {
+            cudaError_t e = moe::set_small_smem_limit(pl->smem_optin);
+            if (e != cudaSuccess) {
+                pl->stats.rejected_calls++;
+                return fail(MOE_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            }
+            pl->small_smem_attr = pl->smem_optin;
+        }
+    }
+    const SmallLayout L = small_layout(pl, T);
+    if (L.NS < 2 || L.total > pl->small_smem_attr) {
+        reject(pl);
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "small-launch kernel: shared memory does not fit (%d stages)", L.NS);
+    }
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    const moe_plan_desc &d = pl->d;
+    moe::KernelParams p{};
+    p.gts = d.gate_ts_dev;
+    p.uts = d.up_ts_dev;
+    p.dts = d.down_ts_dev;
+    p.ctrl = reinterpret_cast<uint32_t *>(wsb);
+    p.cnt = reinterpret_cast<uint32_t *>(wsb + pl->off_cnt);
+    p.part = reinterpret_cast<float *>(wsb + pl->off_part);
+    p.sgdone = reinterpret_cast<uint32_t *>(wsb + pl->off_sgdone);
+    p.sapart = reinterpret_cast<float *>(wsb + pl->off_sapart);
+    p.H = d.H;
+    p.I = d.I;
+    p.E = d.E;
+    p.k = d.top_k;
+    p.T = T;
+    p.Pmax = pl->Tc * d.top_k;
+    p.timeout_ns = pl->timeout_ns;
+    for (int i = 0; i < 6; ++i) p.tmt[i] = pl->tmw[i];
+    p.x = static_cast<const uint16_t *>(x);
+    p.ids = ids;
+    p.w = w;
+    p.y = y;
+    p.NS = L.NS;
+    p.NSF = L.NS < 7 ? L.NS : 7;  // (512 - 64 accumulator columns) / 64 per slot
+    p.stage_bytes = moe::kSmStage;
+    p.tab_off = L.tab_off;
+    p.smaxseg = pl->smaxseg;
+    p.sxrows = L.xrows;
+    p.shs = pl->shs;
+    p.s_off_x = L.off_x;
+    p.s_off_xsc = L.off_xsc;
+    p.s_off_h = L.off_h;
+    p.s_off_hsc = L.off_hsc;
+    p.s_off_scr = L.off_scr;
+    cudaError_t e = moe::launch_small(p, pl->num_sms, L.total, pl->pdl, cs);
+    if (e != cudaSuccess) {
+        reject(pl);
+        return fail(MOE_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+    }
+    {
+        std::lock_guard<std::mutex> lk(pl->mu);
+        if (path == Path::Prefill) pl->stats.prefill_launches++;
+        else pl->stats.decode_launches++;
+        pl->stats.tensor_launches++;
+        pl->stats.small_launches++;
+    }
+    if (!env_flag("MOE_QUIET"))
+        std::call_once(g_active_once, [&] {
+            std::fprintf(stderr, "moe_nvfp4: sm_103a routed-experts small-launch tensor-core kernel ACTIVE (%d SMs)\n",
+                         pl->num_sms);
+        });
+    return MOE_OK;
+}
+
 moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, int T, void *ws,
                       void *stream, Path path, const WsOffsets *wo = nullptr)
 {
@@ -498,6 +608,10 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
     // bytes per expert for the tensor-core pipeline's fixed latencies, and the
     // register kernel is faster there (measured: 30.6 vs 52.7 us at T = 1,
     // 192 vs 154 us at T = 16, 330 vs 226 us at T = 24)
+    // launches of at most T_small tokens (the single-token decode) take the
+    // small-launch tensor-core kernel whenever the tensor cores may be used
+    if (pl->use_small && path != Path::Null && !wo && T <= pl->T_small)
+        return run_small(pl, x, ids, w, y, T, ws, static_cast<cudaStream_t>(stream), path);
     if (pl->use_tc && path != Path::Null && !wo &&
         (pl->d.kernel == MOE_KERNEL_TENSOR || T * pl->d.top_k > 8))
         return run_tc(pl, x, ids, w, y, T, ws, static_cast<cudaStream_t>(stream), path);
@@ -817,6 +931,25 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
         o = up(o + static_cast<size_t>(moe::kTcApartUnits) * 2 * 16 * moe::kTcRows * 4, 256);
         pl->off_acnt = o;
         o = up(o + static_cast<size_t>(moe::kTcApartUnits) * 4, 256);
+        // the small-launch kernel: its shares follow from the SM count and the
+        // largest launch it takes (T_small tokens, at most min(T_small * k, E)
+        // active experts and T_small * k down groups)
+        const int ts = std::min(std::min(d.T_max, moe::kSmMaxT), moe::kSmMaxPairs / d.top_k);
+        if (ts >= 1 && !(std::getenv("MOE_SMALL") && std::strcmp(std::getenv("MOE_SMALL"), "0") == 0)) {
+            const long G = sms, KC = d.H / 256, TI = d.I / 128, TO = d.H / 128, Ps = static_cast<long>(ts) * d.top_k;
+            const long NA = std::min<long>(Ps, d.E) * TI * KC, NB = Ps * TO;
+            const long LA = (NA + G - 1) / G, LB = (NB + G - 1) / G;
+            pl->smaxseg = static_cast<int>((LA - 1) / KC + 2);
+            pl->shs = static_cast<int>((LB - 1) / TO + 2);
+            pl->T_small = ts;
+            if (pl->shs <= moe::kSmMaxHSlots && small_layout(pl, ts).NS >= 2) {
+                pl->use_small = true;
+                pl->off_sgdone = o;
+                o = up(o + 4 * static_cast<size_t>(moe::kSmMaxPairs), 256);
+                pl->off_sapart = o;
+                o = up(o + static_cast<size_t>(G) * pl->smaxseg * moe::kSmSlot * 4, 256);
+            }
+        }
     }
     pl->ws_bytes = o;
     pl->stats.num_sms = sms;
@@ -1084,6 +1217,9 @@ moe_status_t moe_debug_poison_workspace(moe_plan_t plan, void *ws_dev, void *str
     if (!aligned(ws_dev, 256)) return fail(MOE_ERR_MISALIGNED, "workspace must be 256-byte aligned");
     cudaError_t e = moe::launch_poison(reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws_dev) + plan->off_done),
                                        moe::kMaxPairs, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess && plan->use_small)
+        e = moe::launch_poison(reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws_dev) + plan->off_sgdone),
+                               moe::kSmMaxPairs, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "poison launch: %s", cudaGetErrorString(e));
     return MOE_OK;
 }

@@ -494,6 +494,24 @@ __device__ __forceinline__ bool warp_spin(const KernelParams &p, Pred pred, vola
     return __all_sync(0xffffffffu, ok);
 }
 
+// Bounded spin of a single thread until pred(); false on abort or timeout.
+template <class Pred>
+__device__ bool spin_one(const KernelParams &p, Pred pred, volatile int *abort_flag)
+{
+    if (pred()) return true;
+    const uint64_t t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        if (pred()) return true;
+        if ((it & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
+                raise_error(p, abort_flag, kErrTimeout);
+                return false;
+            }
+        }
+    }
+}
+
 // Hand a finished ticket to the release warp: slot = ticket sequence number.
 // The warp's global stores (and, through the acq_rel ticket counter or the
 // epilogue's barrier, those of the other warps) precede the release; the

@@ -107,6 +107,14 @@ struct KernelParams {
     int tq_depth;       // tickets the helper fetches ahead of the producer (1 .. 4)
     int Ipad;           // I rounded up to 512
     int xtok;           // 1: x digit rows per token (gate/up MMAs take all tokens, T <= 16); 0: per sorted pair
+
+    // ---- small-launch tensor-core path (moe_small.cu) ----
+    float *sapart;      // [grid * smaxseg][2][kSmMaxT][128] gate / up partial sums of each (CTA, unit) segment
+    uint32_t *sgdone;   // [kSmMaxPairs] per active expert: gate/up atoms finished (reset by the last CTA)
+    int smaxseg;        // partial-sum slots per CTA (units one CTA's atom range can touch)
+    int sxrows;         // rows of one 256-element chunk of the resident x digits (8: T <= 2, 16: T <= 4)
+    int shs;            // h digit slots (down groups one CTA's unit range can touch)
+    int s_off_x, s_off_xsc, s_off_xmul, s_off_h, s_off_hsc, s_off_hmul, s_off_scr;  // shared-memory offsets
 };
 
 // Dynamic shared memory layout of the persistent kernel for P pairs.
@@ -132,6 +140,21 @@ inline int tc_stage_bytes(int N)
 }
 cudaError_t launch_tc(const KernelParams &p, int grid, int smem_bytes, bool pdl, cudaStream_t st);
 cudaError_t set_tc_smem_limit(int bytes);
+
+// Small-launch tensor-core path (moe_small.cu): launches of at most kSmMaxT
+// tokens and kSmMaxPairs pairs.  Every CTA quantises x into resident FP4 digit
+// rows, takes a fixed share of the gate/up atoms (128 rows x 256 elements of
+// gate and of up) and of the down units (128 rows x all of I), and builds the
+// h digit rows of its down groups itself from the gate/up partial sums.
+constexpr int kSmMaxT = 4;          // four digit rows per token: gate/up MMA N = 16
+constexpr int kSmMaxPairs = 32;     // one warp groups the pairs
+constexpr int kSmGroup = 4;         // pairs per down group: down MMA N = 16
+constexpr int kSmStage = 36864;     // two 128 x 256 E2M1 tiles and their scales
+constexpr int kSmSlot = 2 * kSmMaxT * 128;  // floats per partial-sum slot
+constexpr int kSmScrBytes = 512;    // the kernel's private shared tables
+constexpr int kSmMaxHSlots = 8;     // h digit slots a CTA can hold
+cudaError_t launch_small(const KernelParams &p, int grid, int smem_bytes, bool pdl, cudaStream_t st);
+cudaError_t set_small_smem_limit(int bytes);
 
 // moe_route.cu: top-k routing, one warp per token (E <= 1024, k <= min(16, E))
 cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w, bool pdl,

@@ -1,0 +1,786 @@
+// moe_small.cu -- sm_103a tensor-core kernel of the routed-experts MoE step for
+// small launches (T <= 4 tokens, T*k <= 32 pairs: the single-token decode):
+//   y_t = sum_j w_tj * W_down[e_tj] ( SiLU(W_gate[e_tj] x_t) (.) (W_up[e_tj] x_t) )
+// with every weight byte consumed by the block-scaled FP4 MMA straight from its
+// NVFP4 encoding (tcgen05.mma kind::mxf4nvf4, scale_vec::4X) and activations
+// entering as four FP4 "digit" rows each (moe_tcgen05.cuh).
+//
+// A single token streams only ~370 KB of expert weights per SM, so what limits
+// the step is latency, not bandwidth: every dependent round trip through global
+// memory costs about a microsecond against a ~8.5 us weight stream.  The
+// schedule is built to have as few of them as possible on the critical path:
+//
+//  * Static shares instead of tickets.  After grouping (every CTA, one warp),
+//    each CTA knows its share of the work from closed-form arithmetic: a
+//    contiguous range of gate/up ATOMS -- (active expert, 128-row tile, 256-
+//    element K chunk): 128 gate rows and the same 128 up rows, 36 KB -- and a
+//    contiguous range of down UNITS -- (group, 128-row tile of H) over all of
+//    I.  No atomic hands out work, so every CTA starts streaming at once.
+//  * Local x digits.  Every CTA quantises the T tokens' x into resident FP4
+//    digit rows in its own shared memory while its first weight copies are in
+//    flight; the gate/up MMAs read them there (no publish round trip).
+//  * Down weights in flight early.  A CTA's down stages follow its gate/up
+//    atoms in the same ring, so they are issued as soon as ring slots free up,
+//    long before the h they multiply exists; when h arrives the weights are
+//    already on chip.
+//  * h built where it is used.  A gate/up segment (the atoms of one tile a CTA
+//    holds) leaves its fp32 partial sums for the T tokens in the workspace and
+//    adds its atom count to its expert's counter (one release).  The CTA that
+//    holds a down group waits for that counter, sums the partials of every
+//    segment in K order, applies SiLU(g) * u and quantises the pair's whole h
+//    row into digit rows in its own shared memory: one round trip, no
+//    last-arriver chain, and the pair's prescale is known for the whole row.
+//  * The slot-ordered combine of the per-pair down outputs is the one the
+//    other kernels use (moe_device.cuh): bitwise reproducible.
+//
+// Warp roles (12 warps): 0-3 move block scales into tensor memory per stage;
+// 4-7 read accumulators (gate/up partials, h builds, down outputs); 8 issues
+// TMA copies; 9 allocates tensor memory and issues the MMAs; 11 publishes
+// finished down units and lists combines; every warp first helps with the
+// prologue (warps 0-7: x digits; 8-11: grouping) and at the end with the
+// combines.  Every wait is bounded (globaltimer); on expiry the CTA raises the
+// workspace error word, drains its copies and frees tensor memory.
+#include "moe_internal.h"
+
+#include <cuda_fp16.h>
+
+namespace moe {
+namespace {
+
+#include "moe_device.cuh"
+#include "moe_tcgen05.cuh"
+
+constexpr int kOffW0 = 0, kOffW1 = 16384, kOffS0 = 32768, kOffS1 = 34816;  // stage sub-buffers
+constexpr int kTmemCols = 512;
+// tensor memory: two accumulator buffers of 32 columns (gate at +0, up at +16;
+// a down unit uses +0), then NSF scale-factor slots of 64 columns from column
+// 64: sets at +0 (gate or first down chunk), +16 (up or second down chunk),
+// +32 (activation scales of the first chunk), +48 (of the second)
+constexpr int kAccCols = 32;
+constexpr int kSfBase = 2 * kAccCols;
+
+// Kernel-private tables in shared memory (at p.s_off_scr).
+struct SmTabs {
+    int nE;                       // active experts (distinct valid ids)
+    int xready;                   // resident x digits complete (release)
+    int hready[kSmMaxHSlots];     // per h slot: the group's digit rows are built (release)
+    int hexp[kSmMaxHSlots][kSmGroup];  // per h slot and pair: the h row's prescale exponent
+    float red[4];                 // epilogue warps' partial maxima
+    int16_t gae[kSmMaxPairs];     // group -> active expert index
+    int16_t aexp[kSmMaxPairs];    // active expert index -> expert id
+    float xmul[kSmMaxT][4];       // per token and digit: 2^-(prescale + 2 digit)
+    int xe[kSmMaxT];              // per token: the x row's prescale exponent
+};
+static_assert(sizeof(SmTabs) <= kSmScrBytes, "kernel tables too large");
+
+// The static shares.  Atoms a = (ae * TI + i) * KC + c (ae active expert, i
+// 128-row tile of I, c 256-element chunk of H); units b = g * TO + o (g down
+// group, o 128-row tile of H).  CTA j holds atoms [alo(j), alo(j+1)) and units
+// [ulo(j), ulo(j+1)).
+struct SmShape {
+    int TI, KC, TO, KCI, nPB, NA, NB, ng, nE;
+};
+__device__ __forceinline__ int sm_lo(int j, int n, int G) { return static_cast<int>(static_cast<long long>(j) * n / G); }
+// The CTA whose atom range holds atom a (the largest j with alo(j) <= a).
+__device__ __forceinline__ int sm_cta_of(int a, int n, int G)
+{
+    return static_cast<int>((static_cast<long long>(a + 1) * G + n - 1) / n) - 1;
+}
+__device__ __forceinline__ SmShape sm_shape(const KernelParams &p, int ng, int nE)
+{
+    SmShape s;
+    s.TI = p.I / 128;
+    s.KC = p.H / 256;
+    s.TO = p.H / 128;
+    s.KCI = p.I / 256;
+    s.nPB = (s.KCI + 1) / 2;
+    s.NA = nE * s.TI * s.KC;
+    s.NB = ng * s.TO;
+    s.ng = ng;
+    s.nE = nE;
+    return s;
+}
+
+__device__ __forceinline__ void grp8_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }   // warps 8-11
+__device__ __forceinline__ void lo8_sync() { asm volatile("bar.sync 2, 256;" ::: "memory"); }    // warps 0-7
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Byte offset of byte jb (0..127) of digit row n inside one 256-element chunk
+// of a resident digit block: 128-byte rows, eight-row atoms of 1024 bytes, the
+// 16-byte granules of row n XOR-swizzled by n % 8 -- the K-major 128-byte
+// swizzle layout the MMA's shared-memory descriptors describe.
+__device__ __forceinline__ int sw128_off(int n, int jb)
+{
+    return (n >> 3) * 1024 + (n & 7) * 128 + ((((jb >> 4) ^ (n & 7)) << 4) | (jb & 15));
+}
+
+// ------------------------------------------------------------------ prologue
+// Warps 8-11: group the pairs (one warp, groups of at most kSmGroup pairs),
+// list the active experts, count each token's valid slots and zero the y rows
+// of tokens with none.  Publishes hd->grouped.
+__device__ void sm_group(const KernelParams &p, Tabs tb, SmTabs *sx)
+{
+    SmemHdr *hd = tb.hdr;
+    const int lt = threadIdx.x - 256, P = p.T * p.k;
+    if (lt < 32) {
+        group_pairs_warp(p, P, kSmGroup, tb);
+        __syncwarp();
+        const int lane = lt, ng = hd->n_groups;
+        const int ge = lane < ng ? tb.gexp[lane] : -1;
+        const int gprev = __shfl_up_sync(0xffffffffu, ge, 1);
+        const bool fresh = lane < ng && (lane == 0 || gprev != ge);
+        const uint32_t m = __ballot_sync(0xffffffffu, fresh);
+        if (lane < ng) {
+            const int ae = __popc(m & (0xffffffffu >> (31 - lane))) - 1;
+            sx->gae[lane] = static_cast<int16_t>(ae);
+            if (fresh) sx->aexp[ae] = static_cast<int16_t>(ge);
+        }
+        if (lane == 0) sx->nE = __popc(m);
+    }
+    grp8_sync();
+    for (int t = lt; t < p.T; t += 128) {
+        int v = 0;
+        for (int j = 0; j < p.k; ++j) v += (tb.pos[t * p.k + j] != 0xFFFFu);
+        tb.kvalid[t] = static_cast<uint8_t>(v);
+    }
+    grp8_sync();
+    if (blockIdx.x == 0 && lt == 0 && hd->n_bad) atomicOr(p.ctrl + 2, kErrBadId);
+    for (int t = blockIdx.x; t < p.T; t += gridDim.x)
+        if (tb.kvalid[t] == 0)
+            for (int r = lt; r < p.H; r += 128) p.y[static_cast<size_t>(t) * p.H + r] = 0.f;
+    grp8_sync();
+    if (lt == 0) st_rel_cta(&hd->grouped, 1);
+}
+
+// Warps 0-7: the T tokens' x as four FP4 digit rows each (rows 4t .. 4t+3),
+// resident for the whole launch: per token one power-of-two prescale (largest
+// |x| into (1344, 2688]), per 16-element block four digits (quant_block4),
+// written in the MMA's swizzled layout, chunk c at s_off_x + c * sxrows * 128;
+// block scales at s_off_xsc as [chunk][16 rows][16 bytes]; the digit
+// multipliers 2^-(prescale + 2 j) in sx->xmul.  Publishes sx->xready.
+__device__ void sm_quantize_x(const KernelParams &p, uint8_t *smem, SmTabs *sx)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int *xe = sx->xe;
+    if (warp < p.T) {
+        const uint16_t *src = p.x + static_cast<size_t>(warp) * p.H;
+        float amax = 0.f;
+        for (int v = lane; v < p.H / 8; v += 32) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(src + 8 * v);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xffff0000u))));
+        }
+#pragma unroll
+        for (int d = 16; d; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+        if (lane == 0) xe[warp] = prescale_exp(amax);
+    }
+    lo8_sync();
+    if (tid < 4 * p.T) {
+        const int t = tid >> 2, j = tid & 3;
+        sx->xmul[t][j] = mul_pow2(1.f, -xe[t] - 2 * j);
+    }
+    uint8_t *xd = smem + p.s_off_x, *xs = smem + p.s_off_xsc;
+    const int nb = p.H / 16, cstride = p.sxrows * 128;
+    for (int bi = tid; bi < p.T * nb; bi += 256) {
+        const int t = bi / nb, b = bi - t * nb;
+        const uint16_t *src = p.x + static_cast<size_t>(t) * p.H + 16 * b;
+        const uint4 u0 = *reinterpret_cast<const uint4 *>(src);
+        const uint4 u1 = *reinterpret_cast<const uint4 *>(src + 8);
+        const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        const float P = mul_pow2(1.f, xe[t]);
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16) * P;
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u) * P;
+        }
+        uint2 pk[4];
+        uint32_t sc[4];
+        quant_block4(v, pk, sc);
+        const int c = b >> 4, bb = b & 15;
+#pragma unroll
+        for (int d = 0; d < 4; ++d) {
+            const int n = 4 * t + d;
+            *reinterpret_cast<uint2 *>(xd + c * cstride + sw128_off(n, 8 * bb)) = pk[d];
+            xs[c * 256 + n * 16 + bb] = static_cast<uint8_t>(sc[d]);
+        }
+    }
+    fence_async_smem();  // the MMA (async proxy) reads the digit rows
+    lo8_sync();
+    if (tid == 0) st_rel_cta(&sx->xready, 1);
+}
+
+// ------------------------------------------------------------------ stage sequence
+// A CTA's ring carries its atoms a0 .. a1-1, then for each of its units
+// b0 .. b1-1 the nPB down stages (two 256-element chunks of I each, the last
+// one possibly one).  Stage headers: {KIND_A, atom, 0, 0} or {KIND_B, unit,
+// part, 0}; END closes the sequence.
+
+// Producer (warp 8, lane 0): waits for a free stage, then the TMA copies.
+__device__ void sm_producer(const KernelParams &p, uint8_t *smem, Tabs tb, const SmTabs *sx, const SmShape &sh,
+                            volatile int *abort_flag)
+{
+    if ((threadIdx.x & 31) != 0) return;
+    SmemHdr *hd = tb.hdr;
+    const uint64_t pol = policy_evict_first();
+    const int G = gridDim.x, j = blockIdx.x;
+    const int a0 = sm_lo(j, sh.NA, G), a1 = sm_lo(j + 1, sh.NA, G);
+    const int b0 = sm_lo(j, sh.NB, G), b1 = sm_lo(j + 1, sh.NB, G);
+    int s = 0, fill = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    auto next_stage = [&]() -> bool {
+        if (!wait_bar(&hd->empty[s], ph ^ 1u, p, abort_flag)) return false;
+        return true;
+    };
+    auto advance = [&]() {
+        ++fill;
+        if (++s == p.NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+    };
+    for (int a = a0; a < a1 && ok; ++a) {
+        if (!(ok = next_stage())) break;
+        const int u = a / sh.KC, c = a - u * sh.KC, ae = u / sh.TI, i = u - ae * sh.TI;
+        const int row = sx->aexp[ae] * p.I + i * 128;
+        uint8_t *st = smem + s * p.stage_bytes;
+        uint64_t *bar = &hd->full[s];
+        hd->stage_hdr[s] = make_int4(KIND_A, a, 0, 0);
+        mbar_expect_tx(bar, static_cast<uint32_t>(kSmStage));
+        tma2d(st + kOffW0, &p.tmt[0], c * 128, row, bar, pol);
+        tma2d(st + kOffW1, &p.tmt[1], c * 128, row, bar, pol);
+        tma2d(st + kOffS0, &p.tmt[3], c * 16, row, bar, pol);
+        tma2d(st + kOffS1, &p.tmt[4], c * 16, row, bar, pol);
+        advance();
+    }
+    for (int b = b0; b < b1 && ok; ++b) {
+        const int g = b / sh.TO, o = b - g * sh.TO;
+        const int row = tb.gexp[g] * p.H + o * 128;
+        for (int part = 0; part < sh.nPB; ++part) {
+            if (!(ok = next_stage())) break;
+            const int c0 = 2 * part, two = c0 + 1 < sh.KCI;
+            uint8_t *st = smem + s * p.stage_bytes;
+            uint64_t *bar = &hd->full[s];
+            hd->stage_hdr[s] = make_int4(KIND_B, b, part, 0);
+            mbar_expect_tx(bar, static_cast<uint32_t>((two ? 2 : 1) * (16384 + 2048)));
+            tma2d(st + kOffW0, &p.tmt[2], c0 * 128, row, bar, pol);
+            tma2d(st + kOffS0, &p.tmt[5], c0 * 16, row, bar, pol);
+            if (two) {
+                tma2d(st + kOffW1, &p.tmt[2], (c0 + 1) * 128, row, bar, pol);
+                tma2d(st + kOffS1, &p.tmt[5], (c0 + 1) * 16, row, bar, pol);
+            }
+            advance();
+        }
+    }
+    if (ok && next_stage()) {
+        hd->stage_hdr[s] = make_int4(KIND_END, 0, 0, 0);
+        mbar_arrive(&hd->full[s]);
+        ++fill;
+    } else {
+        *abort_flag = 1;
+    }
+    hd->fill_cnt = fill;
+}
+
+// The h slot of down group g for this CTA (its first group is slot 0).
+__device__ __forceinline__ int sm_hslot(int g, const SmShape &sh)
+{
+    return g - sm_lo(blockIdx.x, sh.NB, gridDim.x) / sh.TO;
+}
+
+// Scale warps (0-3): per stage, the weight tiles' block scales (row r = lane
+// 32q + lane) and the activation digit rows' block scales go to the stage's
+// tensor-memory slot in the layout the block-scaled MMA reads (see
+// tc_st_set / tc_st_bset); rows past the activation's digit rows get zero
+// scales.  A down stage's activation scales are its group's h digit scales,
+// which exist once the group's h slot is marked built.
+__device__ void sm_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb, SmTabs *sx, const SmShape &sh,
+                              volatile int *abort_flag)
+{
+    SmemHdr *hd = tb.hdr;
+    const int q = threadIdx.x >> 5, lane = threadIdx.x & 31, r = 32 * q + lane;
+    const uint32_t sfbase = hd->tmem_base + (static_cast<uint32_t>(32 * q) << 16) + kSfBase;
+    auto row = [&](const uint8_t *b, int i) { return *reinterpret_cast<const uint4 *>(b + 16 * i); };
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    int s = 0, n = 0, slot = 0, ms = 0;
+    uint32_t ph = 0, mph = 0;
+    for (;;) {
+        if (!warp_wait_bar(p, &hd->full[s], ph, abort_flag)) break;
+        const int4 h = hd->stage_hdr[s];
+        const uint8_t *st = smem + s * p.stage_bytes;
+        if (h.x != KIND_END) {
+            if (n >= p.NSF) {  // the slot's previous stage's MMAs have completed
+                if (!warp_wait_bar(p, &hd->empty[ms], mph, abort_flag)) break;
+                if (++ms == p.NS) {
+                    ms = 0;
+                    mph ^= 1u;
+                }
+            }
+            const uint32_t col = sfbase + 64u * static_cast<uint32_t>(slot);
+            tc_st_set(col + 0, row(st + kOffS0, r));
+            if (h.x == KIND_A) {
+                tc_st_set(col + 16, row(st + kOffS1, r));
+                const int c = h.y % sh.KC;
+                const uint4 b0 = lane < 4 * p.T ? row(smem + p.s_off_xsc + c * 256, lane) : z;
+                tc_st_bset(col + 32, b0, z, z, z);
+            } else {
+                const int g = h.y / sh.TO, hs = sm_hslot(g, sh), c0 = 2 * h.z;
+                if (!warp_spin(p, [&] { return ld_acq_cta(&sx->hready[hs]) != 0; }, abort_flag)) break;
+                const int rows = 4 * tb.gcnt[g];
+                const uint8_t *hsc = smem + p.s_off_hsc + hs * (sh.KCI * 256);
+                tc_st_bset(col + 32, lane < rows ? row(hsc + c0 * 256, lane) : z, z, z, z);
+                if (c0 + 1 < sh.KCI) {
+                    tc_st_set(col + 16, row(st + kOffS1, r));
+                    tc_st_bset(col + 48, lane < rows ? row(hsc + (c0 + 1) * 256, lane) : z, z, z, z);
+                }
+            }
+            tc_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hd->sfready[s]);
+        if (h.x == KIND_END) break;
+        ++n;
+        if (++slot == p.NSF) slot = 0;
+        if (++s == p.NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+}
+
+// MMA thread (warp 9, lane 0).  Gate/up atom: four K steps of 64 into the
+// gate and the up accumulator (B = the resident x digits of the atom's
+// chunk); down stage: four K steps per chunk into one accumulator (B = the
+// group's h digits).  Accumulator buffers alternate per segment / unit, in
+// the same order the epilogue reads them.
+__device__ void sm_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb, SmTabs *sx, const SmShape &sh,
+                            volatile int *abort_flag)
+{
+    SmemHdr *hd = tb.hdr;
+    const uint32_t tbase = hd->tmem_base, idesc = fp4_idesc(16);
+    const int G = gridDim.x, j = blockIdx.x;
+    const int a0 = sm_lo(j, sh.NA, G), a1 = sm_lo(j + 1, sh.NA, G);
+    int s = 0, nt = 0, slot = 0;
+    uint32_t ph = 0;
+    const uint32_t xdesc = smem_u32(smem + p.s_off_x), xstride = static_cast<uint32_t>(p.sxrows * 128);
+    for (;;) {
+        if (!wait_bar(&hd->sfready[s], ph, p, abort_flag)) break;
+        tc_fence_after();
+        const int4 h = hd->stage_hdr[s];
+        if (h.x == KIND_END) break;
+        bool first, last;
+        if (h.x == KIND_A) {
+            const int c = h.y % sh.KC;
+            first = h.y == a0 || c == 0;
+            last = h.y == a1 - 1 || c == sh.KC - 1;
+        } else {
+            first = h.z == 0;
+            last = h.z == sh.nPB - 1;
+        }
+        const int buf = nt & 1, used = nt >> 1;
+        if (first && used > 0) {
+            if (!wait_bar(&hd->accempty[buf], static_cast<uint32_t>((used - 1) & 1), p, abort_flag)) break;
+            tc_fence_after();
+        }
+        const uint64_t d0 = sw128_desc(smem_u32(smem + s * p.stage_bytes));
+        const uint32_t sfc = tbase + kSfBase + 64u * static_cast<uint32_t>(slot);
+        const uint32_t dcol = tbase + static_cast<uint32_t>(buf * kAccCols);
+        if (h.x == KIND_A) {
+            const int c = h.y % sh.KC;
+            const uint64_t bd = sw128_desc(xdesc + static_cast<uint32_t>(c) * xstride);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
+                tc_mma(dcol, d0 + (kOffW0 + 32 * kk) / 16, bd + 2 * kk, idesc, sfc + 4 * kk, sfc + 32 + 4 * kk, acc);
+                tc_mma(dcol + 16, d0 + (kOffW1 + 32 * kk) / 16, bd + 2 * kk, idesc, sfc + 16 + 4 * kk,
+                       sfc + 32 + 4 * kk, acc);
+            }
+        } else {
+            const int g = h.y / sh.TO, hs = sm_hslot(g, sh), c0 = 2 * h.z;
+            const uint32_t hb = smem_u32(smem + p.s_off_h + hs * (sh.KCI * 2048));
+            const int nch = c0 + 1 < sh.KCI ? 2 : 1;
+            for (int kr = 0; kr < nch; ++kr) {
+                const uint64_t bd = sw128_desc(hb + static_cast<uint32_t>((c0 + kr) * 2048));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t acc = (!first || kr > 0 || kk > 0) ? 1u : 0u;
+                    tc_mma(dcol, d0 + ((kr ? kOffW1 : kOffW0) + 32 * kk) / 16, bd + 2 * kk, idesc,
+                           sfc + 16 * kr + 4 * kk, sfc + 32 + 16 * kr + 4 * kk, acc);
+                }
+            }
+        }
+        tc_commit(&hd->empty[s]);
+        if (last) {
+            tc_commit(&hd->accfull[buf]);
+            ++nt;
+        }
+        if (++slot == p.NSF) slot = 0;
+        if (++s == p.NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+    // every MMA issued must complete before the CTA frees tensor memory
+    tc_commit(&hd->mma_done);
+    int no_abort = 0;
+    wait_bar(&hd->mma_done, 0u, p, &no_abort);
+}
+
+// ------------------------------------------------------------------ epilogue warps
+// Warps 4-7; warp 4+q reads accumulator lanes (rows) 32q .. 32q+31.
+//   1. each gate/up segment of the CTA, in order: per token the four digit
+//      columns of gate and of up, summed with the token's digit multipliers,
+//      times the tensor scales -> the segment's partial-sum slot; then one
+//      release adds the segment's atom count to its expert's counter;
+//   2. for each down group of the CTA, in order: build its h digit rows (wait
+//      for the expert's counter, sum every segment's partials in K order,
+//      h = SiLU(g) * u, one prescale for the pair's whole row, four digits per
+//      16-element block), then the down units of the group: per pair the four
+//      digit columns -> the pair's output rows (fp32), handed to the release
+//      warp for the slot-ordered combine.
+template <int RND>
+__device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb, SmTabs *sx, const SmShape &sh,
+                            volatile int *abort_flag)
+{
+    SmemHdr *hd = tb.hdr;
+    const int q = (threadIdx.x >> 5) - 4, lane = threadIdx.x & 31, r = 32 * q + lane, th = threadIdx.x - 128;
+    const uint32_t lanebase = hd->tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+    const int G = gridDim.x, j = blockIdx.x;
+    const int a0 = sm_lo(j, sh.NA, G), a1 = sm_lo(j + 1, sh.NA, G);
+    const int b0 = sm_lo(j, sh.NB, G), b1 = sm_lo(j + 1, sh.NB, G);
+    const int need = sh.TI * sh.KC;  // atoms of one expert
+    int nt = 0, nsync = 0, npush = 0;
+    bool ok = true;
+    auto epi_sync = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hd->epibar);
+        const bool w = warp_wait_bar(p, &hd->epibar, static_cast<uint32_t>(nsync & 1), abort_flag);
+        ++nsync;
+        return w;
+    };
+    auto take_acc = [&]() -> bool {  // wait for the next accumulator buffer
+        const int buf = nt & 1, used = nt >> 1;
+        if (!warp_wait_bar(p, &hd->accfull[buf], static_cast<uint32_t>(used & 1), abort_flag)) return false;
+        tc_fence_after();
+        return true;
+    };
+    auto give_acc = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hd->accempty[nt & 1]);
+        ++nt;
+    };
+
+    // 1. gate/up segments
+    for (int u = a1 > a0 ? a0 / sh.KC : 0; ok && a1 > a0 && u <= (a1 - 1) / sh.KC; ++u) {
+        if (!(ok = take_acc())) break;
+        const uint32_t dcol = lanebase + static_cast<uint32_t>((nt & 1) * kAccCols);
+        float4 dg[kSmMaxT], du[kSmMaxT];
+#pragma unroll
+        for (int t = 0; t < kSmMaxT; ++t)
+            if (t < p.T) {
+                tc_ld4(dcol + 4 * t, dg[t]);
+                tc_ld4(dcol + 16 + 4 * t, du[t]);
+            }
+        tc_wait_ld();
+        give_acc();
+        const int ae = u / sh.TI, e = sx->aexp[ae];
+        const float tg = __ldg(p.gts + e), tu = __ldg(p.uts + e);
+        float *slot = p.sapart + (static_cast<size_t>(j) * p.smaxseg + (u - a0 / sh.KC)) * kSmSlot;
+#pragma unroll
+        for (int t = 0; t < kSmMaxT; ++t)
+            if (t < p.T) {
+                const float *m = sx->xmul[t];
+                slot[(0 * kSmMaxT + t) * 128 + r] = (dg[t].x * m[0] + dg[t].y * m[1] + dg[t].z * m[2] + dg[t].w * m[3]) * tg;
+                slot[(1 * kSmMaxT + t) * 128 + r] = (du[t].x * m[0] + du[t].y * m[1] + du[t].z * m[2] + du[t].w * m[3]) * tu;
+            }
+        __threadfence();
+        if (!(ok = epi_sync())) break;
+        if (th == 0) {
+            const int lo = max(a0, u * sh.KC), hi = min(a1, (u + 1) * sh.KC);
+            red_add_release_gpu(p.sgdone + ae, static_cast<uint32_t>(hi - lo));
+        }
+    }
+
+    // 2. down groups and their units
+    const int gfirst = b1 > b0 ? b0 / sh.TO : 0, glast = b1 > b0 ? (b1 - 1) / sh.TO : -1;
+    for (int g = gfirst; ok && g <= glast; ++g) {
+        const int hs = g - gfirst, ae = sx->gae[g], gbeg = tb.gbeg[g], gcnt = tb.gcnt[g];
+        // 2a. the expert's gate/up atoms are all done (one thread polls; the
+        // barrier passes what it acquired on to the others)
+        if (th == 0) {
+            const uint64_t t0 = gtimer();
+            for (uint32_t it = 0;; ++it) {
+                if (ld_acquire(p.sgdone + ae) == static_cast<uint32_t>(need)) break;
+                if ((it & 15u) == 15u) {
+                    if (*abort_flag) break;
+                    if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
+                        raise_error(p, abort_flag, kErrTimeout);
+                        break;
+                    }
+                }
+            }
+        }
+        if (!(ok = epi_sync())) break;
+        if (*abort_flag) {
+            ok = false;
+            break;
+        }
+        // 2b. h = SiLU(g) * u of each pair, rows 4 th .. 4 th + 3 of every 512
+        uint8_t *hd_dig = smem + p.s_off_h + hs * (sh.KCI * 2048);
+        uint8_t *hd_sc = smem + p.s_off_hsc + hs * (sh.KCI * 256);
+        for (int i = 0; i < gcnt && ok; ++i) {
+            const int tok = tb.stok[gbeg + i];
+            // h of rows k .. k+3 (k = 512 rr + 4 th < I): every segment's
+            // partials of the row's tile, summed in K order, then SiLU(g) * u
+            auto h_at = [&](int rr) -> float4 {
+                const int k = 512 * rr + 4 * th;
+                const int ti = k >> 7, u = ae * sh.TI + ti, af = u * sh.KC, al = af + sh.KC - 1;
+                float4 sg = make_float4(0.f, 0.f, 0.f, 0.f), su = sg;
+                for (int cb = sm_cta_of(af, sh.NA, G); cb <= sm_cta_of(al, sh.NA, G); ++cb) {
+                    const int lo = sm_lo(cb, sh.NA, G);
+                    if (lo == sm_lo(cb + 1, sh.NA, G)) continue;  // an empty share
+                    const float *sl = p.sapart + (static_cast<size_t>(cb) * p.smaxseg + (u - lo / sh.KC)) * kSmSlot;
+                    const float4 pg = __ldcg(reinterpret_cast<const float4 *>(sl + (0 * kSmMaxT + tok) * 128 + (k & 127)));
+                    const float4 pu = __ldcg(reinterpret_cast<const float4 *>(sl + (1 * kSmMaxT + tok) * 128 + (k & 127)));
+                    sg.x += pg.x; sg.y += pg.y; sg.z += pg.z; sg.w += pg.w;
+                    su.x += pu.x; su.y += pu.y; su.z += pu.z; su.w += pu.w;
+                }
+                return make_float4(sg.x / (1.0f + __expf(-sg.x)) * su.x, sg.y / (1.0f + __expf(-sg.y)) * su.y,
+                                   sg.z / (1.0f + __expf(-sg.z)) * su.z, sg.w / (1.0f + __expf(-sg.w)) * su.w);
+            };
+            // up to four rounds stay in registers; more are recomputed for the
+            // quantisation pass (the same loads, so the same values)
+            constexpr int kKeep = RND <= 4 ? RND : 1;
+            float4 hv[kKeep];
+            float amax = 0.f;
+            auto take_max = [&](const float4 v) {
+                const float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+                if (!(m < 3.0e38f)) atomicOr(p.ctrl + 2, kErrRange);  // h not finite
+                amax = fmaxf(amax, m);
+            };
+            if constexpr (RND <= 4) {
+#pragma unroll
+                for (int rr = 0; rr < RND; ++rr) {
+                    hv[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (512 * rr + 4 * th < p.I) take_max(hv[rr] = h_at(rr));
+                }
+            } else {
+#pragma unroll 1
+                for (int rr = 0; rr < RND; ++rr)
+                    if (512 * rr + 4 * th < p.I) take_max(h_at(rr));
+            }
+#pragma unroll
+            for (int d = 16; d; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+            if (lane == 0) sx->red[q] = amax;
+            if (!(ok = epi_sync())) break;
+            const int eh = prescale_exp(fmaxf(fmaxf(sx->red[0], sx->red[1]), fmaxf(sx->red[2], sx->red[3])));
+            const float P = mul_pow2(1.f, eh);
+            if (th == 0) sx->hexp[hs][i] = eh;
+#pragma unroll(RND <= 4 ? RND : 1)
+            for (int rr = 0; rr < RND; ++rr) {
+                const int k = 512 * rr + 4 * th;
+                if (512 * rr >= p.I) break;
+                if (512 * rr + 128 * (q + 1) > p.I) continue;  // past I: the whole warp (I % 256 == 0)
+                float4 hq;
+                if constexpr (RND <= 4) hq = hv[rr];
+                else hq = h_at(rr);
+                float v[4] = {hq.x * P, hq.y * P, hq.z * P, hq.w * P};
+                uint32_t pk[4], sc[4];
+                quant_block4_quad(v, pk, sc);
+                const int c = k >> 8, jb = (k & 255) >> 1;
+#pragma unroll
+                for (int d = 0; d < 4; ++d) {
+                    const int n = 4 * i + d;
+                    *reinterpret_cast<uint16_t *>(hd_dig + c * 2048 + sw128_off(n, jb)) = static_cast<uint16_t>(pk[d]);
+                    if ((lane & 3) == 0) hd_sc[c * 256 + n * 16 + ((k & 255) >> 4)] = static_cast<uint8_t>(sc[d]);
+                }
+            }
+            // the maxima slot is reused by the next pair
+            if (!(ok = epi_sync())) break;
+        }
+        if (!ok) break;
+        fence_async_smem();  // the MMA (async proxy) reads the digit rows
+        if (!(ok = epi_sync())) break;
+        if (th == 0) st_rel_cta(&sx->hready[hs], 1);
+        // 2c. the group's down units held by this CTA
+        const int ulo = max(b0, g * sh.TO), uhi = min(b1, (g + 1) * sh.TO);
+        const int e = tb.gexp[g];
+        const float td = __ldg(p.dts + e);
+        for (int b = ulo; b < uhi; ++b) {
+            if (!(ok = take_acc())) break;
+            const uint32_t dcol = lanebase + static_cast<uint32_t>((nt & 1) * kAccCols);
+            float4 dd[kSmGroup];
+#pragma unroll
+            for (int i = 0; i < kSmGroup; ++i)
+                if (i < gcnt) tc_ld4(dcol + 4 * i, dd[i]);
+            tc_wait_ld();
+            give_acc();
+            const int o = b - g * sh.TO;
+#pragma unroll
+            for (int i = 0; i < kSmGroup; ++i)
+                if (i < gcnt) {
+                    const float v = (dd[i].x + dd[i].y * 0.25f + dd[i].z * 0.0625f + dd[i].w * 0.015625f);
+                    p.part[static_cast<size_t>(gbeg + i) * p.H + o * 128 + r] = mul_pow2(v, -sx->hexp[hs][i]) * td;
+                }
+            // all four warps' stores precede the hand-over to the release warp
+            if (!(ok = epi_sync())) break;
+            if (q == 0) {
+                if (!(ok = push_done(p, hd, npush, KIND_B, g, o, lane, abort_flag))) break;
+            }
+            ++npush;
+        }
+    }
+    __syncwarp();
+    if (lane == 0) atom_add_acqrel_cta(&hd->cons_exited, 1);
+}
+
+// ------------------------------------------------------------------ the kernel
+// RND: 512-row rounds of h per thread in the h builds (I <= 512 * RND)
+template <int RND>
+__global__ void __launch_bounds__(kTcThreads, 1) moe_small_kernel(const __grid_constant__ KernelParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int P = p.T * p.k;
+    Tabs tb = make_tabs(smem, p.tab_off, P);
+    SmemHdr *hd = tb.hdr;
+    SmTabs *sx = reinterpret_cast<SmTabs *>(smem + p.s_off_scr);
+    volatile int *abort_flag = &hd->abort_flag;
+
+    // set-up that touches nothing the previous kernel on the stream may still use
+    if (tid == 0) {
+        for (int i = 0; i < p.NS; ++i) {
+            mbar_init(&hd->full[i], 1);
+            mbar_init(&hd->empty[i], 1);
+            mbar_init(&hd->sfready[i], 4);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&hd->accfull[b], 1);
+            mbar_init(&hd->accempty[b], 4);
+        }
+        mbar_init(&hd->mma_done, 1);
+        mbar_init(&hd->epibar, 4);
+        hd->grouped = 0;
+        hd->abort_flag = 0;
+        hd->fill_cnt = 0;
+        hd->cons_exited = 0;
+        hd->dq_head = 0;
+        hd->cj_count = hd->cj_claim = hd->cj_closed = 0;
+        for (int i = 0; i < kDoneQ; ++i) hd->dq_seq[i] = 0;
+        sx->xready = 0;
+        for (int i = 0; i < kSmMaxHSlots; ++i) sx->hready[i] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 9) tc_alloc(&hd->tmem_base, kTmemCols);
+    if (tid == 256)
+        for (int i = 0; i < 6; ++i)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmt[i])) : "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // x, ids, w and the workspace counters may be written by the previous kernel
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // every CTA of this grid is resident: the next kernel may be queued now (its
+    // CTAs find room only as ours exit, and it waits for this grid to finish)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (warp < 8) {
+        sm_quantize_x(p, smem, sx);
+        if (!warp_spin(p, [&] { return ld_acq_cta(&hd->grouped) != 0; }, abort_flag, 64)) {
+            // aborted before the loops: the other roles leave on the abort flag
+        } else {
+            const SmShape sh = sm_shape(p, hd->n_groups, sx->nE);
+            if (warp < 4) sm_scale_loop(p, smem, tb, sx, sh, abort_flag);
+            else sm_epilogue<RND>(p, smem, tb, sx, sh, abort_flag);
+        }
+    } else {
+        sm_group(p, tb, sx);
+        const SmShape sh = sm_shape(p, hd->n_groups, sx->nE);
+        if (warp == 8) {
+            sm_producer(p, smem, tb, sx, sh, abort_flag);
+        } else if (warp == 9) {
+            if ((tid & 31) == 0 && spin_one(p, [&] { return ld_acq_cta(&sx->xready) != 0; }, abort_flag))
+                sm_mma_loop(p, smem, tb, sx, sh, abort_flag);
+        } else if (warp == 11) {
+            release_loop_common<128>(p, tb, p.H / 128, 4, abort_flag);
+        }
+    }
+    // every warp, its own loop over, helps with the remaining combine jobs
+    __syncwarp();
+    combine_assist<128>(p, tb, abort_flag);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tc_dealloc(hd->tmem_base, kTmemCols);
+    }
+    if (tid == 0) {
+        if (*abort_flag) {
+            // no copy may land after the CTA exits: wait (bounded) for the last
+            // fill of every stage
+            const uint64_t t0 = gtimer();
+            const int F = hd->fill_cnt;
+            for (int i = 0; i < p.NS; ++i) {
+                const int fi = F / p.NS + (i < F % p.NS ? 1 : 0);
+                if (fi == 0) continue;
+                while (!mbar_test(&hd->full[i], static_cast<uint32_t>((fi - 1) & 1))) {
+                    if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) break;
+                }
+            }
+        }
+        __threadfence();
+        const uint32_t done = atomicAdd(p.ctrl + 1, 1u);
+        if (done == gridDim.x - 1) {
+            // last CTA out: reset the counters for the next launch
+            __threadfence();
+            const bool err = (ld_relaxed(p.ctrl + 2) & kErrTimeout) != 0;
+            const int nE = err ? kSmMaxPairs : sx->nE;
+            for (int i = 0; i < nE; ++i) p.sgdone[i] = 0u;
+            if (err)
+                for (int i = 0; i < p.T * (p.H / 128); ++i) p.cnt[i] = 0u;
+            p.ctrl[0] = 0u;
+            p.ctrl[1] = 0u;
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t set_small_smem_limit(int bytes)
+{
+    const void *fns[] = {reinterpret_cast<const void *>(moe_small_kernel<2>),
+                         reinterpret_cast<const void *>(moe_small_kernel<4>),
+                         reinterpret_cast<const void *>(moe_small_kernel<8>)};
+    for (const void *f : fns) {
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_small(const KernelParams &p, int grid, int smem_bytes, bool pdl, cudaStream_t st)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (p.I <= 1024) return cudaLaunchKernelEx(&cfg, moe_small_kernel<2>, p);
+    if (p.I <= 2048) return cudaLaunchKernelEx(&cfg, moe_small_kernel<4>, p);
+    return cudaLaunchKernelEx(&cfg, moe_small_kernel<8>, p);
+}
+
+}  // namespace moe

@@ -406,6 +406,32 @@ def test_poisoned_workspace_times_out_and_recovers_tensor_kernel():
     assert rel_err(y.cpu().numpy(), y_ref) <= TOL
 
 
+def test_poisoned_workspace_times_out_and_recovers_small_kernel():
+    """The same on the small-launch tensor-core kernel: with the experts'
+    gate/up counters poisoned no h is ever built, so the waits of the down
+    groups expire; the launch returns (copies drained, MMAs complete, tensor
+    memory freed), moe_check reports the timeout, and after moe_workspace_init
+    the plan computes correctly again."""
+    os.environ["MOE_WAIT_TIMEOUT_MS"] = "200"
+    try:
+        wl = Workload("poison-small", T=2, H=512, I=256, E=8, k=4, routing="uniform", seed=14)
+        x, ids, w = make_x(wl), make_topk_ids(wl), make_topk_w(wl)
+        W = small_weights(wl)
+        plan = MoePlan(W, wl.H, wl.I, wl.E, wl.k, T_max=wl.T)
+    finally:
+        del os.environ["MOE_WAIT_TIMEOUT_MS"]
+    ws = plan.new_workspace()
+    binding.moe_debug_poison_workspace(plan.handle, ws)
+    plan.step(x.to(DEV), ids.to(DEV), w.to(DEV), ws)
+    assert plan.check(ws) == binding.MOE_ERR_TIMEOUT
+    assert plan.stats()["small_launches"] == 1
+    binding.moe_workspace_init(plan.handle, ws)
+    y = plan.step(x.to(DEV), ids.to(DEV), w.to(DEV), ws)
+    assert plan.check(ws) == 0
+    y_ref, _ = oracle.moe_forward(x, ids, w, {k: v.cpu() for k, v in W.items()})
+    assert rel_err(y.cpu().numpy(), y_ref) <= TOL
+
+
 # ------------------------------------------------------------------ programmatic dependent launch
 def test_pdl_back_to_back_matches(cache):
     """Steps launched with programmatic dependent launch, back to back on one
