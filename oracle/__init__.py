@@ -36,7 +36,7 @@ def build(force: bool = False) -> str:
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-Wall", "-Wextra",
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-Wall", "-Wextra",
                "-o", tmp, _SRC, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB_PATH)
@@ -60,6 +60,9 @@ def _load():
             lib.oracle_expert_pair.restype = None
             lib.oracle_moe_forward.argtypes = [i, i, i, i, i, P, P, P] + [P] * 9 + [P, i, P, i]
             lib.oracle_moe_forward.restype = C.c_int
+            lib.oracle_moe_forward_ext.argtypes = ([i, i, i, i, i, P, P, P] + [P] * 9 + [i, i] + [P] * 7 + [i] +
+                                                   [P, i, P, i])
+            lib.oracle_moe_forward_ext.restype = C.c_int
             lib.oracle_group.argtypes = [P, i, i, P, P, P]
             lib.oracle_group.restype = C.c_int
             lib.oracle_route.argtypes = [P, i, i, i, P, P]
@@ -141,11 +144,30 @@ def expert_pair(x_row, e: int, W, n_threads: int = 0):
     return g, u, h, o
 
 
-def moe_forward(x, ids, w, W, tokens=None, n_threads: int = 0):
-    """y (float64 [n, H]) for `tokens` (default all) and the count of ids >= E."""
+def moe_forward(x, ids, w, W, tokens=None, n_threads: int = 0, shared=None, e_range=None, E=None,
+                act_quant: bool = False):
+    """y (float64 [n, H]) for `tokens` (default all) and the count of ids >= E.
+
+    shared: optional dict gate_q/gate_s/up_q/up_s/down_q/down_s (one expert's
+    arrays) and ts (float32 [3]: gate, up, down tensor scales) -- an always-on
+    expert added to every token with weight 1 after the routed slots.
+    e_range: (e_lo, e_hi) -- W holds experts e_lo .. e_hi-1 only; ids outside
+    the range are another device's and contribute nothing; E (required with
+    e_range) is the total expert count that bounds valid ids.
+    act_quant: x and h quantised once to NVFP4 before the projections."""
     arrs = _weights(W)
-    E, I, H2 = arrs[0].shape
+    El, I, H2 = arrs[0].shape
     H = H2 * 2
+    if e_range is None:
+        e_lo, e_hi, E = 0, El, El
+    else:
+        e_lo, e_hi = e_range
+        if E is None or e_hi - e_lo != El:
+            raise ValueError("e_range needs E and W holding exactly e_hi - e_lo experts")
+    sh = [None] * 7
+    if shared is not None:
+        sh = [_np(shared[n], np.uint8) for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")]
+        sh.append(_np(shared["ts"], np.float32))
     xb = _np(x, np.uint16)
     T = xb.shape[0]
     idsa = _np(ids, np.int32)
@@ -158,9 +180,10 @@ def moe_forward(x, ids, w, W, tokens=None, n_threads: int = 0):
         tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
         n = tok.shape[0]
     y = np.zeros((n, H), np.float64)
-    bad = _load().oracle_moe_forward(H, I, E, k, T, _p(xb), _p(idsa), _p(wa),
-                                     *[_p(a) for a in arrs],
-                                     None if tok is None else _p(tok), n, _p(y), int(n_threads))
+    bad = _load().oracle_moe_forward_ext(H, I, E, k, T, _p(xb), _p(idsa), _p(wa),
+                                         *[_p(a) for a in arrs], int(e_lo), int(e_hi),
+                                         *[None if a is None else _p(a) for a in sh], int(bool(act_quant)),
+                                         None if tok is None else _p(tok), n, _p(y), int(n_threads))
     if bad < 0:
         raise ValueError("oracle_moe_forward rejected its arguments")
     return y, bad

@@ -134,11 +134,15 @@ static int n_threads_eff(int n)
  *   h[i] = g[i] / (1 + exp(-g[i])) * u[i]
  *   o[r] = sum_i Wd[e][r][i] h[i]      (r < H)
  * Any of g, u, h may be NULL (scratch is then allocated internally). */
-void oracle_expert_pair(int H, int I, int e, const double *xr,
-                        const uint8_t *gate_q, const uint8_t *gate_s, const float *gate_ts,
-                        const uint8_t *up_q, const uint8_t *up_s, const float *up_ts,
-                        const uint8_t *down_q, const uint8_t *down_s, const float *down_ts,
-                        double *g, double *u, double *h, double *o, int n_threads)
+static void quant_row_nvfp4(const float *v, int n, double *out);
+
+/* The pair, with h quantised once to NVFP4 before the down projection when
+ * act != 0 (rounded to fp32, then quant_row_nvfp4). */
+static void expert_pair_q(int H, int I, int e, const double *xr,
+                          const uint8_t *gate_q, const uint8_t *gate_s, const float *gate_ts,
+                          const uint8_t *up_q, const uint8_t *up_s, const float *up_ts,
+                          const uint8_t *down_q, const uint8_t *down_s, const float *down_ts,
+                          double *g, double *u, double *h, double *o, int n_threads, int act)
 {
     build_tables();
     double *gbuf = g ? g : (double *)malloc(sizeof(double) * (size_t)I);
@@ -164,6 +168,13 @@ void oracle_expert_pair(int H, int I, int e, const double *xr,
         ubuf[i] = su;
         hbuf[i] = sg / (1.0 + exp(-sg)) * su;
     }
+    if (act) {
+        float *hf = (float *)malloc(sizeof(float) * (size_t)I);
+        for (int i = 0; i < I; ++i)
+            hf[i] = (float)hbuf[i];
+        quant_row_nvfp4(hf, I, hbuf);
+        free(hf);
+    }
 #ifdef _OPENMP
 #pragma omp parallel for schedule(static) num_threads(nt)
 #endif
@@ -178,24 +189,158 @@ void oracle_expert_pair(int H, int I, int e, const double *xr,
     if (!h) free(hbuf);
 }
 
+void oracle_expert_pair(int H, int I, int e, const double *xr,
+                        const uint8_t *gate_q, const uint8_t *gate_s, const float *gate_ts,
+                        const uint8_t *up_q, const uint8_t *up_s, const float *up_ts,
+                        const uint8_t *down_q, const uint8_t *down_s, const float *down_ts,
+                        double *g, double *u, double *h, double *o, int n_threads)
+{
+    expert_pair_q(H, I, e, xr, gate_q, gate_s, gate_ts, up_q, up_s, up_ts, down_q, down_s, down_ts,
+                  g, u, h, o, n_threads, 0);
+}
+
+/* ------------------------------------------------- single NVFP4 quantisation */
+
+/* Largest |v| of a row -> the power-of-two prescale exponent e that puts it in
+ * (1344, 2688] (a = m 2^E, 1 <= m < 2: e = 11 - E if m <= 1.3125, else 10 - E),
+ * clamped to [-100, 100]; 100 for a row of zeros. */
+static int prescale_exp_of(float a)
+{
+    if (!(a > 0.0f))
+        return 100;
+    if (!(a < 3.0e38f))
+        return -100;
+    int ex;
+    double f = frexp((double)a, &ex); /* a = f 2^ex, 0.5 <= f < 1 */
+    double m = 2.0 * f;
+    int E = ex - 1;
+    int e = (m <= 1.3125 ? 11 : 10) - E;
+    return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
+
+/* E4M3 code of the value nearest to a >= 0 (ties: the even code), saturating
+ * at 448 (code 0x7E). */
+static unsigned e4m3_rne_code(float a)
+{
+    build_tables();
+    if (!(a < 448.0f))
+        return 0x7Eu;
+    unsigned best = 0;
+    double bd = fabs(tab_e4m3[0] - (double)a);
+    for (unsigned c = 1; c <= 0x7Eu; ++c) {
+        double d = fabs(tab_e4m3[c] - (double)a);
+        if (d < bd || (d == bd && (c & 1u) == 0))
+            best = c, bd = d;
+    }
+    return best;
+}
+
+/* E2M1 magnitude code of the value nearest to |q| (ties: the even code),
+ * saturating at 6; the sign is applied by the caller. */
+static unsigned e2m1_rne_mag(float q)
+{
+    build_tables();
+    double m = fabs((double)q);
+    if (m >= 6.0)
+        return 7u;
+    unsigned best = 0;
+    double bd = m;
+    for (unsigned c = 1; c < 8u; ++c) {
+        double d = fabs(tab_e2m1[c] - m);
+        if (d < bd || (d == bd && (c & 1u) == 0))
+            best = c, bd = d;
+    }
+    return best;
+}
+
+/* One row of n activations (n a multiple of 16) quantised once to NVFP4 and
+ * dequantised into out (double): one power-of-two prescale for the row (its
+ * largest |v| into (1344, 2688]); per 16-element block the E4M3 scale s = the
+ * smallest E4M3 value >= (block max / 6), found as the round-to-nearest-even
+ * E4M3 of that quotient, moved up one code when it fell below; each element
+ * the round-to-nearest-even E2M1 of (its prescaled value times 1/s).  Every
+ * step that decides a code runs in fp32, in this order: v 2^e, max * (1/6),
+ * 1/s, (v 2^e) * (1/s).  out = E2M1 value * s * 2^-e. */
+static void quant_row_nvfp4(const float *v, int n, double *out)
+{
+    build_tables();
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i)
+        amax = fabsf(v[i]) > amax ? fabsf(v[i]) : amax;
+    int e = prescale_exp_of(amax);
+    volatile float P = ldexpf(1.0f, e);
+    const float sixth = 1.0f / 6.0f;
+    for (int b = 0; b < n; b += 16) {
+        float p[16], bm = 0.0f;
+        for (int i = 0; i < 16; ++i) {
+            volatile float t = v[b + i] * P;
+            p[i] = t;
+            bm = fabsf(t) > bm ? fabsf(t) : bm;
+        }
+        volatile float a = bm * sixth;
+        unsigned c = e4m3_rne_code(a);
+        if (tab_e4m3[c] < (double)a && c < 0x7Eu)
+            ++c;
+        double s = tab_e4m3[c];
+        if (!(s > 0.0)) {
+            for (int i = 0; i < 16; ++i)
+                out[b + i] = 0.0;
+            continue;
+        }
+        volatile float inv = 1.0f / (float)s;
+        for (int i = 0; i < 16; ++i) {
+            volatile float q = p[i] * inv;
+            double val = tab_e2m1[e2m1_rne_mag(q)];
+            out[b + i] = ldexp((signbit(q) ? -val : val) * s, -e);
+        }
+    }
+}
+
+/* One (token, expert) pair; act != 0: x already quantised by the caller, h
+ * quantised here (expert_pair_q). */
+static void expert_pair_mode(int H, int I, int e, const double *xr,
+                             const uint8_t *gate_q, const uint8_t *gate_s, const float *gate_ts,
+                             const uint8_t *up_q, const uint8_t *up_s, const float *up_ts,
+                             const uint8_t *down_q, const uint8_t *down_s, const float *down_ts,
+                             double *o, int n_threads, int act)
+{
+    expert_pair_q(H, I, e, xr, gate_q, gate_s, gate_ts, up_q, up_s, up_ts, down_q, down_s, down_ts,
+                  NULL, NULL, NULL, o, n_threads, act);
+}
+
 /* ---------------------------------------------------------------- full step */
 
 /* y (double [n_tok, H]) for the tokens listed in `tokens` (NULL: all T, in
- * order).  Returns the number of slots whose id is >= E, or -1 on a bad
- * argument.  x holds bf16 bit patterns [T, H]; ids int32 [T, k]; w fp32 [T, k]. */
-int oracle_moe_forward(int H, int I, int E, int k, int T,
-                       const uint16_t *x, const int32_t *ids, const float *w,
-                       const uint8_t *gate_q, const uint8_t *gate_s, const float *gate_ts,
-                       const uint8_t *up_q, const uint8_t *up_s, const float *up_ts,
-                       const uint8_t *down_q, const uint8_t *down_s, const float *down_ts,
-                       const int32_t *tokens, int n_tok, double *y, int n_threads)
+ * order), with the three extensions of the step:
+ *  - expert range: the routed weight arrays hold experts e_lo .. e_hi-1 only
+ *    (array index e - e_lo); a valid id outside the range belongs to another
+ *    device's share and contributes nothing here (it is not counted as bad);
+ *  - shared expert: when sg_q is not NULL, one always-on expert (arrays
+ *    [I, H/2], [I, H/16], [H, I/2], [H, I/16]; s_ts = its gate, up and down
+ *    tensor scales) is added to every token's y with weight 1, after the
+ *    routed slots;
+ *  - act = 1: x and h are quantised once to NVFP4 (quant_row_nvfp4) before
+ *    the projections that read them.
+ * Returns the number of slots whose id is >= E, or -1 on a bad argument. */
+int oracle_moe_forward_ext(int H, int I, int E, int k, int T,
+                           const uint16_t *x, const int32_t *ids, const float *w,
+                           const uint8_t *gate_q, const uint8_t *gate_s, const float *gate_ts,
+                           const uint8_t *up_q, const uint8_t *up_s, const float *up_ts,
+                           const uint8_t *down_q, const uint8_t *down_s, const float *down_ts,
+                           int e_lo, int e_hi,
+                           const uint8_t *sg_q, const uint8_t *sg_s, const uint8_t *su_q, const uint8_t *su_s,
+                           const uint8_t *sd_q, const uint8_t *sd_s, const float *s_ts, int act,
+                           const int32_t *tokens, int n_tok, double *y, int n_threads)
 {
     if (H <= 0 || I <= 0 || E <= 0 || k <= 0 || T < 0 || (H % 16) || (I % 16))
+        return -1;
+    if (e_lo < 0 || e_hi > E || e_lo >= e_hi)
         return -1;
     if (!tokens)
         n_tok = T;
     double *xr = (double *)malloc(sizeof(double) * (size_t)H);
     double *o = (double *)malloc(sizeof(double) * (size_t)H);
+    float *xf = (float *)malloc(sizeof(float) * (size_t)H);
     int bad = 0;
     for (int n = 0; n < n_tok; ++n) {
         int t = tokens ? tokens[n] : n;
@@ -206,6 +351,11 @@ int oracle_moe_forward(int H, int I, int E, int k, int T,
             continue;
         for (int c = 0; c < H; ++c)
             xr[c] = bf16_to_double(x[(size_t)t * H + (size_t)c]);
+        if (act) {
+            for (int c = 0; c < H; ++c)
+                xf[c] = (float)xr[c];
+            quant_row_nvfp4(xf, H, xr);
+        }
         for (int j = 0; j < k; ++j) {
             int e = ids[(size_t)t * k + (size_t)j];
             if (e < 0)
@@ -214,16 +364,38 @@ int oracle_moe_forward(int H, int I, int E, int k, int T,
                 ++bad;
                 continue;
             }
-            oracle_expert_pair(H, I, e, xr, gate_q, gate_s, gate_ts, up_q, up_s, up_ts,
-                               down_q, down_s, down_ts, NULL, NULL, NULL, o, n_threads);
+            if (e < e_lo || e >= e_hi)
+                continue;
+            expert_pair_mode(H, I, e - e_lo, xr, gate_q, gate_s, gate_ts, up_q, up_s, up_ts,
+                             down_q, down_s, down_ts, o, n_threads, act);
             double wj = (double)w[(size_t)t * k + (size_t)j];
             for (int r = 0; r < H; ++r)
                 yt[r] += wj * o[r];
         }
+        if (sg_q) {
+            expert_pair_mode(H, I, 0, xr, sg_q, sg_s, s_ts + 0, su_q, su_s, s_ts + 1, sd_q, sd_s, s_ts + 2,
+                             o, n_threads, act);
+            for (int r = 0; r < H; ++r)
+                yt[r] += o[r];
+        }
     }
     free(xr);
     free(o);
+    free(xf);
     return bad;
+}
+
+/* The plain step: every expert local, no shared expert, exact activations. */
+int oracle_moe_forward(int H, int I, int E, int k, int T,
+                       const uint16_t *x, const int32_t *ids, const float *w,
+                       const uint8_t *gate_q, const uint8_t *gate_s, const float *gate_ts,
+                       const uint8_t *up_q, const uint8_t *up_s, const float *up_ts,
+                       const uint8_t *down_q, const uint8_t *down_s, const float *down_ts,
+                       const int32_t *tokens, int n_tok, double *y, int n_threads)
+{
+    return oracle_moe_forward_ext(H, I, E, k, T, x, ids, w, gate_q, gate_s, gate_ts, up_q, up_s, up_ts,
+                                  down_q, down_s, down_ts, 0, E, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0,
+                                  tokens, n_tok, y, n_threads);
 }
 
 /* ---------------------------------------------------------------- grouping */

@@ -945,7 +945,7 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
             if (pl->shs <= moe::kSmMaxHSlots && small_layout(pl, ts).NS >= 2) {
                 pl->use_small = true;
                 pl->off_sgdone = o;
-                o = up(o + 4 * static_cast<size_t>(moe::kSmMaxPairs), 256);
+                o = up(o + 2 * 4 * static_cast<size_t>(moe::kSmMaxPairs), 256);
                 pl->off_sapart = o;
                 o = up(o + static_cast<size_t>(G) * pl->smaxseg * moe::kSmSlot * 4, 256);
             }
@@ -1219,7 +1219,7 @@ moe_status_t moe_debug_poison_workspace(moe_plan_t plan, void *ws_dev, void *str
                                        moe::kMaxPairs, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess && plan->use_small)
         e = moe::launch_poison(reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws_dev) + plan->off_sgdone),
-                               moe::kSmMaxPairs, static_cast<cudaStream_t>(stream));
+                               2 * moe::kSmMaxPairs, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "poison launch: %s", cudaGetErrorString(e));
     return MOE_OK;
 }

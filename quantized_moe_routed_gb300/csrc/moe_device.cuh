@@ -131,6 +131,10 @@ __device__ __forceinline__ uint32_t atom_add_acqrel_gpu(uint32_t *a, uint32_t v)
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
     return old;
 }
+__device__ __forceinline__ void st_release_gpu(uint32_t *a, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
 __device__ __forceinline__ void red_add_release_gpu(uint32_t *a, uint32_t v)
 {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");

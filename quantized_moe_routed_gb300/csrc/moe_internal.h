@@ -43,6 +43,8 @@ inline int tab_bytes_for(int P, int T)
 //   word 0: ticket counter   word 1: CTAs finished   word 2: error bits
 //   word 3: activation rows gathered (x, fp16) so far in this launch
 //   word 4: activation rows claimed for gathering so far in this launch
+//   word 5: small-launch kernel: the expert-counter set the next launch uses
+//   word 6: small-launch kernel: CTAs that have read word 5 in this launch
 constexpr size_t kCtrlBytes = 256;
 
 struct KernelParams {
@@ -110,7 +112,7 @@ struct KernelParams {
 
     // ---- small-launch tensor-core path (moe_small.cu) ----
     float *sapart;      // [grid * smaxseg][2][kSmMaxT][128] gate / up partial sums of each (CTA, unit) segment
-    uint32_t *sgdone;   // [kSmMaxPairs] per active expert: gate/up atoms finished (reset by the last CTA)
+    uint32_t *sgdone;   // [2][kSmMaxPairs] per active expert: gate/up atoms finished (two sets, alternating)
     int smaxseg;        // partial-sum slots per CTA (units one CTA's atom range can touch)
     int sxrows;         // rows of one 256-element chunk of the resident x digits (8: T <= 2, 16: T <= 4)
     int shs;            // h digit slots (down groups one CTA's unit range can touch)

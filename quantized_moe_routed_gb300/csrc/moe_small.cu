@@ -44,6 +44,8 @@
 
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 namespace moe {
 namespace {
 
@@ -70,6 +72,7 @@ struct SmTabs {
     int16_t aexp[kSmMaxPairs];    // active expert index -> expert id
     float xmul[kSmMaxT][4];       // per token and digit: 2^-(prescale + 2 digit)
     int xe[kSmMaxT];              // per token: the x row's prescale exponent
+    int par;                      // this launch's counter set + 1 (0: not known yet)
 };
 static_assert(sizeof(SmTabs) <= kSmScrBytes, "kernel tables too large");
 
@@ -455,6 +458,9 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
     const int need = sh.TI * sh.KC;  // atoms of one expert
     int nt = 0, nsync = 0, npush = 0;
     bool ok = true;
+    // this launch's set of expert counters (published by warp 10 at the start)
+    if (!warp_spin(p, [&] { return ld_acq_cta(&sx->par) != 0; }, abort_flag)) ok = false;
+    uint32_t *gdone = p.sgdone + (ok ? (sx->par - 1) * kSmMaxPairs : 0);
     auto epi_sync = [&]() -> bool {
         __syncwarp();
         if (lane == 0) mbar_arrive(&hd->epibar);
@@ -498,11 +504,12 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
                 slot[(0 * kSmMaxT + t) * 128 + r] = (dg[t].x * m[0] + dg[t].y * m[1] + dg[t].z * m[2] + dg[t].w * m[3]) * tg;
                 slot[(1 * kSmMaxT + t) * 128 + r] = (du[t].x * m[0] + du[t].y * m[1] + du[t].z * m[2] + du[t].w * m[3]) * tu;
             }
-        __threadfence();
+        // the four warps' stores precede thread 0's gpu-scope release through
+        // the barrier (mbarrier arrive / wait: release / acquire at CTA scope)
         if (!(ok = epi_sync())) break;
         if (th == 0) {
             const int lo = max(a0, u * sh.KC), hi = min(a1, (u + 1) * sh.KC);
-            red_add_release_gpu(p.sgdone + ae, static_cast<uint32_t>(hi - lo));
+            red_add_release_gpu(gdone + ae, static_cast<uint32_t>(hi - lo));
         }
     }
 
@@ -515,7 +522,7 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
         if (th == 0) {
             const uint64_t t0 = gtimer();
             for (uint32_t it = 0;; ++it) {
-                if (ld_acquire(p.sgdone + ae) == static_cast<uint32_t>(need)) break;
+                if (ld_acquire(gdone + ae) == static_cast<uint32_t>(need)) break;
                 if ((it & 15u) == 15u) {
                     if (*abort_flag) break;
                     if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
@@ -535,26 +542,65 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
         uint8_t *hd_sc = smem + p.s_off_hsc + hs * (sh.KCI * 256);
         for (int i = 0; i < gcnt && ok; ++i) {
             const int tok = tb.stok[gbeg + i];
-            // h of rows k .. k+3 (k = 512 rr + 4 th < I): every segment's
-            // partials of the row's tile, summed in K order, then SiLU(g) * u
-            auto h_at = [&](int rr) -> float4 {
-                const int k = 512 * rr + 4 * th;
-                const int ti = k >> 7, u = ae * sh.TI + ti, af = u * sh.KC, al = af + sh.KC - 1;
-                float4 sg = make_float4(0.f, 0.f, 0.f, 0.f), su = sg;
-                for (int cb = sm_cta_of(af, sh.NA, G); cb <= sm_cta_of(al, sh.NA, G); ++cb) {
-                    const int lo = sm_lo(cb, sh.NA, G);
-                    if (lo == sm_lo(cb + 1, sh.NA, G)) continue;  // an empty share
-                    const float *sl = p.sapart + (static_cast<size_t>(cb) * p.smaxseg + (u - lo / sh.KC)) * kSmSlot;
-                    const float4 pg = __ldcg(reinterpret_cast<const float4 *>(sl + (0 * kSmMaxT + tok) * 128 + (k & 127)));
-                    const float4 pu = __ldcg(reinterpret_cast<const float4 *>(sl + (1 * kSmMaxT + tok) * 128 + (k & 127)));
-                    sg.x += pg.x; sg.y += pg.y; sg.z += pg.z; sg.w += pg.w;
-                    su.x += pu.x; su.y += pu.y; su.z += pu.z; su.w += pu.w;
+            // h of rows k .. k+3 (k = 512 rr + 4 th < I) for NR consecutive
+            // rounds: every segment's partials of the row's tile, summed in K
+            // order, then SiLU(g) * u.  All the rounds' loads (up to four
+            // segments each at a time) are issued before any sum, so a batch
+            // costs one round trip to L2.
+            auto h_rounds = [&](int r0, auto nr_c, float4 *out) {
+                constexpr int NR = decltype(nr_c)::value;
+                int cb0[NR], cb1[NR], uu[NR], kk[NR];
+                float4 sg[NR], su[NR];
+#pragma unroll
+                for (int m = 0; m < NR; ++m) {
+                    kk[m] = 512 * (r0 + m) + 4 * th;
+                    uu[m] = ae * sh.TI + (kk[m] >> 7);
+                    const bool live = kk[m] < p.I;
+                    cb0[m] = live ? sm_cta_of(uu[m] * sh.KC, sh.NA, G) : 1;
+                    cb1[m] = live ? sm_cta_of(uu[m] * sh.KC + sh.KC - 1, sh.NA, G) : 0;
+                    sg[m] = su[m] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                return make_float4(sg.x / (1.0f + __expf(-sg.x)) * su.x, sg.y / (1.0f + __expf(-sg.y)) * su.y,
-                                   sg.z / (1.0f + __expf(-sg.z)) * su.z, sg.w / (1.0f + __expf(-sg.w)) * su.w);
+                constexpr int SB = RND <= 2 ? 4 : 2;  // segments per batch (register budget)
+                for (int base = 0;; base += SB) {
+                    bool any = false;
+                    float4 pg[NR][SB], pu[NR][SB];
+                    bool ld[NR][SB];
+#pragma unroll
+                    for (int m = 0; m < NR; ++m)
+#pragma unroll
+                        for (int i = 0; i < SB; ++i) {
+                            const int cb = cb0[m] + base + i;
+                            const int lo = sm_lo(cb, sh.NA, G);
+                            ld[m][i] = cb <= cb1[m] && lo != sm_lo(cb + 1, sh.NA, G);  // an empty share holds nothing
+                            any |= cb <= cb1[m];
+                            if (ld[m][i]) {
+                                const float *sl = p.sapart + (static_cast<size_t>(cb) * p.smaxseg + (uu[m] - lo / sh.KC)) * kSmSlot;
+                                pg[m][i] = __ldcg(reinterpret_cast<const float4 *>(sl + (0 * kSmMaxT + tok) * 128 + (kk[m] & 127)));
+                                pu[m][i] = __ldcg(reinterpret_cast<const float4 *>(sl + (1 * kSmMaxT + tok) * 128 + (kk[m] & 127)));
+                            }
+                        }
+                    if (!any) break;
+#pragma unroll
+                    for (int m = 0; m < NR; ++m)
+#pragma unroll
+                        for (int i = 0; i < SB; ++i)
+                            if (ld[m][i]) {
+                                sg[m].x += pg[m][i].x; sg[m].y += pg[m][i].y; sg[m].z += pg[m][i].z; sg[m].w += pg[m][i].w;
+                                su[m].x += pu[m][i].x; su[m].y += pu[m][i].y; su[m].z += pu[m][i].z; su[m].w += pu[m][i].w;
+                            }
+                }
+#pragma unroll
+                for (int m = 0; m < NR; ++m) {
+                    const float4 g4 = sg[m], u4 = su[m];
+                    out[m] = make_float4(g4.x / (1.0f + __expf(-g4.x)) * u4.x, g4.y / (1.0f + __expf(-g4.y)) * u4.y,
+                                         g4.z / (1.0f + __expf(-g4.z)) * u4.z, g4.w / (1.0f + __expf(-g4.w)) * u4.w);
+                }
             };
-            // up to four rounds stay in registers; more are recomputed for the
-            // quantisation pass (the same loads, so the same values)
+            using two_c = std::integral_constant<int, 2>;
+            using one_c = std::integral_constant<int, 1>;
+            // up to four rounds stay in registers (loaded two rounds per batch);
+            // more are recomputed for the quantisation pass (the same loads, so
+            // the same values)
             constexpr int kKeep = RND <= 4 ? RND : 1;
             float4 hv[kKeep];
             float amax = 0.f;
@@ -563,16 +609,25 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
                 if (!(m < 3.0e38f)) atomicOr(p.ctrl + 2, kErrRange);  // h not finite
                 amax = fmaxf(amax, m);
             };
-            if constexpr (RND <= 4) {
+            if constexpr (RND <= 2) {
+                h_rounds(0, two_c{}, hv);
 #pragma unroll
-                for (int rr = 0; rr < RND; ++rr) {
-                    hv[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (512 * rr + 4 * th < p.I) take_max(hv[rr] = h_at(rr));
-                }
+                for (int rr = 0; rr < RND; ++rr)
+                    if (512 * rr + 4 * th < p.I) take_max(hv[rr]);
+            } else if constexpr (RND <= 4) {
+#pragma unroll
+                for (int rr = 0; rr < RND; ++rr) h_rounds(rr, one_c{}, hv + rr);
+#pragma unroll
+                for (int rr = 0; rr < RND; ++rr)
+                    if (512 * rr + 4 * th < p.I) take_max(hv[rr]);
             } else {
 #pragma unroll 1
                 for (int rr = 0; rr < RND; ++rr)
-                    if (512 * rr + 4 * th < p.I) take_max(h_at(rr));
+                    if (512 * rr + 4 * th < p.I) {
+                        float4 v;
+                        h_rounds(rr, one_c{}, &v);
+                        take_max(v);
+                    }
             }
 #pragma unroll
             for (int d = 16; d; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
@@ -588,7 +643,7 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
                 if (512 * rr + 128 * (q + 1) > p.I) continue;  // past I: the whole warp (I % 256 == 0)
                 float4 hq;
                 if constexpr (RND <= 4) hq = hv[rr];
-                else hq = h_at(rr);
+                else h_rounds(rr, one_c{}, &hq);
                 float v[4] = {hq.x * P, hq.y * P, hq.z * P, hq.w * P};
                 uint32_t pk[4], sc[4];
                 quant_block4_quad(v, pk, sc);
@@ -674,6 +729,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_small_kernel(const __grid_c
         hd->cj_count = hd->cj_claim = hd->cj_closed = 0;
         for (int i = 0; i < kDoneQ; ++i) hd->dq_seq[i] = 0;
         sx->xready = 0;
+        sx->par = 0;
         for (int i = 0; i < kSmMaxHSlots; ++i) sx->hready[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -708,6 +764,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_small_kernel(const __grid_c
         } else if (warp == 9) {
             if ((tid & 31) == 0 && spin_one(p, [&] { return ld_acq_cta(&sx->xready) != 0; }, abort_flag))
                 sm_mma_loop(p, smem, tb, sx, sh, abort_flag);
+        } else if (warp == 10) {
+            // Two sets of expert counters alternate between launches, so none
+            // needs resetting at the end of a launch: this launch uses set P
+            // (control word 5), and the last CTA to arrive here (control word 6)
+            // zeroes the other set -- the previous launch's, which has finished
+            // -- and flips word 5 for the next launch.  Every CTA reads word 5
+            // before it arrives, so none can see the flip.
+            if ((tid & 31) == 0) {
+                const uint32_t P = ld_acquire(p.ctrl + 5) & 1u;
+                if (atom_add_acqrel_gpu(p.ctrl + 6, 1u) == gridDim.x - 1) {
+                    p.ctrl[6] = 0u;
+                    for (int i = 0; i < kSmMaxPairs; ++i) p.sgdone[(P ^ 1u) * kSmMaxPairs + i] = 0u;
+                    __threadfence();
+                    st_release_gpu(p.ctrl + 5, P ^ 1u);
+                }
+                st_rel_cta(&sx->par, static_cast<int>(P) + 1);
+            }
         } else if (warp == 11) {
             release_loop_common<128>(p, tb, p.H / 128, 4, abort_flag);
         }
@@ -735,20 +808,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_small_kernel(const __grid_c
                 }
             }
         }
-        __threadfence();
-        const uint32_t done = atomicAdd(p.ctrl + 1, 1u);
-        if (done == gridDim.x - 1) {
-            // last CTA out: reset the counters for the next launch
-            __threadfence();
-            const bool err = (ld_relaxed(p.ctrl + 2) & kErrTimeout) != 0;
-            const int nE = err ? kSmMaxPairs : sx->nE;
-            for (int i = 0; i < nE; ++i) p.sgdone[i] = 0u;
-            if (err)
-                for (int i = 0; i < p.T * (p.H / 128); ++i) p.cnt[i] = 0u;
-            p.ctrl[0] = 0u;
-            p.ctrl[1] = 0u;
-            __threadfence();
-        }
+        // nothing to reset: the expert counters alternate between two sets
+        // and the combine counters are reset by their last arrivals; after a
+        // device-side error the caller re-initialises the workspace
     }
 }
 

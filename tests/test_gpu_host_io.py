@@ -30,14 +30,16 @@ def fill(io, x, ids, w):
     io.w.copy_(w)
 
 
-# T = 1 x top-8: the register kernel; T = 12 x top-4: the tensor-core kernel;
+# T = 1 x top-8: the small-launch tensor-core kernel (and the register kernel
+# on a register plan); T = 12 x top-4: the tensor-core ticket kernel;
 # T = 40: the prefill path (a strict plan takes it through this entry)
-@pytest.mark.parametrize("T,k,path", [(1, 8, "register"), (12, 4, "tensor"), (40, 4, "prefill")])
+@pytest.mark.parametrize("T,k,path", [(1, 8, "small"), (1, 8, "register"), (12, 4, "tensor"), (40, 4, "prefill")])
 def test_step_host_is_bitwise_the_device_step(T, k, path):
     wl = Workload("hostio", T=T, H=512, I=256, E=16, k=k, routing="uniform", seed=21)
     x, ids, w = make_x(wl), make_topk_ids(wl), make_topk_w(wl)
     W = make_expert_weights(wl, device=DEV, experts=None)
-    plan = MoePlan(W, wl.H, wl.I, wl.E, wl.k, T_max=T, strict=True)
+    kern = binding.MOE_KERNEL_REGISTER if path == "register" else binding.MOE_KERNEL_AUTO
+    plan = MoePlan(W, wl.H, wl.I, wl.E, wl.k, T_max=T, strict=True, kernel=kern)
     ws = plan.new_workspace()
     y_dev_path = plan.step(x.to(DEV), ids.to(DEV), w.to(DEV), ws)
     assert plan.check(ws) == 0
@@ -54,6 +56,8 @@ def test_step_host_is_bitwise_the_device_step(T, k, path):
     assert bool(torch.isnan(io.y_dev).all())
     if path == "tensor":
         assert after["tensor_launches"] == before["tensor_launches"] + 1
+    elif path == "small":
+        assert after["small_launches"] == before["small_launches"] + 1
     elif path == "register":
         assert after["tensor_launches"] == before["tensor_launches"]
         assert after["decode_launches"] == before["decode_launches"] + 1
