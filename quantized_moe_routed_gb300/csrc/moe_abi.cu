@@ -942,7 +942,9 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
             pl->smaxseg = static_cast<int>((LA - 1) / KC + 2);
             pl->shs = static_cast<int>((LB - 1) / TO + 2);
             pl->T_small = ts;
-            if (pl->shs <= moe::kSmMaxHSlots && small_layout(pl, ts).NS >= 2) {
+            // the kernel's share arithmetic is 32-bit: (grid + 1) * atoms < 2^32
+            if (pl->shs <= moe::kSmMaxHSlots && small_layout(pl, ts).NS >= 2 && NA < 65536 && NB < 65536 &&
+                G < 4096) {
                 pl->use_small = true;
                 pl->off_sgdone = o;
                 o = up(o + 2 * 4 * static_cast<size_t>(moe::kSmMaxPairs), 256);

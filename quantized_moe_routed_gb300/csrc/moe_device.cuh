@@ -261,6 +261,7 @@ struct SmemHdr {
     int4 tinfo[2];  // {kind, group, tile, k-split}
     uint64_t mma_done;
     uint64_t epibar;  // the four epilogue warps' meeting point (bounded waits)
+    uint64_t teambar; // small-launch kernel: warps 0-7 building h together
     int tseq[2];    // accumulator buffer use published with tinfo (release/acquire)
     uint32_t tmem_base;
     int ep_last;

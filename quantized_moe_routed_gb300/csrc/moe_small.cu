@@ -67,7 +67,7 @@ struct SmTabs {
     int xready;                   // resident x digits complete (release)
     int hready[kSmMaxHSlots];     // per h slot: the group's digit rows are built (release)
     int hexp[kSmMaxHSlots][kSmGroup];  // per h slot and pair: the h row's prescale exponent
-    float red[4];                 // epilogue warps' partial maxima
+    float red[8];                 // the h-build team's per-warp maxima
     int16_t gae[kSmMaxPairs];     // group -> active expert index
     int16_t aexp[kSmMaxPairs];    // active expert index -> expert id
     float xmul[kSmMaxT][4];       // per token and digit: 2^-(prescale + 2 digit)
@@ -83,11 +83,16 @@ static_assert(sizeof(SmTabs) <= kSmScrBytes, "kernel tables too large");
 struct SmShape {
     int TI, KC, TO, KCI, nPB, NA, NB, ng, nE;
 };
-__device__ __forceinline__ int sm_lo(int j, int n, int G) { return static_cast<int>(static_cast<long long>(j) * n / G); }
+// (32-bit arithmetic: j <= G and n < 2^16 atoms or units, so j * n < 2^32.)
+__device__ __forceinline__ int sm_lo(int j, int n, int G)
+{
+    return static_cast<int>(static_cast<uint32_t>(j) * static_cast<uint32_t>(n) / static_cast<uint32_t>(G));
+}
 // The CTA whose atom range holds atom a (the largest j with alo(j) <= a).
 __device__ __forceinline__ int sm_cta_of(int a, int n, int G)
 {
-    return static_cast<int>((static_cast<long long>(a + 1) * G + n - 1) / n) - 1;
+    return static_cast<int>((static_cast<uint32_t>(a + 1) * static_cast<uint32_t>(G) + static_cast<uint32_t>(n) - 1u) /
+                            static_cast<uint32_t>(n)) - 1;
 }
 __device__ __forceinline__ SmShape sm_shape(const KernelParams &p, int ng, int nE)
 {
@@ -294,17 +299,35 @@ __device__ __forceinline__ int sm_hslot(int g, const SmShape &sh)
     return g - sm_lo(blockIdx.x, sh.NB, gridDim.x) / sh.TO;
 }
 
+template <int RND, class Sync>
+__device__ bool sm_build_h(const KernelParams &p, uint8_t *smem, const Tabs &tb, SmTabs *sx, const SmShape &sh, int g,
+                           int hs, const uint32_t *gdone, Sync &&team_sync, volatile int *abort_flag);
+
 // Scale warps (0-3): per stage, the weight tiles' block scales (row r = lane
 // 32q + lane) and the activation digit rows' block scales go to the stage's
 // tensor-memory slot in the layout the block-scaled MMA reads (see
 // tc_st_set / tc_st_bset); rows past the activation's digit rows get zero
 // scales.  A down stage's activation scales are its group's h digit scales,
 // which exist once the group's h slot is marked built.
+template <int RND>
 __device__ void sm_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb, SmTabs *sx, const SmShape &sh,
                               volatile int *abort_flag)
 {
     SmemHdr *hd = tb.hdr;
     const int q = threadIdx.x >> 5, lane = threadIdx.x & 31, r = 32 * q + lane;
+    // the h builds this team takes part in (before the first down stage of each
+    // slot; the epilogue warps are the other half of the team)
+    int nteam = 0, built = 0;
+    auto team_sync = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hd->teambar);
+        const bool w = warp_wait_bar(p, &hd->teambar, static_cast<uint32_t>(nteam & 1), abort_flag);
+        ++nteam;
+        return w;
+    };
+    if (!warp_spin(p, [&] { return ld_acq_cta(&sx->par) != 0; }, abort_flag)) return;
+    const uint32_t *gdone = p.sgdone + (sx->par - 1) * kSmMaxPairs;
+    const int gfirst = sm_lo(blockIdx.x, sh.NB, gridDim.x) / sh.TO;
     const uint32_t sfbase = hd->tmem_base + (static_cast<uint32_t>(32 * q) << 16) + kSfBase;
     auto row = [&](const uint8_t *b, int i) { return *reinterpret_cast<const uint4 *>(b + 16 * i); };
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -330,15 +353,17 @@ __device__ void sm_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
                 const uint4 b0 = lane < 4 * p.T ? row(smem + p.s_off_xsc + c * 256, lane) : z;
                 tc_st_bset(col + 32, b0, z, z, z);
             } else {
-                const int g = h.y / sh.TO, hs = sm_hslot(g, sh), c0 = 2 * h.z;
-                if (!warp_spin(p, [&] { return ld_acq_cta(&sx->hready[hs]) != 0; }, abort_flag)) break;
+                const int g = h.y / sh.TO, hs = g - gfirst, c0 = 2 * h.z;
+                const bool two = c0 + 1 < sh.KCI;
+                if (two) tc_st_set(col + 16, row(st + kOffS1, r));  // the weights' scales need no h
+                bool okb = true;
+                for (; okb && built <= hs; ++built)
+                    okb = sm_build_h<RND>(p, smem, tb, sx, sh, gfirst + built, built, gdone, team_sync, abort_flag);
+                if (!okb || !warp_spin(p, [&] { return ld_acq_cta(&sx->hready[hs]) != 0; }, abort_flag)) break;
                 const int rows = 4 * tb.gcnt[g];
                 const uint8_t *hsc = smem + p.s_off_hsc + hs * (sh.KCI * 256);
                 tc_st_bset(col + 32, lane < rows ? row(hsc + c0 * 256, lane) : z, z, z, z);
-                if (c0 + 1 < sh.KCI) {
-                    tc_st_set(col + 16, row(st + kOffS1, r));
-                    tc_st_bset(col + 48, lane < rows ? row(hsc + (c0 + 1) * 256, lane) : z, z, z, z);
-                }
+                if (two) tc_st_bset(col + 48, lane < rows ? row(hsc + (c0 + 1) * 256, lane) : z, z, z, z);
             }
             tc_wait_st();
         }
@@ -433,6 +458,133 @@ __device__ void sm_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
     wait_bar(&hd->mma_done, 0u, p, &no_abort);
 }
 
+// ------------------------------------------------------------------ h builds
+// The h digit rows of down group g (slot hs), built by warps 0-7 together
+// (tt = threadIdx.x, 256 threads): wait until the group's expert has all its
+// gate/up atoms (thread 0 polls; the team barrier passes what it acquired on),
+// then per pair h = SiLU(g) * u of rows 4 tt .. 4 tt + 3 of every 1024 -- the
+// partials of every segment of the row's tile summed in K order, all loads of
+// a batch in flight before any sum -- one prescale for the pair's whole row
+// (largest |h| into (1344, 2688]), four digits per 16-row block, written in
+// the MMA's swizzled layout; then the slot is marked built.  Both teams of
+// four warps call this for the same slots in the same order, and the team
+// barrier (bounded waits) sees the same number of arrivals on both sides.
+// RND: 1024-row rounds per thread (I <= 1024 RND).  false on abort.
+template <int RND, class Sync>
+__device__ bool sm_build_h(const KernelParams &p, uint8_t *smem, const Tabs &tb, SmTabs *sx, const SmShape &sh, int g,
+                           int hs, const uint32_t *gdone, Sync &&team_sync, volatile int *abort_flag)
+{
+    const int tt = threadIdx.x, lane = tt & 31, wq = tt >> 5;
+    const int G = gridDim.x, ae = sx->gae[g], gbeg = tb.gbeg[g], gcnt = tb.gcnt[g];
+    const int need = sh.TI * sh.KC;
+    if (tt == 0 && !spin_one(p, [&] { return ld_acquire(gdone + ae) == static_cast<uint32_t>(need); }, abort_flag)) {
+        // the abort flag is up; the barrier below returns false for everyone
+    }
+    if (!team_sync() || *abort_flag) return false;
+    uint8_t *hd_dig = smem + p.s_off_h + hs * (sh.KCI * 2048);
+    uint8_t *hd_sc = smem + p.s_off_hsc + hs * (sh.KCI * 256);
+    for (int i = 0; i < gcnt; ++i) {
+        const int tok = tb.stok[gbeg + i];
+        float4 hv[RND];
+        // NR rounds from r0: every live row's segments, SB at a time per round
+        auto h_rounds = [&](int r0, auto nr_c) {
+            constexpr int NR = decltype(nr_c)::value;
+            constexpr int SB = NR == 1 ? 4 : 3;
+            int cb0[NR], cb1[NR], uu[NR], kk[NR];
+            float4 sg[NR], su[NR];
+#pragma unroll
+            for (int m = 0; m < NR; ++m) {
+                kk[m] = 1024 * (r0 + m) + 4 * tt;
+                uu[m] = ae * sh.TI + (kk[m] >> 7);
+                const bool live = kk[m] < p.I;
+                cb0[m] = live ? sm_cta_of(uu[m] * sh.KC, sh.NA, G) : 1;
+                cb1[m] = live ? sm_cta_of(uu[m] * sh.KC + sh.KC - 1, sh.NA, G) : 0;
+                sg[m] = su[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            for (int base = 0;; base += SB) {
+                bool any = false;
+                float4 pg[NR][SB], pu[NR][SB];
+                bool ld[NR][SB];
+#pragma unroll
+                for (int m = 0; m < NR; ++m)
+#pragma unroll
+                    for (int c = 0; c < SB; ++c) {
+                        const int cb = cb0[m] + base + c;
+                        const int lo = sm_lo(cb, sh.NA, G);
+                        ld[m][c] = cb <= cb1[m] && lo != sm_lo(cb + 1, sh.NA, G);  // an empty share holds nothing
+                        any |= cb <= cb1[m];
+                        if (ld[m][c]) {
+                            const float *sl = p.sapart + (static_cast<size_t>(cb) * p.smaxseg + (uu[m] - lo / sh.KC)) * kSmSlot;
+                            pg[m][c] = __ldcg(reinterpret_cast<const float4 *>(sl + (0 * kSmMaxT + tok) * 128 + (kk[m] & 127)));
+                            pu[m][c] = __ldcg(reinterpret_cast<const float4 *>(sl + (1 * kSmMaxT + tok) * 128 + (kk[m] & 127)));
+                        }
+                    }
+                if (!any) break;
+#pragma unroll
+                for (int m = 0; m < NR; ++m)
+#pragma unroll
+                    for (int c = 0; c < SB; ++c)
+                        if (ld[m][c]) {
+                            sg[m].x += pg[m][c].x; sg[m].y += pg[m][c].y; sg[m].z += pg[m][c].z; sg[m].w += pg[m][c].w;
+                            su[m].x += pu[m][c].x; su[m].y += pu[m][c].y; su[m].z += pu[m][c].z; su[m].w += pu[m][c].w;
+                        }
+            }
+#pragma unroll
+            for (int m = 0; m < NR; ++m) {
+                const float4 a = sg[m], b = su[m];
+                hv[r0 + m] = make_float4(a.x / (1.0f + __expf(-a.x)) * b.x, a.y / (1.0f + __expf(-a.y)) * b.y,
+                                         a.z / (1.0f + __expf(-a.z)) * b.z, a.w / (1.0f + __expf(-a.w)) * b.w);
+            }
+        };
+        if constexpr (RND == 2) {
+            h_rounds(0, std::integral_constant<int, 2>{});
+        } else {
+#pragma unroll
+            for (int rr = 0; rr < RND; ++rr) h_rounds(rr, std::integral_constant<int, 1>{});
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int rr = 0; rr < RND; ++rr)
+            if (1024 * rr + 4 * tt < p.I) {
+                const float4 v = hv[rr];
+                const float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+                if (!(m < 3.0e38f)) atomicOr(p.ctrl + 2, kErrRange);  // h not finite
+                amax = fmaxf(amax, m);
+            }
+#pragma unroll
+        for (int d = 16; d; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+        if (lane == 0) sx->red[wq] = amax;
+        if (!team_sync()) return false;
+        float rm = sx->red[0];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) rm = fmaxf(rm, sx->red[w]);
+        const int eh = prescale_exp(rm);
+        const float P = mul_pow2(1.f, eh);
+        if (tt == 0) sx->hexp[hs][i] = eh;
+#pragma unroll
+        for (int rr = 0; rr < RND; ++rr) {
+            const int k = 1024 * rr + 4 * tt;
+            if (1024 * rr + 128 * (wq + 1) > p.I) continue;  // past I: the whole warp (I % 256 == 0)
+            float v[4] = {hv[rr].x * P, hv[rr].y * P, hv[rr].z * P, hv[rr].w * P};
+            uint32_t pk[4], sc[4];
+            quant_block4_quad(v, pk, sc);
+            const int c = k >> 8, jb = (k & 255) >> 1;
+#pragma unroll
+            for (int d = 0; d < 4; ++d) {
+                const int n = 4 * i + d;
+                *reinterpret_cast<uint16_t *>(hd_dig + c * 2048 + sw128_off(n, jb)) = static_cast<uint16_t>(pk[d]);
+                if ((lane & 3) == 0) hd_sc[c * 256 + n * 16 + ((k & 255) >> 4)] = static_cast<uint8_t>(sc[d]);
+            }
+        }
+        // the maxima slots are reused by the next pair
+        if (!team_sync()) return false;
+    }
+    fence_async_smem();  // the MMA (async proxy) reads the digit rows
+    if (!team_sync()) return false;
+    if (tt == 0) st_rel_cta(&sx->hready[hs], 1);
+    return true;
+}
+
 // ------------------------------------------------------------------ epilogue warps
 // Warps 4-7; warp 4+q reads accumulator lanes (rows) 32q .. 32q+31.
 //   1. each gate/up segment of the CTA, in order: per token the four digit
@@ -455,7 +607,6 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
     const int G = gridDim.x, j = blockIdx.x;
     const int a0 = sm_lo(j, sh.NA, G), a1 = sm_lo(j + 1, sh.NA, G);
     const int b0 = sm_lo(j, sh.NB, G), b1 = sm_lo(j + 1, sh.NB, G);
-    const int need = sh.TI * sh.KC;  // atoms of one expert
     int nt = 0, nsync = 0, npush = 0;
     bool ok = true;
     // this launch's set of expert counters (published by warp 10 at the start)
@@ -466,6 +617,14 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
         if (lane == 0) mbar_arrive(&hd->epibar);
         const bool w = warp_wait_bar(p, &hd->epibar, static_cast<uint32_t>(nsync & 1), abort_flag);
         ++nsync;
+        return w;
+    };
+    int nteam = 0;
+    auto team_sync = [&]() -> bool {  // warps 0-7 (the h builds)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hd->teambar);
+        const bool w = warp_wait_bar(p, &hd->teambar, static_cast<uint32_t>(nteam & 1), abort_flag);
+        ++nteam;
         return w;
     };
     auto take_acc = [&]() -> bool {  // wait for the next accumulator buffer
@@ -516,152 +675,9 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
     // 2. down groups and their units
     const int gfirst = b1 > b0 ? b0 / sh.TO : 0, glast = b1 > b0 ? (b1 - 1) / sh.TO : -1;
     for (int g = gfirst; ok && g <= glast; ++g) {
-        const int hs = g - gfirst, ae = sx->gae[g], gbeg = tb.gbeg[g], gcnt = tb.gcnt[g];
-        // 2a. the expert's gate/up atoms are all done (one thread polls; the
-        // barrier passes what it acquired on to the others)
-        if (th == 0) {
-            const uint64_t t0 = gtimer();
-            for (uint32_t it = 0;; ++it) {
-                if (ld_acquire(gdone + ae) == static_cast<uint32_t>(need)) break;
-                if ((it & 15u) == 15u) {
-                    if (*abort_flag) break;
-                    if (static_cast<long long>(gtimer() - t0) > p.timeout_ns) {
-                        raise_error(p, abort_flag, kErrTimeout);
-                        break;
-                    }
-                }
-            }
-        }
-        if (!(ok = epi_sync())) break;
-        if (*abort_flag) {
-            ok = false;
-            break;
-        }
-        // 2b. h = SiLU(g) * u of each pair, rows 4 th .. 4 th + 3 of every 512
-        uint8_t *hd_dig = smem + p.s_off_h + hs * (sh.KCI * 2048);
-        uint8_t *hd_sc = smem + p.s_off_hsc + hs * (sh.KCI * 256);
-        for (int i = 0; i < gcnt && ok; ++i) {
-            const int tok = tb.stok[gbeg + i];
-            // h of rows k .. k+3 (k = 512 rr + 4 th < I) for NR consecutive
-            // rounds: every segment's partials of the row's tile, summed in K
-            // order, then SiLU(g) * u.  All the rounds' loads (up to four
-            // segments each at a time) are issued before any sum, so a batch
-            // costs one round trip to L2.
-            auto h_rounds = [&](int r0, auto nr_c, float4 *out) {
-                constexpr int NR = decltype(nr_c)::value;
-                int cb0[NR], cb1[NR], uu[NR], kk[NR];
-                float4 sg[NR], su[NR];
-#pragma unroll
-                for (int m = 0; m < NR; ++m) {
-                    kk[m] = 512 * (r0 + m) + 4 * th;
-                    uu[m] = ae * sh.TI + (kk[m] >> 7);
-                    const bool live = kk[m] < p.I;
-                    cb0[m] = live ? sm_cta_of(uu[m] * sh.KC, sh.NA, G) : 1;
-                    cb1[m] = live ? sm_cta_of(uu[m] * sh.KC + sh.KC - 1, sh.NA, G) : 0;
-                    sg[m] = su[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-                constexpr int SB = RND <= 2 ? 4 : 2;  // segments per batch (register budget)
-                for (int base = 0;; base += SB) {
-                    bool any = false;
-                    float4 pg[NR][SB], pu[NR][SB];
-                    bool ld[NR][SB];
-#pragma unroll
-                    for (int m = 0; m < NR; ++m)
-#pragma unroll
-                        for (int i = 0; i < SB; ++i) {
-                            const int cb = cb0[m] + base + i;
-                            const int lo = sm_lo(cb, sh.NA, G);
-                            ld[m][i] = cb <= cb1[m] && lo != sm_lo(cb + 1, sh.NA, G);  // an empty share holds nothing
-                            any |= cb <= cb1[m];
-                            if (ld[m][i]) {
-                                const float *sl = p.sapart + (static_cast<size_t>(cb) * p.smaxseg + (uu[m] - lo / sh.KC)) * kSmSlot;
-                                pg[m][i] = __ldcg(reinterpret_cast<const float4 *>(sl + (0 * kSmMaxT + tok) * 128 + (kk[m] & 127)));
-                                pu[m][i] = __ldcg(reinterpret_cast<const float4 *>(sl + (1 * kSmMaxT + tok) * 128 + (kk[m] & 127)));
-                            }
-                        }
-                    if (!any) break;
-#pragma unroll
-                    for (int m = 0; m < NR; ++m)
-#pragma unroll
-                        for (int i = 0; i < SB; ++i)
-                            if (ld[m][i]) {
-                                sg[m].x += pg[m][i].x; sg[m].y += pg[m][i].y; sg[m].z += pg[m][i].z; sg[m].w += pg[m][i].w;
-                                su[m].x += pu[m][i].x; su[m].y += pu[m][i].y; su[m].z += pu[m][i].z; su[m].w += pu[m][i].w;
-                            }
-                }
-#pragma unroll
-                for (int m = 0; m < NR; ++m) {
-                    const float4 g4 = sg[m], u4 = su[m];
-                    out[m] = make_float4(g4.x / (1.0f + __expf(-g4.x)) * u4.x, g4.y / (1.0f + __expf(-g4.y)) * u4.y,
-                                         g4.z / (1.0f + __expf(-g4.z)) * u4.z, g4.w / (1.0f + __expf(-g4.w)) * u4.w);
-                }
-            };
-            using two_c = std::integral_constant<int, 2>;
-            using one_c = std::integral_constant<int, 1>;
-            // up to four rounds stay in registers (loaded two rounds per batch);
-            // more are recomputed for the quantisation pass (the same loads, so
-            // the same values)
-            constexpr int kKeep = RND <= 4 ? RND : 1;
-            float4 hv[kKeep];
-            float amax = 0.f;
-            auto take_max = [&](const float4 v) {
-                const float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-                if (!(m < 3.0e38f)) atomicOr(p.ctrl + 2, kErrRange);  // h not finite
-                amax = fmaxf(amax, m);
-            };
-            if constexpr (RND <= 2) {
-                h_rounds(0, two_c{}, hv);
-#pragma unroll
-                for (int rr = 0; rr < RND; ++rr)
-                    if (512 * rr + 4 * th < p.I) take_max(hv[rr]);
-            } else if constexpr (RND <= 4) {
-#pragma unroll
-                for (int rr = 0; rr < RND; ++rr) h_rounds(rr, one_c{}, hv + rr);
-#pragma unroll
-                for (int rr = 0; rr < RND; ++rr)
-                    if (512 * rr + 4 * th < p.I) take_max(hv[rr]);
-            } else {
-#pragma unroll 1
-                for (int rr = 0; rr < RND; ++rr)
-                    if (512 * rr + 4 * th < p.I) {
-                        float4 v;
-                        h_rounds(rr, one_c{}, &v);
-                        take_max(v);
-                    }
-            }
-#pragma unroll
-            for (int d = 16; d; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-            if (lane == 0) sx->red[q] = amax;
-            if (!(ok = epi_sync())) break;
-            const int eh = prescale_exp(fmaxf(fmaxf(sx->red[0], sx->red[1]), fmaxf(sx->red[2], sx->red[3])));
-            const float P = mul_pow2(1.f, eh);
-            if (th == 0) sx->hexp[hs][i] = eh;
-#pragma unroll(RND <= 4 ? RND : 1)
-            for (int rr = 0; rr < RND; ++rr) {
-                const int k = 512 * rr + 4 * th;
-                if (512 * rr >= p.I) break;
-                if (512 * rr + 128 * (q + 1) > p.I) continue;  // past I: the whole warp (I % 256 == 0)
-                float4 hq;
-                if constexpr (RND <= 4) hq = hv[rr];
-                else h_rounds(rr, one_c{}, &hq);
-                float v[4] = {hq.x * P, hq.y * P, hq.z * P, hq.w * P};
-                uint32_t pk[4], sc[4];
-                quant_block4_quad(v, pk, sc);
-                const int c = k >> 8, jb = (k & 255) >> 1;
-#pragma unroll
-                for (int d = 0; d < 4; ++d) {
-                    const int n = 4 * i + d;
-                    *reinterpret_cast<uint16_t *>(hd_dig + c * 2048 + sw128_off(n, jb)) = static_cast<uint16_t>(pk[d]);
-                    if ((lane & 3) == 0) hd_sc[c * 256 + n * 16 + ((k & 255) >> 4)] = static_cast<uint8_t>(sc[d]);
-                }
-            }
-            // the maxima slot is reused by the next pair
-            if (!(ok = epi_sync())) break;
-        }
-        if (!ok) break;
-        fence_async_smem();  // the MMA (async proxy) reads the digit rows
-        if (!(ok = epi_sync())) break;
-        if (th == 0) st_rel_cta(&sx->hready[hs], 1);
+        const int hs = g - gfirst, gbeg = tb.gbeg[g], gcnt = tb.gcnt[g];
+        // 2a. the group's h digit rows, with the scale warps
+        if (!(ok = sm_build_h<RND>(p, smem, tb, sx, sh, g, hs, gdone, team_sync, abort_flag))) break;
         // 2c. the group's down units held by this CTA
         const int ulo = max(b0, g * sh.TO), uhi = min(b1, (g + 1) * sh.TO);
         const int e = tb.gexp[g];
@@ -695,7 +711,7 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
 }
 
 // ------------------------------------------------------------------ the kernel
-// RND: 512-row rounds of h per thread in the h builds (I <= 512 * RND)
+// RND: 1024-row rounds of h per thread in the h builds (I <= 1024 * RND)
 template <int RND>
 __global__ void __launch_bounds__(kTcThreads, 1) moe_small_kernel(const __grid_constant__ KernelParams p)
 {
@@ -721,6 +737,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_small_kernel(const __grid_c
         }
         mbar_init(&hd->mma_done, 1);
         mbar_init(&hd->epibar, 4);
+        mbar_init(&hd->teambar, 8);
         hd->grouped = 0;
         hd->abort_flag = 0;
         hd->fill_cnt = 0;
@@ -753,7 +770,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_small_kernel(const __grid_c
             // aborted before the loops: the other roles leave on the abort flag
         } else {
             const SmShape sh = sm_shape(p, hd->n_groups, sx->nE);
-            if (warp < 4) sm_scale_loop(p, smem, tb, sx, sh, abort_flag);
+            if (warp < 4) sm_scale_loop<RND>(p, smem, tb, sx, sh, abort_flag);
             else sm_epilogue<RND>(p, smem, tb, sx, sh, abort_flag);
         }
     } else {
@@ -818,9 +835,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_small_kernel(const __grid_c
 
 cudaError_t set_small_smem_limit(int bytes)
 {
-    const void *fns[] = {reinterpret_cast<const void *>(moe_small_kernel<2>),
-                         reinterpret_cast<const void *>(moe_small_kernel<4>),
-                         reinterpret_cast<const void *>(moe_small_kernel<8>)};
+    const void *fns[] = {reinterpret_cast<const void *>(moe_small_kernel<1>),
+                         reinterpret_cast<const void *>(moe_small_kernel<2>),
+                         reinterpret_cast<const void *>(moe_small_kernel<4>)};
     for (const void *f : fns) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
@@ -840,9 +857,9 @@ cudaError_t launch_small(const KernelParams &p, int grid, int smem_bytes, bool p
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (p.I <= 1024) return cudaLaunchKernelEx(&cfg, moe_small_kernel<2>, p);
-    if (p.I <= 2048) return cudaLaunchKernelEx(&cfg, moe_small_kernel<4>, p);
-    return cudaLaunchKernelEx(&cfg, moe_small_kernel<8>, p);
+    if (p.I <= 1024) return cudaLaunchKernelEx(&cfg, moe_small_kernel<1>, p);
+    if (p.I <= 2048) return cudaLaunchKernelEx(&cfg, moe_small_kernel<2>, p);
+    return cudaLaunchKernelEx(&cfg, moe_small_kernel<4>, p);
 }
 
 }  // namespace moe
