@@ -473,7 +473,8 @@ moe_status_t run_tc(moe_plan *pl, const void *x, const int32_t *ids, const float
 // the kernel's tables, the common control block and tables; NS = 0 if fewer
 // than two stages fit.
 struct SmallLayout {
-    int NS = 0, xrows = 0, off_x = 0, off_xsc = 0, off_h = 0, off_hsc = 0, off_scr = 0, tab_off = 0, total = 0;
+    int NS = 0, xrows = 0, off_x = 0, off_xsc = 0, off_h = 0, off_hsc = 0, off_scr = 0, off_alo = 0, tab_off = 0;
+    int total = 0;
 };
 SmallLayout small_layout(const moe_plan *pl, int T)
 {
@@ -483,8 +484,9 @@ SmallLayout small_layout(const moe_plan *pl, int T)
     // rows 8-15 of the last chunk are read (and ignored) when a chunk holds 8 rows
     const int xbytes = KC * L.xrows * 128 + (L.xrows == 8 ? 1024 : 0);
     const int hbytes = pl->shs * KCI * 2048, hsbytes = pl->shs * KCI * 256;
+    const int alobytes = 8 * (pl->num_sms + 1);  // every CTA's atom-range start and unit
     const int rest = up1024(xbytes) + up1024(KC * 256) + hbytes + static_cast<int>(up(hsbytes, 16)) +
-                     moe::kSmScrBytes + 128 + moe::tab_bytes_for(P, T) + 1024;
+                     moe::kSmScrBytes + static_cast<int>(up(alobytes, 16)) + 128 + moe::tab_bytes_for(P, T) + 1024;
     int ns = (pl->smem_optin - rest) / moe::kSmStage;
     if (ns > moe::kMaxStages) ns = moe::kMaxStages;
     if (ns < 2) return L;
@@ -494,7 +496,8 @@ SmallLayout small_layout(const moe_plan *pl, int T)
     L.off_h = L.off_xsc + up1024(KC * 256);
     L.off_hsc = L.off_h + hbytes;
     L.off_scr = static_cast<int>(up(L.off_hsc + hsbytes, 16));
-    L.tab_off = static_cast<int>(up(L.off_scr + moe::kSmScrBytes, 128));
+    L.off_alo = L.off_scr + moe::kSmScrBytes;
+    L.tab_off = static_cast<int>(up(L.off_alo + alobytes, 128));
     L.total = L.tab_off + moe::tab_bytes_for(P, T) + 1024;
     return L;
 }
@@ -554,6 +557,7 @@ moe_status_t run_small(moe_plan *pl, const void *x, const int32_t *ids, const fl
     p.s_off_h = L.off_h;
     p.s_off_hsc = L.off_hsc;
     p.s_off_scr = L.off_scr;
+    p.s_off_alo = L.off_alo;
     cudaError_t e = moe::launch_small(p, pl->num_sms, L.total, pl->pdl, cs);
     if (e != cudaSuccess) {
         reject(pl);

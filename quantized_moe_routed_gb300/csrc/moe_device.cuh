@@ -70,6 +70,23 @@ __device__ __forceinline__ void tma2d(void *dst, const CUtensorMap *tm, int c0, 
         : "memory");
 }
 
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Fire-and-forget L2 prefetch of one 2-D tensor-map box (no shared memory, no
+// barrier): the later TMA load of the same box finds it in L2.
+__device__ __forceinline__ void tma2d_prefetch_l2(const CUtensorMap *tm, int c0, int c1, uint64_t pol)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(c0), "r"(c1), "l"(pol)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *tm, int c0, int c1, int c2, uint64_t *bar,
                                       uint64_t pol)
 {

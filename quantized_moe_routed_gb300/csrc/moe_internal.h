@@ -116,7 +116,7 @@ struct KernelParams {
     int smaxseg;        // partial-sum slots per CTA (units one CTA's atom range can touch)
     int sxrows;         // rows of one 256-element chunk of the resident x digits (8: T <= 2, 16: T <= 4)
     int shs;            // h digit slots (down groups one CTA's unit range can touch)
-    int s_off_x, s_off_xsc, s_off_xmul, s_off_h, s_off_hsc, s_off_hmul, s_off_scr;  // shared-memory offsets
+    int s_off_x, s_off_xsc, s_off_xmul, s_off_h, s_off_hsc, s_off_hmul, s_off_scr, s_off_alo;  // shared-memory offsets
 };
 
 // Dynamic shared memory layout of the persistent kernel for P pairs.

@@ -73,6 +73,7 @@ struct SmTabs {
     float xmul[kSmMaxT][4];       // per token and digit: 2^-(prescale + 2 digit)
     int xe[kSmMaxT];              // per token: the x row's prescale exponent
     int par;                      // this launch's counter set + 1 (0: not known yet)
+    int aloready;                 // the share table at s_off_alo is filled (release)
 };
 static_assert(sizeof(SmTabs) <= kSmScrBytes, "kernel tables too large");
 
@@ -243,6 +244,7 @@ __device__ void sm_producer(const KernelParams &p, uint8_t *smem, Tabs tb, const
         if (!wait_bar(&hd->empty[s], ph ^ 1u, p, abort_flag)) return false;
         return true;
     };
+
     auto advance = [&]() {
         ++fill;
         if (++s == p.NS) {
@@ -481,6 +483,9 @@ __device__ bool sm_build_h(const KernelParams &p, uint8_t *smem, const Tabs &tb,
         // the abort flag is up; the barrier below returns false for everyone
     }
     if (!team_sync() || *abort_flag) return false;
+    // every CTA's atom-range start and its first unit (filled by warp 10 at the start)
+    const int2 *alo = reinterpret_cast<const int2 *>(smem + p.s_off_alo);
+    if (!warp_spin(p, [&] { return ld_acq_cta(&sx->aloready) != 0; }, abort_flag)) return false;
     uint8_t *hd_dig = smem + p.s_off_h + hs * (sh.KCI * 2048);
     uint8_t *hd_sc = smem + p.s_off_hsc + hs * (sh.KCI * 256);
     for (int i = 0; i < gcnt; ++i) {
@@ -510,11 +515,12 @@ __device__ bool sm_build_h(const KernelParams &p, uint8_t *smem, const Tabs &tb,
 #pragma unroll
                     for (int c = 0; c < SB; ++c) {
                         const int cb = cb0[m] + base + c;
-                        const int lo = sm_lo(cb, sh.NA, G);
-                        ld[m][c] = cb <= cb1[m] && lo != sm_lo(cb + 1, sh.NA, G);  // an empty share holds nothing
-                        any |= cb <= cb1[m];
+                        const bool in = cb <= cb1[m];
+                        const int2 lo = in ? alo[cb] : make_int2(0, 0);
+                        ld[m][c] = in && lo.x != alo[cb + 1].x;  // an empty share holds nothing
+                        any |= in;
                         if (ld[m][c]) {
-                            const float *sl = p.sapart + (static_cast<size_t>(cb) * p.smaxseg + (uu[m] - lo / sh.KC)) * kSmSlot;
+                            const float *sl = p.sapart + (static_cast<size_t>(cb) * p.smaxseg + (uu[m] - lo.y)) * kSmSlot;
                             pg[m][c] = __ldcg(reinterpret_cast<const float4 *>(sl + (0 * kSmMaxT + tok) * 128 + (kk[m] & 127)));
                             pu[m][c] = __ldcg(reinterpret_cast<const float4 *>(sl + (1 * kSmMaxT + tok) * 128 + (kk[m] & 127)));
                         }
@@ -747,6 +753,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_small_kernel(const __grid_c
         for (int i = 0; i < kDoneQ; ++i) hd->dq_seq[i] = 0;
         sx->xready = 0;
         sx->par = 0;
+        sx->aloready = 0;
         for (int i = 0; i < kSmMaxHSlots; ++i) sx->hready[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -782,6 +789,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_small_kernel(const __grid_c
             if ((tid & 31) == 0 && spin_one(p, [&] { return ld_acq_cta(&sx->xready) != 0; }, abort_flag))
                 sm_mma_loop(p, smem, tb, sx, sh, abort_flag);
         } else if (warp == 10) {
+            // the atom-range start of every CTA and the unit it falls in, for
+            // the h builds (no divisions on their critical path)
+            int2 *alo = reinterpret_cast<int2 *>(smem + p.s_off_alo);
+            for (int jj = tid & 31; jj <= static_cast<int>(gridDim.x); jj += 32) {
+                const int lo = sm_lo(jj, sh.NA, gridDim.x);
+                alo[jj] = make_int2(lo, sh.KC ? lo / sh.KC : 0);
+            }
+            __syncwarp();
+            if ((tid & 31) == 0) st_rel_cta(&sx->aloready, 1);
             // Two sets of expert counters alternate between launches, so none
             // needs resetting at the end of a launch: this launch uses set P
             // (control word 5), and the last CTA to arrive here (control word 6)

@@ -142,7 +142,8 @@ __device__ __forceinline__ void quant_block4(float (&r)[16], uint2 (&pk)[4], uin
         sc[j] = e4m3_ceil(amax * f * (1.0f / 6.0f), s);
         uint32_t w[2] = {0u, 0u};
         if (s > 0.f) {
-            const float inv = f / s, back = s / f;
+            // f is a power of two: f / s == f * RN(1 / s) and s / f == s * (1 / f), exactly
+            const float inv = f * __frcp_rn(s), back = s * (1.0f / f);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const uint32_t b = e2m1_pack2(r[2 * i] * inv, r[2 * i + 1] * inv);
@@ -173,7 +174,8 @@ __device__ __forceinline__ void quant_block4_quad(float (&r)[4], uint32_t (&pk)[
         sc[j] = e4m3_ceil(amax * f * (1.0f / 6.0f), s);
         uint32_t w = 0u;
         if (s > 0.f) {
-            const float inv = f / s, back = s / f;
+            // f is a power of two: f / s == f * RN(1 / s) and s / f == s * (1 / f), exactly
+            const float inv = f * __frcp_rn(s), back = s * (1.0f / f);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const uint32_t b = e2m1_pack2(r[2 * i] * inv, r[2 * i + 1] * inv);
