@@ -382,18 +382,24 @@ __device__ void sm_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
     }
 }
 
-// MMA thread (warp 9, lane 0).  Gate/up atom: four K steps of 64 into the
-// gate and the up accumulator (B = the resident x digits of the atom's
-// chunk); down stage: four K steps per chunk into one accumulator (B = the
-// group's h digits).  Accumulator buffers alternate per segment / unit, in
-// the same order the epilogue reads them.
+// MMA threads (lane 0 of warps 9 and 10: who = 0, 1).  One thread issues a
+// tcgen05.mma every ~80 cycles, well below what the tensor pipe takes at
+// N = 16, so two threads share the work, each always writing its own
+// accumulators (a fixed order of accumulation: bitwise reproducible):
+// gate/up stage: four K steps of 64 each into the gate (who 0) and the up
+// (who 1) accumulator, B = the resident x digits of the atom's chunk; down
+// stage: four K steps per chunk into one accumulator (B = the group's h
+// digits), by who 0 for the CTA's even units and who 1 for the odd ones.
+// Accumulator buffers alternate per segment / unit, in the order the
+// epilogue reads them; the stage, accumulator and completion barriers take
+// one commit from each thread.
 __device__ void sm_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb, SmTabs *sx, const SmShape &sh,
-                            volatile int *abort_flag)
+                            int who, volatile int *abort_flag)
 {
     SmemHdr *hd = tb.hdr;
     const uint32_t tbase = hd->tmem_base, idesc = fp4_idesc(16);
     const int G = gridDim.x, j = blockIdx.x;
-    const int a0 = sm_lo(j, sh.NA, G), a1 = sm_lo(j + 1, sh.NA, G);
+    const int a0 = sm_lo(j, sh.NA, G), a1 = sm_lo(j + 1, sh.NA, G), b0 = sm_lo(j, sh.NB, G);
     int s = 0, nt = 0, slot = 0;
     uint32_t ph = 0;
     const uint32_t xdesc = smem_u32(smem + p.s_off_x), xstride = static_cast<uint32_t>(p.sxrows * 128);
@@ -402,17 +408,19 @@ __device__ void sm_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
         tc_fence_after();
         const int4 h = hd->stage_hdr[s];
         if (h.x == KIND_END) break;
-        bool first, last;
+        bool first, last, mine;
         if (h.x == KIND_A) {
             const int c = h.y % sh.KC;
             first = h.y == a0 || c == 0;
             last = h.y == a1 - 1 || c == sh.KC - 1;
+            mine = true;
         } else {
             first = h.z == 0;
             last = h.z == sh.nPB - 1;
+            mine = ((h.y - b0) & 1) == who;
         }
         const int buf = nt & 1, used = nt >> 1;
-        if (first && used > 0) {
+        if (mine && first && used > 0) {
             if (!wait_bar(&hd->accempty[buf], static_cast<uint32_t>((used - 1) & 1), p, abort_flag)) break;
             tc_fence_after();
         }
@@ -422,14 +430,14 @@ __device__ void sm_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
         if (h.x == KIND_A) {
             const int c = h.y % sh.KC;
             const uint64_t bd = sw128_desc(xdesc + static_cast<uint32_t>(c) * xstride);
+            const uint32_t off = who ? static_cast<uint32_t>(kOffW1) : static_cast<uint32_t>(kOffW0);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
-                tc_mma(dcol, d0 + (kOffW0 + 32 * kk) / 16, bd + 2 * kk, idesc, sfc + 4 * kk, sfc + 32 + 4 * kk, acc);
-                tc_mma(dcol + 16, d0 + (kOffW1 + 32 * kk) / 16, bd + 2 * kk, idesc, sfc + 16 + 4 * kk,
+                tc_mma(dcol + 16u * who, d0 + (off + 32 * kk) / 16, bd + 2 * kk, idesc, sfc + 16u * who + 4 * kk,
                        sfc + 32 + 4 * kk, acc);
             }
-        } else {
+        } else if (mine) {
             const int g = h.y / sh.TO, hs = sm_hslot(g, sh), c0 = 2 * h.z;
             const uint32_t hb = smem_u32(smem + p.s_off_h + hs * (sh.KCI * 2048));
             const int nch = c0 + 1 < sh.KCI ? 2 : 1;
@@ -734,14 +742,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_small_kernel(const __grid_c
     if (tid == 0) {
         for (int i = 0; i < p.NS; ++i) {
             mbar_init(&hd->full[i], 1);
-            mbar_init(&hd->empty[i], 1);
+            mbar_init(&hd->empty[i], 2);  // one commit from each MMA thread
             mbar_init(&hd->sfready[i], 4);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&hd->accfull[b], 1);
+            mbar_init(&hd->accfull[b], 2);
             mbar_init(&hd->accempty[b], 4);
         }
-        mbar_init(&hd->mma_done, 1);
+        mbar_init(&hd->mma_done, 2);
         mbar_init(&hd->epibar, 4);
         mbar_init(&hd->teambar, 8);
         hd->grouped = 0;
@@ -786,18 +794,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_small_kernel(const __grid_c
         if (warp == 8) {
             sm_producer(p, smem, tb, sx, sh, abort_flag);
         } else if (warp == 9) {
-            if ((tid & 31) == 0 && spin_one(p, [&] { return ld_acq_cta(&sx->xready) != 0; }, abort_flag))
-                sm_mma_loop(p, smem, tb, sx, sh, abort_flag);
-        } else if (warp == 10) {
-            // the atom-range start of every CTA and the unit it falls in, for
-            // the h builds (no divisions on their critical path)
-            int2 *alo = reinterpret_cast<int2 *>(smem + p.s_off_alo);
-            for (int jj = tid & 31; jj <= static_cast<int>(gridDim.x); jj += 32) {
-                const int lo = sm_lo(jj, sh.NA, gridDim.x);
-                alo[jj] = make_int2(lo, sh.KC ? lo / sh.KC : 0);
+            if ((tid & 31) == 0) {
+                if (spin_one(p, [&] { return ld_acq_cta(&sx->xready) != 0; }, abort_flag))
+                    sm_mma_loop(p, smem, tb, sx, sh, 0, abort_flag);
+                else
+                    tc_commit(&hd->mma_done);  // (no MMA issued: arrives at once)
             }
-            __syncwarp();
-            if ((tid & 31) == 0) st_rel_cta(&sx->aloready, 1);
+        } else if (warp == 10) {
             // Two sets of expert counters alternate between launches, so none
             // needs resetting at the end of a launch: this launch uses set P
             // (control word 5), and the last CTA to arrive here (control word 6)
@@ -813,6 +816,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_small_kernel(const __grid_c
                     st_release_gpu(p.ctrl + 5, P ^ 1u);
                 }
                 st_rel_cta(&sx->par, static_cast<int>(P) + 1);
+            }
+            // the atom-range start of every CTA and the unit it falls in, for
+            // the h builds (no divisions on their critical path)
+            int2 *alo = reinterpret_cast<int2 *>(smem + p.s_off_alo);
+            for (int jj = tid & 31; jj <= static_cast<int>(gridDim.x); jj += 32) {
+                const int lo = sm_lo(jj, sh.NA, gridDim.x);
+                alo[jj] = make_int2(lo, sh.KC ? lo / sh.KC : 0);
+            }
+            __syncwarp();
+            if ((tid & 31) == 0) st_rel_cta(&sx->aloready, 1);
+            // then the second MMA thread (after what the other warps wait for)
+            if ((tid & 31) == 0) {
+                if (spin_one(p, [&] { return ld_acq_cta(&sx->xready) != 0; }, abort_flag))
+                    sm_mma_loop(p, smem, tb, sx, sh, 1, abort_flag);
+                else
+                    tc_commit(&hd->mma_done);
             }
         } else if (warp == 11) {
             release_loop_common<128>(p, tb, p.H / 128, 4, abort_flag);
