@@ -95,6 +95,26 @@ __device__ __forceinline__ int sm_cta_of(int a, int n, int G)
     return static_cast<int>((static_cast<uint32_t>(a + 1) * static_cast<uint32_t>(G) + static_cast<uint32_t>(n) - 1u) /
                             static_cast<uint32_t>(n)) - 1;
 }
+// CTA j's down units [b0, b1).  With no more groups than CTAs, every CTA
+// serves one group: CTA j takes group floor(j ng / G) and an even share of its
+// TO units among that group's CTAs, so no CTA waits for a second group's h
+// after finishing the first.  With more groups than CTAs the units are split
+// evenly in order.
+__device__ __forceinline__ void sm_units(int j, const SmShape &sh, int G, int &b0, int &b1)
+{
+    if (sh.ng <= G && sh.ng > 0) {
+        const int g = static_cast<int>(static_cast<uint32_t>(j) * sh.ng / static_cast<uint32_t>(G));
+        const int j0 = static_cast<int>((static_cast<uint32_t>(g) * G + sh.ng - 1) / static_cast<uint32_t>(sh.ng));
+        const int j1 = static_cast<int>((static_cast<uint32_t>(g + 1) * G + sh.ng - 1) / static_cast<uint32_t>(sh.ng));
+        const int n = j1 - j0;
+        b0 = g * sh.TO + (j - j0) * sh.TO / n;
+        b1 = g * sh.TO + (j - j0 + 1) * sh.TO / n;
+    } else {
+        b0 = sm_lo(j, sh.NB, G);
+        b1 = sm_lo(j + 1, sh.NB, G);
+    }
+}
+
 __device__ __forceinline__ SmShape sm_shape(const KernelParams &p, int ng, int nE)
 {
     SmShape s;
@@ -236,7 +256,8 @@ __device__ void sm_producer(const KernelParams &p, uint8_t *smem, Tabs tb, const
     const uint64_t pol = policy_evict_first();
     const int G = gridDim.x, j = blockIdx.x;
     const int a0 = sm_lo(j, sh.NA, G), a1 = sm_lo(j + 1, sh.NA, G);
-    const int b0 = sm_lo(j, sh.NB, G), b1 = sm_lo(j + 1, sh.NB, G);
+    int b0, b1;
+    sm_units(j, sh, G, b0, b1);
     int s = 0, fill = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -298,7 +319,9 @@ __device__ void sm_producer(const KernelParams &p, uint8_t *smem, Tabs tb, const
 // The h slot of down group g for this CTA (its first group is slot 0).
 __device__ __forceinline__ int sm_hslot(int g, const SmShape &sh)
 {
-    return g - sm_lo(blockIdx.x, sh.NB, gridDim.x) / sh.TO;
+    int b0, b1;
+    sm_units(blockIdx.x, sh, gridDim.x, b0, b1);
+    return g - b0 / sh.TO;
 }
 
 template <int RND, class Sync>
@@ -329,7 +352,9 @@ __device__ void sm_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
     };
     if (!warp_spin(p, [&] { return ld_acq_cta(&sx->par) != 0; }, abort_flag)) return;
     const uint32_t *gdone = p.sgdone + (sx->par - 1) * kSmMaxPairs;
-    const int gfirst = sm_lo(blockIdx.x, sh.NB, gridDim.x) / sh.TO;
+    int ub0, ub1;
+    sm_units(blockIdx.x, sh, gridDim.x, ub0, ub1);
+    const int gfirst = ub0 / sh.TO;
     const uint32_t sfbase = hd->tmem_base + (static_cast<uint32_t>(32 * q) << 16) + kSfBase;
     auto row = [&](const uint8_t *b, int i) { return *reinterpret_cast<const uint4 *>(b + 16 * i); };
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -399,7 +424,9 @@ __device__ void sm_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
     SmemHdr *hd = tb.hdr;
     const uint32_t tbase = hd->tmem_base, idesc = fp4_idesc(16);
     const int G = gridDim.x, j = blockIdx.x;
-    const int a0 = sm_lo(j, sh.NA, G), a1 = sm_lo(j + 1, sh.NA, G), b0 = sm_lo(j, sh.NB, G);
+    const int a0 = sm_lo(j, sh.NA, G), a1 = sm_lo(j + 1, sh.NA, G);
+    int b0, b1;
+    sm_units(j, sh, G, b0, b1);
     int s = 0, nt = 0, slot = 0;
     uint32_t ph = 0;
     const uint32_t xdesc = smem_u32(smem + p.s_off_x), xstride = static_cast<uint32_t>(p.sxrows * 128);
@@ -502,7 +529,7 @@ __device__ bool sm_build_h(const KernelParams &p, uint8_t *smem, const Tabs &tb,
         // NR rounds from r0: every live row's segments, SB at a time per round
         auto h_rounds = [&](int r0, auto nr_c) {
             constexpr int NR = decltype(nr_c)::value;
-            constexpr int SB = NR == 1 ? 4 : 3;
+            constexpr int SB = 4;
             int cb0[NR], cb1[NR], uu[NR], kk[NR];
             float4 sg[NR], su[NR];
 #pragma unroll
@@ -550,12 +577,8 @@ __device__ bool sm_build_h(const KernelParams &p, uint8_t *smem, const Tabs &tb,
                                          a.z / (1.0f + __expf(-a.z)) * b.z, a.w / (1.0f + __expf(-a.w)) * b.w);
             }
         };
-        if constexpr (RND == 2) {
-            h_rounds(0, std::integral_constant<int, 2>{});
-        } else {
 #pragma unroll
-            for (int rr = 0; rr < RND; ++rr) h_rounds(rr, std::integral_constant<int, 1>{});
-        }
+        for (int rr = 0; rr < RND; ++rr) h_rounds(rr, std::integral_constant<int, 1>{});
         float amax = 0.f;
 #pragma unroll
         for (int rr = 0; rr < RND; ++rr)
@@ -620,7 +643,8 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
     const uint32_t lanebase = hd->tmem_base + (static_cast<uint32_t>(32 * q) << 16);
     const int G = gridDim.x, j = blockIdx.x;
     const int a0 = sm_lo(j, sh.NA, G), a1 = sm_lo(j + 1, sh.NA, G);
-    const int b0 = sm_lo(j, sh.NB, G), b1 = sm_lo(j + 1, sh.NB, G);
+    int b0, b1;
+    sm_units(j, sh, G, b0, b1);
     int nt = 0, nsync = 0, npush = 0;
     bool ok = true;
     // this launch's set of expert counters (published by warp 10 at the start)
