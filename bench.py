@@ -43,25 +43,95 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def measured_traffic():
-    """DRAM bytes per launch of the decode step from the committed ncu summary,
-    if that capture was taken of the kernel sources as they are now (the hash
-    of moe_kernels.cu followed by moe_device.cuh); else None."""
+# The sources each step kernel is built from (a recorded capture stays valid
+# only while they hash the same).
+KERNEL_SOURCES = {
+    "moe_small_kernel": ("moe_small.cu", "moe_device.cuh", "moe_tcgen05.cuh"),
+    "moe_tc_kernel": ("moe_tc.cu", "moe_device.cuh", "moe_tcgen05.cuh"),
+    "moe_step_kernel": ("moe_kernels.cu", "moe_device.cuh"),
+}
+# The kernel the automatic choice runs for each benchmarked workload.
+WORKLOAD_KERNEL = {"decode": "moe_small_kernel", "spec_verify": "moe_tc_kernel", "upper_decode": "moe_tc_kernel",
+                   "prefill": "moe_tc_kernel", "tiny": "moe_step_kernel"}
+# What each kernel computes in: its MMA operand types and accumulator.
+KERNEL_DTYPE = {
+    "moe_small_kernel": ("fp4", "tcgen05 block-scaled FP4 MMA: NVFP4 weights as stored, activations as four "
+                                "FP4 digit rows, fp32 accumulation"),
+    "moe_tc_kernel": ("fp4", "tcgen05 block-scaled FP4 MMA: NVFP4 weights as stored, activations as four FP4 "
+                             "digit rows, fp32 accumulation"),
+    "moe_step_kernel": ("fp16", "mma.sync fp16 operands (E2M1 x E4M3 dequantised exactly, prescaled "
+                                "activations), fp32 accumulation"),
+}
+
+
+def traffic_file():
+    return os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def kernel_source_sha(kernel):
     import hashlib
+    csrc = os.path.join(ROOT, "quantized_moe_routed_gb300", "csrc")
+    return hashlib.sha256(b"".join(open(os.path.join(csrc, f), "rb").read()
+                                   for f in KERNEL_SOURCES[kernel])).hexdigest()
+
+
+def measured_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from profiles/traffic.json
+    (written by --record-traffic from an ncu report), if that capture was taken
+    of the kernel's sources as they are now; else None."""
     try:
-        csrc = os.path.join(ROOT, "quantized_moe_routed_gb300", "csrc")
-        src = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ("moe_kernels.cu", "moe_device.cuh"))
-        sha = hashlib.sha256(src).hexdigest()
-        fields = {}
-        for line in open(os.path.join(ROOT, "profiles", "moe_step_kernel_decode.md")):
-            if ":" in line:
-                key, val = line.split(":", 1)
-                fields[key.strip()] = val.strip()
-        if fields.get("kernel_source_sha256") == sha:
-            return int(fields["traffic_bytes_per_launch"])
-    except (OSError, KeyError, ValueError):
+        rec = json.load(open(traffic_file())).get(f"{kernel}/{workload}")
+        if rec and rec.get("kernel_source_sha256") == kernel_source_sha(kernel):
+            return int(rec["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError, TypeError):
         pass
     return None
+
+
+def record_traffic(report, workload, command):
+    """Read one captured launch's DRAM bytes (read + write) and kernel name from
+    an ncu report and record them in profiles/traffic.json under the kernel's
+    current source hash."""
+    import csv
+    import io
+    out = subprocess.run(["ncu", "-i", report, "--page", "raw", "--csv"], check=True, capture_output=True,
+                         text=True).stdout
+    rows = list(csv.reader(io.StringIO(out)))
+    hdr, vals = rows[0], rows[2]
+    col = {h: i for i, h in enumerate(hdr)}
+    name = vals[col["Kernel Name"]]
+    kernel = next(k for k in KERNEL_SOURCES if k in name)
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    tot = 0.0
+    for m in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+        tot += float(vals[col[m]].replace(",", "")) * scale[rows[1][col[m]]]
+    try:
+        data = json.load(open(traffic_file()))
+    except (OSError, ValueError):
+        data = {}
+    data[f"{kernel}/{workload}"] = {"kernel": kernel, "workload": workload, "dram_bytes_per_launch": int(round(tot)),
+                                    "kernel_source_sha256": kernel_source_sha(kernel), "command": command}
+    with open(traffic_file(), "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+        f.write("\n")
+    return data[f"{kernel}/{workload}"]
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the baseline."""
+    try:
+        for line in subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:  # noqa: BLE001 -- reported as unknown
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 def aggregate_ranks(ms, nbytes, world, device):
@@ -147,7 +217,11 @@ def setup(wl_name, device, kernel=None):
     ws = plan.new_workspace()
     nrot = max(8, GRAPH_STEPS)
     ids_rot = [rotate_ids(ids, s, delta, wl.E).to(device) for s in range(nrot)]
-    return dict(wl=wl, x=x, ids=ids, w=w, W=W, plan=plan, ws=ws, ids_rot=ids_rot, delta=delta,
+    kname = WORKLOAD_KERNEL[wl_name] if kern == binding.MOE_KERNEL_AUTO else (
+        "moe_step_kernel" if kern == binding.MOE_KERNEL_REGISTER else WORKLOAD_KERNEL[wl_name])
+    if kname == "moe_step_kernel" and kern == binding.MOE_KERNEL_AUTO and wl.T * wl.k > 8 and wl.I % 256 == 0:
+        kname = "moe_tc_kernel"
+    return dict(wl=wl, x=x, ids=ids, w=w, W=W, plan=plan, ws=ws, ids_rot=ids_rot, delta=delta, kernel=kname,
                 bytes=algorithmic_bytes(wl, ids), xd=x.to(device), wd=w.to(device),
                 y=torch.empty((wl.T, wl.H), dtype=torch.float32, device=device))
 
@@ -292,7 +366,7 @@ def cpu_baseline(S, seconds=10.0):
     cores = os.cpu_count() or 1
     n, dt = _time_oracle(S, Wc, cores, seconds / 2, 20)
     n1, dt1 = _time_oracle(S, Wc, 1, seconds / 2, 20)
-    return {"value": S["bytes"] / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+    return {"value": S["bytes"] / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle", "cpu": cpu_model(),
             "sample": f"{n} whole step(s) of the {wl.name} workload (T={wl.T}, all touched experts), "
                       f"{dt * 1e3:.1f} ms per step, OpenMP over output rows",
             "single_thread": {"value": S["bytes"] / dt1 / 1e9, "unit": "GB/s", "cores": 1,
@@ -327,7 +401,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "top_k": wl.k,
                    "routing": wl.routing},
-        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle", "cpu": cpu_model(),
                          "sample": f"{args.steps} whole steps of the {wl.name} workload"},
         "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
@@ -344,7 +418,13 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="direct launches only (W warm-up + K steps), for running under a profiler")
+    ap.add_argument("--record-traffic", metavar="NCU_REPORT",
+                    help="record the DRAM bytes of the report's captured launch in profiles/traffic.json")
+    ap.add_argument("--command", default="", help="with --record-traffic: the command the capture ran")
     args = ap.parse_args()
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.record_traffic, args.workload, args.command)))
+        return
     if args.impl == "reference":
         if args.steps > 50:
             args.steps = 5
@@ -376,7 +456,8 @@ def main():
                           "warmup": args.warmup, "status": st_code}))
         return
     g, st = capture(S)
-    reps = max(1, args.steps // GRAPH_STEPS)
+    # at least four graph replays (a spread for the percentiles), at least K steps
+    reps = max(4, -(-args.steps // GRAPH_STEPS))
     steps = reps * GRAPH_STEPS
     warm = max(args.warmup, 3)
     time_graph(g, st, 1, warm)  # warm-up replays (untimed)
@@ -400,7 +481,8 @@ def main():
         "warmup": warm * GRAPH_STEPS, "ms_per_step": ms, "us_per_step": ms * 1e3, "higher_is_better": True,
         # spread over the timed graph replays (each the mean of GRAPH_STEPS steps)
         "us_per_step_p10_p50_p90": [float(np.percentile(per_rep, q)) * 1e3 for q in (10, 50, 90)],
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
+        "scaling": "weak", "vs_baseline": None, "dtype": KERNEL_DTYPE[S["kernel"]][0],
+        "dtype_detail": KERNEL_DTYPE[S["kernel"]][1], "kernel": S["kernel"],
         "data": "synthetic (seeded NVFP4 experts, N(0,0.02) quantised)",
         "config": {"workload": S["wl"].name, "T": S["wl"].T, "H": S["wl"].H, "I": S["wl"].I, "E": S["wl"].E,
                    "top_k": S["wl"].k, "routing": S["wl"].routing, "parallelism": f"replicas x{world}",
@@ -410,7 +492,9 @@ def main():
                                                                        "CUDA events on the launch stream"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                      "frac_of_nominal_8000": gbs / 8000.0,
-                     "traffic": measured_traffic() if S["wl"].name == "decode" else None,
+                     "traffic": measured_traffic(S["kernel"], S["wl"].name),
+                     "traffic_source": "profiles/traffic.json (ncu dram__bytes_read.sum + dram__bytes_write.sum "
+                                       "of one launch, recorded for the kernel's current sources)",
                      "peak_kind": peak_kind},
         "gpu_launches": steps,
         "clocks": ck.summary(),
@@ -419,7 +503,10 @@ def main():
         # null-dequant ceiling (same bytes, no math) on the same schedule
         gn, stn = capture(S, null=True)
         ms_null = time_graph(gn, stn, max(1, reps // 4), 2)
-        out["null_dequant"] = {"us_per_step": ms_null * 1e3, "GB/s": S["bytes"] / (ms_null * 1e-3) / 1e9}
+        out["null_dequant"] = {"us_per_step": ms_null * 1e3, "GB/s": S["bytes"] / (ms_null * 1e-3) / 1e9,
+                               "kernel": "moe_step_kernel",
+                               "form": "the register kernel's schedule with the dequantisation and arithmetic "
+                                       "removed (moe_null_step): its streaming ceiling"}
         ms_e2e, h2d, d2h = time_e2e(S, min(steps, 2000))
         out["e2e"] = {"value": S["bytes"] / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "us_per_step": ms_e2e * 1e3,
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -436,7 +523,9 @@ def main():
                 assert S["plan"].check(S["ws"]) == 0
                 b2 = S["bytes"] / (ms2 * 1e-3) / 1e9
                 sweep[name] = {"T": S["wl"].T, "us_per_step": ms2 * 1e3, "GB/s": b2, "frac": b2 / hbm,
-                               "algorithmic_bytes_per_step": S["bytes"]}
+                               "algorithmic_bytes_per_step": S["bytes"], "kernel": S["kernel"],
+                               "dtype": KERNEL_DTYPE[S["kernel"]][0], "dtype_detail": KERNEL_DTYPE[S["kernel"]][1],
+                               "traffic": measured_traffic(S["kernel"], name)}
             out["decode_sweep"] = sweep
             del S
             S = setup(args.workload, device)

@@ -5,6 +5,7 @@
  * The operation (one MoE layer's routed experts, one step):
  *
  *   y_t = sum_{j < k, slot valid} w_tj * W_down[e_tj] ( SiLU(W_gate[e_tj] x_t) (.) (W_up[e_tj] x_t) )
+ *         [ + W_down_s ( SiLU(W_gate_s x_t) (.) (W_up_s x_t) )   with a shared expert ]
  *
  * for T tokens with router ids e_tj and weights w_tj.  This is the step the
  * serving pages' "lna2" kernel computes ("LNA-CANON.md", section "lna2 とは":
@@ -40,7 +41,7 @@
 extern "C" {
 #endif
 
-#define MOE_NVFP4_ABI_VERSION 4
+#define MOE_NVFP4_ABI_VERSION 5
 
 typedef enum {
     MOE_OK = 0,
@@ -95,6 +96,25 @@ typedef struct {
                 /*     allow it).  Its block scales must be non-negative E4M3     */
                 /*     codes (the MMA reads them unsigned), as an NVFP4 quantiser */
                 /*     writes them.                                               */
+    /* Shared expert (optional; NULL shared_gate_q_dev: none).  One always-on
+     * SwiGLU expert in the same NVFP4 format, added to every token's y with
+     * weight 1 after the routed slots, inside the same launch (the serving
+     * pages run it on a second stream, which deadlocked: "dsv4-carve" README,
+     * "The three traps", trap 3; "LNA-CANON.md" launches with the shared-expert
+     * fusion switched off).  Layouts: gate_q, up_q [I, H/2]; down_q [H, I/2];
+     * gate_s, up_s [I, H/16]; down_s [H, I/16]; ts float [3] = the gate, up
+     * and down tensor scales.  Same alignment rules as the routed arrays. */
+    const uint8_t *shared_gate_q_dev, *shared_up_q_dev, *shared_down_q_dev;
+    const uint8_t *shared_gate_s_dev, *shared_up_s_dev, *shared_down_s_dev;
+    const float *shared_ts_dev;
+    /* Expert range (expert parallelism): this plan serves experts e_lo ..
+     * e_hi-1 of the E the router picks from, and the routed weight arrays
+     * above hold only those (expert e at index e - e_lo).  A valid id outside
+     * the range belongs to another plan and counts as an empty slot here (not
+     * as an error); y is then this plan's partial sum, and the partial sums of
+     * plans over disjoint ranges covering [0, E) add up to the whole step (the
+     * shared expert belongs in exactly one of them).  e_lo = e_hi = 0: all E. */
+    int e_lo, e_hi;
 } moe_plan_desc;
 
 enum { MOE_KERNEL_AUTO = 0, MOE_KERNEL_REGISTER = 1, MOE_KERNEL_TENSOR = 2 };

@@ -13,6 +13,7 @@ Functions:
   moe_forward(...)                 -- y (float64) for all or selected tokens
   group(ids, E)                    -- counts, offsets, perm (stable) + bad count
   route(logits, k)                 -- top-k ids and softmax weights per token
+  quant_row_nvfp4(v)               -- one row quantised once to NVFP4, dequantised
 """
 from __future__ import annotations
 
@@ -65,6 +66,8 @@ def _load():
             lib.oracle_moe_forward_ext.restype = C.c_int
             lib.oracle_group.argtypes = [P, i, i, P, P, P]
             lib.oracle_group.restype = C.c_int
+            lib.oracle_quant_row.argtypes = [P, i, P]
+            lib.oracle_quant_row.restype = None
             lib.oracle_route.argtypes = [P, i, i, i, P, P]
             lib.oracle_route.restype = C.c_int
             _lib = lib
@@ -198,6 +201,17 @@ def group(ids, E: int):
     perm = np.empty(max(P, 1), np.int32)
     bad = _load().oracle_group(_p(idsa), P, E, _p(counts), _p(offsets), _p(perm))
     return counts, offsets, perm[:P], bad
+
+
+def quant_row_nvfp4(v) -> np.ndarray:
+    """One activation row (fp32, length a multiple of 16) quantised once to
+    NVFP4 (row prescale, per-16 E4M3 scale, E2M1) and dequantised (float64)."""
+    va = _np(v, np.float32).reshape(-1)
+    if va.shape[0] % 16:
+        raise ValueError("the row length must be a multiple of 16")
+    out = np.empty(va.shape[0], np.float64)
+    _load().oracle_quant_row(_p(va), va.shape[0], _p(out))
+    return out
 
 
 def route(logits, k: int):

@@ -296,6 +296,12 @@ static void quant_row_nvfp4(const float *v, int n, double *out)
     }
 }
 
+/* quant_row_nvfp4 as an entry point (n a multiple of 16). */
+void oracle_quant_row(const float *v, int n, double *out)
+{
+    quant_row_nvfp4(v, n, out);
+}
+
 /* One (token, expert) pair; act != 0: x already quantised by the caller, h
  * quantised here (expert_pair_q). */
 static void expert_pair_mode(int H, int I, int e, const double *xr,

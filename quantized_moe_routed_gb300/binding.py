@@ -32,7 +32,10 @@ class moe_plan_desc(C.Structure):
                 ("gate_q_dev", C.c_void_p), ("up_q_dev", C.c_void_p), ("down_q_dev", C.c_void_p),
                 ("gate_s_dev", C.c_void_p), ("up_s_dev", C.c_void_p), ("down_s_dev", C.c_void_p),
                 ("gate_ts_dev", C.c_void_p), ("up_ts_dev", C.c_void_p), ("down_ts_dev", C.c_void_p),
-                ("device", C.c_int), ("strict", C.c_int), ("pdl", C.c_int), ("kernel", C.c_int)]
+                ("device", C.c_int), ("strict", C.c_int), ("pdl", C.c_int), ("kernel", C.c_int),
+                ("shared_gate_q_dev", C.c_void_p), ("shared_up_q_dev", C.c_void_p), ("shared_down_q_dev", C.c_void_p),
+                ("shared_gate_s_dev", C.c_void_p), ("shared_up_s_dev", C.c_void_p), ("shared_down_s_dev", C.c_void_p),
+                ("shared_ts_dev", C.c_void_p), ("e_lo", C.c_int), ("e_hi", C.c_int)]
 
 
 MOE_KERNEL_AUTO, MOE_KERNEL_REGISTER, MOE_KERNEL_TENSOR = 0, 1, 2
@@ -122,19 +125,35 @@ def _need(t, dtype, name):
 
 
 # ----------------------------------------------------------------------------- ABI functions
+_SHARED_ARRAYS = ("gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s")
+
+
 def moe_plan_create(weights: dict, H: int, I: int, E: int, top_k: int, T_max: int, device: int = -1,
-                    strict: bool = False, pdl: bool = False, kernel: int = MOE_KERNEL_AUTO):
+                    strict: bool = False, pdl: bool = False, kernel: int = MOE_KERNEL_AUTO, shared: dict = None,
+                    e_range=None):
     """weights: dict with gate_q/up_q/down_q/gate_s/up_s/down_s (uint8) and
-    gate_ts/up_ts/down_ts (float32) CUDA tensors in the ABI layout."""
+    gate_ts/up_ts/down_ts (float32) CUDA tensors in the ABI layout (with
+    e_range = (e_lo, e_hi): the arrays of those experts only).  shared: an
+    optional always-on expert, dict of gate_q/up_q/down_q/gate_s/up_s/down_s
+    (one expert's arrays) and ts (float32 [3])."""
     lib = load_library()
     for n in ("gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s"):
         _need(weights[n], torch.uint8, n)
     for n in ("gate_ts", "up_ts", "down_ts"):
         _need(weights[n], torch.float32, n)
+    sp = [None] * 7
+    if shared is not None:
+        for n in _SHARED_ARRAYS:
+            _need(shared[n], torch.uint8, "shared " + n)
+        _need(shared["ts"], torch.float32, "shared ts")
+        if shared["ts"].numel() != 3:
+            raise MoeError(MOE_ERR_INVALID_ARG, "shared ts must hold the gate, up and down tensor scales")
+        sp = [shared[n].data_ptr() for n in _SHARED_ARRAYS] + [shared["ts"].data_ptr()]
+    e_lo, e_hi = (0, 0) if e_range is None else (int(e_range[0]), int(e_range[1]))
     d = moe_plan_desc(H, I, E, top_k, T_max,
                       *[weights[n].data_ptr() for n in ("gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s",
                                                         "gate_ts", "up_ts", "down_ts")],
-                      device, int(strict), int(pdl), int(kernel))
+                      device, int(strict), int(pdl), int(kernel), *sp, e_lo, e_hi)
     out = C.c_void_p()
     _check(lib.moe_plan_create(C.byref(d), C.byref(out)))
     return out
@@ -282,17 +301,30 @@ def moe_abi_version() -> int:
     return int(load_library().moe_abi_version())
 
 
+def expert_range(E: int, rank: int, world: int):
+    """Experts [e_lo, e_hi) of rank `rank` when `world` ranks split E experts
+    into contiguous ranges whose sizes differ by at most one (the first E %
+    world ranks take one more).  Each rank's plan then holds those experts'
+    arrays only, and the ranks' partial outputs sum to the whole step."""
+    if world < 1 or not 0 <= rank < world or E < world:
+        raise MoeError(MOE_ERR_INVALID_ARG, f"cannot split {E} experts over {world} ranks (rank {rank})")
+    q, r = divmod(E, world)
+    lo = rank * q + min(rank, r)
+    return lo, lo + q + (1 if rank < r else 0)
+
+
 # ----------------------------------------------------------------------------- convenience wrapper
 class MoePlan:
     """Owns a plan handle and keeps the weight tensors alive."""
 
     def __init__(self, weights: dict, H: int, I: int, E: int, top_k: int, T_max: int, device=None,
-                 strict: bool = False, pdl: bool = False, kernel: int = MOE_KERNEL_AUTO):
-        self.weights = weights
+                 strict: bool = False, pdl: bool = False, kernel: int = MOE_KERNEL_AUTO, shared: dict = None,
+                 e_range=None):
+        self.weights, self.shared = weights, shared
         self.H, self.I, self.E, self.top_k, self.T_max = H, I, E, top_k, T_max
         dev = weights["gate_q"].device.index if device is None else device
         self.handle = moe_plan_create(weights, H, I, E, top_k, T_max, device=dev, strict=strict, pdl=pdl,
-                                      kernel=kernel)
+                                      kernel=kernel, shared=shared, e_range=e_range)
 
     def __del__(self):
         h = getattr(self, "handle", None)

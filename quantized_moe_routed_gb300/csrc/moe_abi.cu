@@ -53,6 +53,14 @@ struct Tiling {
     int scale_tmaA = 0, spA = 0, shA = 0, mkA = 0, scale_tmaB = 0, spB = 0, shB = 0, mkB = 0;
     int offGq = 0, offUq = 0, offGs = 0, offUs = 0, offAa = 0, offDq = 0, offDs = 0, offAb = 0;
     CUtensorMap tm[6];
+    CUtensorMap tms[6];  // the shared expert's arrays, same boxes
+};
+
+// One set of expert weight arrays: the routed experts (nexp of them) or the
+// shared expert (nexp = 1).
+struct WeightSet {
+    const void *gq, *uq, *dq, *gs, *us, *ds;
+    uint64_t nexp;
 };
 
 struct moe_plan {
@@ -72,6 +80,11 @@ struct moe_plan {
     // tensor-core kernel: weight tensor maps (128-row boxes), workspace pieces
     bool use_tc = false;
     CUtensorMap tmw[6];
+    CUtensorMap tmws[6];  // the shared expert's, same boxes
+    // pair space: kp slots per token (top_k + a shared expert), Ek experts the
+    // kernels group by (the Eloc routed experts of [e_lo, e_hi) + the shared one)
+    bool shared = false;
+    int kp = 0, Ek = 0, Eloc = 0, e_lo = 0;
     int tc_smem_attr = 0;
     int tc_rows = 0;  // digit rows of xq / hq (4 per pair, at least 64)
     int Ipad = 0;     // I rounded up to 512
@@ -173,15 +186,15 @@ CUresult encode_scale(CUtensorMap *m, const void *base, uint64_t rows_total, int
 
 // Kernel variant for a launch of T tokens: groups of at most 8 pairs (one MMA
 // n-tile) when T*k <= 8, else at most 16 pairs (two n-tiles).
-int ntiles_for(const moe_plan *pl, int T) { return T * pl->d.top_k <= 8 ? 1 : 2; }
+int ntiles_for(const moe_plan *pl, int T) { return T * pl->kp <= 8 ? 1 : 2; }
 
 moe::SmemLayout layout_for(const moe_plan *pl, int T)
 {
     moe::SmemLayout L{};
-    const int P = T * pl->d.top_k;
+    const int P = T * pl->kp;
     const int nt = ntiles_for(pl, T);
     const int red_need = 2 * 8192 * nt;  // two ticket-end reduction buffers
-    const int scr_need = align16i(2 * P) + 8 * pl->d.E + 4 + 16;
+    const int scr_need = align16i(2 * P) + 8 * pl->Ek + 4 + 16;
     L.red_bytes = static_cast<int>(up(red_need > scr_need ? red_need : scr_need, 128));
     L.tab_bytes = moe::tab_bytes_for(P, T);
     {
@@ -241,25 +254,39 @@ moe_status_t build_tiling(const moe_plan_desc &d, int nt, Tiling &tl)
     tl.offDs = moe::kMB * tl.KB / 2;
     tl.offAb = tl.offDs + up1024(moe::kMB * tl.spB);
     // tensor maps (host-only encoding; no device memory involved)
-    const uint64_t rowsGU = static_cast<uint64_t>(d.E) * d.I, rowsD = static_cast<uint64_t>(d.E) * d.H;
+    const WeightSet rw{d.gate_q_dev, d.up_q_dev, d.down_q_dev, d.gate_s_dev, d.up_s_dev, d.down_s_dev,
+                       static_cast<uint64_t>(d.e_hi > d.e_lo ? d.e_hi - d.e_lo : d.E)};
     CUresult cr = CUDA_SUCCESS;
     int mode = 0;
     for (; mode < 2; ++mode) {
         if (mode == 1 && (d.H % 256 || d.I % 256)) break;
-        cr = encode_nib(&tl.tm[0], mode, d.gate_q_dev, rowsGU, d.H, tl.RA, tl.KA);
-        if (cr == CUDA_SUCCESS) cr = encode_nib(&tl.tm[1], mode, d.up_q_dev, rowsGU, d.H, tl.RA, tl.KA);
-        if (cr == CUDA_SUCCESS) cr = encode_nib(&tl.tm[2], mode, d.down_q_dev, rowsD, d.I, moe::kMB, tl.KB);
+        cr = encode_nib(&tl.tm[0], mode, rw.gq, rw.nexp * d.I, d.H, tl.RA, tl.KA);
+        if (cr == CUDA_SUCCESS) cr = encode_nib(&tl.tm[1], mode, rw.uq, rw.nexp * d.I, d.H, tl.RA, tl.KA);
+        if (cr == CUDA_SUCCESS) cr = encode_nib(&tl.tm[2], mode, rw.dq, rw.nexp * d.H, d.I, moe::kMB, tl.KB);
         if (cr == CUDA_SUCCESS) break;
     }
     if (cr != CUDA_SUCCESS || mode >= 2)
         return fail(MOE_ERR_UNSUPPORTED_SHAPE, "tensor-map encoding of the E2M1 rows failed (CUresult %d)",
                     static_cast<int>(cr));
     tl.nib_mode = mode;
-    if (tl.scale_tmaA) {
-        cr = encode_scale(&tl.tm[3], d.gate_s_dev, rowsGU, d.H, tl.RA, pa);
-        if (cr == CUDA_SUCCESS) cr = encode_scale(&tl.tm[4], d.up_s_dev, rowsGU, d.H, tl.RA, pa);
+    auto scales = [&](CUtensorMap *m, const WeightSet &w) {
+        CUresult r = CUDA_SUCCESS;
+        if (tl.scale_tmaA) {
+            r = encode_scale(&m[3], w.gs, w.nexp * d.I, d.H, tl.RA, pa);
+            if (r == CUDA_SUCCESS) r = encode_scale(&m[4], w.us, w.nexp * d.I, d.H, tl.RA, pa);
+        }
+        if (r == CUDA_SUCCESS && tl.scale_tmaB) r = encode_scale(&m[5], w.ds, w.nexp * d.H, d.I, moe::kMB, pb);
+        return r;
+    };
+    cr = scales(tl.tm, rw);
+    if (cr == CUDA_SUCCESS && d.shared_gate_q_dev) {
+        const WeightSet sw{d.shared_gate_q_dev, d.shared_up_q_dev, d.shared_down_q_dev, d.shared_gate_s_dev,
+                           d.shared_up_s_dev, d.shared_down_s_dev, 1};
+        cr = encode_nib(&tl.tms[0], mode, sw.gq, d.I, d.H, tl.RA, tl.KA);
+        if (cr == CUDA_SUCCESS) cr = encode_nib(&tl.tms[1], mode, sw.uq, d.I, d.H, tl.RA, tl.KA);
+        if (cr == CUDA_SUCCESS) cr = encode_nib(&tl.tms[2], mode, sw.dq, d.H, d.I, moe::kMB, tl.KB);
+        if (cr == CUDA_SUCCESS) cr = scales(tl.tms, sw);
     }
-    if (cr == CUDA_SUCCESS && tl.scale_tmaB) cr = encode_scale(&tl.tm[5], d.down_s_dev, rowsD, d.I, moe::kMB, pb);
     if (cr != CUDA_SUCCESS)
         return fail(MOE_ERR_UNSUPPORTED_SHAPE, "tensor-map encoding of the E4M3 scale rows failed (CUresult %d)",
                     static_cast<int>(cr));
@@ -271,16 +298,16 @@ moe_status_t build_tiling(const moe_plan_desc &d, int nt, Tiling &tl)
 // slices of 128 rows in I (the per-pair slice exponent row).
 bool tc_shape_ok(const moe_plan_desc &d) { return d.H % 256 == 0 && d.I % 256 == 0 && d.I <= 4096; }
 
-moe_status_t build_tc_maps(const moe_plan_desc &d, CUtensorMap (&m)[6])
+moe_status_t build_tc_maps(const moe_plan_desc &d, const WeightSet &w, CUtensorMap (&m)[6])
 {
-    const uint64_t rowsGU = static_cast<uint64_t>(d.E) * d.I, rowsD = static_cast<uint64_t>(d.E) * d.H;
+    const uint64_t rowsGU = w.nexp * d.I, rowsD = w.nexp * d.H;
     const PartPlan sp{256, 1, 16, 0, 0};  // scale box: 16 bytes (one 256-element tile) x 128 rows, no swizzle
-    CUresult cr = encode_nib(&m[0], 1, d.gate_q_dev, rowsGU, d.H, moe::kTcRows, 256);
-    if (cr == CUDA_SUCCESS) cr = encode_nib(&m[1], 1, d.up_q_dev, rowsGU, d.H, moe::kTcRows, 256);
-    if (cr == CUDA_SUCCESS) cr = encode_nib(&m[2], 1, d.down_q_dev, rowsD, d.I, moe::kTcRows, 256);
-    if (cr == CUDA_SUCCESS) cr = encode_scale(&m[3], d.gate_s_dev, rowsGU, d.H, moe::kTcRows, sp);
-    if (cr == CUDA_SUCCESS) cr = encode_scale(&m[4], d.up_s_dev, rowsGU, d.H, moe::kTcRows, sp);
-    if (cr == CUDA_SUCCESS) cr = encode_scale(&m[5], d.down_s_dev, rowsD, d.I, moe::kTcRows, sp);
+    CUresult cr = encode_nib(&m[0], 1, w.gq, rowsGU, d.H, moe::kTcRows, 256);
+    if (cr == CUDA_SUCCESS) cr = encode_nib(&m[1], 1, w.uq, rowsGU, d.H, moe::kTcRows, 256);
+    if (cr == CUDA_SUCCESS) cr = encode_nib(&m[2], 1, w.dq, rowsD, d.I, moe::kTcRows, 256);
+    if (cr == CUDA_SUCCESS) cr = encode_scale(&m[3], w.gs, rowsGU, d.H, moe::kTcRows, sp);
+    if (cr == CUDA_SUCCESS) cr = encode_scale(&m[4], w.us, rowsGU, d.H, moe::kTcRows, sp);
+    if (cr == CUDA_SUCCESS) cr = encode_scale(&m[5], w.ds, rowsD, d.I, moe::kTcRows, sp);
     if (cr != CUDA_SUCCESS)
         return fail(MOE_ERR_UNSUPPORTED_SHAPE, "tensor-map encoding for the tensor-core kernel failed (CUresult %d)",
                     static_cast<int>(cr));
@@ -327,6 +354,20 @@ struct WsOffsets {
     int Pmax;  // rows of each part block of xs / hbuf
 };
 
+// Shape and pair-space fields every step kernel takes.
+void set_pair_space(const moe_plan *pl, moe::KernelParams &p)
+{
+    p.H = pl->d.H;
+    p.I = pl->d.I;
+    p.E = pl->Ek;
+    p.k = pl->kp;
+    p.kr = pl->d.top_k;
+    p.Eloc = pl->Eloc;
+    p.Eg = pl->d.E;
+    p.e_lo = pl->e_lo;
+    p.sts = pl->d.shared_ts_dev;
+}
+
 // The tensor-core kernel over T tokens, in launches of at most Tc tokens.
 moe_status_t run_tc(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, int T, void *ws,
                     cudaStream_t cs, Path path)
@@ -366,20 +407,20 @@ moe_status_t run_tc(moe_plan *pl, const void *x, const int32_t *ids, const float
     p.hexp = reinterpret_cast<int8_t *>(wsb + pl->off_hexp);
     p.apart = reinterpret_cast<float *>(wsb + pl->off_apart);
     p.acnt = reinterpret_cast<uint32_t *>(wsb + pl->off_acnt);
-    p.Pmax = pl->Tc * d.top_k;
-    p.H = d.H;
-    p.I = d.I;
-    p.E = d.E;
-    p.k = d.top_k;
+    p.Pmax = pl->Tc * pl->kp;
+    set_pair_space(pl, p);
     p.nHt = d.H / moe::kTcRows;
     p.Ipad = pl->Ipad;
     p.timeout_ns = pl->timeout_ns;
-    for (int i = 0; i < 6; ++i) p.tmt[i] = pl->tmw[i];
+    for (int i = 0; i < 6; ++i) {
+        p.tmt[i] = pl->tmw[i];
+        p.tmts[i] = pl->tmws[i];
+    }
     int launches = 0;
     for (int t0 = 0; t0 < T; t0 += pl->Tc) {
         const int Tn = (T - t0) < pl->Tc ? (T - t0) : pl->Tc;
         const int N = tc_n_for(Tn), G = N / 4;
-        const int P = Tn * d.top_k;
+        const int P = Tn * pl->kp;
         const int tab = moe::tab_bytes_for(P, Tn);
         const int stage = moe::tc_stage_bytes(N);
         const int ep_scratch = 4 * moe::kTcRows * 4;  // the epilogue's h rows, four pairs at a time, fp32
@@ -395,7 +436,7 @@ moe_status_t run_tc(moe_plan *pl, const void *x, const int32_t *ids, const float
         if (nsf > ns) nsf = ns;
         // grouping scratch, aliases the ring: the counting sort's or (P <= 256) the
         // rank sort's ([4][256] u16 tables, 8 ints, the per-expert offsets)
-        const int scr = std::max(align16i(2 * P) + 8 * d.E + 16, 2048 + 32 + 4 * d.E);
+        const int scr = std::max(align16i(2 * P) + 8 * pl->Ek + 16, 2048 + 32 + 4 * pl->Ek);
         if (ns < 2 || nsf < 2 || scr > ns * stage) {
             reject(pl);
             return fail(MOE_ERR_UNSUPPORTED_SHAPE, "tensor-core kernel: shared memory does not fit (%d stages)", ns);
@@ -403,7 +444,7 @@ moe_status_t run_tc(moe_plan *pl, const void *x, const int32_t *ids, const float
         // K splits of the gate/up units: enough tickets for two per SM while
         // every split keeps >= 2 stages and the partial buffer holds them
         const int TA = d.I / moe::kTcRows;
-        int ngmax = d.E + P / G;
+        int ngmax = pl->Ek + P / G;
         if (ngmax > P) ngmax = P;
         const long units = static_cast<long>(ngmax) * TA;
         int KS = 1;
@@ -479,7 +520,7 @@ struct SmallLayout {
 SmallLayout small_layout(const moe_plan *pl, int T)
 {
     SmallLayout L;
-    const int KC = pl->d.H / 256, KCI = pl->d.I / 256, P = T * pl->d.top_k;
+    const int KC = pl->d.H / 256, KCI = pl->d.I / 256, P = T * pl->kp;
     L.xrows = T <= 2 ? 8 : 16;
     // rows 8-15 of the last chunk are read (and ignored) when a chunk holds 8 rows
     const int xbytes = KC * L.xrows * 128 + (L.xrows == 8 ? 1024 : 0);
@@ -533,14 +574,14 @@ moe_status_t run_small(moe_plan *pl, const void *x, const int32_t *ids, const fl
     p.part = reinterpret_cast<float *>(wsb + pl->off_part);
     p.sgdone = reinterpret_cast<uint32_t *>(wsb + pl->off_sgdone);
     p.sapart = reinterpret_cast<float *>(wsb + pl->off_sapart);
-    p.H = d.H;
-    p.I = d.I;
-    p.E = d.E;
-    p.k = d.top_k;
+    set_pair_space(pl, p);
     p.T = T;
-    p.Pmax = pl->Tc * d.top_k;
+    p.Pmax = pl->Tc * pl->kp;
     p.timeout_ns = pl->timeout_ns;
-    for (int i = 0; i < 6; ++i) p.tmt[i] = pl->tmw[i];
+    for (int i = 0; i < 6; ++i) {
+        p.tmt[i] = pl->tmw[i];
+        p.tmts[i] = pl->tmws[i];
+    }
     p.x = static_cast<const uint16_t *>(x);
     p.ids = ids;
     p.w = w;
@@ -617,7 +658,7 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
     if (pl->use_small && path != Path::Null && !wo && T <= pl->T_small)
         return run_small(pl, x, ids, w, y, T, ws, static_cast<cudaStream_t>(stream), path);
     if (pl->use_tc && path != Path::Null && !wo &&
-        (pl->d.kernel == MOE_KERNEL_TENSOR || T * pl->d.top_k > 8))
+        (pl->d.kernel == MOE_KERNEL_TENSOR || T * pl->kp > 8))
         return run_tc(pl, x, ids, w, y, T, ws, static_cast<cudaStream_t>(stream), path);
     // kernel smem attribute: allow up to the device's opt-in limit (once per plan)
     {
@@ -650,12 +691,12 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
     p.href = reinterpret_cast<uint32_t *>(wsb + (wo ? wo->off_href : pl->off_href));
     p.xexp = reinterpret_cast<int32_t *>(wsb + (wo ? wo->off_xexp : pl->off_xexp));
     p.hte = reinterpret_cast<int8_t *>(wsb + (wo ? wo->off_hte : pl->off_hte));
-    p.Pmax = wo ? wo->Pmax : pl->Tc * pl->d.top_k;
+    p.Pmax = wo ? wo->Pmax : pl->Tc * pl->kp;
     p.part = reinterpret_cast<float *>(wsb + (wo ? wo->off_part : pl->off_part));
-    p.H = pl->d.H;
-    p.I = pl->d.I;
-    p.E = pl->d.E;
-    p.k = pl->d.top_k;
+    set_pair_space(pl, p);
+    p.sgs = pl->d.shared_gate_s_dev;
+    p.sus = pl->d.shared_up_s_dev;
+    p.sds = pl->d.shared_down_s_dev;
     p.nHt = pl->nHt;
     p.timeout_ns = pl->timeout_ns;
     p.null_mode = path == Path::Null ? 1 : 0;
@@ -687,7 +728,10 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
             p.nPA = tl.nPA;
             p.KB = tl.KB;
             p.nPB = tl.nPB;
-            for (int i = 0; i < 6; ++i) p.tm[i] = tl.tm[i];
+            for (int i = 0; i < 6; ++i) {
+                p.tm[i] = tl.tm[i];
+                p.tms[i] = tl.tms[i];
+            }
             p.nib_mode = tl.nib_mode;
             p.scale_tmaA = tl.scale_tmaA;
             p.spA = tl.spA;
@@ -767,7 +811,7 @@ moe_status_t static_scratch(int dev, void **out)
 WsOffsets static_layout(const moe_plan *pl, int T)
 {
     WsOffsets o{};
-    const size_t P = static_cast<size_t>(T) * pl->d.top_k;
+    const size_t P = static_cast<size_t>(T) * pl->kp;
     o.off_done = moe::kCtrlBytes;
     o.off_cnt = up(o.off_done + 4 * static_cast<size_t>(moe::kMaxPairs), 256);
     o.off_href = up(o.off_cnt + 4 * static_cast<size_t>(T) * pl->nHt, 256);
@@ -828,6 +872,19 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
         if (!q) return fail(MOE_ERR_INVALID_ARG, "null tensor-scale pointer");
         if (!aligned(q, 4)) return fail(MOE_ERR_MISALIGNED, "tensor-scale pointers must be 4-byte aligned");
     }
+    if (d.shared_gate_q_dev) {
+        const void *sp[] = {d.shared_gate_q_dev, d.shared_up_q_dev, d.shared_down_q_dev,
+                            d.shared_gate_s_dev, d.shared_up_s_dev, d.shared_down_s_dev};
+        for (const void *q : sp) {
+            if (!q) return fail(MOE_ERR_INVALID_ARG, "null shared-expert weight pointer");
+            if (!aligned(q, 16)) return fail(MOE_ERR_MISALIGNED, "shared-expert weight pointers must be 16-byte aligned");
+        }
+        if (!d.shared_ts_dev) return fail(MOE_ERR_INVALID_ARG, "null shared-expert tensor-scale pointer");
+        if (!aligned(d.shared_ts_dev, 4))
+            return fail(MOE_ERR_MISALIGNED, "the shared-expert tensor scales must be 4-byte aligned");
+    }
+    if (!(d.e_lo == 0 && d.e_hi == 0) && !(d.e_lo >= 0 && d.e_lo < d.e_hi && d.e_hi <= d.E))
+        return fail(MOE_ERR_INVALID_ARG, "expert range [%d, %d) is not inside [0, E=%d)", d.e_lo, d.e_hi, d.E);
     int dev = d.device;
     cudaError_t e;
     if (dev < 0) {
@@ -861,6 +918,15 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
         return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     }
     pl->nHt = d.H / moe::kMB;
+    pl->shared = d.shared_gate_q_dev != nullptr;
+    pl->e_lo = d.e_hi > d.e_lo ? d.e_lo : 0;
+    pl->Eloc = d.e_hi > d.e_lo ? d.e_hi - d.e_lo : d.E;
+    pl->kp = d.top_k + (pl->shared ? 1 : 0);
+    pl->Ek = pl->Eloc + (pl->shared ? 1 : 0);
+    if (pl->Ek > moe::kMaxExperts) {
+        delete pl;
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "E=%d plus a shared expert exceeds %d", d.E, moe::kMaxExperts);
+    }
     for (int nt = 1; nt <= 2; ++nt) {
         const moe_status_t ts = build_tiling(d, nt, pl->tl[nt]);
         if (ts != MOE_OK) {
@@ -881,13 +947,20 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
     // not excluded; which kernel a launch takes is decided per launch (run_step)
     pl->use_tc = d.kernel != MOE_KERNEL_REGISTER && tc_shape_ok(d);
     if (pl->use_tc) {
-        const moe_status_t ts = build_tc_maps(d, pl->tmw);
+        const WeightSet rw{d.gate_q_dev, d.up_q_dev, d.down_q_dev, d.gate_s_dev, d.up_s_dev, d.down_s_dev,
+                           static_cast<uint64_t>(pl->Eloc)};
+        moe_status_t ts = build_tc_maps(d, rw, pl->tmw);
+        if (ts == MOE_OK && pl->shared) {
+            const WeightSet sw{d.shared_gate_q_dev, d.shared_up_q_dev, d.shared_down_q_dev, d.shared_gate_s_dev,
+                               d.shared_up_s_dev, d.shared_down_s_dev, 1};
+            ts = build_tc_maps(d, sw, pl->tmws);
+        }
         if (ts != MOE_OK) {
             delete pl;
             return ts;
         }
     }
-    const int tc = moe::kMaxPairs / d.top_k;
+    const int tc = moe::kMaxPairs / pl->kp;
     pl->Tc = d.T_max < tc ? d.T_max : tc;
     const moe::SmemLayout L = layout_for(pl, pl->Tc);
     if (L.NS < 2 || L.total > optin) {
@@ -902,7 +975,7 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
     o = up(o + 4 * static_cast<size_t>(moe::kMaxPairs), 256);
     pl->off_cnt = o;
     o = up(o + 4 * static_cast<size_t>(pl->Tc) * pl->nHt, 256);
-    const size_t Pc = static_cast<size_t>(pl->Tc) * d.top_k;
+    const size_t Pc = static_cast<size_t>(pl->Tc) * pl->kp;
     pl->off_href = o;
     o = up(o + 4 * Pc, 256);
     pl->off_h = o;
@@ -938,10 +1011,10 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
         // the small-launch kernel: its shares follow from the SM count and the
         // largest launch it takes (T_small tokens, at most min(T_small * k, E)
         // active experts and T_small * k down groups)
-        const int ts = std::min(std::min(d.T_max, moe::kSmMaxT), moe::kSmMaxPairs / d.top_k);
+        const int ts = std::min(std::min(d.T_max, moe::kSmMaxT), moe::kSmMaxPairs / pl->kp);
         if (ts >= 1 && !(std::getenv("MOE_SMALL") && std::strcmp(std::getenv("MOE_SMALL"), "0") == 0)) {
-            const long G = sms, KC = d.H / 256, TI = d.I / 128, TO = d.H / 128, Ps = static_cast<long>(ts) * d.top_k;
-            const long NA = std::min<long>(Ps, d.E) * TI * KC, NB = Ps * TO;
+            const long G = sms, KC = d.H / 256, TI = d.I / 128, TO = d.H / 128, Ps = static_cast<long>(ts) * pl->kp;
+            const long NA = std::min<long>(Ps, pl->Ek) * TI * KC, NB = Ps * TO;
             const long LA = (NA + G - 1) / G, LB = (NB + G - 1) / G;
             pl->smaxseg = static_cast<int>((LA - 1) / KC + 2);
             pl->shs = static_cast<int>((LB - 1) / TO + 2);

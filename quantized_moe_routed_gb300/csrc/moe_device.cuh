@@ -246,6 +246,34 @@ __device__ __forceinline__ uint32_t u4w(const uint4 &v, int i)
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
+// ------------------------------------------------------------------ pair space
+// The expert of pair q = t * p.k + j (local index; Eloc: the shared expert),
+// or -1 for a slot that contributes nothing here; an id >= Eg also sets bad.
+__device__ __forceinline__ int pair_expert(const KernelParams &p, int q, bool &bad)
+{
+    const int t = q / p.k, j = q - t * p.k;
+    if (j >= p.kr) return p.Eloc;
+    const int e = p.ids[t * p.kr + j];
+    if (e < 0) return -1;
+    if (e >= p.Eg) {
+        bad = true;
+        return -1;
+    }
+    const int el = e - p.e_lo;
+    return (el >= 0 && el < p.Eloc) ? el : -1;
+}
+// The routing weight of slot j of token t (1 for the shared expert's slot).
+__device__ __forceinline__ float pair_w(const KernelParams &p, int t, int j)
+{
+    return j >= p.kr ? 1.f : p.w[t * p.kr + j];
+}
+// Tensor scale `which` (0 gate, 1 up, 2 down) of local expert e.
+__device__ __forceinline__ float expert_ts(const KernelParams &p, int which, int e)
+{
+    if (e == p.Eloc) return __ldg(p.sts + which);
+    return __ldg((which == 0 ? p.gts : (which == 1 ? p.uts : p.dts)) + e);
+}
+
 // ------------------------------------------------------------------ shared state
 constexpr int kDoneQ = 16;  // finished tickets in flight from the consumers to the helper
 constexpr int kTq = 4;      // tickets fetched ahead (helper -> producer)
@@ -335,7 +363,8 @@ __device__ Tabs make_tabs(uint8_t *smem, int tab_off, int P)
 // threads of the CTA.  Scratch (ids16 [P], ecnt [E], eoff [E+1]) may alias
 // anything not otherwise live.  Results: perm/pos (see Tabs), *n_valid, *n_bad,
 // eoff (exclusive offsets, eoff[E] = n_valid) and ecnt (counts).
-__device__ void group_pairs(const int32_t *__restrict__ ids, int P, int E, int16_t *ids16, int32_t *ecnt,
+template <class GetId>
+__device__ void group_pairs(GetId get_id, int P, int E, int16_t *ids16, int32_t *ecnt,
                             int32_t *eoff, uint16_t *perm, uint16_t *pos, int *n_valid, int *n_bad)
 {
     const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
@@ -344,9 +373,10 @@ __device__ void group_pairs(const int32_t *__restrict__ ids, int P, int E, int16
     __syncthreads();
     int bad = 0;
     for (int p = tid; p < P; p += nthr) {
-        int e = ids[p];
-        if (e >= E) ++bad;
-        ids16[p] = (e >= 0 && e < E) ? static_cast<int16_t>(e) : static_cast<int16_t>(-1);
+        bool b = false;
+        const int e = get_id(p, b);
+        bad += b;
+        ids16[p] = e >= 0 ? static_cast<int16_t>(e) : static_cast<int16_t>(-1);
     }
     if (bad) atomicAdd(n_bad, bad);
     __syncthreads();
@@ -410,9 +440,10 @@ __device__ void group_pairs_warp(const KernelParams &p, int P, int G, Tabs tb)
     SmemHdr *hd = tb.hdr;
     const int lane = threadIdx.x & 31;
     int e = -1;
-    if (lane < P) e = p.ids[lane];
-    const bool valid = lane < P && e >= 0 && e < p.E;
-    const uint32_t badm = __ballot_sync(0xffffffffu, lane < P && e >= p.E);
+    bool b = false;
+    if (lane < P) e = pair_expert(p, lane, b);
+    const bool valid = lane < P && e >= 0;
+    const uint32_t badm = __ballot_sync(0xffffffffu, b);
     const int key = valid ? e : 0x7fffffff;  // invalid pairs sort last
     int rank = 0;
     for (int j = 0; j < P; ++j) {
@@ -583,7 +614,7 @@ __device__ __forceinline__ void combine_tile(const KernelParams &p, const Tabs &
             const int s = j0 + j;
             const int ps = s < p.k ? tb.pos[tok * p.k + s] : 0xFFFF;
             ok[j] = ps != 0xFFFF;
-            wv[j] = ok[j] ? p.w[tok * p.k + s] : 0.f;
+            wv[j] = ok[j] ? pair_w(p, tok, s) : 0.f;
 #pragma unroll
             for (int rr = 0; rr < R; ++rr)
                 pv[rr][j] = ok[j] ? __ldcg(p.part + static_cast<size_t>(ps) * p.H + h0 + rr * 32) : 0.f;

@@ -52,6 +52,8 @@ struct KernelParams {
     //   0 gate_q, 1 up_q, 2 down_q  (E2M1 rows; layout per nib_mode)
     //   3 gate_s, 4 up_s, 5 down_s  (E4M3 scale rows; 2-D box, swizzled)
     CUtensorMap tm[6];
+    CUtensorMap tms[6];   // the same for the shared expert's arrays (rows of one expert)
+    const uint8_t *sgs, *sus, *sds;  // the shared expert's scale arrays
     // weights (NVFP4, layouts as in moe_nvfp4.h)
     const uint8_t *gq, *uq, *dq;
     const uint8_t *gs, *us, *ds;
@@ -71,8 +73,15 @@ struct KernelParams {
     int32_t *xexp;      // [Pmax] register kernel: prescale exponent of each token's x (T > kXexpPrologueT)
     int8_t *hte;        // [nPB][Pmax][kHteRow] register kernel: prescale exponent of each 32-row tile of h
     uint32_t *href;     // [Pmax] register kernel: per pair, 200 - (smallest tile exponent), by red.max
-    // shape
+    // shape.  Pair space: k slots per token = the caller's kr routed slots,
+    // plus one for the shared expert when there is one (its expert index is
+    // Eloc, its weight 1).  E = Eloc + (shared expert): the experts the
+    // kernels group by.  Routed ids are global: [e_lo, e_lo + Eloc) are this
+    // plan's (array index id - e_lo), other ids below Eg belong to another
+    // plan and count as empty slots, ids >= Eg are flagged.
     int H, I, E, k, T;
+    int kr, Eloc, Eg, e_lo;
+    const float *sts;   // the shared expert's tensor scales [3] (gate, up, down)
     int Pmax;           // rows of each part block of xs / hbuf
     // tiling (chosen on the host)
     int RA;             // gate/up: rows of gate (and of up) per ticket (16 or 32)
@@ -95,6 +104,7 @@ struct KernelParams {
     // swizzle); 3 gate_s, 4 up_s, 5 down_s (box 16 B x 128 rows); 6 xq, 8 hq
     // (box 128 B x tcN rows, 128-byte swizzle); 7 xsf, 9 hsf (box 16 B x tcN rows)
     CUtensorMap tmt[10];
+    CUtensorMap tmts[6];  // 0-5 of tmt for the shared expert's arrays
     uint8_t *xq, *xsf;  // [Pmax*4][H/2], [Pmax*4][H/16]: each sorted pair's x as 4 FP4 digit rows
     float *xmul;        // [Pmax*4] multiplier of each x digit row
     uint8_t *hq, *hsf;  // [Pmax*4][Ipad/2], [Pmax*4][Ipad/16]: h digit rows

@@ -479,8 +479,8 @@ __device__ __forceinline__ void consumer_warp(const KernelParams &p, uint8_t *sm
         if (!isA && !warp_spin(p, [&] { return ld_acq_cta_u8(tb.hready + grp) == 2; }, abort_flag)) break;
         if (part == 0) {
             const int e = tb.gexp[grp];
-            ts0 = __ldg(isA ? p.gts + e : p.dts + e);
-            ts1 = isA ? __ldg(p.uts + e) : 0.f;
+            ts0 = expert_ts(p, isA ? 0 : 2, e);
+            ts1 = isA ? expert_ts(p, 1, e) : 0.f;
         }
         const uint8_t *st = smem + s * p.stage_bytes;
         // this warp's tasks in the stage: gate/up chunks q = ksA, ksA + nks, ..
@@ -660,7 +660,12 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
         const int nparts = isA ? p.nPA : p.nPB;
         const int KP = isA ? p.KA : p.KB;
         const uint32_t abytes = static_cast<uint32_t>(gcnt) * 2u * KP;
-        const int row = isA ? e * p.I + tile * p.RA : e * p.H + tile * kMB;
+        // the shared expert (local index Eloc) has arrays of its own
+        const bool shx = e == p.Eloc;
+        const CUtensorMap *TM = shx ? p.tms : p.tm;
+        const uint8_t *GS = shx ? p.sgs : p.gs, *US = shx ? p.sus : p.us, *DS = shx ? p.sds : p.ds;
+        const int eb = shx ? 0 : e;
+        const int row = isA ? eb * p.I + tile * p.RA : eb * p.H + tile * kMB;
         for (int part = 0; part < nparts; ++part) {
             if (!wait_for([&] { return mbar_test(&hd->empty[s], ph ^ 1u); })) {
                 ok = false;
@@ -685,20 +690,20 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
                 mbar_expect_tx(bar, wbytesA + abytes);
                 // gate rows i0..i0+31 and up rows i0..i0+31, K elements part*KA ..
                 if (p.nib_mode == 0) {
-                    tma3d(st + p.offGq, &p.tm[0], 0, row, part * nspA, bar, pol);
-                    tma3d(st + p.offUq, &p.tm[1], 0, row, part * nspA, bar, pol);
+                    tma3d(st + p.offGq, &TM[0], 0, row, part * nspA, bar, pol);
+                    tma3d(st + p.offUq, &TM[1], 0, row, part * nspA, bar, pol);
                 } else {
                     for (int b2 = 0; b2 < p.KA / 256; ++b2) {
-                        tma2d(st + p.offGq + b2 * p.RA * 128, &p.tm[0], part * (p.KA / 2) + b2 * 128, row, bar, pol);
-                        tma2d(st + p.offUq + b2 * p.RA * 128, &p.tm[1], part * (p.KA / 2) + b2 * 128, row, bar, pol);
+                        tma2d(st + p.offGq + b2 * p.RA * 128, &TM[0], part * (p.KA / 2) + b2 * 128, row, bar, pol);
+                        tma2d(st + p.offUq + b2 * p.RA * 128, &TM[1], part * (p.KA / 2) + b2 * 128, row, bar, pol);
                     }
                 }
                 if (p.scale_tmaA) {
-                    tma2d(st + p.offGs, &p.tm[3], part * (p.KA / 16), row, bar, pol);
-                    tma2d(st + p.offUs, &p.tm[4], part * (p.KA / 16), row, bar, pol);
+                    tma2d(st + p.offGs, &TM[3], part * (p.KA / 16), row, bar, pol);
+                    tma2d(st + p.offUs, &TM[4], part * (p.KA / 16), row, bar, pol);
                 } else {
-                    bulk_g2s(st + p.offGs, p.gs + static_cast<size_t>(row) * (p.H / 16), p.RA * (p.H / 16), bar, pol);
-                    bulk_g2s(st + p.offUs, p.us + static_cast<size_t>(row) * (p.H / 16), p.RA * (p.H / 16), bar, pol);
+                    bulk_g2s(st + p.offGs, GS + static_cast<size_t>(row) * (p.H / 16), p.RA * (p.H / 16), bar, pol);
+                    bulk_g2s(st + p.offUs, US + static_cast<size_t>(row) * (p.H / 16), p.RA * (p.H / 16), bar, pol);
                 }
                 if (x_ok) {
                     bulk_g2s(st + p.offAa, p.xs + (static_cast<size_t>(part) * p.Pmax + gbeg) * p.KA, abytes, bar,
@@ -715,15 +720,15 @@ __device__ __forceinline__ void producer_loop(const KernelParams &p, uint8_t *sm
                 mbar_expect_tx(bar, wbytesB + abytes + static_cast<uint32_t>(gcnt) * kHteRow);
                 // down rows h0..h0+63, K elements part*KB ..
                 if (p.nib_mode == 0) {
-                    tma3d(st + p.offDq, &p.tm[2], 0, row, part * nspB, bar, pol);
+                    tma3d(st + p.offDq, &TM[2], 0, row, part * nspB, bar, pol);
                 } else {
                     for (int b2 = 0; b2 < p.KB / 256; ++b2)
-                        tma2d(st + p.offDq + b2 * kMB * 128, &p.tm[2], part * (p.KB / 2) + b2 * 128, row, bar, pol);
+                        tma2d(st + p.offDq + b2 * kMB * 128, &TM[2], part * (p.KB / 2) + b2 * 128, row, bar, pol);
                 }
                 if (p.scale_tmaB)
-                    tma2d(st + p.offDs, &p.tm[5], part * (p.KB / 16), row, bar, pol);
+                    tma2d(st + p.offDs, &TM[5], part * (p.KB / 16), row, bar, pol);
                 else
-                    bulk_g2s(st + p.offDs, p.ds + static_cast<size_t>(row) * (p.I / 16), kMB * (p.I / 16), bar, pol);
+                    bulk_g2s(st + p.offDs, DS + static_cast<size_t>(row) * (p.I / 16), kMB * (p.I / 16), bar, pol);
                 // the h rows: the helper copies them once they exist
                 const int slot = pq_tail % kMaxStages;
                 hd->pq_stage[slot] = s;
@@ -930,7 +935,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_step_kernel(const __grid_cons
             if (tid < 32) group_pairs_warp(p, P, G, tb);
             __syncthreads();
         } else {
-        group_pairs(p.ids, P, p.E, ids16, ecnt, eoff, tb.perm, tb.pos, &hd->n_valid, &hd->n_bad);
+        group_pairs([&](int q, bool &b) { return pair_expert(p, q, b); }, P, p.E, ids16, ecnt, eoff, tb.perm,
+                    tb.pos, &hd->n_valid, &hd->n_bad);
         if (tid < 32) {
             const int lane = tid;
             const int per = (p.E + 31) / 32;
@@ -1039,7 +1045,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t *eoff = ecnt + E;
     uint16_t *perm = reinterpret_cast<uint16_t *>(eoff + E + 1);
     uint16_t *pos = perm + P;
-    group_pairs(ids, P, E, ids16, ecnt, eoff, perm, pos, &n_valid, &n_bad);
+    group_pairs(
+        [&](int q, bool &b) {
+            const int e = ids[q];
+            b = e >= E;
+            return (e >= 0 && e < E) ? e : -1;
+        },
+        P, E, ids16, ecnt, eoff, perm, pos, &n_valid, &n_bad);
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         counts[e] = ecnt[e];
         offsets[e] = eoff[e];

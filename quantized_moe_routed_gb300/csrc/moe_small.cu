@@ -276,20 +276,23 @@ __device__ void sm_producer(const KernelParams &p, uint8_t *smem, Tabs tb, const
     for (int a = a0; a < a1 && ok; ++a) {
         if (!(ok = next_stage())) break;
         const int u = a / sh.KC, c = a - u * sh.KC, ae = u / sh.TI, i = u - ae * sh.TI;
-        const int row = sx->aexp[ae] * p.I + i * 128;
+        const int e = sx->aexp[ae];
+        const CUtensorMap *TM = e == p.Eloc ? p.tmts : p.tmt;  // the shared expert's arrays
+        const int row = (e == p.Eloc ? 0 : e) * p.I + i * 128;
         uint8_t *st = smem + s * p.stage_bytes;
         uint64_t *bar = &hd->full[s];
         hd->stage_hdr[s] = make_int4(KIND_A, a, 0, 0);
         mbar_expect_tx(bar, static_cast<uint32_t>(kSmStage));
-        tma2d(st + kOffW0, &p.tmt[0], c * 128, row, bar, pol);
-        tma2d(st + kOffW1, &p.tmt[1], c * 128, row, bar, pol);
-        tma2d(st + kOffS0, &p.tmt[3], c * 16, row, bar, pol);
-        tma2d(st + kOffS1, &p.tmt[4], c * 16, row, bar, pol);
+        tma2d(st + kOffW0, &TM[0], c * 128, row, bar, pol);
+        tma2d(st + kOffW1, &TM[1], c * 128, row, bar, pol);
+        tma2d(st + kOffS0, &TM[3], c * 16, row, bar, pol);
+        tma2d(st + kOffS1, &TM[4], c * 16, row, bar, pol);
         advance();
     }
     for (int b = b0; b < b1 && ok; ++b) {
-        const int g = b / sh.TO, o = b - g * sh.TO;
-        const int row = tb.gexp[g] * p.H + o * 128;
+        const int g = b / sh.TO, o = b - g * sh.TO, e = tb.gexp[g];
+        const CUtensorMap *TM = e == p.Eloc ? p.tmts : p.tmt;
+        const int row = (e == p.Eloc ? 0 : e) * p.H + o * 128;
         for (int part = 0; part < sh.nPB; ++part) {
             if (!(ok = next_stage())) break;
             const int c0 = 2 * part, two = c0 + 1 < sh.KCI;
@@ -297,11 +300,11 @@ __device__ void sm_producer(const KernelParams &p, uint8_t *smem, Tabs tb, const
             uint64_t *bar = &hd->full[s];
             hd->stage_hdr[s] = make_int4(KIND_B, b, part, 0);
             mbar_expect_tx(bar, static_cast<uint32_t>((two ? 2 : 1) * (16384 + 2048)));
-            tma2d(st + kOffW0, &p.tmt[2], c0 * 128, row, bar, pol);
-            tma2d(st + kOffS0, &p.tmt[5], c0 * 16, row, bar, pol);
+            tma2d(st + kOffW0, &TM[2], c0 * 128, row, bar, pol);
+            tma2d(st + kOffS0, &TM[5], c0 * 16, row, bar, pol);
             if (two) {
-                tma2d(st + kOffW1, &p.tmt[2], (c0 + 1) * 128, row, bar, pol);
-                tma2d(st + kOffS1, &p.tmt[5], (c0 + 1) * 16, row, bar, pol);
+                tma2d(st + kOffW1, &TM[2], (c0 + 1) * 128, row, bar, pol);
+                tma2d(st + kOffS1, &TM[5], (c0 + 1) * 16, row, bar, pol);
             }
             advance();
         }
@@ -692,7 +695,7 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
         tc_wait_ld();
         give_acc();
         const int ae = u / sh.TI, e = sx->aexp[ae];
-        const float tg = __ldg(p.gts + e), tu = __ldg(p.uts + e);
+        const float tg = expert_ts(p, 0, e), tu = expert_ts(p, 1, e);
         float *slot = p.sapart + (static_cast<size_t>(j) * p.smaxseg + (u - a0 / sh.KC)) * kSmSlot;
 #pragma unroll
         for (int t = 0; t < kSmMaxT; ++t)
@@ -719,7 +722,7 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
         // 2c. the group's down units held by this CTA
         const int ulo = max(b0, g * sh.TO), uhi = min(b1, (g + 1) * sh.TO);
         const int e = tb.gexp[g];
-        const float td = __ldg(p.dts + e);
+        const float td = expert_ts(p, 2, e);
         for (int b = ulo; b < uhi; ++b) {
             if (!(ok = take_acc())) break;
             const uint32_t dcol = lanebase + static_cast<uint32_t>((nt & 1) * kAccCols);
@@ -793,6 +796,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_small_kernel(const __grid_c
     if (tid == 256)
         for (int i = 0; i < 6; ++i)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmt[i])) : "memory");
+    if (tid == 288 && p.k > p.kr)
+        for (int i = 0; i < 6; ++i)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmts[i])) : "memory");
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

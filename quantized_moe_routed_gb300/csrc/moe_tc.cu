@@ -108,9 +108,10 @@ __device__ void tc_group_pairs(const KernelParams &p, int P, int16_t *ids16, int
     grp_sync();
     int bad = 0;
     for (int q = lt; q < P; q += 128) {
-        const int e = p.ids[q];
-        if (e >= E) ++bad;
-        ids16[q] = (e >= 0 && e < E) ? static_cast<int16_t>(e) : static_cast<int16_t>(-1);
+        bool b = false;
+        const int e = pair_expert(p, q, b);
+        bad += b;
+        ids16[q] = e >= 0 ? static_cast<int16_t>(e) : static_cast<int16_t>(-1);
     }
     if (bad) atomicAdd(&hd->n_bad, bad);
     grp_sync();
@@ -187,10 +188,10 @@ __device__ void tc_group_small(const KernelParams &p, int P, int G, uint8_t *scr
     for (int q = lt; q < 256; q += 128) {
         int e = -1;
         if (q < P) {
-            e = p.ids[q];
-            bad += e >= E;
-            if (e < 0 || e >= E) e = -1;
-            inval += q < P && e < 0;
+            bool b = false;
+            e = pair_expert(p, q, b);
+            bad += b;
+            inval += e < 0;
         }
         ids16[q] = static_cast<uint16_t>(e);  // 0xFFFF: invalid or past P
     }
@@ -771,13 +772,13 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
         ++nt;
 
         if (!isA) {
-            const float ts = __ldg(p.dts + e);
+            const float ts = expert_ts(p, 2, e);
             const int h0 = tile * kTcRows;
 #pragma unroll
             for (int i = 0; i < GP; ++i)
                 if (i < gcnt) p.part[static_cast<size_t>(gbeg + i) * p.H + h0 + r] = g[i] * ts;
         } else {
-            const float tg = __ldg(p.gts + e), tu = __ldg(p.uts + e);
+            const float tg = expert_ts(p, 0, e), tu = expert_ts(p, 1, e);
 #pragma unroll
             for (int i = 0; i < GP; ++i) {
                 g[i] *= tg;
@@ -1057,15 +1058,18 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
             }
             uint8_t *st = smem + s * p.stage_bytes;
             uint64_t *bar = &hd->full[s];
+            // the shared expert (local index Eloc) has arrays of its own
+            const CUtensorMap *TM = e == p.Eloc ? p.tmts : p.tmt;
+            const int eb = e == p.Eloc ? 0 : e;
             if (ti.isA) {
                 const int kc = ti.ks * nPA + part;  // 256-element chunk of H
-                const int row = e * p.I + ti.tile * kTcRows;
+                const int row = eb * p.I + ti.tile * kTcRows;
                 hd->stage_hdr[s] = make_int4(KIND_A, ti.grp, ti.tile, part | (ti.ks << 16) | (tc_lg(ti.nks) << 20));
                 mbar_expect_tx(bar, static_cast<uint32_t>(2 * kTile + 2 * kSfTile + p.tcNA * 128 + p.tcNA * 16));
-                tma2d(st + kOffW0, &p.tmt[0], kc * 128, row, bar, pol);
-                tma2d(st + kOffW1, &p.tmt[1], kc * 128, row, bar, pol);
-                tma2d(st + kOffS0, &p.tmt[3], kc * 16, row, bar, pol);
-                tma2d(st + kOffS1, &p.tmt[4], kc * 16, row, bar, pol);
+                tma2d(st + kOffW0, &TM[0], kc * 128, row, bar, pol);
+                tma2d(st + kOffW1, &TM[1], kc * 128, row, bar, pol);
+                tma2d(st + kOffS0, &TM[3], kc * 16, row, bar, pol);
+                tma2d(st + kOffS1, &TM[4], kc * 16, row, bar, pol);
                 // x complete (the flag epilogue warp 4 raises; a shared-memory read)
                 if (!x_ok && ld_acq_cta(&hd->xready)) flush_x();
                 if (x_ok) {
@@ -1076,13 +1080,13 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
                 }
             } else {
                 const int kc0 = 2 * part;  // 256-element chunks of I
-                const int row = e * p.H + ti.tile * kTcRows;
+                const int row = eb * p.H + ti.tile * kTcRows;
                 hd->stage_hdr[s] = make_int4(KIND_B, ti.grp, ti.tile, part);
                 mbar_expect_tx(bar, static_cast<uint32_t>(2 * kTile + 2 * kSfTile + 2 * N * 128 + 2 * N * 16));
-                tma2d(st + kOffW0, &p.tmt[2], kc0 * 128, row, bar, pol);
-                tma2d(st + kOffW1, &p.tmt[2], (kc0 + 1) * 128, row, bar, pol);
-                tma2d(st + kOffS0, &p.tmt[5], kc0 * 16, row, bar, pol);
-                tma2d(st + kOffS1, &p.tmt[5], (kc0 + 1) * 16, row, bar, pol);
+                tma2d(st + kOffW0, &TM[2], kc0 * 128, row, bar, pol);
+                tma2d(st + kOffW1, &TM[2], (kc0 + 1) * 128, row, bar, pol);
+                tma2d(st + kOffS0, &TM[5], kc0 * 16, row, bar, pol);
+                tma2d(st + kOffS1, &TM[5], (kc0 + 1) * 16, row, bar, pol);
                 queue_copy(s, ti.grp, part, KIND_B);
             }
             ++fill;

@@ -38,7 +38,8 @@ import torch
 
 __all__ = [
     "Workload", "WORKLOADS", "quantize_nvfp4", "make_x", "make_x_variant", "make_topk_w",
-    "make_topk_ids", "make_router_logits", "make_expert_weights", "make_inputs", "rotate_ids",
+    "make_topk_ids", "make_router_logits", "make_expert_weights", "make_shared_weights", "expert_slice",
+    "make_inputs", "rotate_ids",
     "rotation_delta", "touched_experts", "algorithmic_bytes",
 ]
 
@@ -303,9 +304,34 @@ def rotation_delta(ids: torch.Tensor, E: int, window: int = 4, start: int = 8) -
     return start
 
 
-def algorithmic_bytes(wl: Workload, ids: torch.Tensor) -> int:
+def make_shared_weights(wl: Workload, device="cpu"):
+    """One always-on (shared) expert in the same NVFP4 layout as a routed
+    expert, drawn like expert index E (its own seeded generators): a dict of
+    gate_q/up_q [I, H/2], down_q [H, I/2], gate_s/up_s [I, H/16],
+    down_s [H, I/16] (uint8) and ts (float32 [3]: gate, up, down)."""
+    dev = torch.device(device)
+    H, I = wl.H, wl.I
+    out, ts = {}, []
+    for proj, (name, rows, K) in enumerate((("gate", I, H), ("up", I, H), ("down", H, I))):
+        g = torch.Generator(device=dev).manual_seed(_weight_seed(wl.seed, proj, wl.E))
+        w = torch.randn((rows, K), generator=g, device=dev, dtype=torch.float32)
+        w.mul_(wl.weight_std)
+        q, sc, t = quantize_nvfp4(w)
+        out[name + "_q"], out[name + "_s"] = q.contiguous(), sc.contiguous()
+        ts.append(float(t))
+    out["ts"] = torch.tensor(ts, dtype=torch.float32, device=dev)
+    return out
+
+
+def expert_slice(W: dict, e_lo: int, e_hi: int) -> dict:
+    """The arrays of experts e_lo .. e_hi-1 only (what a plan serving that
+    expert range holds), as contiguous copies."""
+    return {k: v[e_lo:e_hi].contiguous() for k, v in W.items()}
+
+
+def algorithmic_bytes(wl: Workload, ids: torch.Tensor, shared: bool = False) -> int:
     """Bytes the step must move: each touched expert's E2M1 values, E4M3 scales and
     three fp32 tensor scales, plus x (bf16), ids (int32), weights (fp32) and y (fp32)."""
-    n = len(touched_experts(ids, wl.E))
+    n = len(touched_experts(ids, wl.E)) + (1 if shared else 0)
     per_expert = 3 * wl.I * wl.H // 2 + 3 * wl.I * wl.H // 16 + 12
     return n * per_expert + wl.T * wl.H * 2 + wl.T * wl.k * 8 + wl.T * wl.H * 4

@@ -33,12 +33,20 @@ def test_traffic_is_reported_only_for_the_profiled_sources(tmp_path, monkeypatch
     csrc = tmp_path / "quantized_moe_routed_gb300" / "csrc"
     csrc.mkdir(parents=True)
     (tmp_path / "profiles").mkdir()
-    (csrc / "moe_kernels.cu").write_bytes(b"kernel v1\n")
-    (csrc / "moe_device.cuh").write_bytes(b"helpers v1\n")
-    sha = hashlib.sha256(b"kernel v1\nhelpers v1\n").hexdigest()
-    (tmp_path / "profiles" / "moe_step_kernel_decode.md").write_text(
-        f"# summary\nkernel_source_sha256: {sha}\ntraffic_bytes_per_launch: 57300480\n")
+    for f, body in (("moe_small.cu", b"kernel v1\n"), ("moe_device.cuh", b"helpers v1\n"),
+                    ("moe_tcgen05.cuh", b"tc v1\n")):
+        (csrc / f).write_bytes(body)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.measured_traffic() == 57300480
+    sha = hashlib.sha256(b"kernel v1\nhelpers v1\ntc v1\n").hexdigest()
+    assert bench.kernel_source_sha("moe_small_kernel") == sha
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
+        {"moe_small_kernel/decode": {"kernel": "moe_small_kernel", "workload": "decode",
+                                     "dram_bytes_per_launch": 56773376, "kernel_source_sha256": sha}}))
+    assert bench.measured_traffic("moe_small_kernel", "decode") == 56773376
+    assert bench.measured_traffic("moe_small_kernel", "spec_verify") is None   # not captured
     (csrc / "moe_device.cuh").write_bytes(b"helpers v2\n")       # a source changed since the capture
-    assert bench.measured_traffic() is None
+    assert bench.measured_traffic("moe_small_kernel", "decode") is None
+
+
+def test_cpu_model_is_named():
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()

@@ -16,6 +16,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_ext as ext
 import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(os.path.abspath(oracle.__file__)), "moe_oracle.c")
@@ -67,6 +68,18 @@ MUTANTS = {
     "route_inf_winner_as_softmax": ("double ej = (m == INFINITY) ? (sel[j] == INFINITY ? 1.0 : 0.0) : exp(sel[j] - m);",
                                     "double ej = exp(sel[j] - m);"),
     "route_ids_of_token_0": ("const float *lt = logits + (size_t)t * E;", "const float *lt = logits;"),
+    # the step's extensions: shared expert, expert range, single NVFP4 activation quantisation
+    "shared_with_last_slot_weight": ("            for (int r = 0; r < H; ++r)\n                yt[r] += o[r];",
+                                     "            for (int r = 0; r < H; ++r)\n                yt[r] += (double)w[(size_t)t * k + (size_t)(k - 1)] * o[r];"),
+    "shared_up_scale_for_gate": ("sg_q, sg_s, s_ts + 0,", "sg_q, sg_s, s_ts + 1,"),
+    "range_offset_dropped": ("expert_pair_mode(H, I, e - e_lo,", "expert_pair_mode(H, I, e,"),
+    "range_outside_counted_bad": ("            if (e < e_lo || e >= e_hi)\n                continue;",
+                                  "            if (e < e_lo || e >= e_hi) {\n                ++bad;\n                continue;\n            }"),
+    "quant_scale_not_raised": ("        if (tab_e4m3[c] < (double)a && c < 0x7Eu)\n            ++c;",
+                               "        if (0)\n            ++c;"),
+    "quant_e2m1_ties_up": ("if (d < bd || (d == bd && (c & 1u) == 0))\n            best = c, bd = d;\n    }\n    return best;\n}\n\n/* One row",
+                           "if (d <= bd)\n            best = c, bd = d;\n    }\n    return best;\n}\n\n/* One row"),
+    "quant_prescale_off_by_one": ("int e = (m <= 1.3125 ? 11 : 10) - E;", "int e = (m <= 1.3125 ? 12 : 10) - E;"),
 }
 
 
@@ -88,7 +101,18 @@ def _pin_checks():
         ("route_brute_force", lambda: pins.test_route_against_brute_force(16, 256, 8, 1)),
         ("route_ties_nan_extremes", pins.test_route_ties_nan_and_extremes),
         ("route_invariants", pins.test_route_invariants),
+        ("quant_row_grid", ext.test_quant_row_is_exact_on_the_grid),
+        ("quant_row_ties", ext.test_quant_row_ties_to_even),
+        ("quant_row_raised_scale", ext.test_quant_row_raises_the_block_scale),
+        ("quant_row_bound", lambda: ext.test_quant_row_scale_sign_invariance_and_bound(0)),
+        ("quant_row_zeros", ext.test_quant_row_of_zeros_and_tiny_blocks),
     ]
+    ecase = ext.make_case()
+    for name in ("shared_expert_alone_is_the_dense_mlp", "shared_expert_adds_after_the_routed_slots",
+                 "expert_range_still_flags_ids_past_E", "one_expert_range_is_the_step_with_other_slots_emptied"):
+        fn = getattr(ext, "test_" + name)
+        checks.append((name, lambda fn=fn: fn(ecase)))
+    checks.append(("expert_range_partials", lambda: ext.test_expert_range_partials_sum_to_the_whole_step(ecase, 3)))
     for name in ("zero_weights_give_zero", "token_permutation_permutes_output", "power_of_two_scaling",
                  "slot_linearity", "empty_and_bad_slots", "duplicate_slots_add", "token_subset_matches_full",
                  "thread_count_does_not_change_result"):
@@ -102,7 +126,8 @@ def _build(src_text, out_dir, name):
     lib = os.path.join(out_dir, "lib" + name + ".so")
     with open(src, "w") as f:
         f.write(src_text)
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", lib, src, "-lm"],
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-o", lib, src,
+                    "-lm"],
                    check=True, capture_output=True)
     return lib
 
