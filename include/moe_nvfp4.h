@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define MOE_NVFP4_ABI_VERSION 5
+#define MOE_NVFP4_ABI_VERSION 6
 
 typedef enum {
     MOE_OK = 0,
@@ -115,6 +115,17 @@ typedef struct {
      * plans over disjoint ranges covering [0, E) add up to the whole step (the
      * shared expert belongs in exactly one of them).  e_lo = e_hi = 0: all E. */
     int e_lo, e_hi;
+    /* Activation quantisation.  0: x and h enter the MMAs as four FP4 digit
+     * rows (close to their bf16 / fp32 values).  1: x and h are quantised
+     * once to NVFP4 before each projection, as a checkpoint that ships
+     * activation input scales expects (the V100 page, section 3.0, adds the
+     * missing input_scale tensors before launch): per row one power-of-two
+     * prescale (largest |v| into (1344, 2688]), per 16 elements the smallest
+     * E4M3 scale >= block max / 6, each element the nearest E2M1 value (ties
+     * to even) of v / scale.  Tensor-core kernels only: a plan with kernel =
+     * MOE_KERNEL_REGISTER or a shape they do not take is refused with
+     * UNSUPPORTED_SHAPE, and moe_decode_static refuses such a plan. */
+    int act_quant;
 } moe_plan_desc;
 
 enum { MOE_KERNEL_AUTO = 0, MOE_KERNEL_REGISTER = 1, MOE_KERNEL_TENSOR = 2 };

@@ -35,7 +35,7 @@ class moe_plan_desc(C.Structure):
                 ("device", C.c_int), ("strict", C.c_int), ("pdl", C.c_int), ("kernel", C.c_int),
                 ("shared_gate_q_dev", C.c_void_p), ("shared_up_q_dev", C.c_void_p), ("shared_down_q_dev", C.c_void_p),
                 ("shared_gate_s_dev", C.c_void_p), ("shared_up_s_dev", C.c_void_p), ("shared_down_s_dev", C.c_void_p),
-                ("shared_ts_dev", C.c_void_p), ("e_lo", C.c_int), ("e_hi", C.c_int)]
+                ("shared_ts_dev", C.c_void_p), ("e_lo", C.c_int), ("e_hi", C.c_int), ("act_quant", C.c_int)]
 
 
 MOE_KERNEL_AUTO, MOE_KERNEL_REGISTER, MOE_KERNEL_TENSOR = 0, 1, 2
@@ -130,12 +130,13 @@ _SHARED_ARRAYS = ("gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s")
 
 def moe_plan_create(weights: dict, H: int, I: int, E: int, top_k: int, T_max: int, device: int = -1,
                     strict: bool = False, pdl: bool = False, kernel: int = MOE_KERNEL_AUTO, shared: dict = None,
-                    e_range=None):
+                    e_range=None, act_quant: bool = False):
     """weights: dict with gate_q/up_q/down_q/gate_s/up_s/down_s (uint8) and
     gate_ts/up_ts/down_ts (float32) CUDA tensors in the ABI layout (with
     e_range = (e_lo, e_hi): the arrays of those experts only).  shared: an
     optional always-on expert, dict of gate_q/up_q/down_q/gate_s/up_s/down_s
-    (one expert's arrays) and ts (float32 [3])."""
+    (one expert's arrays) and ts (float32 [3]).  act_quant: x and h quantised
+    once to NVFP4 before each projection (tensor-core kernels only)."""
     lib = load_library()
     for n in ("gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s"):
         _need(weights[n], torch.uint8, n)
@@ -153,7 +154,7 @@ def moe_plan_create(weights: dict, H: int, I: int, E: int, top_k: int, T_max: in
     d = moe_plan_desc(H, I, E, top_k, T_max,
                       *[weights[n].data_ptr() for n in ("gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s",
                                                         "gate_ts", "up_ts", "down_ts")],
-                      device, int(strict), int(pdl), int(kernel), *sp, e_lo, e_hi)
+                      device, int(strict), int(pdl), int(kernel), *sp, e_lo, e_hi, int(bool(act_quant)))
     out = C.c_void_p()
     _check(lib.moe_plan_create(C.byref(d), C.byref(out)))
     return out
@@ -319,12 +320,12 @@ class MoePlan:
 
     def __init__(self, weights: dict, H: int, I: int, E: int, top_k: int, T_max: int, device=None,
                  strict: bool = False, pdl: bool = False, kernel: int = MOE_KERNEL_AUTO, shared: dict = None,
-                 e_range=None):
+                 e_range=None, act_quant: bool = False):
         self.weights, self.shared = weights, shared
         self.H, self.I, self.E, self.top_k, self.T_max = H, I, E, top_k, T_max
         dev = weights["gate_q"].device.index if device is None else device
         self.handle = moe_plan_create(weights, H, I, E, top_k, T_max, device=dev, strict=strict, pdl=pdl,
-                                      kernel=kernel, shared=shared, e_range=e_range)
+                                      kernel=kernel, shared=shared, e_range=e_range, act_quant=act_quant)
 
     def __del__(self):
         h = getattr(self, "handle", None)

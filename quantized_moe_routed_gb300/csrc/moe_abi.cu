@@ -85,10 +85,12 @@ struct moe_plan {
     // kernels group by (the Eloc routed experts of [e_lo, e_hi) + the shared one)
     bool shared = false;
     int kp = 0, Ek = 0, Eloc = 0, e_lo = 0;
+    int nd = 4;  // FP4 digits per activation block: 4, or 1 (act_quant: x and h quantised once)
     int tc_smem_attr = 0;
     int tc_rows = 0;  // digit rows of xq / hq (4 per pair, at least 64)
     int Ipad = 0;     // I rounded up to 512
     size_t off_xq = 0, off_xsf = 0, off_xmul = 0, off_hq = 0, off_hsf = 0, off_hexp = 0, off_apart = 0, off_acnt = 0;
+    size_t off_hf = 0;  // act_quant: h in fp32 ([Tc * kp][I])
     // small-launch tensor-core kernel (launches of at most T_small tokens)
     bool use_small = false;
     int T_small = 0, smaxseg = 0, shs = 0, small_smem_attr = 0;
@@ -366,6 +368,7 @@ void set_pair_space(const moe_plan *pl, moe::KernelParams &p)
     p.Eg = pl->d.E;
     p.e_lo = pl->e_lo;
     p.sts = pl->d.shared_ts_dev;
+    p.nd = pl->nd;
 }
 
 // The tensor-core kernel over T tokens, in launches of at most Tc tokens.
@@ -407,6 +410,7 @@ moe_status_t run_tc(moe_plan *pl, const void *x, const int32_t *ids, const float
     p.hexp = reinterpret_cast<int8_t *>(wsb + pl->off_hexp);
     p.apart = reinterpret_cast<float *>(wsb + pl->off_apart);
     p.acnt = reinterpret_cast<uint32_t *>(wsb + pl->off_acnt);
+    p.hf = pl->nd == 1 ? reinterpret_cast<float *>(wsb + pl->off_hf) : nullptr;
     p.Pmax = pl->Tc * pl->kp;
     set_pair_space(pl, p);
     p.nHt = d.H / moe::kTcRows;
@@ -658,7 +662,7 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
     if (pl->use_small && path != Path::Null && !wo && T <= pl->T_small)
         return run_small(pl, x, ids, w, y, T, ws, static_cast<cudaStream_t>(stream), path);
     if (pl->use_tc && path != Path::Null && !wo &&
-        (pl->d.kernel == MOE_KERNEL_TENSOR || T * pl->kp > 8))
+        (pl->d.kernel == MOE_KERNEL_TENSOR || T * pl->kp > 8 || pl->nd == 1))
         return run_tc(pl, x, ids, w, y, T, ws, static_cast<cudaStream_t>(stream), path);
     // kernel smem attribute: allow up to the device's opt-in limit (once per plan)
     {
@@ -885,6 +889,7 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
     }
     if (!(d.e_lo == 0 && d.e_hi == 0) && !(d.e_lo >= 0 && d.e_lo < d.e_hi && d.e_hi <= d.E))
         return fail(MOE_ERR_INVALID_ARG, "expert range [%d, %d) is not inside [0, E=%d)", d.e_lo, d.e_hi, d.E);
+    if (d.act_quant != 0 && d.act_quant != 1) return fail(MOE_ERR_INVALID_ARG, "act_quant=%d is not 0 or 1", d.act_quant);
     int dev = d.device;
     cudaError_t e;
     if (dev < 0) {
@@ -946,6 +951,14 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
     // the tensor-core kernel is available when the shape allows it and it was
     // not excluded; which kernel a launch takes is decided per launch (run_step)
     pl->use_tc = d.kernel != MOE_KERNEL_REGISTER && tc_shape_ok(d);
+    pl->nd = d.act_quant ? 1 : 4;
+    if (d.act_quant && !pl->use_tc) {
+        delete pl;
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE,
+                    "act_quant runs on the tensor-core kernels only: kernel=%d, H=%d, I=%d (H and I multiples of 256, "
+                    "I <= 4096, kernel not MOE_KERNEL_REGISTER)",
+                    d.kernel, d.H, d.I);
+    }
     if (pl->use_tc) {
         const WeightSet rw{d.gate_q_dev, d.up_q_dev, d.down_q_dev, d.gate_s_dev, d.up_s_dev, d.down_s_dev,
                            static_cast<uint64_t>(pl->Eloc)};
@@ -1008,6 +1021,10 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
         o = up(o + static_cast<size_t>(moe::kTcApartUnits) * 2 * 16 * moe::kTcRows * 4, 256);
         pl->off_acnt = o;
         o = up(o + static_cast<size_t>(moe::kTcApartUnits) * 4, 256);
+        if (pl->nd == 1) {
+            pl->off_hf = o;
+            o = up(o + Pc * d.I * 4, 256);
+        }
         // the small-launch kernel: its shares follow from the SM count and the
         // largest launch it takes (T_small tokens, at most min(T_small * k, E)
         // active experts and T_small * k down groups)
@@ -1109,6 +1126,10 @@ moe_status_t moe_decode_static(moe_plan_t plan, const void *x_dev, const int32_t
         reject(plan);
         return fail(MOE_ERR_INVALID_ARG, "moe_decode_static takes 0 <= T <= min(%d, T_max=%d), got %d",
                     moe::kDecodeMaxT, plan->d.T_max, T);
+    }
+    if (plan->nd == 1) {  // the static scratch serves the register kernel, which has no single quantisation
+        reject(plan);
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "moe_decode_static does not take an act_quant plan");
     }
     if (T == 0) return MOE_OK;
     moe_status_t st = check_device(plan);

@@ -82,6 +82,7 @@ struct KernelParams {
     int H, I, E, k, T;
     int kr, Eloc, Eg, e_lo;
     const float *sts;   // the shared expert's tensor scales [3] (gate, up, down)
+    int nd;             // FP4 digits per activation block: 4, or 1 (x and h quantised once to NVFP4)
     int Pmax;           // rows of each part block of xs / hbuf
     // tiling (chosen on the host)
     int RA;             // gate/up: rows of gate (and of up) per ticket (16 or 32)
@@ -109,6 +110,7 @@ struct KernelParams {
     float *xmul;        // [Pmax*4] multiplier of each x digit row
     uint8_t *hq, *hsf;  // [Pmax*4][Ipad/2], [Pmax*4][Ipad/16]: h digit rows
     int8_t *hexp;       // [Pmax][64]: prescale exponent of each 128-row slice of h; [32] the pair's reference
+    float *hf;          // [Pmax][I] (nd == 1 only): h in fp32, for the blocks whose rebased scale is subnormal
     float *apart;       // split-K partial gate/up sums
     uint32_t *acnt;     // split-K arrivals per gate/up unit
     int tcN;            // MMA N: digit rows per group (16, 32 or 64; a group has <= tcN/4 pairs)

@@ -227,7 +227,7 @@ __device__ void sm_quantize_x(const KernelParams &p, uint8_t *smem, SmTabs *sx)
         }
         uint2 pk[4];
         uint32_t sc[4];
-        quant_block4(v, pk, sc);
+        quant_block4(v, pk, sc, p.nd);
         const int c = b >> 4, bb = b & 15;
 #pragma unroll
         for (int d = 0; d < 4; ++d) {
@@ -607,7 +607,7 @@ __device__ bool sm_build_h(const KernelParams &p, uint8_t *smem, const Tabs &tb,
             if (1024 * rr + 128 * (wq + 1) > p.I) continue;  // past I: the whole warp (I % 256 == 0)
             float v[4] = {hv[rr].x * P, hv[rr].y * P, hv[rr].z * P, hv[rr].w * P};
             uint32_t pk[4], sc[4];
-            quant_block4_quad(v, pk, sc);
+            quant_block4_quad(v, pk, sc, p.nd);
             const int c = k >> 8, jb = (k & 255) >> 1;
 #pragma unroll
             for (int d = 0; d < 4; ++d) {

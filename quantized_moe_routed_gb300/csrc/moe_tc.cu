@@ -413,7 +413,7 @@ __device__ void tc_quantize_x(const KernelParams &p, const Tabs &tb, volatile in
                 v[2 * i] = __uint_as_float(w[i] << 16) * P;
                 v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u) * P;
             }
-            quant_block4(v, pk, sc);
+            quant_block4(v, pk, sc, p.nd);
         }
         auto put = [&](int r) {
             if (b < nblk) {
@@ -857,6 +857,9 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
                     const int pi = i0 + q;
                     if (pi < gcnt) {
                         const float4 x4 = *reinterpret_cast<const float4 *>(hs + q * kTcRows + 4 * lane);
+                        if (p.nd == 1)  // kept for the finisher (blocks whose rebased scale is subnormal)
+                            *reinterpret_cast<float4 *>(p.hf + static_cast<size_t>(gbeg + pi) * p.I + tile * kTcRows +
+                                                        4 * lane) = x4;
                         float v[4] = {x4.x, x4.y, x4.z, x4.w};
                         float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
@@ -866,7 +869,7 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
 #pragma unroll
                         for (int e4 = 0; e4 < 4; ++e4) v[e4] *= P;
                         uint32_t pk[4], sc[4];
-                        quant_block4_quad(v, pk, sc);
+                        quant_block4_quad(v, pk, sc, p.nd);
                         const int k0 = tile * kTcRows + 4 * lane;  // this lane's first row of h
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -914,9 +917,43 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
                 for (int wd = t; wd < gcnt * 4 * wpr; wd += 128) {
                     const int row = wd / wpr, wi = wd - row * wpr, pl = row >> 2;
                     const int d = ex[pl * 33 + (wi >> 1)] - ex[pl * 33 + 32];
-                    if (d <= 0) continue;
+                    if (d <= 0 || (p.nd == 1 && (row & 3))) continue;  // single quantisation: digits 1-3 are zero
                     uint32_t *sw = reinterpret_cast<uint32_t *>(p.hsf + (static_cast<size_t>(gbeg) * 4 + row) * srow) + wi;
-                    *sw = rebase4(__ldcg(sw), d);
+                    const uint32_t w0 = __ldcg(sw);
+                    if (p.nd == 4) {
+                        *sw = rebase4(w0, d);
+                        continue;
+                    }
+                    // single quantisation: a block whose scale stays normal after
+                    // the shift has the codes the pair's own prescale gives; any
+                    // other block is quantised again from h at that prescale
+                    uint32_t w1 = 0;
+#pragma unroll 1
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t c = (w0 >> (8 * i)) & 0xFFu;
+                        uint32_t cn = e4m3_shift_down(c, d);
+                        if (c != 0u && static_cast<int>(c >> 3) - d < 1) {
+                            const int kb = 64 * wi + 16 * i;  // the block's first row of h
+                            const float *src = p.hf + static_cast<size_t>(gbeg + pl) * p.I + kb;
+                            const float P = mul_pow2(1.f, ex[pl * 33 + 32]);
+                            float v[16];
+#pragma unroll
+                            for (int e4 = 0; e4 < 16; e4 += 4) {
+                                const float4 f = __ldcg(reinterpret_cast<const float4 *>(src + e4));
+                                v[e4] = f.x * P;
+                                v[e4 + 1] = f.y * P;
+                                v[e4 + 2] = f.z * P;
+                                v[e4 + 3] = f.w * P;
+                            }
+                            uint2 pk[4];
+                            uint32_t sc[4];
+                            quant_block4(v, pk, sc, 1);
+                            *reinterpret_cast<uint2 *>(p.hq + (static_cast<size_t>(gbeg) * 4 + row) * hrow + kb / 2) = pk[0];
+                            cn = sc[0];
+                        }
+                        w1 |= cn << (8 * i);
+                    }
+                    *sw = w1;
                 }
                 __threadfence();
                 if (!epi_sync()) break;

@@ -130,10 +130,17 @@ __device__ __forceinline__ float2 e2m1_unpack2(uint32_t b)
 // Quantise one 16-element block, prescaled, into four digits: digit j encodes
 // 4^j times the residual r_j, E4M3 scale rounded up, E2M1 RNE.  r is consumed
 // (left as the final residual); pk[j] = the 8 code bytes, sc[j] = scale code.
-__device__ __forceinline__ void quant_block4(float (&r)[16], uint2 (&pk)[4], uint32_t (&sc)[4])
+// Digits j >= nd are left zero (codes and scale): nd = 1 is the single NVFP4
+// quantisation of the block.
+__device__ __forceinline__ void quant_block4(float (&r)[16], uint2 (&pk)[4], uint32_t (&sc)[4], int nd = 4)
 {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
+        if (j >= nd) {
+            pk[j] = make_uint2(0u, 0u);
+            sc[j] = 0u;
+            continue;
+        }
         const float f = static_cast<float>(1 << (2 * j));
         float amax = 0.f;
 #pragma unroll
@@ -161,11 +168,17 @@ __device__ __forceinline__ void quant_block4(float (&r)[16], uint2 (&pk)[4], uin
 // elements 4(lane & 3) .. +3): the same arithmetic per element, the block's
 // largest magnitude of each digit's residual by two shuffles.  pk[j] = this
 // lane's two code bytes of digit j (elements in order, low nibble first),
-// sc[j] = the digit's scale code (the same in all four lanes).
-__device__ __forceinline__ void quant_block4_quad(float (&r)[4], uint32_t (&pk)[4], uint32_t (&sc)[4])
+// sc[j] = the digit's scale code (the same in all four lanes); digits j >= nd
+// zero, as in quant_block4 (nd is the same in all four lanes).
+__device__ __forceinline__ void quant_block4_quad(float (&r)[4], uint32_t (&pk)[4], uint32_t (&sc)[4], int nd = 4)
 {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
+        if (j >= nd) {
+            pk[j] = 0u;
+            sc[j] = 0u;
+            continue;
+        }
         const float f = static_cast<float>(1 << (2 * j));
         float amax = fmaxf(fmaxf(fabsf(r[0]), fabsf(r[1])), fmaxf(fabsf(r[2]), fabsf(r[3])));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));

@@ -38,7 +38,8 @@ import torch
 
 __all__ = [
     "Workload", "WORKLOADS", "quantize_nvfp4", "make_x", "make_x_variant", "make_topk_w",
-    "make_topk_ids", "make_router_logits", "make_expert_weights", "make_shared_weights", "expert_slice",
+    "make_topk_ids", "make_router_logits", "make_expert_weights", "make_uneven_expert_weights", "make_shared_weights",
+    "expert_slice",
     "make_inputs", "rotate_ids",
     "rotation_delta", "touched_experts", "algorithmic_bytes",
 ]
@@ -264,6 +265,30 @@ def make_expert_weights(wl: Workload, device="cpu", experts=None, fill: str = "r
             out[name + "_s"][e].copy_(s)
             out[name + "_ts"][e] = ts
     return out
+
+
+def make_uneven_expert_weights(wl: Workload, lo: int, hi: int, gain_exp: int, device="cpu"):
+    """Every expert drawn as in make_expert_weights, except that before the
+    quantisation the gate rows [lo, hi) are scaled by 2^-gain_exp and the down
+    columns [lo, hi) by 2^gain_exp: the h rows [lo, hi) then lie about
+    gain_exp binades below the rest of h, yet they carry most of y."""
+    dev = torch.device(device)
+    E, H, I = wl.E, wl.H, wl.I
+    out = {n: [] for n in ("gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s", "gate_ts", "up_ts", "down_ts")}
+    for e in range(E):
+        for proj, (name, rows, K) in enumerate((("gate", I, H), ("up", I, H), ("down", H, I))):
+            g = torch.Generator(device=dev).manual_seed(_weight_seed(wl.seed, proj, e))
+            w = torch.randn((rows, K), generator=g, device=dev, dtype=torch.float32)
+            w.mul_(wl.weight_std)
+            if name == "gate":
+                w[lo:hi] *= 2.0 ** -gain_exp
+            elif name == "down":
+                w[:, lo:hi] *= 2.0 ** gain_exp
+            q, sc, ts = quantize_nvfp4(w)
+            out[name + "_q"].append(q)
+            out[name + "_s"].append(sc)
+            out[name + "_ts"].append(ts.reshape(1))
+    return {n: torch.cat(v) if n.endswith("_ts") else torch.stack(v) for n, v in out.items()}
 
 
 def make_inputs(wl: Workload, device="cpu", experts="touched", fill="random"):
