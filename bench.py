@@ -46,15 +46,18 @@ def peaks():
 # The sources each step kernel is built from (a recorded capture stays valid
 # only while they hash the same).
 KERNEL_SOURCES = {
+    "moe_gemv_kernel": ("moe_gemv.cu", "moe_device.cuh"),
     "moe_small_kernel": ("moe_small.cu", "moe_device.cuh", "moe_tcgen05.cuh"),
     "moe_tc_kernel": ("moe_tc.cu", "moe_device.cuh", "moe_tcgen05.cuh"),
     "moe_step_kernel": ("moe_kernels.cu", "moe_device.cuh"),
 }
 # The kernel the automatic choice runs for each benchmarked workload.
-WORKLOAD_KERNEL = {"decode": "moe_small_kernel", "spec_verify": "moe_tc_kernel", "upper_decode": "moe_tc_kernel",
+WORKLOAD_KERNEL = {"decode": "moe_gemv_kernel", "spec_verify": "moe_tc_kernel", "upper_decode": "moe_tc_kernel",
                    "prefill": "moe_tc_kernel", "tiny": "moe_step_kernel"}
 # What each kernel computes in: its MMA operand types and accumulator.
 KERNEL_DTYPE = {
+    "moe_gemv_kernel": ("fp16", "mma.sync fp16 operands (E2M1 x E4M3 dequantised exactly in registers, prescaled "
+                                "x and h), fp32 accumulation"),
     "moe_small_kernel": ("fp4", "tcgen05 block-scaled FP4 MMA: NVFP4 weights as stored, activations as four "
                                 "FP4 digit rows, fp32 accumulation"),
     "moe_tc_kernel": ("fp4", "tcgen05 block-scaled FP4 MMA: NVFP4 weights as stored, activations as four FP4 "

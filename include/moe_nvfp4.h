@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define MOE_NVFP4_ABI_VERSION 6
+#define MOE_NVFP4_ABI_VERSION 7
 
 typedef enum {
     MOE_OK = 0,
@@ -80,11 +80,21 @@ typedef struct {
                 /*    the environment variable MOE_STRICT=1 forces it on          */
     int pdl;    /* 1: launch with programmatic dependent launch allowed          */
     int kernel; /* which step kernel runs moe_decode / moe_prefill:               */
-                /*   MOE_KERNEL_AUTO: per launch, where the shape allows the      */
-                /*     tensor cores (H and I multiples of 256, I <= 4096): the    */
-                /*     small-launch tensor-core kernel for at most 4 tokens and  */
-                /*     32 (token, slot) pairs, the tensor-core ticket kernel for */
-                /*     more than 8 pairs; otherwise the register kernel;          */
+                /*   MOE_KERNEL_AUTO: per launch: for one token (T = 1), where H */
+                /*     is a multiple of 2048, I a multiple of 256 and at most    */
+                /*     4096 and act_quant is 0, the one-token row kernel (E2M1 x */
+                /*     E4M3 dequantised in registers, fp16 mma.sync, one grid-    */
+                /*     wide barrier between gate/up and down; the environment    */
+                /*     variable MOE_GEMV=0 at plan creation leaves it out); else, */
+                /*     where the shape allows the tensor cores (H and I           */
+                /*     multiples of 256, I <= 4096): the small-launch tensor-core */
+                /*     kernel for at most 4 tokens and 32 (token, slot) pairs,   */
+                /*     the tensor-core ticket kernel for more than 8 pairs;       */
+                /*     otherwise the register kernel.  The one-token row kernel   */
+                /*     needs every CTA of its grid (one per SM) resident at once: */
+                /*     a step that shares the device with other work may wait     */
+                /*     for SMs, and past the plan's wait limit reports            */
+                /*     MOE_ERR_TIMEOUT;                                           */
                 /*   MOE_KERNEL_REGISTER: E2M1 x E4M3 dequantised in registers,   */
                 /*     fp16 mma.sync (any shape the plan accepts);                */
                 /*   MOE_KERNEL_TENSOR: tcgen05 block-scaled FP4 MMA on the        */
@@ -140,6 +150,7 @@ typedef struct {
     uint64_t tensor_launches;  /* of decode + prefill: tensor-core kernel       */
     uint64_t route_launches;   /* top-k routing kernel (moe_route)              */
     uint64_t small_launches;   /* of tensor_launches: the small-launch kernel   */
+    uint64_t gemv_launches;    /* of decode + prefill: the one-token row kernel */
     int num_sms;               /* SMs on the plan's device (grid size)          */
     int stages;                /* shared-memory ring stages at the largest T    */
     int smem_bytes;            /* dynamic shared memory per CTA at the largest T */

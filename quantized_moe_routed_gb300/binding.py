@@ -45,6 +45,7 @@ class moe_stats_t(C.Structure):
     _fields_ = [("decode_launches", C.c_uint64), ("prefill_launches", C.c_uint64), ("null_launches", C.c_uint64),
                 ("group_launches", C.c_uint64), ("rejected_calls", C.c_uint64),
                 ("tensor_launches", C.c_uint64), ("route_launches", C.c_uint64), ("small_launches", C.c_uint64),
+                ("gemv_launches", C.c_uint64),
                 ("num_sms", C.c_int),
                 ("stages", C.c_int), ("smem_bytes", C.c_int)]
 

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe_nvfp4.so")
-SOURCES = ("moe_kernels.cu", "moe_tc.cu", "moe_small.cu", "moe_route.cu", "moe_abi.cu")
+SOURCES = ("moe_kernels.cu", "moe_tc.cu", "moe_small.cu", "moe_gemv.cu", "moe_route.cu", "moe_abi.cu")
 HEADERS = ("moe_internal.h", "moe_device.cuh", "moe_tcgen05.cuh")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -48,7 +48,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     for src in SOURCES:
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
         cmd = [cc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
-        if src in ("moe_kernels.cu", "moe_tc.cu", "moe_small.cu", "moe_route.cu"):
+        if src in ("moe_kernels.cu", "moe_tc.cu", "moe_small.cu", "moe_gemv.cu", "moe_route.cu"):
             cmd += ["-Xptxas", "-v"]
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
         objs.append(obj)

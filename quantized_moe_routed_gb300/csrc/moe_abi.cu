@@ -42,6 +42,7 @@ bool env_flag(const char *name)
 }
 
 std::once_flag g_active_once;
+std::once_flag g_gv_once;
 
 }  // namespace
 
@@ -95,6 +96,11 @@ struct moe_plan {
     bool use_small = false;
     int T_small = 0, smaxseg = 0, shs = 0, small_smem_attr = 0;
     size_t off_sgdone = 0, off_sapart = 0;
+    // one-token row kernel (launches of one token)
+    bool use_gv = false;
+    int gv_smem_attr = 0;
+    CUtensorMap gvm[6], gvms[6];
+    size_t off_gv_h = 0, off_gv_cnt = 0;
     std::mutex mu;
     moe_stats_t stats{};
 };
@@ -331,6 +337,69 @@ CUresult encode_rows(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, i
 // MMA N (digit rows per group) for a launch of T tokens: a group holds at
 // most N/4 pairs, and one expert takes at most T pairs of a launch.
 int tc_n_for(int T) { return T <= 4 ? 16 : (T <= 8 ? 32 : 64); }
+
+// ---- the one-token row kernel (moe_gemv.cu)
+constexpr int kGvKS = 2048, kGvStageA = 18432, kGvThreadsHost = 544;
+
+// Shapes it takes: whole 2048-element stages of H, 256-element chunks of I
+// (scale rows a whole number of 16-byte units), down scale rows of at most
+// 256 bytes (one TMA box).
+bool gv_shape_ok(const moe_plan_desc &d) { return d.H % kGvKS == 0 && d.I % 256 == 0 && d.I <= 4096; }
+
+struct GvLayout {
+    int slot = 0, NS = 0, off_hdr = 0, off_x16 = 0, off_h16 = 0, h16p = 0, off_red1 = 0, off_red2 = 0, qb = 0, total = 0;
+};
+GvLayout gv_layout(const moe_plan *pl)
+{
+    GvLayout L;
+    const int H = pl->d.H, I = pl->d.I, kp = pl->kp, G = pl->num_sms;
+    L.qb = up1024(2 * I);
+    L.slot = up1024(std::max(kGvStageA, kp * (L.qb + (I / 4 + 127) / 128 * 128)));
+    L.h16p = 2 * I + 16;
+    const int units = (kp * (I / 8) + G - 1) / G, groups = (H / 4 + G - 1) / G, nsets = (kp + 3) / 4;
+    const int rest = moe::kGvHdrBytes + 2 * H + kp * L.h16p + units * 16 * 16 * 4 + groups * nsets * (I / 128) * 16 * 4;
+    int ns = (pl->smem_optin - 1024 - rest) / L.slot;
+    if (ns > moe::kGvMaxSlots) ns = moe::kGvMaxSlots;
+    if (ns < 2) return L;
+    L.NS = ns;
+    L.off_hdr = ns * L.slot;
+    L.off_x16 = L.off_hdr + moe::kGvHdrBytes;
+    L.off_h16 = L.off_x16 + 2 * H;
+    L.off_red1 = L.off_h16 + kp * L.h16p;
+    L.off_red2 = L.off_red1 + units * 16 * 16 * 4;
+    L.total = L.off_red2 + groups * nsets * (I / 128) * 16 * 4 + 1024;
+    return L;
+}
+
+CUresult encode_gv(CUtensorMap (&m)[6], const WeightSet &w, const moe_plan_desc &d)
+{
+    const cuuint32_t es[3] = {1, 1, 1};
+    const uint64_t rowsGU = w.nexp * d.I, rowsD = w.nexp * d.H;
+    auto q3 = [&](CUtensorMap *t, const void *base, uint64_t rows, int K, int box_rows) {
+        const cuuint64_t dims[3] = {128, rows, static_cast<cuuint64_t>(K / 256)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 2), 128};
+        const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows),
+                                   static_cast<cuuint32_t>(box_rows == 8 ? kGvKS / 256 : K / 256)};
+        return encoder()(t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    };
+    auto s2 = [&](CUtensorMap *t, const void *base, uint64_t rows, int K, int box_c, int box_rows, bool sw) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 16), rows};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 16)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_c), static_cast<cuuint32_t>(box_rows)};
+        return encoder()(t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    };
+    CUresult r = q3(&m[0], w.gq, rowsGU, d.H, 8);
+    if (r == CUDA_SUCCESS) r = q3(&m[1], w.uq, rowsGU, d.H, 8);
+    if (r == CUDA_SUCCESS) r = s2(&m[2], w.gs, rowsGU, d.H, 128, 8, true);
+    if (r == CUDA_SUCCESS) r = s2(&m[3], w.us, rowsGU, d.H, 128, 8, true);
+    if (r == CUDA_SUCCESS) r = q3(&m[4], w.dq, rowsD, d.I, 4);
+    if (r == CUDA_SUCCESS) r = s2(&m[5], w.ds, rowsD, d.I, d.I / 16, 4, false);
+    return r;
+}
 
 moe_status_t check_device(const moe_plan *pl)
 {
@@ -591,7 +660,7 @@ moe_status_t run_small(moe_plan *pl, const void *x, const int32_t *ids, const fl
     p.w = w;
     p.y = y;
     p.NS = L.NS;
-    p.NSF = L.NS < 7 ? L.NS : 7;  // (512 - 64 accumulator columns) / 64 per slot
+    p.NSF = L.NS < moe::kSmMaxNSF ? L.NS : moe::kSmMaxNSF;  // the tensor memory beside the accumulators
     p.stage_bytes = moe::kSmStage;
     p.tab_off = L.tab_off;
     p.smaxseg = pl->smaxseg;
@@ -618,6 +687,70 @@ moe_status_t run_small(moe_plan *pl, const void *x, const int32_t *ids, const fl
     if (!env_flag("MOE_QUIET"))
         std::call_once(g_active_once, [&] {
             std::fprintf(stderr, "moe_nvfp4: sm_103a routed-experts small-launch tensor-core kernel ACTIVE (%d SMs)\n",
+                         pl->num_sms);
+        });
+    return MOE_OK;
+}
+
+// The one-token row kernel (one launch, T = 1).
+moe_status_t run_gv(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, void *ws,
+                    cudaStream_t cs, Path path)
+{
+    const GvLayout L = gv_layout(pl);
+    {
+        std::lock_guard<std::mutex> lk(pl->mu);
+        if (pl->gv_smem_attr == 0) {
+            cudaError_t e = moe::set_gemv_smem_limit(pl->smem_optin);
+            if (e != cudaSuccess) {
+                pl->stats.rejected_calls++;
+                return fail(MOE_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            }
+            pl->gv_smem_attr = pl->smem_optin;
+        }
+    }
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    const moe_plan_desc &d = pl->d;
+    moe::KernelParams p{};
+    p.gts = d.gate_ts_dev;
+    p.uts = d.up_ts_dev;
+    p.dts = d.down_ts_dev;
+    p.ctrl = reinterpret_cast<uint32_t *>(wsb);
+    p.gv_h = reinterpret_cast<float *>(wsb + pl->off_gv_h);
+    p.gv_cnt = reinterpret_cast<unsigned long long *>(wsb + pl->off_gv_cnt);
+    set_pair_space(pl, p);
+    p.T = 1;
+    p.timeout_ns = pl->timeout_ns;
+    for (int i = 0; i < 6; ++i) {
+        p.gv[i] = pl->gvm[i];
+        p.gvs[i] = pl->gvms[i];
+    }
+    p.x = static_cast<const uint16_t *>(x);
+    p.ids = ids;
+    p.w = w;
+    p.y = y;
+    p.NS = L.NS;
+    p.stage_bytes = L.slot;
+    p.gv_off_hdr = L.off_hdr;
+    p.gv_off_x16 = L.off_x16;
+    p.gv_off_h16 = L.off_h16;
+    p.gv_h16p = L.h16p;
+    p.gv_off_red1 = L.off_red1;
+    p.gv_off_red2 = L.off_red2;
+    p.gv_qb = L.qb;
+    cudaError_t e = moe::launch_gemv(p, pl->num_sms, L.total, pl->pdl, cs);
+    if (e != cudaSuccess) {
+        reject(pl);
+        return fail(MOE_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+    }
+    {
+        std::lock_guard<std::mutex> lk(pl->mu);
+        if (path == Path::Prefill) pl->stats.prefill_launches++;
+        else pl->stats.decode_launches++;
+        pl->stats.gemv_launches++;
+    }
+    if (!env_flag("MOE_QUIET"))
+        std::call_once(g_gv_once, [&] {
+            std::fprintf(stderr, "moe_nvfp4: sm_103a routed-experts one-token row kernel ACTIVE (%d SMs)\n",
                          pl->num_sms);
         });
     return MOE_OK;
@@ -659,6 +792,8 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
     // 192 vs 154 us at T = 16, 330 vs 226 us at T = 24)
     // launches of at most T_small tokens (the single-token decode) take the
     // small-launch tensor-core kernel whenever the tensor cores may be used
+    if (pl->use_gv && path != Path::Null && !wo && T == 1)
+        return run_gv(pl, x, ids, w, y, ws, static_cast<cudaStream_t>(stream), path);
     if (pl->use_small && path != Path::Null && !wo && T <= pl->T_small)
         return run_small(pl, x, ids, w, y, T, ws, static_cast<cudaStream_t>(stream), path);
     if (pl->use_tc && path != Path::Null && !wo &&
@@ -1047,6 +1182,26 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
             }
         }
     }
+    // the one-token row kernel: automatic kernel choice, four-digit activations
+    // (it keeps x and h in fp16), its shapes, and its ring fits
+    if (d.kernel == MOE_KERNEL_AUTO && pl->nd == 4 && gv_shape_ok(d) &&
+        !(std::getenv("MOE_GEMV") && std::strcmp(std::getenv("MOE_GEMV"), "0") == 0) && gv_layout(pl).NS >= 2) {
+        const WeightSet rw{d.gate_q_dev, d.up_q_dev, d.down_q_dev, d.gate_s_dev, d.up_s_dev, d.down_s_dev,
+                           static_cast<uint64_t>(pl->Eloc)};
+        CUresult cr = encode_gv(pl->gvm, rw, d);
+        if (cr == CUDA_SUCCESS && pl->shared) {
+            const WeightSet sw{d.shared_gate_q_dev, d.shared_up_q_dev, d.shared_down_q_dev, d.shared_gate_s_dev,
+                               d.shared_up_s_dev, d.shared_down_s_dev, 1};
+            cr = encode_gv(pl->gvms, sw, d);
+        }
+        if (cr == CUDA_SUCCESS) {
+            pl->use_gv = true;
+            pl->off_gv_cnt = o;
+            o = up(o + 8, 256);
+            pl->off_gv_h = o;
+            o = up(o + static_cast<size_t>(pl->kp) * d.I * 4, 256);
+        }
+    }
     pl->ws_bytes = o;
     pl->stats.num_sms = sms;
     pl->stats.stages = L.NS;
@@ -1320,6 +1475,10 @@ moe_status_t moe_debug_poison_workspace(moe_plan_t plan, void *ws_dev, void *str
     if (e == cudaSuccess && plan->use_small)
         e = moe::launch_poison(reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws_dev) + plan->off_sgdone),
                                2 * moe::kSmMaxPairs, static_cast<cudaStream_t>(stream));
+    // the row kernel's grid-barrier count, off a multiple of the grid: some CTA's barrier never opens
+    if (e == cudaSuccess && plan->use_gv)
+        e = moe::launch_poison(reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws_dev) + plan->off_gv_cnt), 2,
+                               static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "poison launch: %s", cudaGetErrorString(e));
     return MOE_OK;
 }

@@ -54,11 +54,15 @@ namespace {
 
 constexpr int kOffW0 = 0, kOffW1 = 16384, kOffS0 = 32768, kOffS1 = 34816;  // stage sub-buffers
 constexpr int kTmemCols = 512;
-// tensor memory: two accumulator buffers of 32 columns (gate at +0, up at +16;
-// a down unit uses +0), then NSF scale-factor slots of 64 columns from column
-// 64: sets at +0 (gate or first down chunk), +16 (up or second down chunk),
-// +32 (activation scales of the first chunk), +48 (of the second)
-constexpr int kAccCols = 32;
+// tensor memory: two accumulator buffers of kSmAccCols (128) columns, then
+// NSF scale-factor slots of 64 columns from column 256: sets at +0 (gate or
+// first down chunk), +16 (up or second down chunk), +32 (activation scales of
+// the first chunk), +48 (of the second).  An accumulator buffer holds four
+// independent chains per operand, one per K step of a stage (gate chain c at
+// +16c, up chain c at +64 + 16c; a down unit's chain c at +16c): consecutive
+// MMAs never wait on each other's accumulator, and the epilogue sums the
+// four chains in a fixed order.
+constexpr int kAccCols = kSmAccCols;
 constexpr int kSfBase = 2 * kAccCols;
 
 // Kernel-private tables in shared memory (at p.s_off_scr).
@@ -462,11 +466,9 @@ __device__ void sm_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
             const uint64_t bd = sw128_desc(xdesc + static_cast<uint32_t>(c) * xstride);
             const uint32_t off = who ? static_cast<uint32_t>(kOffW1) : static_cast<uint32_t>(kOffW0);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
-                tc_mma(dcol + 16u * who, d0 + (off + 32 * kk) / 16, bd + 2 * kk, idesc, sfc + 16u * who + 4 * kk,
-                       sfc + 32 + 4 * kk, acc);
-            }
+            for (int kk = 0; kk < 4; ++kk)  // chain kk of the gate (who 0) or up (who 1) accumulator
+                tc_mma(dcol + 64u * who + 16u * kk, d0 + (off + 32 * kk) / 16, bd + 2 * kk, idesc,
+                       sfc + 16u * who + 4 * kk, sfc + 32 + 4 * kk, first ? 0u : 1u);
         } else if (mine) {
             const int g = h.y / sh.TO, hs = sm_hslot(g, sh), c0 = 2 * h.z;
             const uint32_t hb = smem_u32(smem + p.s_off_h + hs * (sh.KCI * 2048));
@@ -474,9 +476,9 @@ __device__ void sm_mma_loop(const KernelParams &p, uint8_t *smem, const Tabs &tb
             for (int kr = 0; kr < nch; ++kr) {
                 const uint64_t bd = sw128_desc(hb + static_cast<uint32_t>((c0 + kr) * 2048));
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t acc = (!first || kr > 0 || kk > 0) ? 1u : 0u;
-                    tc_mma(dcol, d0 + ((kr ? kOffW1 : kOffW0) + 32 * kk) / 16, bd + 2 * kk, idesc,
+                for (int kk = 0; kk < 4; ++kk) {  // chain kk
+                    const uint32_t acc = (!first || kr > 0) ? 1u : 0u;
+                    tc_mma(dcol + 16u * kk, d0 + ((kr ? kOffW1 : kOffW0) + 32 * kk) / 16, bd + 2 * kk, idesc,
                            sfc + 16 * kr + 4 * kk, sfc + 32 + 16 * kr + 4 * kk, acc);
                 }
             }
@@ -686,13 +688,24 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
         if (!(ok = take_acc())) break;
         const uint32_t dcol = lanebase + static_cast<uint32_t>((nt & 1) * kAccCols);
         float4 dg[kSmMaxT], du[kSmMaxT];
+        // the four chains, added in order c0 + c1 + c2 + c3
 #pragma unroll
-        for (int t = 0; t < kSmMaxT; ++t)
-            if (t < p.T) {
-                tc_ld4(dcol + 4 * t, dg[t]);
-                tc_ld4(dcol + 16 + 4 * t, du[t]);
-            }
-        tc_wait_ld();
+        for (int ch = 0; ch < 4; ++ch) {
+            float4 g[kSmMaxT], u[kSmMaxT];
+#pragma unroll
+            for (int t = 0; t < kSmMaxT; ++t)
+                if (t < p.T) {
+                    tc_ld4(dcol + 16 * ch + 4 * t, g[t]);
+                    tc_ld4(dcol + 64 + 16 * ch + 4 * t, u[t]);
+                }
+            tc_wait_ld();
+#pragma unroll
+            for (int t = 0; t < kSmMaxT; ++t)
+                if (t < p.T) {
+                    dg[t] = ch ? f4add(dg[t], g[t]) : g[t];
+                    du[t] = ch ? f4add(du[t], u[t]) : u[t];
+                }
+        }
         give_acc();
         const int ae = u / sh.TI, e = sx->aexp[ae];
         const float tg = expert_ts(p, 0, e), tu = expert_ts(p, 1, e);
@@ -728,9 +741,16 @@ __device__ void sm_epilogue(const KernelParams &p, uint8_t *smem, const Tabs &tb
             const uint32_t dcol = lanebase + static_cast<uint32_t>((nt & 1) * kAccCols);
             float4 dd[kSmGroup];
 #pragma unroll
-            for (int i = 0; i < kSmGroup; ++i)
-                if (i < gcnt) tc_ld4(dcol + 4 * i, dd[i]);
-            tc_wait_ld();
+            for (int ch = 0; ch < 4; ++ch) {  // the four chains, added in order
+                float4 c[kSmGroup];
+#pragma unroll
+                for (int i = 0; i < kSmGroup; ++i)
+                    if (i < gcnt) tc_ld4(dcol + 16 * ch + 4 * i, c[i]);
+                tc_wait_ld();
+#pragma unroll
+                for (int i = 0; i < kSmGroup; ++i)
+                    if (i < gcnt) dd[i] = ch ? f4add(dd[i], c[i]) : c[i];
+            }
             give_acc();
             const int o = b - g * sh.TO;
 #pragma unroll

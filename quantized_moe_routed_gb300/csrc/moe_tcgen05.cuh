@@ -76,6 +76,10 @@ __device__ __forceinline__ void tc_ld4(uint32_t taddr, float4 &r)
     r = make_float4(__uint_as_float(a), __uint_as_float(b), __uint_as_float(c), __uint_as_float(d));
 }
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ float4 f4add(const float4 &a, const float4 &b)
+{
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
 
 // Shared-memory matrix descriptor: K-major rows of 128 bytes, 128-byte swizzle,
 // 8-row groups 1024 bytes apart (tcgen05 descriptor version 1).

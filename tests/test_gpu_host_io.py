@@ -30,12 +30,14 @@ def fill(io, x, ids, w):
     io.w.copy_(w)
 
 
-# T = 1 x top-8: the small-launch tensor-core kernel (and the register kernel
-# on a register plan); T = 12 x top-4: the tensor-core ticket kernel;
-# T = 40: the prefill path (a strict plan takes it through this entry)
-@pytest.mark.parametrize("T,k,path", [(1, 8, "small"), (1, 8, "register"), (12, 4, "tensor"), (40, 4, "prefill")])
+# T = 1 x top-8: the small-launch tensor-core kernel at H = 512, the one-token
+# row kernel at H = 2048 (and the register kernel on a register plan);
+# T = 12 x top-4: the tensor-core ticket kernel; T = 40: the prefill path (a
+# strict plan takes it through this entry)
+@pytest.mark.parametrize("T,k,path", [(1, 8, "small"), (1, 8, "gemv"), (1, 8, "register"), (12, 4, "tensor"),
+                                      (40, 4, "prefill")])
 def test_step_host_is_bitwise_the_device_step(T, k, path):
-    wl = Workload("hostio", T=T, H=512, I=256, E=16, k=k, routing="uniform", seed=21)
+    wl = Workload("hostio", T=T, H=2048 if path == "gemv" else 512, I=256, E=16, k=k, routing="uniform", seed=21)
     x, ids, w = make_x(wl), make_topk_ids(wl), make_topk_w(wl)
     W = make_expert_weights(wl, device=DEV, experts=None)
     kern = binding.MOE_KERNEL_REGISTER if path == "register" else binding.MOE_KERNEL_AUTO
@@ -58,6 +60,8 @@ def test_step_host_is_bitwise_the_device_step(T, k, path):
         assert after["tensor_launches"] == before["tensor_launches"] + 1
     elif path == "small":
         assert after["small_launches"] == before["small_launches"] + 1
+    elif path == "gemv":
+        assert after["gemv_launches"] == before["gemv_launches"] + 1
     elif path == "register":
         assert after["tensor_launches"] == before["tensor_launches"]
         assert after["decode_launches"] == before["decode_launches"] + 1

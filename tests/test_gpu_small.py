@@ -82,12 +82,15 @@ def test_small_kernel_bitwise_reproducible_and_recovers_after_a_launch():
     ys = [plan.step(xd, idd, wd, ws).clone() for _ in range(3)]
     assert plan.check(ws) == 0
     assert torch.equal(ys[0], ys[1]) and torch.equal(ys[1], ys[2])
-    # a one-token launch on the same workspace after the two-token ones
+    # a one-token launch on the same workspace after the two-token ones (the
+    # one-token row kernel takes it: H is a multiple of 2048), then two tokens again
     y1 = plan.step(xd[:1].contiguous(), idd[:1].contiguous(), wd[:1].contiguous(), ws)
     assert plan.check(ws) == 0
     y_ref, _ = oracle.moe_forward(x[:1], ids[:1], w[:1], {k: v.cpu() for k, v in W.items()})
     assert rel_err(y1.cpu().numpy(), y_ref) <= TOL
-    assert plan.stats()["small_launches"] == 4
+    y2 = plan.step(xd, idd, wd, ws)
+    assert plan.check(ws) == 0 and torch.equal(y2, ys[0])
+    assert plan.stats()["small_launches"] == 4 and plan.stats()["gemv_launches"] == 1
 
 
 def test_register_kernel_plan_never_takes_the_small_kernel():
