@@ -81,15 +81,16 @@ typedef struct {
     int pdl;    /* 1: launch with programmatic dependent launch allowed          */
     int kernel; /* which step kernel runs moe_decode / moe_prefill:               */
                 /*   MOE_KERNEL_AUTO: per launch: for one token (T = 1), where H */
-                /*     is a multiple of 2048, I a multiple of 256 and at most    */
-                /*     4096 and act_quant is 0, the one-token row kernel (E2M1 x */
-                /*     E4M3 dequantised in registers, fp16 mma.sync, one grid-    */
-                /*     wide barrier between gate/up and down; the environment    */
-                /*     variable MOE_GEMV=0 at plan creation leaves it out); else, */
-                /*     where the shape allows the tensor cores (H and I           */
-                /*     multiples of 256, I <= 4096): the small-launch tensor-core */
-                /*     kernel for at most 4 tokens and 32 (token, slot) pairs,   */
-                /*     the tensor-core ticket kernel for more than 8 pairs;       */
+                /*     is a multiple of 2048 up to 16384, I a multiple of 256 up */
+                /*     to 4096 and act_quant is 0, the one-token row kernel      */
+                /*     (E2M1 x E4M3 dequantised in registers, fp16 mma.sync, one */
+                /*     grid-wide barrier between gate/up and down; the           */
+                /*     environment variable MOE_GEMV=0 at plan creation leaves   */
+                /*     it out); else, where the shape allows the tensor cores    */
+                /*     (H and I multiples of 256, I <= 4096): the small-launch   */
+                /*     tensor-core kernel for at most 4 tokens and 32 (token,    */
+                /*     slot) pairs, the tensor-core ticket kernel for more than  */
+                /*     8 pairs;                                                  */
                 /*     otherwise the register kernel.  The one-token row kernel   */
                 /*     needs every CTA of its grid (one per SM) resident at once: */
                 /*     a step that shares the device with other work may wait     */

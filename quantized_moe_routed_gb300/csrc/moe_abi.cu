@@ -339,65 +339,76 @@ CUresult encode_rows(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, i
 int tc_n_for(int T) { return T <= 4 ? 16 : (T <= 8 ? 32 : 64); }
 
 // ---- the one-token row kernel (moe_gemv.cu)
-constexpr int kGvKS = 2048, kGvStageA = 18432, kGvThreadsHost = 544;
-
-// Shapes it takes: whole 2048-element stages of H, 256-element chunks of I
-// (scale rows a whole number of 16-byte units), down scale rows of at most
-// 256 bytes (one TMA box).
-bool gv_shape_ok(const moe_plan_desc &d) { return d.H % kGvKS == 0 && d.I % 256 == 0 && d.I <= 4096; }
+// Shapes it takes: H a multiple of 2048 up to 16384 (whole gate/up stages of
+// 2048 or 4096 elements; x is held in registers), I a multiple of 256 up to
+// 4096 (down stages over pieces of I of at most 2048 elements).
+bool gv_shape_ok(const moe_plan_desc &d)
+{
+    return d.H % 2048 == 0 && d.H <= 16384 && d.I % 256 == 0 && d.I <= 4096;
+}
 
 struct GvLayout {
-    int slot = 0, NS = 0, off_hdr = 0, off_x16 = 0, off_h16 = 0, h16p = 0, off_red1 = 0, off_red2 = 0, qb = 0, total = 0;
+    int KS = 0, PK = 0, RB = 0, tiles = 0, qb = 0, db = 0, ep = 0;
+    int slot = 0, NS = 0, off_hdr = 0, off_x16 = 0, off_h16 = 0, h16p = 0, off_red1 = 0, off_red2 = 0, total = 0;
 };
 GvLayout gv_layout(const moe_plan *pl)
 {
     GvLayout L;
     const int H = pl->d.H, I = pl->d.I, kp = pl->kp, G = pl->num_sms;
-    L.qb = up1024(2 * I);
-    L.slot = up1024(std::max(kGvStageA, kp * (L.qb + (I / 4 + 127) / 128 * 128)));
+    L.KS = H % 4096 == 0 ? 4096 : 2048;
+    for (int pk = 2048; pk >= 256; pk -= 256)
+        if (I % pk == 0) {
+            L.PK = pk;
+            break;
+        }
+    L.RB = 4 * ((H / 4 + G - 1) / G);
+    L.tiles = (L.RB + 15) / 16;
+    L.qb = up1024(L.RB * L.PK / 2);
+    L.db = up1024(L.qb + L.RB * L.PK / 16);
+    L.slot = std::max(9 * L.KS, L.db);  // (both multiples of 1 KB)
+    L.ep = std::max(1, std::min(std::min(kp, 16), L.slot / L.db));  // experts per down stage (two copies each: <= 32 lanes)
     L.h16p = 2 * I + 16;
-    const int units = (kp * (I / 8) + G - 1) / G, groups = (H / 4 + G - 1) / G, nsets = (kp + 3) / 4;
-    const int rest = moe::kGvHdrBytes + 2 * H + kp * L.h16p + units * 16 * 16 * 4 + groups * nsets * (I / 128) * 16 * 4;
+    const int units = (kp * (I / 8) + G - 1) / G;
+    const int rest = moe::kGvHdrBytes + 2 * H + kp * L.h16p + units * 16 * 16 * 4 + kp * (I / 128) * 16 * L.tiles * 4;
     int ns = (pl->smem_optin - 1024 - rest) / L.slot;
     if (ns > moe::kGvMaxSlots) ns = moe::kGvMaxSlots;
-    if (ns < 2) return L;
+    if (ns < 2 || L.RB > 256) return L;
     L.NS = ns;
     L.off_hdr = ns * L.slot;
     L.off_x16 = L.off_hdr + moe::kGvHdrBytes;
     L.off_h16 = L.off_x16 + 2 * H;
     L.off_red1 = L.off_h16 + kp * L.h16p;
     L.off_red2 = L.off_red1 + units * 16 * 16 * 4;
-    L.total = L.off_red2 + groups * nsets * (I / 128) * 16 * 4 + 1024;
+    L.total = L.off_red2 + kp * (I / 128) * 16 * L.tiles * 4 + 1024;
     return L;
 }
 
-CUresult encode_gv(CUtensorMap (&m)[6], const WeightSet &w, const moe_plan_desc &d)
+CUresult encode_gv(CUtensorMap (&m)[6], const WeightSet &w, const moe_plan_desc &d, const GvLayout &L)
 {
     const cuuint32_t es[3] = {1, 1, 1};
     const uint64_t rowsGU = w.nexp * d.I, rowsD = w.nexp * d.H;
-    auto q3 = [&](CUtensorMap *t, const void *base, uint64_t rows, int K, int box_rows) {
-        const cuuint64_t dims[3] = {128, rows, static_cast<cuuint64_t>(K / 256)};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 2), 128};
-        const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows),
-                                   static_cast<cuuint32_t>(box_rows == 8 ? kGvKS / 256 : K / 256)};
+    // {128 B, rows, K/CH chunks} of rows of `pitch` bytes, box {128, box_rows, box_chunks}
+    auto c3 = [&](CUtensorMap *t, const void *base, uint64_t rows, int pitch, int box_rows, int box_chunks) {
+        const cuuint64_t dims[3] = {128, rows, static_cast<cuuint64_t>(pitch / 128)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch), 128};
+        const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(box_chunks)};
         return encoder()(t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     };
-    auto s2 = [&](CUtensorMap *t, const void *base, uint64_t rows, int K, int box_c, int box_rows, bool sw) {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 16), rows};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 16)};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_c), static_cast<cuuint32_t>(box_rows)};
-        return encoder()(t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    };
-    CUresult r = q3(&m[0], w.gq, rowsGU, d.H, 8);
-    if (r == CUDA_SUCCESS) r = q3(&m[1], w.uq, rowsGU, d.H, 8);
-    if (r == CUDA_SUCCESS) r = s2(&m[2], w.gs, rowsGU, d.H, 128, 8, true);
-    if (r == CUDA_SUCCESS) r = s2(&m[3], w.us, rowsGU, d.H, 128, 8, true);
-    if (r == CUDA_SUCCESS) r = q3(&m[4], w.dq, rowsD, d.I, 4);
-    if (r == CUDA_SUCCESS) r = s2(&m[5], w.ds, rowsD, d.I, d.I / 16, 4, false);
+    CUresult r = c3(&m[0], w.gq, rowsGU, d.H / 2, 8, L.KS / 256);
+    if (r == CUDA_SUCCESS) r = c3(&m[1], w.uq, rowsGU, d.H / 2, 8, L.KS / 256);
+    if (r == CUDA_SUCCESS) r = c3(&m[2], w.gs, rowsGU, d.H / 16, 8, L.KS / 2048);
+    if (r == CUDA_SUCCESS) r = c3(&m[3], w.us, rowsGU, d.H / 16, 8, L.KS / 2048);
+    if (r == CUDA_SUCCESS) r = c3(&m[4], w.dq, rowsD, d.I / 2, L.RB, L.PK / 256);
+    if (r == CUDA_SUCCESS) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.I / 16), rowsD};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.I / 16)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(L.PK / 16), static_cast<cuuint32_t>(L.RB)};
+        r = encoder()(&m[5], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(w.ds), dims, strides, box, es,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r;
 }
 
@@ -737,6 +748,12 @@ moe_status_t run_gv(moe_plan *pl, const void *x, const int32_t *ids, const float
     p.gv_off_red1 = L.off_red1;
     p.gv_off_red2 = L.off_red2;
     p.gv_qb = L.qb;
+    p.gv_ks = L.KS;
+    p.gv_pk = L.PK;
+    p.gv_rb = L.RB;
+    p.gv_tiles = L.tiles;
+    p.gv_ep = L.ep;
+    p.gv_db = L.db;
     cudaError_t e = moe::launch_gemv(p, pl->num_sms, L.total, pl->pdl, cs);
     if (e != cudaSuccess) {
         reject(pl);
@@ -1188,11 +1205,12 @@ moe_status_t moe_plan_create(const moe_plan_desc *desc, moe_plan_t *out)
         !(std::getenv("MOE_GEMV") && std::strcmp(std::getenv("MOE_GEMV"), "0") == 0) && gv_layout(pl).NS >= 2) {
         const WeightSet rw{d.gate_q_dev, d.up_q_dev, d.down_q_dev, d.gate_s_dev, d.up_s_dev, d.down_s_dev,
                            static_cast<uint64_t>(pl->Eloc)};
-        CUresult cr = encode_gv(pl->gvm, rw, d);
+        const GvLayout GL = gv_layout(pl);
+        CUresult cr = encode_gv(pl->gvm, rw, d, GL);
         if (cr == CUDA_SUCCESS && pl->shared) {
             const WeightSet sw{d.shared_gate_q_dev, d.shared_up_q_dev, d.shared_down_q_dev, d.shared_gate_s_dev,
                                d.shared_up_s_dev, d.shared_down_s_dev, 1};
-            cr = encode_gv(pl->gvms, sw, d);
+            cr = encode_gv(pl->gvms, sw, d, GL);
         }
         if (cr == CUDA_SUCCESS) {
             pl->use_gv = true;

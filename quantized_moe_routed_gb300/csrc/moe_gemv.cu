@@ -13,15 +13,18 @@
 //    range of units (closed-form shares, no tickets), so it finishes every
 //    h_i = SiLU(g_i) u_i of its rows itself -- no partial sums leave the CTA.
 //    The 16 compute warps split each stage's K range; their partials are
-//    summed in a fixed order in shared memory.
+//    summed in a fixed order in shared memory.  A stage is one unit over up
+//    to 4096 of H (four copies: a copy costs the issuing thread ~100-200
+//    cycles whatever its size, so stages are few and large).
 //  * One grid-wide barrier (a launch-count counter; the grid is one CTA per SM,
 //    all resident): every h row of every active expert is in the workspace.
 //  * Phase 2 (down): CTA j holds a contiguous range of 4-row GROUPS of H and
 //    computes those output rows for every active expert, so the weighted sum
 //    over the token's slots (in slot order: bitwise reproducible) is formed in
-//    the CTA -- no cross-CTA combine.  The down rows stream through the same
-//    ring as the gate/up rows, right behind them, so they are on chip by the
-//    time the barrier opens.
+//    the CTA -- no cross-CTA combine.  A down stage is one active expert's
+//    rows of the CTA (RB rows, one box) over up to 2048 of I; the down stages
+//    stream through the same ring as the gate/up stages, right behind them,
+//    so they are on chip by the time the barrier opens.
 //
 // Warp roles (17 warps): 0-15 compute (warp 0 also builds the expert tables);
 // 16 issues the TMA copies.  Every wait is bounded (globaltimer); on expiry
@@ -29,15 +32,13 @@
 //
 // Shared-memory stage layouts (each box at a 1024-byte boundary, 128-byte
 // swizzle: the 16-byte granule j of a 128-byte row segment at address A sits
-// at granule j ^ ((A >> 7) & 7)):
-//   gate/up stage: [0, 8K) gate E2M1 box {128 B, 8 rows, 8 chunks} -> [chunk][row][128 B];
-//                  [8K, 16K) up, the same; [16K, 17K) gate scales {128 B, 8 rows};
-//                  [17K, 18K) up scales.
-//   down stage:    per active expert a: E2M1 box {128 B, 4 rows, I/256 chunks}
-//                  at a * QB (QB = 2I rounded up to 1 KB) -> [chunk][row][128 B];
-//                  then its scale box {I/16 B, 4 rows} (no swizzle) at nE * QB + a * SB
-//                  (SB = I/4 rounded up to 128 bytes: a tensor copy's destination is
-//                  128-byte aligned).
+// at granule j ^ ((A >> 7) & 7)), KS = the gate/up stage's K (2048 or 4096):
+//   gate/up stage: [0, 4KS) gate E2M1 box {128 B, 8 rows, KS/256 chunks} -> [chunk][row][128 B];
+//                  [4KS, 8KS) up, the same; [8KS, 8.5KS) gate scales {128 B, 8 rows,
+//                  KS/2048 chunks}; [8.5KS, 9KS) up scales.
+//   down stage:    expert a, piece kp of I (PK = min(I, 2048) elements): E2M1 box
+//                  {128 B, RB rows, PK/256 chunks} -> [chunk][row][128 B]; at QB (the
+//                  box rounded up to 1 KB) its scale box {PK/16 B, RB rows}, no swizzle.
 //
 // The fp16 MMA's K order is a permutation of the weights' K order, the same on
 // both operands: in a warp's 128-element K range, lane quarter t (t = lane % 4)
@@ -55,26 +56,26 @@ namespace {
 
 constexpr int kGvWarps = 16;                      // compute warps
 constexpr int kGvThreads = (kGvWarps + 1) * 32;   // + the TMA producer warp
-constexpr int kGvKS = 2048;                       // K elements of H per gate/up stage
 constexpr int kGvUnit = 8;                        // gate (and up) rows per unit
 constexpr int kGvGroup = 4;                       // output rows per down group
-constexpr int kGvStageA = 18432;                  // gate/up stage bytes
 constexpr int kGvMaxE = kMaxTopK + 1;             // active experts (top-k + a shared one)
 
 struct GvHdr {
     uint64_t full[kGvMaxSlots];
     uint64_t empty[kGvMaxSlots];
+    uint64_t readybar;           // the expert tables are built (warp 0 arrives)
     int abort_flag;
     int fill_cnt;
-    int ready;                   // tables and x16 published (release)
     int nE;                      // active experts
     int ex;                      // x prescale exponent
     int eh[kGvMaxE];             // per active expert: h prescale exponent
     int16_t aexp[kGvMaxE];       // active index -> local expert index (Eloc: the shared expert)
     int8_t slot_ae[kGvMaxE];     // slot j -> active index, -1: empty slot
     float red[kGvWarps];         // block-wide maximum scratch
+    float slot_w[kGvMaxE];       // slot j's routing weight (1 for the shared expert's slot)
+    float ts[3][kGvMaxE];        // per active expert: gate, up, down tensor scales
+    uint4 zero16[4];             // 64 zero bytes: the B operand of lanes without a column
 };
-
 static_assert(sizeof(GvHdr) <= kGvHdrBytes, "control block too large");
 
 __device__ __forceinline__ void gv_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }  // compute warps
@@ -91,13 +92,90 @@ __device__ __forceinline__ uint64_t ld_acquire_u64(const unsigned long long *p)
     return v;
 }
 
-// Bytes per expert of a down stage's scale boxes: the box ({I/16 B, 4 rows},
-// I/4 bytes) rounded up to 128, the alignment a tensor copy's destination needs.
-__device__ __forceinline__ int gv_sb(int I) { return (I / 4 + 127) & ~127; }
-
 // {lo, lo} and {hi, hi} of an f16x2
 __device__ __forceinline__ uint32_t f16x2_lo2(uint32_t v) { return (v & 0xffffu) | (v << 16); }
 __device__ __forceinline__ uint32_t f16x2_hi2(uint32_t v) { return (v >> 16) | (v & 0xffff0000u); }
+
+// The CTA's work: gate/up units [u0, u0 + nu) (H / KS stages each), then
+// down stages for each group of gv_ep active experts and piece of I, over
+// its output rows [4 g0, 4 g0 + R).  Stage i of the sequence goes to ring
+// slot i % NS.
+struct GvSeq {
+    int u0, nu, nks, n1;  // units, stages per unit, gate/up stages
+    int g0, R, npc, n;    // first group, output rows, pieces of I, all stages
+    int neg;              // groups of gv_ep experts
+};
+__device__ __forceinline__ GvSeq gv_seq(const KernelParams &p, int nE)
+{
+    const int G = gridDim.x, j = blockIdx.x, NU = nE * (p.I / kGvUnit), NG = p.H / kGvGroup;
+    GvSeq q;
+    q.u0 = gv_lo(j, NU, G);
+    q.nu = gv_lo(j + 1, NU, G) - q.u0;
+    q.nks = p.H / p.gv_ks;
+    q.n1 = q.nu * q.nks;
+    q.g0 = gv_lo(j, NG, G);
+    q.R = kGvGroup * (gv_lo(j + 1, NG, G) - q.g0);
+    q.npc = p.I / p.gv_pk;
+    q.neg = (nE + p.gv_ep - 1) / p.gv_ep;
+    q.n = q.n1 + (q.R > 0 ? q.neg * q.npc : 0);
+    return q;
+}
+// Bytes of one expert's down boxes (E2M1 + scales); each sits at a multiple
+// of gv_db in its stage.
+__device__ __forceinline__ int gv_down_bytes(const KernelParams &p)
+{
+    return p.gv_rb * p.gv_pk / 2 + p.gv_rb * p.gv_pk / 16;
+}
+
+// ------------------------------------------------------------------ producer
+// Warp 16: the CTA's stages in sequence, each into the next free ring slot.
+// Lane 0 arms the slot's barrier; lanes 0-3 (gate/up) or 0-1 (down) issue
+// one copy each.
+__device__ void gv_producer(const KernelParams &p, GvHdr *hd, uint8_t *smem, volatile int *abort_flag)
+{
+    const int lane = threadIdx.x & 31, nE = hd->nE, KS = p.gv_ks, PK = p.gv_pk;
+    const uint64_t pol = policy_evict_first();
+    const GvSeq q = gv_seq(p, nE);
+    const int upe = p.I / kGvUnit;
+    int s = 0, fill = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int i = 0; i < q.n && ok; ++i) {
+        if (!(ok = warp_wait_bar(p, &hd->empty[s], ph ^ 1u, abort_flag))) break;
+        uint8_t *st = smem + s * p.stage_bytes;
+        uint64_t *bar = &hd->full[s];
+        if (i < q.n1) {
+            const int u = q.u0 + i / q.nks, ks = i - (i / q.nks) * q.nks;
+            const int a = u / upe, ib = u - a * upe, e = hd->aexp[a];
+            const CUtensorMap *TM = e == p.Eloc ? p.gvs : p.gv;
+            const int row = (e == p.Eloc ? 0 : e) * p.I + ib * kGvUnit;
+            if (lane == 0) mbar_expect_tx(bar, static_cast<uint32_t>(9 * KS));
+            __syncwarp();
+            if (lane < 2) tma3d(st + 4 * KS * lane, &TM[lane], 0, row, ks * (KS / 256), bar, pol);
+            else if (lane < 4) tma3d(st + 8 * KS + KS / 2 * (lane - 2), &TM[lane], 0, row, ks * (KS / 2048), bar, pol);
+        } else {
+            const int jd = i - q.n1, ag = jd / q.npc, kp = jd - ag * q.npc;
+            const int na = min(p.gv_ep, nE - ag * p.gv_ep);  // experts in this stage
+            if (lane == 0) mbar_expect_tx(bar, static_cast<uint32_t>(na * gv_down_bytes(p)));
+            __syncwarp();
+            if (lane < 2 * na) {
+                const int ea = lane >> 1, a = ag * p.gv_ep + ea, e = hd->aexp[a];
+                const CUtensorMap *TM = e == p.Eloc ? p.gvs : p.gv;
+                const int row = (e == p.Eloc ? 0 : e) * p.H + kGvGroup * q.g0;
+                uint8_t *sa = st + ea * p.gv_db;
+                if ((lane & 1) == 0) tma3d(sa, &TM[4], 0, row, kp * (PK / 256), bar, pol);
+                else tma2d(sa + p.gv_qb, &TM[5], kp * (PK / 16), row, bar, pol);
+            }
+        }
+        ++fill;
+        if (++s == p.NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+    if (!ok && lane == 0) *abort_flag = 1;
+    if (lane == 0) hd->fill_cnt = fill;
+}
 
 // ------------------------------------------------------------------ prologue
 // Warp 0: the token's active experts (distinct local experts of its valid
@@ -109,37 +187,57 @@ __device__ void gv_tables(const KernelParams &p, GvHdr *hd)
     int e = -1;
     if (lane < p.k) e = pair_expert(p, lane, bad);
     if (blockIdx.x == 0 && __any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.ctrl + 2, kErrBadId);
-    // first slot of each distinct expert
-    bool first = e >= 0;
-    for (int i = 0; i < 32; ++i) {
-        const int ei = __shfl_sync(0xffffffffu, e, i);
-        if (i < lane && ei == e) first = false;
-    }
+    // the lanes naming this lane's expert; the first of them is the expert's
+    // first slot, which gets the next active index in slot order
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    const int lead = __ffs(same) - 1;
+    const bool first = e >= 0 && lead == lane;
     const uint32_t fm = __ballot_sync(0xffffffffu, first);
     const int ae_first = __popc(fm & ((1u << lane) - 1u));
     // every slot takes the active index of its expert's first slot
-    int ae = -1;
-    for (int i = 0; i < 32; ++i) {
-        const int ei = __shfl_sync(0xffffffffu, e, i);
-        const int ai = __shfl_sync(0xffffffffu, ae_first, i);
-        if (ae < 0 && e >= 0 && ei == e && ((fm >> i) & 1u)) ae = ai;
-    }
+    const int ae_lead = __shfl_sync(0xffffffffu, ae_first, lead);
+    const int ae = e >= 0 ? ae_lead : -1;
     if (lane < p.k) hd->slot_ae[lane] = static_cast<int8_t>(ae);
     if (first) hd->aexp[ae_first] = static_cast<int16_t>(e);
     if (lane == 0) hd->nE = __popc(fm);
+    if (lane < 4) hd->zero16[lane] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Warp 0, after the producer has started: the slots' routing weights and the
+// active experts' tensor scales, into shared memory (read at the h and y
+// writes, long after these loads land).
+__device__ void gv_tables2(const KernelParams &p, GvHdr *hd)
+{
+    const int lane = threadIdx.x & 31;
+    if (lane < p.k) hd->slot_w[lane] = pair_w(p, 0, lane);
+    if (lane < hd->nE) {
+        const int e = hd->aexp[lane];
+        hd->ts[0][lane] = expert_ts(p, 0, e);
+        hd->ts[1][lane] = expert_ts(p, 1, e);
+        hd->ts[2][lane] = expert_ts(p, 2, e);
+    }
 }
 
 // Compute warps: x as fp16 times 2^ex (its largest magnitude into [2^14, 2^15)).
+// x is read once, into registers (H <= 16384: at most four 16-byte words per
+// thread), as the first global access of the launch: once the ring's copies
+// are in flight, every further load waits behind them.
 __device__ void gv_x16(const KernelParams &p, GvHdr *hd, uint8_t *smem)
 {
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    float m = 0.f;
-    for (int v = tid; v < p.H / 8; v += 512) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p.x) + v);
-        const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+    uint4 xr[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(ww[i] << 16)), fabsf(__uint_as_float(ww[i] & 0xffff0000u))));
+    for (int i = 0; i < 4; ++i) {
+        const int v = tid + 512 * i;
+        xr[i] = v < p.H / 8 ? __ldg(reinterpret_cast<const uint4 *>(p.x) + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t ww[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(ww[k] << 16)), fabsf(__uint_as_float(ww[k] & 0xffff0000u))));
     }
 #pragma unroll
     for (int d = 16; d; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
@@ -151,77 +249,23 @@ __device__ void gv_x16(const KernelParams &p, GvHdr *hd, uint8_t *smem)
     const int ex = f16_prescale_exp(mx);
     const float s = mul_pow2(1.f, ex);
     uint4 *x16 = reinterpret_cast<uint4 *>(smem + p.gv_off_x16);
-    for (int v = tid; v < p.H / 8; v += 512) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p.x) + v);
-        x16[v] = make_uint4(bf16x2_to_f16x2_scaled(u.x, s), bf16x2_to_f16x2_scaled(u.y, s),
-                            bf16x2_to_f16x2_scaled(u.z, s), bf16x2_to_f16x2_scaled(u.w, s));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int v = tid + 512 * i;
+        if (v < p.H / 8)
+            x16[v] = make_uint4(bf16x2_to_f16x2_scaled(xr[i].x, s), bf16x2_to_f16x2_scaled(xr[i].y, s),
+                                bf16x2_to_f16x2_scaled(xr[i].z, s), bf16x2_to_f16x2_scaled(xr[i].w, s));
     }
     if (tid == 0) hd->ex = ex;
-}
-
-// ------------------------------------------------------------------ producer
-// Warp 16, lane 0: the CTA's gate/up stages (units u0 .. u1-1, H / kGvKS
-// stages each), then its down stages (groups g0 .. g1-1), each into the next
-// free ring slot.
-__device__ void gv_producer(const KernelParams &p, GvHdr *hd, uint8_t *smem, volatile int *abort_flag)
-{
-    if ((threadIdx.x & 31) != 0) return;
-    const uint64_t pol = policy_evict_first();
-    const int G = gridDim.x, j = blockIdx.x, nE = hd->nE;
-    const int upe = p.I / kGvUnit, NU = nE * upe, nks = p.H / kGvKS;
-    const int u0 = gv_lo(j, NU, G), u1 = gv_lo(j + 1, NU, G);
-    const int NG = p.H / kGvGroup, g0 = gv_lo(j, NG, G), g1 = gv_lo(j + 1, NG, G);
-    const int QB = p.gv_qb, SB = gv_sb(p.I);
-    int s = 0, fill = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    auto next = [&]() -> bool { return wait_bar(&hd->empty[s], ph ^ 1u, p, abort_flag); };
-    auto advance = [&]() {
-        ++fill;
-        if (++s == p.NS) {
-            s = 0;
-            ph ^= 1u;
-        }
-    };
-    for (int u = u0; u < u1 && ok; ++u) {
-        const int a = u / upe, ib = u - a * upe, e = hd->aexp[a];
-        const CUtensorMap *TM = e == p.Eloc ? p.gvs : p.gv;
-        const int row = (e == p.Eloc ? 0 : e) * p.I + ib * kGvUnit;
-        for (int ks = 0; ks < nks; ++ks) {
-            if (!(ok = next())) break;
-            uint8_t *st = smem + s * p.stage_bytes;
-            uint64_t *bar = &hd->full[s];
-            mbar_expect_tx(bar, static_cast<uint32_t>(kGvStageA));
-            tma3d(st, &TM[0], 0, row, ks * (kGvKS / 256), bar, pol);
-            tma3d(st + 8192, &TM[1], 0, row, ks * (kGvKS / 256), bar, pol);
-            tma2d(st + 16384, &TM[2], ks * (kGvKS / 16), row, bar, pol);
-            tma2d(st + 17408, &TM[3], ks * (kGvKS / 16), row, bar, pol);
-            advance();
-        }
-    }
-    for (int g = g0; g < g1 && ok; ++g) {
-        if (!(ok = next())) break;
-        uint8_t *st = smem + s * p.stage_bytes;
-        uint64_t *bar = &hd->full[s];
-        mbar_expect_tx(bar, static_cast<uint32_t>(nE * (2 * p.I + p.I / 4)));
-        for (int a = 0; a < nE; ++a) {
-            const int e = hd->aexp[a];
-            const CUtensorMap *TM = e == p.Eloc ? p.gvs : p.gv;
-            const int row = (e == p.Eloc ? 0 : e) * p.H + g * kGvGroup;
-            tma3d(st + a * QB, &TM[4], 0, row, 0, bar, pol);
-            tma2d(st + nE * QB + a * SB, &TM[5], 0, row, bar, pol);
-        }
-        advance();
-    }
-    if (!ok) *abort_flag = 1;
-    hd->fill_cnt = fill;
 }
 
 // ------------------------------------------------------------------ compute
 // Eight fp16 MMAs over one 16-byte granule of E2M1 codes per A row (row g: gA,
 // its scales sA; row g + 8: gB, sB, each an E4M3 pair {first block, second})
-// and the matching 32 fp16 B elements of this lane (b[16], f16x2).
-__device__ __forceinline__ void gv_granule(float (&d)[4], const uint4 &gA, uint16_t sA, const uint4 &gB,
+// and the matching 32 fp16 B elements of this lane (b[16], f16x2).  MMA m
+// accumulates into chain m % 4: four independent chains, so the warp does
+// not wait out one MMA's latency before issuing the next (gv_sum4 adds them).
+__device__ __forceinline__ void gv_granule(float (&d)[4][4], const uint4 &gA, uint16_t sA, const uint4 &gB,
                                            uint16_t sB, const uint32_t (&b)[16])
 {
     const uint32_t a2 = e4m3x2_to_f16x2(sA), b2 = e4m3x2_to_f16x2(sB);
@@ -232,52 +276,58 @@ __device__ __forceinline__ void gv_granule(float (&d)[4], const uint4 &gA, uint1
         uint32_t p0, p1, p2, p3, q0, q1, q2, q3;
         e2m1x8_to_f16x2(wa[i], p0, p1, p2, p3);
         e2m1x8_to_f16x2(wb[i], q0, q1, q2, q3);
-        mma16816(d, hmul2(p0, sa), hmul2(q0, sb), hmul2(p1, sa), hmul2(q1, sb), b[4 * i], b[4 * i + 1]);
-        mma16816(d, hmul2(p2, sa), hmul2(q2, sb), hmul2(p3, sa), hmul2(q3, sb), b[4 * i + 2], b[4 * i + 3]);
+        mma16816(d[(2 * i) & 3], hmul2(p0, sa), hmul2(q0, sb), hmul2(p1, sa), hmul2(q1, sb), b[4 * i], b[4 * i + 1]);
+        mma16816(d[(2 * i + 1) & 3], hmul2(p2, sa), hmul2(q2, sb), hmul2(p3, sa), hmul2(q3, sb), b[4 * i + 2],
+                 b[4 * i + 3]);
     }
 }
+// Element k of the four chains, summed in a fixed order.
+__device__ __forceinline__ float gv_sum4(const float (&d)[4][4], int k)
+{
+    return (d[0][k] + d[1][k]) + (d[2][k] + d[3][k]);
+}
 
-// Phase 1, compute warp w: per stage the granule 4w + t of the stage's K range
-// (chunk w / 2), rows g (gate) and g + 8 (up = the same row of I); the unit's
-// partial sums (lanes of quarter t = 0 hold column 0: the token) go to
-// red1[unit][w][16] after its last stage.  false on abort.
-__device__ bool gv_phase1(const KernelParams &p, GvHdr *hd, uint8_t *smem, int &s, uint32_t &ph,
+// Phase 1, compute warp w: stage (unit u, K slice ks) of KS elements; the
+// warp takes elements [w KS/16, (w + 1) KS/16) in steps of 128 (granules
+// 4 step + t of its range); rows g (gate) and g + 8 (up = the same row of I).
+// The unit's partial sums (lanes of quarter t = 0 hold column 0: the token)
+// go to red1[unit][w][16] after its last stage.  false on abort.
+__device__ bool gv_phase1(const KernelParams &p, GvHdr *hd, uint8_t *smem, const GvSeq &q, int &s, uint32_t &ph,
                           volatile int *abort_flag)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
-    const int G = gridDim.x, j = blockIdx.x, nE = hd->nE;
-    const int upe = p.I / kGvUnit, NU = nE * upe, nks = p.H / kGvKS;
-    const int u0 = gv_lo(j, NU, G), u1 = gv_lo(j + 1, NU, G);
-    const int c = w >> 1, gi = ((w & 1) << 2) | t;  // chunk of the stage, granule in the chunk
-    const int offq = c * 1024 + g * 128 + 16 * (gi ^ g);
-    const int offs = g * 128 + 16 * (c ^ g) + 2 * gi;
+    const int KS = p.gv_ks, nstep = KS / 2048;
     const uint4 *x16 = reinterpret_cast<const uint4 *>(smem + p.gv_off_x16);
     float *red1 = reinterpret_cast<float *>(smem + p.gv_off_red1);
-    for (int u = u0; u < u1; ++u) {
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int ks = 0; ks < nks; ++ks) {
+    for (int ul = 0; ul < q.nu; ++ul) {
+        float d[4][4] = {};
+        for (int ks = 0; ks < q.nks; ++ks) {
             if (!warp_wait_bar(p, &hd->full[s], ph, abort_flag)) return false;
             const uint8_t *st = smem + s * p.stage_bytes;
-            const uint4 qg = *reinterpret_cast<const uint4 *>(st + offq);
-            const uint4 qu = *reinterpret_cast<const uint4 *>(st + 8192 + offq);
-            const uint16_t sg = *reinterpret_cast<const uint16_t *>(st + 16384 + offs);
-            const uint16_t su = *reinterpret_cast<const uint16_t *>(st + 17408 + offs);
-            uint32_t b[16];
-            if (g == 0) {  // column 0: x at the lane's 32 elements
-                const uint4 *xs = x16 + (ks * kGvKS + 32 * (4 * w + t)) / 8;
+            for (int step = 0; step < nstep; ++step) {
+                const int G = w * (KS / 512) + 4 * step + t;  // this lane's granule of the stage
+                const int c = G >> 3, gi = G & 7;
+                const int offq = c * 1024 + g * 128 + 16 * (gi ^ g);
+                const int b2 = (2 * G) & 127;  // the granule's first scale byte in its 128-byte scale row
+                const int offs = (G >> 6) * 1024 + g * 128 + 16 * ((b2 >> 4) ^ g) + (b2 & 15);
+                const uint4 qg = *reinterpret_cast<const uint4 *>(st + offq);
+                const uint4 qu = *reinterpret_cast<const uint4 *>(st + 4 * KS + offq);
+                const uint16_t sg = *reinterpret_cast<const uint16_t *>(st + 8 * KS + offs);
+                const uint16_t su = *reinterpret_cast<const uint16_t *>(st + 8 * KS + KS / 2 + offs);
+                uint32_t b[16];
+                {  // column 0 (lanes g = 0): x at the granule's 32 elements; the other columns read zeros
+                    const uint4 *xs = g == 0 ? x16 + (ks * KS + 32 * G) / 8 : hd->zero16;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint4 v = xs[i];
-                    b[4 * i] = v.x;
-                    b[4 * i + 1] = v.y;
-                    b[4 * i + 2] = v.z;
-                    b[4 * i + 3] = v.w;
+                    for (int k = 0; k < 4; ++k) {
+                        const uint4 v = xs[k];
+                        b[4 * k] = v.x;
+                        b[4 * k + 1] = v.y;
+                        b[4 * k + 2] = v.z;
+                        b[4 * k + 3] = v.w;
+                    }
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) b[i] = 0u;
+                gv_granule(d, qg, sg, qu, su, b);
             }
-            gv_granule(d, qg, sg, qu, su, b);
             __syncwarp();
             if (lane == 0) mbar_arrive(&hd->empty[s]);
             if (++s == p.NS) {
@@ -286,9 +336,9 @@ __device__ bool gv_phase1(const KernelParams &p, GvHdr *hd, uint8_t *smem, int &
             }
         }
         if (t == 0) {
-            float *r = red1 + ((u - u0) * kGvWarps + w) * 16;
-            r[g] = d[0];
-            r[8 + g] = d[2];
+            float *r = red1 + (ul * kGvWarps + w) * 16;
+            r[g] = gv_sum4(d, 0);
+            r[8 + g] = gv_sum4(d, 2);
         }
     }
     return true;
@@ -313,8 +363,7 @@ __device__ void gv_write_h(const KernelParams &p, GvHdr *hd, const uint8_t *smem
             sg += rr[w * 16 + r];
             su += rr[w * 16 + 8 + r];
         }
-        const int e = hd->aexp[a];
-        const float gv = sg * expert_ts(p, 0, e) * xm, uv = su * expert_ts(p, 1, e) * xm;
+        const float gv = sg * hd->ts[0][a] * xm, uv = su * hd->ts[1][a] * xm;
         const float h = gv / (1.0f + __expf(-gv)) * uv;
         if (!(fabsf(h) < 3.0e38f)) atomicOr(p.ctrl + 2, kErrRange);
         p.gv_h[static_cast<size_t>(a) * p.I + ib * kGvUnit + r] = h;
@@ -371,60 +420,58 @@ __device__ void gv_h16(const KernelParams &p, GvHdr *hd, uint8_t *smem)
     }
 }
 
-// Phase 2, compute warp w: per down stage (group of 4 rows), items (expert set
-// s of 4 active experts, 128-element K range kr of I), warp w taking items w,
-// w + 16, ...  A rows: row g = (expert 4s + g/4, group row g%4), row g + 8 =
-// (expert 4s + 2 + g/4, row g%4); B column n (n < 4) = h16 of expert 4s + n.
-// The useful outputs: expert 4s + g/4 at column g/4 (quarter t = 0, d[g/4]),
-// expert 4s + 2 + g/4 at column 2 + g/4 (t = 1, d[2 + g/4]) -> red2[group][s][kr][expert in set * 4 + row].
-__device__ bool gv_phase2(const KernelParams &p, GvHdr *hd, uint8_t *smem, int &s, uint32_t &ph,
+// Phase 2, compute warp w: per down stage (gv_ep active experts, piece kp of
+// I), items (expert of the stage, 16-row tile tl of the CTA's rows,
+// 128-element K range kr of the piece), warp w taking items w, w + 16, ...; A rows tl 16 + g and tl 16 + g
+// + 8 of the CTA's rows (zero past R), B column 0 = h16 of expert a.  The
+// outputs (quarter t = 0: d[0], d[2]) go to red2[a][K range of I][row].
+__device__ bool gv_phase2(const KernelParams &p, GvHdr *hd, uint8_t *smem, const GvSeq &q, int &s, uint32_t &ph,
                           volatile int *abort_flag)
 {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
-    const int G = gridDim.x, j = blockIdx.x, nE = hd->nE;
-    const int NG = p.H / kGvGroup, g0 = gv_lo(j, NG, G), g1 = gv_lo(j + 1, NG, G);
-    const int nsets = (nE + 3) >> 2, nkr = p.I / 128, items = nsets * nkr;
-    const int QB = p.gv_qb, SB = gv_sb(p.I), r = g & 3;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, t = lane & 3, nE = hd->nE;
+    const int PK = p.gv_pk, RB = p.gv_rb, nkr = PK / 128, per = p.gv_tiles * nkr, rows16 = 16 * p.gv_tiles;
     float *red2 = reinterpret_cast<float *>(smem + p.gv_off_red2);
-    for (int gp = g0; gp < g1; ++gp) {
+    if (q.R == 0) return true;
+    for (int jd = 0; jd < q.neg * q.npc; ++jd) {
         if (!warp_wait_bar(p, &hd->full[s], ph, abort_flag)) return false;
-        const uint8_t *st = smem + s * p.stage_bytes;
-        for (int it = w; it < items; it += kGvWarps) {
-            const int sset = it / nkr, kr = it - sset * nkr;
-            const int alo = 4 * sset + (g >> 2), ahi = alo + 2;
-            const int G16 = 4 * kr + t, c = G16 >> 3, gi = G16 & 7;  // granule of the row, its chunk
-            const int offq = c * 512 + r * 128 + 16 * (gi ^ (((c << 2) + r) & 7));
+        const int ag = jd / q.npc, kp = jd - ag * q.npc, na = min(p.gv_ep, nE - ag * p.gv_ep);
+        for (int it = w; it < na * per; it += kGvWarps) {
+            const int ea = it / per, ir = it - ea * per, a = ag * p.gv_ep + ea;
+            const uint8_t *st = smem + s * p.stage_bytes + ea * p.gv_db;
+            const int tl = ir / nkr, kr = ir - tl * nkr;
+            const int rlo = 16 * tl + g, rhi = rlo + 8;
+            const int G16 = 4 * kr + t, c = G16 >> 3, gi = G16 & 7;
             uint4 qa = make_uint4(0u, 0u, 0u, 0u), qb = qa;
             uint16_t sa = 0, sb = 0;
-            if (alo < nE) {
-                qa = *reinterpret_cast<const uint4 *>(st + alo * QB + offq);
-                sa = *reinterpret_cast<const uint16_t *>(st + nE * QB + alo * SB + r * (p.I / 16) + 2 * G16);
+            if (rlo < q.R) {
+                qa = *reinterpret_cast<const uint4 *>(st + c * (RB * 128) + rlo * 128 + 16 * (gi ^ ((c * RB + rlo) & 7)));
+                sa = *reinterpret_cast<const uint16_t *>(st + p.gv_qb + rlo * (PK / 16) + 2 * G16);
             }
-            if (ahi < nE) {
-                qb = *reinterpret_cast<const uint4 *>(st + ahi * QB + offq);
-                sb = *reinterpret_cast<const uint16_t *>(st + nE * QB + ahi * SB + r * (p.I / 16) + 2 * G16);
+            if (rhi < q.R) {
+                qb = *reinterpret_cast<const uint4 *>(st + c * (RB * 128) + rhi * 128 + 16 * (gi ^ ((c * RB + rhi) & 7)));
+                sb = *reinterpret_cast<const uint16_t *>(st + p.gv_qb + rhi * (PK / 16) + 2 * G16);
             }
             uint32_t b[16];
-            const int an = 4 * sset + g;
-            if (g < 4 && an < nE) {
-                const uint4 *hs = reinterpret_cast<const uint4 *>(smem + p.gv_off_h16 + an * p.gv_h16p) + (kr * 128 + 32 * t) / 8;
+            {  // column 0 (lanes g = 0): h16 of expert a at the granule's 32 elements
+                const uint4 *hs = g == 0 ? reinterpret_cast<const uint4 *>(smem + p.gv_off_h16 + a * p.gv_h16p) +
+                                               (kp * PK + kr * 128 + 32 * t) / 8
+                                         : hd->zero16;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint4 v = hs[i];
-                    b[4 * i] = v.x;
-                    b[4 * i + 1] = v.y;
-                    b[4 * i + 2] = v.z;
-                    b[4 * i + 3] = v.w;
+                for (int k = 0; k < 4; ++k) {
+                    const uint4 v = hs[k];
+                    b[4 * k] = v.x;
+                    b[4 * k + 1] = v.y;
+                    b[4 * k + 2] = v.z;
+                    b[4 * k + 3] = v.w;
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) b[i] = 0u;
             }
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            float d[4][4] = {};
             gv_granule(d, qa, sa, qb, sb, b);
-            float *rr = red2 + (((gp - g0) * nsets + sset) * nkr + kr) * 16;
-            if (t == 0) rr[(g >> 2) * 4 + r] = (g >> 2) ? d[1] : d[0];
-            if (t == 1) rr[(2 + (g >> 2)) * 4 + r] = (g >> 2) ? d[3] : d[2];
+            if (t == 0) {
+                float *rr = red2 + (a * (p.I / 128) + kp * nkr + kr) * rows16;
+                rr[rlo] = gv_sum4(d, 0);
+                rr[rhi] = gv_sum4(d, 2);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&hd->empty[s]);
@@ -436,28 +483,24 @@ __device__ bool gv_phase2(const KernelParams &p, GvHdr *hd, uint8_t *smem, int &
     return true;
 }
 
-// After phase 2: y rows of the CTA's groups, each the token's slots in slot
-// order: w_j * (sum over K ranges of the expert's partials) * down tensor
-// scale * 2^-eh.
-__device__ void gv_write_y(const KernelParams &p, const GvHdr *hd, const uint8_t *smem)
+// After phase 2: the CTA's y rows, each the token's slots in slot order:
+// w_j * (the expert's partials summed over I in order) * down tensor scale * 2^-eh.
+__device__ void gv_write_y(const KernelParams &p, const GvHdr *hd, const uint8_t *smem, const GvSeq &q)
 {
-    const int tid = threadIdx.x, G = gridDim.x, j = blockIdx.x, nE = hd->nE;
-    const int NG = p.H / kGvGroup, g0 = gv_lo(j, NG, G), g1 = gv_lo(j + 1, NG, G);
-    const int nsets = (nE + 3) >> 2, nkr = p.I / 128;
+    const int nkr = p.I / 128, rows16 = 16 * p.gv_tiles;
     const float *red2 = reinterpret_cast<const float *>(smem + p.gv_off_red2);
-    for (int i = tid; i < (g1 - g0) * kGvGroup; i += 512) {
-        const int gl = i >> 2, r = i & 3;
+    for (int r = threadIdx.x; r < q.R; r += 512) {
         float y = 0.f;
         for (int jj = 0; jj < p.k; ++jj) {
             const int a = hd->slot_ae[jj];
             if (a < 0) continue;
-            const float *rr = red2 + ((gl * nsets + (a >> 2)) * nkr) * 16 + (a & 3) * 4 + r;
+            const float *rr = red2 + a * nkr * rows16 + r;
             float o = 0.f;
-            for (int kr = 0; kr < nkr; ++kr) o += rr[kr * 16];
-            o = mul_pow2(o * expert_ts(p, 2, hd->aexp[a]), -hd->eh[a]);
-            y += pair_w(p, 0, jj) * o;
+            for (int kr = 0; kr < nkr; ++kr) o += rr[kr * rows16];
+            o = mul_pow2(o * hd->ts[2][a], -hd->eh[a]);
+            y += hd->slot_w[jj] * o;
         }
-        p.y[(g0 + gl) * kGvGroup + r] = y;
+        p.y[kGvGroup * q.g0 + r] = y;
     }
 }
 
@@ -475,9 +518,9 @@ __global__ void __launch_bounds__(kGvThreads, 1) moe_gemv_kernel(const __grid_co
             mbar_init(&hd->full[i], 1);
             mbar_init(&hd->empty[i], kGvWarps);
         }
+        mbar_init(&hd->readybar, 1);
         hd->abort_flag = 0;
         hd->fill_cnt = 0;
-        hd->ready = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (tid == 32)
@@ -486,19 +529,32 @@ __global__ void __launch_bounds__(kGvThreads, 1) moe_gemv_kernel(const __grid_co
     if (tid == 64 && p.k > p.kr)
         for (int i = 0; i < 6; ++i)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.gvs[i])) : "memory");
+    {   // the whole parameter block through the constant cache while the
+        // previous kernel drains: its first reads after the wait below would
+        // otherwise be misses queued behind other CTAs' weight copies
+        const uint32_t *pw = reinterpret_cast<const uint32_t *>(&p);
+        uint32_t acc = 0;
+        for (int i = tid; i < static_cast<int>(sizeof(KernelParams) / 4); i += kGvThreads) acc ^= pw[i];
+        asm volatile("" ::"r"(acc));
+    }
     __syncthreads();
     // x, ids, w and the workspace may be written by the previous kernel
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp < kGvWarps) {
-        if (warp == 0) gv_tables(p, hd);
-        gv_x16(p, hd, smem);  // (its barrier also publishes the tables)
+        if (warp == 0) {
+            gv_tables(p, hd);
+            __syncwarp();
+            if (tid == 0) mbar_arrive(&hd->readybar);  // the producer starts now
+            gv_tables2(p, hd);
+        }
+        gv_x16(p, hd, smem);  // (its barrier also publishes the tables to the compute warps)
         gv_sync();
-        if (tid == 0) st_rel_cta(&hd->ready, 1);
+        const GvSeq q = gv_seq(p, hd->nE);
         int s = 0;
         uint32_t ph = 0;
-        bool ok = gv_phase1(p, hd, smem, s, ph, abort_flag);
+        bool ok = gv_phase1(p, hd, smem, q, s, ph, abort_flag);
         gv_sync();
         if (ok && !*abort_flag) gv_write_h(p, hd, smem);
         gv_sync();
@@ -524,11 +580,12 @@ __global__ void __launch_bounds__(kGvThreads, 1) moe_gemv_kernel(const __grid_co
         gv_sync();
         if (!*abort_flag) gv_h16(p, hd, smem);
         gv_sync();
-        if (ok && !*abort_flag) ok = gv_phase2(p, hd, smem, s, ph, abort_flag);
+        if (ok && !*abort_flag) ok = gv_phase2(p, hd, smem, q, s, ph, abort_flag);
         gv_sync();
-        if (ok && !*abort_flag) gv_write_y(p, hd, smem);
+        if (ok && !*abort_flag) gv_write_y(p, hd, smem, q);
     } else {
-        if (!warp_spin(p, [&] { return ld_acq_cta(&hd->ready) != 0; }, abort_flag)) {
+        // (an mbarrier wait suspends the warp instead of spinning)
+        if (!warp_wait_bar(p, &hd->readybar, 0u, abort_flag)) {
             if ((tid & 31) == 0) *abort_flag = 1;
         } else {
             gv_producer(p, hd, smem, abort_flag);

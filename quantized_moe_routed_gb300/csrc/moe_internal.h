@@ -131,16 +131,21 @@ struct KernelParams {
     int s_off_x, s_off_xsc, s_off_xmul, s_off_h, s_off_hsc, s_off_hmul, s_off_scr, s_off_alo;  // shared-memory offsets
 
     // ---- one-token row kernel (moe_gemv.cu) ----
-    // TMA descriptors: 0 gate_q, 1 up_q (box {128 B, 8 rows, 8 256-element
-    // chunks}, 128-byte swizzle), 2 gate_s, 3 up_s (box {128 B, 8 rows}, 128-byte
-    // swizzle), 4 down_q (box {128 B, 4 rows, I/256 chunks}, 128-byte swizzle),
-    // 5 down_s (box {I/16 B, 4 rows}); gvs: the same for the shared expert
+    // TMA descriptors: 0 gate_q, 1 up_q (box {128 B, 8 rows, KS/256 chunks},
+    // 128-byte swizzle), 2 gate_s, 3 up_s (box {128 B, 8 rows, KS/2048 chunks},
+    // 128-byte swizzle), 4 down_q (box {128 B, RB rows, PK/256 chunks}, 128-byte
+    // swizzle), 5 down_s (box {PK/16 B, RB rows}); gvs: the same for the shared expert
     CUtensorMap gv[6];
     CUtensorMap gvs[6];
     float *gv_h;                  // [active experts][I] h rows (fp32)
     unsigned long long *gv_cnt;   // grid-barrier arrivals (one per CTA per launch)
     int gv_off_hdr, gv_off_x16, gv_off_h16, gv_h16p, gv_off_red1, gv_off_red2;  // shared-memory layout
-    int gv_qb;                    // bytes per expert of a down stage's E2M1 boxes (2I rounded up to 1 KB)
+    int gv_qb;                    // bytes of a down stage's E2M1 box, rounded up to 1 KB (its scale box follows)
+    int gv_ks;                    // K elements of H per gate/up stage (2048 or 4096)
+    int gv_pk;                    // K elements of I per down stage (a divisor of I, at most 2048)
+    int gv_rb;                    // rows of a down stage's boxes (4 x the largest group count of a CTA)
+    int gv_tiles;                 // 16-row tiles over gv_rb
+    int gv_ep, gv_db;             // experts per down stage, bytes per expert in it (1 KB multiple)
 };
 
 // Dynamic shared memory layout of the persistent kernel for P pairs.
@@ -183,7 +188,7 @@ constexpr int kSmAccCols = 128;     // tensor-memory columns of one accumulator 
 constexpr int kSmMaxNSF = (512 - 2 * kSmAccCols) / 64;  // scale-factor slots beside two accumulator buffers
 // One-token row kernel (moe_gemv.cu): ring slots and the control block size.
 constexpr int kGvMaxSlots = 12;
-constexpr int kGvHdrBytes = 512;
+constexpr int kGvHdrBytes = 1024;
 cudaError_t launch_gemv(const KernelParams &p, int grid, int smem_bytes, bool pdl, cudaStream_t st);
 cudaError_t set_gemv_smem_limit(int bytes);
 cudaError_t launch_small(const KernelParams &p, int grid, int smem_bytes, bool pdl, cudaStream_t st);
