@@ -74,6 +74,7 @@ struct GvHdr {
     float red[kGvWarps];         // block-wide maximum scratch
     float slot_w[kGvMaxE];       // slot j's routing weight (1 for the shared expert's slot)
     float ts[3][kGvMaxE];        // per active expert: gate, up, down tensor scales
+    float fa[kGvMaxE];           // per active expert: routing weight * down tensor scale * 2^-eh (after the h16 build)
     uint4 zero16[4];             // 64 zero bytes: the B operand of lanes without a column
 };
 static_assert(sizeof(GvHdr) <= kGvHdrBytes, "control block too large");
@@ -291,20 +292,45 @@ __device__ __forceinline__ float gv_sum4(const float (&d)[4][4], int k)
 // warp takes elements [w KS/16, (w + 1) KS/16) in steps of 128 (granules
 // 4 step + t of its range); rows g (gate) and g + 8 (up = the same row of I).
 // The unit's partial sums (lanes of quarter t = 0 hold column 0: the token)
-// go to red1[unit][w][16] after its last stage.  false on abort.
+// go to red1[unit][w][16] after its last stage.  XN > 0: one K slice covers
+// all of H (KS = H, XN = KS / 2048 steps), so the warp's x operand is the
+// same in every stage and is read once into registers; XN = 0: read per
+// step.  false on abort.
+__device__ __forceinline__ void gv_x_operand(const GvHdr *hd, const uint4 *x16, int e0, int g, uint32_t (&b)[16])
+{
+    // column 0 (lanes g = 0): x at elements e0 .. e0 + 31; the other columns read zeros
+    const uint4 *xs = g == 0 ? x16 + e0 / 8 : hd->zero16;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint4 v = xs[k];
+        b[4 * k] = v.x;
+        b[4 * k + 1] = v.y;
+        b[4 * k + 2] = v.z;
+        b[4 * k + 3] = v.w;
+    }
+}
+template <int XN>
 __device__ bool gv_phase1(const KernelParams &p, GvHdr *hd, uint8_t *smem, const GvSeq &q, int &s, uint32_t &ph,
                           volatile int *abort_flag)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
-    const int KS = p.gv_ks, nstep = KS / 2048;
+    const int KS = p.gv_ks, nstep = XN > 0 ? XN : KS / 2048;
     const uint4 *x16 = reinterpret_cast<const uint4 *>(smem + p.gv_off_x16);
     float *red1 = reinterpret_cast<float *>(smem + p.gv_off_red1);
+    uint32_t xb[XN > 0 ? XN : 1][16];
+    if (XN > 0) {
+#pragma unroll
+        for (int step = 0; step < (XN > 0 ? XN : 1); ++step)
+            gv_x_operand(hd, x16, 32 * (w * (KS / 512) + 4 * step + t), g, xb[step]);
+    }
     for (int ul = 0; ul < q.nu; ++ul) {
         float d[4][4] = {};
         for (int ks = 0; ks < q.nks; ++ks) {
             if (!warp_wait_bar(p, &hd->full[s], ph, abort_flag)) return false;
             const uint8_t *st = smem + s * p.stage_bytes;
-            for (int step = 0; step < nstep; ++step) {
+#pragma unroll
+            for (int step = 0; step < (XN > 0 ? XN : 2); ++step) {
+                if (XN == 0 && step >= nstep) break;
                 const int G = w * (KS / 512) + 4 * step + t;  // this lane's granule of the stage
                 const int c = G >> 3, gi = G & 7;
                 const int offq = c * 1024 + g * 128 + 16 * (gi ^ g);
@@ -314,19 +340,13 @@ __device__ bool gv_phase1(const KernelParams &p, GvHdr *hd, uint8_t *smem, const
                 const uint4 qu = *reinterpret_cast<const uint4 *>(st + 4 * KS + offq);
                 const uint16_t sg = *reinterpret_cast<const uint16_t *>(st + 8 * KS + offs);
                 const uint16_t su = *reinterpret_cast<const uint16_t *>(st + 8 * KS + KS / 2 + offs);
-                uint32_t b[16];
-                {  // column 0 (lanes g = 0): x at the granule's 32 elements; the other columns read zeros
-                    const uint4 *xs = g == 0 ? x16 + (ks * KS + 32 * G) / 8 : hd->zero16;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint4 v = xs[k];
-                        b[4 * k] = v.x;
-                        b[4 * k + 1] = v.y;
-                        b[4 * k + 2] = v.z;
-                        b[4 * k + 3] = v.w;
-                    }
+                if (XN > 0) {
+                    gv_granule(d, qg, sg, qu, su, xb[XN > 0 ? step : 0]);
+                } else {
+                    uint32_t b[16];
+                    gv_x_operand(hd, x16, ks * KS + 32 * G, g, b);
+                    gv_granule(d, qg, sg, qu, su, b);
                 }
-                gv_granule(d, qg, sg, qu, su, b);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&hd->empty[s]);
@@ -400,7 +420,13 @@ __device__ void gv_h16(const KernelParams &p, GvHdr *hd, uint8_t *smem)
                     __half2 lo = __floats2half2_rn(v[i].x * sc, v[i].y * sc), hi = __floats2half2_rn(v[i].z * sc, v[i].w * sc);
                     dst[32 * i + lane] = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
                 }
-            if (lane == 0) hd->eh[a] = eh;
+            if (lane == 0) {
+                hd->eh[a] = eh;
+                float wa = 0.f;  // the expert's routing weight: its slots' weights, in slot order
+                for (int jj = 0; jj < p.k; ++jj)
+                    if (hd->slot_ae[jj] == a) wa += hd->slot_w[jj];
+                hd->fa[a] = mul_pow2(hd->ts[2][a], -eh) * wa;
+            }
         } else {  // two passes over L2
             for (int i = lane; i < p.I / 4; i += 32) {
                 const float4 v = __ldcg(src + i);
@@ -415,42 +441,37 @@ __device__ void gv_h16(const KernelParams &p, GvHdr *hd, uint8_t *smem)
                 __half2 lo = __floats2half2_rn(v.x * sc, v.y * sc), hi = __floats2half2_rn(v.z * sc, v.w * sc);
                 dst[i] = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
             }
-            if (lane == 0) hd->eh[a] = eh;
+            if (lane == 0) {
+                hd->eh[a] = eh;
+                float wa = 0.f;  // the expert's routing weight: its slots' weights, in slot order
+                for (int jj = 0; jj < p.k; ++jj)
+                    if (hd->slot_ae[jj] == a) wa += hd->slot_w[jj];
+                hd->fa[a] = mul_pow2(hd->ts[2][a], -eh) * wa;
+            }
         }
     }
 }
 
 // Phase 2, compute warp w: per down stage (gv_ep active experts, piece kp of
-// I), items (expert of the stage, 16-row tile tl of the CTA's rows,
-// 128-element K range kr of the piece), warp w taking items w, w + 16, ...; A rows tl 16 + g and tl 16 + g
-// + 8 of the CTA's rows (zero past R), B column 0 = h16 of expert a.  The
-// outputs (quarter t = 0: d[0], d[2]) go to red2[a][K range of I][row].
+// I), items (expert of the stage, 128-element K range kr of the piece), warp
+// w taking items w, w + 16, ...; per item the B operand (column 0 = h16 of
+// expert a at the K range) is read once and serves every 16-row tile tl of
+// the CTA's rows: A rows tl 16 + g and tl 16 + g + 8 (zero past R).  The
+// outputs (quarter t = 0: d[0], d[2]) times fa[a] go to red2[a][row][K range of I].
 __device__ bool gv_phase2(const KernelParams &p, GvHdr *hd, uint8_t *smem, const GvSeq &q, int &s, uint32_t &ph,
                           volatile int *abort_flag)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, t = lane & 3, nE = hd->nE;
-    const int PK = p.gv_pk, RB = p.gv_rb, nkr = PK / 128, per = p.gv_tiles * nkr, rows16 = 16 * p.gv_tiles;
+    const int PK = p.gv_pk, RB = p.gv_rb, nkr = PK / 128, nkt = p.I / 128, rows16 = 16 * p.gv_tiles;
     float *red2 = reinterpret_cast<float *>(smem + p.gv_off_red2);
     if (q.R == 0) return true;
     for (int jd = 0; jd < q.neg * q.npc; ++jd) {
         if (!warp_wait_bar(p, &hd->full[s], ph, abort_flag)) return false;
         const int ag = jd / q.npc, kp = jd - ag * q.npc, na = min(p.gv_ep, nE - ag * p.gv_ep);
-        for (int it = w; it < na * per; it += kGvWarps) {
-            const int ea = it / per, ir = it - ea * per, a = ag * p.gv_ep + ea;
+        for (int it = w; it < na * nkr; it += kGvWarps) {
+            const int ea = it / nkr, kr = it - ea * nkr, a = ag * p.gv_ep + ea;
             const uint8_t *st = smem + s * p.stage_bytes + ea * p.gv_db;
-            const int tl = ir / nkr, kr = ir - tl * nkr;
-            const int rlo = 16 * tl + g, rhi = rlo + 8;
             const int G16 = 4 * kr + t, c = G16 >> 3, gi = G16 & 7;
-            uint4 qa = make_uint4(0u, 0u, 0u, 0u), qb = qa;
-            uint16_t sa = 0, sb = 0;
-            if (rlo < q.R) {
-                qa = *reinterpret_cast<const uint4 *>(st + c * (RB * 128) + rlo * 128 + 16 * (gi ^ ((c * RB + rlo) & 7)));
-                sa = *reinterpret_cast<const uint16_t *>(st + p.gv_qb + rlo * (PK / 16) + 2 * G16);
-            }
-            if (rhi < q.R) {
-                qb = *reinterpret_cast<const uint4 *>(st + c * (RB * 128) + rhi * 128 + 16 * (gi ^ ((c * RB + rhi) & 7)));
-                sb = *reinterpret_cast<const uint16_t *>(st + p.gv_qb + rhi * (PK / 16) + 2 * G16);
-            }
             uint32_t b[16];
             {  // column 0 (lanes g = 0): h16 of expert a at the granule's 32 elements
                 const uint4 *hs = g == 0 ? reinterpret_cast<const uint4 *>(smem + p.gv_off_h16 + a * p.gv_h16p) +
@@ -465,12 +486,26 @@ __device__ bool gv_phase2(const KernelParams &p, GvHdr *hd, uint8_t *smem, const
                     b[4 * k + 3] = v.w;
                 }
             }
-            float d[4][4] = {};
-            gv_granule(d, qa, sa, qb, sb, b);
-            if (t == 0) {
-                float *rr = red2 + (a * (p.I / 128) + kp * nkr + kr) * rows16;
-                rr[rlo] = gv_sum4(d, 0);
-                rr[rhi] = gv_sum4(d, 2);
+            float *rr = red2 + a * rows16 * nkt + kp * nkr + kr;
+            const float fa = hd->fa[a];
+            for (int tl = 0; tl < p.gv_tiles; ++tl) {
+                const int rlo = 16 * tl + g, rhi = rlo + 8;
+                uint4 qa = make_uint4(0u, 0u, 0u, 0u), qb = qa;
+                uint16_t sa = 0, sb = 0;
+                if (rlo < q.R) {
+                    qa = *reinterpret_cast<const uint4 *>(st + c * (RB * 128) + rlo * 128 + 16 * (gi ^ ((c * RB + rlo) & 7)));
+                    sa = *reinterpret_cast<const uint16_t *>(st + p.gv_qb + rlo * (PK / 16) + 2 * G16);
+                }
+                if (rhi < q.R) {
+                    qb = *reinterpret_cast<const uint4 *>(st + c * (RB * 128) + rhi * 128 + 16 * (gi ^ ((c * RB + rhi) & 7)));
+                    sb = *reinterpret_cast<const uint16_t *>(st + p.gv_qb + rhi * (PK / 16) + 2 * G16);
+                }
+                float d[4][4] = {};
+                gv_granule(d, qa, sa, qb, sb, b);
+                if (t == 0) {
+                    rr[rlo * nkt] = gv_sum4(d, 0) * fa;
+                    rr[rhi * nkt] = gv_sum4(d, 2) * fa;
+                }
             }
         }
         __syncwarp();
@@ -483,24 +518,25 @@ __device__ bool gv_phase2(const KernelParams &p, GvHdr *hd, uint8_t *smem, const
     return true;
 }
 
-// After phase 2: the CTA's y rows, each the token's slots in slot order:
-// w_j * (the expert's partials summed over I in order) * down tensor scale * 2^-eh.
+// After phase 2: the CTA's y rows, warp w taking rows w, w + 16, ...: lane
+// kr (kr < I / 128) adds red2[a][row][kr] over the active experts a in
+// order, and the lanes' sums are added in a fixed butterfly (every lane ends
+// with the same bits).  red2 already carries each expert's factor fa[a].
 __device__ void gv_write_y(const KernelParams &p, const GvHdr *hd, const uint8_t *smem, const GvSeq &q)
 {
-    const int nkr = p.I / 128, rows16 = 16 * p.gv_tiles;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nkt = p.I / 128, nE = hd->nE;
+    const int astride = 16 * p.gv_tiles * nkt;
     const float *red2 = reinterpret_cast<const float *>(smem + p.gv_off_red2);
-    for (int r = threadIdx.x; r < q.R; r += 512) {
+    for (int r = w; r < q.R; r += kGvWarps) {
         float y = 0.f;
-        for (int jj = 0; jj < p.k; ++jj) {
-            const int a = hd->slot_ae[jj];
-            if (a < 0) continue;
-            const float *rr = red2 + a * nkr * rows16 + r;
-            float o = 0.f;
-            for (int kr = 0; kr < nkr; ++kr) o += rr[kr * rows16];
-            o = mul_pow2(o * hd->ts[2][a], -hd->eh[a]);
-            y += hd->slot_w[jj] * o;
+        if (lane < nkt) {
+            const float *rr = red2 + r * nkt + lane;
+#pragma unroll 4
+            for (int a = 0; a < nE; ++a) y += rr[a * astride];
         }
-        p.y[kGvGroup * q.g0 + r] = y;
+#pragma unroll
+        for (int d = 16; d; d >>= 1) y += __shfl_xor_sync(0xffffffffu, y, d);
+        if (lane == 0) p.y[kGvGroup * q.g0 + r] = y;
     }
 }
 
@@ -554,7 +590,9 @@ __global__ void __launch_bounds__(kGvThreads, 1) moe_gemv_kernel(const __grid_co
         const GvSeq q = gv_seq(p, hd->nE);
         int s = 0;
         uint32_t ph = 0;
-        bool ok = gv_phase1(p, hd, smem, q, s, ph, abort_flag);
+        bool ok = q.nks > 1           ? gv_phase1<0>(p, hd, smem, q, s, ph, abort_flag)
+                  : p.gv_ks == 2048     ? gv_phase1<1>(p, hd, smem, q, s, ph, abort_flag)
+                                        : gv_phase1<2>(p, hd, smem, q, s, ph, abort_flag);
         gv_sync();
         if (ok && !*abort_flag) gv_write_h(p, hd, smem);
         gv_sync();
