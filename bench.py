@@ -6,7 +6,8 @@ H=4096, I=1024, E=256, top-k=8.  Reported metric: achieved HBM GB/s
 (algorithmic bytes of the touched experts' weights and scales plus x, ids,
 weights and y, divided by the step time); ms_per_step and us_per_step beside
 it.  The T=16 and T=24 decode workloads are measured the same way and reported
-under "decode_sweep".
+under "decode_sweep"; the shared expert (T=1, T=24) and the single NVFP4
+activation quantisation (T=24, prefill T=512) under "variants".
 
 Cold reads: every step relabels the expert ids by (id + step*delta) mod E, with
 delta chosen so that 8 consecutive steps touch disjoint experts; the bytes
@@ -64,6 +65,8 @@ KERNEL_DTYPE = {
                              "digit rows, fp32 accumulation"),
     "moe_step_kernel": ("fp16", "mma.sync fp16 operands (E2M1 x E4M3 dequantised exactly, prescaled "
                                 "activations), fp32 accumulation"),
+    "act_quant": ("fp4", "tcgen05 block-scaled FP4 MMA: NVFP4 weights as stored, x and h quantised once to NVFP4 "
+                         "(one FP4 row, E4M3 scale per 16), fp32 accumulation"),
 }
 
 
@@ -227,6 +230,70 @@ def setup(wl_name, device, kernel=None):
     return dict(wl=wl, x=x, ids=ids, w=w, W=W, plan=plan, ws=ws, ids_rot=ids_rot, delta=delta, kernel=kname,
                 bytes=algorithmic_bytes(wl, ids), xd=x.to(device), wd=w.to(device),
                 y=torch.empty((wl.T, wl.H), dtype=torch.float32, device=device))
+
+
+def variant(S, device, shared=False, act_quant=False):
+    """S with another plan over the same expert weights: a shared expert
+    and/or the single NVFP4 activation quantisation."""
+    from quantized_moe_routed_gb300 import MoePlan
+    from quantized_moe_routed_gb300.inputs import algorithmic_bytes, make_shared_weights
+    wl = S["wl"]
+    sh = make_shared_weights(wl, device=device) if shared else None
+    plan = MoePlan(S["W"], wl.H, wl.I, wl.E, wl.k, T_max=wl.T, strict=True, pdl=True, shared=sh,
+                   act_quant=act_quant)
+    V = dict(S)
+    V.update(plan=plan, ws=plan.new_workspace(), bytes=algorithmic_bytes(wl, S["ids"], shared=shared), sh=sh)
+    return V
+
+
+def time_variant(V, reps):
+    g, st = capture(V)
+    ms = time_graph(g, st, reps, 3)
+    assert V["plan"].check(V["ws"]) == 0
+    return ms
+
+
+def variants(device, hbm, main_ms):
+    """The shared expert (decode and upper_decode) and the single NVFP4
+    activation quantisation (upper_decode and prefill) beside the default
+    plans, each timed like the headline (CUDA graph of GRAPH_STEPS steps)."""
+    out = {"shared_expert": {}, "act_quant": {}}
+    for name in ("decode", "upper_decode"):
+        S = setup(name, device)
+        reps = 16 if S["wl"].T == 1 else 4
+        base = main_ms if name == "decode" and main_ms else time_variant(S, reps)
+        V = variant(S, device, shared=True)
+        ms = time_variant(V, reps)
+        out["shared_expert"][name] = {
+            "T": S["wl"].T, "us_per_step": ms * 1e3, "us_per_step_without": base * 1e3,
+            "added_us": (ms - base) * 1e3, "algorithmic_bytes_per_step": V["bytes"],
+            "shared_expert_bytes": V["bytes"] - S["bytes"], "GB/s": V["bytes"] / (ms * 1e-3) / 1e9,
+            "frac": V["bytes"] / (ms * 1e-3) / 1e9 / hbm, "kernel": S["kernel"],
+            "note": "the shared expert's 7 MB are the same every step (L2-resident between steps); the routed "
+                    "experts rotate (cold)"}
+        if name == "upper_decode":
+            A = variant(S, device, act_quant=True)
+            ms_a = time_variant(A, reps)
+            out["act_quant"][name] = {
+                "T": S["wl"].T, "us_per_step": ms_a * 1e3, "us_per_step_four_digit": base * 1e3,
+                "GB/s": A["bytes"] / (ms_a * 1e-3) / 1e9, "frac": A["bytes"] / (ms_a * 1e-3) / 1e9 / hbm,
+                "algorithmic_bytes_per_step": A["bytes"], "kernel": "moe_tc_kernel",
+                "dtype": KERNEL_DTYPE["act_quant"][0], "dtype_detail": KERNEL_DTYPE["act_quant"][1]}
+        del S, V
+        torch.cuda.empty_cache()
+    S = setup("prefill", device)
+    base = time_variant(S, 2)
+    A = variant(S, device, act_quant=True)
+    ms_a = time_variant(A, 2)
+    out["act_quant"]["prefill"] = {
+        "T": S["wl"].T, "us_per_step": ms_a * 1e3, "us_per_step_four_digit": base * 1e3,
+        "GB/s": A["bytes"] / (ms_a * 1e-3) / 1e9, "frac": A["bytes"] / (ms_a * 1e-3) / 1e9 / hbm,
+        "frac_four_digit": S["bytes"] / (base * 1e-3) / 1e9 / hbm,
+        "algorithmic_bytes_per_step": A["bytes"], "kernel": "moe_tc_kernel",
+        "dtype": KERNEL_DTYPE["act_quant"][0], "dtype_detail": KERNEL_DTYPE["act_quant"][1]}
+    del S, A
+    torch.cuda.empty_cache()
+    return out
 
 
 def capture(S, null=False):
@@ -506,10 +573,11 @@ def main():
         # null-dequant ceiling (same bytes, no math) on the same schedule
         gn, stn = capture(S, null=True)
         ms_null = time_graph(gn, stn, max(1, reps // 4), 2)
+        nk = S["kernel"] if S["kernel"] == "moe_gemv_kernel" else "moe_step_kernel"
         out["null_dequant"] = {"us_per_step": ms_null * 1e3, "GB/s": S["bytes"] / (ms_null * 1e-3) / 1e9,
-                               "kernel": "moe_step_kernel",
-                               "form": "the register kernel's schedule with the dequantisation and arithmetic "
-                                       "removed (moe_null_step): its streaming ceiling"}
+                               "kernel": nk,
+                               "form": f"{nk}'s schedule (the same copies, waits and barriers) with the "
+                                       "dequantisation and arithmetic removed (moe_null_step): its streaming ceiling"}
         ms_e2e, h2d, d2h = time_e2e(S, min(steps, 2000))
         out["e2e"] = {"value": S["bytes"] / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "us_per_step": ms_e2e * 1e3,
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -531,6 +599,14 @@ def main():
                                "traffic": measured_traffic(S["kernel"], name)}
             out["decode_sweep"] = sweep
             del S
+            S = setup(args.workload, device)
+        if not args.no_sweep and args.workload == "decode":
+            try:
+                del S
+                torch.cuda.empty_cache()
+                out["variants"] = variants(device, hbm, ms)
+            except Exception as exc:  # noqa: BLE001 -- reported, never fatal to the line
+                out["variants"] = {"unavailable": str(exc).splitlines()[0][:200] if str(exc) else type(exc).__name__}
             S = setup(args.workload, device)
         if not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline(S)

@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define MOE_NVFP4_ABI_VERSION 7
+#define MOE_NVFP4_ABI_VERSION 8
 
 typedef enum {
     MOE_OK = 0,
@@ -52,7 +52,11 @@ typedef enum {
     MOE_ERR_CUDA = 5,              /* a CUDA runtime call failed (message has details) */
     MOE_ERR_TIMEOUT = 6,           /* device: a bounded wait gave up (see moe_check)   */
     MOE_ERR_BAD_EXPERT_ID = 7,     /* device: an id >= E was seen (slot skipped)       */
-    MOE_ERR_RANGE = 8              /* device: an intermediate (h) was not finite      */
+    MOE_ERR_RANGE = 8,             /* device: an intermediate (h) was not finite      */
+    MOE_ERR_SCALE = 9,             /* device: a weight block scale the tensor-core     */
+                                   /*   kernels cannot read (sign bit set, or NaN)    */
+    MOE_ERR_WORKSPACE_BUSY = 10    /* host: the workspace is in flight on another     */
+                                   /*   stream                                        */
 } moe_status_t;
 
 /* Opaque plan: host memory owned by the library (moe_plan_destroy frees it). */
@@ -104,9 +108,12 @@ typedef struct {
                 /*     ticket kernel (the environment variable MOE_SMALL=0 at    */
                 /*     plan creation leaves the small-launch kernel out) (the plan */
                 /*     is refused with UNSUPPORTED_SHAPE where the shape does not */
-                /*     allow it).  Its block scales must be non-negative E4M3     */
-                /*     codes (the MMA reads them unsigned), as an NVFP4 quantiser */
-                /*     writes them.                                               */
+                /*     allow it).  The tensor-core kernels need non-negative,     */
+                /*     non-NaN E4M3 block scales (the MMA reads them unsigned),   */
+                /*     as an NVFP4 quantiser writes them; their scale warps check */
+                /*     every weight scale they stage and a launch that met a      */
+                /*     negative or NaN one reports MOE_ERR_SCALE (its y is then   */
+                /*     wrong).  The register and row kernels decode the sign.     */
     /* Shared expert (optional; NULL shared_gate_q_dev: none).  One always-on
      * SwiGLU expert in the same NVFP4 format, added to every token's y with
      * weight 1 after the routed slots, inside the same launch (the serving
@@ -172,14 +179,21 @@ void moe_plan_destroy(moe_plan_t plan);
  * one workspace serves every T the plan accepts.
  * One workspace per stream that runs MoE steps concurrently: two launches
  * sharing a workspace at the same time corrupt each other's counters (the
- * pages' two-stream deadlock, "dsv4-carve" README, trap 3).  Returns 0 for
- * an invalid plan or T. */
+ * pages' two-stream deadlock, "dsv4-carve" README, trap 3).  The library
+ * records an event after each launch on a workspace (moe_decode, moe_prefill,
+ * moe_null_step, moe_step_host, moe_group, moe_workspace_init) and refuses a
+ * launch on another stream while that event is pending, or while another
+ * thread is launching on it from another stream, with MOE_ERR_WORKSPACE_BUSY
+ * (nothing queued).  Launches being captured into a CUDA graph are not
+ * checked: the graph's replays are ordered by whoever launches them.
+ * Returns 0 for an invalid plan or T. */
 size_t moe_workspace_bytes(moe_plan_t plan, int T);
 
 /* Zero a workspace of `bytes` bytes (>= moe_workspace_bytes(plan, T_max))
  * on `stream`.  Required once after allocation and after any device-side
  * error; the kernels reset their own counters after every successful launch.
- * ws_dev must be 256-byte aligned. */
+ * ws_dev must be 256-byte aligned.  MOE_ERR_WORKSPACE_BUSY while the
+ * workspace is in flight on another stream. */
 moe_status_t moe_workspace_init(moe_plan_t plan, void *ws_dev, size_t bytes, void *stream);
 
 /* Grouping only (bit-exact, integer): for the P = T*top_k flat pairs
@@ -193,6 +207,9 @@ moe_status_t moe_group(moe_plan_t plan, const int32_t *ids_dev, int T, void *ws_
                        int32_t *counts_dev, int32_t *offsets_dev, int32_t *perm_dev, void *stream);
 
 /* The routed-experts step for 0 <= T <= 24 tokens (decode; T == 0 is a no-op).
+ * Status: MOE_OK (queued), INVALID_ARG, MISALIGNED, NOT_FAST_PATH, CUDA, or
+ * WORKSPACE_BUSY (ws_dev in flight on another stream; nothing queued).
+ * Device-side outcomes go to the workspace error word (moe_check).
  *   x_dev    bf16 [T, H] row-major, 16-byte aligned; any finite bf16 values:
  *            both kernels prescale each token's row by a power of two before
  *            narrowing it (fp16 mma.sync operands, or FP4 digit rows) and undo
@@ -201,8 +218,9 @@ moe_status_t moe_group(moe_plan_t plan, const int32_t *ids_dev, int T, void *ws_
  *   w_dev    float [T, top_k] routing weights, used as given
  *   y_dev    float [T, H] row-major, 16-byte aligned; fully written
  *   ws_dev   workspace of moe_workspace_bytes(plan, T) bytes, 256-byte aligned
- * One persistent launch: grouping in the prologue, gate/up and down tickets,
- * deterministic combine (bitwise identical run to run).  T > 24 is forwarded
+ * One persistent launch of the kernel the plan's `kernel` field picks for T
+ * (grouping, gate/up, SiLU * up, down and the weighted combine all inside it),
+ * bitwise identical run to run.  T > 24 is forwarded
  * to moe_prefill unless strict mode is on (then MOE_ERR_NOT_FAST_PATH).
  * No allocation and no synchronisation inside. */
 moe_status_t moe_decode(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
@@ -226,10 +244,13 @@ moe_status_t moe_decode(moe_plan_t plan, const void *x_dev, const int32_t *ids_d
  * device address, which may load the module); make that first call before
  * any stream capture.  Every call on a device shares the one buffer, so calls
  * that overlap in time (other streams, other threads, other plans on the
- * same device) race and corrupt each other: order them on one stream.
+ * same device) would race: a call while the scratch is in flight on another
+ * stream is refused with MOE_ERR_WORKSPACE_BUSY (order such calls on one
+ * stream).
  * check == 0: asynchronous, no synchronisation.  check != 0: synchronise
  * `stream` after the launch and return the device error status (MOE_OK,
- * MOE_ERR_TIMEOUT, MOE_ERR_BAD_EXPERT_ID or MOE_ERR_RANGE, as moe_check). */
+ * MOE_ERR_TIMEOUT, MOE_ERR_BAD_EXPERT_ID, MOE_ERR_SCALE or MOE_ERR_RANGE, as
+ * moe_check). */
 moe_status_t moe_decode_static(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
                                float *y_dev, int T, int check, void *stream);
 
@@ -283,9 +304,12 @@ moe_status_t moe_prefill(moe_plan_t plan, const void *x_dev, const int32_t *ids_
                          float *y_dev, int T, void *ws_dev, void *stream);
 
 /* Measurement variant of moe_decode/moe_prefill: streams exactly the same
- * weight bytes through the same ticket schedule but skips dequantisation and
- * all arithmetic; y receives a checksum, not the step's result (the pages'
- * "null-decode" variant, "LNA-CANON.md", section "lna2 とは"). */
+ * weight bytes through the same schedule but skips dequantisation and all
+ * arithmetic; y receives a checksum (register kernel) or zeros (one-token row
+ * kernel), not the step's result (the pages' "null-decode" variant,
+ * "LNA-CANON.md", section "lna2 とは").  A single token on a plan that takes
+ * the one-token row kernel runs that kernel's schedule; every other launch the
+ * register kernel's. */
 moe_status_t moe_null_step(moe_plan_t plan, const void *x_dev, const int32_t *ids_dev, const float *w_dev,
                            float *y_dev, int T, void *ws_dev, void *stream);
 
@@ -310,8 +334,10 @@ moe_status_t moe_route(moe_plan_t plan, const float *logits_dev, int T, int32_t 
                        void *stream);
 
 /* Synchronise `stream`, read and clear the workspace's device error word.
- * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_BAD_EXPERT_ID or MOE_ERR_RANGE
- * (the first set, in that order), or MOE_ERR_CUDA. */
+ * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_BAD_EXPERT_ID, MOE_ERR_SCALE or
+ * MOE_ERR_RANGE (the first set, in that order: an unreadable scale also makes
+ * h non-finite), or MOE_ERR_CUDA.  Not a
+ * launch: it does not take part in the workspace's stream check. */
 moe_status_t moe_check(moe_plan_t plan, void *ws_dev, void *stream);
 
 /* Test support for the failure path: set every gate/up completion counter in

@@ -19,9 +19,10 @@ LIB_PATH = os.path.join(_HERE, "_build", "libmoe_nvfp4.so")
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_NOT_FAST_PATH",
                 4: "MOE_ERR_MISALIGNED", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_BAD_EXPERT_ID",
-                8: "MOE_ERR_RANGE"}
+                8: "MOE_ERR_RANGE", 9: "MOE_ERR_SCALE", 10: "MOE_ERR_WORKSPACE_BUSY"}
 MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_NOT_FAST_PATH, MOE_ERR_MISALIGNED = 1, 2, 3, 4
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_BAD_EXPERT_ID, MOE_ERR_RANGE = 5, 6, 7, 8
+MOE_ERR_SCALE, MOE_ERR_WORKSPACE_BUSY = 9, 10
 
 # Every function include/moe_nvfp4.h declares: name -> (restype, argtypes).
 _P, _I, _S = C.c_void_p, C.c_int, C.c_size_t

@@ -44,6 +44,100 @@ bool env_flag(const char *name)
 std::once_flag g_active_once;
 std::once_flag g_gv_once;
 
+// ------------------------------------------------------------------ workspace ownership
+// Which stream each workspace was last launched on, with an event recorded
+// after that launch.  A launch on another stream while that event is pending
+// (or while another thread is between its claim and its record) is refused
+// with MOE_ERR_WORKSPACE_BUSY: two launches in flight on one workspace would
+// share its counters and scratch.  Launches captured into a CUDA graph are
+// not tracked (the graph's replays are ordered by whoever launches them).
+struct WsUse {
+    const void *ws = nullptr;
+    cudaStream_t st = nullptr;
+    cudaEvent_t ev = nullptr;
+    bool recorded = false;
+    int pending = 0;  // claims on st not yet released
+};
+std::mutex g_ws_mu;
+WsUse g_ws[64];
+
+struct WsTicket {
+    WsUse *u = nullptr;  // null: not tracked (graph capture)
+    cudaStream_t st = nullptr;
+};
+
+moe_status_t ws_claim(const void *ws, cudaStream_t st, WsTicket &t)
+{
+    t = WsTicket{};
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) {
+        (void)cudaGetLastError();
+        cap = cudaStreamCaptureStatusNone;
+    }
+    if (cap != cudaStreamCaptureStatusNone) return MOE_OK;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    WsUse *u = nullptr, *free_slot = nullptr, *idle = nullptr;
+    for (WsUse &e : g_ws) {
+        if (e.ws == ws) {
+            u = &e;
+            break;
+        }
+        if (!e.ws && !free_slot) free_slot = &e;
+    }
+    if (!u && !free_slot) {
+        // table full: reuse an entry whose last launch has completed
+        for (WsUse &e : g_ws)
+            if (e.pending == 0 && (!e.recorded || cudaEventQuery(e.ev) == cudaSuccess)) {
+                idle = &e;
+                break;
+            }
+        (void)cudaGetLastError();
+        if (!idle) return MOE_OK;  // every entry busy: this launch goes untracked
+        idle->ws = nullptr;
+        idle->recorded = false;
+        free_slot = idle;
+    }
+    if (!u) {
+        u = free_slot;
+        if (!u->ev && cudaEventCreateWithFlags(&u->ev, cudaEventDisableTiming) != cudaSuccess) {
+            u->ev = nullptr;
+            return fail(MOE_ERR_CUDA, "cudaEventCreateWithFlags: %s", cudaGetErrorString(cudaGetLastError()));
+        }
+        u->ws = ws;
+        u->st = st;
+        u->recorded = false;
+        u->pending = 0;
+    }
+    if (u->st != st) {
+        if (u->pending > 0)
+            return fail(MOE_ERR_WORKSPACE_BUSY, "workspace %p is being launched on another stream", ws);
+        if (u->recorded) {
+            const cudaError_t q = cudaEventQuery(u->ev);
+            if (q == cudaErrorNotReady) {
+                (void)cudaGetLastError();
+                return fail(MOE_ERR_WORKSPACE_BUSY, "workspace %p is still in use by a launch on another stream", ws);
+            }
+            if (q != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaEventQuery: %s", cudaGetErrorString(q));
+        }
+        u->st = st;
+        u->recorded = false;
+    }
+    u->pending++;
+    t.u = u;
+    t.st = st;
+    return MOE_OK;
+}
+
+// After the launch (or its refusal): the event marks the end of what was queued.
+void ws_release(WsTicket &t, bool launched)
+{
+    if (!t.u) return;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    if (launched && cudaEventRecord(t.u->ev, t.st) == cudaSuccess) t.u->recorded = true;
+    t.u->pending--;
+    t.u = nullptr;
+}
+
 }  // namespace
 
 // One tiling of the step kernel: gate/up tiles of RA rows and K parts of KA
@@ -730,6 +824,7 @@ moe_status_t run_gv(moe_plan *pl, const void *x, const int32_t *ids, const float
     p.gv_cnt = reinterpret_cast<unsigned long long *>(wsb + pl->off_gv_cnt);
     set_pair_space(pl, p);
     p.T = 1;
+    p.null_mode = path == Path::Null ? 1 : 0;
     p.timeout_ns = pl->timeout_ns;
     for (int i = 0; i < 6; ++i) {
         p.gv[i] = pl->gvm[i];
@@ -761,7 +856,8 @@ moe_status_t run_gv(moe_plan *pl, const void *x, const int32_t *ids, const float
     }
     {
         std::lock_guard<std::mutex> lk(pl->mu);
-        if (path == Path::Prefill) pl->stats.prefill_launches++;
+        if (path == Path::Null) pl->stats.null_launches++;
+        else if (path == Path::Prefill) pl->stats.prefill_launches++;
         else pl->stats.decode_launches++;
         pl->stats.gemv_launches++;
     }
@@ -772,6 +868,9 @@ moe_status_t run_gv(moe_plan *pl, const void *x, const int32_t *ids, const float
         });
     return MOE_OK;
 }
+
+moe_status_t launch_step(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, int T, void *ws,
+                         void *stream, Path path, const WsOffsets *wo);
 
 moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, int T, void *ws,
                       void *stream, Path path, const WsOffsets *wo = nullptr)
@@ -802,14 +901,31 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
         reject(pl);
         return st;
     }
-    // kernel choice: the tensor-core kernel when asked for, or (automatic) for
-    // more than 8 pairs per launch; a single token's 8 pairs stream too few
-    // bytes per expert for the tensor-core pipeline's fixed latencies, and the
-    // register kernel is faster there (measured: 30.6 vs 52.7 us at T = 1,
-    // 192 vs 154 us at T = 16, 330 vs 226 us at T = 24)
-    // launches of at most T_small tokens (the single-token decode) take the
-    // small-launch tensor-core kernel whenever the tensor cores may be used
-    if (pl->use_gv && path != Path::Null && !wo && T == 1)
+    // the workspace must not be in flight on another stream (the static
+    // scratch path claims its scratch itself, before clearing it)
+    WsTicket tk;
+    if (!wo) {
+        st = ws_claim(ws, static_cast<cudaStream_t>(stream), tk);
+        if (st != MOE_OK) {
+            reject(pl);
+            return st;
+        }
+    }
+    st = launch_step(pl, x, ids, w, y, T, ws, stream, path, wo);
+    ws_release(tk, st == MOE_OK);
+    return st;
+}
+
+// The launch itself: kernel choice and arguments (the checks above passed).
+moe_status_t launch_step(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, int T, void *ws,
+                         void *stream, Path path, const WsOffsets *wo)
+{
+    // kernel choice (automatic): a single token takes the one-token row
+    // kernel when its shape allows; launches of at most T_small tokens the
+    // small-launch tensor-core kernel; more than 8 pairs (or MOE_KERNEL_TENSOR,
+    // or an act_quant plan) the ticket tensor-core kernel; the rest the
+    // register kernel
+    if (pl->use_gv && !wo && T == 1)
         return run_gv(pl, x, ids, w, y, ws, static_cast<cudaStream_t>(stream), path);
     if (pl->use_small && path != Path::Null && !wo && T <= pl->T_small)
         return run_small(pl, x, ids, w, y, T, ws, static_cast<cudaStream_t>(stream), path);
@@ -1245,7 +1361,11 @@ moe_status_t moe_workspace_init(moe_plan_t plan, void *ws_dev, size_t bytes, voi
         return fail(MOE_ERR_INVALID_ARG, "workspace of %zu bytes < %zu needed", bytes, plan->ws_bytes);
     moe_status_t st = check_device(plan);
     if (st != MOE_OK) return st;
+    WsTicket tk;
+    st = ws_claim(ws_dev, static_cast<cudaStream_t>(stream), tk);
+    if (st != MOE_OK) return st;
     cudaError_t e = cudaMemsetAsync(ws_dev, 0, plan->ws_bytes, static_cast<cudaStream_t>(stream));
+    ws_release(tk, e == cudaSuccess);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
     return MOE_OK;
 }
@@ -1274,8 +1394,15 @@ moe_status_t moe_group(moe_plan_t plan, const int32_t *ids_dev, int T, void *ws_
         reject(plan);
         return st;
     }
+    WsTicket tk;
+    st = ws_claim(ws_dev, static_cast<cudaStream_t>(stream), tk);
+    if (st != MOE_OK) {
+        reject(plan);
+        return st;
+    }
     cudaError_t e = moe::launch_group(ids_dev, P, plan->d.E, static_cast<uint32_t *>(ws_dev), counts_dev,
                                       offsets_dev, perm_dev, static_cast<cudaStream_t>(stream));
+    ws_release(tk, e == cudaSuccess);
     if (e != cudaSuccess) {
         reject(plan);
         return fail(MOE_ERR_CUDA, "grouping launch: %s", cudaGetErrorString(e));
@@ -1324,13 +1451,22 @@ moe_status_t moe_decode_static(moe_plan_t plan, const void *x_dev, const int32_t
         return st;
     }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // the device's one static scratch must not be in flight on another stream
+    WsTicket tk;
+    st = ws_claim(scr, cs, tk);
+    if (st != MOE_OK) {
+        reject(plan);
+        return st;
+    }
     // the control block and the counters must start at zero
     cudaError_t e = cudaMemsetAsync(scr, 0, wo.off_h, cs);
     if (e != cudaSuccess) {
+        ws_release(tk, false);
         reject(plan);
         return fail(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
     }
     st = run_step(plan, x_dev, ids_dev, w_dev, y_dev, T, scr, stream, Path::Decode, &wo);
+    ws_release(tk, true);  // (the memset at least was queued)
     if (st != MOE_OK || !check) return st;
     // check: wait for the step and report what the device recorded
     uint32_t word = 0;
@@ -1340,6 +1476,10 @@ moe_status_t moe_decode_static(moe_plan_t plan, const void *x_dev, const int32_t
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "moe_decode_static check: %s", cudaGetErrorString(e));
     if (word & moe::kErrTimeout) return fail(MOE_ERR_TIMEOUT, "a device-side wait timed out");
     if (word & moe::kErrBadId) return fail(MOE_ERR_BAD_EXPERT_ID, "an expert id >= E was seen and skipped");
+    // an unreadable scale first: it also makes h non-finite
+    if (word & moe::kErrScale)
+        return fail(MOE_ERR_SCALE, "a weight block scale is negative or NaN (the tensor-core kernels read E4M3 scales as "
+                                   "unsigned)");
     if (word & moe::kErrRange) return fail(MOE_ERR_RANGE, "an intermediate (h) was not finite");
     return MOE_OK;
 }
@@ -1480,6 +1620,10 @@ moe_status_t moe_check(moe_plan_t plan, void *ws_dev, void *stream)
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "moe_check: %s", cudaGetErrorString(e));
     if (word & moe::kErrTimeout) return fail(MOE_ERR_TIMEOUT, "a device-side wait timed out");
     if (word & moe::kErrBadId) return fail(MOE_ERR_BAD_EXPERT_ID, "an expert id >= E was seen and skipped");
+    // an unreadable scale first: it also makes h non-finite
+    if (word & moe::kErrScale)
+        return fail(MOE_ERR_SCALE, "a weight block scale is negative or NaN (the tensor-core kernels read E4M3 scales as "
+                                   "unsigned)");
     if (word & moe::kErrRange) return fail(MOE_ERR_RANGE, "an intermediate (h) was not finite");
     return MOE_OK;
 }

@@ -340,7 +340,8 @@ __device__ bool gv_phase1(const KernelParams &p, GvHdr *hd, uint8_t *smem, const
                 const uint4 qu = *reinterpret_cast<const uint4 *>(st + 4 * KS + offq);
                 const uint16_t sg = *reinterpret_cast<const uint16_t *>(st + 8 * KS + offs);
                 const uint16_t su = *reinterpret_cast<const uint16_t *>(st + 8 * KS + KS / 2 + offs);
-                if (XN > 0) {
+                if (p.null_mode) {  // measurement variant: the same copies and waits, no arithmetic
+                } else if (XN > 0) {
                     gv_granule(d, qg, sg, qu, su, xb[XN > 0 ? step : 0]);
                 } else {
                     uint32_t b[16];
@@ -501,7 +502,7 @@ __device__ bool gv_phase2(const KernelParams &p, GvHdr *hd, uint8_t *smem, const
                     sb = *reinterpret_cast<const uint16_t *>(st + p.gv_qb + rhi * (PK / 16) + 2 * G16);
                 }
                 float d[4][4] = {};
-                gv_granule(d, qa, sa, qb, sb, b);
+                if (!p.null_mode) gv_granule(d, qa, sa, qb, sb, b);
                 if (t == 0) {
                     rr[rlo * nkt] = gv_sum4(d, 0) * fa;
                     rr[rhi * nkt] = gv_sum4(d, 2) * fa;

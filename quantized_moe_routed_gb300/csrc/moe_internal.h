@@ -28,6 +28,7 @@ constexpr int kHteRow = 32;         // register kernel: bytes of h tile exponent
 constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrBadId = 2u;
 constexpr uint32_t kErrRange = 4u;
+constexpr uint32_t kErrScale = 8u;  // a weight block scale the block-scaled MMA would misread
 
 // Shared-memory tables of the step kernel: a 3072-byte control block, then
 // five uint16 arrays of P entries, two uint8 arrays of P and one of T, each

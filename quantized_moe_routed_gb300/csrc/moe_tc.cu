@@ -413,7 +413,10 @@ __device__ void tc_quantize_x(const KernelParams &p, const Tabs &tb, volatile in
                 v[2 * i] = __uint_as_float(w[i] << 16) * P;
                 v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u) * P;
             }
-            quant_block4(v, pk, sc, p.nd);
+            // the digit count as a constant in each branch: a runtime count costs the hot
+            // quantiser its unrolling (measured: 4 us of a 157 us step at T = 24)
+            if (p.nd == 1) quant_block4(v, pk, sc, 1);
+            else quant_block4(v, pk, sc, 4);
         }
         auto put = [&](int r) {
             if (b < nblk) {
@@ -513,6 +516,7 @@ __device__ void tc_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
     int s = 0, n = 0, slot = 0, ms = 0;
     uint32_t ph = 0, mph = 0;
     const uint32_t sfbase = lanebase + 4 * NA;
+    bool sbad = false;  // a weight scale code the MMA would misread (sign bit or NaN)
     for (;;) {
         if (!warp_wait_bar(p, &hd->full[s], ph, abort_flag)) break;
         const int4 h = hd->stage_hdr[s];
@@ -527,8 +531,10 @@ __device__ void tc_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
                 }
             }
             const uint32_t col = sfbase + 64u * static_cast<uint32_t>(slot);
-            tc_st_set(col + 0, row(st + kOffS0, r));
-            tc_st_set(col + 16, row(st + kOffS1, r));
+            const uint4 ws0 = row(st + kOffS0, r), ws1 = row(st + kOffS1, r);
+            sbad = sbad || scale_row_bad(ws0) || scale_row_bad(ws1);
+            tc_st_set(col + 0, ws0);
+            tc_st_set(col + 16, ws1);
             const uint8_t *sb0 = st + offSB0(N);
             if (h.x == KIND_B) {
                 // h rows lane and 32 + lane, K ranges 0 and 1
@@ -558,6 +564,7 @@ __device__ void tc_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
             ph ^= 1u;
         }
     }
+    if (__any_sync(0xffffffffu, sbad) && lane == 0) atomicOr(p.ctrl + 2, kErrScale);
 }
 
 // ------------------------------------------------------------------ MMA thread
@@ -869,7 +876,10 @@ __device__ void tc_epilogue_loop(const KernelParams &p, uint8_t *smem, const Tab
 #pragma unroll
                         for (int e4 = 0; e4 < 4; ++e4) v[e4] *= P;
                         uint32_t pk[4], sc[4];
-                        quant_block4_quad(v, pk, sc, p.nd);
+                        // the digit count as a constant in each branch: a runtime count costs the hot
+                        // quantiser its unrolling (measured: 4 us of a 157 us step at T = 24)
+                        if (p.nd == 1) quant_block4_quad(v, pk, sc, 1);
+                        else quant_block4_quad(v, pk, sc, 4);
                         const int k0 = tile * kTcRows + 4 * lane;  // this lane's first row of h
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {

@@ -23,7 +23,7 @@ def test_library_exports_every_declared_symbol():
     for name in decl:
         assert hasattr(lib, name), name
     lib.moe_abi_version.restype = ctypes.c_int
-    assert lib.moe_abi_version() == 7
+    assert lib.moe_abi_version() == 8
     lib.moe_status_string.restype = ctypes.c_char_p
     assert lib.moe_status_string(6) == b"MOE_ERR_TIMEOUT"
 

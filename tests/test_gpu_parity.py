@@ -188,14 +188,21 @@ def test_zero_routing_weights_give_zero(cache):
     assert st == 0 and bool((y == 0).all())
 
 
-def test_null_step_runs(cache):
+@pytest.mark.parametrize("kernel,counter", [(binding.MOE_KERNEL_AUTO, "gemv_launches"),
+                                            (binding.MOE_KERNEL_REGISTER, "decode_launches")])
+def test_null_step_runs(cache, kernel, counter):
+    """The measurement variant on the one-token row kernel (the automatic
+    choice at T = 1) and on the register kernel."""
     wl, x, ids, w, W = workload_inputs("decode", cache)
-    plan = MoePlan(W, wl.H, wl.I, wl.E, wl.k, T_max=wl.T, strict=True)
+    plan = MoePlan(W, wl.H, wl.I, wl.E, wl.k, T_max=wl.T, strict=True, kernel=kernel)
     ws = plan.new_workspace()
     plan.step(x.to(DEV), ids.to(DEV), w.to(DEV), ws, null=True)
-    assert plan.check(ws) == 0 and plan.stats()["null_launches"] == 1
+    s = plan.stats()
+    assert plan.check(ws) == 0 and s["null_launches"] == 1
+    assert s["gemv_launches"] == (1 if counter == "gemv_launches" else 0)
     # the workspace counters are clean afterwards: a real step still matches
     y = plan.step(x.to(DEV), ids.to(DEV), w.to(DEV), ws)
+    assert plan.stats()[counter] >= 1
     y_ref, _ = oracle.moe_forward(x, ids, w, weights_cpu(W, touched_experts(ids, wl.E)))
     assert rel_err(y.cpu().numpy(), y_ref) <= TOL
 
