@@ -1037,6 +1037,11 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
     if ((threadIdx.x & 31) != 0) return;
     SmemHdr *hd = tb.hdr;
     const uint64_t pol = policy_evict_first();
+    // the activation digit rows (x, h), read once per weight tile of their
+    // group, take the weights' evict_first hint too: evict_last or
+    // evict_normal on them measured more DRAM traffic on a prefill chunk
+    // (4379 MB against 3957 MB read, T = 512) and a slower step
+    const uint64_t pol_act = policy_evict_first();
     const int ng = hd->n_groups, nHt = p.H / kTcRows;
     const TcSplit sp = tc_split(p, ng);
     const int nPB = (p.I + 511) / 512;
@@ -1061,8 +1066,8 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
             const int lg = (sh.w >> 20) & 3;
             const int kc = ((sh.w >> 16) & 15) * ((p.H >> lg) / 256) + (sh.w & 0xFFFF);
             const int gb = tb.gbeg[sh.y];
-            tma2d(st + kOffB0, &p.tmt[6], kc * 128, p.xtok ? 0 : gb * 4, bar, pol);
-            tma2d(st + offSB0(N), &p.tmt[7], kc * 16, p.xtok ? 0 : gb * 4, bar, pol);
+            tma2d(st + kOffB0, &p.tmt[6], kc * 128, p.xtok ? 0 : gb * 4, bar, pol_act);
+            tma2d(st + offSB0(N), &p.tmt[7], kc * 16, p.xtok ? 0 : gb * 4, bar, pol_act);
             if (++ps == p.NS) ps = 0;
         }
         npend = 0;
@@ -1120,8 +1125,8 @@ __device__ void tc_producer_loop(const KernelParams &p, uint8_t *smem, Tabs tb, 
                 // x complete (the flag epilogue warp 4 raises; a shared-memory read)
                 if (!x_ok && ld_acq_cta(&hd->xready)) flush_x();
                 if (x_ok) {
-                    tma2d(st + kOffB0, &p.tmt[6], kc * 128, p.xtok ? 0 : gbeg * 4, bar, pol);
-                    tma2d(st + offSB0(N), &p.tmt[7], kc * 16, p.xtok ? 0 : gbeg * 4, bar, pol);
+                    tma2d(st + kOffB0, &p.tmt[6], kc * 128, p.xtok ? 0 : gbeg * 4, bar, pol_act);
+                    tma2d(st + offSB0(N), &p.tmt[7], kc * 16, p.xtok ? 0 : gbeg * 4, bar, pol_act);
                 } else {
                     if (npend++ == 0) pend0 = s;
                 }
@@ -1171,6 +1176,11 @@ __device__ void tc_helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, vo
     const int lane = threadIdx.x & 31;
     SmemHdr *hd = tb.hdr;
     const uint64_t pol = policy_evict_first();
+    // the activation digit rows (x, h), read once per weight tile of their
+    // group, take the weights' evict_first hint too: evict_last or
+    // evict_normal on them measured more DRAM traffic on a prefill chunk
+    // (4379 MB against 3957 MB read, T = 512) and a slower step
+    const uint64_t pol_act = policy_evict_first();
     const int ng = hd->n_groups;
     const int TA = p.I / kTcRows, nHt = p.H / kTcRows;
     const TcSplit sp = tc_split(p, ng);
@@ -1244,14 +1254,14 @@ __device__ void tc_helper_loop(const KernelParams &p, uint8_t *smem, Tabs tb, vo
                 uint64_t *bar = &hd->full[si];
                 const int gbeg = tb.gbeg[grp];
                 if (kind == KIND_A) {
-                    tma2d(st + kOffB0, &p.tmt[6], part * 128, p.xtok ? 0 : gbeg * 4, bar, pol);
-                    tma2d(st + offSB0(N), &p.tmt[7], part * 16, p.xtok ? 0 : gbeg * 4, bar, pol);
+                    tma2d(st + kOffB0, &p.tmt[6], part * 128, p.xtok ? 0 : gbeg * 4, bar, pol_act);
+                    tma2d(st + offSB0(N), &p.tmt[7], part * 16, p.xtok ? 0 : gbeg * 4, bar, pol_act);
                 } else {
                     const int kc0 = 2 * part;
-                    tma2d(st + kOffB0, &p.tmt[8], kc0 * 128, gbeg * 4, bar, pol);
-                    tma2d(st + offB1(N), &p.tmt[8], (kc0 + 1) * 128, gbeg * 4, bar, pol);
-                    tma2d(st + offSB0(N), &p.tmt[9], kc0 * 16, gbeg * 4, bar, pol);
-                    tma2d(st + offSB1(N), &p.tmt[9], (kc0 + 1) * 16, gbeg * 4, bar, pol);
+                    tma2d(st + kOffB0, &p.tmt[8], kc0 * 128, gbeg * 4, bar, pol_act);
+                    tma2d(st + offB1(N), &p.tmt[8], (kc0 + 1) * 128, gbeg * 4, bar, pol_act);
+                    tma2d(st + offSB0(N), &p.tmt[9], kc0 * 16, gbeg * 4, bar, pol_act);
+                    tma2d(st + offSB1(N), &p.tmt[9], (kc0 + 1) * 16, gbeg * 4, bar, pol_act);
                 }
             }
             ++pq_head;
