@@ -466,11 +466,17 @@ __device__ bool gv_phase2(const KernelParams &p, GvHdr *hd, uint8_t *smem, const
     const int PK = p.gv_pk, RB = p.gv_rb, nkr = PK / 128, nkt = p.I / 128, rows16 = 16 * p.gv_tiles;
     float *red2 = reinterpret_cast<float *>(smem + p.gv_off_red2);
     if (q.R == 0) return true;
+    // the warp's first item (it = w) as (expert of the stage, K range), divided
+    // out once; later items, and the stages' (group, piece), step without a
+    // division (a runtime division sits on the item's dependency chain)
+    const int ea0 = w / nkr, kr0 = w - ea0 * nkr;
+    int ag = 0, kp = 0;
     for (int jd = 0; jd < q.neg * q.npc; ++jd) {
         if (!warp_wait_bar(p, &hd->full[s], ph, abort_flag)) return false;
-        const int ag = jd / q.npc, kp = jd - ag * q.npc, na = min(p.gv_ep, nE - ag * p.gv_ep);
+        const int na = min(p.gv_ep, nE - ag * p.gv_ep);
+        int ea = ea0, kr = kr0;
         for (int it = w; it < na * nkr; it += kGvWarps) {
-            const int ea = it / nkr, kr = it - ea * nkr, a = ag * p.gv_ep + ea;
+            const int a = ag * p.gv_ep + ea;
             const uint8_t *st = smem + s * p.stage_bytes + ea * p.gv_db;
             const int G16 = 4 * kr + t, c = G16 >> 3, gi = G16 & 7;
             uint32_t b[16];
@@ -508,12 +514,17 @@ __device__ bool gv_phase2(const KernelParams &p, GvHdr *hd, uint8_t *smem, const
                     rr[rhi * nkt] = gv_sum4(d, 2) * fa;
                 }
             }
+            for (kr += kGvWarps; kr >= nkr; kr -= nkr) ++ea;  // the next item, it + 16
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&hd->empty[s]);
         if (++s == p.NS) {
             s = 0;
             ph ^= 1u;
+        }
+        if (++kp == q.npc) {
+            kp = 0;
+            ++ag;
         }
     }
     return true;
