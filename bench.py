@@ -581,8 +581,9 @@ def main():
         ms_e2e, h2d, d2h = time_e2e(S, min(steps, 2000))
         out["e2e"] = {"value": S["bytes"] / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "us_per_step": ms_e2e * 1e3,
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                      "api": "moe_step_host, one call per step from Python: one host->device copy of the packed "
-                             "x/ids/w block, the step storing y into pinned host memory"}
+                      "api": "moe_step_host, one call per step from Python: the packed x/ids/w block from pinned "
+                             "host memory (copied in one piece, or read in place by the one-token row kernel), "
+                             "the step storing y into pinned host memory"}
         if not args.no_sweep and args.workload == "decode":
             sweep = {}
             for name in ("spec_verify", "upper_decode"):

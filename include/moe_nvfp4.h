@@ -265,7 +265,13 @@ size_t moe_io_bytes(moe_plan_t plan, int T, size_t *off_ids, size_t *off_w);
 
 /* The step from host buffers to a host buffer, in one call: one host->device
  * copy of the packed input block, then the step (moe_decode for T <= 24,
- * moe_prefill above), which writes y.  If y_host is page-locked memory that
+ * moe_prefill above), which writes y.  For T = 1 on a plan whose single-token
+ * step is the one-token row kernel, and io_host device-addressable (pinned
+ * and mapped, as below), there is no copy: that kernel reads x, ids and w from
+ * io_host in place with plain loads, and io_dev is not written.  With the
+ * plan's pdl flag it then reads them before the previous kernel on the stream
+ * has finished (its workspace writes still wait for that kernel), so io_host
+ * must not be written by device work queued before the call.  If y_host is page-locked memory that
  * the device can address (cudaHostAlloc, or cudaHostRegister with mapping, on a
  * system with unified addressing), the step's kernels store y into it
  * directly and y_dev is not written.  Otherwise the step writes y_dev, and one
@@ -278,7 +284,7 @@ size_t moe_io_bytes(moe_plan_t plan, int T, size_t *off_ids, size_t *off_w);
  *            pageable memory they still work, but the runtime stages them
  *            and the call returns later.
  *   io_dev   device block of the same size, 256-byte aligned; after the call,
- *            it holds the copied x, ids and w
+ *            it holds the copied x, ids and w (unless they were read in place)
  *   y_dev    device float [T, H], 16-byte aligned: the step's output when
  *            y_host is not device-addressable
  *   y_host   host float [T, H], receives y (pinned, like io_host)

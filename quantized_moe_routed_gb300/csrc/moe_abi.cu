@@ -799,7 +799,7 @@ moe_status_t run_small(moe_plan *pl, const void *x, const int32_t *ids, const fl
 
 // The one-token row kernel (one launch, T = 1).
 moe_status_t run_gv(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, void *ws,
-                    cudaStream_t cs, Path path)
+                    cudaStream_t cs, Path path, bool inputs_early)
 {
     const GvLayout L = gv_layout(pl);
     {
@@ -825,6 +825,7 @@ moe_status_t run_gv(moe_plan *pl, const void *x, const int32_t *ids, const float
     set_pair_space(pl, p);
     p.T = 1;
     p.null_mode = path == Path::Null ? 1 : 0;
+    p.inputs_early = inputs_early ? 1 : 0;
     p.timeout_ns = pl->timeout_ns;
     for (int i = 0; i < 6; ++i) {
         p.gv[i] = pl->gvm[i];
@@ -870,10 +871,12 @@ moe_status_t run_gv(moe_plan *pl, const void *x, const int32_t *ids, const float
 }
 
 moe_status_t launch_step(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, int T, void *ws,
-                         void *stream, Path path, const WsOffsets *wo);
+                         void *stream, Path path, const WsOffsets *wo, bool inputs_early);
 
+// inputs_early: x, ids and w are not written by the previous kernel on the
+// stream (the host-buffer entry's in-place inputs)
 moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, int T, void *ws,
-                      void *stream, Path path, const WsOffsets *wo = nullptr)
+                      void *stream, Path path, const WsOffsets *wo = nullptr, bool inputs_early = false)
 {
     if (!pl) return fail(MOE_ERR_INVALID_ARG, "null plan");
     if (T < 0 || T > pl->d.T_max) {
@@ -911,14 +914,14 @@ moe_status_t run_step(moe_plan *pl, const void *x, const int32_t *ids, const flo
             return st;
         }
     }
-    st = launch_step(pl, x, ids, w, y, T, ws, stream, path, wo);
+    st = launch_step(pl, x, ids, w, y, T, ws, stream, path, wo, inputs_early);
     ws_release(tk, st == MOE_OK);
     return st;
 }
 
 // The launch itself: kernel choice and arguments (the checks above passed).
 moe_status_t launch_step(moe_plan *pl, const void *x, const int32_t *ids, const float *w, float *y, int T, void *ws,
-                         void *stream, Path path, const WsOffsets *wo)
+                         void *stream, Path path, const WsOffsets *wo, bool inputs_early)
 {
     // kernel choice (automatic): a single token takes the one-token row
     // kernel when its shape allows; launches of at most T_small tokens the
@@ -926,7 +929,7 @@ moe_status_t launch_step(moe_plan *pl, const void *x, const int32_t *ids, const 
     // or an act_quant plan) the ticket tensor-core kernel; the rest the
     // register kernel
     if (pl->use_gv && !wo && T == 1)
-        return run_gv(pl, x, ids, w, y, ws, static_cast<cudaStream_t>(stream), path);
+        return run_gv(pl, x, ids, w, y, ws, static_cast<cudaStream_t>(stream), path, inputs_early);
     if (pl->use_small && path != Path::Null && !wo && T <= pl->T_small)
         return run_small(pl, x, ids, w, y, T, ws, static_cast<cudaStream_t>(stream), path);
     if (pl->use_tc && path != Path::Null && !wo &&
@@ -1533,18 +1536,35 @@ moe_status_t moe_step_host(moe_plan_t plan, const void *io_host, void *io_dev, f
     }
     size_t oi = 0, ow = 0;
     const size_t in_bytes = moe_io_bytes(plan, T, &oi, &ow);
-    uint8_t *dev = static_cast<uint8_t *>(io_dev);
+    const uint8_t *dev = static_cast<const uint8_t *>(io_dev);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemcpyAsync(io_dev, io_host, in_bytes, cudaMemcpyHostToDevice, cs);
-    if (e != cudaSuccess) {
-        reject(plan);
-        return fail(MOE_ERR_CUDA, "input copy: %s", cudaGetErrorString(e));
+    // a single token on the one-token row kernel: that kernel reads x, ids and
+    // w with plain loads, so a device-addressable io_host is read where it is
+    // (its bytes cross to the device inside the step) and nothing is copied
+    bool in_place = false;
+    if (T == 1 && plan->use_gv) {
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, io_host) == cudaSuccess) {
+            if (a.type == cudaMemoryTypeHost && a.devicePointer && aligned(a.devicePointer, 256)) {
+                dev = static_cast<const uint8_t *>(a.devicePointer);
+                in_place = true;
+            }
+        } else {
+            (void)cudaGetLastError();
+        }
+    }
+    if (!in_place) {
+        cudaError_t e = cudaMemcpyAsync(io_dev, io_host, in_bytes, cudaMemcpyHostToDevice, cs);
+        if (e != cudaSuccess) {
+            reject(plan);
+            return fail(MOE_ERR_CUDA, "input copy: %s", cudaGetErrorString(e));
+        }
     }
     st = run_step(plan, dev, reinterpret_cast<const int32_t *>(dev + oi), reinterpret_cast<const float *>(dev + ow),
-                  y_out, T, ws_dev, stream, T <= moe::kDecodeMaxT ? Path::Decode : Path::Prefill);
+                  y_out, T, ws_dev, stream, T <= moe::kDecodeMaxT ? Path::Decode : Path::Prefill, nullptr, in_place);
     if (st != MOE_OK || y_out != y_dev) return st;
-    e = cudaMemcpyAsync(y_host, y_dev, static_cast<size_t>(T) * plan->d.H * sizeof(float), cudaMemcpyDeviceToHost,
-                        cs);
+    cudaError_t e = cudaMemcpyAsync(y_host, y_dev, static_cast<size_t>(T) * plan->d.H * sizeof(float),
+                                    cudaMemcpyDeviceToHost, cs);
     if (e != cudaSuccess) {
         reject(plan);
         return fail(MOE_ERR_CUDA, "result copy: %s", cudaGetErrorString(e));

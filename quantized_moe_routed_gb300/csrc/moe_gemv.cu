@@ -586,8 +586,11 @@ __global__ void __launch_bounds__(kGvThreads, 1) moe_gemv_kernel(const __grid_co
         asm volatile("" ::"r"(acc));
     }
     __syncthreads();
-    // x, ids, w and the workspace may be written by the previous kernel
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // x, ids, w and the workspace may be written by the previous kernel; with
+    // inputs_early only the workspace, which phase 1 does not touch: the
+    // compute warps then wait just before their first workspace write, and
+    // the tables, x and the first copies overlap the previous kernel's end
+    if (!p.inputs_early) asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp < kGvWarps) {
@@ -606,6 +609,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) moe_gemv_kernel(const __grid_co
                   : p.gv_ks == 2048     ? gv_phase1<1>(p, hd, smem, q, s, ph, abort_flag)
                                         : gv_phase1<2>(p, hd, smem, q, s, ph, abort_flag);
         gv_sync();
+        if (p.inputs_early) asm volatile("griddepcontrol.wait;" ::: "memory");
         if (ok && !*abort_flag) gv_write_h(p, hd, smem);
         gv_sync();
         // the grid barrier: every CTA's h rows are in the workspace

@@ -100,6 +100,7 @@ struct KernelParams {
     int ntiles;                                 // kernel variant: n-tiles per group (1 or 2)
     long long timeout_ns;
     int null_mode;      // 1: measurement variant (no dequant / math)
+    int inputs_early;   // 1: x, ids and w are not written by the previous kernel (row kernel: read before its end)
 
     // ---- tensor-core path (moe_tc.cu) ----
     // TMA descriptors: 0 gate_q, 1 up_q, 2 down_q (box 128 B x 128 rows, 128-byte

@@ -1,5 +1,6 @@
 """The host-buffer entry (moe_step_host): one copy of the packed x / ids / w
-block in, then the step, which stores y straight into a pinned host y (or into
+block in (none for the one-token row kernel, which reads the pinned block in
+place), then the step, which stores y straight into a pinned host y (or into
 y_dev, with one copy out, when y is pageable).  Its result is bitwise the
 result of the same step on device buffers, on every path it routes to
 (register kernel, tensor-core kernel, prefill), and it refuses bad arguments
@@ -49,6 +50,7 @@ def test_step_host_is_bitwise_the_device_step(T, k, path):
     io = HostIO(plan, T)
     fill(io, x, ids, w)
     io.y_dev.fill_(float("nan"))
+    io.dev.fill_(0xAB)
     y = plan.step_host(io, ws)
     torch.cuda.synchronize()
     assert plan.check(ws) == 0
@@ -56,6 +58,11 @@ def test_step_host_is_bitwise_the_device_step(T, k, path):
     assert torch.equal(y, y_dev_path.cpu())
     # the pinned y is device-addressable: the kernels stored y there directly
     assert bool(torch.isnan(io.y_dev).all())
+    # the row kernel reads the pinned input block in place; every other path copies it
+    if path == "gemv":
+        assert bool((io.dev == 0xAB).all())
+    else:
+        assert torch.equal(io.dev.cpu(), io.host)
     if path == "tensor":
         assert after["tensor_launches"] == before["tensor_launches"] + 1
     elif path == "small":
