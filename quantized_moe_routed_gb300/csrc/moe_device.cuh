@@ -251,9 +251,14 @@ __device__ __forceinline__ uint32_t u4w(const uint4 &v, int i)
 // or -1 for a slot that contributes nothing here; an id >= Eg also sets bad.
 __device__ __forceinline__ int pair_expert(const KernelParams &p, int q, bool &bad)
 {
-    const int t = q / p.k, j = q - t * p.k;
-    if (j >= p.kr) return p.Eloc;
-    const int e = p.ids[t * p.kr + j];
+    int e;
+    if (p.k == p.kr) {
+        e = p.ids[q];  // no shared slot: pair q is entry q of ids (no division on the grouping's path)
+    } else {
+        const int t = q / p.k, j = q - t * p.k;
+        if (j >= p.kr) return p.Eloc;
+        e = p.ids[t * p.kr + j];
+    }
     if (e < 0) return -1;
     if (e >= p.Eg) {
         bad = true;
