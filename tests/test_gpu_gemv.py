@@ -68,6 +68,24 @@ def test_gemv_kernel_shapes(H, I, E, k):
     assert err <= TOL
 
 
+@pytest.mark.parametrize("H,I,E,k", [(16384, 512, 64, 8), (16384, 4096, 32, 16)])
+def test_largest_shapes_match_the_oracle(H, I, E, k):
+    """H = 16384 (the row kernel's largest): at I = 512 the row kernel takes the
+    step; at I = 4096 with 16 slots its shared memory does not hold the layout,
+    and the plan takes another kernel.  Either way y matches the oracle."""
+    wl = Workload("gemv-max", T=1, H=H, I=I, E=E, k=k, routing="uniform", seed=98)
+    plan, ws, y, st, x, ids, w, W, Wc = run(wl)
+    assert st == 0, binding.STATUS_NAMES.get(st)
+    s = plan.stats()
+    if I == 512:
+        assert s["gemv_launches"] == 1
+    assert s["decode_launches"] == 1
+    y_ref, _ = oracle.moe_forward(x, ids, w, Wc)
+    err = rel_err(y.cpu().numpy(), y_ref)
+    print(f"H={H} I={I} k={k}: rel err {err:.3e}, row kernel {s['gemv_launches']}")
+    assert err <= TOL
+
+
 def test_gemv_repeated_empty_and_bad_slots():
     """One expert named three times (its h is computed once, weighted per
     slot), empty slots, an id >= E (skipped, flagged)."""
