@@ -54,9 +54,10 @@ typedef enum {
     MOE_ERR_BAD_EXPERT_ID = 7,     /* device: an id >= E was seen (slot skipped)       */
     MOE_ERR_RANGE = 8,             /* device: an intermediate (h) was not finite      */
     MOE_ERR_SCALE = 9,             /* device: a weight block scale the tensor-core     */
-                                   /*   kernels cannot read (sign bit set, or NaN)    */
-    MOE_ERR_WORKSPACE_BUSY = 10    /* host: the workspace is in flight on another     */
-                                   /*   stream                                        */
+                                   /*   kernels cannot read (sign bit set, or NaN;    */
+                                   /*   found by moe_workspace_init's scan)           */
+    MOE_ERR_WORKSPACE_BUSY = 10    /* host: another thread is launching on the        */
+                                   /*   workspace from another stream                 */
 } moe_status_t;
 
 /* Opaque plan: host memory owned by the library (moe_plan_destroy frees it). */
@@ -110,10 +111,11 @@ typedef struct {
                 /*     is refused with UNSUPPORTED_SHAPE where the shape does not */
                 /*     allow it).  The tensor-core kernels need non-negative,     */
                 /*     non-NaN E4M3 block scales (the MMA reads them unsigned),   */
-                /*     as an NVFP4 quantiser writes them; their scale warps check */
-                /*     every weight scale they stage and a launch that met a      */
-                /*     negative or NaN one reports MOE_ERR_SCALE (its y is then   */
-                /*     wrong).  The register and row kernels decode the sign.     */
+                /*     as an NVFP4 quantiser writes them: moe_workspace_init of a */
+                /*     plan that may run them scans every weight block scale and  */
+                /*     a negative or NaN one makes moe_check report MOE_ERR_SCALE */
+                /*     (their y would be wrong).  The register and row kernels    */
+                /*     decode the sign.                                           */
     /* Shared expert (optional; NULL shared_gate_q_dev: none).  One always-on
      * SwiGLU expert in the same NVFP4 format, added to every token's y with
      * weight 1 after the routed slots, inside the same launch (the serving
@@ -181,19 +183,25 @@ void moe_plan_destroy(moe_plan_t plan);
  * sharing a workspace at the same time corrupt each other's counters (the
  * pages' two-stream deadlock, "dsv4-carve" README, trap 3).  The library
  * records an event after each launch on a workspace (moe_decode, moe_prefill,
- * moe_null_step, moe_step_host, moe_group, moe_workspace_init) and refuses a
- * launch on another stream while that event is pending, or while another
- * thread is launching on it from another stream, with MOE_ERR_WORKSPACE_BUSY
- * (nothing queued).  Launches being captured into a CUDA graph are not
- * checked: the graph's replays are ordered by whoever launches them.
+ * moe_null_step, moe_step_host, moe_group, moe_workspace_init); a launch on
+ * another stream while that event is pending is ordered after it (the new
+ * stream waits on the event), and a launch while another thread is launching
+ * on it from another stream is refused with MOE_ERR_WORKSPACE_BUSY (nothing
+ * queued).  Launches being captured into a CUDA graph are not checked: the
+ * graph's replays are ordered by whoever launches them.
  * Returns 0 for an invalid plan or T. */
 size_t moe_workspace_bytes(moe_plan_t plan, int T);
 
 /* Zero a workspace of `bytes` bytes (>= moe_workspace_bytes(plan, T_max))
  * on `stream`.  Required once after allocation and after any device-side
  * error; the kernels reset their own counters after every successful launch.
- * ws_dev must be 256-byte aligned.  MOE_ERR_WORKSPACE_BUSY while the
- * workspace is in flight on another stream. */
+ * For a plan that may run a tensor-core kernel (T_max > 1, or the one-token row
+ * kernel not available) it also scans every weight block scale once (one
+ * launch reading them all) and records MOE_ERR_SCALE in the workspace's error
+ * word when one has its sign bit set or is NaN (see `kernel`); moe_check
+ * reports it.  ws_dev must be 256-byte aligned.  Ordered after a launch
+ * still in flight on the workspace from another stream (see
+ * moe_workspace_bytes). */
 moe_status_t moe_workspace_init(moe_plan_t plan, void *ws_dev, size_t bytes, void *stream);
 
 /* Grouping only (bit-exact, integer): for the P = T*top_k flat pairs
@@ -208,7 +216,9 @@ moe_status_t moe_group(moe_plan_t plan, const int32_t *ids_dev, int T, void *ws_
 
 /* The routed-experts step for 0 <= T <= 24 tokens (decode; T == 0 is a no-op).
  * Status: MOE_OK (queued), INVALID_ARG, MISALIGNED, NOT_FAST_PATH, CUDA, or
- * WORKSPACE_BUSY (ws_dev in flight on another stream; nothing queued).
+ * WORKSPACE_BUSY (another thread is launching on ws_dev from another stream;
+ * nothing queued).  A launch still in flight on ws_dev from another stream is
+ * waited for (see moe_workspace_bytes).
  * Device-side outcomes go to the workspace error word (moe_check).
  *   x_dev    bf16 [T, H] row-major, 16-byte aligned; any finite bf16 values:
  *            both kernels prescale each token's row by a power of two before
@@ -245,8 +255,7 @@ moe_status_t moe_decode(moe_plan_t plan, const void *x_dev, const int32_t *ids_d
  * any stream capture.  Every call on a device shares the one buffer, so calls
  * that overlap in time (other streams, other threads, other plans on the
  * same device) would race: a call while the scratch is in flight on another
- * stream is refused with MOE_ERR_WORKSPACE_BUSY (order such calls on one
- * stream).
+ * stream is ordered after that call (its stream waits), as for a workspace.
  * check == 0: asynchronous, no synchronisation.  check != 0: synchronise
  * `stream` after the launch and return the device error status (MOE_OK,
  * MOE_ERR_TIMEOUT, MOE_ERR_BAD_EXPERT_ID, MOE_ERR_SCALE or MOE_ERR_RANGE, as

@@ -46,11 +46,13 @@ std::once_flag g_gv_once;
 
 // ------------------------------------------------------------------ workspace ownership
 // Which stream each workspace was last launched on, with an event recorded
-// after that launch.  A launch on another stream while that event is pending
-// (or while another thread is between its claim and its record) is refused
-// with MOE_ERR_WORKSPACE_BUSY: two launches in flight on one workspace would
-// share its counters and scratch.  Launches captured into a CUDA graph are
-// not tracked (the graph's replays are ordered by whoever launches them).
+// after that launch.  Two launches in flight on one workspace would share its
+// counters and scratch, so a launch on another stream while that event is
+// pending is ordered after it (the new stream waits on the event); a launch
+// while another thread is between its claim and its record on another stream
+// (no event to wait on yet) is refused with MOE_ERR_WORKSPACE_BUSY.  Launches
+// captured into a CUDA graph are not tracked (the graph's replays are ordered
+// by whoever launches them).
 struct WsUse {
     const void *ws = nullptr;
     cudaStream_t st = nullptr;
@@ -112,12 +114,16 @@ moe_status_t ws_claim(const void *ws, cudaStream_t st, WsTicket &t)
         if (u->pending > 0)
             return fail(MOE_ERR_WORKSPACE_BUSY, "workspace %p is being launched on another stream", ws);
         if (u->recorded) {
+            // the last launch on the workspace may still run on the other
+            // stream: this stream waits for it (the two are ordered, not raced)
             const cudaError_t q = cudaEventQuery(u->ev);
             if (q == cudaErrorNotReady) {
                 (void)cudaGetLastError();
-                return fail(MOE_ERR_WORKSPACE_BUSY, "workspace %p is still in use by a launch on another stream", ws);
+                const cudaError_t w = cudaStreamWaitEvent(st, u->ev, 0);
+                if (w != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaStreamWaitEvent: %s", cudaGetErrorString(w));
+            } else if (q != cudaSuccess) {
+                return fail(MOE_ERR_CUDA, "cudaEventQuery: %s", cudaGetErrorString(q));
             }
-            if (q != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaEventQuery: %s", cudaGetErrorString(q));
         }
         u->st = st;
         u->recorded = false;
@@ -1368,8 +1374,31 @@ moe_status_t moe_workspace_init(moe_plan_t plan, void *ws_dev, size_t bytes, voi
     st = ws_claim(ws_dev, static_cast<cudaStream_t>(stream), tk);
     if (st != MOE_OK) return st;
     cudaError_t e = cudaMemsetAsync(ws_dev, 0, plan->ws_bytes, static_cast<cudaStream_t>(stream));
+    // a plan that may run a tensor-core kernel: scan every weight block scale
+    // once for codes the block-scaled MMA would misread (sign bit, NaN); the
+    // bit lands in the error word just zeroed, for moe_check to report
+    if (e == cudaSuccess && plan->use_tc && (plan->d.T_max > 1 || !plan->use_gv)) {
+        const moe_plan_desc &d = plan->d;
+        const size_t ne = static_cast<size_t>(d.e_hi > d.e_lo ? d.e_hi - d.e_lo : d.E);
+        moe::ScaleArrays a{};
+        auto add = [&](const uint8_t *ptr, size_t bytes) {
+            a.ptr[a.n] = ptr;
+            a.bytes[a.n] = bytes;
+            ++a.n;
+        };
+        add(d.gate_s_dev, ne * d.I * (d.H / 16));
+        add(d.up_s_dev, ne * d.I * (d.H / 16));
+        add(d.down_s_dev, ne * d.H * (d.I / 16));
+        if (d.shared_gate_q_dev) {
+            add(d.shared_gate_s_dev, static_cast<size_t>(d.I) * (d.H / 16));
+            add(d.shared_up_s_dev, static_cast<size_t>(d.I) * (d.H / 16));
+            add(d.shared_down_s_dev, static_cast<size_t>(d.H) * (d.I / 16));
+        }
+        e = moe::launch_scale_scan(a, reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws_dev) + 8),
+                                   static_cast<cudaStream_t>(stream));
+    }
     ws_release(tk, e == cudaSuccess);
-    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "workspace initialisation: %s", cudaGetErrorString(e));
     return MOE_OK;
 }
 

@@ -160,6 +160,15 @@ cudaError_t launch_step(const KernelParams &p, int grid, int smem_bytes, bool pd
 cudaError_t launch_group(const int32_t *ids, int P, int E, uint32_t *ctrl, int32_t *counts,
                          int32_t *offsets, int32_t *perm, cudaStream_t st);
 cudaError_t launch_poison(uint32_t *doneA, int n, cudaStream_t st);
+// The weight block-scale arrays a plan's tensor-core kernels read (up to six:
+// gate, up, down of the routed experts and of the shared one), for the scan
+// that flags codes the block-scaled MMA would misread.
+struct ScaleArrays {
+    const uint8_t *ptr[6];
+    size_t bytes[6];  // each a multiple of 16, each pointer 16-byte aligned
+    int n;
+};
+cudaError_t launch_scale_scan(const ScaleArrays &a, uint32_t *err_word, cudaStream_t st);
 cudaError_t set_step_smem_limit(int bytes);
 // Tensor-core path (moe_tc.cu).
 constexpr int kTcThreads = 384;    // 12 warps: 4 scale, 4 epilogue, producer, MMA, helper, release

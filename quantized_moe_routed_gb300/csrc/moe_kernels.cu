@@ -1068,6 +1068,26 @@ __global__ void moe_poison_kernel(uint32_t *doneA, int n)
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) doneA[i] = 0x40000000u;
 }
 
+// Every weight block-scale byte: a code with the sign bit set (a negative
+// scale, or the NaN code 0xFF) or the NaN code 0x7F sets kErrScale in the
+// workspace error word.  Grid-stride over 16-byte words; one atomic per warp
+// that saw one.
+__global__ void moe_scale_scan_kernel(const ScaleArrays a, uint32_t *err_word)
+{
+    uint32_t bad = 0;
+    for (int k = 0; k < a.n; ++k) {
+        const uint4 *v = reinterpret_cast<const uint4 *>(a.ptr[k]);
+        const size_t n16 = a.bytes[k] / 16;
+        for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+             i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+            const uint4 w = __ldg(v + i);
+            bad |= ((w.x | w.y | w.z | w.w) & 0x80808080u) | __vcmpeq4(w.x, 0x7F7F7F7Fu) | __vcmpeq4(w.y, 0x7F7F7F7Fu) |
+                   __vcmpeq4(w.z, 0x7F7F7F7Fu) | __vcmpeq4(w.w, 0x7F7F7F7Fu);
+        }
+    }
+    if (__any_sync(0xffffffffu, bad != 0u) && (threadIdx.x & 31) == 0) atomicOr(err_word, kErrScale);
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ launch helpers
@@ -1121,6 +1141,16 @@ cudaError_t launch_group(const int32_t *ids, int P, int E, uint32_t *ctrl, int32
 cudaError_t launch_poison(uint32_t *doneA, int n, cudaStream_t st)
 {
     moe_poison_kernel<<<8, 256, 0, st>>>(doneA, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale_scan(const ScaleArrays &a, uint32_t *err_word, cudaStream_t st)
+{
+    if (a.n == 0) return cudaSuccess;
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    moe_scale_scan_kernel<<<2 * (sms > 0 ? sms : 1), 512, 0, st>>>(a, err_word);
     return cudaGetLastError();
 }
 

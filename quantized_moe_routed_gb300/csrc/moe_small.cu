@@ -370,7 +370,6 @@ __device__ void sm_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     int s = 0, n = 0, slot = 0, ms = 0;
     uint32_t ph = 0, mph = 0;
-    bool sbad = false;  // a weight scale code the MMA would misread (sign bit or NaN)
     for (;;) {
         if (!warp_wait_bar(p, &hd->full[s], ph, abort_flag)) break;
         const int4 h = hd->stage_hdr[s];
@@ -384,24 +383,16 @@ __device__ void sm_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
                 }
             }
             const uint32_t col = sfbase + 64u * static_cast<uint32_t>(slot);
-            const uint4 ws0 = row(st + kOffS0, r);
-            sbad = sbad || scale_row_bad(ws0);
-            tc_st_set(col + 0, ws0);
+            tc_st_set(col + 0, row(st + kOffS0, r));
             if (h.x == KIND_A) {
-                const uint4 ws1 = row(st + kOffS1, r);
-                sbad = sbad || scale_row_bad(ws1);
-                tc_st_set(col + 16, ws1);
+                tc_st_set(col + 16, row(st + kOffS1, r));
                 const int c = h.y % sh.KC;
                 const uint4 b0 = lane < 4 * p.T ? row(smem + p.s_off_xsc + c * 256, lane) : z;
                 tc_st_bset(col + 32, b0, z, z, z);
             } else {
                 const int g = h.y / sh.TO, hs = g - gfirst, c0 = 2 * h.z;
                 const bool two = c0 + 1 < sh.KCI;
-                if (two) {  // the weights' scales need no h
-                    const uint4 ws1 = row(st + kOffS1, r);
-                    sbad = sbad || scale_row_bad(ws1);
-                    tc_st_set(col + 16, ws1);
-                }
+                if (two) tc_st_set(col + 16, row(st + kOffS1, r));  // the weights' scales need no h
                 bool okb = true;
                 for (; okb && built <= hs; ++built)
                     okb = sm_build_h<RND>(p, smem, tb, sx, sh, gfirst + built, built, gdone, team_sync, abort_flag);
@@ -424,7 +415,6 @@ __device__ void sm_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
             ph ^= 1u;
         }
     }
-    if (__any_sync(0xffffffffu, sbad) && lane == 0) atomicOr(p.ctrl + 2, kErrScale);
 }
 
 // MMA threads (lane 0 of warps 9 and 10: who = 0, 1).  One thread issues a

@@ -516,7 +516,6 @@ __device__ void tc_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
     int s = 0, n = 0, slot = 0, ms = 0;
     uint32_t ph = 0, mph = 0;
     const uint32_t sfbase = lanebase + 4 * NA;
-    bool sbad = false;  // a weight scale code the MMA would misread (sign bit or NaN)
     for (;;) {
         if (!warp_wait_bar(p, &hd->full[s], ph, abort_flag)) break;
         const int4 h = hd->stage_hdr[s];
@@ -531,10 +530,8 @@ __device__ void tc_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
                 }
             }
             const uint32_t col = sfbase + 64u * static_cast<uint32_t>(slot);
-            const uint4 ws0 = row(st + kOffS0, r), ws1 = row(st + kOffS1, r);
-            sbad = sbad || scale_row_bad(ws0) || scale_row_bad(ws1);
-            tc_st_set(col + 0, ws0);
-            tc_st_set(col + 16, ws1);
+            tc_st_set(col + 0, row(st + kOffS0, r));
+            tc_st_set(col + 16, row(st + kOffS1, r));
             const uint8_t *sb0 = st + offSB0(N);
             if (h.x == KIND_B) {
                 // h rows lane and 32 + lane, K ranges 0 and 1
@@ -564,7 +561,6 @@ __device__ void tc_scale_loop(const KernelParams &p, uint8_t *smem, const Tabs &
             ph ^= 1u;
         }
     }
-    if (__any_sync(0xffffffffu, sbad) && lane == 0) atomicOr(p.ctrl + 2, kErrScale);
 }
 
 // ------------------------------------------------------------------ MMA thread

@@ -81,17 +81,6 @@ __device__ __forceinline__ float4 f4add(const float4 &a, const float4 &b)
     return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
 
-// Sixteen weight block-scale codes that the block-scaled MMA, which reads
-// its scales as unsigned E4M3, would misread: a code with the sign bit set
-// (a negative scale, or the NaN code 0xFF) or the NaN code 0x7F.
-__device__ __forceinline__ bool scale_row_bad(const uint4 &v)
-{
-    const uint32_t o = v.x | v.y | v.z | v.w;
-    const uint32_t nan = __vcmpeq4(v.x, 0x7F7F7F7Fu) | __vcmpeq4(v.y, 0x7F7F7F7Fu) | __vcmpeq4(v.z, 0x7F7F7F7Fu) |
-                         __vcmpeq4(v.w, 0x7F7F7F7Fu);
-    return (o & 0x80808080u) != 0u || nan != 0u;
-}
-
 // Shared-memory matrix descriptor: K-major rows of 128 bytes, 128-byte swizzle,
 // 8-row groups 1024 bytes apart (tcgen05 descriptor version 1).
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)

@@ -252,6 +252,11 @@ def make_expert_weights(wl: Workload, device="cpu", experts=None, fill: str = "r
                 if v.dtype == torch.uint8:
                     v.copy_(torch.randint(0, 256, v.shape, generator=g, device=dev,
                                           dtype=torch.uint8))
+                    if name.endswith("_s"):
+                        # block scales stay valid E4M3 codes of a quantiser: no sign
+                        # bit, no NaN (0x7F becomes 0x7E)
+                        v.bitwise_and_(0x7F)
+                        v.sub_((v == 0x7F).to(torch.uint8))
                 else:
                     v.fill_(1.0)
     shapes = (("gate", I, H), ("up", I, H), ("down", H, I))
