@@ -453,12 +453,14 @@ __device__ void gv_h16(const KernelParams &p, GvHdr *hd, uint8_t *smem)
     }
 }
 
-// Phase 2, compute warp w: per down stage (gv_ep active experts, piece kp of
+// Phase 2, compute warp w (NT > 0: the CTA's row tiles, known at compile
+// time; 0: read from the parameters): per down stage (gv_ep active experts, piece kp of
 // I), items (expert of the stage, 128-element K range kr of the piece), warp
 // w taking items w, w + 16, ...; per item the B operand (column 0 = h16 of
 // expert a at the K range) is read once and serves every 16-row tile tl of
 // the CTA's rows: A rows tl 16 + g and tl 16 + g + 8 (zero past R).  The
 // outputs (quarter t = 0: d[0], d[2]) times fa[a] go to red2[a][row][K range of I].
+template <int NT>
 __device__ bool gv_phase2(const KernelParams &p, GvHdr *hd, uint8_t *smem, const GvSeq &q, int &s, uint32_t &ph,
                           volatile int *abort_flag)
 {
@@ -495,7 +497,8 @@ __device__ bool gv_phase2(const KernelParams &p, GvHdr *hd, uint8_t *smem, const
             }
             float *rr = red2 + a * rows16 * nkt + kp * nkr + kr;
             const float fa = hd->fa[a];
-            for (int tl = 0; tl < p.gv_tiles; ++tl) {
+#pragma unroll
+            for (int tl = 0; tl < (NT > 0 ? NT : p.gv_tiles); ++tl) {
                 const int rlo = 16 * tl + g, rhi = rlo + 8;
                 uint4 qa = make_uint4(0u, 0u, 0u, 0u), qb = qa;
                 uint16_t sa = 0, sb = 0;
@@ -530,15 +533,34 @@ __device__ bool gv_phase2(const KernelParams &p, GvHdr *hd, uint8_t *smem, const
     return true;
 }
 
-// After phase 2: the CTA's y rows, warp w taking rows w, w + 16, ...: lane
-// kr (kr < I / 128) adds red2[a][row][kr] over the active experts a in
-// order, and the lanes' sums are added in a fixed butterfly (every lane ends
-// with the same bits).  red2 already carries each expert's factor fa[a].
+// After phase 2: the CTA's y rows.  Lane kr of a row's lane group
+// (kr < I / 128) adds red2[a][row][kr] over the active experts a in order,
+// and the group's sums are added in a fixed butterfly (every lane ends with
+// the same bits); red2 already carries each expert's factor fa[a].  Up to
+// I = 1024 a group is eight lanes and a warp takes four rows at once (R is a
+// multiple of 4, so a warp's four rows are all in range or all past it);
+// above, a group is the whole warp.
 __device__ void gv_write_y(const KernelParams &p, const GvHdr *hd, const uint8_t *smem, const GvSeq &q)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nkt = p.I / 128, nE = hd->nE;
     const int astride = 16 * p.gv_tiles * nkt;
     const float *red2 = reinterpret_cast<const float *>(smem + p.gv_off_red2);
+    if (nkt <= 8) {  // four rows per warp, eight lanes per row (R is a multiple of 4)
+        const int l8 = lane & 7;
+        for (int r = 4 * w + (lane >> 3); r < q.R; r += 4 * kGvWarps) {
+            float y = 0.f;
+            if (l8 < nkt) {
+                const float *rr = red2 + r * nkt + l8;
+#pragma unroll 4
+                for (int a = 0; a < nE; ++a) y += rr[a * astride];
+            }
+            y += __shfl_xor_sync(0xffffffffu, y, 4);
+            y += __shfl_xor_sync(0xffffffffu, y, 2);
+            y += __shfl_xor_sync(0xffffffffu, y, 1);
+            if (l8 == 0) p.y[kGvGroup * q.g0 + r] = y;
+        }
+        return;
+    }
     for (int r = w; r < q.R; r += kGvWarps) {
         float y = 0.f;
         if (lane < nkt) {
@@ -634,7 +656,10 @@ __global__ void __launch_bounds__(kGvThreads, 1) moe_gemv_kernel(const __grid_co
         gv_sync();
         if (!*abort_flag) gv_h16(p, hd, smem);
         gv_sync();
-        if (ok && !*abort_flag) ok = gv_phase2(p, hd, smem, q, s, ph, abort_flag);
+        if (ok && !*abort_flag)
+            ok = p.gv_tiles == 2   ? gv_phase2<2>(p, hd, smem, q, s, ph, abort_flag)
+                 : p.gv_tiles == 1 ? gv_phase2<1>(p, hd, smem, q, s, ph, abort_flag)
+                                   : gv_phase2<0>(p, hd, smem, q, s, ph, abort_flag);
         gv_sync();
         if (ok && !*abort_flag) gv_write_y(p, hd, smem, q);
     } else {
