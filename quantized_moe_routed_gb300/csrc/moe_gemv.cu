@@ -453,19 +453,21 @@ __device__ void gv_h16(const KernelParams &p, GvHdr *hd, uint8_t *smem)
     }
 }
 
-// Phase 2, compute warp w (NT > 0: the CTA's row tiles, known at compile
-// time; 0: read from the parameters): per down stage (gv_ep active experts, piece kp of
+// Phase 2, compute warp w (NT > 0: the CTA's row tiles and NKR > 0: the
+// 128-element K ranges of a piece, known at compile time; 0: read from the
+// parameters): per down stage (gv_ep active experts, piece kp of
 // I), items (expert of the stage, 128-element K range kr of the piece), warp
 // w taking items w, w + 16, ...; per item the B operand (column 0 = h16 of
 // expert a at the K range) is read once and serves every 16-row tile tl of
 // the CTA's rows: A rows tl 16 + g and tl 16 + g + 8 (zero past R).  The
 // outputs (quarter t = 0: d[0], d[2]) times fa[a] go to red2[a][row][K range of I].
-template <int NT>
+template <int NT, int NKR>
 __device__ bool gv_phase2(const KernelParams &p, GvHdr *hd, uint8_t *smem, const GvSeq &q, int &s, uint32_t &ph,
                           volatile int *abort_flag)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, t = lane & 3, nE = hd->nE;
-    const int PK = p.gv_pk, RB = p.gv_rb, nkr = PK / 128, nkt = p.I / 128, rows16 = 16 * p.gv_tiles;
+    const int PK = NKR > 0 ? NKR * 128 : p.gv_pk, RB = p.gv_rb, nkr = NKR > 0 ? NKR : PK / 128, nkt = p.I / 128;
+    const int rows16 = 16 * (NT > 0 ? NT : p.gv_tiles);
     float *red2 = reinterpret_cast<float *>(smem + p.gv_off_red2);
     if (q.R == 0) return true;
     // the warp's first item (it = w) as (expert of the stage, K range), divided
@@ -657,9 +659,10 @@ __global__ void __launch_bounds__(kGvThreads, 1) moe_gemv_kernel(const __grid_co
         if (!*abort_flag) gv_h16(p, hd, smem);
         gv_sync();
         if (ok && !*abort_flag)
-            ok = p.gv_tiles == 2   ? gv_phase2<2>(p, hd, smem, q, s, ph, abort_flag)
-                 : p.gv_tiles == 1 ? gv_phase2<1>(p, hd, smem, q, s, ph, abort_flag)
-                                   : gv_phase2<0>(p, hd, smem, q, s, ph, abort_flag);
+            ok = p.gv_tiles == 2 && p.gv_pk == 1024 ? gv_phase2<2, 8>(p, hd, smem, q, s, ph, abort_flag)
+                 : p.gv_tiles == 2                ? gv_phase2<2, 0>(p, hd, smem, q, s, ph, abort_flag)
+                 : p.gv_tiles == 1                ? gv_phase2<1, 0>(p, hd, smem, q, s, ph, abort_flag)
+                                                  : gv_phase2<0, 0>(p, hd, smem, q, s, ph, abort_flag);
         gv_sync();
         if (ok && !*abort_flag) gv_write_y(p, hd, smem, q);
     } else {
